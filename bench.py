@@ -1,0 +1,341 @@
+"""Benchmark: batch-1 bf16 KV-cached greedy decode of the Qwen2.5-1.5B shape.
+
+One step = one generation of the workload: prefill of a 128-token uniform-random prompt
+into a 2048-position KV cache, then 99 greedy decode steps (100 tokens in total), inputs
+already on the device. ``value`` is decode tokens per second over the decode portion of
+the K timed steps; ``ttft_ms`` is the device time of the prefill (first token on device).
+Weights are random N(0, 0.02) bf16 of the real architecture (3.09 GB, far larger than L2,
+read once per token), so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+``--impl reference`` times the CPU oracle (float64 numpy) on a bounded sample of the same
+workload, on the host cores. Under torchrun every rank runs its own replica (batch-1
+decode does not shard; no collective is used on the data path) and rank 0 prints the line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import SHAPES, WORKLOADS, make_prompt, make_weights  # noqa: E402
+
+METRIC = "decode tok/s (Qwen2.5-1.5B shape, bs1, bf16)"
+WORKLOAD = "1p5b"
+
+
+def decode_bytes_per_token(s, ctx):
+    """Algorithmic HBM bytes of one decode token: every weight once (tied LM head read
+    once), the KV cache of ctx positions, the embedding row, and the fp32 logits."""
+    H, I, V, L = s.hidden, s.intermediate, s.vocab, s.n_layers
+    qd, kvd = s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim
+    e = 2 if s.dtype == "bf16" else 4
+    per_layer = (H * (qd + 2 * kvd) + (qd + 2 * kvd) + qd * H + 3 * H * I + 2 * H) * e
+    kv = L * 2 * kvd * ctx * e
+    return L * per_layer + V * H * e + H * e + H * e + kv + V * 4
+
+
+def gateup_bytes(s):
+    e = 2 if s.dtype == "bf16" else 4
+    return 2 * s.intermediate * s.hidden * e + s.hidden * e
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "qwen2_decoder_forward_decode_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, src_hash):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this
+    exact kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != src_hash:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r.split(",") for r in (self.out or "").strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_decode_sample(s, wl, n_decode, warmup=0):
+    """Time the CPU oracle: one untimed prefill of the workload's prompt, then decode
+    steps; returns (seconds per decode step list, threads)."""
+    import oracle
+    w = make_weights(s)
+    prompt = make_prompt(s, wl.prompt_len)
+    om = oracle.OracleModel(oracle.OracleConfig.from_shape(s), w)
+    del w
+    cache = oracle.KVCache(s.n_layers)
+    t, _ = oracle.step(om, list(prompt), np.arange(len(prompt)), cache)
+    seq = list(prompt) + [t]
+    times = []
+    for i in range(warmup + n_decode):
+        t0 = time.perf_counter()
+        t, _ = oracle.step(om, [seq[-1]], np.array([len(seq) - 1]), cache)
+        dt = time.perf_counter() - t0
+        seq.append(t)
+        if i >= warmup:
+            times.append(dt)
+    return times, os.cpu_count()
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    wl = WORKLOADS[WORKLOAD]
+    s = SHAPES[wl.shape]
+    times, cores = oracle_decode_sample(s, wl, args.steps, warmup=args.warmup)
+    total = sum(times)
+    value = len(times) / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "Qwen2.5-1.5B shape, bs1, 128-token prompt, KV cache 2048, "
+                               "greedy decode; one step = one oracle decode step after an untimed prefill",
+                   "global_batch": 1, "seq_len": wl.prompt_len},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{len(times)} decode steps at context {wl.prompt_len}+, float64 numpy"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args):
+    import torch
+    import __graft_entry__
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    __graft_entry__.build()
+    from qwen2_decoder_forward_decode_gb300 import DeviceWeights, Model
+
+    torch.cuda.set_device(local)
+    wl = WORKLOADS[WORKLOAD]
+    s = SHAPES[wl.shape]
+    n_dec = wl.new_tokens - 1
+    w = make_weights(s)
+    dw = DeviceWeights(w, 1)
+    prompt = make_prompt(s, wl.prompt_len)
+    stream = torch.cuda.Stream()
+    m = Model(s, dw, wl.kv_capacity, stream=stream.cuda_stream)
+    ids_dev = torch.from_numpy(prompt).to(f"cuda:{local}")
+    torch.cuda.synchronize()
+
+    def one_step():
+        m.prefill_device(ids_dev.data_ptr(), len(prompt))
+        m.decode_steps(n_dec)
+
+    for _ in range(args.warmup):
+        one_step()
+    m.sync()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_host0 = time.perf_counter()
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            m.prefill_device(ids_dev.data_ptr(), len(prompt))
+            ev[k][1].record(stream)
+            m.decode_steps(n_dec)
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        t_host = time.perf_counter() - t_host0
+    if ws > 1:
+        torch.distributed.barrier()
+    m.sync()
+    prefill_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
+    decode_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
+    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(args.steps)]
+    dec_s = sum(decode_ms) / 1000.0
+    if ws > 1:
+        t = torch.tensor([dec_s, sum(step_ms) / 1000.0], device=f"cuda:{local}", dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dec_s, tot_s = float(t[0]), float(t[1])
+    else:
+        tot_s = sum(step_ms) / 1000.0
+    tokens = n_dec * args.steps * ws
+    value = tokens / dec_s
+    ctx_mean = wl.prompt_len + (n_dec - 1) / 2.0 + 1  # positions read per decode token, mean
+    bpt = decode_bytes_per_token(s, ctx_mean)
+    peak, peak_kind = read_peaks()
+
+    # ---- dominant kernel (gate/up GEMV, 59% of a layer's bytes) timed with CUDA events
+    # around every layer's launch, over a traced pass of decode steps right after the
+    # timed region (the traced kernel runs without PDL overlap).
+    begin = [torch.cuda.Event(enable_timing=True) for _ in range(s.n_layers)]
+    end = [torch.cuda.Event(enable_timing=True) for _ in range(s.n_layers)]
+    m.set_trace(3, begin, end)
+    m.prefill_device(ids_dev.data_ptr(), len(prompt))
+    kt = []
+    for i in range(16):
+        m.decode_steps(1)
+        stream.synchronize()
+        if i >= 2:
+            kt += [b.elapsed_time(e) for b, e in zip(begin, end)]
+    m.set_trace(3, None, None)
+    gu_ms = float(np.mean(kt))
+    gu_bytes = gateup_bytes(s)
+    achieved = gu_bytes / (gu_ms / 1000.0) / 1e9
+    src = source_hash()
+    traffic = recorded_traffic("gateup_gemv", src)
+
+    # ---- end to end through the public API with host buffers (qw_generate: H2D of the
+    # prompt, prefill, decode loop, D2H of the tokens) and host-side TTFT (qw_prefill).
+    e2e_steps = max(1, min(args.steps, 5))
+    t_gen, t_pref = [], []
+    for _ in range(e2e_steps):
+        t0 = time.perf_counter()
+        toks = m.generate(prompt, wl.new_tokens)
+        t_gen.append(time.perf_counter() - t0)
+        assert len(toks) == wl.new_tokens
+        t0 = time.perf_counter()
+        m.prefill(prompt)
+        t_pref.append(time.perf_counter() - t0)
+    e2e_decode_s = max(1e-9, float(np.mean(t_gen)) - float(np.mean(t_pref)))
+    e2e_value = n_dec / e2e_decode_s * ws
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        times, cores = oracle_decode_sample(s, wl, 3)
+        cpu = {"value": len(times) / sum(times), "unit": "tok/s", "cores": cores, "kind": "oracle",
+               "sample": "3 float64-numpy decode steps after an untimed 128-token prefill "
+                         "(same weights, prompt and cache length)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * tot_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (random N(0,0.02) bf16 weights, uniform-random prompt ids)",
+            "config": {"workload": "Qwen2.5-1.5B shape (28 layers, hidden 1536, 12/2 heads, "
+                                   "head_dim 128, MLP 8960, vocab 151936, tied), bs1, 128-token "
+                                   "prompt, 100 greedy tokens, KV cache 2048",
+                       "global_batch": ws, "seq_len": wl.prompt_len,
+                       "parallelism": "replicas" if ws > 1 else "single",
+                       "l2": "inputs larger than L2 (3.09 GB of weights per token)",
+                       "step": "prefill + 99 decode steps; value counts decode tokens over decode time"},
+            "ttft_ms": float(np.mean(prefill_ms)),
+            "hbm_gbs": bpt * value / ws / 1e9,
+            "decode_bytes_per_token": bpt,
+            "decode_frac_of_hbm_peak": bpt * value / ws / 1e9 / peak,
+            "roofline": {"bound": "hbm", "kernel": "gateup_gemv", "achieved": achieved,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": gu_bytes, "launch_us": gu_ms * 1000.0},
+            "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4 * wl.prompt_len,
+                    "d2h_bytes_per_step": 4 * wl.new_tokens + 4,
+                    "how": "qw_generate with host buffers minus qw_prefill with host buffers, host wall clock",
+                    "generate_ms": 1000 * float(np.mean(t_gen)), "ttft_ms": 1000 * float(np.mean(t_pref))},
+            "gpu_launches": args.steps * ((2 + 12 * s.n_layers) + (5 * s.n_layers + 2) * n_dec),
+            "clocks": clk.summary(),
+            "host_ms_per_step": 1000 * t_host / args.steps,
+            "source_hash": src,
+        }
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    m.close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

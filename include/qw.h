@@ -1,0 +1,185 @@
+/*
+ * qw.h - C ABI of libqw, a GB300 (sm_103a) implementation of the forward pass of a
+ * Qwen2-style decoder-only transformer: prompt prefill into a preallocated KV cache and
+ * KV-cached greedy decode.
+ *
+ * The operations follow these pages (cited by title and section):
+ *   [LSA] "LLM Speedrun: Architecture": Transformer architecture (attention, causal mask,
+ *         SwiGLU FFN, pre-norm residual stacking, GQA, RoPE, Decoding / LM head / KV
+ *         cache) and Implementing Qwen (q/k/v bias, split-half RoPE, the model code's
+ *         Decoder.step and generate_tokens).
+ *   [AUG] "augur": Features (prefill/decode split, preallocated KV cache, greedy
+ *         generation, EOS stopping).
+ *   [QIE] "Building a Qwen2.5-1.5B Inference Engine From Scratch": §1 (prefill is
+ *         compute-bound, decode is memory-bandwidth-bound).
+ *
+ * Conventions for every call:
+ *   - Every call returns a qw_status; nothing aborts and nothing throws across the ABI.
+ *     qw_last_error() gives a message for the last failing call on the calling thread.
+ *   - "device" pointers are CUDA global-memory addresses on the device that was current
+ *     when qw_create ran; "host" pointers are ordinary CPU memory.
+ *   - Weights are BORROWED: the caller owns them, keeps them alive and unchanged until
+ *     qw_destroy, and the library never writes them.
+ *   - The library OWNS the KV cache, activations, logits, the RoPE table and the CUDA
+ *     graph of a decode step; all are released by qw_destroy.
+ *   - Work runs on the stream given to qw_create (or a stream the library creates when
+ *     that argument is NULL). Calls that return host values synchronise that stream
+ *     before returning.
+ *   - After QW_ERR_CUDA or QW_ERR_TIMEOUT the model must be destroyed.
+ */
+#ifndef QW_H
+#define QW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QW_OK = 0,
+  QW_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent config */
+  QW_ERR_UNSUPPORTED = 2,   /* a shape this build has no kernel for */
+  QW_ERR_CAPACITY = 3,      /* a sequence would exceed kv_capacity */
+  QW_ERR_TOKEN_RANGE = 4,   /* a token id outside [0, vocab) */
+  QW_ERR_CUDA = 5,          /* a CUDA runtime call failed; destroy the model */
+  QW_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up; destroy the model */
+  QW_ERR_FAULT_INJECTED = 7,/* QW_FAULT environment variable forced a failure */
+  QW_ERR_NUMERIC = 8        /* non-finite logits */
+} qw_status;
+
+typedef enum { QW_F32 = 0, QW_BF16 = 1 } qw_dtype;
+
+/* Model shape [LSA Implementing Qwen, the model configuration; AUG Qwen model config].
+ * head_dim must be even and equal hidden / n_heads (the score scale 1/sqrt(d_k) uses
+ * d_k = hidden / n_heads); n_heads must be a multiple of n_kv_heads. dtype is the storage
+ * type of weights and of the KV cache; activations, accumulators and logits are fp32. */
+typedef struct {
+  int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab;
+  float rms_eps;          /* RMSNorm epsilon, inside the square root (1e-6) */
+  float rope_theta;       /* RoPE base (1e6) */
+  int32_t tied_embeddings;/* 1: LM head is the embedding matrix */
+  int32_t qkv_bias;       /* 1: q/k/v projections carry a bias [LSA Introducing bias] */
+  int32_t dtype;          /* qw_dtype */
+  int32_t max_seqs;       /* independent sequences held at once (1..16) */
+  int32_t kv_capacity;    /* positions per sequence in the preallocated KV cache */
+} qw_config;
+
+/* Device pointers of one decoder layer, row-major [out, in], in qw_config.dtype.
+ * Sizes: in_norm, post_norm [hidden]; wq [n_heads*head_dim, hidden]; wk, wv
+ * [n_kv_heads*head_dim, hidden]; bq/bk/bv the matching vectors (NULL when qkv_bias is 0);
+ * wo [hidden, n_heads*head_dim]; w_gate, w_up [intermediate, hidden];
+ * w_down [hidden, intermediate]. Every pointer must be 16-byte aligned. */
+typedef struct {
+  const void *in_norm, *wq, *bq, *wk, *bk, *wv, *bv, *wo, *post_norm, *w_gate, *w_up,
+      *w_down;
+} qw_layer_weights;
+
+/* embed [vocab, hidden]; final_norm [hidden]; lm_head [vocab, hidden] or NULL when tied;
+ * layers is a HOST array of n_layers entries (copied by qw_create). */
+typedef struct {
+  const void *embed, *final_norm, *lm_head;
+  const qw_layer_weights *layers;
+} qw_weights;
+
+typedef struct qw_model qw_model;
+
+/* Validate the shape, allocate the KV cache [max_seqs][n_layers][2][n_kv_heads]
+ * [kv_capacity][head_dim] and the working buffers, and build the RoPE cos/sin table
+ * (angles in float64 on the host). cuda_stream is a cudaStream_t or NULL. */
+qw_status qw_create(const qw_config *cfg, const qw_weights *w, void *cuda_stream,
+                    qw_model **out);
+void qw_destroy(qw_model *m);
+
+/* Prefill [AUG Prefill/decode split; LSA Decoder.step on the whole prompt]: reset
+ * sequence `seq`, run the n prompt tokens (host array) at positions 0..n-1, fill their
+ * keys and values into the cache and compute the logits of the last position and its
+ * greedy token. Afterwards the sequence holds n positions and its next decode step feeds
+ * that token. next_token (host, may be NULL) receives it. Errors: QW_ERR_CAPACITY when
+ * n > kv_capacity, QW_ERR_TOKEN_RANGE for an id outside [0, vocab). */
+qw_status qw_prefill(qw_model *m, int32_t seq, const int32_t *ids, int32_t n,
+                     int32_t *next_token);
+
+/* The same with the prompt already in device memory; nothing is copied back and the
+ * stream is not synchronised (token ids are range-checked on the device, reported by
+ * qw_sync). */
+qw_status qw_prefill_device(qw_model *m, int32_t seq, const int32_t *ids_dev, int32_t n);
+
+/* One greedy decode step [LSA Decoding / KV cache; AUG greedy generation] for every
+ * sequence that has been prefilled: run one token at position pos (the sequence's current
+ * length), append its key and value at pos, compute the logits and the argmax, and
+ * advance the length by one. feed (host [max_seqs], may be NULL) overrides the token run
+ * for each sequence (teacher forcing); NULL runs each sequence's previous greedy token.
+ * next_tokens (host [max_seqs], may be NULL) receives the new tokens; when it is NULL the
+ * call does not synchronise. Errors: QW_ERR_CAPACITY when a sequence is full. */
+qw_status qw_decode_step(qw_model *m, const int32_t *feed, int32_t *next_tokens);
+
+/* n_steps decode steps of every active sequence, each feeding its own greedy token, with
+ * no host synchronisation. Tokens are kept on the device (qw_tokens_device). */
+qw_status qw_decode_steps(qw_model *m, int32_t n_steps);
+
+/* Greedy generation of one sequence (seq 0) [AUG EOS stopping; LSA generate_tokens]:
+ * prefill the n prompt ids (host), then decode until max_new tokens exist in total (the
+ * prefill's token counts) or a token equal to eos (eos < 0: never) has been produced; that
+ * token is kept. out (host [max_new]) receives the tokens, n_out their number. */
+qw_status qw_generate(qw_model *m, const int32_t *ids, int32_t n, int32_t max_new,
+                      int32_t eos, int32_t *out, int32_t *n_out);
+
+/* Wait for queued work and report a device-side error (token range, non-finite logits). */
+qw_status qw_sync(qw_model *m);
+
+/* Device pointer to the fp32 logits [max_seqs][vocab] of the last step; valid until the
+ * next call that runs the model. */
+const float *qw_logits(const qw_model *m);
+
+/* Copy the fp32 logits [vocab] of sequence seq's last step to host memory (synchronises). */
+qw_status qw_read_logits(qw_model *m, int32_t seq, float *host_out);
+
+/* Device pointer to int32 [max_seqs]: the greedy token of each sequence's last step. */
+const int32_t *qw_tokens_device(const qw_model *m);
+
+/* Current length (positions held in the cache) of sequence seq. */
+qw_status qw_position(const qw_model *m, int32_t seq, int32_t *pos);
+
+/* Forget sequence seq (length 0, inactive). */
+qw_status qw_reset(qw_model *m, int32_t seq);
+
+/* Profiling hook. With begin and end non-NULL (host arrays of n_layers cudaEvent_t created
+ * with timing enabled), every later decode step records begin[l] just before and end[l]
+ * just after kernel `kind` of layer l: 0 qkv, 1 attention, 2 o_proj, 3 gate/up, 4 down;
+ * kind 5 is the LM head (begin[0], end[0] only). The traced kernel and the one after it
+ * then launch without programmatic dependent launch. NULL arrays remove the hook. The
+ * decode graphs are rebuilt on the next step. */
+qw_status qw_set_trace(qw_model *m, int32_t kind, void *const *begin, void *const *end);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char *qw_last_error(void);
+
+/* ---- single operations, for testing a step of the path in isolation ---- */
+
+/* GQA decode attention of one token [LSA Attention, Causal mask, GQA]: for every query
+ * head h, scores s_j = q_h . K_j / sqrt(head_dim) over positions j = 0..ctx-1 of KV head
+ * h / (n_heads / n_kv_heads), softmax, and out_h = sum_j p_j V_j. The context is split
+ * into chunks whose partial softmax statistics are merged exactly (log-sum-exp).
+ *   q    device fp32 [n_heads*head_dim]
+ *   k, v device, dtype elements, [n_kv_heads][kv_stride][head_dim] (position-major per
+ *        head), ctx <= kv_stride
+ *   out  device fp32 [n_heads*head_dim]
+ *   workspace device, at least qw_op_decode_attention_workspace() bytes, 16-byte
+ *        aligned; its counters must be zero before the first call (cudaMemset) and the
+ *        call leaves them zero again.
+ * Runs on cuda_stream (NULL = default stream) and does not synchronise. */
+size_t qw_op_decode_attention_workspace(int32_t n_heads, int32_t n_kv_heads,
+                                        int32_t head_dim, int32_t max_ctx);
+qw_status qw_op_decode_attention(int32_t dtype, int32_t n_heads, int32_t n_kv_heads,
+                                 int32_t head_dim, int32_t ctx, int32_t kv_stride,
+                                 const float *q, const void *k, const void *v, float *out,
+                                 void *workspace, size_t workspace_bytes,
+                                 void *cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QW_H */

@@ -1,0 +1,609 @@
+// libqw C ABI: model creation, prefill, KV-cached greedy decode, generation.
+//
+// The model keeps all state on the device: the KV cache of every sequence, each
+// sequence's length and next token, the argmax key and a token history. A decode step of
+// one sequence is one CUDA graph (embedding, n_layers x {qkv, attn, o_proj, gate/up,
+// down}, LM head) captured on first use with programmatic-dependent-launch edges; because
+// positions and tokens live in device memory the same graph serves every step.
+#include "../../include/qw.h"
+#include "internal.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+using namespace qw;
+
+namespace {
+
+thread_local std::string g_err;
+
+qw_status fail(qw_status s, const std::string& msg) {
+  g_err = msg;
+  return s;
+}
+
+qw_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(QW_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+#define QW_CUDA(call)                                  \
+  do {                                                 \
+    cudaError_t e_ = (call);                           \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+bool fault_injected(const char* what) {
+  const char* f = std::getenv("QW_FAULT");
+  return f && std::strcmp(f, what) == 0;
+}
+
+constexpr int ATTN_CHUNK_MIN = 32;
+constexpr int OP_SM_HINT = 152;  // split count of the single-op attention entry point
+
+}  // namespace
+
+struct qw_model {
+  Dims d;
+  qw_config cfg;
+  std::vector<LayerPtrs> layers;
+  const void *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  int device = 0;
+  size_t esize = 4;
+  // device state
+  void* kv = nullptr;
+  float *x = nullptr, *q = nullptr, *attn = nullptr, *act = nullptr, *logits = nullptr;
+  float2* rope = nullptr;
+  void* attn_ws = nullptr;
+  size_t attn_smem = 0;
+  unsigned long long* keys = nullptr;
+  unsigned int* lm_counter = nullptr;
+  int *pos = nullptr, *tok = nullptr, *hist = nullptr, *hist_n = nullptr, *err = nullptr;
+  int* ids = nullptr;
+  int* pinned = nullptr;  // host staging, max(cap, max_seqs) ints
+  PrefillBufs pf{};
+  void* pf_block = nullptr;
+  // host mirror
+  std::vector<int> h_pos;
+  std::vector<char> active;
+  std::vector<cudaGraphExec_t> graphs;
+  bool use_graphs = true;
+  int trace_kind = -1;
+  std::vector<cudaEvent_t> trace_begin, trace_end;
+
+  size_t seq_kv_elems() const { return (size_t)d.L * 2 * d.nkv * d.cap * d.hd; }
+  char* kv_seq(int s) const { return (char*)kv + (size_t)s * seq_kv_elems() * esize; }
+  char* kc_layer(int s, int l) const {
+    return kv_seq(s) + (size_t)l * 2 * d.nkv * d.cap * d.hd * esize;
+  }
+  char* vc_layer(int s, int l) const {
+    return kc_layer(s, l) + (size_t)d.nkv * d.cap * d.hd * esize;
+  }
+  const void* head_w() const { return lm_head ? lm_head : embed; }
+
+  Finalize fin(int s, int pos_set) const {
+    Finalize f;
+    f.key = keys + s;
+    f.counter = lm_counter + s;
+    f.tok = tok + s;
+    f.pos = pos + s;
+    f.pos_set = pos_set;
+    f.hist = hist + (size_t)s * d.cap;
+    f.hist_n = hist_n + s;
+    f.hist_cap = d.cap;
+    f.err = err;
+    return f;
+  }
+
+  // Enqueue one decode step of sequence s (no host work besides launches).
+  cudaError_t enqueue_decode(int s) {
+    cudaError_t e;
+    float* xs = x + (size_t)s * d.H;
+    bool pdl = true;
+    // launch k-th kernel of layer l, with the optional trace events around it
+    auto run = [&](int kind, int l, auto&& launch) -> cudaError_t {
+      const bool traced = kind == trace_kind;
+      cudaError_t r;
+      if (traced && (r = cudaEventRecordWithFlags(trace_begin[l], stream, cudaEventRecordExternal)))
+        return r;
+      if ((r = launch(pdl && !traced))) return r;
+      pdl = true;
+      if (traced) {
+        if ((r = cudaEventRecordWithFlags(trace_end[l], stream, cudaEventRecordExternal))) return r;
+        pdl = false;
+      }
+      return cudaSuccess;
+    };
+    if ((e = launch_embed(d, embed, tok + s, xs, err, stream, false))) return e;
+    for (int l = 0; l < d.L; ++l) {
+      const LayerPtrs& w = layers[l];
+      void* kc = kc_layer(s, l);
+      void* vc = vc_layer(s, l);
+      if ((e = run(0, l, [&](bool p) { return launch_qkv(d, w, xs, pos + s, rope, q, kc, vc, stream, p); })))
+        return e;
+      if ((e = run(1, l, [&](bool p) {
+             return launch_attn(d.dtype, d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min,
+                                attn_smem, q, kc, vc, d.cap, pos + s, 0, attn, attn_ws, stream, p);
+           })))
+        return e;
+      if ((e = run(2, l, [&](bool p) { return launch_resid(d, w.wo, d.H, d.nq * d.hd, attn, xs, stream, p); })))
+        return e;
+      if ((e = run(3, l, [&](bool p) { return launch_gateup(d, w, xs, act, stream, p); }))) return e;
+      if ((e = run(4, l, [&](bool p) { return launch_resid(d, w.w_down, d.H, d.I, act, xs, stream, p); })))
+        return e;
+    }
+    return run(5, 0, [&](bool p) {
+      return launch_lmhead(d, head_w(), final_norm, xs, logits + (size_t)s * d.V, fin(s, -1), stream, p);
+    });
+  }
+
+  void drop_graphs() {
+    for (auto& g : graphs)
+      if (g) { cudaGraphExecDestroy(g); g = nullptr; }
+  }
+
+  cudaError_t run_decode(int s) {
+    if (!use_graphs) return enqueue_decode(s);
+    if (!graphs[s]) {
+      cudaGraph_t g = nullptr;
+      cudaError_t e = cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal);
+      if (e) return e;
+      e = enqueue_decode(s);
+      cudaError_t e2 = cudaStreamEndCapture(stream, &g);
+      if (e) { if (g) cudaGraphDestroy(g); return e; }
+      if (e2) return e2;
+      e = cudaGraphInstantiate(&graphs[s], g, 0);
+      cudaGraphDestroy(g);
+      if (e) { graphs[s] = nullptr; return e; }
+    }
+    return cudaGraphLaunch(graphs[s], stream);
+  }
+
+  cudaError_t ensure_prefill(int T) {
+    if (pf.cap_tokens >= T) return cudaSuccess;
+    if (pf_block) { cudaFree(pf_block); pf_block = nullptr; }
+    const size_t H = d.H, qd = (size_t)d.nq * d.hd, W = qd + 2 * (size_t)d.nkv * d.hd, I = d.I;
+    const size_t per_tok = H * 2 + W + qd * 2 + I * 2;  // X Xn Y Q O G U
+    cudaError_t e = cudaMalloc(&pf_block, per_tok * T * sizeof(float));
+    if (e) { pf_block = nullptr; pf.cap_tokens = 0; return e; }
+    float* p = (float*)pf_block;
+    pf.X = p; p += H * T;
+    pf.Xn = p; p += H * T;
+    pf.Y = p; p += W * T;
+    pf.Q = p; p += qd * T;
+    pf.O = p; p += qd * T;
+    pf.G = p; p += I * T;
+    pf.U = p;
+    pf.cap_tokens = T;
+    return cudaSuccess;
+  }
+
+  // prompt already in device memory at ids_dev
+  cudaError_t enqueue_prefill(int s, const int* ids_dev, int n) {
+    cudaError_t e;
+    if ((e = ensure_prefill(n))) return e;
+    if ((e = cudaMemsetAsync(hist_n + s, 0, sizeof(int), stream))) return e;
+    if ((e = prefill_layers(d, layers.data(), embed, ids_dev, n, 0, rope, kv_seq(s), nullptr, pf,
+                            err, stream)))
+      return e;
+    return launch_lmhead(d, head_w(), final_norm, pf.X + (size_t)(n - 1) * d.H,
+                         logits + (size_t)s * d.V, fin(s, n), stream, false);
+  }
+
+  qw_status check_device_errors() {
+    int h = 0;
+    QW_CUDA(cudaMemcpyAsync(&h, err, sizeof(int), cudaMemcpyDeviceToHost, stream));
+    QW_CUDA(cudaStreamSynchronize(stream));
+    if (h) {
+      QW_CUDA(cudaMemsetAsync(err, 0, sizeof(int), stream));
+      QW_CUDA(cudaStreamSynchronize(stream));
+      if (h & ERR_TOKEN) return fail(QW_ERR_TOKEN_RANGE, "token id outside [0, vocab) on the device");
+      if (h & ERR_NONFINITE) return fail(QW_ERR_NUMERIC, "non-finite logits");
+      if (h & ERR_TIMEOUT) return fail(QW_ERR_TIMEOUT, "device wait timed out");
+    }
+    return QW_OK;
+  }
+
+  void release() {
+    for (auto& g : graphs)
+      if (g) cudaGraphExecDestroy(g);
+    graphs.clear();
+    void* bufs[] = {kv, x, q, attn, act, logits, rope, attn_ws, keys, lm_counter, pos, tok,
+                    hist, hist_n, err, ids, pf_block};
+    for (void* b : bufs)
+      if (b) cudaFree(b);
+    if (pinned) cudaFreeHost(pinned);
+    if (own_stream && stream) cudaStreamDestroy(stream);
+  }
+};
+
+static qw_status validate(const qw_config* c, const qw_weights* w) {
+  if (!c || !w) return fail(QW_ERR_INVALID_ARG, "null config or weights");
+  if (c->n_layers < 1 || c->hidden < 1 || c->n_heads < 1 || c->n_kv_heads < 1 ||
+      c->head_dim < 2 || c->intermediate < 1 || c->vocab < 1 || c->kv_capacity < 1 ||
+      c->max_seqs < 1)
+    return fail(QW_ERR_INVALID_ARG, "non-positive dimension in config");
+  if (c->max_seqs > 16) return fail(QW_ERR_UNSUPPORTED, "max_seqs above 16");
+  if (c->head_dim % 2) return fail(QW_ERR_INVALID_ARG, "head_dim must be even");
+  if (c->n_heads % c->n_kv_heads) return fail(QW_ERR_INVALID_ARG, "n_heads not a multiple of n_kv_heads");
+  if (c->n_heads * c->head_dim != c->hidden)
+    return fail(QW_ERR_UNSUPPORTED, "head_dim must equal hidden / n_heads");
+  if (c->n_heads / c->n_kv_heads > 8) return fail(QW_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+  if (c->dtype != QW_F32 && c->dtype != QW_BF16) return fail(QW_ERR_INVALID_ARG, "unknown dtype");
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return fail(QW_ERR_INVALID_ARG, "bad eps or theta");
+  const int hd = c->head_dim;
+  if (hd != 16 && hd != 32 && hd != 64 && hd != 128) return fail(QW_ERR_UNSUPPORTED, "head_dim must be 16, 32, 64 or 128");
+  const int vec = c->dtype == QW_BF16 ? 8 : 4;
+  if (c->hidden % vec || c->intermediate % vec)
+    return fail(QW_ERR_UNSUPPORTED, "hidden and intermediate must be multiples of 16 bytes of weights");
+  if (c->hidden > 8 * 32 * 8 * vec || c->intermediate > 8 * 32 * 8 * vec)
+    return fail(QW_ERR_UNSUPPORTED, "hidden or intermediate too large for the decode GEMV");
+  if (!w->embed || !w->final_norm || !w->layers) return fail(QW_ERR_INVALID_ARG, "null weight pointer");
+  if (!c->tied_embeddings && !w->lm_head) return fail(QW_ERR_INVALID_ARG, "untied model without lm_head");
+  for (int l = 0; l < c->n_layers; ++l) {
+    const qw_layer_weights& L = w->layers[l];
+    const void* req[] = {L.in_norm, L.wq, L.wk, L.wv, L.wo, L.post_norm, L.w_gate, L.w_up, L.w_down};
+    for (const void* p : req) {
+      if (!p) return fail(QW_ERR_INVALID_ARG, "null layer weight pointer");
+      if ((uintptr_t)p % 16) return fail(QW_ERR_INVALID_ARG, "layer weight not 16-byte aligned");
+    }
+    if (c->qkv_bias && (!L.bq || !L.bk || !L.bv)) return fail(QW_ERR_INVALID_ARG, "qkv_bias set but a bias is null");
+  }
+  if ((uintptr_t)w->embed % 16) return fail(QW_ERR_INVALID_ARG, "embedding not 16-byte aligned");
+  if (w->lm_head && (uintptr_t)w->lm_head % 16) return fail(QW_ERR_INVALID_ARG, "lm_head not 16-byte aligned");
+  return QW_OK;
+}
+
+extern "C" {
+
+const char* qw_last_error(void) { return g_err.c_str(); }
+
+qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream, qw_model** out) {
+  g_err.clear();
+  if (!out) return fail(QW_ERR_INVALID_ARG, "null output pointer");
+  *out = nullptr;
+  qw_status st = validate(cfg, w);
+  if (st) return st;
+  if (fault_injected("alloc")) return fail(QW_ERR_FAULT_INJECTED, "QW_FAULT=alloc");
+  qw_model* m = new qw_model();
+  m->cfg = *cfg;
+  Dims& d = m->d;
+  d.L = cfg->n_layers; d.H = cfg->hidden; d.nq = cfg->n_heads; d.nkv = cfg->n_kv_heads;
+  d.hd = cfg->head_dim; d.I = cfg->intermediate; d.V = cfg->vocab;
+  d.eps = cfg->rms_eps; d.theta = cfg->rope_theta; d.dtype = cfg->dtype;
+  d.cap = cfg->kv_capacity; d.max_seqs = cfg->max_seqs;
+  m->esize = cfg->dtype == QW_BF16 ? 2 : 4;
+  auto bail = [&](cudaError_t e, const char* where) {
+    m->release();
+    delete m;
+    return cuda_fail(e, where);
+  };
+  cudaError_t e;
+  if ((e = cudaGetDevice(&m->device))) return bail(e, "cudaGetDevice");
+  if ((e = cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, m->device)))
+    return bail(e, "cudaDeviceGetAttribute");
+  d.attn_chunk_min = ATTN_CHUNK_MIN;
+  d.attn_nsplit = attn_nsplit_for(d.nsm, d.nkv, d.cap, d.attn_chunk_min);
+  m->attn_smem = attn_smem_bytes(d.nq / d.nkv, d.hd, d.cap, d.attn_nsplit, d.attn_chunk_min);
+  if (cuda_stream) {
+    m->stream = (cudaStream_t)cuda_stream;
+  } else {
+    if ((e = cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking))) return bail(e, "cudaStreamCreate");
+    m->own_stream = true;
+  }
+  m->embed = w->embed;
+  m->final_norm = w->final_norm;
+  m->lm_head = cfg->tied_embeddings ? nullptr : w->lm_head;
+  for (int l = 0; l < d.L; ++l) {
+    const qw_layer_weights& L = w->layers[l];
+    LayerPtrs p{L.in_norm, L.wq, cfg->qkv_bias ? L.bq : nullptr, L.wk, cfg->qkv_bias ? L.bk : nullptr,
+                L.wv, cfg->qkv_bias ? L.bv : nullptr, L.wo, L.post_norm, L.w_gate, L.w_up, L.w_down};
+    m->layers.push_back(p);
+  }
+  const int S = d.max_seqs;
+  const size_t kv_bytes = (size_t)S * m->seq_kv_elems() * m->esize;
+  if ((e = cudaMalloc(&m->kv, kv_bytes))) return bail(e, "cudaMalloc(kv cache)");
+  if ((e = cudaMemset(m->kv, 0, kv_bytes))) return bail(e, "cudaMemset(kv cache)");
+  if ((e = cudaMalloc(&m->x, sizeof(float) * S * d.H))) return bail(e, "cudaMalloc");
+  if ((e = cudaMalloc(&m->q, sizeof(float) * d.nq * d.hd))) return bail(e, "cudaMalloc");
+  if ((e = cudaMalloc(&m->attn, sizeof(float) * d.nq * d.hd))) return bail(e, "cudaMalloc");
+  if ((e = cudaMalloc(&m->act, sizeof(float) * d.I))) return bail(e, "cudaMalloc");
+  if ((e = cudaMalloc(&m->logits, sizeof(float) * S * (size_t)d.V))) return bail(e, "cudaMalloc");
+  if ((e = cudaMemset(m->logits, 0, sizeof(float) * S * (size_t)d.V))) return bail(e, "cudaMemset");
+  const size_t ws = attn_workspace_bytes(d.nq, d.nkv, d.hd, d.attn_nsplit);
+  if ((e = cudaMalloc(&m->attn_ws, ws))) return bail(e, "cudaMalloc");
+  if ((e = cudaMemset(m->attn_ws, 0, ws))) return bail(e, "cudaMemset");
+  if ((e = cudaMalloc(&m->keys, sizeof(unsigned long long) * S))) return bail(e, "cudaMalloc");
+  if ((e = cudaMemset(m->keys, 0, sizeof(unsigned long long) * S))) return bail(e, "cudaMemset");
+  if ((e = cudaMalloc(&m->lm_counter, sizeof(unsigned int) * S))) return bail(e, "cudaMalloc");
+  if ((e = cudaMemset(m->lm_counter, 0, sizeof(unsigned int) * S))) return bail(e, "cudaMemset");
+  if ((e = cudaMalloc(&m->pos, sizeof(int) * S))) return bail(e, "cudaMalloc");
+  if ((e = cudaMalloc(&m->tok, sizeof(int) * S))) return bail(e, "cudaMalloc");
+  if ((e = cudaMalloc(&m->hist_n, sizeof(int) * S))) return bail(e, "cudaMalloc");
+  if ((e = cudaMalloc(&m->err, sizeof(int)))) return bail(e, "cudaMalloc");
+  if ((e = cudaMalloc(&m->hist, sizeof(int) * S * (size_t)d.cap))) return bail(e, "cudaMalloc");
+  if ((e = cudaMalloc(&m->ids, sizeof(int) * (size_t)d.cap))) return bail(e, "cudaMalloc");
+  cudaMemset(m->pos, 0, sizeof(int) * S);
+  cudaMemset(m->tok, 0, sizeof(int) * S);
+  cudaMemset(m->hist_n, 0, sizeof(int) * S);
+  cudaMemset(m->err, 0, sizeof(int));
+  const size_t pin_n = (size_t)(d.cap > S ? d.cap : S);
+  if ((e = cudaMallocHost(&m->pinned, sizeof(int) * pin_n))) return bail(e, "cudaMallocHost");
+  // RoPE table: angle = pos * theta^(-2i/hd), evaluated in double precision
+  {
+    const int half = d.hd / 2;
+    std::vector<float2> tab((size_t)d.cap * half);
+    for (int p = 0; p < d.cap; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double ang = (double)p * std::pow((double)cfg->rope_theta, -2.0 * i / d.hd);
+        tab[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    if ((e = cudaMalloc(&m->rope, sizeof(float2) * tab.size()))) return bail(e, "cudaMalloc");
+    if ((e = cudaMemcpy(m->rope, tab.data(), sizeof(float2) * tab.size(), cudaMemcpyHostToDevice)))
+      return bail(e, "cudaMemcpy(rope)");
+  }
+  if ((e = decode_set_attributes(d))) return bail(e, "decode attributes");
+  if ((e = attn_set_attributes(m->attn_smem))) return bail(e, "attention attributes");
+  if ((e = prefill_set_attributes(d))) return bail(e, "prefill attributes");
+  if ((e = cudaDeviceSynchronize())) return bail(e, "cudaDeviceSynchronize");
+  m->h_pos.assign(S, 0);
+  m->active.assign(S, 0);
+  m->graphs.assign(S, nullptr);
+  const char* ng = std::getenv("QW_NO_GRAPH");
+  m->use_graphs = !(ng && ng[0] == '1');
+  *out = m;
+  return QW_OK;
+}
+
+void qw_destroy(qw_model* m) {
+  if (!m) return;
+  cudaStreamSynchronize(m->stream);
+  m->release();
+  delete m;
+}
+
+static qw_status prefill_common(qw_model* m, int32_t seq, int32_t n) {
+  if (!m) return fail(QW_ERR_INVALID_ARG, "null model");
+  if (seq < 0 || seq >= m->d.max_seqs) return fail(QW_ERR_INVALID_ARG, "sequence index out of range");
+  if (n < 1) return fail(QW_ERR_INVALID_ARG, "empty prompt");
+  if (n > m->d.cap) return fail(QW_ERR_CAPACITY, "prompt longer than kv_capacity");
+  return QW_OK;
+}
+
+qw_status qw_prefill_device(qw_model* m, int32_t seq, const int32_t* ids_dev, int32_t n) {
+  g_err.clear();
+  qw_status st = prefill_common(m, seq, n);
+  if (st) return st;
+  if (!ids_dev) return fail(QW_ERR_INVALID_ARG, "null ids");
+  QW_CUDA(m->enqueue_prefill(seq, ids_dev, n));
+  m->h_pos[seq] = n;
+  m->active[seq] = 1;
+  return QW_OK;
+}
+
+qw_status qw_prefill(qw_model* m, int32_t seq, const int32_t* ids, int32_t n, int32_t* next_token) {
+  g_err.clear();
+  qw_status st = prefill_common(m, seq, n);
+  if (st) return st;
+  if (!ids) return fail(QW_ERR_INVALID_ARG, "null ids");
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= m->d.V) return fail(QW_ERR_TOKEN_RANGE, "prompt token id outside [0, vocab)");
+  QW_CUDA(cudaStreamSynchronize(m->stream));  // the pinned staging buffer is reused
+  std::memcpy(m->pinned, ids, sizeof(int) * n);
+  QW_CUDA(cudaMemcpyAsync(m->ids, m->pinned, sizeof(int) * n, cudaMemcpyHostToDevice, m->stream));
+  QW_CUDA(m->enqueue_prefill(seq, m->ids, n));
+  m->h_pos[seq] = n;
+  m->active[seq] = 1;
+  if (next_token) {
+    QW_CUDA(cudaMemcpyAsync(m->pinned, m->tok + seq, sizeof(int), cudaMemcpyDeviceToHost, m->stream));
+    st = m->check_device_errors();
+    if (st) return st;
+    *next_token = m->pinned[0];
+  }
+  return QW_OK;
+}
+
+static qw_status decode_prepare(qw_model* m) {
+  bool any = false;
+  for (int s = 0; s < m->d.max_seqs; ++s) {
+    if (!m->active[s]) continue;
+    any = true;
+    if (m->h_pos[s] + 1 > m->d.cap) return fail(QW_ERR_CAPACITY, "sequence reached kv_capacity");
+  }
+  if (!any) return fail(QW_ERR_INVALID_ARG, "no prefilled sequence");
+  if (fault_injected("launch")) return fail(QW_ERR_FAULT_INJECTED, "QW_FAULT=launch");
+  return QW_OK;
+}
+
+qw_status qw_decode_step(qw_model* m, const int32_t* feed, int32_t* next_tokens) {
+  g_err.clear();
+  if (!m) return fail(QW_ERR_INVALID_ARG, "null model");
+  qw_status st = decode_prepare(m);
+  if (st) return st;
+  const int S = m->d.max_seqs;
+  if (feed) {
+    for (int s = 0; s < S; ++s)
+      if (m->active[s] && (feed[s] < 0 || feed[s] >= m->d.V))
+        return fail(QW_ERR_TOKEN_RANGE, "fed token id outside [0, vocab)");
+    QW_CUDA(cudaStreamSynchronize(m->stream));
+    for (int s = 0; s < S; ++s) m->pinned[s] = feed[s];
+    for (int s = 0; s < S; ++s)
+      if (m->active[s])
+        QW_CUDA(cudaMemcpyAsync(m->tok + s, m->pinned + s, sizeof(int), cudaMemcpyHostToDevice, m->stream));
+  }
+  for (int s = 0; s < S; ++s) {
+    if (!m->active[s]) continue;
+    QW_CUDA(m->run_decode(s));
+    m->h_pos[s] += 1;
+  }
+  if (next_tokens) {
+    QW_CUDA(cudaStreamSynchronize(m->stream));
+    QW_CUDA(cudaMemcpyAsync(m->pinned, m->tok, sizeof(int) * S, cudaMemcpyDeviceToHost, m->stream));
+    st = m->check_device_errors();
+    if (st) return st;
+    for (int s = 0; s < S; ++s) next_tokens[s] = m->active[s] ? m->pinned[s] : -1;
+  }
+  return QW_OK;
+}
+
+qw_status qw_decode_steps(qw_model* m, int32_t n_steps) {
+  g_err.clear();
+  if (!m) return fail(QW_ERR_INVALID_ARG, "null model");
+  if (n_steps < 0) return fail(QW_ERR_INVALID_ARG, "negative step count");
+  for (int i = 0; i < n_steps; ++i) {
+    qw_status st = decode_prepare(m);
+    if (st) return st;
+    for (int s = 0; s < m->d.max_seqs; ++s) {
+      if (!m->active[s]) continue;
+      QW_CUDA(m->run_decode(s));
+      m->h_pos[s] += 1;
+    }
+  }
+  return QW_OK;
+}
+
+qw_status qw_generate(qw_model* m, const int32_t* ids, int32_t n, int32_t max_new, int32_t eos,
+                      int32_t* out, int32_t* n_out) {
+  g_err.clear();
+  if (!m || !out || !n_out) return fail(QW_ERR_INVALID_ARG, "null argument");
+  if (max_new < 1) return fail(QW_ERR_INVALID_ARG, "max_new must be positive");
+  qw_status st = prefill_common(m, 0, n);
+  if (st) return st;
+  if ((int64_t)n + max_new - 1 > m->d.cap) return fail(QW_ERR_CAPACITY, "prompt + max_new - 1 exceeds kv_capacity");
+  for (int s = 1; s < m->d.max_seqs; ++s) m->active[s] = 0;
+  st = qw_prefill(m, 0, ids, n, nullptr);
+  if (st) return st;
+  const int chunk = eos >= 0 ? 16 : max_new;
+  int done = 1;  // tokens produced so far
+  int produced_total = 1;
+  while (true) {
+    const int steps = std::min(chunk, max_new - done);
+    for (int i = 0; i < steps; ++i) {
+      QW_CUDA(m->run_decode(0));
+      m->h_pos[0] += 1;
+    }
+    done += steps;
+    produced_total = done;
+    QW_CUDA(cudaMemcpyAsync(m->pinned, m->hist, sizeof(int) * done, cudaMemcpyDeviceToHost, m->stream));
+    st = m->check_device_errors();
+    if (st) return st;
+    int cut = -1;
+    if (eos >= 0)
+      for (int i = 0; i < done; ++i)
+        if (m->pinned[i] == eos) { cut = i + 1; break; }
+    if (cut > 0 || done >= max_new) {
+      const int k = cut > 0 ? cut : done;
+      std::memcpy(out, m->pinned, sizeof(int) * k);
+      *n_out = k;
+      if (k < produced_total) {  // steps ran past eos: roll length and next token back
+        const int len = n + k - 1;
+        m->h_pos[0] = len;
+        m->pinned[0] = len;
+        m->pinned[1] = out[k - 1];
+        QW_CUDA(cudaMemcpyAsync(m->pos, &m->pinned[0], sizeof(int), cudaMemcpyHostToDevice, m->stream));
+        QW_CUDA(cudaMemcpyAsync(m->tok, &m->pinned[1], sizeof(int), cudaMemcpyHostToDevice, m->stream));
+        QW_CUDA(cudaStreamSynchronize(m->stream));
+      }
+      return QW_OK;
+    }
+  }
+}
+
+qw_status qw_sync(qw_model* m) {
+  g_err.clear();
+  if (!m) return fail(QW_ERR_INVALID_ARG, "null model");
+  return m->check_device_errors();
+}
+
+const float* qw_logits(const qw_model* m) { return m ? m->logits : nullptr; }
+qw_status qw_set_trace(qw_model* m, int32_t kind, void* const* begin, void* const* end) {
+  g_err.clear();
+  if (!m) return fail(QW_ERR_INVALID_ARG, "null model");
+  QW_CUDA(cudaStreamSynchronize(m->stream));
+  m->drop_graphs();
+  if (!begin || !end) {
+    m->trace_kind = -1;
+    m->trace_begin.clear();
+    m->trace_end.clear();
+    return QW_OK;
+  }
+  if (kind < 0 || kind > 5) return fail(QW_ERR_INVALID_ARG, "unknown kernel kind");
+  const int n = kind == 5 ? 1 : m->d.L;
+  m->trace_begin.assign((cudaEvent_t*)begin, (cudaEvent_t*)begin + n);
+  m->trace_end.assign((cudaEvent_t*)end, (cudaEvent_t*)end + n);
+  for (int i = 0; i < n; ++i)
+    if (!m->trace_begin[i] || !m->trace_end[i]) return fail(QW_ERR_INVALID_ARG, "null event");
+  m->trace_kind = kind;
+  return QW_OK;
+}
+
+qw_status qw_read_logits(qw_model* m, int32_t seq, float* host_out) {
+  g_err.clear();
+  if (!m || !host_out) return fail(QW_ERR_INVALID_ARG, "null argument");
+  if (seq < 0 || seq >= m->d.max_seqs) return fail(QW_ERR_INVALID_ARG, "sequence index out of range");
+  QW_CUDA(cudaMemcpyAsync(host_out, m->logits + (size_t)seq * m->d.V, sizeof(float) * m->d.V,
+                          cudaMemcpyDeviceToHost, m->stream));
+  return m->check_device_errors();
+}
+
+const int32_t* qw_tokens_device(const qw_model* m) { return m ? m->tok : nullptr; }
+
+qw_status qw_position(const qw_model* m, int32_t seq, int32_t* pos) {
+  if (!m || !pos) return fail(QW_ERR_INVALID_ARG, "null argument");
+  if (seq < 0 || seq >= m->d.max_seqs) return fail(QW_ERR_INVALID_ARG, "sequence index out of range");
+  *pos = m->active[seq] ? m->h_pos[seq] : 0;
+  return QW_OK;
+}
+
+qw_status qw_reset(qw_model* m, int32_t seq) {
+  if (!m) return fail(QW_ERR_INVALID_ARG, "null model");
+  if (seq < 0 || seq >= m->d.max_seqs) return fail(QW_ERR_INVALID_ARG, "sequence index out of range");
+  m->active[seq] = 0;
+  m->h_pos[seq] = 0;
+  QW_CUDA(cudaMemsetAsync(m->pos + seq, 0, sizeof(int), m->stream));
+  return QW_OK;
+}
+
+// ---- single-op entry points ----
+
+static int op_attn_nsplit(int nkv, int max_ctx) {
+  return attn_nsplit_for(OP_SM_HINT, nkv, max_ctx, ATTN_CHUNK_MIN);
+}
+
+size_t qw_op_decode_attention_workspace(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                        int32_t max_ctx) {
+  if (n_heads < 1 || n_kv_heads < 1 || head_dim < 2 || max_ctx < 1) return 0;
+  return attn_workspace_bytes(n_heads, n_kv_heads, head_dim, op_attn_nsplit(n_kv_heads, max_ctx));
+}
+
+qw_status qw_op_decode_attention(int32_t dtype, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                 int32_t ctx, int32_t kv_stride, const float* q, const void* k,
+                                 const void* v, float* out, void* workspace, size_t workspace_bytes,
+                                 void* cuda_stream) {
+  g_err.clear();
+  if (!q || !k || !v || !out || !workspace) return fail(QW_ERR_INVALID_ARG, "null pointer");
+  if (dtype != QW_F32 && dtype != QW_BF16) return fail(QW_ERR_INVALID_ARG, "unknown dtype");
+  if (n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || head_dim < 2 || ctx < 1 || kv_stride < ctx)
+    return fail(QW_ERR_INVALID_ARG, "bad attention shape");
+  if (n_heads / n_kv_heads > 8) return fail(QW_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+  const int nsplit = op_attn_nsplit(n_kv_heads, kv_stride);
+  const size_t need = attn_workspace_bytes(n_heads, n_kv_heads, head_dim, nsplit);
+  if (workspace_bytes < need) return fail(QW_ERR_INVALID_ARG, "workspace too small");
+  if ((uintptr_t)workspace % 16) return fail(QW_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  const size_t smem = attn_smem_bytes(n_heads / n_kv_heads, head_dim, kv_stride, nsplit, ATTN_CHUNK_MIN);
+  if (smem > 200 * 1024) return fail(QW_ERR_UNSUPPORTED, "attention chunk too large");
+  cudaError_t e = attn_set_attributes(smem);
+  if (e) return cuda_fail(e, "decode attention attributes");
+  e = launch_attn(dtype, n_heads, n_kv_heads, head_dim, nsplit, ATTN_CHUNK_MIN, smem, q, k, v,
+                              kv_stride, nullptr, ctx, out, workspace, (cudaStream_t)cuda_stream, false);
+  if (e) return cuda_fail(e, "decode attention launch");
+  return QW_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// Shared device helpers for the libqw kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qw {
+
+typedef __nv_bfloat16 bf16;
+
+// Programmatic dependent launch: wait for the upstream grid's completion and memory,
+// and allow the downstream grid to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename T> struct Vec;
+template <> struct Vec<float> { static constexpr int N = 4; };
+template <> struct Vec<bf16> { static constexpr int N = 8; };
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// 16-byte streaming load of read-only data (weights): no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// dot of one 16-byte vector of weights with VEC fp32 inputs
+__device__ __forceinline__ float dotv(const uint4& w, const float* x, float acc, float) {
+  acc = fmaf(__uint_as_float(w.x), x[0], acc);
+  acc = fmaf(__uint_as_float(w.y), x[1], acc);
+  acc = fmaf(__uint_as_float(w.z), x[2], acc);
+  acc = fmaf(__uint_as_float(w.w), x[3], acc);
+  return acc;
+}
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float dotv(const uint4& w, const float* x, float acc, bf16) {
+  acc = fmaf(bf_lo(w.x), x[0], acc);
+  acc = fmaf(bf_hi(w.x), x[1], acc);
+  acc = fmaf(bf_lo(w.y), x[2], acc);
+  acc = fmaf(bf_hi(w.y), x[3], acc);
+  acc = fmaf(bf_lo(w.z), x[4], acc);
+  acc = fmaf(bf_hi(w.z), x[5], acc);
+  acc = fmaf(bf_lo(w.w), x[6], acc);
+  acc = fmaf(bf_hi(w.w), x[7], acc);
+  return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Sum over the block (any blockDim multiple of 32, <= 1024). All threads get the result.
+__device__ __forceinline__ float block_sum(float v, float* scratch32) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) scratch32[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int i = 0; i < nw; ++i) t += scratch32[i];  // fixed order: deterministic
+  return t;
+}
+
+// Orderable 64-bit argmax key: larger value wins, then the lower index.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xffffffffu - (uint32_t)idx);
+}
+__device__ __forceinline__ int argmax_key_index(unsigned long long k) {
+  return (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+}
+
+}  // namespace qw

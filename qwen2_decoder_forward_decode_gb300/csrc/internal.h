@@ -1,0 +1,78 @@
+// Host-side declarations shared by the libqw translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace qw {
+
+// Device-side error bits, OR-ed into the model's status word.
+enum : int { ERR_TOKEN = 1, ERR_NONFINITE = 2, ERR_TIMEOUT = 4 };
+
+struct Dims {
+  int L, H, nq, nkv, hd, I, V;
+  float eps, theta;
+  int dtype;      // 0 f32, 1 bf16 (weights and KV cache)
+  int cap;        // KV positions per sequence
+  int max_seqs;
+  int nsm;        // SM count of the device
+  int attn_nsplit;  // maximum context splits of decode attention
+  int attn_chunk_min;
+};
+
+struct LayerPtrs {
+  const void *in_norm, *wq, *bq, *wk, *bk, *wv, *bv, *wo, *post_norm, *w_gate, *w_up, *w_down;
+};
+
+// Argmax / position bookkeeping written by the last CTA of the LM-head kernel.
+struct Finalize {
+  unsigned long long* key;  // packed argmax key, reset to 0 after use
+  unsigned int* counter;    // CTA arrival counter, reset to 0 after use
+  int* tok;                 // greedy token out
+  int* pos;                 // sequence length
+  int pos_set;              // >= 0: set length to this value; < 0: length += 1
+  int* hist;                // token history (may be null)
+  int* hist_n;              // its count
+  int hist_cap;
+  int* err;
+};
+
+// ---- decode.cu ----
+size_t attn_workspace_bytes(int nq, int nkv, int hd, int nsplit);
+int attn_nsplit_for(int nsm, int nkv, int cap, int chunk_min);
+size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min);
+cudaError_t decode_set_attributes(const Dims& d);
+cudaError_t attn_set_attributes(size_t smem);  // not during stream capture
+
+cudaError_t launch_embed(const Dims& d, const void* E, const int* tok, float* x, int* err,
+                         cudaStream_t s, bool pdl);
+cudaError_t launch_qkv(const Dims& d, const LayerPtrs& w, const float* x, const int* d_pos,
+                       const float2* rope, float* q, void* kc, void* vc, cudaStream_t s,
+                       bool pdl);
+// ctx = d_pos ? d_pos[0] + 1 : ctx_host
+cudaError_t launch_attn(int dtype, int nq, int nkv, int hd, int nsplit, int chunk_min,
+                        size_t smem, const float* q, const void* kc, const void* vc,
+                        int kv_stride, const int* d_pos, int ctx_host, float* out, void* ws,
+                        cudaStream_t s, bool pdl);
+// y[r] += W[r,:] . in  (r < N), W [N, K]
+cudaError_t launch_resid(const Dims& d, const void* W, int N, int K, const float* in, float* y,
+                         cudaStream_t s, bool pdl);
+cudaError_t launch_gateup(const Dims& d, const LayerPtrs& w, const float* x, float* act,
+                          cudaStream_t s, bool pdl);
+cudaError_t launch_lmhead(const Dims& d, const void* W, const void* final_norm, const float* x,
+                          float* logits, const Finalize& f, cudaStream_t s, bool pdl);
+
+// ---- prefill.cu ----
+struct PrefillBufs {
+  float *X, *Xn, *Y, *Q, *O, *G, *U;  // [T][..] fp32 activations
+  int cap_tokens;
+};
+cudaError_t prefill_set_attributes(const Dims& d);
+// Runs all layers over T tokens at positions pos0..pos0+T-1 of one sequence.
+cudaError_t prefill_layers(const Dims& d, const LayerPtrs* layers, const void* embed,
+                           const int* ids_dev, int T, int pos0, const float2* rope,
+                           void* kcache_seq, void* vcache_seq, const PrefillBufs& b, int* err,
+                           cudaStream_t s);
+
+}  // namespace qw

@@ -1,0 +1,311 @@
+// Prefill of T prompt tokens of one sequence ("augur", Features: prefill/decode split;
+// "LLM Speedrun: Architecture", Transformer architecture / Implementing Qwen).
+//
+// Row-major activations [T][features] in fp32. Per layer:
+//   norm rows -> Q/K/V GEMMs (+bias) -> RoPE + KV-cache write -> causal GQA attention ->
+//   o_proj GEMM (+= residual) -> norm rows -> gate/up GEMMs -> SwiGLU -> down GEMM (+=).
+// This translation unit holds the CUDA-core (SIMT) versions: exact fp32 arithmetic on
+// any shape, used by the fp32 models and as the general path.
+#include "common.cuh"
+#include "internal.h"
+
+#include <math.h>
+
+namespace qw {
+
+// ---- row kernels -------------------------------------------------------------------------
+
+template <typename T>
+__global__ void embed_rows_kernel(const T* E, int V, int H, const int* ids, float* X, int* err) {
+  const int t = blockIdx.x;
+  int id = ids[t];
+  if (id < 0 || id >= V) {
+    if (threadIdx.x == 0) atomicOr(err, ERR_TOKEN);
+    id = 0;
+  }
+  const T* row = E + (size_t)id * H;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) X[(size_t)t * H + k] = to_f32(row[k]);
+}
+
+template <typename T>
+__global__ void norm_rows_kernel(const float* X, const T* gain, int H, float eps, float* Y) {
+  __shared__ float scratch[32];
+  const float* x = X + (size_t)blockIdx.x * H;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) ss = fmaf(x[k], x[k], ss);
+  ss = block_sum(ss, scratch);
+  const float inv = rsqrtf(ss / (float)H + eps);
+  float* y = Y + (size_t)blockIdx.x * H;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) y[k] = x[k] * inv * to_f32(gain[k]);
+}
+
+__global__ void swiglu_kernel(const float* G, const float* U, float* A, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float g = G[i];
+    A[i] = (g / (1.f + expf(-g))) * U[i];
+  }
+}
+
+// Y [T][nq*hd + 2*nkv*hd] (q | k | v, bias included) -> Q [T][nq*hd] rotated;
+// K, V rotated/copied into the cache at positions pos0 + t.
+template <typename T>
+__global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, int pos0, int cap,
+                               const float2* rope, float* Q, T* kc, T* vc) {
+  const int t = blockIdx.x;
+  const int half = hd / 2;
+  const int width = (nq + 2 * nkv) * hd;
+  const int pos = pos0 + t;
+  const float* y = Y + (size_t)t * width;
+  for (int idx = threadIdx.x; idx < (nq + 2 * nkv) * half; idx += blockDim.x) {
+    const int head = idx / half, i = idx - head * half;
+    const float a = y[head * hd + i], b = y[head * hd + i + half];
+    if (head < nq + nkv) {
+      const float2 cs = rope[(size_t)pos * half + i];
+      const float ra = a * cs.x - b * cs.y, rb = b * cs.x + a * cs.y;
+      if (head < nq) {
+        Q[(size_t)t * nq * hd + head * hd + i] = ra;
+        Q[(size_t)t * nq * hd + head * hd + i + half] = rb;
+      } else {
+        T* dst = kc + ((size_t)(head - nq) * cap + pos) * hd;
+        dst[i] = from_f32<T>(ra);
+        dst[i + half] = from_f32<T>(rb);
+      }
+    } else {
+      T* dst = vc + ((size_t)(head - nq - nkv) * cap + pos) * hd;
+      dst[i] = from_f32<T>(a);
+      dst[i + half] = from_f32<T>(b);
+    }
+  }
+}
+
+// ---- SIMT GEMM: C[M,N] (=|+=) A[M,K] . B[N,K]^T (+ bias) ---------------------------------
+
+constexpr int GB_M = 64, GB_N = 64, GB_K = 16;
+
+template <typename T, bool ACCUM>
+__global__ void __launch_bounds__(256)
+gemm_simt_kernel(const float* A, int lda, const T* B, int ldb, const T* bias, float* C, int ldc,
+                 int M, int N, int K) {
+  __shared__ float As[GB_K][GB_M + 4];
+  __shared__ float Bs[GB_K][GB_N + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * GB_M, n0 = blockIdx.x * GB_N;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += GB_K) {
+    for (int i = threadIdx.x; i < GB_M * GB_K; i += 256) {
+      const int r = i / GB_K, c = i - r * GB_K;
+      const int gm = m0 + r, gk = k0 + c;
+      As[c][r] = (gm < M && gk < K) ? A[(size_t)gm * lda + gk] : 0.f;
+      const int gn = n0 + r;
+      Bs[c][r] = (gn < N && gk < K) ? to_f32(B[(size_t)gn * ldb + gk]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < GB_K; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int gm = m0 + ty + 16 * i;
+    if (gm >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int gn = n0 + tx + 16 * j;
+      if (gn >= N) continue;
+      float v = acc[i][j];
+      if (bias) v += to_f32(bias[gn]);
+      float* c = C + (size_t)gm * ldc + gn;
+      *c = ACCUM ? *c + v : v;
+    }
+  }
+}
+
+template <typename T>
+static void gemm_simt(const float* A, int lda, const void* B, int ldb, const void* bias, float* C,
+                      int ldc, int M, int N, int K, bool accum, cudaStream_t s) {
+  dim3 grid((N + GB_N - 1) / GB_N, (M + GB_M - 1) / GB_M), block(256);
+  if (accum)
+    gemm_simt_kernel<T, true><<<grid, block, 0, s>>>(A, lda, (const T*)B, ldb, (const T*)bias, C, ldc, M, N, K);
+  else
+    gemm_simt_kernel<T, false><<<grid, block, 0, s>>>(A, lda, (const T*)B, ldb, (const T*)bias, C, ldc, M, N, K);
+}
+
+// ---- causal GQA flash attention (SIMT) -----------------------------------------------------
+//
+// One CTA per (block of 64 queries, query head). Keys and values of the head's KV group
+// stream through shared memory in blocks of 64 positions; scores, the running max and
+// the running sum follow the online-softmax recurrence, so each query row ends with
+// exactly softmax(q K^T / sqrt(d)) V over keys at positions <= its own.
+constexpr int FA_BQ = 64, FA_BK = 64;
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(256)
+attn_prefill_simt_kernel(const float* Q, int T_, int nq, int nkv, int pos0, const T* kc,
+                         const T* vc, int cap, float scale, float* O) {
+  extern __shared__ float fsm[];
+  float* qs = fsm;                       // [BQ][HD+1]
+  float* ks = qs + FA_BQ * (HD + 1);     // [BK][HD+1]
+  float* vs = ks + FA_BK * (HD + 1);     // [BK][HD]
+  float* ps = vs + FA_BK * HD;           // [BQ][BK+1]
+  const int qb = blockIdx.x, h = blockIdx.y, g = h / (nq / nkv);
+  const int tid = threadIdx.x;
+  const int r = tid >> 2, c = tid & 3;   // row r of the query block; quarter c
+  const int q0 = qb * FA_BQ;
+  const int nrows = min(FA_BQ, T_ - q0);
+  for (int i = tid; i < FA_BQ * HD; i += 256) {
+    const int rr = i / HD, dd = i - rr * HD;
+    qs[rr * (HD + 1) + dd] = rr < nrows ? Q[(size_t)(q0 + rr) * nq * HD + h * HD + dd] * scale : 0.f;
+  }
+  const int my_pos = pos0 + q0 + r;
+  const int last_pos = pos0 + q0 + nrows - 1;
+  constexpr int DPT = HD / 4;  // output dims per thread
+  float o[DPT];
+#pragma unroll
+  for (int i = 0; i < DPT; ++i) o[i] = 0.f;
+  float m = -INFINITY, l = 0.f;
+  const T* K = kc + (size_t)g * cap * HD;
+  const T* V = vc + (size_t)g * cap * HD;
+  for (int k0 = 0; k0 <= last_pos; k0 += FA_BK) {
+    const int nk = min(FA_BK, last_pos + 1 - k0);
+    __syncthreads();
+    for (int i = tid; i < FA_BK * HD; i += 256) {
+      const int jj = i / HD, dd = i - jj * HD;
+      const bool ok = jj < nk;
+      ks[jj * (HD + 1) + dd] = ok ? to_f32(K[(size_t)(k0 + jj) * HD + dd]) : 0.f;
+      vs[jj * HD + dd] = ok ? to_f32(V[(size_t)(k0 + jj) * HD + dd]) : 0.f;
+    }
+    __syncthreads();
+    // scores of row r against keys c, c+4, ..., (16 per thread)
+    float s[FA_BK / 4];
+    float mloc = -INFINITY;
+#pragma unroll
+    for (int jj = 0; jj < FA_BK / 4; ++jj) {
+      const int j = c + 4 * jj;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int dd = 0; dd < HD; ++dd) acc = fmaf(qs[r * (HD + 1) + dd], ks[j * (HD + 1) + dd], acc);
+      const bool open = (j < nk) && (k0 + j <= my_pos) && (r < nrows);
+      s[jj] = open ? acc : -INFINITY;
+      mloc = fmaxf(mloc, s[jj]);
+    }
+    mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+    mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+    const float mnew = fmaxf(m, mloc);
+    const float corr = (mnew == -INFINITY) ? 1.f : expf(m - mnew);
+    float lsum = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < FA_BK / 4; ++jj) {
+      const float p = (s[jj] == -INFINITY) ? 0.f : expf(s[jj] - mnew);
+      ps[r * (FA_BK + 1) + c + 4 * jj] = p;
+      lsum += p;
+    }
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+    l = l * corr + lsum;
+    m = mnew;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < DPT; ++i) o[i] *= corr;
+    for (int j = 0; j < nk; ++j) {
+      const float p = ps[r * (FA_BK + 1) + j];
+#pragma unroll
+      for (int i = 0; i < DPT; ++i) o[i] = fmaf(p, vs[j * HD + c * DPT + i], o[i]);
+    }
+  }
+  if (r < nrows) {
+    const float inv = 1.f / l;
+    float* out = O + (size_t)(q0 + r) * nq * HD + h * HD + c * DPT;
+#pragma unroll
+    for (int i = 0; i < DPT; ++i) out[i] = o[i] * inv;
+  }
+}
+
+template <typename T, int HD>
+static size_t fa_smem() {
+  return (size_t)(FA_BQ * (HD + 1) + FA_BK * (HD + 1) + FA_BK * HD + FA_BQ * (FA_BK + 1)) * sizeof(float);
+}
+
+template <typename T, int HD>
+static cudaError_t fa_set_attr() {
+  return cudaFuncSetAttribute(attn_prefill_simt_kernel<T, HD>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fa_smem<T, HD>());
+}
+
+template <typename T>
+static cudaError_t attn_prefill(const Dims& d, const float* Q, int T_, int pos0, const void* kc,
+                                const void* vc, float* O, cudaStream_t s) {
+  const dim3 grid((T_ + FA_BQ - 1) / FA_BQ, d.nq), block(256);
+  const float scale = 1.f / sqrtf((float)d.hd);
+  switch (d.hd) {
+    case 16: attn_prefill_simt_kernel<T, 16><<<grid, block, fa_smem<T, 16>(), s>>>(Q, T_, d.nq, d.nkv, pos0, (const T*)kc, (const T*)vc, d.cap, scale, O); break;
+    case 32: attn_prefill_simt_kernel<T, 32><<<grid, block, fa_smem<T, 32>(), s>>>(Q, T_, d.nq, d.nkv, pos0, (const T*)kc, (const T*)vc, d.cap, scale, O); break;
+    case 64: attn_prefill_simt_kernel<T, 64><<<grid, block, fa_smem<T, 64>(), s>>>(Q, T_, d.nq, d.nkv, pos0, (const T*)kc, (const T*)vc, d.cap, scale, O); break;
+    case 128: attn_prefill_simt_kernel<T, 128><<<grid, block, fa_smem<T, 128>(), s>>>(Q, T_, d.nq, d.nkv, pos0, (const T*)kc, (const T*)vc, d.cap, scale, O); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t set_attr_t() {
+  cudaError_t e;
+  if ((e = fa_set_attr<T, 16>())) return e;
+  if ((e = fa_set_attr<T, 32>())) return e;
+  if ((e = fa_set_attr<T, 64>())) return e;
+  return fa_set_attr<T, 128>();
+}
+
+cudaError_t prefill_set_attributes(const Dims& d) {
+  return d.dtype == 1 ? set_attr_t<bf16>() : set_attr_t<float>();
+}
+
+template <typename T>
+static cudaError_t prefill_t(const Dims& d, const LayerPtrs* layers, const void* embed,
+                             const int* ids, int T_, int pos0, const float2* rope, void* kcache,
+                             void* vcache, const PrefillBufs& b, int* err, cudaStream_t s) {
+  const int H = d.H, qd = d.nq * d.hd, kvd = d.nkv * d.hd, W = qd + 2 * kvd;
+  embed_rows_kernel<T><<<T_, 256, 0, s>>>((const T*)embed, d.V, H, ids, b.X, err);
+  const size_t layer_stride = (size_t)d.nkv * d.cap * d.hd;  // elements per layer per K or V
+  for (int l = 0; l < d.L; ++l) {
+    const LayerPtrs& w = layers[l];
+    T* kc = (T*)kcache + (size_t)l * 2 * layer_stride;
+    T* vc = kc + layer_stride;
+    norm_rows_kernel<T><<<T_, 256, 0, s>>>(b.X, (const T*)w.in_norm, H, d.eps, b.Xn);
+    gemm_simt<T>(b.Xn, H, w.wq, H, w.bq, b.Y, W, T_, qd, H, false, s);
+    gemm_simt<T>(b.Xn, H, w.wk, H, w.bk, b.Y + qd, W, T_, kvd, H, false, s);
+    gemm_simt<T>(b.Xn, H, w.wv, H, w.bv, b.Y + qd + kvd, W, T_, kvd, H, false, s);
+    rope_kv_kernel<T><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc);
+    cudaError_t e = attn_prefill<T>(d, b.Q, T_, pos0, kc, vc, b.O, s);
+    if (e) return e;
+    gemm_simt<T>(b.O, qd, w.wo, qd, nullptr, b.X, H, T_, H, qd, true, s);
+    norm_rows_kernel<T><<<T_, 256, 0, s>>>(b.X, (const T*)w.post_norm, H, d.eps, b.Xn);
+    gemm_simt<T>(b.Xn, H, w.w_gate, H, nullptr, b.G, d.I, T_, d.I, H, false, s);
+    gemm_simt<T>(b.Xn, H, w.w_up, H, nullptr, b.U, d.I, T_, d.I, H, false, s);
+    const size_t n = (size_t)T_ * d.I;
+    swiglu_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, s>>>(b.G, b.U, b.G, n);
+    gemm_simt<T>(b.G, d.I, w.w_down, d.I, nullptr, b.X, H, T_, H, d.I, true, s);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_layers(const Dims& d, const LayerPtrs* layers, const void* embed,
+                           const int* ids_dev, int T, int pos0, const float2* rope,
+                           void* kcache_seq, void* vcache_seq, const PrefillBufs& b, int* err,
+                           cudaStream_t s) {
+  (void)vcache_seq;
+  return d.dtype == 1
+             ? prefill_t<bf16>(d, layers, embed, ids_dev, T, pos0, rope, kcache_seq, vcache_seq, b, err, s)
+             : prefill_t<float>(d, layers, embed, ids_dev, T, pos0, rope, kcache_seq, vcache_seq, b, err, s);
+}
+
+}  // namespace qw

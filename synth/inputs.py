@@ -3,8 +3,9 @@
 Recipe (the same for every consumer):
   * every weight matrix, embedding and bias is N(0, 0.02); RMSNorm gains are
     1 + N(0, 0.02) (unit gains, perturbed so that a dropped gain multiply shows);
-  * each tensor draws from its own stream ``default_rng([seed, index])`` so any
-    subset can be regenerated alone;
+  * tensor ``index`` (its position in ``tensor_shapes``) is drawn flat, in blocks of
+    2^22 values; block c draws from its own stream ``default_rng([seed, index, c])``, so
+    any subset can be regenerated alone and blocks are drawn in parallel;
   * bf16 shapes round every value to bf16 (round-to-nearest-even) and keep it as the
     exactly representable float32 value; f32 shapes keep the float32 draw;
   * prompt ids are uniform on [0, vocab) from ``default_rng(1)``; batched prompt
@@ -75,11 +76,12 @@ def param_count(s: Shape) -> int:
 
 
 def round_to_bf16(a: np.ndarray) -> np.ndarray:
-    """Round float32 values to the nearest bf16 (ties to even); returns float32."""
+    """Round finite float32 values to the nearest bf16 (ties to even); returns float32."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32).reshape(a.shape)
+    u = a.view(np.uint32)
+    r = u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))
+    r &= np.uint32(0xFFFF0000)
+    return r.view(np.float32).reshape(a.shape)
 
 
 def bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -88,31 +90,42 @@ def bf16_bits(a: np.ndarray) -> np.ndarray:
     return (a.view(np.uint32) >> 16).astype(np.uint16)
 
 
-def _draw(seed, index, shp, kind, bf16):
-    rng = np.random.default_rng([seed, index])
-    a = rng.standard_normal(size=shp, dtype=np.float32)
+BLOCK = 1 << 22
+
+
+def _fill_block(out_flat, seed, index, c, kind, bf16):
+    lo = c * BLOCK
+    hi = min(out_flat.size, lo + BLOCK)
+    rng = np.random.default_rng([seed, index, c])
+    a = rng.standard_normal(size=hi - lo, dtype=np.float32)
     a *= np.float32(WEIGHT_STD)
     if kind == "gain":
         a += np.float32(1.0)
     if bf16:
         a = round_to_bf16(a)
-    return a
+    out_flat[lo:hi] = a
 
 
-def make_weights(s: Shape, seed: int = 0, layers=None, threads: int = 8):
+def make_weights(s: Shape, seed: int = 0, layers=None, threads: int = None):
     """Return {name: float32 ndarray}. ``layers`` limits the per-layer tensors drawn
     (None = all); the global tensors are always drawn."""
+    import os
     bf16 = s.dtype == "bf16"
-    jobs = []
+    out, jobs = {}, []
     for idx, (name, shp, kind) in enumerate(tensor_shapes(s)):
         if layers is not None and name.startswith("model.layers."):
             li = int(name.split(".")[2])
             if li not in layers:
                 continue
-        jobs.append((idx, name, shp, kind))
-    with ThreadPoolExecutor(max_workers=threads) as ex:
-        arrays = list(ex.map(lambda j: _draw(seed, j[0], j[2], j[3], bf16), jobs))
-    return {j[1]: a for j, a in zip(jobs, arrays)}
+        arr = np.empty(shp, dtype=np.float32)
+        out[name] = arr
+        flat = arr.reshape(-1)
+        for c in range((flat.size + BLOCK - 1) // BLOCK):
+            jobs.append((flat, idx, c, kind))
+    n = threads or min(32, os.cpu_count() or 1)
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(lambda j: _fill_block(j[0], seed, j[1], j[2], j[3], bf16), jobs))
+    return out
 
 
 def make_prompt(s: Shape, n: int, seed: int = 1) -> np.ndarray:
