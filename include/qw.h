@@ -49,12 +49,16 @@ typedef enum {
   QW_ERR_NUMERIC = 8        /* non-finite logits */
 } qw_status;
 
-typedef enum { QW_F32 = 0, QW_BF16 = 1 } qw_dtype;
+typedef enum { QW_F32 = 0, QW_BF16 = 1, QW_F16 = 2 } qw_dtype;
 
 /* Model shape [LSA Implementing Qwen, the model configuration; AUG Qwen model config].
  * head_dim must be even and equal hidden / n_heads (the score scale 1/sqrt(d_k) uses
  * d_k = hidden / n_heads); n_heads must be a multiple of n_kv_heads. dtype is the storage
- * type of weights and of the KV cache; activations, accumulators and logits are fp32. */
+ * type of the weights, QW_F32 or QW_BF16. The KV cache is fp32 for QW_F32 models and fp16
+ * for QW_BF16 models (same two bytes as bf16, eight times finer rounding); decode
+ * activations, accumulators and logits are fp32; the prefill projections of QW_BF16 models
+ * run on the tensor cores with fp16 operands (exact fp16 copies of the weights, made by
+ * qw_create) and fp32 accumulation. */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab;
   float rms_eps;          /* RMSNorm epsilon, inside the square root (1e-6) */
@@ -163,8 +167,8 @@ const char *qw_last_error(void);
  * h / (n_heads / n_kv_heads), softmax, and out_h = sum_j p_j V_j. The context is split
  * into chunks whose partial softmax statistics are merged exactly (log-sum-exp).
  *   q    device fp32 [n_heads*head_dim]
- *   k, v device, dtype elements, [n_kv_heads][kv_stride][head_dim] (position-major per
- *        head), ctx <= kv_stride
+ *   k, v device, kv_dtype (QW_F32 or QW_F16) elements, [n_kv_heads][kv_stride][head_dim]
+ *        (position-major per head), ctx <= kv_stride
  *   out  device fp32 [n_heads*head_dim]
  *   workspace device, at least qw_op_decode_attention_workspace() bytes, 16-byte
  *        aligned; its counters must be zero before the first call (cudaMemset) and the
@@ -172,10 +176,28 @@ const char *qw_last_error(void);
  * Runs on cuda_stream (NULL = default stream) and does not synchronise. */
 size_t qw_op_decode_attention_workspace(int32_t n_heads, int32_t n_kv_heads,
                                         int32_t head_dim, int32_t max_ctx);
-qw_status qw_op_decode_attention(int32_t dtype, int32_t n_heads, int32_t n_kv_heads,
+qw_status qw_op_decode_attention(int32_t kv_dtype, int32_t n_heads, int32_t n_kv_heads,
                                  int32_t head_dim, int32_t ctx, int32_t kv_stride,
                                  const float *q, const void *k, const void *v, float *out,
                                  void *workspace, size_t workspace_bytes,
+                                 void *cuda_stream);
+
+/* Dense GEMM on the tensor cores (tcgen05), the contraction of every prefill projection
+ * [LSA Implementing Qwen: W @ x for all prompt columns at once; QIE §1: prefill is
+ * compute-bound]: C[M][N] = A[M][K] . B[N][K]^T (+ bias[N]), or C += A . B^T when
+ * accumulate is 1 (the residual add). A, B fp16 row-major, bias bf16 (may be NULL), C fp32
+ * row-major, all device, contiguous (row pitch = K for A and B, N for C), 16-byte aligned;
+ * K and N multiples of 8. err_dev is a device int32 that receives QW device error bits (a
+ * bounded wait that expired). Runs on cuda_stream without synchronising. */
+qw_status qw_op_gemm_f16(int32_t M, int32_t N, int32_t K, const void *A, const void *B,
+                          const void *bias, float *C, int32_t accumulate, int32_t *err_dev,
+                          void *cuda_stream);
+
+/* Fused gate/up projection and SwiGLU [LSA SwiGLU FFN]: act[M][N] =
+ * silu(A . Wg^T) * (A . Wu^T), A [M][K], Wg/Wu [N][K] fp16, act fp16 [M][N]; the same
+ * layout rules as qw_op_gemm_f16. */
+qw_status qw_op_gemm_swiglu_f16(int32_t M, int32_t N, int32_t K, const void *A,
+                                 const void *Wg, const void *Wu, void *act, int32_t *err_dev,
                                  void *cuda_stream);
 
 #ifdef __cplusplus

@@ -19,7 +19,7 @@ STATUS = {
     4: "QW_ERR_TOKEN_RANGE", 5: "QW_ERR_CUDA", 6: "QW_ERR_TIMEOUT",
     7: "QW_ERR_FAULT_INJECTED", 8: "QW_ERR_NUMERIC",
 }
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 
 
 class QwError(RuntimeError):
@@ -78,6 +78,8 @@ def lib():
         "qw_reset": ([VP, I32], I32),
         "qw_last_error": ([], ctypes.c_char_p),
         "qw_set_trace": ([VP, I32, P(VP), P(VP)], I32),
+        "qw_op_gemm_f16": ([I32, I32, I32, VP, VP, VP, VP, I32, VP, VP], I32),
+        "qw_op_gemm_swiglu_f16": ([I32, I32, I32, VP, VP, VP, VP, VP, VP], I32),
         "qw_op_decode_attention_workspace": ([I32, I32, I32, I32], SZ),
         "qw_op_decode_attention": ([I32, I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP], I32),
     }
@@ -93,7 +95,8 @@ def exported_symbols():
     return ["qw_create", "qw_destroy", "qw_prefill", "qw_prefill_device", "qw_decode_step",
             "qw_decode_steps", "qw_generate", "qw_sync", "qw_logits", "qw_read_logits",
             "qw_tokens_device", "qw_position", "qw_reset", "qw_last_error", "qw_set_trace",
-            "qw_op_decode_attention_workspace", "qw_op_decode_attention"]
+            "qw_op_decode_attention_workspace", "qw_op_decode_attention", "qw_op_gemm_f16",
+            "qw_op_gemm_swiglu_f16"]
 
 
 def check(status):
@@ -251,3 +254,11 @@ def decode_attention(dtype, n_heads, n_kv_heads, head_dim, ctx, kv_stride, q_ptr
 
 def decode_attention_workspace(n_heads, n_kv_heads, head_dim, max_ctx):
     return int(lib().qw_op_decode_attention_workspace(n_heads, n_kv_heads, head_dim, max_ctx))
+
+
+def gemm_f16(M, N, K, a_ptr, b_ptr, bias_ptr, c_ptr, accumulate, err_ptr, stream=None):
+    check(lib().qw_op_gemm_f16(M, N, K, a_ptr, b_ptr, bias_ptr, c_ptr, int(accumulate), err_ptr, stream))
+
+
+def gemm_swiglu_f16(M, N, K, a_ptr, wg_ptr, wu_ptr, act_ptr, err_ptr, stream=None):
+    check(lib().qw_op_gemm_swiglu_f16(M, N, K, a_ptr, wg_ptr, wu_ptr, act_ptr, err_ptr, stream))

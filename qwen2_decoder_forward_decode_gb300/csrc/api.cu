@@ -6,6 +6,7 @@
 // down}, LM head) captured on first use with programmatic-dependent-launch edges; because
 // positions and tokens live in device memory the same graph serves every step.
 #include "../../include/qw.h"
+#include "common.cuh"
 #include "internal.h"
 
 #include <algorithm>
@@ -69,6 +70,7 @@ struct qw_model {
   int* pinned = nullptr;  // host staging, max(cap, max_seqs) ints
   PrefillBufs pf{};
   void* pf_block = nullptr;
+  void* w16 = nullptr;  // fp16 copies of the layer matrices (bf16 models)
   // host mirror
   std::vector<int> h_pos;
   std::vector<char> active;
@@ -128,7 +130,7 @@ struct qw_model {
       if ((e = run(0, l, [&](bool p) { return launch_qkv(d, w, xs, pos + s, rope, q, kc, vc, stream, p); })))
         return e;
       if ((e = run(1, l, [&](bool p) {
-             return launch_attn(d.dtype, d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min,
+             return launch_attn(d.dtype == QW_BF16 ? 2 : 0, d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min,
                                 attn_smem, q, kc, vc, d.cap, pos + s, 0, attn, attn_ws, stream, p);
            })))
         return e;
@@ -169,8 +171,10 @@ struct qw_model {
     if (pf.cap_tokens >= T) return cudaSuccess;
     if (pf_block) { cudaFree(pf_block); pf_block = nullptr; }
     const size_t H = d.H, qd = (size_t)d.nq * d.hd, W = qd + 2 * (size_t)d.nkv * d.hd, I = d.I;
-    const size_t per_tok = H * 2 + W + qd * 2 + I * 2;  // X Xn Y Q O G U
-    cudaError_t e = cudaMalloc(&pf_block, per_tok * T * sizeof(float));
+    const size_t per_tok = H * 2 + W + qd * 2 + I * 2;  // X Xn Y Q O G U (fp32)
+    const size_t per_tok_h = H + qd + I;               // Xh Oh Ah (fp16)
+    const size_t f32_bytes = (per_tok * T * sizeof(float) + 255) & ~(size_t)255;
+    cudaError_t e = cudaMalloc(&pf_block, f32_bytes + per_tok_h * T * sizeof(__half) + 256);
     if (e) { pf_block = nullptr; pf.cap_tokens = 0; return e; }
     float* p = (float*)pf_block;
     pf.X = p; p += H * T;
@@ -180,6 +184,10 @@ struct qw_model {
     pf.O = p; p += qd * T;
     pf.G = p; p += I * T;
     pf.U = p;
+    __half* h = (__half*)((char*)pf_block + f32_bytes);
+    pf.Xh = h; h += H * T;
+    pf.Oh = h; h += qd * T;
+    pf.Ah = h;
     pf.cap_tokens = T;
     return cudaSuccess;
   }
@@ -189,8 +197,7 @@ struct qw_model {
     cudaError_t e;
     if ((e = ensure_prefill(n))) return e;
     if ((e = cudaMemsetAsync(hist_n + s, 0, sizeof(int), stream))) return e;
-    if ((e = prefill_layers(d, layers.data(), embed, ids_dev, n, 0, rope, kv_seq(s), nullptr, pf,
-                            err, stream)))
+    if ((e = prefill_layers(d, layers.data(), embed, ids_dev, n, 0, rope, kv_seq(s), pf, err, stream)))
       return e;
     return launch_lmhead(d, head_w(), final_norm, pf.X + (size_t)(n - 1) * d.H,
                          logits + (size_t)s * d.V, fin(s, n), stream, false);
@@ -215,7 +222,7 @@ struct qw_model {
       if (g) cudaGraphExecDestroy(g);
     graphs.clear();
     void* bufs[] = {kv, x, q, attn, act, logits, rope, attn_ws, keys, lm_counter, pos, tok,
-                    hist, hist_n, err, ids, pf_block};
+                    hist, hist_n, err, ids, pf_block, w16};
     for (void* b : bufs)
       if (b) cudaFree(b);
     if (pinned) cudaFreeHost(pinned);
@@ -303,7 +310,8 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
   for (int l = 0; l < d.L; ++l) {
     const qw_layer_weights& L = w->layers[l];
     LayerPtrs p{L.in_norm, L.wq, cfg->qkv_bias ? L.bq : nullptr, L.wk, cfg->qkv_bias ? L.bk : nullptr,
-                L.wv, cfg->qkv_bias ? L.bv : nullptr, L.wo, L.post_norm, L.w_gate, L.w_up, L.w_down};
+                L.wv, cfg->qkv_bias ? L.bv : nullptr, L.wo, L.post_norm, L.w_gate, L.w_up, L.w_down,
+                nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     m->layers.push_back(p);
   }
   const int S = d.max_seqs;
@@ -347,6 +355,37 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
     if ((e = cudaMalloc(&m->rope, sizeof(float2) * tab.size()))) return bail(e, "cudaMalloc");
     if ((e = cudaMemcpy(m->rope, tab.data(), sizeof(float2) * tab.size(), cudaMemcpyHostToDevice)))
       return bail(e, "cudaMemcpy(rope)");
+  }
+  m->pf.use_tc = false;
+  if (cfg->dtype == QW_BF16 && gemm_tc_available()) {
+    const char* simt = std::getenv("QW_PREFILL_SIMT");
+    m->pf.use_tc = !(simt && simt[0] == '1');
+  }
+  if (m->pf.use_tc) {
+    // fp16 copies of the layer matrices: the tensor-core operands of the prefill GEMMs
+    const size_t H = d.H, qd = (size_t)d.nq * d.hd, kvd = (size_t)d.nkv * d.hd, I = d.I;
+    const size_t sizes[7] = {qd * H, kvd * H, kvd * H, H * qd, I * H, I * H, H * I};
+    size_t per_layer = 0;
+    for (size_t n : sizes) per_layer += (n * 2 + 255) & ~(size_t)255;
+    if ((e = cudaMalloc(&m->w16, per_layer * d.L))) return bail(e, "cudaMalloc(fp16 weights)");
+    char* p = (char*)m->w16;
+    for (int l = 0; l < d.L; ++l) {
+      LayerPtrs& L = m->layers[l];
+      const void* src[7] = {L.wq, L.wk, L.wv, L.wo, L.w_gate, L.w_up, L.w_down};
+      const void** dst[7] = {&L.wq16, &L.wk16, &L.wv16, &L.wo16, &L.wg16, &L.wu16, &L.wd16};
+      for (int i = 0; i < 7; ++i) {
+        *dst[i] = p;
+        if ((e = convert_bf16_to_half(src[i], p, sizes[i], m->err, 0))) return bail(e, "fp16 weight copy");
+        p += (sizes[i] * 2 + 255) & ~(size_t)255;
+      }
+    }
+    int h_err = 0;
+    if ((e = cudaMemcpy(&h_err, m->err, sizeof(int), cudaMemcpyDeviceToHost))) return bail(e, "cudaMemcpy");
+    if (h_err) {
+      m->release();
+      delete m;
+      return fail(QW_ERR_NUMERIC, "a weight lies outside the fp16 range of the prefill operands");
+    }
   }
   if ((e = decode_set_attributes(d))) return bail(e, "decode attributes");
   if ((e = attn_set_attributes(m->attn_smem))) return bail(e, "attention attributes");
@@ -582,13 +621,13 @@ size_t qw_op_decode_attention_workspace(int32_t n_heads, int32_t n_kv_heads, int
   return attn_workspace_bytes(n_heads, n_kv_heads, head_dim, op_attn_nsplit(n_kv_heads, max_ctx));
 }
 
-qw_status qw_op_decode_attention(int32_t dtype, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+qw_status qw_op_decode_attention(int32_t kv_dtype, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                  int32_t ctx, int32_t kv_stride, const float* q, const void* k,
                                  const void* v, float* out, void* workspace, size_t workspace_bytes,
                                  void* cuda_stream) {
   g_err.clear();
   if (!q || !k || !v || !out || !workspace) return fail(QW_ERR_INVALID_ARG, "null pointer");
-  if (dtype != QW_F32 && dtype != QW_BF16) return fail(QW_ERR_INVALID_ARG, "unknown dtype");
+  if (kv_dtype != QW_F32 && kv_dtype != QW_F16) return fail(QW_ERR_INVALID_ARG, "kv dtype must be QW_F32 or QW_F16");
   if (n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || head_dim < 2 || ctx < 1 || kv_stride < ctx)
     return fail(QW_ERR_INVALID_ARG, "bad attention shape");
   if (n_heads / n_kv_heads > 8) return fail(QW_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
@@ -600,9 +639,48 @@ qw_status qw_op_decode_attention(int32_t dtype, int32_t n_heads, int32_t n_kv_he
   if (smem > 200 * 1024) return fail(QW_ERR_UNSUPPORTED, "attention chunk too large");
   cudaError_t e = attn_set_attributes(smem);
   if (e) return cuda_fail(e, "decode attention attributes");
-  e = launch_attn(dtype, n_heads, n_kv_heads, head_dim, nsplit, ATTN_CHUNK_MIN, smem, q, k, v,
+  e = launch_attn(kv_dtype, n_heads, n_kv_heads, head_dim, nsplit, ATTN_CHUNK_MIN, smem, q, k, v,
                               kv_stride, nullptr, ctx, out, workspace, (cudaStream_t)cuda_stream, false);
   if (e) return cuda_fail(e, "decode attention launch");
+  return QW_OK;
+}
+
+static qw_status gemm_args(int32_t M, int32_t N, int32_t K, const void* A, const void* B) {
+  if (M < 1 || N < 1 || K < 1) return fail(QW_ERR_INVALID_ARG, "non-positive GEMM size");
+  if (!A || !B) return fail(QW_ERR_INVALID_ARG, "null pointer");
+  if (N % 8 || K % 8) return fail(QW_ERR_UNSUPPORTED, "N and K must be multiples of 8");
+  if (((uintptr_t)A | (uintptr_t)B) & 15) return fail(QW_ERR_INVALID_ARG, "operand not 16-byte aligned");
+  if (!gemm_tc_available()) return fail(QW_ERR_UNSUPPORTED, "tensor-map encoder unavailable");
+  return QW_OK;
+}
+
+qw_status qw_op_gemm_f16(int32_t M, int32_t N, int32_t K, const void* A, const void* B, const void* bias,
+                          float* C, int32_t accumulate, int32_t* err_dev, void* cuda_stream) {
+  g_err.clear();
+  qw_status st = gemm_args(M, N, K, A, B);
+  if (st) return st;
+  if (!C || !err_dev) return fail(QW_ERR_INVALID_ARG, "null pointer");
+  if ((uintptr_t)C & 15) return fail(QW_ERR_INVALID_ARG, "C not 16-byte aligned");
+  cudaError_t e = gemm_tc_set_attributes();
+  if (e) return cuda_fail(e, "gemm attributes");
+  e = gemm_tc((const f16*)A, K, (const f16*)B, K, (const bf16*)bias, C, N, M, N, K, accumulate != 0,
+              err_dev, (cudaStream_t)cuda_stream);
+  if (e) return cuda_fail(e, "gemm launch");
+  return QW_OK;
+}
+
+qw_status qw_op_gemm_swiglu_f16(int32_t M, int32_t N, int32_t K, const void* A, const void* Wg,
+                                 const void* Wu, void* act, int32_t* err_dev, void* cuda_stream) {
+  g_err.clear();
+  qw_status st = gemm_args(M, N, K, A, Wg);
+  if (st) return st;
+  if (!Wu || !act || !err_dev) return fail(QW_ERR_INVALID_ARG, "null pointer");
+  if (((uintptr_t)Wu | (uintptr_t)act) & 15) return fail(QW_ERR_INVALID_ARG, "operand not 16-byte aligned");
+  cudaError_t e = gemm_tc_set_attributes();
+  if (e) return cuda_fail(e, "gemm attributes");
+  e = gemm_tc_swiglu((const f16*)A, K, (const f16*)Wg, (const f16*)Wu, K, (f16*)act, N, M, N, K, err_dev,
+                     (cudaStream_t)cuda_stream);
+  if (e) return cuda_fail(e, "gemm launch");
   return QW_OK;
 }
 

@@ -2,12 +2,14 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace qw {
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 // Programmatic dependent launch: wait for the upstream grid's completion and memory,
 // and allow the downstream grid to be scheduled.
@@ -22,9 +24,11 @@ template <> struct Vec<bf16> { static constexpr int N = 8; };
 
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(f16 v) { return __half2float(v); }
 template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+template <> __device__ __forceinline__ f16 from_f32<f16>(float v) { return __float2half_rn(v); }
 
 // 16-byte streaming load of read-only data (weights): no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream(const void* p) {

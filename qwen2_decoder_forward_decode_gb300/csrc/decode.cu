@@ -47,8 +47,8 @@ __device__ __forceinline__ void prologue_copy(float* xs, const float* x, int K) 
 // ---- GEMV ops ----------------------------------------------------------------------------
 
 // q/k/v rows in RoPE pairs (i, i + hd/2) of one head; items run over q heads, k heads,
-// v heads, hd/2 pairs each.
-template <typename T>
+// v heads, hd/2 pairs each. T: weight type, KV: cache element type.
+template <typename T, typename KV>
 struct OpQKV {
   int K, n_items, hd, nq, nkv, cap;
   const T *wq, *wk, *wv, *bq, *bk, *bv, *gain;
@@ -57,7 +57,7 @@ struct OpQKV {
   const int* d_pos;
   const float2* rope;  // [cap][hd/2] (cos, sin)
   float* q_out;
-  T *kc, *vc;  // [nkv][cap][hd] of this layer and sequence
+  KV *kc, *vc;  // [nkv][cap][hd] of this layer and sequence
   int pos;
 
   __device__ void prologue(float* xs, float* scratch) {
@@ -98,10 +98,10 @@ struct OpQKV {
       q_out[h * hd + i] = a;
       q_out[h * hd + i + half] = b;
     } else {
-      T* c = head < nq + nkv ? kc : vc;
-      T* dst = c + ((size_t)h * cap + pos) * hd;
-      dst[i] = from_f32<T>(a);
-      dst[i + half] = from_f32<T>(b);
+      KV* c = head < nq + nkv ? kc : vc;
+      KV* dst = c + ((size_t)h * cap + pos) * hd;
+      dst[i] = from_f32<KV>(a);
+      dst[i + half] = from_f32<KV>(b);
     }
   }
   __device__ void finish(float*) {}
@@ -520,7 +520,7 @@ size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min) {
   return ((size_t)group * hd + (size_t)group * chunk + 2 * group) * sizeof(float);
 }
 
-cudaError_t launch_attn(int dtype, int nq, int nkv, int hd, int nsplit, int chunk_min,
+cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int chunk_min,
                         size_t smem, const float* q, const void* kc, const void* vc,
                         int kv_stride, const int* d_pos, int ctx_host, float* out, void* ws,
                         cudaStream_t s, bool pdl) {
@@ -528,11 +528,11 @@ cudaError_t launch_attn(int dtype, int nq, int nkv, int hd, int nsplit, int chun
   if (G > GMAX) return cudaErrorInvalidValue;
   size_t part_bytes = ((size_t)nq * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
   const dim3 grid(nkv, nsplit), block(128);
-  if (dtype == 1) {
-    AttnArgs<bf16> a{q, (const bf16*)kc, (const bf16*)vc, kv_stride, hd, G, nsplit, chunk_min,
+  if (kv_dtype == 2) {
+    AttnArgs<f16> a{q, (const f16*)kc, (const f16*)vc, kv_stride, hd, G, nsplit, chunk_min,
                      ctx_host, d_pos, 1.f / sqrtf((float)hd), out, (float*)ws,
                      (unsigned int*)((char*)ws + part_bytes)};
-    return launch_k(attn_decode_kernel<bf16>, grid, block, smem, s, pdl, a);
+    return launch_k(attn_decode_kernel<f16>, grid, block, smem, s, pdl, a);
   }
   AttnArgs<float> a{q, (const float*)kc, (const float*)vc, kv_stride, hd, G, nsplit, chunk_min,
                     ctx_host, d_pos, 1.f / sqrtf((float)hd), out, (float*)ws,
@@ -542,7 +542,7 @@ cudaError_t launch_attn(int dtype, int nq, int nkv, int hd, int nsplit, int chun
 
 cudaError_t attn_set_attributes(size_t smem) {
   if (smem <= 48 * 1024) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<bf16>,
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<f16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e) return e;
   return cudaFuncSetAttribute(attn_decode_kernel<float>,
@@ -552,7 +552,8 @@ cudaError_t attn_set_attributes(size_t smem) {
 template <typename T>
 static cudaError_t set_attrs_t(const Dims& d) {
   cudaError_t e;
-  if ((e = set_gemv_smem<T, OpQKV<T>>(d.H))) return e;
+  if ((e = set_gemv_smem<T, OpQKV<T, float>>(d.H))) return e;
+  if ((e = set_gemv_smem<T, OpQKV<T, f16>>(d.H))) return e;
   if ((e = set_gemv_smem<T, OpGateUp<T>>(d.H))) return e;
   if ((e = set_gemv_smem<T, OpResid<T>>(d.I > d.nq * d.hd ? d.I : d.nq * d.hd))) return e;
   return set_gemv_smem<T, OpLMHead<T>>(d.H);
@@ -569,10 +570,10 @@ cudaError_t launch_embed(const Dims& d, const void* E, const int* tok, float* x,
   return launch_k(embed_kernel<float>, dim3(1), dim3(256), 0, s, pdl, (const float*)E, d.V, d.H, tok, x, err);
 }
 
-template <typename T>
+template <typename T, typename KV>
 static cudaError_t qkv_t(const Dims& d, const LayerPtrs& w, const float* x, const int* d_pos,
                          const float2* rope, float* q, void* kc, void* vc, cudaStream_t s, bool pdl) {
-  OpQKV<T> op{};
+  OpQKV<T, KV> op{};
   op.K = d.H;
   op.n_items = (d.nq + 2 * d.nkv) * (d.hd / 2);
   op.hd = d.hd; op.nq = d.nq; op.nkv = d.nkv; op.cap = d.cap;
@@ -580,13 +581,13 @@ static cudaError_t qkv_t(const Dims& d, const LayerPtrs& w, const float* x, cons
   op.bq = (const T*)w.bq; op.bk = (const T*)w.bk; op.bv = (const T*)w.bv;
   op.gain = (const T*)w.in_norm;
   op.x = x; op.eps = d.eps; op.d_pos = d_pos; op.rope = rope; op.q_out = q;
-  op.kc = (T*)kc; op.vc = (T*)vc;
+  op.kc = (KV*)kc; op.vc = (KV*)vc;
   return run_gemv<T>(op, d.nsm, s, pdl);
 }
 cudaError_t launch_qkv(const Dims& d, const LayerPtrs& w, const float* x, const int* d_pos,
                        const float2* rope, float* q, void* kc, void* vc, cudaStream_t s, bool pdl) {
-  return d.dtype == 1 ? qkv_t<bf16>(d, w, x, d_pos, rope, q, kc, vc, s, pdl)
-                      : qkv_t<float>(d, w, x, d_pos, rope, q, kc, vc, s, pdl);
+  return d.dtype == 1 ? qkv_t<bf16, f16>(d, w, x, d_pos, rope, q, kc, vc, s, pdl)
+                      : qkv_t<float, float>(d, w, x, d_pos, rope, q, kc, vc, s, pdl);
 }
 
 template <typename T>

@@ -1,0 +1,376 @@
+// Prefill GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+//   C[M, N] = A[M, K] . B[N, K]^T     A: fp16 activations, B: fp16 weights, both K-major
+//
+// One CTA computes a 128 x BN tile with a TMEM fp32 accumulator:
+//   warp 0 (one lane)  TMA producer: 128-byte-swizzled A and B tiles of 64 K-elements into
+//                      a STAGES-deep shared-memory ring (mbarrier full/empty pairs)
+//   warp 1 (one lane)  MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16,
+//                      four per stage; tcgen05.commit frees a stage when its MMAs retire
+//   warps 2..5         epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows), fused
+//                      bias / residual-add / SwiGLU, stores to global memory
+// Every mbarrier wait is bounded (clock budget); on expiry the CTA flags ERR_TIMEOUT,
+// stops issuing work, and still releases its TMEM.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace qw {
+
+namespace tc {
+
+constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int THREADS = 192;
+constexpr long long WAIT_BUDGET = 4000000000ll;  // clock cycles (~2 s) before giving up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false (and the error bit set) if the phase did not complete in budget.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > WAIT_BUDGET) {
+      atomicOr(err, ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with 128-byte swizzle:
+// rows of 128 bytes, 8-row atoms 1024 bytes apart (stride byte offset), descriptor
+// version 1, swizzle mode 2 (128B). The tile base must be 1024-byte aligned; stepping K
+// by 16 elements inside the 128-byte row adds 32 bytes to the start address.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16 (type code 0 in
+// bits 7-9 and 10-12), both K-major (bits 15, 16 = 0), N/8 in bits 17-22, M/16 in 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(tmem_d), "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace tc
+
+// Epilogues
+enum : int { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2 };
+
+struct TcEpi {
+  float* C;          // EPI_STORE: C = acc (+ bias); EPI_ADD: C += acc   (fp32, ld = ldc)
+  const bf16* bias;  // [N] or null (EPI_STORE)
+  f16* Cb;           // EPI_SWIGLU: Cb[m][n] = silu(gate) * up as fp16, ld = ldc
+  int ldc;
+};
+
+// BN columns per tile. For EPI_SWIGLU the B ring holds BN/2 gate rows then BN/2 up rows of
+// the same output columns; the accumulator keeps gate in TMEM columns [0, BN/2) and up in
+// [BN/2, BN).
+template <int BN, int EPI>
+__global__ void __launch_bounds__(tc::THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmB2, TcEpi ep, int M, int N, int K, int* err) {
+  using namespace tc;
+  constexpr int A_BYTES = BM * BK * 2;
+  constexpr int B_BYTES = BN * BK * 2;
+  constexpr int STAGE = A_BYTES + B_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 1);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES), accum = smem_u32(bars + 2 * STAGES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM;
+  const int n0 = blockIdx.x * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+  const int nk = (K + BK - 1) / BK;
+  __shared__ int s_abort;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(full0 + 8 * s, 1);
+      tc::mbar_init(empty0 + 8 * s, 1);
+    }
+    tc::mbar_init(accum, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tc::tmem_alloc(smem_u32(tmem_slot), BN);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+    int issued = 0;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      if (kb >= STAGES && !tc::mbar_wait(empty0 + 8 * s, ph ^ 1, err)) { s_abort = 1; break; }
+      if (s_abort) break;
+      const uint32_t a_dst = smem_u32(smem + s * STAGE);
+      const uint32_t b_dst = a_dst + A_BYTES;
+      tc::mbar_expect_tx(full0 + 8 * s, STAGE);
+      tc::tma_load_2d(a_dst, &tmA, full0 + 8 * s, kb * BK, m0);
+      if (EPI == EPI_SWIGLU) {
+        tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kb * BK, n0);
+        tc::tma_load_2d(b_dst + B_BYTES / 2, &tmB2, full0 + 8 * s, kb * BK, n0);
+      } else {
+        tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kb * BK, n0);
+      }
+      ++issued;
+    }
+    // drain: every issued stage must land before the CTA may exit
+    for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
+      tc::mbar_wait(full0 + 8 * (kb % STAGES), (kb / STAGES) & 1, err);
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = EPI == EPI_SWIGLU ? tc::idesc_f16(BM, BN / 2) : tc::idesc_f16(BM, BN);
+    bool ok = true;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % STAGES;
+      if (!tc::mbar_wait(full0 + 8 * s, (kb / STAGES) & 1, err)) { ok = false; s_abort = 1; break; }
+      tc::tc_fence_after();
+      const uint32_t a_base = smem_u32(smem + s * STAGE);
+      const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k) {
+        const uint64_t da = tc::smem_desc_sw128(a_base + 32 * k);
+        if (EPI == EPI_SWIGLU) {
+          tc::mma_f16(tmem, da, tc::smem_desc_sw128(b_base + 32 * k), idesc, (kb | k) != 0);
+          tc::mma_f16(tmem + BN / 2, da, tc::smem_desc_sw128(b_base + B_BYTES / 2 + 32 * k), idesc,
+                       (kb | k) != 0);
+        } else {
+          tc::mma_f16(tmem, da, tc::smem_desc_sw128(b_base + 32 * k), idesc, (kb | k) != 0);
+        }
+      }
+      tc::mma_commit(empty0 + 8 * s);
+    }
+    if (ok) tc::mma_commit(accum);
+  } else if (warp >= 2) {
+    // ---- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
+    const int q = warp & 3;
+    const int row = m0 + q * 32 + lane;
+    if (tc::mbar_wait(accum, 0, err)) {
+      tc::tc_fence_after();
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      if (EPI == EPI_SWIGLU) {
+        for (int c = 0; c < BN / 2; c += 32) {
+          float g[32], u[32];
+          tc::tmem_ld32(lane_base + c, g);
+          tc::tmem_ld32(lane_base + BN / 2 + c, u);
+          if (row < M) {
+            f16* out = ep.Cb + (size_t)row * ep.ldc + n0 + c;
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int col = n0 + c + i;
+              const float a0 = (g[i] / (1.f + expf(-g[i]))) * u[i];
+              const float a1 = (g[i + 1] / (1.f + expf(-g[i + 1]))) * u[i + 1];
+              if (col + 1 < N) {
+                *reinterpret_cast<__half2*>(out + i) = __floats2half2_rn(a0, a1);
+              } else if (col < N) {
+                out[i] = __float2half_rn(a0);
+              }
+            }
+          }
+        }
+      } else {
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tc::tmem_ld32(lane_base + c, v);
+          if (row < M) {
+            float* out = ep.C + (size_t)row * ep.ldc + n0 + c;
+            if (n0 + c + 32 <= N) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                float4 o;
+                if (EPI == EPI_ADD) {
+                  o = *reinterpret_cast<const float4*>(out + i);
+                  o.x += v[i]; o.y += v[i + 1]; o.z += v[i + 2]; o.w += v[i + 3];
+                } else {
+                  o = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                  if (ep.bias) {
+                    o.x += to_f32(ep.bias[n0 + c + i]);
+                    o.y += to_f32(ep.bias[n0 + c + i + 1]);
+                    o.z += to_f32(ep.bias[n0 + c + i + 2]);
+                    o.w += to_f32(ep.bias[n0 + c + i + 3]);
+                  }
+                }
+                *reinterpret_cast<float4*>(out + i) = o;
+              }
+            } else {
+              for (int i = 0; i < 32 && n0 + c + i < N; ++i) {
+                float o = v[i];
+                if (EPI == EPI_ADD) o += out[i];
+                else if (ep.bias) o += to_f32(ep.bias[n0 + c + i]);
+                out[i] = o;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, BN);
+  }
+}
+
+// ---- host side ------------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+// 2-D fp16 row-major [rows][cols] (row pitch ld elements), box 64 x box_rows, 128B swizzle
+static bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int ld, int box_rows) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  if (((uintptr_t)base & 15) || ((size_t)ld * 2) % 16) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)tc::BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+static constexpr size_t tc_smem() {
+  return (size_t)tc::STAGES * (tc::BM * tc::BK * 2 + BN * tc::BK * 2) + 1024 + 256;
+}
+
+constexpr int TC_BN = 256;
+
+cudaError_t gemm_tc_set_attributes() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>()))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>()))) return e;
+  return cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>());
+}
+
+bool gemm_tc_available() { return encode_fn() != nullptr; }
+
+// C[M][N] (fp32, ldc) = / += A[M][K] (fp16, lda) . B[N][K]^T (fp16, ldb) (+ bias[N], bf16)
+cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bias, float* C, int ldc,
+                    int M, int N, int K, bool accumulate, int* err, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mb, B, N, K, ldb, TC_BN)) return cudaErrorInvalidValue;
+  TcEpi ep{C, bias, nullptr, ldc};
+  const dim3 grid((N + TC_BN - 1) / TC_BN, (M + tc::BM - 1) / tc::BM);
+  if (accumulate)
+    gemm_tc_kernel<TC_BN, EPI_ADD><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err);
+  else
+    gemm_tc_kernel<TC_BN, EPI_STORE><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err);
+  return cudaGetLastError();
+}
+
+// Act[M][N] (fp16, ldc) = silu(A . Wg^T) * (A . Wu^T)
+cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, int ldb, f16* Act,
+                           int ldc, int M, int N, int K, int* err, cudaStream_t s) {
+  CUtensorMap ma, mg, mu;
+  if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mg, Wg, N, K, ldb, TC_BN / 2) ||
+      !make_map(&mu, Wu, N, K, ldb, TC_BN / 2))
+    return cudaErrorInvalidValue;
+  TcEpi ep{nullptr, nullptr, Act, ldc};
+  const dim3 grid((N + TC_BN / 2 - 1) / (TC_BN / 2), (M + tc::BM - 1) / tc::BM);
+  gemm_tc_kernel<TC_BN, EPI_SWIGLU><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mg, mu, ep, M, N, K, err);
+  return cudaGetLastError();
+}
+
+}  // namespace qw

@@ -1,6 +1,8 @@
 // Host-side declarations shared by the libqw translation units.
 #pragma once
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -23,6 +25,8 @@ struct Dims {
 
 struct LayerPtrs {
   const void *in_norm, *wq, *bq, *wk, *bk, *wv, *bv, *wo, *post_norm, *w_gate, *w_up, *w_down;
+  // fp16 copies of the matrices (bf16 models; prefill tensor-core operands)
+  const void *wq16, *wk16, *wv16, *wo16, *wg16, *wu16, *wd16;
 };
 
 // Argmax / position bookkeeping written by the last CTA of the LM-head kernel.
@@ -51,7 +55,8 @@ cudaError_t launch_qkv(const Dims& d, const LayerPtrs& w, const float* x, const 
                        const float2* rope, float* q, void* kc, void* vc, cudaStream_t s,
                        bool pdl);
 // ctx = d_pos ? d_pos[0] + 1 : ctx_host
-cudaError_t launch_attn(int dtype, int nq, int nkv, int hd, int nsplit, int chunk_min,
+// kv_dtype: 0 fp32, 2 fp16
+cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int chunk_min,
                         size_t smem, const float* q, const void* kc, const void* vc,
                         int kv_stride, const int* d_pos, int ctx_host, float* out, void* ws,
                         cudaStream_t s, bool pdl);
@@ -63,16 +68,28 @@ cudaError_t launch_gateup(const Dims& d, const LayerPtrs& w, const float* x, flo
 cudaError_t launch_lmhead(const Dims& d, const void* W, const void* final_norm, const float* x,
                           float* logits, const Finalize& f, cudaStream_t s, bool pdl);
 
+// ---- gemm_tc.cu (tcgen05 tensor-core GEMMs, bf16 in, fp32 accumulate) ----
+bool gemm_tc_available();
+cudaError_t gemm_tc_set_attributes();
+// fp16 operands (A activations, B weights), fp32 accumulate; bias bf16
+cudaError_t gemm_tc(const __half* A, int lda, const __half* B, int ldb, const __nv_bfloat16* bias,
+                    float* C, int ldc, int M, int N, int K, bool accumulate, int* err,
+                    cudaStream_t s);
+cudaError_t gemm_tc_swiglu(const __half* A, int lda, const __half* Wg, const __half* Wu, int ldb,
+                           __half* Act, int ldc, int M, int N, int K, int* err, cudaStream_t s);
+
 // ---- prefill.cu ----
 struct PrefillBufs {
   float *X, *Xn, *Y, *Q, *O, *G, *U;  // [T][..] fp32 activations
+  __half *Xh, *Oh, *Ah;               // fp16 tensor-core operands [T][H], [T][nq*hd], [T][I]
   int cap_tokens;
+  bool use_tc;
 };
 cudaError_t prefill_set_attributes(const Dims& d);
 // Runs all layers over T tokens at positions pos0..pos0+T-1 of one sequence.
 cudaError_t prefill_layers(const Dims& d, const LayerPtrs* layers, const void* embed,
                            const int* ids_dev, int T, int pos0, const float2* rope,
-                           void* kcache_seq, void* vcache_seq, const PrefillBufs& b, int* err,
-                           cudaStream_t s);
+                           void* kcache_seq, const PrefillBufs& b, int* err, cudaStream_t s);
+cudaError_t convert_bf16_to_half(const void* src, void* dst, size_t n, int* err, cudaStream_t s);
 
 }  // namespace qw

@@ -27,16 +27,22 @@ __global__ void embed_rows_kernel(const T* E, int V, int H, const int* ids, floa
   for (int k = threadIdx.x; k < H; k += blockDim.x) X[(size_t)t * H + k] = to_f32(row[k]);
 }
 
-template <typename T>
-__global__ void norm_rows_kernel(const float* X, const T* gain, int H, float eps, float* Y) {
+template <typename T, typename OutT>
+__global__ void norm_rows_kernel(const float* X, const T* gain, int H, float eps, OutT* Y) {
   __shared__ float scratch[32];
   const float* x = X + (size_t)blockIdx.x * H;
   float ss = 0.f;
   for (int k = threadIdx.x; k < H; k += blockDim.x) ss = fmaf(x[k], x[k], ss);
   ss = block_sum(ss, scratch);
   const float inv = rsqrtf(ss / (float)H + eps);
-  float* y = Y + (size_t)blockIdx.x * H;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) y[k] = x[k] * inv * to_f32(gain[k]);
+  OutT* y = Y + (size_t)blockIdx.x * H;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) y[k] = from_f32<OutT>(x[k] * inv * to_f32(gain[k]));
+}
+
+// fp32 -> fp16 rows (tensor-core A operand)
+__global__ void to_half_kernel(const float* X, f16* Y, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    Y[i] = __float2half_rn(X[i]);
 }
 
 __global__ void swiglu_kernel(const float* G, const float* U, float* A, size_t n) {
@@ -48,9 +54,9 @@ __global__ void swiglu_kernel(const float* G, const float* U, float* A, size_t n
 
 // Y [T][nq*hd + 2*nkv*hd] (q | k | v, bias included) -> Q [T][nq*hd] rotated;
 // K, V rotated/copied into the cache at positions pos0 + t.
-template <typename T>
+template <typename KV>
 __global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, int pos0, int cap,
-                               const float2* rope, float* Q, T* kc, T* vc) {
+                               const float2* rope, float* Q, KV* kc, KV* vc) {
   const int t = blockIdx.x;
   const int half = hd / 2;
   const int width = (nq + 2 * nkv) * hd;
@@ -66,14 +72,14 @@ __global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, 
         Q[(size_t)t * nq * hd + head * hd + i] = ra;
         Q[(size_t)t * nq * hd + head * hd + i + half] = rb;
       } else {
-        T* dst = kc + ((size_t)(head - nq) * cap + pos) * hd;
-        dst[i] = from_f32<T>(ra);
-        dst[i + half] = from_f32<T>(rb);
+        KV* dst = kc + ((size_t)(head - nq) * cap + pos) * hd;
+        dst[i] = from_f32<KV>(ra);
+        dst[i + half] = from_f32<KV>(rb);
       }
     } else {
-      T* dst = vc + ((size_t)(head - nq - nkv) * cap + pos) * hd;
-      dst[i] = from_f32<T>(a);
-      dst[i + half] = from_f32<T>(b);
+      KV* dst = vc + ((size_t)(head - nq - nkv) * cap + pos) * hd;
+      dst[i] = from_f32<KV>(a);
+      dst[i + half] = from_f32<KV>(b);
     }
   }
 }
@@ -151,7 +157,7 @@ constexpr int FA_BQ = 64, FA_BK = 64;
 template <typename T, int HD>
 __global__ void __launch_bounds__(256)
 attn_prefill_simt_kernel(const float* Q, int T_, int nq, int nkv, int pos0, const T* kc,
-                         const T* vc, int cap, float scale, float* O) {
+                         const T* vc, int cap, float scale, float* O) {  // T: KV element type
   extern __shared__ float fsm[];
   float* qs = fsm;                       // [BQ][HD+1]
   float* ks = qs + FA_BQ * (HD + 1);     // [BK][HD+1]
@@ -266,46 +272,94 @@ static cudaError_t set_attr_t() {
 }
 
 cudaError_t prefill_set_attributes(const Dims& d) {
-  return d.dtype == 1 ? set_attr_t<bf16>() : set_attr_t<float>();
+  cudaError_t e = d.dtype == 1 ? set_attr_t<f16>() : set_attr_t<float>();
+  if (e || d.dtype != 1) return e;
+  return gemm_tc_available() ? gemm_tc_set_attributes() : cudaSuccess;
 }
 
-template <typename T>
-static cudaError_t prefill_t(const Dims& d, const LayerPtrs* layers, const void* embed,
-                             const int* ids, int T_, int pos0, const float2* rope, void* kcache,
-                             void* vcache, const PrefillBufs& b, int* err, cudaStream_t s) {
-  const int H = d.H, qd = d.nq * d.hd, kvd = d.nkv * d.hd, W = qd + 2 * kvd;
-  embed_rows_kernel<T><<<T_, 256, 0, s>>>((const T*)embed, d.V, H, ids, b.X, err);
+template <typename W, typename KV>
+static cudaError_t prefill_simt(const Dims& d, const LayerPtrs* layers, const void* embed,
+                                const int* ids, int T_, int pos0, const float2* rope, void* kcache,
+                                const PrefillBufs& b, int* err, cudaStream_t s) {
+  const int H = d.H, qd = d.nq * d.hd, kvd = d.nkv * d.hd, Wd = qd + 2 * kvd;
+  embed_rows_kernel<W><<<T_, 256, 0, s>>>((const W*)embed, d.V, H, ids, b.X, err);
   const size_t layer_stride = (size_t)d.nkv * d.cap * d.hd;  // elements per layer per K or V
   for (int l = 0; l < d.L; ++l) {
     const LayerPtrs& w = layers[l];
-    T* kc = (T*)kcache + (size_t)l * 2 * layer_stride;
-    T* vc = kc + layer_stride;
-    norm_rows_kernel<T><<<T_, 256, 0, s>>>(b.X, (const T*)w.in_norm, H, d.eps, b.Xn);
-    gemm_simt<T>(b.Xn, H, w.wq, H, w.bq, b.Y, W, T_, qd, H, false, s);
-    gemm_simt<T>(b.Xn, H, w.wk, H, w.bk, b.Y + qd, W, T_, kvd, H, false, s);
-    gemm_simt<T>(b.Xn, H, w.wv, H, w.bv, b.Y + qd + kvd, W, T_, kvd, H, false, s);
-    rope_kv_kernel<T><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc);
-    cudaError_t e = attn_prefill<T>(d, b.Q, T_, pos0, kc, vc, b.O, s);
+    KV* kc = (KV*)kcache + (size_t)l * 2 * layer_stride;
+    KV* vc = kc + layer_stride;
+    norm_rows_kernel<W, float><<<T_, 256, 0, s>>>(b.X, (const W*)w.in_norm, H, d.eps, b.Xn);
+    gemm_simt<W>(b.Xn, H, w.wq, H, w.bq, b.Y, Wd, T_, qd, H, false, s);
+    gemm_simt<W>(b.Xn, H, w.wk, H, w.bk, b.Y + qd, Wd, T_, kvd, H, false, s);
+    gemm_simt<W>(b.Xn, H, w.wv, H, w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, s);
+    rope_kv_kernel<KV><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc);
+    cudaError_t e = attn_prefill<KV>(d, b.Q, T_, pos0, kc, vc, b.O, s);
     if (e) return e;
-    gemm_simt<T>(b.O, qd, w.wo, qd, nullptr, b.X, H, T_, H, qd, true, s);
-    norm_rows_kernel<T><<<T_, 256, 0, s>>>(b.X, (const T*)w.post_norm, H, d.eps, b.Xn);
-    gemm_simt<T>(b.Xn, H, w.w_gate, H, nullptr, b.G, d.I, T_, d.I, H, false, s);
-    gemm_simt<T>(b.Xn, H, w.w_up, H, nullptr, b.U, d.I, T_, d.I, H, false, s);
+    gemm_simt<W>(b.O, qd, w.wo, qd, nullptr, b.X, H, T_, H, qd, true, s);
+    norm_rows_kernel<W, float><<<T_, 256, 0, s>>>(b.X, (const W*)w.post_norm, H, d.eps, b.Xn);
+    gemm_simt<W>(b.Xn, H, w.w_gate, H, nullptr, b.G, d.I, T_, d.I, H, false, s);
+    gemm_simt<W>(b.Xn, H, w.w_up, H, nullptr, b.U, d.I, T_, d.I, H, false, s);
     const size_t n = (size_t)T_ * d.I;
     swiglu_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, s>>>(b.G, b.U, b.G, n);
-    gemm_simt<T>(b.G, d.I, w.w_down, d.I, nullptr, b.X, H, T_, H, d.I, true, s);
+    gemm_simt<W>(b.G, d.I, w.w_down, d.I, nullptr, b.X, H, T_, H, d.I, true, s);
+  }
+  return cudaGetLastError();
+}
+
+// bf16 models: every projection on the tensor cores with fp16 operands (fp16 copies of the
+// bf16 weights are exact; fp16 activations round 8x finer than bf16), fp32 accumulation,
+// fp32 residual stream, fp16 KV cache.
+static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void* embed,
+                              const int* ids, int T_, int pos0, const float2* rope, void* kcache,
+                              const PrefillBufs& b, int* err, cudaStream_t s) {
+  const int H = d.H, qd = d.nq * d.hd, kvd = d.nkv * d.hd, Wd = qd + 2 * kvd;
+  embed_rows_kernel<bf16><<<T_, 256, 0, s>>>((const bf16*)embed, d.V, H, ids, b.X, err);
+  const size_t layer_stride = (size_t)d.nkv * d.cap * d.hd;
+  cudaError_t e;
+  for (int l = 0; l < d.L; ++l) {
+    const LayerPtrs& w = layers[l];
+    f16* kc = (f16*)kcache + (size_t)l * 2 * layer_stride;
+    f16* vc = kc + layer_stride;
+    norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.in_norm, H, d.eps, b.Xh);
+    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wq16, H, (const bf16*)w.bq, b.Y, Wd, T_, qd, H, false, err, s))) return e;
+    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wk16, H, (const bf16*)w.bk, b.Y + qd, Wd, T_, kvd, H, false, err, s))) return e;
+    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wv16, H, (const bf16*)w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, err, s))) return e;
+    rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc);
+    if ((e = attn_prefill<f16>(d, b.Q, T_, pos0, kc, vc, b.O, s))) return e;
+    const size_t no = (size_t)T_ * qd;
+    to_half_kernel<<<(unsigned)((no + 255) / 256 < 4096 ? (no + 255) / 256 : 4096), 256, 0, s>>>(b.O, b.Oh, no);
+    if ((e = gemm_tc(b.Oh, qd, (const f16*)w.wo16, qd, nullptr, b.X, H, T_, H, qd, true, err, s))) return e;
+    norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.post_norm, H, d.eps, b.Xh);
+    if ((e = gemm_tc_swiglu(b.Xh, H, (const f16*)w.wg16, (const f16*)w.wu16, H, b.Ah, d.I, T_, d.I, H, err, s)))
+      return e;
+    if ((e = gemm_tc(b.Ah, d.I, (const f16*)w.wd16, d.I, nullptr, b.X, H, T_, H, d.I, true, err, s))) return e;
   }
   return cudaGetLastError();
 }
 
 cudaError_t prefill_layers(const Dims& d, const LayerPtrs* layers, const void* embed,
                            const int* ids_dev, int T, int pos0, const float2* rope,
-                           void* kcache_seq, void* vcache_seq, const PrefillBufs& b, int* err,
-                           cudaStream_t s) {
-  (void)vcache_seq;
-  return d.dtype == 1
-             ? prefill_t<bf16>(d, layers, embed, ids_dev, T, pos0, rope, kcache_seq, vcache_seq, b, err, s)
-             : prefill_t<float>(d, layers, embed, ids_dev, T, pos0, rope, kcache_seq, vcache_seq, b, err, s);
+                           void* kcache_seq, const PrefillBufs& b, int* err, cudaStream_t s) {
+  if (d.dtype == 1) {
+    if (b.use_tc) return prefill_tc(d, layers, embed, ids_dev, T, pos0, rope, kcache_seq, b, err, s);
+    return prefill_simt<bf16, f16>(d, layers, embed, ids_dev, T, pos0, rope, kcache_seq, b, err, s);
+  }
+  return prefill_simt<float, float>(d, layers, embed, ids_dev, T, pos0, rope, kcache_seq, b, err, s);
+}
+
+// bf16 -> fp16 weight copy (exact for |x| >= 2^-24 * 2^8 and below 65504); flags overflow
+__global__ void bf16_to_half_kernel(const bf16* src, f16* dst, size_t n, int* err) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float v = __bfloat162float(src[i]);
+    if (fabsf(v) > 65504.f) atomicOr(err, ERR_NONFINITE);
+    dst[i] = __float2half_rn(v);
+  }
+}
+
+cudaError_t convert_bf16_to_half(const void* src, void* dst, size_t n, int* err, cudaStream_t s) {
+  const size_t blocks = (n + 255) / 256;
+  bf16_to_half_kernel<<<(unsigned)(blocks < 8192 ? blocks : 8192), 256, 0, s>>>((const bf16*)src, (f16*)dst, n, err);
+  return cudaGetLastError();
 }
 
 }  // namespace qw

@@ -16,11 +16,7 @@ def _built():
     __graft_entry__.build()
 
 
-def _bf16_round(a):
-    return torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).to(torch.float32).numpy()
-
-
-@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("dtype", [0, 2])  # KV cache element: fp32, fp16
 @pytest.mark.parametrize("nq,nkv,hd,ctx,stride", [
     (12, 2, 128, 1, 2048),
     (12, 2, 128, 31, 2048),
@@ -40,10 +36,10 @@ def test_decode_attention_matches_oracle(dtype, nq, nkv, hd, ctx, stride):
     q = rng.standard_normal(nq * hd).astype(np.float32)
     k = rng.standard_normal((nkv, stride, hd)).astype(np.float32)
     v = rng.standard_normal((nkv, stride, hd)).astype(np.float32)
-    if dtype == 1:
-        k, v = _bf16_round(k), _bf16_round(v)
-        tk = torch.from_numpy(k).to(torch.bfloat16).cuda()
-        tv = torch.from_numpy(v).to(torch.bfloat16).cuda()
+    if dtype == 2:
+        k, v = k.astype(np.float16).astype(np.float32), v.astype(np.float16).astype(np.float32)
+        tk = torch.from_numpy(k).to(torch.float16).cuda()
+        tv = torch.from_numpy(v).to(torch.float16).cuda()
     else:
         tk, tv = torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda()
     tq = torch.from_numpy(q).cuda()
@@ -67,6 +63,8 @@ def test_decode_attention_matches_oracle(dtype, nq, nkv, hd, ctx, stride):
 def test_decode_attention_rejects_bad_arguments():
     from qwen2_decoder_forward_decode_gb300 import binding
     with pytest.raises(binding.QwError):
-        binding.decode_attention(1, 12, 2, 128, 100, 50, 1, 1, 1, 1, 1, 1 << 20)  # ctx > stride
+        binding.decode_attention(2, 12, 2, 128, 100, 50, 1, 1, 1, 1, 1, 1 << 20)  # ctx > stride
     with pytest.raises(binding.QwError):
-        binding.decode_attention(1, 12, 2, 128, 10, 64, 16, 16, 16, 16, 16, 8)   # workspace small
+        binding.decode_attention(2, 12, 2, 128, 10, 64, 16, 16, 16, 16, 16, 8)   # workspace small
+    with pytest.raises(binding.QwError):
+        binding.decode_attention(1, 12, 2, 128, 10, 64, 16, 16, 16, 16, 16, 1 << 20)  # bf16 KV

@@ -64,6 +64,19 @@ def test_tiny_without_graphs_matches(monkeypatch):
         m.close()
 
 
+@pytest.mark.parametrize("simt", ["0", "1"])
+def test_bf16_prefill_paths(monkeypatch, simt):
+    """The tensor-core prefill (default for bf16) and the CUDA-core prefill
+    (QW_PREFILL_SIMT=1) both match the oracle on a ragged shape."""
+    monkeypatch.setenv("QW_PREFILL_SIMT", simt)
+    w, prompt, toks, logits = oracle_run("small_bf16", 300, 4)
+    m = _model("small_bf16", w, 320)
+    try:
+        run_teacher_forced(m, SHAPES["small_bf16"], prompt, toks, logits)
+    finally:
+        m.close()
+
+
 def test_0p5b_workload_full():
     wl = WORKLOADS["0p5b"]
     w, prompt, toks, logits = oracle_run(wl.shape, wl.prompt_len, wl.new_tokens)
