@@ -17,7 +17,7 @@ Sources (page title, then the section on it):
 Notation follows [LSA]: activations are column matrices [features, T] ("all vectors
 are column vectors"); weights are [out, in] so a projection is ``W @ x``.
 
-Readings where the pages are garbled or silent (each is listed in the design doc too):
+Readings where the pages are garbled or silent:
   * RoPE frequency of pair i is theta^(-2i/head_dim), i < head_dim/2; pairs are
     (i, i + head_dim/2) ("split-half"); angle = position * frequency in float64.
   * RoPE is applied to q and k after the bias and before k enters the cache; v is not
