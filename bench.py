@@ -192,6 +192,9 @@ def run_native(args):
     torch.cuda.set_device(local)
     wl = WORKLOADS[WORKLOAD]
     s = SHAPES[wl.shape]
+    if args.layers:
+        import dataclasses
+        s = dataclasses.replace(s, n_layers=args.layers)
     n_dec = wl.new_tokens - 1
     w = make_weights(s)
     dw = DeviceWeights(w, 1)
@@ -247,6 +250,9 @@ def run_native(args):
     # timed region (the traced kernel runs without PDL overlap).
     begin = [torch.cuda.Event(enable_timing=True) for _ in range(s.n_layers)]
     end = [torch.cuda.Event(enable_timing=True) for _ in range(s.n_layers)]
+    for e in begin + end:  # torch creates the CUDA event at its first record
+        e.record(stream)
+    stream.synchronize()
     m.set_trace(3, begin, end)
     m.prefill_device(ids_dev.data_ptr(), len(prompt))
     kt = []
@@ -261,6 +267,14 @@ def run_native(args):
     achieved = gu_bytes / (gu_ms / 1000.0) / 1e9
     src = source_hash()
     traffic = recorded_traffic("gateup_gemv", src)
+
+    if args.layers:
+        # profiling run on a reduced stack: timed loop only, not a bench line
+        if rank == 0:
+            print(json.dumps({"profile_run": True, "layers": s.n_layers, "decode_tok_s": value,
+                              "gateup_us": gu_ms * 1000.0}), flush=True)
+        m.close()
+        return
 
     # ---- end to end through the public API with host buffers (qw_generate: H2D of the
     # prompt, prefill, decode loop, D2H of the tokens) and host-side TTFT (qw_prefill).
@@ -330,6 +344,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: build the 1.5B shape with this many layers")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
