@@ -182,6 +182,30 @@ qw_status qw_op_decode_attention(int32_t kv_dtype, int32_t n_heads, int32_t n_kv
                                  void *workspace, size_t workspace_bytes,
                                  void *cuda_stream);
 
+/* Decode attention for callers that cannot allocate device memory. The pages have no
+ * counterpart: this is a deployment variant of qw_op_decode_attention, computing the same
+ * result (same kernel) with its scratch (the split-context partials and the per-KV-head
+ * counters) in one fixed 1 MiB array inside the library instead of a caller workspace.
+ * It is meant for callers that cannot call cudaMalloc where they call attention: code
+ * embedded in another runtime that owns all device memory, or loops that must not pay
+ * cudaMalloc's implicit device synchronisation or risk an allocation failure mid-run.
+ *   - Arguments, layouts and errors are those of qw_op_decode_attention, without the
+ *     workspace. Shapes whose scratch exceeds qw_op_decode_attention_noalloc_limit()
+ *     bytes are rejected with QW_ERR_UNSUPPORTED (1 MiB fits, for example, 12 query /
+ *     2 KV heads of dimension 128 with kv_stride up to 8192).
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library routine. Every
+ *     GPU that loads the library holds the array until the process exits.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - Each call clears the counters it needs (cudaMemsetAsync on cuda_stream). All calls
+ *     share the one array: calls that overlap on the GPU (other streams, other threads)
+ *     race on it and must be serialised by the caller. */
+qw_status qw_op_decode_attention_noalloc(int32_t kv_dtype, int32_t n_heads, int32_t n_kv_heads,
+                                         int32_t head_dim, int32_t ctx, int32_t kv_stride,
+                                         const float *q, const void *k, const void *v,
+                                         float *out, void *cuda_stream);
+size_t qw_op_decode_attention_noalloc_limit(void);
+
 /* Dense GEMM on the tensor cores (tcgen05), the contraction of every prefill projection
  * [LSA Implementing Qwen: W @ x for all prompt columns at once; QIE §1: prefill is
  * compute-bound]: C[M][N] = A[M][K] . B[N][K]^T (+ bias[N]), or C += A . B^T when

@@ -78,6 +78,8 @@ def lib():
         "qw_reset": ([VP, I32], I32),
         "qw_last_error": ([], ctypes.c_char_p),
         "qw_set_trace": ([VP, I32, P(VP), P(VP)], I32),
+        "qw_op_decode_attention_noalloc": ([I32, I32, I32, I32, I32, I32, VP, VP, VP, VP, VP], I32),
+        "qw_op_decode_attention_noalloc_limit": ([], SZ),
         "qw_op_gemm_f16": ([I32, I32, I32, VP, VP, VP, VP, I32, VP, VP], I32),
         "qw_op_gemm_swiglu_f16": ([I32, I32, I32, VP, VP, VP, VP, VP, VP], I32),
         "qw_op_decode_attention_workspace": ([I32, I32, I32, I32], SZ),
@@ -95,7 +97,8 @@ def exported_symbols():
     return ["qw_create", "qw_destroy", "qw_prefill", "qw_prefill_device", "qw_decode_step",
             "qw_decode_steps", "qw_generate", "qw_sync", "qw_logits", "qw_read_logits",
             "qw_tokens_device", "qw_position", "qw_reset", "qw_last_error", "qw_set_trace",
-            "qw_op_decode_attention_workspace", "qw_op_decode_attention", "qw_op_gemm_f16",
+            "qw_op_decode_attention_workspace", "qw_op_decode_attention",
+            "qw_op_decode_attention_noalloc", "qw_op_decode_attention_noalloc_limit", "qw_op_gemm_f16",
             "qw_op_gemm_swiglu_f16"]
 
 
@@ -250,6 +253,13 @@ def decode_attention(dtype, n_heads, n_kv_heads, head_dim, ctx, kv_stride, q_ptr
                      out_ptr, ws_ptr, ws_bytes, stream=None):
     check(lib().qw_op_decode_attention(dtype, n_heads, n_kv_heads, head_dim, ctx, kv_stride,
                                        q_ptr, k_ptr, v_ptr, out_ptr, ws_ptr, ws_bytes, stream))
+
+
+def decode_attention_noalloc(kv_dtype, n_heads, n_kv_heads, head_dim, ctx, kv_stride, q_ptr, k_ptr,
+                             v_ptr, out_ptr, stream=None):
+    """Decode attention whose scratch is the library's fixed array (no allocation)."""
+    check(lib().qw_op_decode_attention_noalloc(kv_dtype, n_heads, n_kv_heads, head_dim, ctx,
+                                               kv_stride, q_ptr, k_ptr, v_ptr, out_ptr, stream))
 
 
 def decode_attention_workspace(n_heads, n_kv_heads, head_dim, max_ctx):

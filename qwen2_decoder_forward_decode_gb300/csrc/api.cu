@@ -48,6 +48,8 @@ constexpr int OP_SM_HINT = 152;  // split count of the single-op attention entry
 
 }  // namespace
 
+void qw::set_error_message(const char* msg) { g_err = msg; }
+
 struct qw_model {
   Dims d;
   qw_config cfg;

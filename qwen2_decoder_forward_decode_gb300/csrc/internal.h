@@ -42,6 +42,9 @@ struct Finalize {
   int* err;
 };
 
+// ---- api.cu ----
+void set_error_message(const char* msg);  // message returned by qw_last_error on this thread
+
 // ---- decode.cu ----
 size_t attn_workspace_bytes(int nq, int nkv, int hd, int nsplit);
 int attn_nsplit_for(int nsm, int nkv, int cap, int chunk_min);
