@@ -44,7 +44,6 @@ bool fault_injected(const char* what) {
 }
 
 constexpr int ATTN_CHUNK_MIN = 32;
-constexpr int OP_SM_HINT = 152;  // split count of the single-op attention entry point
 
 }  // namespace
 
@@ -298,8 +297,9 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
   if ((e = cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, m->device)))
     return bail(e, "cudaDeviceGetAttribute");
   d.attn_chunk_min = ATTN_CHUNK_MIN;
-  d.attn_nsplit = attn_nsplit_for(d.nsm, d.nkv, d.cap, d.attn_chunk_min);
-  m->attn_smem = attn_smem_bytes(d.nq / d.nkv, d.hd, d.cap, d.attn_nsplit, d.attn_chunk_min);
+  d.attn_nsplit = attn_nsplit_for(d.cap, d.attn_chunk_min, d.hd, cfg->dtype == QW_BF16 ? 2 : 4);
+  m->attn_smem = attn_smem_bytes(d.nq / d.nkv, d.hd, d.cap, d.attn_nsplit, d.attn_chunk_min,
+                                 cfg->dtype == QW_BF16 ? 2 : 4);
   if (cuda_stream) {
     m->stream = (cudaStream_t)cuda_stream;
   } else {
@@ -613,14 +613,15 @@ qw_status qw_reset(qw_model* m, int32_t seq) {
 
 // ---- single-op entry points ----
 
-static int op_attn_nsplit(int nkv, int max_ctx) {
-  return attn_nsplit_for(OP_SM_HINT, nkv, max_ctx, ATTN_CHUNK_MIN);
+static int op_attn_nsplit(int head_dim, int max_ctx, int kv_bytes) {
+  return attn_nsplit_for(max_ctx, ATTN_CHUNK_MIN, head_dim, kv_bytes);
 }
 
 size_t qw_op_decode_attention_workspace(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                         int32_t max_ctx) {
   if (n_heads < 1 || n_kv_heads < 1 || head_dim < 2 || max_ctx < 1) return 0;
-  return attn_workspace_bytes(n_heads, n_kv_heads, head_dim, op_attn_nsplit(n_kv_heads, max_ctx));
+  // fp32 keys and values need the most chunks; the fp16 case fits the same workspace
+  return attn_workspace_bytes(n_heads, n_kv_heads, head_dim, op_attn_nsplit(head_dim, max_ctx, 4));
 }
 
 qw_status qw_op_decode_attention(int32_t kv_dtype, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
@@ -633,12 +634,13 @@ qw_status qw_op_decode_attention(int32_t kv_dtype, int32_t n_heads, int32_t n_kv
   if (n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || head_dim < 2 || ctx < 1 || kv_stride < ctx)
     return fail(QW_ERR_INVALID_ARG, "bad attention shape");
   if (n_heads / n_kv_heads > 8) return fail(QW_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
-  const int nsplit = op_attn_nsplit(n_kv_heads, kv_stride);
+  const int nsplit = op_attn_nsplit(head_dim, kv_stride, kv_dtype == QW_F16 ? 2 : 4);
   const size_t need = attn_workspace_bytes(n_heads, n_kv_heads, head_dim, nsplit);
   if (workspace_bytes < need) return fail(QW_ERR_INVALID_ARG, "workspace too small");
   if ((uintptr_t)workspace % 16) return fail(QW_ERR_INVALID_ARG, "workspace not 16-byte aligned");
-  const size_t smem = attn_smem_bytes(n_heads / n_kv_heads, head_dim, kv_stride, nsplit, ATTN_CHUNK_MIN);
-  if (smem > 200 * 1024) return fail(QW_ERR_UNSUPPORTED, "attention chunk too large");
+  const size_t smem = attn_smem_bytes(n_heads / n_kv_heads, head_dim, kv_stride, nsplit, ATTN_CHUNK_MIN,
+                                      kv_dtype == QW_F16 ? 2 : 4);
+  if (smem > 220 * 1024) return fail(QW_ERR_UNSUPPORTED, "attention chunk too large for shared memory");
   cudaError_t e = attn_set_attributes(smem);
   if (e) return cuda_fail(e, "decode attention attributes");
   e = launch_attn(kv_dtype, n_heads, n_kv_heads, head_dim, nsplit, ATTN_CHUNK_MIN, smem, q, k, v,

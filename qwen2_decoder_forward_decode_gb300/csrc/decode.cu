@@ -25,23 +25,74 @@ constexpr int GMAX = 8;  // most query heads per KV head handled by decode atten
 
 // ---- input-vector prologues ------------------------------------------------------------
 
-// xs = x / sqrt(mean(x^2) + eps) * gain
+// Four consecutive gains as fp32 (weights: read-only path).
+__device__ __forceinline__ float4 load_gain4(const float* g, int j) {
+  return __ldg(reinterpret_cast<const float4*>(g) + j);
+}
+__device__ __forceinline__ float4 load_gain4(const bf16* g, int j) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(g) + j);
+  return make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
+}
+
+constexpr int PRO_BATCH = 4;  // float4 loads per thread kept in flight by the prologues
+
+// xs = x / sqrt(mean(x^2) + eps) * gain, K % 4 == 0. The loads of x and of the gains are
+// issued in batches of PRO_BATCH per thread before any is used, so the prologue costs one
+// memory round trip per 4 * 4 * blockDim elements instead of one per loop iteration.
 template <typename T>
-__device__ __forceinline__ void prologue_norm(float* xs, float* scratch, const float* x,
+__device__ __forceinline__ void prologue_norm(float* xs, float* gs, float* scratch, const float* x,
                                               const T* gain, int K, float eps) {
+  const int n4 = K >> 2;
+  float4* xs4 = reinterpret_cast<float4*>(xs);
+  float4* gs4 = reinterpret_cast<float4*>(gs);
   float ss = 0.f;
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
-    float v = __ldcg(x + k);
-    xs[k] = v;
-    ss = fmaf(v, v, ss);
+  for (int base = threadIdx.x; base < n4; base += PRO_BATCH * blockDim.x) {
+    float4 v[PRO_BATCH], g[PRO_BATCH];
+#pragma unroll
+    for (int i = 0; i < PRO_BATCH; ++i) {
+      const int j = base + i * blockDim.x;
+      v[i] = j < n4 ? __ldcg(reinterpret_cast<const float4*>(x) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      g[i] = j < n4 ? load_gain4(gain, j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < PRO_BATCH; ++i) {
+      const int j = base + i * blockDim.x;
+      if (j < n4) {
+        xs4[j] = v[i];
+        gs4[j] = g[i];
+        ss = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, fmaf(v[i].w, v[i].w, ss))));
+      }
+    }
   }
   ss = block_sum(ss, scratch);
   const float inv = rsqrtf(ss / (float)K + eps);
-  for (int k = threadIdx.x; k < K; k += blockDim.x) xs[k] = xs[k] * inv * to_f32(gain[k]);
+  for (int j = threadIdx.x; j < n4; j += blockDim.x) {
+    float4 v = xs4[j];
+    const float4 g = gs4[j];
+    v.x = v.x * inv * g.x;
+    v.y = v.y * inv * g.y;
+    v.z = v.z * inv * g.z;
+    v.w = v.w * inv * g.w;
+    xs4[j] = v;
+  }
 }
 
 __device__ __forceinline__ void prologue_copy(float* xs, const float* x, int K) {
-  for (int k = threadIdx.x; k < K; k += blockDim.x) xs[k] = __ldcg(x + k);
+  const int n4 = K >> 2;
+  float4* xs4 = reinterpret_cast<float4*>(xs);
+  for (int base = threadIdx.x; base < n4; base += PRO_BATCH * blockDim.x) {
+    float4 v[PRO_BATCH];
+#pragma unroll
+    for (int i = 0; i < PRO_BATCH; ++i) {
+      const int j = base + i * blockDim.x;
+      v[i] = j < n4 ? __ldcg(reinterpret_cast<const float4*>(x) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < PRO_BATCH; ++i) {
+      const int j = base + i * blockDim.x;
+      if (j < n4) xs4[j] = v[i];
+    }
+  }
 }
 
 // ---- GEMV ops ----------------------------------------------------------------------------
@@ -60,8 +111,8 @@ struct OpQKV {
   KV *kc, *vc;  // [nkv][cap][hd] of this layer and sequence
   int pos;
 
-  __device__ void prologue(float* xs, float* scratch) {
-    prologue_norm(xs, scratch, x, gain, K, eps);
+  __device__ void prologue(float* xs, float* gs, float* scratch) {
+    prologue_norm(xs, gs, scratch, x, gain, K, eps);
     pos = __ldcg(d_pos);
   }
   __device__ const T* row(int item, int r) const {
@@ -115,7 +166,7 @@ struct OpGateUp {
   const float* x;
   float eps;
   float* act;
-  __device__ void prologue(float* xs, float* scratch) { prologue_norm(xs, scratch, x, gain, K, eps); }
+  __device__ void prologue(float* xs, float* gs, float* scratch) { prologue_norm(xs, gs, scratch, x, gain, K, eps); }
   __device__ const T* row(int item, int r) const {
     return (r == 0 ? wg : wu) + (size_t)item * K;
   }
@@ -132,7 +183,7 @@ struct OpResid {
   const T* W;
   const float* in;
   float* y;
-  __device__ void prologue(float* xs, float*) { prologue_copy(xs, in, K); }
+  __device__ void prologue(float* xs, float*, float*) { prologue_copy(xs, in, K); }
   __device__ const T* row(int item, int r) const {
     const int rr = 2 * item + r;
     return rr < N ? W + (size_t)rr * K : nullptr;
@@ -157,8 +208,8 @@ struct OpLMHead {
   float best_v;
   int best_i;
   bool nonfinite;
-  __device__ void prologue(float* xs, float* scratch) {
-    prologue_norm(xs, scratch, x, gain, K, eps);
+  __device__ void prologue(float* xs, float* gs, float* scratch) {
+    prologue_norm(xs, gs, scratch, x, gain, K, eps);
     best_v = -INFINITY;
     best_i = -1;
     nonfinite = false;
@@ -257,7 +308,7 @@ gemv_kernel(const Op op_in, int KS) {
   int base = blockIdx.x * RG;
   if (base + rg < op.n_items) load(base + rg);  // weights do not depend on upstream kernels
   pdl_wait();
-  op.prologue(smem, scratch);
+  op.prologue(smem, smem + op.K, scratch);
   __syncthreads();
   pdl_trigger();
 
@@ -303,6 +354,9 @@ gemv_kernel(const Op op_in, int KS) {
   op.finish(smem);
 }
 
+// dynamic shared memory of a GEMV: the input vector and (norm prologues) the gains
+static size_t gemv_smem_bytes(int K) { return (size_t)2 * K * sizeof(float); }
+
 // ---- launch helpers ------------------------------------------------------------------
 
 template <typename... KArgs, typename... Args>
@@ -321,31 +375,54 @@ static cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
 }
 
-// Choose the K split and the register tile (vectors per lane) of a GEMV.
+// Choose the K split and the register tile (vectors per lane) of a GEMV, and a grid that
+// is resident at once (each warp then loops over its items).
 struct GemvPlan {
   int KS, MAXV, grid;
 };
-static GemvPlan plan_gemv(int K, int vec, int n_items, int nsm) {
-  const int nvec = K / vec;
-  int KS = 1;
-  while (KS < GEMV_WARPS && (((nvec + KS - 1) / KS) + 31) / 32 > 8) KS *= 2;
-  // spread small matrices over all SMs
-  while (KS < GEMV_WARPS && (n_items + GEMV_WARPS / KS - 1) / (GEMV_WARPS / KS) < 2 * nsm) KS *= 2;
+static int maxv_for(int nvec, int KS) {
   const int need = (((nvec + KS - 1) / KS) + 31) / 32;
-  int MAXV = need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 6 ? 6 : 8;
+  return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 6 ? 6 : need <= 8 ? 8 : 99;
+}
+
+template <typename T, class Op>
+static void* gemv_fn(int maxv) {
+  switch (maxv) {
+    case 1: return (void*)gemv_kernel<T, 1, Op>;
+    case 2: return (void*)gemv_kernel<T, 2, Op>;
+    case 4: return (void*)gemv_kernel<T, 4, Op>;
+    case 6: return (void*)gemv_kernel<T, 6, Op>;
+    default: return (void*)gemv_kernel<T, 8, Op>;
+  }
+}
+
+template <typename T, class Op>
+static GemvPlan plan_gemv(int K, int n_items, int nsm) {
+  const int nvec = K / Vec<T>::N;
+  const size_t smem = gemv_smem_bytes(K);
+  int KS = 1;
+  while (KS < GEMV_WARPS && maxv_for(nvec, KS) > 8) KS *= 2;
+  auto resident = [&](int ks) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_fn<T, Op>(maxv_for(nvec, ks)),
+                                                  GEMV_WARPS * 32, smem);
+    return (per_sm < 1 ? 1 : per_sm) * nsm;
+  };
+  // split K further while there are too few items to give every resident CTA one
+  while (KS < GEMV_WARPS && (n_items + GEMV_WARPS / KS - 1) / (GEMV_WARPS / KS) < resident(KS)) KS *= 2;
   const int RG = GEMV_WARPS / KS;
   int grid = (n_items + RG - 1) / RG;
-  const int cap = nsm * 8;
+  const int cap = resident(KS);
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  return {KS, MAXV, grid};
+  return {KS, maxv_for(nvec, KS), grid};
 }
 
 template <typename T, class Op>
 static cudaError_t run_gemv(const Op& op, int nsm, cudaStream_t s, bool pdl) {
-  const GemvPlan p = plan_gemv(op.K, Vec<T>::N, op.n_items, nsm);
+  const GemvPlan p = plan_gemv<T, Op>(op.K, op.n_items, nsm);
   if (p.MAXV > 8) return cudaErrorInvalidValue;
-  const size_t smem = (size_t)op.K * sizeof(float);
+  const size_t smem = gemv_smem_bytes(op.K);
   const dim3 g(p.grid), b(GEMV_WARPS * 32);
   switch (p.MAXV) {
     case 1: return launch_k(gemv_kernel<T, 1, Op>, g, b, smem, s, pdl, op, p.KS);
@@ -358,7 +435,7 @@ static cudaError_t run_gemv(const Op& op, int nsm, cudaStream_t s, bool pdl) {
 
 template <typename T, class Op>
 static cudaError_t set_gemv_smem(int K) {
-  const int bytes = K * (int)sizeof(float);
+  const int bytes = (int)gemv_smem_bytes(K);
   if (bytes <= 48 * 1024) return cudaSuccess;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(gemv_kernel<T, 1, Op>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
@@ -372,14 +449,27 @@ static cudaError_t set_gemv_smem(int K) {
 
 template <typename T>
 __global__ void embed_kernel(const T* E, int V, int H, const int* tok, float* x, int* err) {
+  constexpr int VN = Vec<T>::N;
   pdl_wait();
   int t = __ldcg(tok);
   if (t < 0 || t >= V) {
     if (threadIdx.x == 0) atomicOr(err, ERR_TOKEN);
     t = 0;
   }
-  const T* row = E + (size_t)t * H;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) x[k] = to_f32(row[k]);
+  const uint4* row = reinterpret_cast<const uint4*>(E + (size_t)t * H);
+  for (int v = threadIdx.x; v < H / VN; v += blockDim.x) {
+    const uint4 w = __ldg(row + v);
+    float f[8];
+    if (VN == 8) {
+      f[0] = bf_lo(w.x); f[1] = bf_hi(w.x); f[2] = bf_lo(w.y); f[3] = bf_hi(w.y);
+      f[4] = bf_lo(w.z); f[5] = bf_hi(w.z); f[6] = bf_lo(w.w); f[7] = bf_hi(w.w);
+    } else {
+      f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
+      f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+    }
+#pragma unroll
+    for (int e = 0; e < VN; ++e) x[v * VN + e] = f[e];
+  }
   pdl_trigger();
 }
 
@@ -397,12 +487,17 @@ struct AttnArgs {
   unsigned int* counter;  // [nkv]
 };
 
-// One CTA per (KV head, context chunk). The CTA scores its chunk for all query heads of
-// the KV head, keeps (max, sum of exp, unnormalised output) per head, and the last CTA of
-// the KV head to finish merges the chunks in chunk order (deterministic).
-template <typename T>
-__global__ void __launch_bounds__(128) attn_decode_kernel(const AttnArgs<T> a) {
-  extern __shared__ float sm[];
+// One CTA per (KV head, context chunk). The CTA copies q of its g query heads and the K and
+// V rows of its chunk into shared memory with one batch of 16-byte loads, scores the chunk
+// for all g heads (each K row read once for g heads), and keeps (max, sum of exp,
+// unnormalised output) per head. The last CTA of the KV head to finish merges the chunks
+// in chunk order (deterministic log-sum-exp combine).
+constexpr int ATTN_THREADS = 256;
+constexpr int COPY_BATCH = 8;
+
+template <typename KV>
+__global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArgs<KV> a) {
+  extern __shared__ __align__(16) float sm[];
   __shared__ bool s_last;
   const int g = blockIdx.x, split = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -414,19 +509,51 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const AttnArgs<T> a) {
   const int nsplit = (ctx + chunk - 1) / chunk;
   if (split >= nsplit) return;
   const int j0 = split * chunk, j1 = min(ctx, j0 + chunk), n = j1 - j0;
-  float* qs = sm;                 // [G][hd]
-  float* sc = sm + G * hd;        // [G][chunk]
-  float* st = sc + G * chunk;     // [G][2]
-  for (int i = tid; i < G * hd; i += blockDim.x) qs[i] = __ldcg(a.q + (size_t)g * G * hd + i) * a.scale;
+  // shared layout: q [G][hd] f32 | scores [G][chunk] f32 | stats [G][2] | weights [G][nsplit_max]
+  //                | K [chunk][hd] KV | V [chunk][hd] KV
+  float* qs = sm;
+  float* sc = qs + G * hd;
+  float* st = sc + G * chunk;
+  float* wts = st + 2 * G;
+  const int kv_off = (G * hd + G * chunk + 2 * G + G * a.nsplit_max + 3) & ~3;  // 16-byte aligned
+  KV* ks = reinterpret_cast<KV*>(sm + kv_off);
+  KV* vs = ks + (size_t)chunk * hd;
+  {
+    const int qv = G * hd / 4;                               // 16-byte vectors of q
+    const int kvv = n * hd * (int)sizeof(KV) / 16;           // of the K (and the V) rows
+    const int total = qv + 2 * kvv;
+    const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (size_t)g * G * hd);
+    const uint4* ksrc = reinterpret_cast<const uint4*>(a.k + ((size_t)g * a.stride + j0) * hd);
+    const uint4* vsrc = reinterpret_cast<const uint4*>(a.v + ((size_t)g * a.stride + j0) * hd);
+    uint4* qdst = reinterpret_cast<uint4*>(qs);
+    uint4* kdst = reinterpret_cast<uint4*>(ks);
+    uint4* vdst = reinterpret_cast<uint4*>(vs);
+    for (int base = tid; base < total; base += COPY_BATCH * blockDim.x) {
+      uint4 r[COPY_BATCH];
+#pragma unroll
+      for (int i = 0; i < COPY_BATCH; ++i) {
+        const int j = base + i * blockDim.x;
+        if (j < qv) r[i] = __ldcg(qsrc + j);
+        else if (j < qv + kvv) r[i] = __ldcg(ksrc + (j - qv));
+        else if (j < total) r[i] = __ldcg(vsrc + (j - qv - kvv));
+      }
+#pragma unroll
+      for (int i = 0; i < COPY_BATCH; ++i) {
+        const int j = base + i * blockDim.x;
+        if (j < qv) qdst[j] = r[i];
+        else if (j < qv + kvv) kdst[j - qv] = r[i];
+        else if (j < total) vdst[j - qv - kvv] = r[i];
+      }
+    }
+  }
   __syncthreads();
-  const T* K = a.k + (size_t)g * a.stride * hd;
-  const T* V = a.v + (size_t)g * a.stride * hd;
-  for (int j = j0 + warp; j < j1; j += nwarps) {
+  // scores: a warp per position, lanes over the head dimension
+  for (int jj = warp; jj < n; jj += nwarps) {
     float part[GMAX];
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) part[h] = 0.f;
     for (int dd = lane; dd < hd; dd += 32) {
-      const float kv = to_f32(K[(size_t)j * hd + dd]);
+      const float kv = to_f32(ks[jj * hd + dd]);
 #pragma unroll
       for (int h = 0; h < GMAX; ++h)
         if (h < G) part[h] = fmaf(qs[h * hd + dd], kv, part[h]);
@@ -434,8 +561,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const AttnArgs<T> a) {
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) {
       if (h < G) {
-        const float s = warp_sum(part[h]);
-        if (lane == 0) sc[h * chunk + (j - j0)] = s;
+        const float sv = warp_sum(part[h]);
+        if (lane == 0) sc[h * chunk + jj] = sv * a.scale;
       }
     }
   }
@@ -458,19 +585,11 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const AttnArgs<T> a) {
   }
   __syncthreads();
   const int pstride = hd + 2;
-  for (int dd = tid; dd < hd; dd += blockDim.x) {
-    float acc[GMAX];
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h) acc[h] = 0.f;
-    for (int jj = 0; jj < n; ++jj) {
-      const float vv = to_f32(V[(size_t)(j0 + jj) * hd + dd]);
-#pragma unroll
-      for (int h = 0; h < GMAX; ++h)
-        if (h < G) acc[h] = fmaf(sc[h * chunk + jj], vv, acc[h]);
-    }
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h)
-      if (h < G) a.part[((size_t)(g * G + h) * a.nsplit_max + split) * pstride + dd] = acc[h];
+  for (int idx = tid; idx < G * hd; idx += blockDim.x) {
+    const int h = idx / hd, dd = idx - h * hd;
+    float acc = 0.f;
+    for (int jj = 0; jj < n; ++jj) acc = fmaf(sc[h * chunk + jj], to_f32(vs[jj * hd + dd]), acc);
+    a.part[((size_t)(g * G + h) * a.nsplit_max + split) * pstride + dd] = acc;
   }
   if (tid < G) {
     float* p = a.part + ((size_t)(g * G + tid) * a.nsplit_max + split) * pstride;
@@ -483,18 +602,58 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const AttnArgs<T> a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int idx = tid; idx < G * hd; idx += blockDim.x) {
-    const int h = idx / hd, dd = idx - h * hd;
-    const float* p = a.part + (size_t)(g * G + h) * a.nsplit_max * pstride;
+  // merge: weights w_s = exp(m_s - M) / sum_s l_s exp(m_s - M) per head, then out = sum_s w_s O_s
+  for (int i = tid; i < G * nsplit; i += blockDim.x) {
+    const int h = i / nsplit, sp = i - h * nsplit;
+    const float* p = a.part + ((size_t)(g * G + h) * a.nsplit_max + sp) * pstride + hd;
+    wts[h * a.nsplit_max + sp] = __ldcg(p);  // m_s
+  }
+  __syncthreads();
+  for (int h = warp; h < G; h += nwarps) {
     float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(p + s * pstride + hd));
-    float L = 0.f, o = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float w = expf(__ldcg(p + s * pstride + hd) - M);
-      L = fmaf(__ldcg(p + s * pstride + hd + 1), w, L);
-      o = fmaf(__ldcg(p + s * pstride + dd), w, o);
+    for (int sp = lane; sp < nsplit; sp += 32) M = fmaxf(M, wts[h * a.nsplit_max + sp]);
+    M = warp_max(M);
+    float L = 0.f;
+    for (int sp = lane; sp < nsplit; sp += 32) {
+      const float* p = a.part + ((size_t)(g * G + h) * a.nsplit_max + sp) * pstride + hd;
+      const float w = expf(wts[h * a.nsplit_max + sp] - M);
+      wts[h * a.nsplit_max + sp] = w;
+      L = fmaf(__ldcg(p + 1), w, L);
     }
-    a.out[(size_t)(g * G + h) * hd + dd] = o / L;
+    L = warp_sum(L);
+    const float inv = 1.f / L;
+    for (int sp = lane; sp < nsplit; sp += 32) wts[h * a.nsplit_max + sp] *= inv;
+  }
+  __syncthreads();
+  constexpr int EPT = GMAX * 128 / ATTN_THREADS;  // output elements per thread (G*hd <= 1024)
+  float acc[EPT];
+#pragma unroll
+  for (int k = 0; k < EPT; ++k) acc[k] = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += 4) {
+    float v[EPT][4];
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const int idx = tid + k * blockDim.x;
+      const int h = idx / hd, dd = idx - h * hd;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v[k][u] = (idx < G * hd && s0 + u < nsplit)
+                      ? __ldcg(a.part + ((size_t)(g * G + h) * a.nsplit_max + s0 + u) * pstride + dd)
+                      : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const int idx = tid + k * blockDim.x;
+      const int h = idx / hd;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (idx < G * hd && s0 + u < nsplit) acc[k] = fmaf(v[k][u], wts[h * a.nsplit_max + s0 + u], acc[k]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < EPT; ++k) {
+    const int idx = tid + k * blockDim.x;
+    if (idx < G * hd) a.out[(size_t)g * G * hd + idx] = acc[k];
   }
   if (tid == 0) a.counter[g] = 0u;
 }
@@ -507,17 +666,27 @@ size_t attn_workspace_bytes(int nq, int nkv, int hd, int nsplit) {
   return part + (size_t)nkv * sizeof(unsigned int);
 }
 
-int attn_nsplit_for(int nsm, int nkv, int cap, int chunk_min) {
-  int by_ctx = (cap + chunk_min - 1) / chunk_min;
-  int by_sm = (2 * nsm + nkv - 1) / nkv;
-  int n = by_ctx < by_sm ? by_ctx : by_sm;
+// Chunks of at least chunk_min positions and at most MAX_SPLITS chunks per KV head (short
+// contexts spread over several CTAs, the merge stays short), unless the K and V rows of a
+// chunk would exceed ~160 KB of shared memory; then the chunk count grows instead.
+constexpr int MAX_SPLITS = 16;
+int attn_nsplit_for(int cap, int chunk_min, int hd, int kv_bytes) {
+  int chunk_max = (160 * 1024) / (2 * hd * kv_bytes);
+  if (chunk_max > 256) chunk_max = 256;
+  if (chunk_max < chunk_min) chunk_max = chunk_min;
+  int n = (cap + chunk_min - 1) / chunk_min;
+  if (n > MAX_SPLITS) n = MAX_SPLITS;
+  const int need = (cap + chunk_max - 1) / chunk_max;
+  if (n < need) n = need;
   return n < 1 ? 1 : n;
 }
 
-size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min) {
+size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min, int kv_bytes) {
   int chunk = (cap + nsplit - 1) / nsplit;
   if (chunk < chunk_min) chunk = chunk_min;
-  return ((size_t)group * hd + (size_t)group * chunk + 2 * group) * sizeof(float);
+  const size_t f = ((size_t)group * hd + (size_t)group * chunk + 2 * group + (size_t)group * nsplit + 3) &
+                   ~(size_t)3;
+  return f * sizeof(float) + 2 * (size_t)chunk * hd * kv_bytes;
 }
 
 cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int chunk_min,
@@ -527,7 +696,7 @@ cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int c
   const int G = nq / nkv;
   if (G > GMAX) return cudaErrorInvalidValue;
   size_t part_bytes = ((size_t)nq * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
-  const dim3 grid(nkv, nsplit), block(128);
+  const dim3 grid(nkv, nsplit), block(ATTN_THREADS);
   if (kv_dtype == 2) {
     AttnArgs<f16> a{q, (const f16*)kc, (const f16*)vc, kv_stride, hd, G, nsplit, chunk_min,
                      ctx_host, d_pos, 1.f / sqrtf((float)hd), out, (float*)ws,

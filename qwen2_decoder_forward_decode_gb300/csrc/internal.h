@@ -47,8 +47,8 @@ void set_error_message(const char* msg);  // message returned by qw_last_error o
 
 // ---- decode.cu ----
 size_t attn_workspace_bytes(int nq, int nkv, int hd, int nsplit);
-int attn_nsplit_for(int nsm, int nkv, int cap, int chunk_min);
-size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min);
+int attn_nsplit_for(int cap, int chunk_min, int hd, int kv_bytes);
+size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min, int kv_bytes);
 cudaError_t decode_set_attributes(const Dims& d);
 cudaError_t attn_set_attributes(size_t smem);  // not during stream capture
 
