@@ -128,17 +128,17 @@ struct qw_model {
       const LayerPtrs& w = layers[l];
       void* kc = kc_layer(s, l);
       void* vc = vc_layer(s, l);
-      if ((e = run(0, l, [&](bool p) { return launch_qkv(d, w, xs, pos + s, rope, q, kc, vc, stream, p); })))
+      if ((e = run(0, l, [&](bool p) { return launch_qkv(d, w, xs, pos + s, rope, q, kc, vc, err, stream, p); })))
         return e;
       if ((e = run(1, l, [&](bool p) {
              return launch_attn(d.dtype == QW_BF16 ? 2 : 0, d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min,
                                 attn_smem, q, kc, vc, d.cap, pos + s, 0, attn, attn_ws, stream, p);
            })))
         return e;
-      if ((e = run(2, l, [&](bool p) { return launch_resid(d, w.wo, d.H, d.nq * d.hd, attn, xs, stream, p); })))
+      if ((e = run(2, l, [&](bool p) { return launch_resid(d, w.wo, d.H, d.nq * d.hd, attn, xs, err, stream, p); })))
         return e;
-      if ((e = run(3, l, [&](bool p) { return launch_gateup(d, w, xs, act, stream, p); }))) return e;
-      if ((e = run(4, l, [&](bool p) { return launch_resid(d, w.w_down, d.H, d.I, act, xs, stream, p); })))
+      if ((e = run(3, l, [&](bool p) { return launch_gateup(d, w, xs, act, err, stream, p); }))) return e;
+      if ((e = run(4, l, [&](bool p) { return launch_resid(d, w.w_down, d.H, d.I, act, xs, err, stream, p); })))
         return e;
     }
     return run(5, 0, [&](bool p) {

@@ -55,7 +55,7 @@ cudaError_t attn_set_attributes(size_t smem);  // not during stream capture
 cudaError_t launch_embed(const Dims& d, const void* E, const int* tok, float* x, int* err,
                          cudaStream_t s, bool pdl);
 cudaError_t launch_qkv(const Dims& d, const LayerPtrs& w, const float* x, const int* d_pos,
-                       const float2* rope, float* q, void* kc, void* vc, cudaStream_t s,
+                       const float2* rope, float* q, void* kc, void* vc, int* err, cudaStream_t s,
                        bool pdl);
 // ctx = d_pos ? d_pos[0] + 1 : ctx_host
 // kv_dtype: 0 fp32, 2 fp16
@@ -65,8 +65,8 @@ cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int c
                         cudaStream_t s, bool pdl);
 // y[r] += W[r,:] . in  (r < N), W [N, K]
 cudaError_t launch_resid(const Dims& d, const void* W, int N, int K, const float* in, float* y,
-                         cudaStream_t s, bool pdl);
-cudaError_t launch_gateup(const Dims& d, const LayerPtrs& w, const float* x, float* act,
+                         int* err, cudaStream_t s, bool pdl);
+cudaError_t launch_gateup(const Dims& d, const LayerPtrs& w, const float* x, float* act, int* err,
                           cudaStream_t s, bool pdl);
 cudaError_t launch_lmhead(const Dims& d, const void* W, const void* final_norm, const float* x,
                           float* logits, const Finalize& f, cudaStream_t s, bool pdl);
