@@ -9,12 +9,8 @@
 //   gateup : RMSNorm(x) -> gate/up projections -> SwiGLU
 // then the LM head: final RMSNorm -> logits = E . h -> greedy argmax.
 //
-// Every projection is a GEMV whose weight rows stream once from HBM. Each CTA (one per SM)
-// owns a strided set of tiles of consecutive rows and pulls them through a ring of shared-
-// memory stages with 1-D bulk copies (TMA); warps multiply rows from shared memory with the
-// input vector held in registers. The first ring-full of copies is issued before
-// griddepcontrol.wait and each CTA stays under half an SM, so under programmatic dependent
-// launch kernel n+1 is resident and streaming its weights while kernel n finishes.
+// Every projection is a GEMV whose weight rows stream once from HBM through per-warp rings
+// of shared-memory slots filled by 1-D bulk copies (TMA); see the GEMV kernel below.
 #include "common.cuh"
 #include "internal.h"
 
@@ -98,9 +94,8 @@ __device__ __forceinline__ void prologue_copy(float* xs, const float* x, int K) 
 
 // ---- GEMV ops ----------------------------------------------------------------------------
 //
-// An op names its rows as tiles of IPT items. PAIRED ops take item j's two rows from two
-// row segments (the RoPE pair (i, i + hd/2) of a head; gate row i and up row i); the
-// others take RPI consecutive rows per item from one segment.
+// An item is RPI weight rows that one warp (or KS warps, splitting K) reduces together:
+// the RoPE pair (i, i + hd/2) of a head, gate row i with up row i, or consecutive rows.
 
 // q/k/v rows in RoPE pairs (i, i + hd/2) of one head; items run over q heads, k heads,
 // v heads, hd/2 pairs each. T: weight type, KV: cache element type.
@@ -122,18 +117,17 @@ struct OpQKV {
     prologue_norm(xs, gs, scratch, x, gain, K, eps);
     pos = __ldcg(d_pos);
   }
-  // first row of segment seg (0: i, 1: i + hd/2) for the tile starting at item0
-  __device__ const T* seg_ptr(int item0, int seg) const {
+  // row r (0: i, 1: i + hd/2) of item (head, i)
+  __device__ const T* row(int item, int r) const {
     const int half = hd >> 1;
-    int head = item0 / half;
-    const int rr = item0 - head * half + seg * half;
+    int head = item / half;
+    const int rr = item - head * half + r * half;
     if (head < nq) return wq + (size_t)(head * hd + rr) * K;
     head -= nq;
     if (head < nkv) return wk + (size_t)(head * hd + rr) * K;
     head -= nkv;
     return wv + (size_t)(head * hd + rr) * K;
   }
-  __device__ int seg_rows(int, int nit, int) const { return nit; }
   __device__ const float* xin() const { return x; }
   __device__ void epilogue(int item, float a, float b) {
     const int half = hd >> 1;
@@ -179,8 +173,7 @@ struct OpGateUp {
   float eps;
   float* act;
   __device__ void prologue(float* xs, float* gs, float* scratch) { prologue_norm(xs, gs, scratch, x, gain, K, eps); }
-  __device__ const T* seg_ptr(int item0, int seg) const { return (seg == 0 ? wg : wu) + (size_t)item0 * K; }
-  __device__ int seg_rows(int, int nit, int) const { return nit; }
+  __device__ const T* row(int item, int r) const { return (r == 0 ? wg : wu) + (size_t)item * K; }
   __device__ const float* xin() const { return x; }
   __device__ void epilogue(int item, float g, float u) { act[item] = (g / (1.f + expf(-g))) * u; }
   __device__ void finish() {}
@@ -196,8 +189,10 @@ struct OpResid {
   const float* in;
   float* y;
   __device__ void prologue(float* xs, float*, float*) { prologue_copy(xs, in, K); }
-  __device__ const T* seg_ptr(int item0, int) const { return W + (size_t)item0 * RPI * K; }
-  __device__ int seg_rows(int item0, int nit, int) const { return min(RPI * nit, N - RPI * item0); }
+  __device__ const T* row(int item, int r) const {
+    const int rr = RPI * item + r;
+    return rr < N ? W + (size_t)rr * K : nullptr;
+  }
   __device__ const float* xin() const { return in; }
   __device__ void epilogue(int item, float a, float b) {
     const int r0 = RPI * item;
@@ -227,8 +222,10 @@ struct OpLMHead {
     best_i = -1;
     nonfinite = false;
   }
-  __device__ const T* seg_ptr(int item0, int) const { return W + (size_t)item0 * 2 * K; }
-  __device__ int seg_rows(int item0, int nit, int) const { return min(2 * nit, N - 2 * item0); }
+  __device__ const T* row(int item, int r) const {
+    const int rr = 2 * item + r;
+    return rr < N ? W + (size_t)rr * K : nullptr;
+  }
   __device__ const float* xin() const { return x; }
   __device__ void take(int r, float v) {
     logits[r] = v;
@@ -283,64 +280,66 @@ struct OpLMHead {
 
 // ---- the GEMV kernel ---------------------------------------------------------------------
 //
-// KS warps share an item (its two rows, or one) and split K into contiguous segments; the
-// CTA's 8 warps cover IPT = 8/KS items per tile. A tile's rows land in one stage of a
-// shared-memory ring by bulk copy (one copy per row segment) and an mbarrier counts their
-// bytes. Lane l of a warp reads 16-byte vectors l, l+32, ... of its segment, and the input
-// vector slice it needs never changes and lives in registers. Partial sums over segments
-// meet in shared memory in a fixed order (deterministic).
+// Each warp runs its own pipeline: it owns NS slots of shared memory and NS mbarriers, and
+// lane 0 bulk-copies (TMA, 1-D) the rows of its next items into free slots while the warp
+// multiplies earlier ones with the input-vector slice held in registers. Warps never wait
+// for each other in the main loop (KS > 1 warps sharing an item meet at a named barrier).
+// The first NS items are requested before griddepcontrol.wait, and a CTA stays under half
+// an SM, so under programmatic dependent launch the next kernel's weights are in flight
+// while this one finishes. Partial sums over K segments add in a fixed order.
 struct GemvCfg {
-  int KS, IPT, n_tiles, stages, stage_bytes, seg1_off, x_direct;
+  int KS, NS, slot_bytes, x_direct;
   int* err;
 };
-constexpr int MAX_STAGES = 8;
+constexpr int MAX_SLOTS = 8;
 
 template <typename T, int MAXV, class Op>
 __global__ void __launch_bounds__(GEMV_WARPS * 32, 2)
 gemv_kernel(const Op op_in, const GemvCfg c) {
   Op op = op_in;
   extern __shared__ __align__(128) unsigned char dsm[];
-  __shared__ __align__(8) unsigned long long full[MAX_STAGES];
+  __shared__ __align__(8) unsigned long long bars[GEMV_WARPS][MAX_SLOTS];
   __shared__ float scratch[32];
   __shared__ float red[GEMV_WARPS][2];
+  __shared__ volatile int s_abort[GEMV_WARPS];
   constexpr int VN = Vec<T>::N;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int KS = c.KS, IPT = c.IPT;
+  const int KS = c.KS, NS = c.NS, RG = GEMV_WARPS / KS;
   const int rg = warp / KS, ks = warp - rg * KS;
   const int nvec = op.K / VN;
   const int seg = (nvec + KS - 1) / KS;
   const int v0 = ks * seg, v1 = min(nvec, v0 + seg);
-  const int my_tiles = (int)blockIdx.x < c.n_tiles ? (c.n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  const uint32_t row_bytes = (uint32_t)op.K * sizeof(T);
-  const uint32_t ring = smem_addr(dsm);
-  const uint32_t bar0 = smem_addr(full);
-  float* xs = reinterpret_cast<float*>(dsm + (size_t)c.stages * c.stage_bytes);
+  const uint32_t seg_bytes = (uint32_t)(v1 > v0 ? v1 - v0 : 0) * 16u;
+  // items of this warp: first + k * step
+  const int first = (int)blockIdx.x * RG + rg, step = (int)gridDim.x * RG;
+  const int my_items = first < op.n_items ? (op.n_items - 1 - first) / step + 1 : 0;
+  unsigned char* wslots = dsm + (size_t)warp * NS * c.slot_bytes;
+  const uint32_t wslot0 = smem_addr(wslots);
+  const uint32_t bar0 = smem_addr(&bars[warp][0]);
+  float* xs = reinterpret_cast<float*>(dsm + (size_t)GEMV_WARPS * NS * c.slot_bytes);
 
-  auto issue = [&](int i) {  // one thread: bulk-copy tile i of this CTA into stage i % stages
-    const int s = i % c.stages;
-    const int item0 = ((int)blockIdx.x + i * (int)gridDim.x) * IPT;
-    const int nit = min(IPT, op.n_items - item0);
-    const int nseg = Op::PAIRED ? 2 : 1;
-    uint32_t total = 0;
-    for (int g = 0; g < nseg; ++g) total += (uint32_t)op.seg_rows(item0, nit, g) * row_bytes;
-    mbar_expect_tx(bar0 + 8 * s, total);
-    for (int g = 0; g < nseg; ++g) {
-      const uint32_t bytes = (uint32_t)op.seg_rows(item0, nit, g) * row_bytes;
-      if (bytes) bulk_copy_g2s(ring + s * c.stage_bytes + g * c.seg1_off, op.seg_ptr(item0, g), bytes, bar0 + 8 * s);
+  auto issue = [&](int k) {  // lane 0: copy this warp's K segment of item k's rows
+    const int slot = k % NS;
+    const int item = first + k * step;
+    const T* r0 = op.row(item, 0);
+    const T* r1 = Op::RPI == 2 ? op.row(item, 1) : nullptr;
+    const uint32_t bar = bar0 + 8 * slot;
+    mbar_expect_tx(bar, seg_bytes * (r1 ? 2u : 1u));
+    const uint32_t dst = wslot0 + slot * c.slot_bytes;
+    if (seg_bytes) {
+      bulk_copy_g2s(dst, reinterpret_cast<const unsigned char*>(r0) + (size_t)v0 * 16, seg_bytes, bar);
+      if (r1) bulk_copy_g2s(dst + seg_bytes, reinterpret_cast<const unsigned char*>(r1) + (size_t)v0 * 16, seg_bytes, bar);
     }
   };
 
-  if (tid == 0) {
-    for (int s = 0; s < c.stages; ++s) mbar_init(bar0 + 8 * s, 1);
+  if (lane == 0) {
+    s_abort[warp] = 0;
+    for (int sl = 0; sl < NS; ++sl) mbar_init(bar0 + 8 * sl, 1);
     mbar_fence_init();
+    const int n0 = min(NS, my_items);  // weights do not depend on upstream kernels
+    for (int k = 0; k < n0; ++k) issue(k);
   }
-  __syncthreads();
-  int issued = 0;
-  if (tid == 0) {  // weights do not depend on upstream kernels: start streaming now
-    const int n0 = min(c.stages, my_tiles);
-    for (int i = 0; i < n0; ++i) issue(i);
-    issued = n0;
-  }
+  __syncwarp();
   pdl_wait();
   if (!c.x_direct) op.prologue(xs, xs + op.K, scratch);
   __syncthreads();
@@ -363,73 +362,67 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
     }
   }
 
-  int consumed = 0;
-  bool aborted = false;
-  for (int i = 0; i < my_tiles; ++i) {
-    const int s = i % c.stages;
-    const bool ok = mbar_wait_bounded(bar0 + 8 * s, (uint32_t)((i / c.stages) & 1));
-    if (__syncthreads_or(!ok)) { aborted = true; break; }
-    consumed = i + 1;
-    const int item = ((int)blockIdx.x + i * (int)gridDim.x) * IPT + rg;
+  bool timed_out = false;
+  int issued = min(NS, my_items), consumed = 0;
+  for (int k = 0; k < my_items; ++k) {
+    const int slot = k % NS;
+    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * slot, (uint32_t)((k / NS) & 1)));
+    if (KS > 1) {  // the KS warps sharing these items give up together
+      if (!ok && lane == 0) s_abort[rg] = 1;
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KS * 32) : "memory");
+      ok = s_abort[rg] == 0;
+    }
+    if (!ok) { timed_out = true; break; }
+    consumed = k + 1;
+    const int item = first + k * step;
+    const uint4* s0 = reinterpret_cast<const uint4*>(wslots + (size_t)slot * c.slot_bytes);
+    const uint4* s1 = reinterpret_cast<const uint4*>(wslots + (size_t)slot * c.slot_bytes + seg_bytes);
     float a0 = 0.f, a1 = 0.f;
-    if (item < op.n_items) {
-      const unsigned char* st = dsm + (size_t)s * c.stage_bytes;
-      const uint4* r0;
-      const uint4* r1;
-      if (Op::PAIRED) {
-        r0 = reinterpret_cast<const uint4*>(st + (size_t)rg * row_bytes);
-        r1 = reinterpret_cast<const uint4*>(st + c.seg1_off + (size_t)rg * row_bytes);
-      } else {
-        r0 = reinterpret_cast<const uint4*>(st + (size_t)rg * Op::RPI * row_bytes);
-        r1 = reinterpret_cast<const uint4*>(st + ((size_t)rg * Op::RPI + 1) * row_bytes);
-      }
 #pragma unroll
-      for (int q = 0; q < MAXV; ++q) {
-        const int v = v0 + lane + 32 * q;
-        if (v < v1) {
-          a0 = dotv(r0[v], xr[q], a0, T());
-          if (Op::RPI == 2) a1 = dotv(r1[v], xr[q], a1, T());
-        }
+    for (int q = 0; q < MAXV; ++q) {
+      const int v = lane + 32 * q;
+      if (v0 + v < v1) {
+        a0 = dotv(s0[v], xr[q], a0, T());
+        if (Op::RPI == 2) a1 = dotv(s1[v], xr[q], a1, T());
       }
+    }
+    __syncwarp();
+    if (lane == 0 && k + NS < my_items) {  // slot free: request item k + NS
+      fence_proxy_async();
+      issue(k + NS);
+      ++issued;
     }
     a0 = warp_sum(a0);
     if (Op::RPI == 2) a1 = warp_sum(a1);
-    if (KS > 1) {
+    if (KS > 1) {  // the KS warps of this item meet at named barrier 1 + rg
       if (lane == 0) {
         red[warp][0] = a0;
         red[warp][1] = a1;
       }
-      __syncthreads();
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KS * 32) : "memory");
       if (ks == 0 && lane == 0) {
         a0 = 0.f;
         a1 = 0.f;
-        for (int k = 0; k < KS; ++k) {
-          a0 += red[warp + k][0];
-          a1 += red[warp + k][1];
+        for (int j = 0; j < KS; ++j) {
+          a0 += red[warp + j][0];
+          a1 += red[warp + j][1];
         }
       }
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KS * 32) : "memory");
     }
-    if (ks == 0 && lane == 0 && item < op.n_items) op.epilogue(item, a0, a1);
-    __syncthreads();  // stage s (and red) free again
-    if (tid == 0 && i + c.stages < my_tiles) {
-      fence_proxy_async();
-      issue(i + c.stages);
-      ++issued;
-    }
+    if (ks == 0 && lane == 0) op.epilogue(item, a0, a1);
   }
-  if (aborted && tid == 0) {
+  if (timed_out && lane == 0) {
     atomicOr(c.err, ERR_TIMEOUT);
-    for (int j = consumed; j < issued; ++j)  // copies still in flight must land before exit
-      mbar_wait_bounded(bar0 + 8 * (j % c.stages), (uint32_t)((j / c.stages) & 1));
+    for (int j = consumed; j < issued; ++j)  // copies in flight must land before exit
+      mbar_wait_bounded(bar0 + 8 * (j % NS), (uint32_t)((j / NS) & 1));
   }
   op.finish();
 }
 
-// dynamic shared memory: the stage ring and, unless x is read straight into registers, the
-// input vector (and the gains of a norm prologue)
-static constexpr int RING_BUDGET = 96 * 1024;
-static constexpr int SMEM_CAP = 112 * 1024;   // two CTAs (of consecutive kernels) fit an SM
-static constexpr int TILE_TARGET = 24 * 1024;
+// dynamic shared memory: per-warp slot rings and, unless x is read straight into
+// registers, the input vector (and the gains of a norm prologue)
+static constexpr int WARP_BUDGET = 12 * 1024;  // bytes of slots per warp (8 warps: 96 KB)
 static constexpr int X_SMEM_MAX = 16 * 1024;
 
 static int maxv_for(int nvec, int KS) {
@@ -446,39 +439,31 @@ struct GemvPlan {
 template <typename T, class Op>
 static bool plan_gemv(const Op& op, int nsm, int* err, GemvPlan* p) {
   const int nvec = op.K / Vec<T>::N;
-  const size_t row_bytes = (size_t)op.K * sizeof(T);
   const int x_direct = (!Op::NORM && (size_t)op.K * 4 > X_SMEM_MAX) ? 1 : 0;
   const size_t xs = x_direct ? 0 : (size_t)(Op::NORM ? 2 : 1) * op.K * 4;
-  int chosen = -1;
-  for (int KS = 1; KS <= GEMV_WARPS; KS *= 2) {
-    if (maxv_for(nvec, KS) > 8) continue;
-    const int IPT = GEMV_WARPS / KS;
-    const size_t tile = (size_t)IPT * Op::RPI * row_bytes;
-    const int n_tiles = (op.n_items + IPT - 1) / IPT;
-    chosen = KS;
-    if (tile <= TILE_TARGET && n_tiles >= nsm) break;
-  }
-  if (chosen < 0) return false;
-  const int KS = chosen, IPT = GEMV_WARPS / KS;
-  const size_t tile = (size_t)IPT * Op::RPI * row_bytes;
-  const size_t stage_bytes = (tile + 127) & ~(size_t)127;
-  size_t budget = RING_BUDGET;
-  if (budget + xs > SMEM_CAP) budget = SMEM_CAP > xs ? SMEM_CAP - xs : 0;
-  int stages = (int)(budget / stage_bytes);
-  if (stages > MAX_STAGES) stages = MAX_STAGES;
-  if (stages < 2) stages = 2;
-  if (stages * stage_bytes + xs > 220 * 1024) return false;
+  // smallest K split whose slot (RPI row segments) fits the warp budget twice and whose
+  // register tile fits; then split further while too few items exist to fill every warp
+  int KS = 1;
+  auto slot_of = [&](int ks) { return (size_t)Op::RPI * ((nvec + ks - 1) / ks) * 16; };
+  while (KS < GEMV_WARPS && (maxv_for(nvec, KS) > 8 || 2 * slot_of(KS) > WARP_BUDGET)) KS *= 2;
+  if (maxv_for(nvec, KS) > 8) return false;
+  while (KS < GEMV_WARPS && (long long)op.n_items * KS < (long long)nsm * GEMV_WARPS) KS *= 2;
+  const size_t slot = (slot_of(KS) + 127) & ~(size_t)127;
+  int NS = (int)(WARP_BUDGET / slot);
+  if (NS > MAX_SLOTS) NS = MAX_SLOTS;
+  if (NS < 2) NS = 2;
+  const size_t smem = (size_t)GEMV_WARPS * NS * slot + xs;
+  if (smem > 220 * 1024) return false;
+  const int RG = GEMV_WARPS / KS;
   p->c.KS = KS;
-  p->c.IPT = IPT;
-  p->c.n_tiles = (op.n_items + IPT - 1) / IPT;
-  p->c.stages = stages;
-  p->c.stage_bytes = (int)stage_bytes;
-  p->c.seg1_off = (int)((size_t)IPT * row_bytes);
+  p->c.NS = NS;
+  p->c.slot_bytes = (int)slot;
   p->c.x_direct = x_direct;
   p->c.err = err;
   p->maxv = maxv_for(nvec, KS);
-  p->grid = p->c.n_tiles < nsm ? p->c.n_tiles : nsm;
-  p->smem = stages * stage_bytes + xs;
+  const int groups = (op.n_items + RG - 1) / RG;
+  p->grid = groups < nsm ? groups : nsm;
+  p->smem = smem;
   return true;
 }
 
