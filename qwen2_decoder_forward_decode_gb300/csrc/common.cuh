@@ -141,6 +141,11 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
                : "memory");
 }
 
+// Ask L2 to fetch bytes (multiple of 16) at src (16-byte aligned); no completion tracking.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 }  // namespace qw
 
 // ---- host: kernel launch with optional programmatic dependent launch ----------------------

@@ -129,7 +129,12 @@ struct OpQKV {
     return wv + (size_t)(head * hd + rr) * K;
   }
   __device__ const float* xin() const { return x; }
-  __device__ void epilogue(int item, float a, float b) {
+  // bias pair and (cos, sin) of the item, loaded before its weights are waited for
+  struct Epi {
+    float ba, bb;
+    float2 cs;
+  };
+  __device__ Epi epi_load(int item) const {
     const int half = hd >> 1;
     int head = item / half;
     const int i = item - head * half;
@@ -138,12 +143,24 @@ struct OpQKV {
     if (head < nq) { bias = bq; h = head; }
     else if (head < nq + nkv) { bias = bk; h = head - nq; }
     else { bias = bv; h = head - nq - nkv; }
-    if (bias) {
-      a += to_f32(bias[h * hd + i]);
-      b += to_f32(bias[h * hd + i + half]);
-    }
+    Epi e;
+    e.ba = bias ? to_f32(bias[h * hd + i]) : 0.f;
+    e.bb = bias ? to_f32(bias[h * hd + i + half]) : 0.f;
+    e.cs = head < nq + nkv ? rope[(size_t)pos * half + i] : make_float2(1.f, 0.f);
+    return e;
+  }
+  __device__ void epilogue(int item, float a, float b, const Epi& e) {
+    const int half = hd >> 1;
+    int head = item / half;
+    const int i = item - head * half;
+    int h;
+    if (head < nq) h = head;
+    else if (head < nq + nkv) h = head - nq;
+    else h = head - nq - nkv;
+    a += e.ba;
+    b += e.bb;
     if (head < nq + nkv) {  // rotate (split-half RoPE): pair (i, i + hd/2)
-      const float2 cs = rope[(size_t)pos * half + i];
+      const float2 cs = e.cs;
       const float ra = a * cs.x - b * cs.y;
       const float rb = b * cs.x + a * cs.y;
       a = ra;
@@ -175,7 +192,9 @@ struct OpGateUp {
   __device__ void prologue(float* xs, float* gs, float* scratch) { prologue_norm(xs, gs, scratch, x, gain, K, eps); }
   __device__ const T* row(int item, int r) const { return (r == 0 ? wg : wu) + (size_t)item * K; }
   __device__ const float* xin() const { return x; }
-  __device__ void epilogue(int item, float g, float u) { act[item] = (g / (1.f + expf(-g))) * u; }
+  struct Epi {};
+  __device__ Epi epi_load(int) const { return Epi{}; }
+  __device__ void epilogue(int item, float g, float u, const Epi&) { act[item] = (g / (1.f + expf(-g))) * u; }
   __device__ void finish() {}
 };
 
@@ -194,10 +213,14 @@ struct OpResid {
     return rr < N ? W + (size_t)rr * K : nullptr;
   }
   __device__ const float* xin() const { return in; }
-  __device__ void epilogue(int item, float a, float b) {
+  struct Epi {};
+  __device__ Epi epi_load(int) const { return Epi{}; }
+  // y += a as one reduction without a return value (each row has exactly one writer, so
+  // the sum is the same single rounding as a load-add-store, without the load latency)
+  __device__ void epilogue(int item, float a, float b, const Epi&) {
     const int r0 = RPI * item;
-    y[r0] = __ldcg(y + r0) + a;
-    if (RPI == 2 && r0 + 1 < N) y[r0 + 1] = __ldcg(y + r0 + 1) + b;
+    atomicAdd(y + r0, a);
+    if (RPI == 2 && r0 + 1 < N) atomicAdd(y + r0 + 1, b);
   }
   __device__ void finish() {}
 };
@@ -232,7 +255,9 @@ struct OpLMHead {
     if (!isfinite(v)) nonfinite = true;
     if (v > best_v || best_i < 0) { best_v = v; best_i = r; }  // a thread sees rows in increasing order
   }
-  __device__ void epilogue(int item, float a, float b) {
+  struct Epi {};
+  __device__ Epi epi_load(int) const { return Epi{}; }
+  __device__ void epilogue(int item, float a, float b, const Epi&) {
     take(2 * item, a);
     if (2 * item + 1 < N) take(2 * item + 1, b);
   }
@@ -292,6 +317,7 @@ struct GemvCfg {
   int* err;
 };
 constexpr int MAX_SLOTS = 8;
+constexpr int PF_DIST = 8;  // items per warp requested into L2 beyond the shared-memory slots
 
 template <typename T, int MAXV, class Op>
 __global__ void __launch_bounds__(GEMV_WARPS * 32, 2)
@@ -318,6 +344,15 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
   const uint32_t bar0 = smem_addr(&bars[warp][0]);
   float* xs = reinterpret_cast<float*>(dsm + (size_t)GEMV_WARPS * NS * c.slot_bytes);
 
+  auto prefetch = [&](int k) {  // lane 0: ask L2 for item k's row segments ahead of use
+    const int item = first + k * step;
+    const T* r0 = op.row(item, 0);
+    const T* r1 = Op::RPI == 2 ? op.row(item, 1) : nullptr;
+    if (seg_bytes) {
+      prefetch_l2_bulk(reinterpret_cast<const unsigned char*>(r0) + (size_t)v0 * 16, seg_bytes);
+      if (r1) prefetch_l2_bulk(reinterpret_cast<const unsigned char*>(r1) + (size_t)v0 * 16, seg_bytes);
+    }
+  };
   auto issue = [&](int k) {  // lane 0: copy this warp's K segment of item k's rows
     const int slot = k % NS;
     const int item = first + k * step;
@@ -338,12 +373,13 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
     mbar_fence_init();
     const int n0 = min(NS, my_items);  // weights do not depend on upstream kernels
     for (int k = 0; k < n0; ++k) issue(k);
+    for (int k = n0; k < min(NS + PF_DIST, my_items); ++k) prefetch(k);
   }
   __syncwarp();
+  pdl_trigger();  // the next kernel may become resident and start its own weight stream
   pdl_wait();
   if (!c.x_direct) op.prologue(xs, xs + op.K, scratch);
   __syncthreads();
-  pdl_trigger();
 
   float xr[MAXV][VN];
 #pragma unroll
@@ -375,6 +411,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
     if (!ok) { timed_out = true; break; }
     consumed = k + 1;
     const int item = first + k * step;
+    const typename Op::Epi epi = op.epi_load(item);
     const uint4* s0 = reinterpret_cast<const uint4*>(wslots + (size_t)slot * c.slot_bytes);
     const uint4* s1 = reinterpret_cast<const uint4*>(wslots + (size_t)slot * c.slot_bytes + seg_bytes);
     float a0 = 0.f, a1 = 0.f;
@@ -391,6 +428,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
       fence_proxy_async();
       issue(k + NS);
       ++issued;
+      if (k + NS + PF_DIST < my_items) prefetch(k + NS + PF_DIST);
     }
     a0 = warp_sum(a0);
     if (Op::RPI == 2) a1 = warp_sum(a1);
@@ -410,7 +448,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
       }
       asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KS * 32) : "memory");
     }
-    if (ks == 0 && lane == 0) op.epilogue(item, a0, a1);
+    if (ks == 0 && lane == 0) op.epilogue(item, a0, a1, epi);
   }
   if (timed_out && lane == 0) {
     atomicOr(c.err, ERR_TIMEOUT);
