@@ -268,6 +268,33 @@ def run_native(args):
     src = source_hash()
     traffic = recorded_traffic("gateup_gemv", src)
 
+    if args.timeline:
+        # device timeline of single decode steps: per kernel kind, the time from the previous
+        # kernel's end to this kernel's dependency release (gap), and from release to end (run)
+        m.set_timeline(True)
+        m.prefill_device(ids_dev.data_ptr(), len(prompt))
+        kinds = ["embed"] + ["qkv", "attn", "o_proj", "gate_up", "down"] * s.n_layers + ["lm_head"]
+        stats = {k: {"gap_us": [], "run_us": [], "early_us": []} for k in set(kinds)}
+        totals = []
+        for i in range(12):
+            m.decode_steps(1)
+            tl = m.read_timeline().astype(np.int64)
+            if i < 2:
+                continue
+            totals.append((tl[-1, 2] - tl[0, 0]) / 1000.0)
+            for j, k in enumerate(kinds):
+                prev_end = tl[j - 1, 2] if j else tl[0, 0]
+                stats[k]["gap_us"].append((tl[j, 1] - prev_end) / 1000.0)
+                stats[k]["run_us"].append((tl[j, 2] - tl[j, 1]) / 1000.0)
+                stats[k]["early_us"].append((tl[j, 1] - tl[j, 0]) / 1000.0)
+        m.set_timeline(False)
+        out = {"timeline_step_us": float(np.mean(totals)), "kernels": {}}
+        for k, v in stats.items():
+            out["kernels"][k] = {f: round(float(np.mean(x)), 3) for f, x in v.items()}
+            out["kernels"][k]["per_step_us"] = round(float(np.sum(v["run_us"]) + np.sum(v["gap_us"])) / len(totals), 2)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+
     if args.layers:
         # profiling run on a reduced stack: timed loop only, not a bench line
         if rank == 0:
@@ -344,6 +371,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timeline", action="store_true",
+                    help="also print a device timeline summary of single decode steps")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: build the 1.5B shape with this many layers")
     args = ap.parse_args()

@@ -157,6 +157,16 @@ qw_status qw_reset(qw_model *m, int32_t seq);
  * decode graphs are rebuilt on the next step. */
 qw_status qw_set_trace(qw_model *m, int32_t kind, void *const *begin, void *const *end);
 
+/* Device timeline (profiling). With enable 1, every later decode step records, for each of
+ * its kernel launches (embedding, then per layer qkv, attention, o_proj, gate/up, down, then
+ * the LM head), three %globaltimer stamps in ns: the first CTA's start, the first CTA past
+ * its wait for the previous kernel, and the last CTA's end. qw_read_timeline copies the
+ * stamps of the last step, 3 per launch in launch order, into out (host, 3 * max_launches
+ * uint64) and the launch count into n_launches. Timing differs slightly from an
+ * uninstrumented run (one atomic per CTA per stamp). enable 0 frees the buffer. */
+qw_status qw_set_timeline(qw_model *m, int32_t enable);
+qw_status qw_read_timeline(qw_model *m, uint64_t *out, int32_t max_launches, int32_t *n_launches);
+
 /* Message for the last failing call on this thread ("" if none). */
 const char *qw_last_error(void);
 

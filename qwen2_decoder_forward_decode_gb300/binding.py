@@ -78,6 +78,8 @@ def lib():
         "qw_reset": ([VP, I32], I32),
         "qw_last_error": ([], ctypes.c_char_p),
         "qw_set_trace": ([VP, I32, P(VP), P(VP)], I32),
+        "qw_set_timeline": ([VP, I32], I32),
+        "qw_read_timeline": ([VP, P(ctypes.c_uint64), I32, pi], I32),
         "qw_op_decode_attention_noalloc": ([I32, I32, I32, I32, I32, I32, VP, VP, VP, VP, VP], I32),
         "qw_op_decode_attention_noalloc_limit": ([], SZ),
         "qw_op_gemm_f16": ([I32, I32, I32, VP, VP, VP, VP, I32, VP, VP], I32),
@@ -97,6 +99,7 @@ def exported_symbols():
     return ["qw_create", "qw_destroy", "qw_prefill", "qw_prefill_device", "qw_decode_step",
             "qw_decode_steps", "qw_generate", "qw_sync", "qw_logits", "qw_read_logits",
             "qw_tokens_device", "qw_position", "qw_reset", "qw_last_error", "qw_set_trace",
+            "qw_set_timeline", "qw_read_timeline",
             "qw_op_decode_attention_workspace", "qw_op_decode_attention",
             "qw_op_decode_attention_noalloc", "qw_op_decode_attention_noalloc_limit", "qw_op_gemm_f16",
             "qw_op_gemm_swiglu_f16"]
@@ -244,6 +247,18 @@ class Model:
         e = (ctypes.c_void_p * n)(*[x.cuda_event for x in end_events])
         self._trace_keep = (b, e, begin_events, end_events)
         check(lib().qw_set_trace(self.h, kind, b, e))
+
+    def set_timeline(self, enable=True):
+        check(lib().qw_set_timeline(self.h, int(enable)))
+
+    def read_timeline(self):
+        """[(start_ns, wait_released_ns, end_ns)] per kernel of the last decode step."""
+        n_max = 2 + 5 * self.shape.n_layers
+        buf = (ctypes.c_uint64 * (3 * n_max))()
+        n = np.zeros(1, dtype=np.int32)
+        check(lib().qw_read_timeline(self.h, buf, n_max, _iptr(n)))
+        a = np.frombuffer(buf, dtype=np.uint64)[:3 * int(n[0])].reshape(-1, 3)
+        return a
 
     def reset(self, seq=0):
         check(lib().qw_reset(self.h, seq))

@@ -79,6 +79,9 @@ struct qw_model {
   bool use_graphs = true;
   int trace_kind = -1;
   std::vector<cudaEvent_t> trace_begin, trace_end;
+  unsigned long long* tl_buf = nullptr;  // device timeline of one decode step (or null)
+  int tl_n = 0;                          // launches per decode step
+  std::vector<unsigned long long> tl_init;
 
   size_t seq_kv_elems() const { return (size_t)d.L * 2 * d.nkv * d.cap * d.hd; }
   char* kv_seq(int s) const { return (char*)kv + (size_t)s * seq_kv_elems() * esize; }
@@ -109,6 +112,9 @@ struct qw_model {
     cudaError_t e;
     float* xs = x + (size_t)s * d.H;
     bool pdl = true;
+    int launch_idx = 0;
+    // timeline slots of launch i: [i] start, [n + i] past the wait, [2n + i] end
+    auto tl = [&]() -> unsigned long long* { return tl_buf ? tl_buf + 3 * (launch_idx++) : nullptr; };
     // launch k-th kernel of layer l, with the optional trace events around it
     auto run = [&](int kind, int l, auto&& launch) -> cudaError_t {
       const bool traced = kind == trace_kind;
@@ -123,26 +129,26 @@ struct qw_model {
       }
       return cudaSuccess;
     };
-    if ((e = launch_embed(d, embed, tok + s, xs, err, stream, false))) return e;
+    if ((e = launch_embed(d, embed, tok + s, xs, err, tl(), stream, false))) return e;
     for (int l = 0; l < d.L; ++l) {
       const LayerPtrs& w = layers[l];
       void* kc = kc_layer(s, l);
       void* vc = vc_layer(s, l);
-      if ((e = run(0, l, [&](bool p) { return launch_qkv(d, w, xs, pos + s, rope, q, kc, vc, err, stream, p); })))
+      if ((e = run(0, l, [&](bool p) { return launch_qkv(d, w, xs, pos + s, rope, q, kc, vc, err, tl(), stream, p); })))
         return e;
       if ((e = run(1, l, [&](bool p) {
              return launch_attn(d.dtype == QW_BF16 ? 2 : 0, d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min,
-                                attn_smem, q, kc, vc, d.cap, pos + s, 0, attn, attn_ws, stream, p);
+                                attn_smem, q, kc, vc, d.cap, pos + s, 0, attn, attn_ws, tl(), stream, p);
            })))
         return e;
-      if ((e = run(2, l, [&](bool p) { return launch_resid(d, w.wo, d.H, d.nq * d.hd, attn, xs, err, stream, p); })))
+      if ((e = run(2, l, [&](bool p) { return launch_resid(d, w.wo, d.H, d.nq * d.hd, attn, xs, err, tl(), stream, p); })))
         return e;
-      if ((e = run(3, l, [&](bool p) { return launch_gateup(d, w, xs, act, err, stream, p); }))) return e;
-      if ((e = run(4, l, [&](bool p) { return launch_resid(d, w.w_down, d.H, d.I, act, xs, err, stream, p); })))
+      if ((e = run(3, l, [&](bool p) { return launch_gateup(d, w, xs, act, err, tl(), stream, p); }))) return e;
+      if ((e = run(4, l, [&](bool p) { return launch_resid(d, w.w_down, d.H, d.I, act, xs, err, tl(), stream, p); })))
         return e;
     }
     return run(5, 0, [&](bool p) {
-      return launch_lmhead(d, head_w(), final_norm, xs, logits + (size_t)s * d.V, fin(s, -1), stream, p);
+      return launch_lmhead(d, head_w(), final_norm, xs, logits + (size_t)s * d.V, fin(s, -1), tl(), stream, p);
     });
   }
 
@@ -152,6 +158,11 @@ struct qw_model {
   }
 
   cudaError_t run_decode(int s) {
+    if (tl_buf) {  // per launch: start and wait-release reduce with min, end with max
+      cudaError_t e = cudaMemcpyAsync(tl_buf, tl_init.data(), sizeof(unsigned long long) * 3 * tl_n,
+                                      cudaMemcpyHostToDevice, stream);
+      if (e) return e;
+    }
     if (!use_graphs) return enqueue_decode(s);
     if (!graphs[s]) {
       cudaGraph_t g = nullptr;
@@ -201,7 +212,7 @@ struct qw_model {
     if ((e = prefill_layers(d, layers.data(), embed, ids_dev, n, 0, rope, kv_seq(s), pf, err, stream)))
       return e;
     return launch_lmhead(d, head_w(), final_norm, pf.X + (size_t)(n - 1) * d.H,
-                         logits + (size_t)s * d.V, fin(s, n), stream, false);
+                         logits + (size_t)s * d.V, fin(s, n), nullptr, stream, false);
   }
 
   qw_status check_device_errors() {
@@ -223,7 +234,7 @@ struct qw_model {
       if (g) cudaGraphExecDestroy(g);
     graphs.clear();
     void* bufs[] = {kv, x, q, attn, act, logits, rope, attn_ws, keys, lm_counter, pos, tok,
-                    hist, hist_n, err, ids, pf_block, w16};
+                    hist, hist_n, err, ids, pf_block, w16, tl_buf};
     for (void* b : bufs)
       if (b) cudaFree(b);
     if (pinned) cudaFreeHost(pinned);
@@ -584,6 +595,34 @@ qw_status qw_set_trace(qw_model* m, int32_t kind, void* const* begin, void* cons
   return QW_OK;
 }
 
+qw_status qw_set_timeline(qw_model* m, int32_t enable) {
+  g_err.clear();
+  if (!m) return fail(QW_ERR_INVALID_ARG, "null model");
+  QW_CUDA(cudaStreamSynchronize(m->stream));
+  m->drop_graphs();
+  if (m->tl_buf) {
+    cudaFree(m->tl_buf);
+    m->tl_buf = nullptr;
+  }
+  if (!enable) return QW_OK;
+  m->tl_n = 1 + 5 * m->d.L + 1;
+  m->tl_init.assign((size_t)3 * m->tl_n, ~0ull);
+  for (int i = 0; i < m->tl_n; ++i) m->tl_init[3 * i + 2] = 0ull;
+  QW_CUDA(cudaMalloc(&m->tl_buf, sizeof(unsigned long long) * 3 * m->tl_n));
+  return QW_OK;
+}
+
+qw_status qw_read_timeline(qw_model* m, uint64_t* out, int32_t max_launches, int32_t* n_launches) {
+  g_err.clear();
+  if (!m || !out || !n_launches) return fail(QW_ERR_INVALID_ARG, "null argument");
+  if (!m->tl_buf) return fail(QW_ERR_INVALID_ARG, "timeline not enabled");
+  const int n = m->tl_n < max_launches ? m->tl_n : max_launches;
+  QW_CUDA(cudaMemcpyAsync(out, m->tl_buf, sizeof(unsigned long long) * 3 * n, cudaMemcpyDeviceToHost, m->stream));
+  QW_CUDA(cudaStreamSynchronize(m->stream));
+  *n_launches = n;
+  return QW_OK;
+}
+
 qw_status qw_read_logits(qw_model* m, int32_t seq, float* host_out) {
   g_err.clear();
   if (!m || !host_out) return fail(QW_ERR_INVALID_ARG, "null argument");
@@ -644,7 +683,7 @@ qw_status qw_op_decode_attention(int32_t kv_dtype, int32_t n_heads, int32_t n_kv
   cudaError_t e = attn_set_attributes(smem);
   if (e) return cuda_fail(e, "decode attention attributes");
   e = launch_attn(kv_dtype, n_heads, n_kv_heads, head_dim, nsplit, ATTN_CHUNK_MIN, smem, q, k, v,
-                              kv_stride, nullptr, ctx, out, workspace, (cudaStream_t)cuda_stream, false);
+                  kv_stride, nullptr, ctx, out, workspace, nullptr, (cudaStream_t)cuda_stream, false);
   if (e) return cuda_fail(e, "decode attention launch");
   return QW_OK;
 }

@@ -22,6 +22,7 @@ struct AttnArgs {
   float* out;
   float* part;            // [nq][nsplit_max][hd + 2]
   unsigned int* counter;  // [nkv]
+  unsigned long long* tl;  // timeline slots or null
 };
 
 // One CTA per (KV head, context chunk). The CTA copies q of its g query heads and the K and
@@ -39,12 +40,17 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
   const int g = blockIdx.x, split = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int G = a.group, hd = a.hd;
+  tl_stamp(a.tl, 0);
   pdl_wait();
   pdl_trigger();
+  tl_stamp(a.tl, 1);
   const int ctx = a.d_pos ? __ldcg(a.d_pos) + 1 : a.ctx_host;
   const int chunk = max(a.chunk_min, (ctx + a.nsplit_max - 1) / a.nsplit_max);
   const int nsplit = (ctx + chunk - 1) / chunk;
-  if (split >= nsplit) return;
+  if (split >= nsplit) {
+    tl_stamp(a.tl, 2);
+    return;
+  }
   const int j0 = split * chunk, j1 = min(ctx, j0 + chunk), n = j1 - j0;
   // shared layout: q [G][hd] f32 | scores [G][chunk] f32 | stats [G][2] | weights [G][nsplit_max]
   //                | K [chunk][hd] KV | V [chunk][hd] KV
@@ -137,7 +143,10 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
   __syncthreads();
   if (tid == 0) s_last = atomicAdd(a.counter + g, 1u) == (unsigned)(nsplit - 1);
   __syncthreads();
-  if (!s_last) return;
+  if (!s_last) {
+    tl_stamp(a.tl, 2);
+    return;
+  }
   __threadfence();
   // merge: weights w_s = exp(m_s - M) / sum_s l_s exp(m_s - M) per head, then out = sum_s w_s O_s
   for (int i = tid; i < G * nsplit; i += blockDim.x) {
@@ -193,6 +202,7 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
     if (idx < G * hd) a.out[(size_t)g * G * hd + idx] = acc[k];
   }
   if (tid == 0) a.counter[g] = 0u;
+  tl_stamp(a.tl, 2);
 }
 
 // ---- host side ------------------------------------------------------------
@@ -229,7 +239,7 @@ size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min, in
 cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int chunk_min,
                         size_t smem, const float* q, const void* kc, const void* vc,
                         int kv_stride, const int* d_pos, int ctx_host, float* out, void* ws,
-                        cudaStream_t s, bool pdl) {
+                        unsigned long long* tl, cudaStream_t s, bool pdl) {
   const int G = nq / nkv;
   if (G > GMAX) return cudaErrorInvalidValue;
   size_t part_bytes = ((size_t)nq * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
@@ -237,12 +247,12 @@ cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int c
   if (kv_dtype == 2) {
     AttnArgs<f16> a{q, (const f16*)kc, (const f16*)vc, kv_stride, hd, G, nsplit, chunk_min,
                      ctx_host, d_pos, 1.f / sqrtf((float)hd), out, (float*)ws,
-                     (unsigned int*)((char*)ws + part_bytes)};
+                     (unsigned int*)((char*)ws + part_bytes), tl};
     return launch_k(attn_decode_kernel<f16>, grid, block, smem, s, pdl, a);
   }
   AttnArgs<float> a{q, (const float*)kc, (const float*)vc, kv_stride, hd, G, nsplit, chunk_min,
                     ctx_host, d_pos, 1.f / sqrtf((float)hd), out, (float*)ws,
-                    (unsigned int*)((char*)ws + part_bytes)};
+                    (unsigned int*)((char*)ws + part_bytes), tl};
   return launch_k(attn_decode_kernel<float>, grid, block, smem, s, pdl, a);
 }
 

@@ -141,6 +141,20 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
                : "memory");
 }
 
+// Device timeline (profiling): globaltimer stamps reduced with atomics into per-launch slots.
+__device__ __forceinline__ unsigned long long gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// slots: [0] first CTA start, [1] first CTA past the dependency wait, [2] last CTA end
+__device__ __forceinline__ void tl_stamp(unsigned long long* tl, int which) {
+  if (tl && threadIdx.x == 0) {
+    if (which < 2) atomicMin(tl + which, gtime());
+    else atomicMax(tl + 2, gtime());
+  }
+}
+
 // Ask L2 to fetch bytes (multiple of 16) at src (16-byte aligned); no completion tracking.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

@@ -315,6 +315,7 @@ struct OpLMHead {
 struct GemvCfg {
   int KS, NS, slot_bytes, x_direct;
   int* err;
+  unsigned long long* tl;  // timeline slots or null
 };
 constexpr int MAX_SLOTS = 8;
 constexpr int PF_DIST = 8;  // items per warp requested into L2 beyond the shared-memory slots
@@ -367,6 +368,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
     }
   };
 
+  tl_stamp(c.tl, 0);
   if (lane == 0) {
     s_abort[warp] = 0;
     for (int sl = 0; sl < NS; ++sl) mbar_init(bar0 + 8 * sl, 1);
@@ -378,6 +380,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
   __syncwarp();
   pdl_trigger();  // the next kernel may become resident and start its own weight stream
   pdl_wait();
+  tl_stamp(c.tl, 1);
   if (!c.x_direct) op.prologue(xs, xs + op.K, scratch);
   __syncthreads();
 
@@ -456,6 +459,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
       mbar_wait_bounded(bar0 + 8 * (j % NS), (uint32_t)((j / NS) & 1));
   }
   op.finish();
+  tl_stamp(c.tl, 2);
 }
 
 // dynamic shared memory: per-warp slot rings and, unless x is read straight into
@@ -475,7 +479,7 @@ struct GemvPlan {
 };
 
 template <typename T, class Op>
-static bool plan_gemv(const Op& op, int nsm, int* err, GemvPlan* p) {
+static bool plan_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, GemvPlan* p) {
   const int nvec = op.K / Vec<T>::N;
   const int x_direct = (!Op::NORM && (size_t)op.K * 4 > X_SMEM_MAX) ? 1 : 0;
   const size_t xs = x_direct ? 0 : (size_t)(Op::NORM ? 2 : 1) * op.K * 4;
@@ -498,6 +502,7 @@ static bool plan_gemv(const Op& op, int nsm, int* err, GemvPlan* p) {
   p->c.slot_bytes = (int)slot;
   p->c.x_direct = x_direct;
   p->c.err = err;
+  p->c.tl = tl;
   p->maxv = maxv_for(nvec, KS);
   const int groups = (op.n_items + RG - 1) / RG;
   p->grid = groups < nsm ? groups : nsm;
@@ -506,9 +511,9 @@ static bool plan_gemv(const Op& op, int nsm, int* err, GemvPlan* p) {
 }
 
 template <typename T, class Op>
-static cudaError_t run_gemv(const Op& op, int nsm, int* err, cudaStream_t s, bool pdl) {
+static cudaError_t run_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, cudaStream_t s, bool pdl) {
   GemvPlan p;
-  if (!plan_gemv<T, Op>(op, nsm, err, &p)) return cudaErrorInvalidValue;
+  if (!plan_gemv<T, Op>(op, nsm, err, tl, &p)) return cudaErrorInvalidValue;
   const dim3 g(p.grid), b(GEMV_WARPS * 32);
   switch (p.maxv) {
     case 1: return launch_k(gemv_kernel<T, 1, Op>, g, b, p.smem, s, pdl, op, p.c);
@@ -535,9 +540,12 @@ static cudaError_t set_gemv_attrs() {
 // ---- embedding ---------------------------------------------------------------------------
 
 template <typename T>
-__global__ void embed_kernel(const T* E, int V, int H, const int* tok, float* x, int* err) {
+__global__ void embed_kernel(const T* E, int V, int H, const int* tok, float* x, int* err,
+                             unsigned long long* tl) {
   constexpr int VN = Vec<T>::N;
+  tl_stamp(tl, 0);
   pdl_wait();
+  tl_stamp(tl, 1);
   int t = __ldcg(tok);
   if (t < 0 || t >= V) {
     if (threadIdx.x == 0) atomicOr(err, ERR_TOKEN);
@@ -558,6 +566,7 @@ __global__ void embed_kernel(const T* E, int V, int H, const int* tok, float* x,
     for (int e = 0; e < VN; ++e) x[v * VN + e] = f[e];
   }
   pdl_trigger();
+  tl_stamp(tl, 2);
 }
 
 // ---- host launchers ---------------------------------------------------------------------
@@ -578,16 +587,16 @@ cudaError_t decode_set_attributes(const Dims& d) {
 }
 
 cudaError_t launch_embed(const Dims& d, const void* E, const int* tok, float* x, int* err,
-                         cudaStream_t s, bool pdl) {
+                         unsigned long long* tl, cudaStream_t s, bool pdl) {
   if (d.dtype == 1)
-    return launch_k(embed_kernel<bf16>, dim3(1), dim3(256), 0, s, pdl, (const bf16*)E, d.V, d.H, tok, x, err);
-  return launch_k(embed_kernel<float>, dim3(1), dim3(256), 0, s, pdl, (const float*)E, d.V, d.H, tok, x, err);
+    return launch_k(embed_kernel<bf16>, dim3(1), dim3(256), 0, s, pdl, (const bf16*)E, d.V, d.H, tok, x, err, tl);
+  return launch_k(embed_kernel<float>, dim3(1), dim3(256), 0, s, pdl, (const float*)E, d.V, d.H, tok, x, err, tl);
 }
 
 template <typename T, typename KV>
 static cudaError_t qkv_t(const Dims& d, const LayerPtrs& w, const float* x, const int* d_pos,
-                         const float2* rope, float* q, void* kc, void* vc, int* err, cudaStream_t s,
-                         bool pdl) {
+                         const float2* rope, float* q, void* kc, void* vc, int* err,
+                         unsigned long long* tl, cudaStream_t s, bool pdl) {
   OpQKV<T, KV> op{};
   op.K = d.H;
   op.n_items = (d.nq + 2 * d.nkv) * (d.hd / 2);
@@ -597,58 +606,61 @@ static cudaError_t qkv_t(const Dims& d, const LayerPtrs& w, const float* x, cons
   op.gain = (const T*)w.in_norm;
   op.x = x; op.eps = d.eps; op.d_pos = d_pos; op.rope = rope; op.q_out = q;
   op.kc = (KV*)kc; op.vc = (KV*)vc;
-  return run_gemv<T>(op, d.nsm, err, s, pdl);
+  return run_gemv<T>(op, d.nsm, err, tl, s, pdl);
 }
 cudaError_t launch_qkv(const Dims& d, const LayerPtrs& w, const float* x, const int* d_pos,
-                       const float2* rope, float* q, void* kc, void* vc, int* err, cudaStream_t s,
-                       bool pdl) {
-  return d.dtype == 1 ? qkv_t<bf16, f16>(d, w, x, d_pos, rope, q, kc, vc, err, s, pdl)
-                      : qkv_t<float, float>(d, w, x, d_pos, rope, q, kc, vc, err, s, pdl);
+                       const float2* rope, float* q, void* kc, void* vc, int* err,
+                       unsigned long long* tl, cudaStream_t s, bool pdl) {
+  return d.dtype == 1 ? qkv_t<bf16, f16>(d, w, x, d_pos, rope, q, kc, vc, err, tl, s, pdl)
+                      : qkv_t<float, float>(d, w, x, d_pos, rope, q, kc, vc, err, tl, s, pdl);
 }
 
 template <typename T>
 static cudaError_t resid_t(const Dims& d, const void* W, int N, int K, const float* in, float* y,
-                           int* err, cudaStream_t s, bool pdl) {
+                           int* err, unsigned long long* tl, cudaStream_t s, bool pdl) {
   if ((size_t)K * 4 > X_SMEM_MAX) {  // long rows (the down projection): one row per item
     OpResid<T, 1> op{};
     op.K = K; op.N = N; op.n_items = N; op.W = (const T*)W; op.in = in; op.y = y;
-    return run_gemv<T>(op, d.nsm, err, s, pdl);
+    return run_gemv<T>(op, d.nsm, err, tl, s, pdl);
   }
   OpResid<T, 2> op{};
   op.K = K; op.N = N; op.n_items = (N + 1) / 2; op.W = (const T*)W; op.in = in; op.y = y;
-  return run_gemv<T>(op, d.nsm, err, s, pdl);
+  return run_gemv<T>(op, d.nsm, err, tl, s, pdl);
 }
 cudaError_t launch_resid(const Dims& d, const void* W, int N, int K, const float* in, float* y,
-                         int* err, cudaStream_t s, bool pdl) {
-  return d.dtype == 1 ? resid_t<bf16>(d, W, N, K, in, y, err, s, pdl)
-                      : resid_t<float>(d, W, N, K, in, y, err, s, pdl);
+                         int* err, unsigned long long* tl, cudaStream_t s, bool pdl) {
+  return d.dtype == 1 ? resid_t<bf16>(d, W, N, K, in, y, err, tl, s, pdl)
+                      : resid_t<float>(d, W, N, K, in, y, err, tl, s, pdl);
 }
 
 template <typename T>
 static cudaError_t gateup_t(const Dims& d, const LayerPtrs& w, const float* x, float* act, int* err,
-                            cudaStream_t s, bool pdl) {
+                            unsigned long long* tl, cudaStream_t s, bool pdl) {
   OpGateUp<T> op{};
   op.K = d.H; op.n_items = d.I; op.wg = (const T*)w.w_gate; op.wu = (const T*)w.w_up;
   op.gain = (const T*)w.post_norm; op.x = x; op.eps = d.eps; op.act = act;
-  return run_gemv<T>(op, d.nsm, err, s, pdl);
+  return run_gemv<T>(op, d.nsm, err, tl, s, pdl);
 }
 cudaError_t launch_gateup(const Dims& d, const LayerPtrs& w, const float* x, float* act, int* err,
-                          cudaStream_t s, bool pdl) {
-  return d.dtype == 1 ? gateup_t<bf16>(d, w, x, act, err, s, pdl) : gateup_t<float>(d, w, x, act, err, s, pdl);
+                          unsigned long long* tl, cudaStream_t s, bool pdl) {
+  return d.dtype == 1 ? gateup_t<bf16>(d, w, x, act, err, tl, s, pdl)
+                      : gateup_t<float>(d, w, x, act, err, tl, s, pdl);
 }
 
 template <typename T>
 static cudaError_t lmhead_t(const Dims& d, const void* W, const void* fn, const float* x,
-                            float* logits, const Finalize& f, cudaStream_t s, bool pdl) {
+                            float* logits, const Finalize& f, unsigned long long* tl, cudaStream_t s,
+                            bool pdl) {
   OpLMHead<T> op{};
   op.K = d.H; op.N = d.V; op.n_items = (d.V + 1) / 2; op.W = (const T*)W; op.gain = (const T*)fn;
   op.x = x; op.eps = d.eps; op.logits = logits; op.f = f;
-  return run_gemv<T>(op, d.nsm, f.err, s, pdl);
+  return run_gemv<T>(op, d.nsm, f.err, tl, s, pdl);
 }
 cudaError_t launch_lmhead(const Dims& d, const void* W, const void* final_norm, const float* x,
-                          float* logits, const Finalize& f, cudaStream_t s, bool pdl) {
-  return d.dtype == 1 ? lmhead_t<bf16>(d, W, final_norm, x, logits, f, s, pdl)
-                      : lmhead_t<float>(d, W, final_norm, x, logits, f, s, pdl);
+                          float* logits, const Finalize& f, unsigned long long* tl, cudaStream_t s,
+                          bool pdl) {
+  return d.dtype == 1 ? lmhead_t<bf16>(d, W, final_norm, x, logits, f, tl, s, pdl)
+                      : lmhead_t<float>(d, W, final_norm, x, logits, f, tl, s, pdl);
 }
 
 }  // namespace qw

@@ -52,24 +52,26 @@ size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min, in
 cudaError_t decode_set_attributes(const Dims& d);
 cudaError_t attn_set_attributes(size_t smem);  // not during stream capture
 
+// tl: three timeline slots (start, past the dependency wait, end) or null
 cudaError_t launch_embed(const Dims& d, const void* E, const int* tok, float* x, int* err,
-                         cudaStream_t s, bool pdl);
+                         unsigned long long* tl, cudaStream_t s, bool pdl);
 cudaError_t launch_qkv(const Dims& d, const LayerPtrs& w, const float* x, const int* d_pos,
-                       const float2* rope, float* q, void* kc, void* vc, int* err, cudaStream_t s,
-                       bool pdl);
+                       const float2* rope, float* q, void* kc, void* vc, int* err,
+                       unsigned long long* tl, cudaStream_t s, bool pdl);
 // ctx = d_pos ? d_pos[0] + 1 : ctx_host
 // kv_dtype: 0 fp32, 2 fp16
 cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int chunk_min,
                         size_t smem, const float* q, const void* kc, const void* vc,
                         int kv_stride, const int* d_pos, int ctx_host, float* out, void* ws,
-                        cudaStream_t s, bool pdl);
+                        unsigned long long* tl, cudaStream_t s, bool pdl);
 // y[r] += W[r,:] . in  (r < N), W [N, K]
 cudaError_t launch_resid(const Dims& d, const void* W, int N, int K, const float* in, float* y,
-                         int* err, cudaStream_t s, bool pdl);
+                         int* err, unsigned long long* tl, cudaStream_t s, bool pdl);
 cudaError_t launch_gateup(const Dims& d, const LayerPtrs& w, const float* x, float* act, int* err,
-                          cudaStream_t s, bool pdl);
+                          unsigned long long* tl, cudaStream_t s, bool pdl);
 cudaError_t launch_lmhead(const Dims& d, const void* W, const void* final_norm, const float* x,
-                          float* logits, const Finalize& f, cudaStream_t s, bool pdl);
+                          float* logits, const Finalize& f, unsigned long long* tl, cudaStream_t s,
+                          bool pdl);
 
 // ---- gemm_tc.cu (tcgen05 tensor-core GEMMs, bf16 in, fp32 accumulate) ----
 bool gemm_tc_available();
