@@ -15,6 +15,7 @@
 #include "internal.h"
 
 #include <math.h>
+#include <stdlib.h>
 
 namespace qw {
 
@@ -313,12 +314,11 @@ struct OpLMHead {
 // an SM, so under programmatic dependent launch the next kernel's weights are in flight
 // while this one finishes. Partial sums over K segments add in a fixed order.
 struct GemvCfg {
-  int KS, NS, slot_bytes, x_direct;
+  int KS, NS, slot_bytes, x_direct, pf_dist;
   int* err;
   unsigned long long* tl;  // timeline slots or null
 };
 constexpr int MAX_SLOTS = 8;
-constexpr int PF_DIST = 8;  // items per warp requested into L2 beyond the shared-memory slots
 
 template <typename T, int MAXV, class Op>
 __global__ void __launch_bounds__(GEMV_WARPS * 32, 2)
@@ -375,7 +375,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
     mbar_fence_init();
     const int n0 = min(NS, my_items);  // weights do not depend on upstream kernels
     for (int k = 0; k < n0; ++k) issue(k);
-    for (int k = n0; k < min(NS + PF_DIST, my_items); ++k) prefetch(k);
+    for (int k = n0; k < min(NS + c.pf_dist, my_items); ++k) prefetch(k);
   }
   __syncwarp();
   pdl_trigger();  // the next kernel may become resident and start its own weight stream
@@ -431,7 +431,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
       fence_proxy_async();
       issue(k + NS);
       ++issued;
-      if (k + NS + PF_DIST < my_items) prefetch(k + NS + PF_DIST);
+      if (c.pf_dist && k + NS + c.pf_dist < my_items) prefetch(k + NS + c.pf_dist);
     }
     a0 = warp_sum(a0);
     if (Op::RPI == 2) a1 = warp_sum(a1);
@@ -464,8 +464,21 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
 
 // dynamic shared memory: per-warp slot rings and, unless x is read straight into
 // registers, the input vector (and the gains of a norm prologue)
-static constexpr int WARP_BUDGET = 12 * 1024;  // bytes of slots per warp (8 warps: 96 KB)
 static constexpr int X_SMEM_MAX = 16 * 1024;
+// Tuning: bytes of slots per warp (8 warps: 96 KB keeps two kernels' CTAs on one SM) and
+// the L2 prefetch distance in items; QW_GEMV_SLOT_KB / QW_GEMV_PF override them.
+static int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  return v && *v ? std::atoi(v) : dflt;
+}
+static int warp_budget() {
+  static const int b = env_int("QW_GEMV_SLOT_KB", 12) * 1024;
+  return b;
+}
+static int pf_dist() {
+  static const int p = env_int("QW_GEMV_PF", 0);
+  return p;
+}
 
 static int maxv_for(int nvec, int KS) {
   const int need = (((nvec + KS - 1) / KS) + 31) / 32;
@@ -487,7 +500,8 @@ static bool plan_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, G
   // register tile fits; then split further while too few items exist to fill every warp
   int KS = 1;
   auto slot_of = [&](int ks) { return (size_t)Op::RPI * ((nvec + ks - 1) / ks) * 16; };
-  while (KS < GEMV_WARPS && (maxv_for(nvec, KS) > 8 || 2 * slot_of(KS) > WARP_BUDGET)) KS *= 2;
+  const int WARP_BUDGET = warp_budget();
+  while (KS < GEMV_WARPS && (maxv_for(nvec, KS) > 8 || 2 * slot_of(KS) > (size_t)WARP_BUDGET)) KS *= 2;
   if (maxv_for(nvec, KS) > 8) return false;
   while (KS < GEMV_WARPS && (long long)op.n_items * KS < (long long)nsm * GEMV_WARPS) KS *= 2;
   const size_t slot = (slot_of(KS) + 127) & ~(size_t)127;
@@ -501,6 +515,7 @@ static bool plan_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, G
   p->c.NS = NS;
   p->c.slot_bytes = (int)slot;
   p->c.x_direct = x_direct;
+  p->c.pf_dist = pf_dist();
   p->c.err = err;
   p->c.tl = tl;
   p->maxv = maxv_for(nvec, KS);
