@@ -79,6 +79,14 @@ struct qw_model {
   bool use_graphs = true;
   int trace_kind = -1;
   std::vector<cudaEvent_t> trace_begin, trace_end;
+  // persistent decode-step kernel (bf16 models)
+  bool use_step = false;
+  StepLayer* step_layers = nullptr;
+  float* step_part = nullptr;
+  unsigned* step_bar = nullptr;
+  int* step_abort = nullptr;
+  int step_nslots = 0;
+  size_t step_smem = 0;
   unsigned long long* tl_buf = nullptr;  // device timeline of one decode step (or null)
   int tl_n = 0;                          // launches per decode step
   std::vector<unsigned long long> tl_init;
@@ -157,7 +165,37 @@ struct qw_model {
       if (g) { cudaGraphExecDestroy(g); g = nullptr; }
   }
 
+  cudaError_t run_step_kernel(int s) {
+    StepLaunch a{};
+    a.d = d;
+    a.layers_dev = step_layers;
+    a.embed = embed;
+    a.final_norm = final_norm;
+    a.head = head_w();
+    a.rope = rope;
+    a.kv_seq = kv_seq(s);
+    a.x = x + (size_t)s * d.H;
+    a.q = q;
+    a.act = act;
+    a.logits = logits + (size_t)s * d.V;
+    a.part = step_part;
+    a.tok = tok + s;
+    a.pos = pos + s;
+    a.key = keys + s;
+    a.hist = hist + (size_t)s * d.cap;
+    a.hist_n = hist_n + s;
+    a.hist_cap = d.cap;
+    a.bar = step_bar;
+    a.abort = step_abort;
+    a.err = err;
+    a.nslots = step_nslots;
+    a.grid = d.nsm;
+    a.smem = step_smem;
+    return launch_step(a, stream);
+  }
+
   cudaError_t run_decode(int s) {
+    if (use_step && !tl_buf && trace_kind < 0) return run_step_kernel(s);
     if (tl_buf) {  // per launch: start and wait-release reduce with min, end with max
       cudaError_t e = cudaMemcpyAsync(tl_buf, tl_init.data(), sizeof(unsigned long long) * 3 * tl_n,
                                       cudaMemcpyHostToDevice, stream);
@@ -234,7 +272,8 @@ struct qw_model {
       if (g) cudaGraphExecDestroy(g);
     graphs.clear();
     void* bufs[] = {kv, x, q, attn, act, logits, rope, attn_ws, keys, lm_counter, pos, tok,
-                    hist, hist_n, err, ids, pf_block, w16, tl_buf};
+                    hist, hist_n, err, ids, pf_block, w16, tl_buf, step_layers, step_part, step_bar,
+                    step_abort};
     for (void* b : bufs)
       if (b) cudaFree(b);
     if (pinned) cudaFreeHost(pinned);
@@ -401,6 +440,31 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
     }
   }
   if ((e = decode_set_attributes(d))) return bail(e, "decode attributes");
+  {
+    const char* sk = std::getenv("QW_STEP_KERNEL");
+    int coop = 0;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device);
+    if (step_kernel_supported(d) && coop && !(sk && sk[0] == '0')) {
+      if ((e = step_set_attributes(d, &m->step_nslots, &m->step_smem))) return bail(e, "step attributes");
+      std::vector<StepLayer> sl(d.L);
+      for (int l = 0; l < d.L; ++l) {
+        const LayerPtrs& w = m->layers[l];
+        sl[l] = StepLayer{(const bf16*)w.in_norm, (const bf16*)w.wq, (const bf16*)w.wk, (const bf16*)w.wv,
+                          (const bf16*)w.bq, (const bf16*)w.bk, (const bf16*)w.bv, (const bf16*)w.wo,
+                          (const bf16*)w.post_norm, (const bf16*)w.w_gate, (const bf16*)w.w_up,
+                          (const bf16*)w.w_down};
+      }
+      if ((e = cudaMalloc(&m->step_layers, sizeof(StepLayer) * d.L))) return bail(e, "cudaMalloc");
+      if ((e = cudaMemcpy(m->step_layers, sl.data(), sizeof(StepLayer) * d.L, cudaMemcpyHostToDevice)))
+        return bail(e, "cudaMemcpy");
+      if ((e = cudaMalloc(&m->step_part, step_part_bytes(d)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMalloc(&m->step_bar, 2 * sizeof(unsigned)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMemset(m->step_bar, 0, 2 * sizeof(unsigned)))) return bail(e, "cudaMemset");
+      if ((e = cudaMalloc(&m->step_abort, sizeof(int)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMemset(m->step_abort, 0, sizeof(int)))) return bail(e, "cudaMemset");
+      m->use_step = true;
+    }
+  }
   if ((e = attn_set_attributes(m->attn_smem))) return bail(e, "attention attributes");
   if ((e = prefill_set_attributes(d))) return bail(e, "prefill attributes");
   if ((e = cudaDeviceSynchronize())) return bail(e, "cudaDeviceSynchronize");

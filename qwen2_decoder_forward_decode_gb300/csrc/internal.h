@@ -83,6 +83,32 @@ cudaError_t gemm_tc(const __half* A, int lda, const __half* B, int ldb, const __
 cudaError_t gemm_tc_swiglu(const __half* A, int lda, const __half* Wg, const __half* Wu, int ldb,
                            __half* Act, int ldc, int M, int N, int K, int* err, cudaStream_t s);
 
+// ---- step.cu (persistent decode step of one sequence, bf16 models) ----
+struct StepLayer {
+  const __nv_bfloat16 *in_norm, *wq, *wk, *wv, *bq, *bk, *bv, *wo, *post_norm, *wg, *wu, *wd;
+};
+struct StepLaunch {
+  Dims d;
+  const StepLayer* layers_dev;  // device array [L]
+  const void *embed, *final_norm, *head;
+  const float2* rope;
+  void* kv_seq;                 // fp16 cache of the sequence [L][2][nkv][cap][hd]
+  float *x, *q, *act, *logits, *part;
+  int *tok, *pos;
+  unsigned long long* key;
+  int *hist, *hist_n;
+  int hist_cap;
+  unsigned* bar;                // 2 words, zero at creation
+  int *abort, *err;
+  int nslots, grid;
+  size_t smem;
+};
+int step_xs_floats(const Dims& d);
+bool step_kernel_supported(const Dims& d);
+size_t step_part_bytes(const Dims& d);
+cudaError_t step_set_attributes(const Dims& d, int* nslots_out, size_t* smem_out);
+cudaError_t launch_step(const StepLaunch& a, cudaStream_t s);
+
 // ---- prefill.cu ----
 struct PrefillBufs {
   float *X, *Xn, *Y, *Q, *O, *G, *U;  // [T][..] fp32 activations
