@@ -179,6 +179,36 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def timeline_per_kernel(m, s, ids_dev, prompt, rank):
+    """Device timeline of single decode steps run as one kernel per operation: per kernel
+    kind, the gap from the previous kernel's end to this kernel's dependency release, the
+    run from release to end, and how early its CTAs were resident."""
+    m.set_timeline(True)
+    m.prefill_device(ids_dev.data_ptr(), len(prompt))
+    kinds = ["embed"] + ["qkv", "attn", "o_proj", "gate_up", "down"] * s.n_layers + ["lm_head"]
+    stats = {k: {"gap_us": [], "run_us": [], "early_us": []} for k in set(kinds)}
+    totals = []
+    for i in range(12):
+        m.decode_steps(1)
+        tl = m.read_timeline().astype(np.int64)
+        if i < 2:
+            continue
+        totals.append((tl[-1, 2] - tl[0, 0]) / 1000.0)
+        for j, k in enumerate(kinds):
+            prev_end = tl[j - 1, 2] if j else tl[0, 0]
+            stats[k]["gap_us"].append((tl[j, 1] - prev_end) / 1000.0)
+            stats[k]["run_us"].append((tl[j, 2] - tl[j, 1]) / 1000.0)
+            stats[k]["early_us"].append((tl[j, 1] - tl[j, 0]) / 1000.0)
+    m.set_timeline(False)
+    out = {"timeline_step_us": float(np.mean(totals)), "kernels": {}}
+    for k, v in stats.items():
+        out["kernels"][k] = {f: round(float(np.mean(x)), 3) for f, x in v.items()}
+        out["kernels"][k]["per_step_us"] = round(float(np.sum(v["run_us"]) + np.sum(v["gap_us"])) / len(totals), 2)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+
 def run_native(args):
     import torch
     import __graft_entry__
@@ -269,31 +299,33 @@ def run_native(args):
     traffic = recorded_traffic("gateup_gemv", src)
 
     if args.timeline:
-        # device timeline of single decode steps: per kernel kind, the time from the previous
-        # kernel's end to this kernel's dependency release (gap), and from release to end (run)
-        m.set_timeline(True)
-        m.prefill_device(ids_dev.data_ptr(), len(prompt))
-        kinds = ["embed"] + ["qkv", "attn", "o_proj", "gate_up", "down"] * s.n_layers + ["lm_head"]
-        stats = {k: {"gap_us": [], "run_us": [], "early_us": []} for k in set(kinds)}
-        totals = []
-        for i in range(12):
-            m.decode_steps(1)
-            tl = m.read_timeline().astype(np.int64)
-            if i < 2:
-                continue
-            totals.append((tl[-1, 2] - tl[0, 0]) / 1000.0)
-            for j, k in enumerate(kinds):
-                prev_end = tl[j - 1, 2] if j else tl[0, 0]
-                stats[k]["gap_us"].append((tl[j, 1] - prev_end) / 1000.0)
-                stats[k]["run_us"].append((tl[j, 2] - tl[j, 1]) / 1000.0)
-                stats[k]["early_us"].append((tl[j, 1] - tl[j, 0]) / 1000.0)
-        m.set_timeline(False)
-        out = {"timeline_step_us": float(np.mean(totals)), "kernels": {}}
-        for k, v in stats.items():
-            out["kernels"][k] = {f: round(float(np.mean(x)), 3) for f, x in v.items()}
-            out["kernels"][k]["per_step_us"] = round(float(np.sum(v["run_us"]) + np.sum(v["gap_us"])) / len(totals), 2)
-        if rank == 0:
-            print(json.dumps(out), flush=True)
+        # device timeline of single decode steps
+        if os.environ.get("QW_STEP_KERNEL", "1") != "0":
+            m.set_timeline(True)
+            m.prefill_device(ids_dev.data_ptr(), len(prompt))
+            # persistent step kernel: per phase [start, end, producer issued] of the first CTA
+            kinds = ["qkv", "attn", "o_proj", "gate_up", "down"] * s.n_layers + ["lm_head"]
+            st = {k: {"run_us": [], "barrier_us": [], "producer_lead_us": []} for k in set(kinds)}
+            tot = []
+            for i in range(12):
+                m.decode_steps(1)
+                tl = m.read_timeline().astype(np.int64)[:len(kinds)]
+                if i < 2:
+                    continue
+                tot.append((tl[-1, 1] - tl[0, 0]) / 1000.0)
+                for j, k in enumerate(kinds):
+                    st[k]["run_us"].append((tl[j, 1] - tl[j, 0]) / 1000.0)
+                    if j + 1 < len(kinds):
+                        st[k]["barrier_us"].append((tl[j + 1, 0] - tl[j, 1]) / 1000.0)
+                    if tl[j, 2] > 0:
+                        st[k]["producer_lead_us"].append((tl[j, 1] - tl[j, 2]) / 1000.0)
+            m.set_timeline(False)
+            out = {"step_kernel_us": float(np.mean(tot)), "phases": {
+                k: {f: round(float(np.mean(x)), 3) if x else None for f, x in v.items()} for k, v in st.items()}}
+            if rank == 0:
+                print(json.dumps(out), flush=True)
+        else:
+            timeline_per_kernel(m, s, ids_dev, prompt, rank)
 
     if args.layers:
         # profiling run on a reduced stack: timed loop only, not a bench line

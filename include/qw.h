@@ -163,7 +163,11 @@ qw_status qw_set_trace(qw_model *m, int32_t kind, void *const *begin, void *cons
  * its wait for the previous kernel, and the last CTA's end. qw_read_timeline copies the
  * stamps of the last step, 3 per launch in launch order, into out (host, 3 * max_launches
  * uint64) and the launch count into n_launches. Timing differs slightly from an
- * uninstrumented run (one atomic per CTA per stamp). enable 0 frees the buffer. */
+ * uninstrumented run (one atomic per CTA per stamp). enable 0 frees the buffer.
+ * When the model runs decode steps as one persistent kernel (bf16 models), the entries
+ * are instead per phase of the step (q/k/v, attention, o_proj, gate/up, down per layer,
+ * then the LM head), each [consumer start, consumer end, producer finished issuing the
+ * phase's weight copies], stamped by the first CTA. */
 qw_status qw_set_timeline(qw_model *m, int32_t enable);
 qw_status qw_read_timeline(qw_model *m, uint64_t *out, int32_t max_launches, int32_t *n_launches);
 

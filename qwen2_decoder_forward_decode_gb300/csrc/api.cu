@@ -191,11 +191,12 @@ struct qw_model {
     a.nslots = step_nslots;
     a.grid = d.nsm;
     a.smem = step_smem;
+    a.tl = tl_buf;
     return launch_step(a, stream);
   }
 
   cudaError_t run_decode(int s) {
-    if (use_step && !tl_buf && trace_kind < 0) return run_step_kernel(s);
+    if (use_step && trace_kind < 0) return run_step_kernel(s);
     if (tl_buf) {  // per launch: start and wait-release reduce with min, end with max
       cudaError_t e = cudaMemcpyAsync(tl_buf, tl_init.data(), sizeof(unsigned long long) * 3 * tl_n,
                                       cudaMemcpyHostToDevice, stream);
@@ -672,6 +673,7 @@ qw_status qw_set_timeline(qw_model* m, int32_t enable) {
   m->tl_n = 1 + 5 * m->d.L + 1;
   m->tl_init.assign((size_t)3 * m->tl_n, ~0ull);
   for (int i = 0; i < m->tl_n; ++i) m->tl_init[3 * i + 2] = 0ull;
+  if (m->use_step) m->tl_init.assign((size_t)3 * m->tl_n, 0ull);
   QW_CUDA(cudaMalloc(&m->tl_buf, sizeof(unsigned long long) * 3 * m->tl_n));
   return QW_OK;
 }

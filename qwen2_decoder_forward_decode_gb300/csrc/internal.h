@@ -102,6 +102,7 @@ struct StepLaunch {
   int *abort, *err;
   int nslots, grid;
   size_t smem;
+  unsigned long long* tl;       // per phase [start, end, producer issued] or null
 };
 int step_xs_floats(const Dims& d);
 bool step_kernel_supported(const Dims& d);

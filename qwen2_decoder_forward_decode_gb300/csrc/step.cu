@@ -57,6 +57,7 @@ struct Params {
   int* err;
   int nslots;
   int xs_floats;    // floats of the staged input vector region
+  unsigned long long* tl;  // timeline: per phase [start, end, producer issued] (CTA 0), or null
 };
 
 constexpr int MAX_SPLIT = 16;
@@ -510,6 +511,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
             if (r1) bulk_copy_g2s(dst + g.chunk * 2, r1 + k0, bytes, full0 + 8 * s);
           }
         }
+        if (p.tl && blockIdx.x == 0) {
+          const int pi = l == p.L ? 5 * p.L : 5 * l + ph;
+          p.tl[3 * pi + 2] = gtime();
+        }
       }
     }
     // let every issued copy land before this thread (and, with it, the CTA) may finish
@@ -573,11 +578,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   };
 
   bool ok = true;
+  int phase_no = 0;
+  auto stamp = [&](int which) {  // CTA 0: [start, end] of consumer phase phase_no
+    if (p.tl && blockIdx.x == 0 && ct == 0) p.tl[3 * phase_no + which] = gtime();
+  };
   for (int l = 0; l < p.L && ok; ++l) {
     const Layer& w = p.layers[l];
     f16* kc = p.kv + (size_t)l * 2 * p.nkv * p.cap * p.hd;
     f16* vc = kc + (size_t)p.nkv * p.cap * p.hd;
     // ---- QKV
+    stamp(0);
     if (l == 0) stage_embed(p, xs, scratch, w.in_norm);
     else stage_norm(p, xs, scratch, p.x, w.in_norm, p.H);
     ok = run_phase(P_QKV, l, [&](int item, float a, float b) {
@@ -608,6 +618,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       }
     }) && ok;
     ok = cbar_and(ok);
+    stamp(1);
+    ++phase_no;
     if (!(ok = ok && grid_barrier(p, gen))) break;
 
     // ---- ATTN: CTA (g, sp) holds the softmax partial of KV head g over positions
@@ -615,32 +627,45 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     const int ctx = pos + 1;
     int nsplit = (ctx + 63) / 64;
     if (nsplit > MAX_SPLIT) nsplit = MAX_SPLIT;
+    stamp(0);
     if ((int)blockIdx.x < p.nkv * nsplit) attention_partial(p, xs, kc, vc, ctx, nsplit);
+    stamp(1);
+    ++phase_no;
     if (!(ok = grid_barrier(p, gen))) break;
 
     // ---- OPROJ: merge the partials into xs = attention output, then x += Wo . xs
+    stamp(0);
     merge_partials(p, xs, nsplit);
     ok = cbar_and(run_phase(P_OPROJ, l, [&](int item, float a, float b) {
       atomicAdd(p.x + 2 * item, a);
       if (2 * item + 1 < p.H) atomicAdd(p.x + 2 * item + 1, b);
     }));
+    stamp(1);
+    ++phase_no;
     if (!(ok = ok && grid_barrier(p, gen))) break;
 
     // ---- GATEUP
+    stamp(0);
     stage_norm(p, xs, scratch, p.x, w.post_norm, p.H);
     ok = cbar_and(run_phase(P_GATEUP, l, [&](int item, float gt, float up) {
       p.act[item] = (gt / (1.f + expf(-gt))) * up;
     }));
+    stamp(1);
+    ++phase_no;
     if (!(ok = ok && grid_barrier(p, gen))) break;
 
     // ---- DOWN
+    stamp(0);
     stage_copy(xs, p.act, p.I);
     ok = cbar_and(run_phase(P_DOWN, l, [&](int item, float a, float) { atomicAdd(p.x + item, a); }));
+    stamp(1);
+    ++phase_no;
     if (!(ok = ok && grid_barrier(p, gen))) break;
   }
 
   // ---- LM head: logits and the greedy argmax (lowest index among equal maxima)
   if (ok) {
+    stamp(0);
     stage_norm(p, xs, scratch, p.x, p.final_norm, p.H);
     auto take = [&](int r, float v) {
       p.logits[r] = v;
@@ -669,6 +694,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       if (k) atomicMax(p.key, k);
       if (bad) atomicOr(p.err, ERR_NONFINITE);
     }
+    stamp(1);
     ok = ok && grid_barrier(p, gen);
     if (ok && blockIdx.x == 0 && ct == 0) {
       const unsigned long long k = atomicAdd(p.key, 0ull);
@@ -731,6 +757,7 @@ cudaError_t launch_step(const StepLaunch& a, cudaStream_t s) {
   p.tok = a.tok; p.pos = a.pos; p.key = a.key; p.hist = a.hist; p.hist_n = a.hist_n; p.hist_cap = a.hist_cap;
   p.bar = a.bar; p.abort = a.abort; p.err = a.err;
   p.nslots = a.nslots; p.xs_floats = step_xs_floats(a.d);
+  p.tl = a.tl;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(step::THREADS);
