@@ -83,7 +83,8 @@ struct qw_model {
   bool use_step = false;
   StepLayer* step_layers = nullptr;
   float* step_part = nullptr;
-  unsigned* step_bar = nullptr;
+  unsigned long long* step_bar = nullptr;
+  unsigned long long step_bar_base = 0;  // barrier counter value before the next launch
   int* step_abort = nullptr;
   int step_nslots = 0;
   size_t step_smem = 0;
@@ -186,6 +187,8 @@ struct qw_model {
     a.hist_n = hist_n + s;
     a.hist_cap = d.cap;
     a.bar = step_bar;
+    a.bar_base = step_bar_base;
+    step_bar_base += (unsigned long long)step_barriers_per_launch(d) * d.nsm;
     a.abort = step_abort;
     a.err = err;
     a.nslots = step_nslots;
@@ -459,8 +462,8 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
       if ((e = cudaMemcpy(m->step_layers, sl.data(), sizeof(StepLayer) * d.L, cudaMemcpyHostToDevice)))
         return bail(e, "cudaMemcpy");
       if ((e = cudaMalloc(&m->step_part, step_part_bytes(d)))) return bail(e, "cudaMalloc");
-      if ((e = cudaMalloc(&m->step_bar, 2 * sizeof(unsigned)))) return bail(e, "cudaMalloc");
-      if ((e = cudaMemset(m->step_bar, 0, 2 * sizeof(unsigned)))) return bail(e, "cudaMemset");
+      if ((e = cudaMalloc(&m->step_bar, sizeof(unsigned long long)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMemset(m->step_bar, 0, sizeof(unsigned long long)))) return bail(e, "cudaMemset");
       if ((e = cudaMalloc(&m->step_abort, sizeof(int)))) return bail(e, "cudaMalloc");
       if ((e = cudaMemset(m->step_abort, 0, sizeof(int)))) return bail(e, "cudaMemset");
       m->use_step = true;

@@ -98,13 +98,15 @@ struct StepLaunch {
   unsigned long long* key;
   int *hist, *hist_n;
   int hist_cap;
-  unsigned* bar;                // 2 words, zero at creation
+  unsigned long long* bar;      // monotonic barrier counter, zero at creation
+  unsigned long long bar_base;  // its value before this launch
   int *abort, *err;
   int nslots, grid;
   size_t smem;
   unsigned long long* tl;       // per phase [start, end, producer issued] or null
 };
 int step_xs_floats(const Dims& d);
+int step_barriers_per_launch(const Dims& d);
 bool step_kernel_supported(const Dims& d);
 size_t step_part_bytes(const Dims& d);
 cudaError_t step_set_attributes(const Dims& d, int* nslots_out, size_t* smem_out);

@@ -52,7 +52,8 @@ struct Params {
   unsigned long long* key;
   int *hist, *hist_n;
   int hist_cap;
-  unsigned* bar;    // [0] arrivals, [1] generation
+  unsigned long long* bar;   // monotonic arrival counter (never reset)
+  unsigned long long bar_base;  // its value when this launch started
   int* abort;
   int* err;
   int nslots;
@@ -154,32 +155,30 @@ __device__ __forceinline__ bool cbar_and(bool v) {
   return r != 0;
 }
 
-// Grid barrier among the consumers of all CTAs (sense: a generation counter).
-__device__ bool grid_barrier(const Params& p, unsigned& gen) {
+// Grid barrier among the consumers of all CTAs: every CTA adds one to a monotonic 64-bit
+// counter and waits until it reaches this barrier's target (launch base + (b + 1) * CTAs).
+__device__ bool grid_barrier(const Params& p, int& b) {
   __shared__ int s_ok;
   cbar();
   if (threadIdx.x == 0) {
     int ok = 1;
     __threadfence();
-    const unsigned arrived = atomicAdd(p.bar, 1u);
-    if (arrived == gridDim.x - 1) {
-      *(volatile unsigned*)p.bar = 0u;
-      __threadfence();
-      atomicAdd(p.bar + 1, 1u);
-    } else {
-      const long long t0 = clock64();
-      for (int it = 0; *(volatile unsigned*)(p.bar + 1) == gen; ++it) {
-        if ((it & 15) == 0 && (aborted(p) || clock64() - t0 > WAIT_CYCLES)) {
-          raise_abort(p);
-          ok = 0;
-          break;
-        }
+    atomicAdd(p.bar, 1ull);
+    const unsigned long long target = p.bar_base + (unsigned long long)(b + 1) * gridDim.x;
+    const long long t0 = clock64();
+    for (int it = 0;; ++it) {
+      unsigned long long v;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p.bar) : "memory");
+      if (v >= target) break;
+      if ((it & 15) == 0 && (aborted(p) || clock64() - t0 > WAIT_CYCLES)) {
+        raise_abort(p);
+        ok = 0;
+        break;
       }
     }
-    __threadfence();
-    gen += 1;
     s_ok = ok && !aborted(p);
   }
+  ++b;
   cbar();
   return s_ok != 0;
 }
@@ -297,7 +296,20 @@ __device__ void attention_partial(const Params& p, float* xs, const f16* kc, con
   float* corr = run + 2 * G;
   f16* ks = reinterpret_cast<f16*>(xs + ((G * hd + G * 64 + 3 * G + 3) & ~3));  // 16-byte aligned
   f16* vs = ks + 64 * hd;
-  for (int i = ct; i < G * hd; i += NCT) qs[i] = __ldcg(p.q + (size_t)g * G * hd + i);
+  {
+    const float4* qsrc = reinterpret_cast<const float4*>(p.q + (size_t)g * G * hd);
+    float4 r[GMAX * 128 / 4 / NCT];
+#pragma unroll
+    for (int i = 0; i < GMAX * 128 / 4 / NCT; ++i) {
+      const int jv = ct + i * NCT;
+      r[i] = jv < G * hd / 4 ? __ldcg(qsrc + jv) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < GMAX * 128 / 4 / NCT; ++i) {
+      const int jv = ct + i * NCT;
+      if (jv < G * hd / 4) reinterpret_cast<float4*>(qs)[jv] = r[i];
+    }
+  }
   if (ct < G) {
     run[2 * ct] = -INFINITY;
     run[2 * ct + 1] = 0.f;
@@ -478,7 +490,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
 
   // ---------------- producer ----------------
   if (warp == NCW) {
-    if (lane != 0) return;
+    // Units of a phase are issued in batches: lane k of the warp computes the addresses of
+    // unit (batch + k), waits for that unit's slot to be free and issues its copies. A batch
+    // holds at most NS units, so no two lanes of a batch share a slot.
+    const int NSB = NS < 32 ? NS : 32;
     long long seq = 0;
     bool ok = true;
     for (int l = 0; l <= p.L && ok; ++l) {
@@ -492,37 +507,80 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         }
         const Geo g = geo(p, phase);
         const int nl = n_local(g.n_items);
-        for (int j = 0; j < nl && ok; ++j) {
-          const int item = blockIdx.x + j * gridDim.x;
-          for (int u = 0; u < g.U; ++u, ++seq) {
-            const int s = (int)(seq % NS);
-            if (seq >= NS && !slot_wait(p, empty0 + 8 * s, (uint32_t)(((seq / NS) - 1) & 1))) {
-              ok = false;
-              break;
+        const int total = nl * g.U;
+        // this phase's matrices, once per phase
+        const Layer* lw = p.layers + (l < p.L ? l : 0);
+        const bf16* mq = lw->wq;
+        const bf16* mk = lw->wk;
+        const bf16* mv = lw->wv;
+        const bf16* mo = lw->wo;
+        const bf16* mg = lw->wg;
+        const bf16* mu = lw->wu;
+        const bf16* md = lw->wd;
+        for (int b0 = 0; b0 < total && ok; b0 += NSB) {
+          const int k = b0 + lane;
+          bool lane_ok = true;
+          if (lane < NSB && k < total) {
+            const int j = k / g.U, u = k - j * g.U;
+            const int item = blockIdx.x + j * gridDim.x;
+            const bf16* r0;
+            const bf16* r1 = nullptr;
+            switch (phase) {
+              case P_QKV: {
+                const int half = p.hd >> 1;
+                int head = item / half;
+                const int i = item - head * half;
+                const bf16* m = mq;
+                if (head >= p.nq) { head -= p.nq; m = mk; if (head >= p.nkv) { head -= p.nkv; m = mv; } }
+                r0 = m + (size_t)(head * p.hd + i) * p.H;
+                r1 = r0 + (size_t)half * p.H;
+                break;
+              }
+              case P_OPROJ:
+                r0 = mo + (size_t)(2 * item) * g.K;
+                r1 = 2 * item + 1 < p.H ? r0 + g.K : nullptr;
+                break;
+              case P_GATEUP:
+                r0 = mg + (size_t)item * p.H;
+                r1 = mu + (size_t)item * p.H;
+                break;
+              case P_DOWN:
+                r0 = md + (size_t)item * p.I;
+                break;
+              default:
+                r0 = p.head + (size_t)(2 * item) * p.H;
+                r1 = 2 * item + 1 < p.V ? r0 + p.H : nullptr;
+                break;
             }
-            const int k0 = u * g.chunk;
-            const int len = min(g.chunk, g.K - k0);
-            const uint32_t bytes = (uint32_t)len * 2;
-            const bf16* r0 = row_ptr(p, phase, l, item, 0);
-            const bf16* r1 = g.rows == 2 ? row_ptr(p, phase, l, item, 1) : nullptr;
-            mbar_expect_tx(full0 + 8 * s, bytes * (r1 ? 2u : 1u));
-            const uint32_t dst = ring + s * SLOT;
-            bulk_copy_g2s(dst, r0 + k0, bytes, full0 + 8 * s);
-            if (r1) bulk_copy_g2s(dst + g.chunk * 2, r1 + k0, bytes, full0 + 8 * s);
+            const long long sq = seq + k;
+            const int s = (int)(sq % NS);
+            if (sq >= NS) lane_ok = slot_wait(p, empty0 + 8 * s, (uint32_t)(((sq / NS) - 1) & 1));
+            if (lane_ok) {
+              const int k0 = u * g.chunk;
+              const uint32_t bytes = (uint32_t)min(g.chunk, g.K - k0) * 2;
+              mbar_expect_tx(full0 + 8 * s, bytes * (r1 ? 2u : 1u));
+              const uint32_t dst = ring + s * SLOT;
+              bulk_copy_g2s(dst, r0 + k0, bytes, full0 + 8 * s);
+              if (r1) bulk_copy_g2s(dst + g.chunk * 2, r1 + k0, bytes, full0 + 8 * s);
+            }
           }
+          ok = __all_sync(0xffffffffu, lane_ok);
         }
-        if (p.tl && blockIdx.x == 0) {
+        seq += total;
+        if (p.tl && blockIdx.x == 0 && lane == 0) {
           const int pi = l == p.L ? 5 * p.L : 5 * l + ph;
           p.tl[3 * pi + 2] = gtime();
         }
       }
     }
-    // let every issued copy land before this thread (and, with it, the CTA) may finish
-    const long long first = seq > NS ? seq - NS : 0;
-    for (long long k = first; k < seq; ++k) {
-      const int s = (int)(k % NS);
-      const long long t0 = clock64();
-      while (!mbar_test(full0 + 8 * s, (uint32_t)((k / NS) & 1)) && clock64() - t0 < WAIT_CYCLES) {
+    // let every issued copy land before this warp (and, with it, the CTA) may finish
+    if (lane == 0) {
+      const long long first = seq > NS ? seq - NS : 0;
+      for (long long k = first; k < seq; ++k) {
+        const int s = (int)(k % NS);
+        const long long t0 = clock64();
+        while (!mbar_test(full0 + 8 * s, (uint32_t)((k / NS) & 1)) && clock64() - t0 < WAIT_CYCLES) {
+        }
       }
     }
     return;
@@ -530,7 +588,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
 
   // ---------------- consumers ----------------
   const int ct = threadIdx.x;
-  unsigned gen = *(volatile unsigned*)(p.bar + 1);
+  int gen = 0;  // barriers passed in this launch
   long long base = 0;  // ring sequence number of the current phase's first unit
   const int half = p.hd >> 1;
   const int G = p.nq / p.nkv;
@@ -727,6 +785,8 @@ int step_xs_floats(const Dims& d) {
   return (n + 31) & ~31;
 }
 
+int step_barriers_per_launch(const Dims& d) { return 5 * d.L + 1; }
+
 bool step_kernel_supported(const Dims& d) {
   return d.dtype == 1 && d.hd <= 128 && d.hd % 8 == 0 && d.nq / d.nkv <= step::GMAX &&
          d.H % 8 == 0 && d.I % 8 == 0 && (size_t)step_xs_floats(d) * 4 + 16 * step::SLOT <= 220 * 1024;
@@ -755,7 +815,7 @@ cudaError_t launch_step(const StepLaunch& a, cudaStream_t s) {
   p.rope = a.rope; p.kv = (f16*)a.kv_seq;
   p.x = a.x; p.q = a.q; p.act = a.act; p.logits = a.logits; p.part = a.part;
   p.tok = a.tok; p.pos = a.pos; p.key = a.key; p.hist = a.hist; p.hist_n = a.hist_n; p.hist_cap = a.hist_cap;
-  p.bar = a.bar; p.abort = a.abort; p.err = a.err;
+  p.bar = a.bar; p.bar_base = a.bar_base; p.abort = a.abort; p.err = a.err;
   p.nslots = a.nslots; p.xs_floats = step_xs_floats(a.d);
   p.tl = a.tl;
   cudaLaunchConfig_t cfg = {};
