@@ -85,7 +85,7 @@ struct qw_model {
   float* step_part = nullptr;
   unsigned long long* step_bar = nullptr;
   unsigned long long step_bar_base = 0;  // barrier counter value before the next launch
-  int* step_abort = nullptr;
+  int* step_abort = nullptr;  // [0] abort flag, [1..4] diagnostic of the first expired wait
   int step_nslots = 0;
   size_t step_smem = 0;
   unsigned long long* tl_buf = nullptr;  // device timeline of one decode step (or null)
@@ -190,6 +190,7 @@ struct qw_model {
     a.bar_base = step_bar_base;
     step_bar_base += (unsigned long long)step_barriers_per_launch(d) * d.nsm;
     a.abort = step_abort;
+    a.diag = step_abort + 1;
     a.err = err;
     a.nslots = step_nslots;
     a.grid = d.nsm;
@@ -266,7 +267,14 @@ struct qw_model {
       QW_CUDA(cudaStreamSynchronize(stream));
       if (h & ERR_TOKEN) return fail(QW_ERR_TOKEN_RANGE, "token id outside [0, vocab) on the device");
       if (h & ERR_NONFINITE) return fail(QW_ERR_NUMERIC, "non-finite logits");
-      if (h & ERR_TIMEOUT) return fail(QW_ERR_TIMEOUT, "device wait timed out");
+      if (h & ERR_TIMEOUT) {
+        int dg[5] = {0, 0, 0, 0, 0};
+        if (step_abort) cudaMemcpy(dg, step_abort, sizeof(dg), cudaMemcpyDeviceToHost);
+        char msg[160];
+        std::snprintf(msg, sizeof(msg), "device wait timed out (site %d, CTA %d, warp %d, detail %d)", dg[1],
+                      dg[2], dg[3], dg[4]);
+        return fail(QW_ERR_TIMEOUT, msg);
+      }
     }
     return QW_OK;
   }
@@ -464,8 +472,8 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
       if ((e = cudaMalloc(&m->step_part, step_part_bytes(d)))) return bail(e, "cudaMalloc");
       if ((e = cudaMalloc(&m->step_bar, sizeof(unsigned long long)))) return bail(e, "cudaMalloc");
       if ((e = cudaMemset(m->step_bar, 0, sizeof(unsigned long long)))) return bail(e, "cudaMemset");
-      if ((e = cudaMalloc(&m->step_abort, sizeof(int)))) return bail(e, "cudaMalloc");
-      if ((e = cudaMemset(m->step_abort, 0, sizeof(int)))) return bail(e, "cudaMemset");
+      if ((e = cudaMalloc(&m->step_abort, 5 * sizeof(int)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMemset(m->step_abort, 0, 5 * sizeof(int)))) return bail(e, "cudaMemset");
       m->use_step = true;
     }
   }

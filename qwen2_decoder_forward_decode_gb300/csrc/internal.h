@@ -104,6 +104,7 @@ struct StepLaunch {
   int nslots, grid;
   size_t smem;
   unsigned long long* tl;       // per phase [start, end, producer issued] or null
+  int* diag;                    // 4 ints: first expired wait (site, CTA, warp, detail)
 };
 int step_xs_floats(const Dims& d);
 int step_barriers_per_launch(const Dims& d);

@@ -59,6 +59,7 @@ struct Params {
   int nslots;
   int xs_floats;    // floats of the staged input vector region
   unsigned long long* tl;  // timeline: per phase [start, end, producer issued] (CTA 0), or null
+  int* diag;               // first expired wait: [site, CTA, warp, detail]
 };
 
 constexpr int MAX_SPLIT = 16;
@@ -117,21 +118,30 @@ __device__ __forceinline__ int n_local(int n_items) {
 
 __device__ __forceinline__ bool aborted(const Params& p) { return *(volatile int*)p.abort != 0; }
 
-__device__ __forceinline__ void raise_abort(const Params& p) {
-  atomicExch(p.abort, 1);
+enum : int { SITE_SLOT_FULL = 1, SITE_SLOT_EMPTY = 2, SITE_GRID = 3 };
+
+// First expiry wins the diagnostic record; every later wait sees the abort flag.
+__device__ __forceinline__ void raise_abort(const Params& p, int site, long long detail) {
+  if (atomicExch(p.abort, 1) == 0 && p.diag) {
+    p.diag[0] = site;
+    p.diag[1] = blockIdx.x;
+    p.diag[2] = threadIdx.x >> 5;
+    p.diag[3] = (int)detail;
+  }
   atomicOr(p.err, ERR_TIMEOUT);
 }
 
-// Bounded mbarrier wait that also gives up when another CTA has aborted.
-__device__ __forceinline__ bool slot_wait(const Params& p, uint32_t bar, uint32_t parity) {
-  if (mbar_test(bar, parity)) return true;
+// Bounded wait (non-blocking tests) that also gives up when another CTA has aborted.
+__device__ __forceinline__ bool slot_wait(const Params& p, uint32_t bar, uint32_t parity, int site,
+                                          long long detail) {
+  if (mbar_test_now(bar, parity)) return true;
   const long long t0 = clock64();
   for (int it = 0;; ++it) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_test_now(bar, parity)) return true;
     if ((it & 63) == 0) {
       if (aborted(p)) return false;
       if (clock64() - t0 > WAIT_CYCLES) {
-        raise_abort(p);
+        raise_abort(p, site, detail);
         return false;
       }
     }
@@ -171,7 +181,7 @@ __device__ bool grid_barrier(const Params& p, int& b) {
       asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p.bar) : "memory");
       if (v >= target) break;
       if ((it & 15) == 0 && (aborted(p) || clock64() - t0 > WAIT_CYCLES)) {
-        raise_abort(p);
+        if (!aborted(p)) raise_abort(p, SITE_GRID, b);
         ok = 0;
         break;
       }
@@ -494,8 +504,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     // unit (batch + k), waits for that unit's slot to be free and issues its copies. A batch
     // holds at most NS units, so no two lanes of a batch share a slot.
     const int NSB = NS < 32 ? NS : 32;
-    long long seq = 0;
-    bool ok = true;
+    long long seq = 0, issued = 0;  // units scheduled / actually issued
+    bool ok = !aborted(p);
     for (int l = 0; l <= p.L && ok; ++l) {
       for (int ph = 0; ph < 5 && ok; ++ph) {
         int phase = ph;
@@ -519,12 +529,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         const bf16* md = lw->wd;
         for (int b0 = 0; b0 < total && ok; b0 += NSB) {
           const int k = b0 + lane;
-          bool lane_ok = true;
+          const bf16* r0 = nullptr;
+          const bf16* r1 = nullptr;
+          uint32_t bytes = 0, dst_off = 0;
           if (lane < NSB && k < total) {
             const int j = k / g.U, u = k - j * g.U;
             const int item = blockIdx.x + j * gridDim.x;
-            const bf16* r0;
-            const bf16* r1 = nullptr;
             switch (phase) {
               case P_QKV: {
                 const int half = p.hd >> 1;
@@ -552,19 +562,35 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
                 r1 = 2 * item + 1 < p.V ? r0 + p.H : nullptr;
                 break;
             }
-            const long long sq = seq + k;
-            const int s = (int)(sq % NS);
-            if (sq >= NS) lane_ok = slot_wait(p, empty0 + 8 * s, (uint32_t)(((sq / NS) - 1) & 1));
-            if (lane_ok) {
-              const int k0 = u * g.chunk;
-              const uint32_t bytes = (uint32_t)min(g.chunk, g.K - k0) * 2;
-              mbar_expect_tx(full0 + 8 * s, bytes * (r1 ? 2u : 1u));
-              const uint32_t dst = ring + s * SLOT;
-              bulk_copy_g2s(dst, r0 + k0, bytes, full0 + 8 * s);
-              if (r1) bulk_copy_g2s(dst + g.chunk * 2, r1 + k0, bytes, full0 + 8 * s);
-            }
+            const int k0 = u * g.chunk;
+            bytes = (uint32_t)min(g.chunk, g.K - k0) * 2;
+            r0 += k0;
+            if (r1) r1 += k0;
+            dst_off = (uint32_t)g.chunk * 2;
           }
-          ok = __all_sync(0xffffffffu, lane_ok);
+          // lane 0 waits for each unit's slot and issues its copies, in sequence order
+          const int n = min(NSB, total - b0);
+          for (int kk = 0; kk < n && ok; ++kk) {
+            const bf16* a0 = (const bf16*)__shfl_sync(0xffffffffu, (unsigned long long)r0, kk);
+            const bf16* a1 = (const bf16*)__shfl_sync(0xffffffffu, (unsigned long long)r1, kk);
+            const uint32_t nb = __shfl_sync(0xffffffffu, bytes, kk);
+            const uint32_t off1 = __shfl_sync(0xffffffffu, dst_off, kk);
+            bool lane_ok = true;
+            if (lane == 0) {
+              const long long sq = seq + b0 + kk;
+              const int s = (int)(sq % NS);
+              if (sq >= NS)
+                lane_ok = slot_wait(p, empty0 + 8 * s, (uint32_t)(((sq / NS) - 1) & 1), SITE_SLOT_EMPTY, sq);
+              if (lane_ok) {
+                mbar_expect_tx(full0 + 8 * s, nb * (a1 ? 2u : 1u));
+                const uint32_t dst = ring + s * SLOT;
+                bulk_copy_g2s(dst, a0, nb, full0 + 8 * s);
+                if (a1) bulk_copy_g2s(dst + off1, a1, nb, full0 + 8 * s);
+                issued = sq + 1;
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, lane_ok ? 1 : 0, 0) != 0;
+          }
         }
         seq += total;
         if (p.tl && blockIdx.x == 0 && lane == 0) {
@@ -575,11 +601,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     }
     // let every issued copy land before this warp (and, with it, the CTA) may finish
     if (lane == 0) {
-      const long long first = seq > NS ? seq - NS : 0;
-      for (long long k = first; k < seq; ++k) {
+      const long long first = issued > NS ? issued - NS : 0;
+      for (long long k = first; k < issued; ++k) {
         const int s = (int)(k % NS);
         const long long t0 = clock64();
-        while (!mbar_test(full0 + 8 * s, (uint32_t)((k / NS) & 1)) && clock64() - t0 < WAIT_CYCLES) {
+        while (!mbar_test_now(full0 + 8 * s, (uint32_t)((k / NS) & 1)) && clock64() - t0 < WAIT_CYCLES) {
         }
       }
     }
@@ -607,7 +633,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       for (int u = 0; u < g.U; ++u) {
         const long long seq = base + (long long)j * g.U + u;
         const int s = (int)(seq % NS);
-        if (!__all_sync(0xffffffffu, slot_wait(p, full0 + 8 * s, (uint32_t)((seq / NS) & 1)))) {
+        if (!__all_sync(0xffffffffu, slot_wait(p, full0 + 8 * s, (uint32_t)((seq / NS) & 1), SITE_SLOT_FULL, seq))) {
           ok = false;
           break;
         }
@@ -635,7 +661,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     return ok;
   };
 
-  bool ok = true;
+  bool ok = !aborted(p);  // a failed earlier launch leaves the model unusable: return fast
   int phase_no = 0;
   auto stamp = [&](int which) {  // CTA 0: [start, end] of consumer phase phase_no
     if (p.tl && blockIdx.x == 0 && ct == 0) p.tl[3 * phase_no + which] = gtime();
@@ -818,6 +844,7 @@ cudaError_t launch_step(const StepLaunch& a, cudaStream_t s) {
   p.bar = a.bar; p.bar_base = a.bar_base; p.abort = a.abort; p.err = a.err;
   p.nslots = a.nslots; p.xs_floats = step_xs_floats(a.d);
   p.tl = a.tl;
+  p.diag = a.diag;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(step::THREADS);
