@@ -309,9 +309,11 @@ def run_native(args):
             tot = []
             for i in range(12):
                 m.decode_steps(1)
-                tl = m.read_timeline().astype(np.int64)[:len(kinds)]
+                full_tl = m.read_timeline().astype(np.int64)
+                tl = full_tl[:len(kinds)]
                 if i < 2:
                     continue
+                ring = full_tl[len(kinds)]
                 tot.append((tl[-1, 1] - tl[0, 0]) / 1000.0)
                 for j, k in enumerate(kinds):
                     st[k]["run_us"].append((tl[j, 1] - tl[j, 0]) / 1000.0)
@@ -320,7 +322,10 @@ def run_native(args):
                     if tl[j, 2] > 0:
                         st[k]["producer_lead_us"].append((tl[j, 1] - tl[j, 2]) / 1000.0)
             m.set_timeline(False)
-            out = {"step_kernel_us": float(np.mean(tot)), "phases": {
+            out = {"step_kernel_us": float(np.mean(tot)),
+                   "ring_cta0": {"producer_waits": int(ring[0]), "producer_found_slot_busy": int(ring[1]),
+                                 "consumer_warp0_found_slot_empty": int(ring[2])},
+                   "phases": {
                 k: {f: round(float(np.mean(x)), 3) if x else None for f, x in v.items()} for k, v in st.items()}}
             if rank == 0:
                 print(json.dumps(out), flush=True)

@@ -200,7 +200,14 @@ struct qw_model {
   }
 
   cudaError_t run_decode(int s) {
-    if (use_step && trace_kind < 0) return run_step_kernel(s);
+    if (use_step && trace_kind < 0) {
+      if (tl_buf) {  // fresh counters for this step
+        cudaError_t e = cudaMemcpyAsync(tl_buf, tl_init.data(), sizeof(unsigned long long) * 3 * tl_n,
+                                        cudaMemcpyHostToDevice, stream);
+        if (e) return e;
+      }
+      return run_step_kernel(s);
+    }
     if (tl_buf) {  // per launch: start and wait-release reduce with min, end with max
       cudaError_t e = cudaMemcpyAsync(tl_buf, tl_init.data(), sizeof(unsigned long long) * 3 * tl_n,
                                       cudaMemcpyHostToDevice, stream);
@@ -686,6 +693,8 @@ qw_status qw_set_timeline(qw_model* m, int32_t enable) {
   for (int i = 0; i < m->tl_n; ++i) m->tl_init[3 * i + 2] = 0ull;
   if (m->use_step) m->tl_init.assign((size_t)3 * m->tl_n, 0ull);
   QW_CUDA(cudaMalloc(&m->tl_buf, sizeof(unsigned long long) * 3 * m->tl_n));
+  QW_CUDA(cudaMemcpy(m->tl_buf, m->tl_init.data(), sizeof(unsigned long long) * 3 * m->tl_n,
+                     cudaMemcpyHostToDevice));
   return QW_OK;
 }
 

@@ -579,8 +579,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
             if (lane == 0) {
               const long long sq = seq + b0 + kk;
               const int s = (int)(sq % NS);
-              if (sq >= NS)
-                lane_ok = slot_wait(p, empty0 + 8 * s, (uint32_t)(((sq / NS) - 1) & 1), SITE_SLOT_EMPTY, sq);
+              if (sq >= NS) {
+                const uint32_t par = (uint32_t)(((sq / NS) - 1) & 1);
+                if (p.tl && blockIdx.x == 0) {  // occupancy statistics of the ring (profiling)
+                  p.tl[3 * (5 * p.L + 1) + 0] += 1;
+                  if (!mbar_test_now(empty0 + 8 * s, par)) p.tl[3 * (5 * p.L + 1) + 1] += 1;
+                }
+                lane_ok = slot_wait(p, empty0 + 8 * s, par, SITE_SLOT_EMPTY, sq);
+              }
               if (lane_ok) {
                 mbar_expect_tx(full0 + 8 * s, nb * (a1 ? 2u : 1u));
                 const uint32_t dst = ring + s * SLOT;
@@ -633,6 +639,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       for (int u = 0; u < g.U; ++u) {
         const long long seq = base + (long long)j * g.U + u;
         const int s = (int)(seq % NS);
+        if (p.tl && blockIdx.x == 0 && threadIdx.x == 0 &&
+            !mbar_test_now(full0 + 8 * s, (uint32_t)((seq / NS) & 1)))
+          p.tl[3 * (5 * p.L + 1) + 2] += 1;
         if (!__all_sync(0xffffffffu, slot_wait(p, full0 + 8 * s, (uint32_t)((seq / NS) & 1), SITE_SLOT_FULL, seq))) {
           ok = false;
           break;
