@@ -28,10 +28,11 @@ namespace qw {
 namespace step {
 
 constexpr int NCW = 8;                    // consumer warps
-constexpr int THREADS = (NCW + 1) * 32;   // + one producer warp
+constexpr int NPW = 2;                    // producer warps (each issues every NPW-th unit)
+constexpr int THREADS = (NCW + NPW) * 32;
 constexpr int NCT = NCW * 32;             // consumer threads
-constexpr int SLOT = 6 * 1024;            // bytes per ring slot
-constexpr int MAX_SLOTS = 28;
+constexpr int SLOT = 24 * 1024;           // bytes per ring slot (a unit of whole rows)
+constexpr int MAX_SLOTS = 8;
 constexpr int GMAX = 8;
 
 enum : int { P_QKV = 0, P_ATTN = 1, P_OPROJ = 2, P_GATEUP = 3, P_DOWN = 4, P_LM = 5 };
@@ -64,56 +65,81 @@ struct Params {
 
 constexpr int MAX_SPLIT = 16;
 
+// A phase's items (one or two weight rows each) are split in contiguous blocks over the
+// CTAs. A CTA groups consecutive items of its block into units of whole rows that fit one
+// ring slot (one bulk copy per row segment); an item whose rows alone exceed a slot is
+// split along K into U chunk units instead.
 struct Geo {
-  int n_items, rows, K, chunk, U;
+  int n_items, rows, K;
+  bool paired;   // the two rows of an item come from two segments (RoPE pair, gate/up)
+  int cut;       // units never cross multiples of this item index (0: no constraint)
+  int ipu;       // items per unit
+  int chunk;     // K elements per unit
+  int U;         // chunk units per item (1 unless a row exceeds a slot)
 };
 
 __device__ __forceinline__ Geo geo(const Params& p, int ph) {
   Geo g;
+  g.paired = false;
+  g.cut = 0;
   switch (ph) {
-    case P_QKV: g.n_items = (p.nq + 2 * p.nkv) * (p.hd / 2); g.rows = 2; g.K = p.H; break;
+    case P_QKV: g.n_items = (p.nq + 2 * p.nkv) * (p.hd / 2); g.rows = 2; g.K = p.H; g.paired = true; g.cut = p.hd / 2; break;
     case P_OPROJ: g.n_items = (p.H + 1) / 2; g.rows = 2; g.K = p.nq * p.hd; break;
-    case P_GATEUP: g.n_items = p.I; g.rows = 2; g.K = p.H; break;
+    case P_GATEUP: g.n_items = p.I; g.rows = 2; g.K = p.H; g.paired = true; break;
     case P_DOWN: g.n_items = p.H; g.rows = 1; g.K = p.I; break;
     default: g.n_items = (p.V + 1) / 2; g.rows = 2; g.K = p.H; break;
   }
-  int chunk = SLOT / (g.rows * 2);
-  chunk &= ~7;
-  g.chunk = g.K < chunk ? g.K : chunk;
-  g.U = (g.K + g.chunk - 1) / g.chunk;
+  const int item_bytes = g.rows * g.K * 2;
+  if (item_bytes <= SLOT) {
+    g.ipu = SLOT / item_bytes;
+    if (g.ipu > 16) g.ipu = 16;
+    g.chunk = g.K;
+    g.U = 1;
+  } else {
+    g.ipu = 1;
+    g.chunk = (SLOT / (g.rows * 2)) & ~7;
+    g.U = (g.K + g.chunk - 1) / g.chunk;
+  }
   return g;
 }
 
-// row r of item `item` in phase ph of layer l (null when the row does not exist)
-__device__ __forceinline__ const bf16* row_ptr(const Params& p, int ph, int l, int item, int r) {
-  const Layer& w = p.layers[l < p.L ? l : 0];
+// first row of item `item` in segment `seg` (paired ops), else the item's first row
+__device__ __forceinline__ const bf16* item_row(const Params& p, const Layer* lw, int ph, int item, int seg) {
   switch (ph) {
     case P_QKV: {
       const int half = p.hd >> 1;
       int head = item / half;
-      const int rr = item - head * half + r * half;
-      if (head < p.nq) return w.wq + (size_t)(head * p.hd + rr) * p.H;
-      head -= p.nq;
-      if (head < p.nkv) return w.wk + (size_t)(head * p.hd + rr) * p.H;
-      head -= p.nkv;
-      return w.wv + (size_t)(head * p.hd + rr) * p.H;
+      const int i = item - head * half + seg * half;
+      const bf16* m = lw->wq;
+      if (head >= p.nq) { head -= p.nq; m = lw->wk; if (head >= p.nkv) { head -= p.nkv; m = lw->wv; } }
+      return m + (size_t)(head * p.hd + i) * p.H;
     }
-    case P_OPROJ: {
-      const int rr = 2 * item + r;
-      return rr < p.H ? w.wo + (size_t)rr * p.nq * p.hd : nullptr;
-    }
-    case P_GATEUP: return (r == 0 ? w.wg : w.wu) + (size_t)item * p.H;
-    case P_DOWN: return w.wd + (size_t)item * p.I;
-    default: {
-      const int rr = 2 * item + r;
-      return rr < p.V ? p.head + (size_t)rr * p.H : nullptr;
-    }
+    case P_OPROJ: return lw->wo + (size_t)(2 * item) * p.nq * p.hd;
+    case P_GATEUP: return (seg == 0 ? lw->wg : lw->wu) + (size_t)item * p.H;
+    case P_DOWN: return lw->wd + (size_t)item * p.I;
+    default: return p.head + (size_t)(2 * item) * p.H;
   }
 }
 
-__device__ __forceinline__ int n_local(int n_items) {
-  const int c = blockIdx.x, G = gridDim.x;
-  return c < n_items ? (n_items - 1 - c) / G + 1 : 0;
+// rows of the (non-paired) items [i, i + n) that exist: the last pair of an odd-sized
+// matrix has one row
+__device__ __forceinline__ int consecutive_rows(const Params& p, int ph, const Geo& g, int i, int n) {
+  if (g.rows == 1) return n;
+  const int N = ph == P_OPROJ ? p.H : p.V;
+  return min(2 * n, N - 2 * i);
+}
+
+// contiguous item block [i0, i1) of this CTA
+__device__ __forceinline__ void item_block(int n_items, int& i0, int& i1) {
+  i0 = (int)((long long)blockIdx.x * n_items / gridDim.x);
+  i1 = (int)((long long)(blockIdx.x + 1) * n_items / gridDim.x);
+}
+
+// length of the unit starting at item i of a block ending at i1
+__device__ __forceinline__ int unit_len(const Geo& g, int i, int i1) {
+  int len = min(g.ipu, i1 - i);
+  if (g.cut) len = min(len, g.cut - i % g.cut);
+  return len;
 }
 
 __device__ __forceinline__ bool aborted(const Params& p) { return *(volatile int*)p.abort != 0; }
@@ -499,12 +525,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   const int pos = __ldcg(p.pos);  // the token of this step sits at position pos
 
   // ---------------- producer ----------------
-  if (warp == NCW) {
-    // Units of a phase are issued in batches: lane k of the warp computes the addresses of
-    // unit (batch + k), waits for that unit's slot to be free and issues its copies. A batch
-    // holds at most NS units, so no two lanes of a batch share a slot.
-    const int NSB = NS < 32 ? NS : 32;
-    long long seq = 0, issued = 0;  // units scheduled / actually issued
+  if (warp >= NCW) {
+    // Producer warp pw issues the units whose sequence number is pw mod NPW (NS is a
+    // multiple of NPW, so its units always land in its own slots). Copies from one thread
+    // are processed one after another, so whole-row units (up to 24 KB) and two issuing
+    // warps keep the stream at full bandwidth.
+    if (lane != 0) return;
+    const int pw = warp - NCW;
+    long long seq = 0, last = -1;
     bool ok = !aborted(p);
     for (int l = 0; l <= p.L && ok; ++l) {
       for (int ph = 0; ph < 5 && ok; ++ph) {
@@ -516,103 +544,65 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           continue;
         }
         const Geo g = geo(p, phase);
-        const int nl = n_local(g.n_items);
-        const int total = nl * g.U;
-        // this phase's matrices, once per phase
         const Layer* lw = p.layers + (l < p.L ? l : 0);
-        const bf16* mq = lw->wq;
-        const bf16* mk = lw->wk;
-        const bf16* mv = lw->wv;
-        const bf16* mo = lw->wo;
-        const bf16* mg = lw->wg;
-        const bf16* mu = lw->wu;
-        const bf16* md = lw->wd;
-        for (int b0 = 0; b0 < total && ok; b0 += NSB) {
-          const int k = b0 + lane;
-          const bf16* r0 = nullptr;
-          const bf16* r1 = nullptr;
-          uint32_t bytes = 0, dst_off = 0;
-          if (lane < NSB && k < total) {
-            const int j = k / g.U, u = k - j * g.U;
-            const int item = blockIdx.x + j * gridDim.x;
-            switch (phase) {
-              case P_QKV: {
-                const int half = p.hd >> 1;
-                int head = item / half;
-                const int i = item - head * half;
-                const bf16* m = mq;
-                if (head >= p.nq) { head -= p.nq; m = mk; if (head >= p.nkv) { head -= p.nkv; m = mv; } }
-                r0 = m + (size_t)(head * p.hd + i) * p.H;
-                r1 = r0 + (size_t)half * p.H;
-                break;
-              }
-              case P_OPROJ:
-                r0 = mo + (size_t)(2 * item) * g.K;
-                r1 = 2 * item + 1 < p.H ? r0 + g.K : nullptr;
-                break;
-              case P_GATEUP:
-                r0 = mg + (size_t)item * p.H;
-                r1 = mu + (size_t)item * p.H;
-                break;
-              case P_DOWN:
-                r0 = md + (size_t)item * p.I;
-                break;
-              default:
-                r0 = p.head + (size_t)(2 * item) * p.H;
-                r1 = 2 * item + 1 < p.V ? r0 + p.H : nullptr;
-                break;
+        int i0, i1;
+        item_block(g.n_items, i0, i1);
+        const uint32_t rb = (uint32_t)g.K * 2;  // bytes of a full row
+        for (int i = i0; i < i1 && ok;) {
+          const int len = unit_len(g, i, i1);
+          for (int u = 0; u < g.U && ok; ++u, ++seq) {
+            if ((int)(seq % NPW) != pw) continue;
+            const int s = (int)(seq % NS);
+            if (p.tl && blockIdx.x == 0 && pw == 0) {  // ring occupancy statistics (profiling)
+              p.tl[3 * (5 * p.L + 1) + 0] += 1;
+              if (seq >= NS && !mbar_test_now(empty0 + 8 * s, (uint32_t)(((seq / NS) - 1) & 1)))
+                p.tl[3 * (5 * p.L + 1) + 1] += 1;
             }
-            const int k0 = u * g.chunk;
-            bytes = (uint32_t)min(g.chunk, g.K - k0) * 2;
-            r0 += k0;
-            if (r1) r1 += k0;
-            dst_off = (uint32_t)g.chunk * 2;
-          }
-          // lane 0 waits for each unit's slot and issues its copies, in sequence order
-          const int n = min(NSB, total - b0);
-          for (int kk = 0; kk < n && ok; ++kk) {
-            const bf16* a0 = (const bf16*)__shfl_sync(0xffffffffu, (unsigned long long)r0, kk);
-            const bf16* a1 = (const bf16*)__shfl_sync(0xffffffffu, (unsigned long long)r1, kk);
-            const uint32_t nb = __shfl_sync(0xffffffffu, bytes, kk);
-            const uint32_t off1 = __shfl_sync(0xffffffffu, dst_off, kk);
-            bool lane_ok = true;
-            if (lane == 0) {
-              const long long sq = seq + b0 + kk;
-              const int s = (int)(sq % NS);
-              if (sq >= NS) {
-                const uint32_t par = (uint32_t)(((sq / NS) - 1) & 1);
-                if (p.tl && blockIdx.x == 0) {  // occupancy statistics of the ring (profiling)
-                  p.tl[3 * (5 * p.L + 1) + 0] += 1;
-                  if (!mbar_test_now(empty0 + 8 * s, par)) p.tl[3 * (5 * p.L + 1) + 1] += 1;
-                }
-                lane_ok = slot_wait(p, empty0 + 8 * s, par, SITE_SLOT_EMPTY, sq);
-              }
-              if (lane_ok) {
-                mbar_expect_tx(full0 + 8 * s, nb * (a1 ? 2u : 1u));
-                const uint32_t dst = ring + s * SLOT;
-                bulk_copy_g2s(dst, a0, nb, full0 + 8 * s);
-                if (a1) bulk_copy_g2s(dst + off1, a1, nb, full0 + 8 * s);
-                issued = sq + 1;
-              }
+            if (seq >= NS &&
+                !slot_wait(p, empty0 + 8 * s, (uint32_t)(((seq / NS) - 1) & 1), SITE_SLOT_EMPTY, seq)) {
+              ok = false;
+              break;
             }
-            ok = __shfl_sync(0xffffffffu, lane_ok ? 1 : 0, 0) != 0;
+            const uint32_t bar = full0 + 8 * s;
+            const uint32_t dst = ring + s * SLOT;
+            if (g.U == 1) {
+              if (g.paired) {
+                const uint32_t b = (uint32_t)len * rb;
+                mbar_expect_tx(bar, 2 * b);
+                bulk_copy_g2s(dst, item_row(p, lw, phase, i, 0), b, bar);
+                bulk_copy_g2s(dst + (uint32_t)g.ipu * rb, item_row(p, lw, phase, i, 1), b, bar);
+              } else {
+                const uint32_t b = (uint32_t)consecutive_rows(p, phase, g, i, len) * rb;
+                mbar_expect_tx(bar, b);
+                bulk_copy_g2s(dst, item_row(p, lw, phase, i, 0), b, bar);
+              }
+            } else {  // one item, K chunk u
+              const int k0 = u * g.chunk;
+              const uint32_t b = (uint32_t)min(g.chunk, g.K - k0) * 2;
+              const bf16* r0 = item_row(p, lw, phase, i, 0) + k0;
+              const bf16* r1 = nullptr;
+              if (g.paired) r1 = item_row(p, lw, phase, i, 1) + k0;
+              else if (g.rows == 2 && consecutive_rows(p, phase, g, i, 1) == 2) r1 = r0 + g.K;
+              mbar_expect_tx(bar, b * (r1 ? 2u : 1u));
+              bulk_copy_g2s(dst, r0, b, bar);
+              if (r1) bulk_copy_g2s(dst + (uint32_t)g.chunk * 2, r1, b, bar);
+            }
+            last = seq;
           }
+          i += len;
         }
-        seq += total;
-        if (p.tl && blockIdx.x == 0 && lane == 0) {
+        if (p.tl && blockIdx.x == 0 && pw == 0) {
           const int pi = l == p.L ? 5 * p.L : 5 * l + ph;
           p.tl[3 * pi + 2] = gtime();
         }
       }
     }
-    // let every issued copy land before this warp (and, with it, the CTA) may finish
-    if (lane == 0) {
-      const long long first = issued > NS ? issued - NS : 0;
-      for (long long k = first; k < issued; ++k) {
-        const int s = (int)(k % NS);
-        const long long t0 = clock64();
-        while (!mbar_test_now(full0 + 8 * s, (uint32_t)((k / NS) & 1)) && clock64() - t0 < WAIT_CYCLES) {
-        }
+    // let every copy this warp issued land before the CTA may finish
+    for (long long k = last - NS + 1 > 0 ? last - NS + 1 : 0; k <= last; ++k) {
+      if ((int)(k % NPW) != pw) continue;
+      const int s = (int)(k % NS);
+      const long long t0 = clock64();
+      while (!mbar_test_now(full0 + 8 * s, (uint32_t)((k / NS) & 1)) && clock64() - t0 < WAIT_CYCLES) {
       }
     }
     return;
@@ -628,45 +618,84 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   int best_i = -1;
   bool nonfinite = false;
 
-  // consume one weight phase: per item, accumulate over its U units, then the epilogue
+  // consume one weight phase: warp w takes every NCW-th unit of this CTA's block; per item
+  // it reduces the rows (over the chunk units of the item when K was split) and runs the
+  // epilogue
   auto run_phase = [&](int phase, int l, auto&& epilogue) -> bool {
     const Geo g = geo(p, phase);
-    const int nl = n_local(g.n_items);
+    int i0, i1;
+    item_block(g.n_items, i0, i1);
+    const size_t rb = (size_t)g.K * 2;
     bool ok = true;
-    for (int j = warp; j < nl; j += NCW) {
-      const int item = blockIdx.x + j * gridDim.x;
-      float a0 = 0.f, a1 = 0.f;
-      for (int u = 0; u < g.U; ++u) {
-        const long long seq = base + (long long)j * g.U + u;
-        const int s = (int)(seq % NS);
-        if (p.tl && blockIdx.x == 0 && threadIdx.x == 0 &&
-            !mbar_test_now(full0 + 8 * s, (uint32_t)((seq / NS) & 1)))
-          p.tl[3 * (5 * p.L + 1) + 2] += 1;
-        if (!__all_sync(0xffffffffu, slot_wait(p, full0 + 8 * s, (uint32_t)((seq / NS) & 1), SITE_SLOT_FULL, seq))) {
-          ok = false;
-          break;
-        }
-        const int k0 = u * g.chunk;
-        const int nv = min(g.chunk, g.K - k0) >> 3;
-        const uint4* w0 = reinterpret_cast<const uint4*>(dsm + (size_t)s * SLOT);
-        const uint4* w1 = reinterpret_cast<const uint4*>(dsm + (size_t)s * SLOT + g.chunk * 2);
-        const float4* x4 = reinterpret_cast<const float4*>(xs + k0);
+    long long seq = base;
+    int unit = 0;
+    for (int i = i0; i < i1; ++unit) {
+      const int len = unit_len(g, i, i1);
+      if (unit % NCW == warp && ok) {
+        float a0 = 0.f, a1 = 0.f;
+        for (int u = 0; u < g.U; ++u) {
+          const long long sq = seq + u;
+          const int s = (int)(sq % NS);
+          if (p.tl && blockIdx.x == 0 && threadIdx.x == 0 &&
+              !mbar_test_now(full0 + 8 * s, (uint32_t)((sq / NS) & 1)))
+            p.tl[3 * (5 * p.L + 1) + 2] += 1;
+          if (!__all_sync(0xffffffffu, slot_wait(p, full0 + 8 * s, (uint32_t)((sq / NS) & 1), SITE_SLOT_FULL, sq))) {
+            ok = false;
+            break;
+          }
+          const unsigned char* slot = dsm + (size_t)s * SLOT;
+          if (g.U == 1) {  // whole rows of len items
+            const int nv = g.K >> 3;
+            const float4* x4 = reinterpret_cast<const float4*>(xs);
+            for (int t = 0; t < len; ++t) {
+              const uint4* w0;
+              const uint4* w1;
+              if (g.paired) {
+                w0 = reinterpret_cast<const uint4*>(slot + t * rb);
+                w1 = reinterpret_cast<const uint4*>(slot + g.ipu * rb + t * rb);
+              } else {
+                w0 = reinterpret_cast<const uint4*>(slot + (size_t)g.rows * t * rb);
+                w1 = reinterpret_cast<const uint4*>(slot + ((size_t)g.rows * t + 1) * rb);
+              }
+              float b0 = 0.f, b1 = 0.f;
 #pragma unroll 4
-        for (int v = lane; v < nv; v += 32) {
-          const float4 xa = x4[2 * v], xb = x4[2 * v + 1];
-          const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-          a0 = dotv(w0[v], xv, a0, bf16());
-          if (g.rows == 2) a1 = dotv(w1[v], xv, a1, bf16());
+              for (int v = lane; v < nv; v += 32) {
+                const float4 xa = x4[2 * v], xb = x4[2 * v + 1];
+                const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+                b0 = dotv(w0[v], xv, b0, bf16());
+                if (g.rows == 2) b1 = dotv(w1[v], xv, b1, bf16());
+              }
+              b0 = warp_sum(b0);
+              if (g.rows == 2) b1 = warp_sum(b1);
+              if (lane == 0) epilogue(i + t, b0, b1);
+            }
+          } else {  // chunk u of one item
+            const int k0 = u * g.chunk;
+            const int nv = min(g.chunk, g.K - k0) >> 3;
+            const uint4* w0 = reinterpret_cast<const uint4*>(slot);
+            const uint4* w1 = reinterpret_cast<const uint4*>(slot + (size_t)g.chunk * 2);
+            const float4* x4 = reinterpret_cast<const float4*>(xs + k0);
+#pragma unroll 4
+            for (int v = lane; v < nv; v += 32) {
+              const float4 xa = x4[2 * v], xb = x4[2 * v + 1];
+              const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+              a0 = dotv(w0[v], xv, a0, bf16());
+              if (g.rows == 2) a1 = dotv(w1[v], xv, a1, bf16());
+            }
+          }
+          __syncwarp();
+          if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * s) : "memory");
         }
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * s) : "memory");
+        if (ok && g.U > 1) {
+          a0 = warp_sum(a0);
+          if (g.rows == 2) a1 = warp_sum(a1);
+          if (lane == 0) epilogue(i, a0, a1);
+        }
       }
-      if (!ok) break;
-      a0 = warp_sum(a0);
-      if (g.rows == 2) a1 = warp_sum(a1);
-      if (lane == 0) epilogue(item, a0, a1);
+      seq += g.U;
+      i += len;
     }
-    base += (long long)nl * g.U;
+    base = seq;
     return ok;
   };
 
@@ -824,7 +853,7 @@ int step_barriers_per_launch(const Dims& d) { return 5 * d.L + 1; }
 
 bool step_kernel_supported(const Dims& d) {
   return d.dtype == 1 && d.hd <= 128 && d.hd % 8 == 0 && d.nq / d.nkv <= step::GMAX &&
-         d.H % 8 == 0 && d.I % 8 == 0 && (size_t)step_xs_floats(d) * 4 + 16 * step::SLOT <= 220 * 1024;
+         d.H % 8 == 0 && d.I % 8 == 0 && (size_t)step_xs_floats(d) * 4 + 4 * step::SLOT <= 224 * 1024;
 }
 
 size_t step_part_bytes(const Dims& d) {
@@ -833,8 +862,9 @@ size_t step_part_bytes(const Dims& d) {
 
 cudaError_t step_set_attributes(const Dims& d, int* nslots_out, size_t* smem_out) {
   const size_t xs = (size_t)step_xs_floats(d) * 4;
-  int ns = (int)((220 * 1024 - xs) / step::SLOT);
+  int ns = (int)((224 * 1024 - xs) / step::SLOT);
   if (ns > step::MAX_SLOTS) ns = step::MAX_SLOTS;
+  ns -= ns % step::NPW;
   const size_t smem = (size_t)ns * step::SLOT + xs;
   *nslots_out = ns;
   *smem_out = smem;
