@@ -85,7 +85,7 @@ struct qw_model {
   float* step_part = nullptr;
   unsigned long long* step_bar = nullptr;
   unsigned long long step_bar_base = 0;  // barrier counter value before the next launch
-  int* step_abort = nullptr;  // [0] abort flag, [1..4] diagnostic of the first expired wait
+  int* step_abort = nullptr;  // [0] abort flag, [1..] diagnostics of expired waits
   int step_nslots = 0;
   size_t step_smem = 0;
   unsigned long long* tl_buf = nullptr;  // device timeline of one decode step (or null)
@@ -277,9 +277,17 @@ struct qw_model {
       if (h & ERR_TIMEOUT) {
         int dg[5] = {0, 0, 0, 0, 0};
         if (step_abort) cudaMemcpy(dg, step_abort, sizeof(dg), cudaMemcpyDeviceToHost);
-        char msg[160];
-        std::snprintf(msg, sizeof(msg), "device wait timed out (site %d, CTA %d, warp %d, detail %d)", dg[1],
-                      dg[2], dg[3], dg[4]);
+        std::string msg = "device wait timed out (site " + std::to_string(dg[1]) + ", CTA " +
+                          std::to_string(dg[2]) + ", warp " + std::to_string(dg[3]) + ", detail " +
+                          std::to_string(dg[4]) + ")";
+        if (step_abort) {  // per CTA: where each gave up (site, warp, detail)
+          std::vector<int> all(4 * (size_t)d.nsm);
+          cudaMemcpy(all.data(), step_abort + 5, all.size() * sizeof(int), cudaMemcpyDeviceToHost);
+          msg += "; per CTA:";
+          for (int c = 0; c < d.nsm; ++c)
+            if (all[4 * c]) msg += " " + std::to_string(c) + ":" + std::to_string(all[4 * c]) + "/" +
+                                   std::to_string(all[4 * c + 1]) + "/" + std::to_string(all[4 * c + 2]);
+        }
         return fail(QW_ERR_TIMEOUT, msg);
       }
     }
@@ -479,8 +487,9 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
       if ((e = cudaMalloc(&m->step_part, step_part_bytes(d)))) return bail(e, "cudaMalloc");
       if ((e = cudaMalloc(&m->step_bar, sizeof(unsigned long long)))) return bail(e, "cudaMalloc");
       if ((e = cudaMemset(m->step_bar, 0, sizeof(unsigned long long)))) return bail(e, "cudaMemset");
-      if ((e = cudaMalloc(&m->step_abort, 5 * sizeof(int)))) return bail(e, "cudaMalloc");
-      if ((e = cudaMemset(m->step_abort, 0, 5 * sizeof(int)))) return bail(e, "cudaMemset");
+      const size_t nd = 5 + 4 * (size_t)d.nsm;
+      if ((e = cudaMalloc(&m->step_abort, nd * sizeof(int)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMemset(m->step_abort, 0, nd * sizeof(int)))) return bail(e, "cudaMemset");
       m->use_step = true;
     }
   }

@@ -60,7 +60,8 @@ struct Params {
   int nslots;
   int xs_floats;    // floats of the staged input vector region
   unsigned long long* tl;  // timeline: per phase [start, end, producer issued] (CTA 0), or null
-  int* diag;               // first expired wait: [site, CTA, warp, detail]
+  int* diag;               // [0..3] first expired wait (site, CTA, warp, detail); then per CTA
+                           // the first wait that gave up: [4 + 4c ..] (site, warp, detail, phase)
 };
 
 constexpr int MAX_SPLIT = 16;
@@ -121,6 +122,24 @@ __device__ __forceinline__ const bf16* item_row(const Params& p, const Layer* lw
   }
 }
 
+// The weight tensor an item row lives in (base, elements), for the copy checks.
+__device__ __forceinline__ void item_tensor(const Params& p, const Layer* lw, int ph, int item, int seg,
+                                            const bf16*& base, size_t& elems) {
+  switch (ph) {
+    case P_QKV: {
+      const int head = item / (p.hd >> 1);
+      if (head < p.nq) { base = lw->wq; elems = (size_t)p.nq * p.hd * p.H; }
+      else if (head < p.nq + p.nkv) { base = lw->wk; elems = (size_t)p.nkv * p.hd * p.H; }
+      else { base = lw->wv; elems = (size_t)p.nkv * p.hd * p.H; }
+      return;
+    }
+    case P_OPROJ: base = lw->wo; elems = (size_t)p.H * p.nq * p.hd; return;
+    case P_GATEUP: base = seg == 0 ? lw->wg : lw->wu; elems = (size_t)p.I * p.H; return;
+    case P_DOWN: base = lw->wd; elems = (size_t)p.H * p.I; return;
+    default: base = p.head; elems = (size_t)p.V * p.H; return;
+  }
+}
+
 // rows of the (non-paired) items [i, i + n) that exist: the last pair of an odd-sized
 // matrix has one row
 __device__ __forceinline__ int consecutive_rows(const Params& p, int ph, const Geo& g, int i, int n) {
@@ -144,9 +163,26 @@ __device__ __forceinline__ int unit_len(const Geo& g, int i, int i1) {
 
 __device__ __forceinline__ bool aborted(const Params& p) { return *(volatile int*)p.abort != 0; }
 
-enum : int { SITE_SLOT_FULL = 1, SITE_SLOT_EMPTY = 2, SITE_GRID = 3 };
+enum : int {
+  SITE_SLOT_FULL = 1,
+  SITE_SLOT_EMPTY = 2,
+  SITE_GRID = 3,
+  SITE_COPY = 4,
+  SITE_SMEM = 5,
+  SITE_STORE = 6,
+  SITE_SLOT_REUSE = 7
+};
 
-// First expiry wins the diagnostic record; every later wait sees the abort flag.
+// Per CTA, the first wait that gave up (expired, or saw another CTA's abort).
+__device__ __forceinline__ void note_giveup(const Params& p, int site, long long detail) {
+  if (!p.diag) return;
+  int* d = p.diag + 4 + 4 * blockIdx.x;
+  if (atomicCAS(d, 0, site) == 0) {
+    d[1] = threadIdx.x >> 5;
+    d[2] = (int)detail;
+  }
+}
+// First expiry wins the global record; every later wait sees the abort flag.
 __device__ __forceinline__ void raise_abort(const Params& p, int site, long long detail) {
   if (atomicExch(p.abort, 1) == 0 && p.diag) {
     p.diag[0] = site;
@@ -154,7 +190,24 @@ __device__ __forceinline__ void raise_abort(const Params& p, int site, long long
     p.diag[2] = threadIdx.x >> 5;
     p.diag[3] = (int)detail;
   }
+  note_giveup(p, site, detail);
   atomicOr(p.err, ERR_TIMEOUT);
+}
+
+// Bulk copy with its source checked against the weight tensor it must lie in and its
+// destination against the ring; a violation is recorded, the copy skipped, and the launch
+// aborted (so no wait is left hanging on the missing bytes).
+__device__ __forceinline__ bool checked_copy(const Params& p, uint32_t dst, const bf16* src, uint32_t bytes,
+                                             uint32_t bar, const bf16* tbase, size_t telems, uint32_t ring_lo,
+                                             uint32_t ring_hi, long long detail) {
+  const bool ok = bytes > 0 && (bytes & 15) == 0 && ((uintptr_t)src & 15) == 0 && (dst & 15) == 0 &&
+                  src >= tbase && src + bytes / 2 <= tbase + telems && dst >= ring_lo && dst + bytes <= ring_hi;
+  if (!ok) {
+    raise_abort(p, SITE_COPY, detail);
+    return false;
+  }
+  bulk_copy_g2s(dst, src, bytes, bar);
+  return true;
 }
 
 // Bounded wait (non-blocking tests) that also gives up when another CTA has aborted.
@@ -165,9 +218,36 @@ __device__ __forceinline__ bool slot_wait(const Params& p, uint32_t bar, uint32_
   for (int it = 0;; ++it) {
     if (mbar_test_now(bar, parity)) return true;
     if ((it & 63) == 0) {
-      if (aborted(p)) return false;
+      if (aborted(p)) {
+        note_giveup(p, site + 10, detail);
+        return false;
+      }
       if (clock64() - t0 > WAIT_CYCLES) {
         raise_abort(p, site, detail);
+        return false;
+      }
+    }
+  }
+}
+
+// A consumer may test a slot's full barrier for unit seq only once the slot's previous unit
+// (seq - NS) has been released: before that the barrier is still in the previous unit's
+// phase, whose parity is the opposite one, and the parity test would pass at once. With
+// fewer slots than consumer warps that previous unit belongs to another warp, so the
+// releases are published per slot in shared memory (monotonic: a slot's units are
+// released in order, each copy waiting for the previous release).
+__device__ __forceinline__ bool reuse_wait(const Params& p, const volatile int* rel, int want, long long detail) {
+  if (*rel >= want) return true;
+  const long long t0 = clock64();
+  for (int it = 0;; ++it) {
+    if (*rel >= want) return true;
+    if ((it & 63) == 0) {
+      if (aborted(p)) {
+        note_giveup(p, SITE_SLOT_REUSE + 10, detail);
+        return false;
+      }
+      if (clock64() - t0 > WAIT_CYCLES) {
+        raise_abort(p, SITE_SLOT_REUSE, detail);
         return false;
       }
     }
@@ -208,6 +288,7 @@ __device__ bool grid_barrier(const Params& p, int& b) {
       if (v >= target) break;
       if ((it & 15) == 0 && (aborted(p) || clock64() - t0 > WAIT_CYCLES)) {
         if (!aborted(p)) raise_abort(p, SITE_GRID, b);
+        else note_giveup(p, SITE_GRID + 10, (long long)b * 100000 + (long long)(v - p.bar_base));
         ok = 0;
         break;
       }
@@ -508,6 +589,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   __shared__ float scratch[32];
   __shared__ unsigned long long s_key[NCW];
   __shared__ int s_bad[NCW];
+  __shared__ int rel[MAX_SLOTS];  // per slot: sequence number of the last released unit
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = p.nslots;
   float* xs = reinterpret_cast<float*>(dsm + (size_t)NS * SLOT);
@@ -518,6 +600,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
+      rel[s] = -1;
     }
     mbar_fence_init();
   }
@@ -565,16 +648,25 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
             }
             const uint32_t bar = full0 + 8 * s;
             const uint32_t dst = ring + s * SLOT;
+            const uint32_t rlo = ring, rhi = ring + (uint32_t)NS * SLOT;
+            const bf16* tb0;
+            const bf16* tb1;
+            size_t te0, te1;
+            item_tensor(p, lw, phase, i, 0, tb0, te0);
+            item_tensor(p, lw, phase, i, 1, tb1, te1);
+            const long long dt = seq * 1000 + phase;
+            bool cok = true;
             if (g.U == 1) {
               if (g.paired) {
                 const uint32_t b = (uint32_t)len * rb;
                 mbar_expect_tx(bar, 2 * b);
-                bulk_copy_g2s(dst, item_row(p, lw, phase, i, 0), b, bar);
-                bulk_copy_g2s(dst + (uint32_t)g.ipu * rb, item_row(p, lw, phase, i, 1), b, bar);
+                cok = checked_copy(p, dst, item_row(p, lw, phase, i, 0), b, bar, tb0, te0, rlo, rhi, dt) &&
+                      checked_copy(p, dst + (uint32_t)g.ipu * rb, item_row(p, lw, phase, i, 1), b, bar, tb1, te1,
+                                   rlo, rhi, dt);
               } else {
                 const uint32_t b = (uint32_t)consecutive_rows(p, phase, g, i, len) * rb;
                 mbar_expect_tx(bar, b);
-                bulk_copy_g2s(dst, item_row(p, lw, phase, i, 0), b, bar);
+                cok = checked_copy(p, dst, item_row(p, lw, phase, i, 0), b, bar, tb0, te0, rlo, rhi, dt);
               }
             } else {  // one item, K chunk u
               const int k0 = u * g.chunk;
@@ -584,8 +676,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
               if (g.paired) r1 = item_row(p, lw, phase, i, 1) + k0;
               else if (g.rows == 2 && consecutive_rows(p, phase, g, i, 1) == 2) r1 = r0 + g.K;
               mbar_expect_tx(bar, b * (r1 ? 2u : 1u));
-              bulk_copy_g2s(dst, r0, b, bar);
-              if (r1) bulk_copy_g2s(dst + (uint32_t)g.chunk * 2, r1, b, bar);
+              cok = checked_copy(p, dst, r0, b, bar, tb0, te0, rlo, rhi, dt);
+              if (cok && r1)
+                cok = checked_copy(p, dst + (uint32_t)g.chunk * 2, r1, b, bar, g.paired ? tb1 : tb0, g.paired ? te1 : te0,
+                                   rlo, rhi, dt);
+            }
+            if (!cok) {
+              ok = false;
+              break;
             }
             last = seq;
           }
@@ -639,11 +737,25 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (p.tl && blockIdx.x == 0 && threadIdx.x == 0 &&
               !mbar_test_now(full0 + 8 * s, (uint32_t)((sq / NS) & 1)))
             p.tl[3 * (5 * p.L + 1) + 2] += 1;
+          if (sq >= NS && !__all_sync(0xffffffffu, reuse_wait(p, rel + s, (int)(sq - NS), sq))) {
+            ok = false;
+            break;
+          }
           if (!__all_sync(0xffffffffu, slot_wait(p, full0 + 8 * s, (uint32_t)((sq / NS) & 1), SITE_SLOT_FULL, sq))) {
             ok = false;
             break;
           }
           const unsigned char* slot = dsm + (size_t)s * SLOT;
+          {  // the rows this unit reads must lie inside its slot, x inside the staged vector
+            const size_t need = g.U == 1 ? (g.paired ? (size_t)(g.ipu + len) * rb : (size_t)g.rows * len * rb)
+                                         : (size_t)g.rows * g.chunk * 2;
+            const int xneed = g.U == 1 ? g.K : u * g.chunk + min(g.chunk, g.K - u * g.chunk);
+            if (need > (size_t)SLOT || xneed > p.xs_floats) {
+              if (lane == 0) raise_abort(p, SITE_SMEM, sq * 1000 + phase);
+              ok = false;
+              break;
+            }
+          }
           if (g.U == 1) {  // whole rows of len items
             const int nv = g.K >> 3;
             const float4* x4 = reinterpret_cast<const float4*>(xs);
@@ -684,7 +796,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
             }
           }
           __syncwarp();
-          if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * s) : "memory");
+          if (lane == 0) {
+            *(volatile int*)(rel + s) = (int)sq;
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * s) : "memory");
+          }
         }
         if (ok && g.U > 1) {
           a0 = warp_sum(a0);
@@ -724,6 +839,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         a += __bfloat162float(bias[h * p.hd + i]);
         b += __bfloat162float(bias[h * p.hd + i + half]);
       }
+      if (item < 0 || item >= (p.nq + 2 * p.nkv) * half || pos < 0 || pos >= p.cap) {
+        raise_abort(p, SITE_STORE, item);
+        return;
+      }
       if (head < p.nq + p.nkv) {
         const float2 cs = p.rope[(size_t)pos * half + i];
         const float ra = a * cs.x - b * cs.y, rb = b * cs.x + a * cs.y;
@@ -759,6 +878,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     stamp(0);
     merge_partials(p, xs, nsplit);
     ok = cbar_and(run_phase(P_OPROJ, l, [&](int item, float a, float b) {
+      if (item < 0 || 2 * item >= p.H) { raise_abort(p, SITE_STORE, 100000 + item); return; }
       atomicAdd(p.x + 2 * item, a);
       if (2 * item + 1 < p.H) atomicAdd(p.x + 2 * item + 1, b);
     }));
@@ -770,6 +890,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     stamp(0);
     stage_norm(p, xs, scratch, p.x, w.post_norm, p.H);
     ok = cbar_and(run_phase(P_GATEUP, l, [&](int item, float gt, float up) {
+      if (item < 0 || item >= p.I) { raise_abort(p, SITE_STORE, 200000 + item); return; }
       p.act[item] = (gt / (1.f + expf(-gt))) * up;
     }));
     stamp(1);
@@ -779,7 +900,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     // ---- DOWN
     stamp(0);
     stage_copy(xs, p.act, p.I);
-    ok = cbar_and(run_phase(P_DOWN, l, [&](int item, float a, float) { atomicAdd(p.x + item, a); }));
+    ok = cbar_and(run_phase(P_DOWN, l, [&](int item, float a, float) {
+      if (item < 0 || item >= p.H) { raise_abort(p, SITE_STORE, 300000 + item); return; }
+      atomicAdd(p.x + item, a);
+    }));
     stamp(1);
     ++phase_no;
     if (!(ok = ok && grid_barrier(p, gen))) break;
@@ -790,6 +914,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     stamp(0);
     stage_norm(p, xs, scratch, p.x, p.final_norm, p.H);
     auto take = [&](int r, float v) {
+      if (r < 0 || r >= p.V) { raise_abort(p, SITE_STORE, 400000 + r); return; }
       p.logits[r] = v;
       if (!isfinite(v)) nonfinite = true;
       if (v > best_v || best_i < 0) {  // a warp sees its rows in increasing order
