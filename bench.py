@@ -179,6 +179,14 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def decode_launches_per_token(s):
+    """Kernels one decode step launches: the persistent step kernel (QW_STEP_KERNEL=1), or
+    embedding, 5 per layer and the LM head."""
+    if os.environ.get("QW_STEP_KERNEL") == "1":
+        return 1
+    return 5 * s.n_layers + 2
+
+
 def timeline_per_kernel(m, s, ids_dev, prompt, rank):
     """Device timeline of single decode steps run as one kernel per operation: per kernel
     kind, the gap from the previous kernel's end to this kernel's dependency release, the
@@ -300,7 +308,7 @@ def run_native(args):
 
     if args.timeline:
         # device timeline of single decode steps
-        if os.environ.get("QW_STEP_KERNEL", "1") != "0":
+        if os.environ.get("QW_STEP_KERNEL") == "1":
             m.set_timeline(True)
             m.prefill_device(ids_dev.data_ptr(), len(prompt))
             # persistent step kernel: per phase [start, end, producer issued] of the first CTA
@@ -388,7 +396,7 @@ def run_native(args):
                     "d2h_bytes_per_step": 4 * wl.new_tokens + 4,
                     "how": "qw_generate with host buffers minus qw_prefill with host buffers, host wall clock",
                     "generate_ms": 1000 * float(np.mean(t_gen)), "ttft_ms": 1000 * float(np.mean(t_pref))},
-            "gpu_launches": args.steps * ((2 + 12 * s.n_layers) + (5 * s.n_layers + 2) * n_dec),
+            "gpu_launches": args.steps * ((2 + 12 * s.n_layers) + decode_launches_per_token(s) * n_dec),
             "clocks": clk.summary(),
             "host_ms_per_step": 1000 * t_host / args.steps,
             "source_hash": src,

@@ -187,6 +187,8 @@ const char *qw_last_error(void);
  *   workspace device, at least qw_op_decode_attention_workspace() bytes, 16-byte
  *        aligned; its counters must be zero before the first call (cudaMemset) and the
  *        call leaves them zero again.
+ * Shapes: head_dim a multiple of 8, at most 8 query heads per KV head and
+ * (n_heads / n_kv_heads) * head_dim <= 1024; others return QW_ERR_UNSUPPORTED.
  * Runs on cuda_stream (NULL = default stream) and does not synchronise. */
 size_t qw_op_decode_attention_workspace(int32_t n_heads, int32_t n_kv_heads,
                                         int32_t head_dim, int32_t max_ctx);

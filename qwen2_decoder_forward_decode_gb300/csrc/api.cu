@@ -87,6 +87,7 @@ struct qw_model {
   unsigned long long step_bar_base = 0;  // barrier counter value before the next launch
   int* step_abort = nullptr;  // [0] abort flag, [1..] diagnostics of expired waits
   int step_nslots = 0;
+  int step_slot = 0;
   size_t step_smem = 0;
   unsigned long long* tl_buf = nullptr;  // device timeline of one decode step (or null)
   int tl_n = 0;                          // launches per decode step
@@ -193,6 +194,7 @@ struct qw_model {
     a.diag = step_abort + 1;
     a.err = err;
     a.nslots = step_nslots;
+    a.slot = step_slot;
     a.grid = d.nsm;
     a.smem = step_smem;
     a.tl = tl_buf;
@@ -468,11 +470,16 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
   }
   if ((e = decode_set_attributes(d))) return bail(e, "decode attributes");
   {
+    // decode path: one kernel per operation (default), or the persistent step kernel
+    // (QW_STEP_KERNEL=1) where the shape supports it
     const char* sk = std::getenv("QW_STEP_KERNEL");
     int coop = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device);
-    if (step_kernel_supported(d) && coop && !(sk && sk[0] == '0')) {
-      if ((e = step_set_attributes(d, &m->step_nslots, &m->step_smem))) return bail(e, "step attributes");
+    if (step_kernel_supported(d) && coop && sk && sk[0] == '1') {
+      const char* skb = std::getenv("QW_STEP_SLOT_KB");  // ring slot size (tuning knob)
+      const int slot_bytes = skb ? (int)(std::atof(skb) * 1024) : 0;
+      if ((e = step_set_attributes(d, slot_bytes, &m->step_slot, &m->step_nslots, &m->step_smem)))
+        return bail(e, "step attributes");
       std::vector<StepLayer> sl(d.L);
       for (int l = 0; l < d.L; ++l) {
         const LayerPtrs& w = m->layers[l];
@@ -768,6 +775,8 @@ qw_status qw_op_decode_attention(int32_t kv_dtype, int32_t n_heads, int32_t n_kv
   if (n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || head_dim < 2 || ctx < 1 || kv_stride < ctx)
     return fail(QW_ERR_INVALID_ARG, "bad attention shape");
   if (n_heads / n_kv_heads > 8) return fail(QW_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+  if (head_dim % 8 || (n_heads / n_kv_heads) * head_dim > 1024)
+    return fail(QW_ERR_UNSUPPORTED, "head_dim must be a multiple of 8 with (n_heads / n_kv_heads) * head_dim <= 1024");
   const int nsplit = op_attn_nsplit(head_dim, kv_stride, kv_dtype == QW_F16 ? 2 : 4);
   const size_t need = attn_workspace_bytes(n_heads, n_kv_heads, head_dim, nsplit);
   if (workspace_bytes < need) return fail(QW_ERR_INVALID_ARG, "workspace too small");

@@ -26,90 +26,153 @@ struct AttnArgs {
 };
 
 // One CTA per (KV head, context chunk). The CTA copies q of its g query heads and the K and
-// V rows of its chunk into shared memory with one batch of 16-byte loads, scores the chunk
-// for all g heads (each K row read once for g heads), and keeps (max, sum of exp,
-// unnormalised output) per head. The last CTA of the KV head to finish merges the chunks
-// in chunk order (deterministic log-sum-exp combine).
+// V rows of its chunk into shared memory with one batch of 16-byte loads, then:
+//   scores  8 lanes per position, each summing over every 8th 16-byte vector of the row for
+//           all g heads at once (each K row read once), the 8 partial dot products added
+//           with 3 shuffles;
+//   softmax a warp per head: running max and sum of exp over the chunk;
+//   values  a thread per (position group, head, 16-byte vector of the row), accumulating
+//           with independent lanes of the vector, the position groups added in shared memory.
+// The unnormalised output, max and sum of every chunk go to the workspace; the last CTA of
+// the KV head to finish merges the chunks (deterministic log-sum-exp combine) with every
+// value it reads requested before the first is used.
 constexpr int ATTN_THREADS = 256;
 constexpr int COPY_BATCH = 8;
+constexpr int RED_FLOATS = ATTN_THREADS * 8;  // position-group partial sums of the values
+constexpr int MERGE_BATCH = 8;                // chunks merged per batch of loads
+
+template <typename KV> struct KVec;
+template <> struct KVec<f16> {
+  static constexpr int N = 8;
+  __device__ static void unpack(const uint4& r, float* f) {
+    const __half2* h = reinterpret_cast<const __half2*>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __half22float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+};
+template <> struct KVec<float> {
+  static constexpr int N = 4;
+  __device__ static void unpack(const uint4& r, float* f) {
+    f[0] = __uint_as_float(r.x);
+    f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z);
+    f[3] = __uint_as_float(r.w);
+  }
+};
 
 template <typename KV>
 __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArgs<KV> a) {
   extern __shared__ __align__(16) float sm[];
   __shared__ bool s_last;
+  constexpr int EV = KVec<KV>::N;  // KV elements per 16-byte vector
   const int g = blockIdx.x, split = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  const int G = a.group, hd = a.hd;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = ATTN_THREADS >> 5;
+  const int G = a.group, hd = a.hd, NV = hd / EV;
   tl_stamp(a.tl, 0);
-  pdl_wait();
-  pdl_trigger();
-  tl_stamp(a.tl, 1);
+  // The context length and every K/V row but the newest were written before this decode
+  // step began (the position by the previous step's LM head, the rows by earlier steps):
+  // they are read before the dependency wait, which only the query and the newest row
+  // (written by the projections just before) have to follow.
   const int ctx = a.d_pos ? __ldcg(a.d_pos) + 1 : a.ctx_host;
   const int chunk = max(a.chunk_min, (ctx + a.nsplit_max - 1) / a.nsplit_max);
   const int nsplit = (ctx + chunk - 1) / chunk;
-  if (split >= nsplit) {
-    tl_stamp(a.tl, 2);
-    return;
-  }
+  if (split >= nsplit) return;  // an exited CTA counts as triggered
   const int j0 = split * chunk, j1 = min(ctx, j0 + chunk), n = j1 - j0;
-  // shared layout: q [G][hd] f32 | scores [G][chunk] f32 | stats [G][2] | weights [G][nsplit_max]
-  //                | K [chunk][hd] KV | V [chunk][hd] KV
+  const int n_old = j1 == ctx ? n - 1 : n;  // rows of the chunk written by earlier steps
+  // shared layout: q [G][hd] | scores [G][chunk] | stats [G][2] | merge (m, l) [2][G][nsplit_max]
+  //                | value partials [RED_FLOATS] | K [chunk][hd] KV | V [chunk][hd] KV
   float* qs = sm;
   float* sc = qs + G * hd;
   float* st = sc + G * chunk;
-  float* wts = st + 2 * G;
-  const int kv_off = (G * hd + G * chunk + 2 * G + G * a.nsplit_max + 3) & ~3;  // 16-byte aligned
+  float* mw = st + 2 * G;
+  float* red = mw + 2 * G * a.nsplit_max;
+  const int kv_off = (G * hd + G * chunk + 2 * G + 2 * G * a.nsplit_max + RED_FLOATS + 3) & ~3;
   KV* ks = reinterpret_cast<KV*>(sm + kv_off);
   KV* vs = ks + (size_t)chunk * hd;
+  const uint4* ksrc = reinterpret_cast<const uint4*>(a.k + ((size_t)g * a.stride + j0) * hd);
+  const uint4* vsrc = reinterpret_cast<const uint4*>(a.v + ((size_t)g * a.stride + j0) * hd);
+  uint4* kdst = reinterpret_cast<uint4*>(ks);
+  uint4* vdst = reinterpret_cast<uint4*>(vs);
   {
-    const int qv = G * hd / 4;                               // 16-byte vectors of q
-    const int kvv = n * hd * (int)sizeof(KV) / 16;           // of the K (and the V) rows
-    const int total = qv + 2 * kvv;
-    const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (size_t)g * G * hd);
-    const uint4* ksrc = reinterpret_cast<const uint4*>(a.k + ((size_t)g * a.stride + j0) * hd);
-    const uint4* vsrc = reinterpret_cast<const uint4*>(a.v + ((size_t)g * a.stride + j0) * hd);
-    uint4* qdst = reinterpret_cast<uint4*>(qs);
-    uint4* kdst = reinterpret_cast<uint4*>(ks);
-    uint4* vdst = reinterpret_cast<uint4*>(vs);
-    for (int base = tid; base < total; base += COPY_BATCH * blockDim.x) {
+    const int kvv = n_old * NV;  // 16-byte vectors of the K (and the V) rows
+    for (int base = tid; base < 2 * kvv; base += COPY_BATCH * ATTN_THREADS) {
       uint4 r[COPY_BATCH];
 #pragma unroll
       for (int i = 0; i < COPY_BATCH; ++i) {
-        const int j = base + i * blockDim.x;
-        if (j < qv) r[i] = __ldcg(qsrc + j);
-        else if (j < qv + kvv) r[i] = __ldcg(ksrc + (j - qv));
-        else if (j < total) r[i] = __ldcg(vsrc + (j - qv - kvv));
+        const int j = base + i * ATTN_THREADS;
+        if (j < kvv) r[i] = __ldcg(ksrc + j);
+        else if (j < 2 * kvv) r[i] = __ldcg(vsrc + (j - kvv));
       }
 #pragma unroll
       for (int i = 0; i < COPY_BATCH; ++i) {
-        const int j = base + i * blockDim.x;
-        if (j < qv) qdst[j] = r[i];
-        else if (j < qv + kvv) kdst[j - qv] = r[i];
-        else if (j < total) vdst[j - qv - kvv] = r[i];
+        const int j = base + i * ATTN_THREADS;
+        if (j < kvv) kdst[j] = r[i];
+        else if (j < 2 * kvv) vdst[j - kvv] = r[i];
       }
     }
   }
-  __syncthreads();
-  // scores: a warp per position, lanes over the head dimension
-  for (int jj = warp; jj < n; jj += nwarps) {
-    float part[GMAX];
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h) part[h] = 0.f;
-    for (int dd = lane; dd < hd; dd += 32) {
-      const float kv = to_f32(ks[jj * hd + dd]);
-#pragma unroll
-      for (int h = 0; h < GMAX; ++h)
-        if (h < G) part[h] = fmaf(qs[h * hd + dd], kv, part[h]);
+  pdl_wait();
+  pdl_trigger();
+  tl_stamp(a.tl, 1);
+  {  // q of the G heads and, in the last chunk, the newest K/V row
+    const int qv = G * hd / 4;
+    const int nv_new = n_old < n ? NV : 0;
+    const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (size_t)g * G * hd);
+    uint4* qdst = reinterpret_cast<uint4*>(qs);
+    for (int j = tid; j < qv + 2 * nv_new; j += ATTN_THREADS) {
+      if (j < qv) qdst[j] = __ldcg(qsrc + j);
+      else if (j < qv + nv_new) kdst[n_old * NV + (j - qv)] = __ldcg(ksrc + n_old * NV + (j - qv));
+      else vdst[n_old * NV + (j - qv - nv_new)] = __ldcg(vsrc + n_old * NV + (j - qv - nv_new));
     }
+  }
+  __syncthreads();
+
+  // ---- scores: position jb + tid / 8, vectors (tid % 8) + 8 i of its K row
+  const int p8 = lane & 7;
+  for (int jb = 0; jb < n; jb += ATTN_THREADS / 8) {
+    const int jj = jb + (tid >> 3);
+    float dot[GMAX];
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) dot[h] = 0.f;
+    if (jj < n) {
+      const uint4* krow = reinterpret_cast<const uint4*>(ks + (size_t)jj * hd);
+      for (int v = p8; v < NV; v += 8) {
+        float kf[EV];
+        KVec<KV>::unpack(krow[v], kf);
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          if (h < G) {
+            const float4* q4 = reinterpret_cast<const float4*>(qs + h * hd + v * EV);
+#pragma unroll
+            for (int e4 = 0; e4 < EV / 4; ++e4) {
+              const float4 t = q4[e4];
+              dot[h] = fmaf(t.x, kf[4 * e4], fmaf(t.y, kf[4 * e4 + 1],
+                       fmaf(t.z, kf[4 * e4 + 2], fmaf(t.w, kf[4 * e4 + 3], dot[h]))));
+            }
+          }
+        }
+      }
+    }
+    float mine = 0.f;  // lane p8 keeps the score of head p8
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) {
       if (h < G) {
-        const float sv = warp_sum(part[h]);
-        if (lane == 0) sc[h * chunk + jj] = sv * a.scale;
+        float d = dot[h];
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        if (p8 == h) mine = d;
       }
     }
+    if (jj < n && p8 < G) sc[p8 * chunk + jj] = mine * a.scale;
   }
   __syncthreads();
+
+  // ---- softmax statistics of the chunk, a warp per head
   for (int h = warp; h < G; h += nwarps) {
     float m = -INFINITY;
     for (int jj = lane; jj < n; jj += 32) m = fmaxf(m, sc[h * chunk + jj]);
@@ -127,12 +190,44 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
     }
   }
   __syncthreads();
+
+  // ---- values: thread (pg, h, v) sums positions pg, pg + PG, ... of head h, vector v
+  const int units = G * NV;  // <= ATTN_THREADS since G * hd <= 1024
+  const int PG = ATTN_THREADS / units;
+  const int t_pg = tid / units, t_u = tid - t_pg * units;
+  const int th = t_u / NV, tv = t_u - th * NV;
+  float acc[EV];
+#pragma unroll
+  for (int e = 0; e < EV; ++e) acc[e] = 0.f;
+  if (t_pg < PG) {
+    const uint4* vcol = reinterpret_cast<const uint4*>(vs) + tv;
+    const float* ph = sc + th * chunk;
+    for (int jj = t_pg; jj < n; jj += PG) {
+      float vf[EV];
+      KVec<KV>::unpack(vcol[(size_t)jj * NV], vf);
+      const float pj = ph[jj];
+#pragma unroll
+      for (int e = 0; e < EV; ++e) acc[e] = fmaf(pj, vf[e], acc[e]);
+    }
+    if (PG > 1) {
+#pragma unroll
+      for (int e = 0; e < EV; ++e) red[tid * EV + e] = acc[e];
+    }
+  }
+  if (PG > 1) {
+    __syncthreads();
+    if (tid < units) {
+      for (int pg = 1; pg < PG; ++pg) {
+#pragma unroll
+        for (int e = 0; e < EV; ++e) acc[e] += red[(pg * units + tid) * EV + e];
+      }
+    }
+  }
   const int pstride = hd + 2;
-  for (int idx = tid; idx < G * hd; idx += blockDim.x) {
-    const int h = idx / hd, dd = idx - h * hd;
-    float acc = 0.f;
-    for (int jj = 0; jj < n; ++jj) acc = fmaf(sc[h * chunk + jj], to_f32(vs[jj * hd + dd]), acc);
-    a.part[((size_t)(g * G + h) * a.nsplit_max + split) * pstride + dd] = acc;
+  if (tid < units) {
+    float* dst = a.part + ((size_t)(g * G + th) * a.nsplit_max + split) * pstride + tv * EV;
+#pragma unroll
+    for (int e = 0; e < EV; ++e) dst[e] = acc[e];
   }
   if (tid < G) {
     float* p = a.part + ((size_t)(g * G + tid) * a.nsplit_max + split) * pstride;
@@ -148,58 +243,66 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
     return;
   }
   __threadfence();
-  // merge: weights w_s = exp(m_s - M) / sum_s l_s exp(m_s - M) per head, then out = sum_s w_s O_s
-  for (int i = tid; i < G * nsplit; i += blockDim.x) {
+
+  // ---- merge: w_s = exp(m_s - M) / sum_s l_s exp(m_s - M) per head, out = sum_s w_s O_s.
+  // The first batch of partial outputs is requested before the (m, l) pairs are read.
+  constexpr int EPT = GMAX * 128 / ATTN_THREADS;  // output elements per thread (G*hd <= 1024)
+  const float* pbase = a.part + (size_t)g * G * a.nsplit_max * pstride;
+  float vals[EPT][MERGE_BATCH];
+  auto load_batch = [&](int s0) {
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const int idx = tid + k * ATTN_THREADS;
+      const int h = idx / hd, dd = idx - h * hd;
+#pragma unroll
+      for (int u = 0; u < MERGE_BATCH; ++u)
+        vals[k][u] = (idx < G * hd && s0 + u < nsplit)
+                         ? __ldcg(pbase + ((size_t)h * a.nsplit_max + s0 + u) * pstride + dd)
+                         : 0.f;
+    }
+  };
+  load_batch(0);
+  for (int i = tid; i < G * nsplit; i += ATTN_THREADS) {  // (m, l) of every (head, chunk)
     const int h = i / nsplit, sp = i - h * nsplit;
-    const float* p = a.part + ((size_t)(g * G + h) * a.nsplit_max + sp) * pstride + hd;
-    wts[h * a.nsplit_max + sp] = __ldcg(p);  // m_s
+    const float* p = pbase + ((size_t)h * a.nsplit_max + sp) * pstride + hd;
+    const float m = __ldcg(p), l = __ldcg(p + 1);
+    mw[h * a.nsplit_max + sp] = m;
+    mw[(G + h) * a.nsplit_max + sp] = l;
   }
   __syncthreads();
   for (int h = warp; h < G; h += nwarps) {
     float M = -INFINITY;
-    for (int sp = lane; sp < nsplit; sp += 32) M = fmaxf(M, wts[h * a.nsplit_max + sp]);
+    for (int sp = lane; sp < nsplit; sp += 32) M = fmaxf(M, mw[h * a.nsplit_max + sp]);
     M = warp_max(M);
     float L = 0.f;
     for (int sp = lane; sp < nsplit; sp += 32) {
-      const float* p = a.part + ((size_t)(g * G + h) * a.nsplit_max + sp) * pstride + hd;
-      const float w = expf(wts[h * a.nsplit_max + sp] - M);
-      wts[h * a.nsplit_max + sp] = w;
-      L = fmaf(__ldcg(p + 1), w, L);
+      const float w = expf(mw[h * a.nsplit_max + sp] - M);
+      mw[h * a.nsplit_max + sp] = w;
+      L = fmaf(mw[(G + h) * a.nsplit_max + sp], w, L);
     }
     L = warp_sum(L);
     const float inv = 1.f / L;
-    for (int sp = lane; sp < nsplit; sp += 32) wts[h * a.nsplit_max + sp] *= inv;
+    for (int sp = lane; sp < nsplit; sp += 32) mw[h * a.nsplit_max + sp] *= inv;
   }
   __syncthreads();
-  constexpr int EPT = GMAX * 128 / ATTN_THREADS;  // output elements per thread (G*hd <= 1024)
-  float acc[EPT];
+  float out[EPT];
 #pragma unroll
-  for (int k = 0; k < EPT; ++k) acc[k] = 0.f;
-  for (int s0 = 0; s0 < nsplit; s0 += 4) {
-    float v[EPT][4];
-#pragma unroll
-    for (int k = 0; k < EPT; ++k) {
-      const int idx = tid + k * blockDim.x;
-      const int h = idx / hd, dd = idx - h * hd;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        v[k][u] = (idx < G * hd && s0 + u < nsplit)
-                      ? __ldcg(a.part + ((size_t)(g * G + h) * a.nsplit_max + s0 + u) * pstride + dd)
-                      : 0.f;
-    }
+  for (int k = 0; k < EPT; ++k) out[k] = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += MERGE_BATCH) {
+    if (s0) load_batch(s0);
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
-      const int idx = tid + k * blockDim.x;
+      const int idx = tid + k * ATTN_THREADS;
       const int h = idx / hd;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (idx < G * hd && s0 + u < nsplit) acc[k] = fmaf(v[k][u], wts[h * a.nsplit_max + s0 + u], acc[k]);
+      for (int u = 0; u < MERGE_BATCH; ++u)
+        if (idx < G * hd && s0 + u < nsplit) out[k] = fmaf(vals[k][u], mw[h * a.nsplit_max + s0 + u], out[k]);
     }
   }
 #pragma unroll
   for (int k = 0; k < EPT; ++k) {
-    const int idx = tid + k * blockDim.x;
-    if (idx < G * hd) a.out[(size_t)g * G * hd + idx] = acc[k];
+    const int idx = tid + k * ATTN_THREADS;
+    if (idx < G * hd) a.out[(size_t)g * G * hd + idx] = out[k];
   }
   if (tid == 0) a.counter[g] = 0u;
   tl_stamp(a.tl, 2);
@@ -231,8 +334,8 @@ int attn_nsplit_for(int cap, int chunk_min, int hd, int kv_bytes) {
 size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min, int kv_bytes) {
   int chunk = (cap + nsplit - 1) / nsplit;
   if (chunk < chunk_min) chunk = chunk_min;
-  const size_t f = ((size_t)group * hd + (size_t)group * chunk + 2 * group + (size_t)group * nsplit + 3) &
-                   ~(size_t)3;
+  const size_t f = ((size_t)group * hd + (size_t)group * chunk + 2 * group + 2 * (size_t)group * nsplit +
+                    RED_FLOATS + 3) & ~(size_t)3;
   return f * sizeof(float) + 2 * (size_t)chunk * hd * kv_bytes;
 }
 

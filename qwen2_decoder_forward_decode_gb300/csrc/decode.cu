@@ -114,10 +114,9 @@ struct OpQKV {
   KV *kc, *vc;  // [nkv][cap][hd] of this layer and sequence
   int pos;
 
-  __device__ void prologue(float* xs, float* gs, float* scratch) {
-    prologue_norm(xs, gs, scratch, x, gain, K, eps);
-    pos = __ldcg(d_pos);
-  }
+  // the position is set by the previous step's LM head, finished before this step began
+  __device__ void pre() { pos = __ldcg(d_pos); }
+  __device__ void prologue(float* xs, float* gs, float* scratch) { prologue_norm(xs, gs, scratch, x, gain, K, eps); }
   // row r (0: i, 1: i + hd/2) of item (head, i)
   __device__ const T* row(int item, int r) const {
     const int half = hd >> 1;
@@ -190,6 +189,7 @@ struct OpGateUp {
   const float* x;
   float eps;
   float* act;
+  __device__ void pre() {}
   __device__ void prologue(float* xs, float* gs, float* scratch) { prologue_norm(xs, gs, scratch, x, gain, K, eps); }
   __device__ const T* row(int item, int r) const { return (r == 0 ? wg : wu) + (size_t)item * K; }
   __device__ const float* xin() const { return x; }
@@ -208,6 +208,7 @@ struct OpResid {
   const T* W;
   const float* in;
   float* y;
+  __device__ void pre() {}
   __device__ void prologue(float* xs, float*, float*) { prologue_copy(xs, in, K); }
   __device__ const T* row(int item, int r) const {
     const int rr = RPI * item + r;
@@ -240,6 +241,7 @@ struct OpLMHead {
   float best_v;
   int best_i;
   bool nonfinite;
+  __device__ void pre() {}
   __device__ void prologue(float* xs, float* gs, float* scratch) {
     prologue_norm(xs, gs, scratch, x, gain, K, eps);
     best_v = -INFINITY;
@@ -315,6 +317,7 @@ struct OpLMHead {
 // while this one finishes. Partial sums over K segments add in a fixed order.
 struct GemvCfg {
   int KS, NS, slot_bytes, x_direct, pf_dist;
+  int prewait_bytes;  // per warp: weight bytes beyond the ring prefetched into L2 before the wait
   int* err;
   unsigned long long* tl;  // timeline slots or null
 };
@@ -375,8 +378,18 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
     mbar_fence_init();
     const int n0 = min(NS, my_items);  // weights do not depend on upstream kernels
     for (int k = 0; k < n0; ++k) issue(k);
-    for (int k = n0; k < min(NS + c.pf_dist, my_items); ++k) prefetch(k);
+    // and while the upstream kernels finish, the next items stream into L2
+    const uint32_t item_bytes = seg_bytes * (uint32_t)Op::RPI;
+    int n_pf = c.pf_dist;
+    if (item_bytes && c.prewait_bytes > 0 && (int)(c.prewait_bytes / item_bytes) > n_pf)
+      n_pf = (int)(c.prewait_bytes / item_bytes);
+    for (int k = n0; k < min(NS + n_pf, my_items); ++k) prefetch(k);
   }
+  // inputs of the epilogue that do not depend on upstream kernels (first two items)
+  op.pre();
+  typename Op::Epi pe[2];
+  if (my_items > 0) pe[0] = op.epi_load(first);
+  if (my_items > 1) pe[1] = op.epi_load(first + step);
   __syncwarp();
   pdl_trigger();  // the next kernel may become resident and start its own weight stream
   pdl_wait();
@@ -414,7 +427,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
     if (!ok) { timed_out = true; break; }
     consumed = k + 1;
     const int item = first + k * step;
-    const typename Op::Epi epi = op.epi_load(item);
+    const typename Op::Epi epi = k == 0 ? pe[0] : k == 1 ? pe[1] : op.epi_load(item);
     const uint4* s0 = reinterpret_cast<const uint4*>(wslots + (size_t)slot * c.slot_bytes);
     const uint4* s1 = reinterpret_cast<const uint4*>(wslots + (size_t)slot * c.slot_bytes + seg_bytes);
     float a0 = 0.f, a1 = 0.f;
@@ -465,8 +478,9 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
 // dynamic shared memory: per-warp slot rings and, unless x is read straight into
 // registers, the input vector (and the gains of a norm prologue)
 static constexpr int X_SMEM_MAX = 16 * 1024;
-// Tuning: bytes of slots per warp (8 warps: 96 KB keeps two kernels' CTAs on one SM) and
-// the L2 prefetch distance in items; QW_GEMV_SLOT_KB / QW_GEMV_PF override them.
+// Tuning: bytes of slots per warp (8 warps: 96 KB keeps two kernels' CTAs on one SM), the
+// in-loop L2 prefetch distance in items, and the bytes per warp prefetched into L2 before
+// the dependency wait; QW_GEMV_SLOT_KB / QW_GEMV_PF / QW_GEMV_PREWAIT_KB override them.
 static int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   return v && *v ? std::atoi(v) : dflt;
@@ -478,6 +492,10 @@ static int warp_budget() {
 static int pf_dist() {
   static const int p = env_int("QW_GEMV_PF", 0);
   return p;
+}
+static int prewait_bytes() {
+  static const int b = env_int("QW_GEMV_PREWAIT_KB", 0) * 1024;
+  return b;
 }
 
 static int maxv_for(int nvec, int KS) {
@@ -516,6 +534,7 @@ static bool plan_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, G
   p->c.slot_bytes = (int)slot;
   p->c.x_direct = x_direct;
   p->c.pf_dist = pf_dist();
+  p->c.prewait_bytes = prewait_bytes();
   p->c.err = err;
   p->c.tl = tl;
   p->maxv = maxv_for(nvec, KS);

@@ -101,7 +101,7 @@ struct StepLaunch {
   unsigned long long* bar;      // monotonic barrier counter, zero at creation
   unsigned long long bar_base;  // its value before this launch
   int *abort, *err;
-  int nslots, grid;
+  int nslots, slot, grid;
   size_t smem;
   unsigned long long* tl;       // per phase [start, end, producer issued] or null
   int* diag;                    // 4 ints: first expired wait (site, CTA, warp, detail)
@@ -110,7 +110,7 @@ int step_xs_floats(const Dims& d);
 int step_barriers_per_launch(const Dims& d);
 bool step_kernel_supported(const Dims& d);
 size_t step_part_bytes(const Dims& d);
-cudaError_t step_set_attributes(const Dims& d, int* nslots_out, size_t* smem_out);
+cudaError_t step_set_attributes(const Dims& d, int slot_bytes, int* slot_out, int* nslots_out, size_t* smem_out);
 cudaError_t launch_step(const StepLaunch& a, cudaStream_t s);
 
 // ---- prefill.cu ----

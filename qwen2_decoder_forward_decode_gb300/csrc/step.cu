@@ -31,8 +31,8 @@ constexpr int NCW = 8;                    // consumer warps
 constexpr int NPW = 2;                    // producer warps (each issues every NPW-th unit)
 constexpr int THREADS = (NCW + NPW) * 32;
 constexpr int NCT = NCW * 32;             // consumer threads
-constexpr int SLOT = 24 * 1024;           // bytes per ring slot (a unit of whole rows)
-constexpr int MAX_SLOTS = 8;
+constexpr int SLOT_DEFAULT = 24 * 1024;   // bytes per ring slot (a unit of whole rows)
+constexpr int MAX_SLOTS = 16;
 constexpr int GMAX = 8;
 
 enum : int { P_QKV = 0, P_ATTN = 1, P_OPROJ = 2, P_GATEUP = 3, P_DOWN = 4, P_LM = 5 };
@@ -58,6 +58,7 @@ struct Params {
   int* abort;
   int* err;
   int nslots;
+  int slot;         // bytes per ring slot (multiple of 16)
   int xs_floats;    // floats of the staged input vector region
   unsigned long long* tl;  // timeline: per phase [start, end, producer issued] (CTA 0), or null
   int* diag;               // [0..3] first expired wait (site, CTA, warp, detail); then per CTA
@@ -90,6 +91,7 @@ __device__ __forceinline__ Geo geo(const Params& p, int ph) {
     case P_DOWN: g.n_items = p.H; g.rows = 1; g.K = p.I; break;
     default: g.n_items = (p.V + 1) / 2; g.rows = 2; g.K = p.H; break;
   }
+  const int SLOT = p.slot;
   const int item_bytes = g.rows * g.K * 2;
   if (item_bytes <= SLOT) {
     g.ipu = SLOT / item_bytes;
@@ -592,6 +594,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   __shared__ int rel[MAX_SLOTS];  // per slot: sequence number of the last released unit
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = p.nslots;
+  const int SLOT = p.slot;
   float* xs = reinterpret_cast<float*>(dsm + (size_t)NS * SLOT);
   const uint32_t ring = smem_addr(dsm);
   const uint32_t full0 = smem_addr(full), empty0 = smem_addr(empty);
@@ -978,19 +981,25 @@ int step_barriers_per_launch(const Dims& d) { return 5 * d.L + 1; }
 
 bool step_kernel_supported(const Dims& d) {
   return d.dtype == 1 && d.hd <= 128 && d.hd % 8 == 0 && d.nq / d.nkv <= step::GMAX &&
-         d.H % 8 == 0 && d.I % 8 == 0 && (size_t)step_xs_floats(d) * 4 + 4 * step::SLOT <= 224 * 1024;
+         d.H % 8 == 0 && d.I % 8 == 0 && (size_t)step_xs_floats(d) * 4 + 4 * step::SLOT_DEFAULT <= 224 * 1024;
 }
 
 size_t step_part_bytes(const Dims& d) {
   return (size_t)d.nq * step::MAX_SPLIT * (d.hd + 2) * sizeof(float);
 }
 
-cudaError_t step_set_attributes(const Dims& d, int* nslots_out, size_t* smem_out) {
+// Ring geometry: slots of slot_bytes (0: the default) filling the shared memory left
+// beside the staged vector, an even number of them (one half per producer warp).
+cudaError_t step_set_attributes(const Dims& d, int slot_bytes, int* slot_out, int* nslots_out, size_t* smem_out) {
   const size_t xs = (size_t)step_xs_floats(d) * 4;
-  int ns = (int)((224 * 1024 - xs) / step::SLOT);
+  int slot = slot_bytes > 0 ? slot_bytes & ~15 : step::SLOT_DEFAULT;
+  if (slot < 4096) slot = 4096;
+  int ns = (int)((224 * 1024 - xs) / slot);
   if (ns > step::MAX_SLOTS) ns = step::MAX_SLOTS;
   ns -= ns % step::NPW;
-  const size_t smem = (size_t)ns * step::SLOT + xs;
+  if (ns < 2) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)ns * slot + xs;
+  *slot_out = slot;
   *nslots_out = ns;
   *smem_out = smem;
   return cudaFuncSetAttribute(step::decode_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1006,7 +1015,7 @@ cudaError_t launch_step(const StepLaunch& a, cudaStream_t s) {
   p.x = a.x; p.q = a.q; p.act = a.act; p.logits = a.logits; p.part = a.part;
   p.tok = a.tok; p.pos = a.pos; p.key = a.key; p.hist = a.hist; p.hist_n = a.hist_n; p.hist_cap = a.hist_cap;
   p.bar = a.bar; p.bar_base = a.bar_base; p.abort = a.abort; p.err = a.err;
-  p.nslots = a.nslots; p.xs_floats = step_xs_floats(a.d);
+  p.nslots = a.nslots; p.slot = a.slot; p.xs_floats = step_xs_floats(a.d);
   p.tl = a.tl;
   p.diag = a.diag;
   cudaLaunchConfig_t cfg = {};

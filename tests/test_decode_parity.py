@@ -112,6 +112,42 @@ def test_1p5b_long_context_sampled():
         m.close()
 
 
+# ---- persistent step kernel (one cooperative launch per decode step) ------------------
+
+@pytest.mark.parametrize("shape_name,P,n_new,cap,slot_kb", [
+    ("small_bf16", 100, 40, 160, None),
+    ("hd128_bf16", 150, 12, 200, None),
+    ("hd128_bf16", 150, 12, 200, "4"),   # 4 KB slots: each 4.5 KB down row split over two units
+])
+def test_step_kernel_small_shapes(monkeypatch, shape_name, P, n_new, cap, slot_kb):
+    monkeypatch.setenv("QW_STEP_KERNEL", "1")
+    if slot_kb:
+        monkeypatch.setenv("QW_STEP_SLOT_KB", slot_kb)
+    w, prompt, toks, logits = oracle_run(shape_name, P, n_new)
+    m = _model(shape_name, w, cap)
+    try:
+        rep = run_teacher_forced(m, SHAPES[shape_name], prompt, toks, logits)
+        assert rep.steps == n_new
+    finally:
+        m.close()
+
+
+@pytest.mark.parametrize("slot_kb", [None, "12"])  # 6 ring slots (fewer than consumer warps), 14
+def test_step_kernel_workloads(monkeypatch, slot_kb):
+    monkeypatch.setenv("QW_STEP_KERNEL", "1")
+    if slot_kb:
+        monkeypatch.setenv("QW_STEP_SLOT_KB", slot_kb)
+    for name, n in (("0p5b", None), ("1p5b", 6)):
+        wl = WORKLOADS[name]
+        w, prompt, toks, logits = oracle_run(wl.shape, wl.prompt_len, n or wl.new_tokens)
+        m = _model(wl.shape, w, wl.kv_capacity)
+        try:
+            rep = run_teacher_forced(m, SHAPES[wl.shape], prompt, toks, logits)
+            print(f"step kernel {name} slot {slot_kb}: steps {rep.steps} max|dz| {rep.max_err:.4f}")
+        finally:
+            m.close()
+
+
 # ---- edge cases ----------------------------------------------------------------------
 
 def test_single_token_prompt_and_full_capacity():
