@@ -313,7 +313,8 @@ def run_native(args):
             m.prefill_device(ids_dev.data_ptr(), len(prompt))
             # persistent step kernel: per phase [start, end, producer issued] of the first CTA
             kinds = ["qkv", "attn", "o_proj", "gate_up", "down"] * s.n_layers + ["lm_head"]
-            st = {k: {"run_us": [], "barrier_us": [], "producer_lead_us": []} for k in set(kinds)}
+            st = {k: {"run_us": [], "barrier_us": [], "producer_lead_us": [], "staged_us": [],
+                      "first_unit_us": [], "units_done_us": []} for k in set(kinds)}
             tot = []
             for i in range(12):
                 m.decode_steps(1)
@@ -322,6 +323,7 @@ def run_native(args):
                 if i < 2:
                     continue
                 ring = full_tl[len(kinds)]
+                sub = full_tl[len(kinds) + 1:2 * len(kinds) + 1]
                 tot.append((tl[-1, 1] - tl[0, 0]) / 1000.0)
                 for j, k in enumerate(kinds):
                     st[k]["run_us"].append((tl[j, 1] - tl[j, 0]) / 1000.0)
@@ -329,6 +331,9 @@ def run_native(args):
                         st[k]["barrier_us"].append((tl[j + 1, 0] - tl[j, 1]) / 1000.0)
                     if tl[j, 2] > 0:
                         st[k]["producer_lead_us"].append((tl[j, 1] - tl[j, 2]) / 1000.0)
+                    for c, f in enumerate(("staged_us", "first_unit_us", "units_done_us")):
+                        if j < len(sub) and sub[j, c] > 0:
+                            st[k][f].append((sub[j, c] - tl[j, 0]) / 1000.0)
             m.set_timeline(False)
             out = {"step_kernel_us": float(np.mean(tot)),
                    "ring_cta0": {"producer_waits": int(ring[0]), "producer_found_slot_busy": int(ring[1]),

@@ -88,7 +88,20 @@ struct qw_model {
   int* step_abort = nullptr;  // [0] abort flag, [1..] diagnostics of expired waits
   int step_nslots = 0;
   int step_slot = 0;
+  int step_pf_units = 0;
   size_t step_smem = 0;
+  // batched decode (bf16 models with the fp16 matrix copies, several sequences)
+  bool use_batched = false;
+  std::vector<BatchedLayerPlans> bplans;
+  SkinnyPlan blm{};
+  void* bblock = nullptr;          // one allocation for the buffers below
+  float *bq = nullptr, *bpart = nullptr;
+  __half *bX16 = nullptr, *bO16 = nullptr, *bA16 = nullptr;
+  __nv_bfloat16* bXb16 = nullptr;
+  void* battn_ws = nullptr;
+  int* bactive = nullptr;          // device copy of the active flags
+  bool bactive_dirty = true;
+  cudaGraphExec_t bgraph = nullptr;
   unsigned long long* tl_buf = nullptr;  // device timeline of one decode step (or null)
   int tl_n = 0;                          // launches per decode step
   std::vector<unsigned long long> tl_init;
@@ -195,6 +208,7 @@ struct qw_model {
     a.err = err;
     a.nslots = step_nslots;
     a.slot = step_slot;
+    a.pf_units = step_pf_units;
     a.grid = d.nsm;
     a.smem = step_smem;
     a.tl = tl_buf;
@@ -229,6 +243,83 @@ struct qw_model {
       if (e) { graphs[s] = nullptr; return e; }
     }
     return cudaGraphLaunch(graphs[s], stream);
+  }
+
+  int n_active() const {
+    int n = 0;
+    for (char a : active) n += a != 0;
+    return n;
+  }
+
+  // One decode step of every active sequence with the weights read once (batched path).
+  cudaError_t run_decode_batched() {
+    cudaError_t e;
+    if (bactive_dirty) {
+      std::vector<int> h(d.max_seqs);
+      for (int s = 0; s < d.max_seqs; ++s) h[s] = active[s] ? 1 : 0;
+      if ((e = cudaMemcpyAsync(bactive, h.data(), sizeof(int) * d.max_seqs, cudaMemcpyHostToDevice, stream)))
+        return e;
+      if ((e = cudaStreamSynchronize(stream))) return e;  // h is a stack buffer
+      bactive_dirty = false;
+    }
+    BatchedCtx c{};
+    c.d = d;
+    c.layers = layers.data();
+    c.plans = bplans.data();
+    c.lm = blm;
+    c.embed = embed;
+    c.final_norm = final_norm;
+    c.rope = rope;
+    c.kv = kv;
+    c.kv_seq_elems = seq_kv_elems();
+    c.x = x;
+    c.q = bq;
+    c.part = bpart;
+    c.logits = logits;
+    c.X16 = bX16;
+    c.O16 = bO16;
+    c.A16 = bA16;
+    c.Xb16 = bXb16;
+    c.tok = tok;
+    c.pos = pos;
+    c.hist = hist;
+    c.hist_n = hist_n;
+    c.err = err;
+    c.active = bactive;
+    c.keys = keys;
+    c.attn_ws = battn_ws;
+    c.attn_smem = attn_smem;
+    if (!use_graphs) return batched_step(c, stream);
+    if (!bgraph) {
+      cudaGraph_t g = nullptr;
+      if ((e = cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal))) return e;
+      e = batched_step(c, stream);
+      cudaError_t e2 = cudaStreamEndCapture(stream, &g);
+      if (e) { if (g) cudaGraphDestroy(g); return e; }
+      if (e2) return e2;
+      e = cudaGraphInstantiate(&bgraph, g, 0);
+      cudaGraphDestroy(g);
+      if (e) { bgraph = nullptr; return e; }
+    }
+    return cudaGraphLaunch(bgraph, stream);
+  }
+
+  // decode step of all active sequences: batched when two or more are active
+  cudaError_t decode_all() {
+    if (use_batched && n_active() >= 2) {
+      cudaError_t e = run_decode_batched();
+      if (e) return e;
+      for (int s = 0; s < d.max_seqs; ++s)
+        if (active[s]) h_pos[s] += 1;
+      return cudaSuccess;
+    }
+    for (int s = 0; s < d.max_seqs; ++s) {
+      if (!active[s]) continue;
+      cudaError_t e = run_decode(s);
+      if (e) return e;
+      h_pos[s] += 1;
+    }
+    return cudaSuccess;
   }
 
   cudaError_t ensure_prefill(int T) {
@@ -300,6 +391,10 @@ struct qw_model {
     for (auto& g : graphs)
       if (g) cudaGraphExecDestroy(g);
     graphs.clear();
+    if (bgraph) cudaGraphExecDestroy(bgraph);
+    bgraph = nullptr;
+    if (bblock) cudaFree(bblock);
+    if (battn_ws) cudaFree(battn_ws);
     void* bufs[] = {kv, x, q, attn, act, logits, rope, attn_ws, keys, lm_counter, pos, tok,
                     hist, hist_n, err, ids, pf_block, w16, tl_buf, step_layers, step_part, step_bar,
                     step_abort};
@@ -478,6 +573,8 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
     if (step_kernel_supported(d) && coop && sk && sk[0] == '1') {
       const char* skb = std::getenv("QW_STEP_SLOT_KB");  // ring slot size (tuning knob)
       const int slot_bytes = skb ? (int)(std::atof(skb) * 1024) : 0;
+      const char* spf = std::getenv("QW_STEP_PF_UNITS");  // L2 prefetch distance (tuning knob)
+      m->step_pf_units = spf ? std::atoi(spf) : 0;
       if ((e = step_set_attributes(d, slot_bytes, &m->step_slot, &m->step_nslots, &m->step_smem)))
         return bail(e, "step attributes");
       std::vector<StepLayer> sl(d.L);
@@ -498,6 +595,71 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
       if ((e = cudaMalloc(&m->step_abort, nd * sizeof(int)))) return bail(e, "cudaMalloc");
       if ((e = cudaMemset(m->step_abort, 0, nd * sizeof(int)))) return bail(e, "cudaMemset");
       m->use_step = true;
+    }
+  }
+  if (m->pf.use_tc && S > 1) {
+    // batched decode: every weight matrix read once per step for all active sequences
+    const char* bz = std::getenv("QW_BATCHED");
+    if (!(bz && bz[0] == '0') && d.H % 8 == 0 && d.I % 8 == 0 && (d.nq * d.hd) % 8 == 0) {
+      const size_t H = d.H, qd = (size_t)d.nq * d.hd, kvd = (size_t)d.nkv * d.hd, I = d.I;
+      auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
+      const size_t sz_q = al(16 * qd * 4), sz_x16 = al(16 * H * 2), sz_o16 = al(16 * qd * 2), sz_a16 = al(16 * I * 2),
+                   sz_xb = al(16 * H * 2), sz_act = al(sizeof(int) * S);
+      m->bplans.resize(d.L);
+      bool ok = true;
+      size_t part_floats = 0;
+      // the fp16 activation rows live at fixed offsets of one block, so the plans can be made
+      // before the allocation is known: make them against the final addresses afterwards
+      char* blk = nullptr;
+      size_t total = sz_q + sz_x16 + sz_o16 + sz_a16 + sz_xb + sz_act;
+      // partial buffer: size from the plans' split counts (computed with a placeholder first)
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        if (pass == 1) {
+          if ((e = cudaMalloc(&m->bblock, total + al(part_floats * 4)))) return bail(e, "cudaMalloc(batched)");
+          if ((e = cudaMemset(m->bblock, 0, total + al(part_floats * 4)))) return bail(e, "cudaMemset(batched)");
+          blk = (char*)m->bblock;
+          m->bq = (float*)blk;
+          m->bX16 = (__half*)(blk + sz_q);
+          m->bO16 = (__half*)(blk + sz_q + sz_x16);
+          m->bA16 = (__half*)(blk + sz_q + sz_x16 + sz_o16);
+          m->bXb16 = (__nv_bfloat16*)(blk + sz_q + sz_x16 + sz_o16 + sz_a16);
+          m->bactive = (int*)(blk + sz_q + sz_x16 + sz_o16 + sz_a16 + sz_xb);
+          m->bpart = (float*)(blk + total);
+        }
+        // pass 0 plans against a 256-aligned placeholder address, only for the split counts
+        const void* X16 = pass ? (const void*)m->bX16 : (const void*)(uintptr_t)4096;
+        const void* O16 = pass ? (const void*)m->bO16 : X16;
+        const void* A16 = pass ? (const void*)m->bA16 : X16;
+        const void* Xb = pass ? (const void*)m->bXb16 : X16;
+        for (int l = 0; l < d.L && ok; ++l) {
+          const LayerPtrs& L = m->layers[l];
+          BatchedLayerPlans& P = m->bplans[l];
+          const void* wqkv[3] = {L.wq16, L.wk16, L.wv16};
+          const int rqkv[3] = {(int)qd, (int)kvd, (int)kvd};
+          const void* wo[1] = {L.wo16};
+          const int ro[1] = {(int)H};
+          const void* wgu[2] = {L.wg16, L.wu16};
+          const int rgu[2] = {(int)I, (int)I};
+          const void* wd[1] = {L.wd16};
+          ok = skinny_plan(&P.qkv, 3, wqkv, rqkv, X16, (int)H, false, d.nsm) &&
+               skinny_plan(&P.o, 1, wo, ro, O16, (int)qd, false, d.nsm) &&
+               skinny_plan(&P.gu, 2, wgu, rgu, X16, (int)H, false, d.nsm) &&
+               skinny_plan(&P.down, 1, wd, ro, A16, (int)I, false, d.nsm);
+          if (ok && pass == 0)
+            for (const SkinnyPlan* sp : {&P.qkv, &P.o, &P.gu, &P.down})
+              part_floats = std::max(part_floats, (size_t)sp->splits * 16 * sp->n_total);
+        }
+        const void* wlm[1] = {m->head_w()};
+        const int rlm[1] = {d.V};
+        ok = ok && skinny_plan(&m->blm, 1, wlm, rlm, Xb, (int)H, true, d.nsm);
+      }
+      if (ok) {
+        const size_t aws = attn_batched_workspace_bytes(d.nq, d.nkv, d.hd, d.attn_nsplit, S);
+        if ((e = cudaMalloc(&m->battn_ws, aws))) return bail(e, "cudaMalloc(batched attention)");
+        if ((e = cudaMemset(m->battn_ws, 0, aws))) return bail(e, "cudaMemset(batched attention)");
+        if ((e = batched_set_attributes())) return bail(e, "batched attributes");
+        m->use_batched = true;
+      }
     }
   }
   if ((e = attn_set_attributes(m->attn_smem))) return bail(e, "attention attributes");
@@ -535,6 +697,7 @@ qw_status qw_prefill_device(qw_model* m, int32_t seq, const int32_t* ids_dev, in
   QW_CUDA(m->enqueue_prefill(seq, ids_dev, n));
   m->h_pos[seq] = n;
   m->active[seq] = 1;
+  m->bactive_dirty = true;
   return QW_OK;
 }
 
@@ -551,6 +714,7 @@ qw_status qw_prefill(qw_model* m, int32_t seq, const int32_t* ids, int32_t n, in
   QW_CUDA(m->enqueue_prefill(seq, m->ids, n));
   m->h_pos[seq] = n;
   m->active[seq] = 1;
+  m->bactive_dirty = true;
   if (next_token) {
     QW_CUDA(cudaMemcpyAsync(m->pinned, m->tok + seq, sizeof(int), cudaMemcpyDeviceToHost, m->stream));
     st = m->check_device_errors();
@@ -588,11 +752,7 @@ qw_status qw_decode_step(qw_model* m, const int32_t* feed, int32_t* next_tokens)
       if (m->active[s])
         QW_CUDA(cudaMemcpyAsync(m->tok + s, m->pinned + s, sizeof(int), cudaMemcpyHostToDevice, m->stream));
   }
-  for (int s = 0; s < S; ++s) {
-    if (!m->active[s]) continue;
-    QW_CUDA(m->run_decode(s));
-    m->h_pos[s] += 1;
-  }
+  QW_CUDA(m->decode_all());
   if (next_tokens) {
     QW_CUDA(cudaStreamSynchronize(m->stream));
     QW_CUDA(cudaMemcpyAsync(m->pinned, m->tok, sizeof(int) * S, cudaMemcpyDeviceToHost, m->stream));
@@ -610,11 +770,7 @@ qw_status qw_decode_steps(qw_model* m, int32_t n_steps) {
   for (int i = 0; i < n_steps; ++i) {
     qw_status st = decode_prepare(m);
     if (st) return st;
-    for (int s = 0; s < m->d.max_seqs; ++s) {
-      if (!m->active[s]) continue;
-      QW_CUDA(m->run_decode(s));
-      m->h_pos[s] += 1;
-    }
+    QW_CUDA(m->decode_all());
   }
   return QW_OK;
 }
@@ -628,6 +784,7 @@ qw_status qw_generate(qw_model* m, const int32_t* ids, int32_t n, int32_t max_ne
   if (st) return st;
   if ((int64_t)n + max_new - 1 > m->d.cap) return fail(QW_ERR_CAPACITY, "prompt + max_new - 1 exceeds kv_capacity");
   for (int s = 1; s < m->d.max_seqs; ++s) m->active[s] = 0;
+  m->bactive_dirty = true;
   st = qw_prefill(m, 0, ids, n, nullptr);
   if (st) return st;
   const int chunk = eos >= 0 ? 16 : max_new;
@@ -707,7 +864,10 @@ qw_status qw_set_timeline(qw_model* m, int32_t enable) {
   m->tl_n = 1 + 5 * m->d.L + 1;
   m->tl_init.assign((size_t)3 * m->tl_n, ~0ull);
   for (int i = 0; i < m->tl_n; ++i) m->tl_init[3 * i + 2] = 0ull;
-  if (m->use_step) m->tl_init.assign((size_t)3 * m->tl_n, 0ull);
+  if (m->use_step) {  // per phase [start, end, producer issued]; ring counters; per phase sub-stamps
+    m->tl_n = 2 * (5 * m->d.L + 1) + 1;
+    m->tl_init.assign((size_t)3 * m->tl_n, 0ull);
+  }
   QW_CUDA(cudaMalloc(&m->tl_buf, sizeof(unsigned long long) * 3 * m->tl_n));
   QW_CUDA(cudaMemcpy(m->tl_buf, m->tl_init.data(), sizeof(unsigned long long) * 3 * m->tl_n,
                      cudaMemcpyHostToDevice));
@@ -747,6 +907,7 @@ qw_status qw_reset(qw_model* m, int32_t seq) {
   if (!m) return fail(QW_ERR_INVALID_ARG, "null model");
   if (seq < 0 || seq >= m->d.max_seqs) return fail(QW_ERR_INVALID_ARG, "sequence index out of range");
   m->active[seq] = 0;
+  m->bactive_dirty = true;
   m->h_pos[seq] = 0;
   QW_CUDA(cudaMemsetAsync(m->pos + seq, 0, sizeof(int), m->stream));
   return QW_OK;

@@ -23,6 +23,12 @@ struct AttnArgs {
   float* part;            // [nq][nsplit_max][hd + 2]
   unsigned int* counter;  // [nkv]
   unsigned long long* tl;  // timeline slots or null
+  // several sequences (grid z): per-sequence strides of q, the KV cache, the output, the
+  // partials (elements) and the counters; an fp16 output instead of out; active flags
+  size_t q_zs, kv_zs, out_zs, part_zs;
+  int counter_zs;
+  f16* out16;
+  const int* active;
 };
 
 // One CTA per (KV head, context chunk). The CTA copies q of its g query heads and the K and
@@ -65,9 +71,20 @@ template <> struct KVec<float> {
 };
 
 template <typename KV>
-__global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArgs<KV> a) {
+__global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArgs<KV> a_in) {
   extern __shared__ __align__(16) float sm[];
   __shared__ bool s_last;
+  const int z = blockIdx.z;  // sequence
+  if (a_in.active && !a_in.active[z]) return;
+  AttnArgs<KV> a = a_in;
+  a.q += z * a.q_zs;
+  a.k += z * a.kv_zs;
+  a.v += z * a.kv_zs;
+  if (a.d_pos) a.d_pos += z;
+  a.part += z * a.part_zs;
+  a.counter += z * a.counter_zs;
+  if (a.out16) a.out16 += z * a.out_zs;
+  else a.out += z * a.out_zs;
   constexpr int EV = KVec<KV>::N;  // KV elements per 16-byte vector
   const int g = blockIdx.x, split = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = ATTN_THREADS >> 5;
@@ -302,7 +319,10 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
 #pragma unroll
   for (int k = 0; k < EPT; ++k) {
     const int idx = tid + k * ATTN_THREADS;
-    if (idx < G * hd) a.out[(size_t)g * G * hd + idx] = out[k];
+    if (idx < G * hd) {
+      if (a.out16) a.out16[(size_t)g * G * hd + idx] = __float2half_rn(out[k]);
+      else a.out[(size_t)g * G * hd + idx] = out[k];
+    }
   }
   if (tid == 0) a.counter[g] = 0u;
   tl_stamp(a.tl, 2);
@@ -350,13 +370,34 @@ cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int c
   if (kv_dtype == 2) {
     AttnArgs<f16> a{q, (const f16*)kc, (const f16*)vc, kv_stride, hd, G, nsplit, chunk_min,
                      ctx_host, d_pos, 1.f / sqrtf((float)hd), out, (float*)ws,
-                     (unsigned int*)((char*)ws + part_bytes), tl};
+                     (unsigned int*)((char*)ws + part_bytes), tl, 0, 0, 0, 0, 0, nullptr, nullptr};
     return launch_k(attn_decode_kernel<f16>, grid, block, smem, s, pdl, a);
   }
   AttnArgs<float> a{q, (const float*)kc, (const float*)vc, kv_stride, hd, G, nsplit, chunk_min,
                     ctx_host, d_pos, 1.f / sqrtf((float)hd), out, (float*)ws,
-                    (unsigned int*)((char*)ws + part_bytes), tl};
+                    (unsigned int*)((char*)ws + part_bytes), tl, 0, 0, 0, 0, 0, nullptr, nullptr};
   return launch_k(attn_decode_kernel<float>, grid, block, smem, s, pdl, a);
+}
+
+// Decode attention of nseq sequences in one launch (grid z = sequence, inactive ones exit):
+// q [nseq][nq*hd] fp32; the fp16 caches of sequence z start kv_zs elements after those of
+// sequence z - 1; output fp16 [nseq][nq*hd]; workspace: partials [nseq][...] then counters
+// [nseq][nkv] (attn_batched_workspace_bytes).
+size_t attn_batched_workspace_bytes(int nq, int nkv, int hd, int nsplit, int nseq) {
+  const size_t part = ((size_t)nq * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
+  return part * nseq + (size_t)nkv * nseq * sizeof(unsigned int);
+}
+cudaError_t launch_attn_batched(int nq, int nkv, int hd, int nsplit, int chunk_min, size_t smem,
+                                const float* q, const f16* kc, const f16* vc, size_t kv_zs, int kv_stride,
+                                const int* d_pos, const int* active, int nseq, f16* out16, void* ws,
+                                cudaStream_t s) {
+  const int G = nq / nkv;
+  if (G > GMAX) return cudaErrorInvalidValue;
+  const size_t part_bytes = ((size_t)nq * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
+  AttnArgs<f16> a{q, kc, vc, kv_stride, hd, G, nsplit, chunk_min, 0, d_pos, 1.f / sqrtf((float)hd), nullptr,
+                  (float*)ws, (unsigned int*)((char*)ws + part_bytes * nseq), nullptr,
+                  (size_t)nq * hd, kv_zs, (size_t)nq * hd, part_bytes / sizeof(float), nkv, out16, active};
+  return launch_k(attn_decode_kernel<f16>, dim3(nkv, nsplit, nseq), dim3(ATTN_THREADS), smem, s, false, a);
 }
 
 cudaError_t attn_set_attributes(size_t smem) {

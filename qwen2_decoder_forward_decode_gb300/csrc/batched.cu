@@ -1,0 +1,199 @@
+// Batched greedy decode: one decode step of up to 16 independent sequences, each at its own
+// position, with every weight matrix read once per step for all of them ("augur",
+// Features: batched generation; the per-sequence computation is the decoder forward pass of
+// "LLM Speedrun: Architecture", Transformer architecture and Implementing Qwen).
+//
+// Per layer:
+//   norm     x[b] -> RMSNorm -> fp16 row b of X            (rows of absent sequences: 0)
+//   qkv      skinny tensor-core GEMM of Wq|Wk|Wv against X (split-K fp32 partials)
+//   qkv_epi  partial sums + bias, split-half RoPE at pos[b], q out, K/V append for seq b
+//   attn     decode attention, grid z = sequence, fp16 output rows
+//   o        skinny GEMM of Wo, then x[b] += partial sums
+//   norm     post-attention RMSNorm -> X
+//   gate/up  skinny GEMM of Wg|Wu, then SwiGLU -> fp16 rows A
+//   down     skinny GEMM of Wd against A, then x[b] += partial sums
+// then the final norm (bf16 rows), the LM head as a skinny GEMM over the bf16 embedding
+// with a fused per-sequence argmax, and the per-sequence token / position bookkeeping.
+//
+// Layer matrices use the fp16 copies made for the prefill (fp16 activations keep the
+// error of the bf16 path inside its tolerance); the LM head uses the bf16 embedding with
+// bf16 activations (a one-layer error, far inside the tolerance).
+#include "common.cuh"
+#include "internal.h"
+
+#include <math.h>
+
+namespace qw {
+
+constexpr int BT = 256;  // threads of the element-wise kernels
+
+__global__ void bembed_kernel(const bf16* E, int V, int H, const int* tok, const int* active, int nseq,
+                              float* x, int* err) {
+  const int b = blockIdx.x;
+  if (b >= nseq || !active[b]) return;
+  int t = __ldcg(tok + b);
+  if (t < 0 || t >= V) {
+    if (threadIdx.x == 0) atomicOr(err, ERR_TOKEN);
+    t = 0;
+  }
+  const bf16* row = E + (size_t)t * H;
+  float* xb = x + (size_t)b * H;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) xb[k] = __bfloat162float(row[k]);
+}
+
+// out row b = x[b] / sqrt(mean(x[b]^2) + eps) * gain, as OutT (fp16 or bf16); rows of
+// absent or inactive sequences are zero
+template <typename OutT>
+__global__ void bnorm_kernel(const float* x, const bf16* gain, int H, float eps, const int* active, int nseq,
+                             OutT* out) {
+  __shared__ float scratch[32];
+  const int b = blockIdx.x;
+  OutT* o = out + (size_t)b * H;
+  if (b >= nseq || !active[b]) {
+    for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = from_f32<OutT>(0.f);
+    return;
+  }
+  const float* xb = x + (size_t)b * H;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) {
+    const float v = __ldcg(xb + k);
+    ss = fmaf(v, v, ss);
+  }
+  ss = block_sum(ss, scratch);
+  const float inv = rsqrtf(ss / (float)H + eps);
+  for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = from_f32<OutT>(__ldcg(xb + k) * inv * __bfloat162float(gain[k]));
+}
+
+// Sum of the split partials of column c of sequence b (fixed split order).
+__device__ __forceinline__ float psum(const float* part, int splits, int n_total, int b, int c) {
+  float acc = 0.f;
+  for (int s = 0; s < splits; ++s) acc += __ldcg(part + ((size_t)s * 16 + b) * n_total + c);
+  return acc;
+}
+
+// q/k/v of sequence b from the partials: + bias, split-half RoPE of q and k at pos[b], q to
+// q_out[b], k and v appended to the sequence's cache at pos[b]. One thread per RoPE pair.
+__global__ void bqkv_epi_kernel(const float* part, int splits, int n_total, int nq, int nkv, int hd,
+                                const bf16* bq, const bf16* bk, const bf16* bv, const float2* rope,
+                                const int* pos, const int* active, float* q_out, f16* kc0, size_t kv_zs,
+                                int cap, int* err) {
+  const int b = blockIdx.y;
+  if (!active[b]) return;
+  const int half = hd >> 1;
+  const int item = blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= (nq + 2 * nkv) * half) return;
+  const int p = __ldcg(pos + b);
+  if (p < 0 || p >= cap) return;  // the host checks capacity before every step
+  int head = item / half;
+  const int i = item - head * half;
+  const int ca = head * hd + i, cb = ca + half;  // columns of the pair in q|k|v
+  float a = psum(part, splits, n_total, b, ca), c = psum(part, splits, n_total, b, cb);
+  const bf16* bias;
+  int h;
+  if (head < nq) { bias = bq; h = head; }
+  else if (head < nq + nkv) { bias = bk; h = head - nq; }
+  else { bias = bv; h = head - nq - nkv; }
+  if (bias) {
+    a += __bfloat162float(bias[h * hd + i]);
+    c += __bfloat162float(bias[h * hd + i + half]);
+  }
+  if (head < nq + nkv) {
+    const float2 cs = rope[(size_t)p * half + i];
+    const float ra = a * cs.x - c * cs.y, rc = c * cs.x + a * cs.y;
+    a = ra;
+    c = rc;
+  }
+  if (head < nq) {
+    float* qb = q_out + (size_t)b * nq * hd;
+    qb[h * hd + i] = a;
+    qb[h * hd + i + half] = c;
+  } else {
+    // the layer's cache of sequence b: [2][nkv][cap][hd], K then V
+    f16* base = kc0 + (size_t)b * kv_zs + (head < nq + nkv ? 0 : (size_t)nkv * cap * hd);
+    f16* dst = base + ((size_t)h * cap + p) * hd;
+    dst[i] = __float2half_rn(a);
+    dst[i + half] = __float2half_rn(c);
+  }
+}
+
+// x[b][n] += sum of the partials of column n (n < N)
+__global__ void bresid_kernel(const float* part, int splits, int n_total, int N, float* x, const int* active) {
+  const int b = blockIdx.y;
+  if (!active[b]) return;
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  x[(size_t)b * N + n] += psum(part, splits, n_total, b, n);
+}
+
+// A[b][i] = silu(gate) * up as fp16 (gate columns [0, I), up columns [I, 2I)); rows of
+// absent or inactive sequences are zero
+__global__ void bswiglu_kernel(const float* part, int splits, int n_total, int I, const int* active, int nseq,
+                               f16* A) {
+  const int b = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= I) return;
+  float v = 0.f;
+  if (b < nseq && active[b]) {
+    const float g = psum(part, splits, n_total, b, i), u = psum(part, splits, n_total, b, I + i);
+    v = (g / (1.f + expf(-g))) * u;
+  }
+  A[(size_t)b * I + i] = __float2half_rn(v);
+}
+
+// per active sequence: token = argmax (lowest index among equal maxima), history, length
+__global__ void bfinalize_kernel(unsigned long long* keys, int* tok, int* pos, int* hist, int* hist_n, int cap,
+                                 const int* active, int nseq) {
+  const int b = threadIdx.x;
+  if (b >= nseq || !active[b]) return;
+  const unsigned long long k = keys[b];
+  const int idx = argmax_key_index(k);
+  tok[b] = idx;
+  const int n = hist_n[b];
+  if (n < cap) hist[(size_t)b * cap + n] = idx;
+  hist_n[b] = n + 1;
+  pos[b] += 1;
+  keys[b] = 0ull;
+}
+
+cudaError_t batched_set_attributes() { return skinny_set_attributes(); }
+
+cudaError_t batched_step(const BatchedCtx& c, cudaStream_t s) {
+  const Dims& d = c.d;
+  const int S = d.max_seqs, H = d.H, qd = d.nq * d.hd, I = d.I;
+  cudaError_t e;
+  bembed_kernel<<<S, BT, 0, s>>>((const bf16*)c.embed, d.V, H, c.tok, c.active, S, c.x, c.err);
+  if ((e = cudaGetLastError())) return e;
+  for (int l = 0; l < d.L; ++l) {
+    const LayerPtrs& w = c.layers[l];
+    const BatchedLayerPlans& pl = c.plans[l];
+    f16* kc0 = (f16*)c.kv + (size_t)l * 2 * d.nkv * d.cap * d.hd;  // layer l of sequence 0
+    bnorm_kernel<f16><<<16, BT, 0, s>>>(c.x, (const bf16*)w.in_norm, H, d.eps, c.active, S, c.X16);
+    if ((e = skinny_run(pl.qkv, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
+    const int pairs = (d.nq + 2 * d.nkv) * (d.hd / 2);
+    bqkv_epi_kernel<<<dim3((pairs + BT - 1) / BT, S), BT, 0, s>>>(
+        c.part, pl.qkv.splits, pl.qkv.n_total, d.nq, d.nkv, d.hd, (const bf16*)w.bq, (const bf16*)w.bk,
+        (const bf16*)w.bv, c.rope, c.pos, c.active, c.q, kc0, c.kv_seq_elems, d.cap, c.err);
+    if ((e = cudaGetLastError())) return e;
+    if ((e = launch_attn_batched(d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min, c.attn_smem, c.q, kc0,
+                                 kc0 + (size_t)d.nkv * d.cap * d.hd, c.kv_seq_elems, d.cap, c.pos, c.active, S,
+                                 c.O16, c.attn_ws, s)))
+      return e;
+    if ((e = skinny_run(pl.o, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
+    bresid_kernel<<<dim3((H + BT - 1) / BT, S), BT, 0, s>>>(c.part, pl.o.splits, pl.o.n_total, H, c.x, c.active);
+    bnorm_kernel<f16><<<16, BT, 0, s>>>(c.x, (const bf16*)w.post_norm, H, d.eps, c.active, S, c.X16);
+    if ((e = skinny_run(pl.gu, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
+    bswiglu_kernel<<<dim3((I + BT - 1) / BT, 16), BT, 0, s>>>(c.part, pl.gu.splits, pl.gu.n_total, I, c.active,
+                                                              S, c.A16);
+    if ((e = skinny_run(pl.down, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
+    bresid_kernel<<<dim3((H + BT - 1) / BT, S), BT, 0, s>>>(c.part, pl.down.splits, pl.down.n_total, H, c.x,
+                                                            c.active);
+    if ((e = cudaGetLastError())) return e;
+  }
+  bnorm_kernel<bf16><<<16, BT, 0, s>>>(c.x, (const bf16*)c.final_norm, H, d.eps, c.active, S, c.Xb16);
+  if ((e = skinny_run(c.lm, nullptr, c.logits, d.V, S, c.active, c.keys, c.err, s))) return e;
+  bfinalize_kernel<<<1, 32, 0, s>>>(c.keys, c.tok, c.pos, c.hist, c.hist_n, d.cap, c.active, S);
+  (void)qd;
+  return cudaGetLastError();
+}
+
+}  // namespace qw

@@ -13,6 +13,8 @@
 // stops issuing work, and still releases its TMEM.
 #include <cuda.h>
 
+#include <cstring>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -125,6 +127,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// kind::f16 with bf16 A and B (type code 1 in bits 7-9 and 10-12)
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return idesc_f16(M, N) | (1u << 7) | (1u << 10);
 }
 
 }  // namespace tc
@@ -297,6 +319,161 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
+// ---- skinny GEMM of a batched decode step ------------------------------------------------
+//
+//   P[split][b][col_off + r] = sum over the split's K range of W[r, k] X[b, k]
+//
+// for up to three weight matrices W (selected per CTA, e.g. q/k/v or gate/up) against the
+// (at most 16) activation rows X of the sequences. The weight rows take the MMA's M side
+// (128 per CTA) and the sequences its N side (N = 16), so every weight byte is read once
+// for all sequences. K is split over grid.y so that about one CTA per SM streams weights;
+// the fp32 partials are summed by the consuming kernel in split order (deterministic).
+// The LM-head variant (one split) stores the logits of active sequences and folds each
+// warp's rows into per-sequence packed argmax keys.
+namespace sk {
+constexpr int BM = 128, BN = 16, BK = 64, STAGES = 8, THREADS = 192;
+constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE = A_BYTES + B_BYTES;
+constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 + 256;
+}  // namespace sk
+
+struct SkinnyArgs {
+  int nz;
+  int tile_start[3];  // first tile of each weight matrix (grid.x = all tiles)
+  int rows[3];        // rows of each matrix
+  int col_off[3];     // partial column of its first row
+  int K, splits, n_total;
+  float* part;        // [splits][16][n_total]
+  // LM head
+  float* logits;      // [nseq][V]
+  int V, nseq;
+  const int* active;
+  unsigned long long* keys;  // [nseq]
+  int* err;
+};
+
+template <bool LM>
+__global__ void __launch_bounds__(sk::THREADS, 1)
+skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUtensorMap w1,
+                 const __grid_constant__ CUtensorMap w2, const __grid_constant__ CUtensorMap xm,
+                 const SkinnyArgs a) {
+  using namespace sk;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 1);
+  const uint32_t full0 = tc::smem_u32(bars), empty0 = tc::smem_u32(bars + STAGES),
+                 accum = tc::smem_u32(bars + 2 * STAGES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x;
+  const int z = (a.nz > 1 && tile >= a.tile_start[1]) + (a.nz > 2 && tile >= a.tile_start[2]);
+  const CUtensorMap* wm = z == 0 ? &w0 : z == 1 ? &w1 : &w2;
+  const int m0 = (tile - a.tile_start[z]) * BM;
+  const int nk = (a.K + BK - 1) / BK;
+  const int kb0 = (int)((long long)blockIdx.y * nk / a.splits);
+  const int kb1 = (int)((long long)(blockIdx.y + 1) * nk / a.splits);
+  __shared__ int s_abort;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(full0 + 8 * s, 1);
+      tc::mbar_init(empty0 + 8 * s, 1);
+    }
+    tc::mbar_init(accum, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), 32);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer: 128 weight rows and the 16 activation rows per 64-wide K block
+    int issued = 0;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int j = kb - kb0, s = j % STAGES;
+      if (j >= STAGES && !tc::mbar_wait(empty0 + 8 * s, ((j / STAGES) & 1) ^ 1, a.err)) { s_abort = 1; break; }
+      if (s_abort) break;
+      const uint32_t a_dst = tc::smem_u32(smem + s * STAGE);
+      tc::mbar_expect_tx(full0 + 8 * s, STAGE);
+      tc::tma_load_2d(a_dst, wm, full0 + 8 * s, kb * BK, m0);
+      tc::tma_load_2d(a_dst + A_BYTES, &xm, full0 + 8 * s, kb * BK, 0);
+      ++issued;
+    }
+    for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
+      tc::mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1, a.err);
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = LM ? tc::idesc_bf16(BM, BN) : tc::idesc_f16(BM, BN);
+    bool ok = true;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int j = kb - kb0, s = j % STAGES;
+      if (!tc::mbar_wait(full0 + 8 * s, (j / STAGES) & 1, a.err)) { ok = false; s_abort = 1; break; }
+      tc::tc_fence_after();
+      const uint32_t a_base = tc::smem_u32(smem + s * STAGE);
+      const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k)
+        tc::mma_f16(tmem, tc::smem_desc_sw128(a_base + 32 * k), tc::smem_desc_sw128(b_base + 32 * k), idesc,
+                    (j | k) != 0);
+      tc::mma_commit(empty0 + 8 * s);
+    }
+    if (ok && kb1 > kb0) tc::mma_commit(accum);
+  } else if (warp >= 2) {
+    // ---- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = weight rows of the tile
+    const int q = warp & 3;
+    const int r = m0 + q * 32 + lane;
+    float v[16];
+    bool have = false;
+    if (kb1 > kb0 && tc::mbar_wait(accum, 0, a.err)) {
+      tc::tc_fence_after();
+      tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16), v);
+      have = true;
+    } else if (kb1 == kb0) {
+#pragma unroll
+      for (int b = 0; b < 16; ++b) v[b] = 0.f;
+      have = true;
+    }
+    if (have) {
+      const bool in = r < a.rows[z];
+      if (!LM) {
+        if (in) {
+          float* dst = a.part + (size_t)blockIdx.y * 16 * a.n_total + a.col_off[z] + r;
+#pragma unroll
+          for (int b = 0; b < 16; ++b) dst[(size_t)b * a.n_total] = v[b];
+        }
+      } else {
+        bool bad = false;
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+          if (b < a.nseq && a.active[b]) {  // uniform over the warp
+            unsigned long long k = 0ull;
+            if (in) {
+              a.logits[(size_t)b * a.V + r] = v[b];
+              if (!isfinite(v[b])) bad = true;
+              k = argmax_key(v[b], r);
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+              const unsigned long long t = __shfl_xor_sync(0xffffffffu, k, o);
+              k = t > k ? t : k;
+            }
+            if (lane == 0 && k) atomicMax(a.keys + b, k);
+          }
+        }
+        if (bad) atomicOr(a.err, ERR_NONFINITE);
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 32);
+  }
+}
+
 // ---- host side ------------------------------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -316,8 +493,10 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D fp16 row-major [rows][cols] (row pitch ld elements), box 64 x box_rows, 128B swizzle
-static bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int ld, int box_rows) {
+// 2-D fp16 (or bf16) row-major [rows][cols] (row pitch ld elements), box 64 x box_rows,
+// 128B swizzle
+static bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int ld, int box_rows,
+                     bool bf = false) {
   EncodeTiledFn f = encode_fn();
   if (!f) return false;
   if (((uintptr_t)base & 15) || ((size_t)ld * 2) % 16) return false;
@@ -325,7 +504,8 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int l
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
   cuuint32_t box[2] = {(cuuint32_t)tc::BK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return f(m, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+           const_cast<void*>(base), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -345,6 +525,74 @@ cudaError_t gemm_tc_set_attributes() {
 }
 
 bool gemm_tc_available() { return encode_fn() != nullptr; }
+
+cudaError_t skinny_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(skinny_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sk::SMEM);
+  if (e) return e;
+  return cudaFuncSetAttribute(skinny_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk::SMEM);
+}
+
+// Tensor maps of one skinny GEMM: nz weight matrices [rows_z][K] (fp16, or bf16 for the LM
+// head) and the activation rows X [16][K] of the same type.
+bool skinny_plan(SkinnyPlan* p, int nz, const void* const* W, const int* rows, const void* X, int K, bool bf,
+                 int nsm) {
+  if (nz < 1 || nz > 3) return false;
+  std::memset(p, 0, sizeof(*p));
+  p->nz = nz;
+  p->K = K;
+  p->lm = bf;
+  int tiles = 0, col = 0;
+  for (int i = 0; i < 3; ++i) {
+    const int zi = i < nz ? i : nz - 1;
+    if (!make_map(reinterpret_cast<CUtensorMap*>(p->wmap[i]), W[zi], rows[zi], K, K, sk::BM, bf)) return false;
+    if (i < nz) {
+      p->tile_start[i] = tiles;
+      p->rows[i] = rows[i];
+      p->col_off[i] = col;
+      tiles += (rows[i] + sk::BM - 1) / sk::BM;
+      col += rows[i];
+    }
+  }
+  if (!make_map(reinterpret_cast<CUtensorMap*>(p->xmap), X, 16, K, K, sk::BN, bf)) return false;
+  p->tiles = tiles;
+  p->n_total = col;
+  const int nk = (K + sk::BK - 1) / sk::BK;
+  int splits = bf ? 1 : nsm / tiles;
+  if (splits < 1) splits = 1;
+  if (splits > nk) splits = nk;
+  p->splits = splits;
+  return true;
+}
+
+cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, int nseq, const int* active,
+                       unsigned long long* keys, int* err, cudaStream_t s) {
+  SkinnyArgs a{};
+  a.nz = p.nz;
+  for (int i = 0; i < 3; ++i) {
+    a.tile_start[i] = p.tile_start[i];
+    a.rows[i] = p.rows[i];
+    a.col_off[i] = p.col_off[i];
+  }
+  a.K = p.K;
+  a.splits = p.splits;
+  a.n_total = p.n_total;
+  a.part = part;
+  a.logits = logits;
+  a.V = V;
+  a.nseq = nseq;
+  a.active = active;
+  a.keys = keys;
+  a.err = err;
+  const CUtensorMap* wm = reinterpret_cast<const CUtensorMap*>(p.wmap);
+  const CUtensorMap* xm = reinterpret_cast<const CUtensorMap*>(p.xmap);
+  const dim3 grid(p.tiles, p.splits);
+  if (p.lm)
+    skinny_tc_kernel<true><<<grid, sk::THREADS, sk::SMEM, s>>>(wm[0], wm[1], wm[2], *xm, a);
+  else
+    skinny_tc_kernel<false><<<grid, sk::THREADS, sk::SMEM, s>>>(wm[0], wm[1], wm[2], *xm, a);
+  return cudaGetLastError();
+}
 
 // C[M][N] (fp32, ldc) = / += A[M][K] (fp16, lda) . B[N][K]^T (fp16, ldb) (+ bias[N], bf16)
 cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bias, float* C, int ldc,

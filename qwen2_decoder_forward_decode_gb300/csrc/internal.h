@@ -51,6 +51,11 @@ int attn_nsplit_for(int cap, int chunk_min, int hd, int kv_bytes);
 size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min, int kv_bytes);
 cudaError_t decode_set_attributes(const Dims& d);
 cudaError_t attn_set_attributes(size_t smem);  // not during stream capture
+size_t attn_batched_workspace_bytes(int nq, int nkv, int hd, int nsplit, int nseq);
+cudaError_t launch_attn_batched(int nq, int nkv, int hd, int nsplit, int chunk_min, size_t smem,
+                                const float* q, const __half* kc, const __half* vc, size_t kv_zs, int kv_stride,
+                                const int* d_pos, const int* active, int nseq, __half* out16, void* ws,
+                                cudaStream_t s);
 
 // tl: three timeline slots (start, past the dependency wait, end) or null
 cudaError_t launch_embed(const Dims& d, const void* E, const int* tok, float* x, int* err,
@@ -102,6 +107,7 @@ struct StepLaunch {
   unsigned long long bar_base;  // its value before this launch
   int *abort, *err;
   int nslots, slot, grid;
+  int pf_units;                 // L2 prefetch distance in ring units (0: off)
   size_t smem;
   unsigned long long* tl;       // per phase [start, end, producer issued] or null
   int* diag;                    // 4 ints: first expired wait (site, CTA, warp, detail)
@@ -112,6 +118,48 @@ bool step_kernel_supported(const Dims& d);
 size_t step_part_bytes(const Dims& d);
 cudaError_t step_set_attributes(const Dims& d, int slot_bytes, int* slot_out, int* nslots_out, size_t* smem_out);
 cudaError_t launch_step(const StepLaunch& a, cudaStream_t s);
+
+// ---- gemm_tc.cu: skinny GEMM of batched decode ----
+// Precomputed tensor maps (opaque 128-byte CUtensorMap storage) and the launch shape of one
+// skinny GEMM: nz weight matrices against the 16 activation rows of the sequences.
+struct SkinnyPlan {
+  alignas(64) unsigned char wmap[3][128];
+  alignas(64) unsigned char xmap[128];
+  int nz, K, tiles, splits, n_total;
+  int tile_start[3], rows[3], col_off[3];
+  bool lm;  // bf16 operands, one split, logits + argmax epilogue
+};
+cudaError_t skinny_set_attributes();
+bool skinny_plan(SkinnyPlan* p, int nz, const void* const* W, const int* rows, const void* X, int K, bool bf,
+                 int nsm);
+cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, int nseq, const int* active,
+                       unsigned long long* keys, int* err, cudaStream_t s);
+
+// ---- batched.cu ----
+struct BatchedLayerPlans {
+  SkinnyPlan qkv, o, gu, down;
+};
+// Everything one batched decode step touches (device pointers; plans built at setup).
+struct BatchedCtx {
+  Dims d;
+  const LayerPtrs* layers;          // host array [L]
+  const BatchedLayerPlans* plans;   // host array [L]
+  SkinnyPlan lm;
+  const void *embed, *final_norm;
+  const float2* rope;
+  void* kv;                         // fp16 caches of all sequences
+  size_t kv_seq_elems;              // elements per sequence
+  float *x, *q, *part, *logits;     // x [S][H], q [16][nq*hd], partials, logits [S][V]
+  __half *X16, *O16, *A16;          // fp16 activation rows [16][H], [16][nq*hd], [16][I]
+  __nv_bfloat16* Xb16;              // bf16 rows of the LM head [16][H]
+  int *tok, *pos, *hist, *hist_n, *err;
+  const int* active;                // [S]
+  unsigned long long* keys;         // [S]
+  void* attn_ws;                    // attn_batched_workspace_bytes(.., S)
+  size_t attn_smem;
+};
+cudaError_t batched_set_attributes();
+cudaError_t batched_step(const BatchedCtx& c, cudaStream_t s);
 
 // ---- prefill.cu ----
 struct PrefillBufs {

@@ -29,7 +29,9 @@ namespace step {
 
 constexpr int NCW = 8;                    // consumer warps
 constexpr int NPW = 2;                    // producer warps (each issues every NPW-th unit)
-constexpr int THREADS = (NCW + NPW) * 32;
+constexpr int PF_WARP = NCW + NPW;        // L2 prefetch warp
+constexpr int THREADS = (NCW + NPW + 1) * 32;
+constexpr int MAXQ = 64;                  // QKV items per CTA whose epilogue inputs are staged
 constexpr int NCT = NCW * 32;             // consumer threads
 constexpr int SLOT_DEFAULT = 24 * 1024;   // bytes per ring slot (a unit of whole rows)
 constexpr int MAX_SLOTS = 16;
@@ -59,6 +61,7 @@ struct Params {
   int* err;
   int nslots;
   int slot;         // bytes per ring slot (multiple of 16)
+  int pf_units;     // L2 prefetch distance ahead of the producers, in units (0: off)
   int xs_floats;    // floats of the staged input vector region
   unsigned long long* tl;  // timeline: per phase [start, end, producer issued] (CTA 0), or null
   int* diag;               // [0..3] first expired wait (site, CTA, warp, detail); then per CTA
@@ -161,6 +164,35 @@ __device__ __forceinline__ int unit_len(const Geo& g, int i, int i1) {
   int len = min(g.ipu, i1 - i);
   if (g.cut) len = min(len, g.cut - i % g.cut);
   return len;
+}
+
+// Calls fn(seq, phase, layer weights, geometry, first item, items, chunk) for every unit
+// of this CTA in stream order (per layer: QKV, OPROJ, GATEUP, DOWN; then LM) until fn
+// returns false.
+template <class Fn>
+__device__ __forceinline__ void walk_units(const Params& p, Fn&& fn) {
+  long long seq = 0;
+  for (int l = 0; l <= p.L; ++l) {
+    for (int ph = 0; ph < 5; ++ph) {
+      int phase = ph;
+      if (l == p.L) {
+        if (ph > 0) break;
+        phase = P_LM;
+      } else if (ph == P_ATTN) {
+        continue;
+      }
+      const Geo g = geo(p, phase);
+      const Layer* lw = p.layers + (l < p.L ? l : 0);
+      int i0, i1;
+      item_block(g.n_items, i0, i1);
+      for (int i = i0; i < i1;) {
+        const int len = unit_len(g, i, i1);
+        for (int u = 0; u < g.U; ++u, ++seq)
+          if (!fn(seq, l, phase, lw, g, i, len, u)) return;
+        i += len;
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ bool aborted(const Params& p) { return *(volatile int*)p.abort != 0; }
@@ -592,6 +624,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   __shared__ unsigned long long s_key[NCW];
   __shared__ int s_bad[NCW];
   __shared__ int rel[MAX_SLOTS];  // per slot: sequence number of the last released unit
+  __shared__ long long s_issued;  // last unit producer 0 issued (paces the prefetch warp)
+  __shared__ float4 s_qkv_epi[MAXQ];  // QKV items of this CTA: (bias a, bias b, cos, sin)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = p.nslots;
   const int SLOT = p.slot;
@@ -605,12 +639,47 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       mbar_init(empty0 + 8 * s, 1);
       rel[s] = -1;
     }
+    s_issued = -1;
     mbar_fence_init();
   }
   __syncthreads();
   const int pos = __ldcg(p.pos);  // the token of this step sits at position pos
 
-  // ---------------- producer ----------------
+  // ---------------- L2 prefetch warp ----------------
+  if (warp == PF_WARP) {
+    // Walks the same schedule up to pf_units units ahead of producer 0 and asks L2 for
+    // each unit's rows, so the HBM stream runs on while the consumers are in phases that
+    // move little data (attention, barriers). Advisory: it gives up silently.
+    if (lane != 0 || p.pf_units <= 0) return;
+    walk_units(p, [&](long long seq, int, int phase, const Layer* lw, const Geo& g, int i, int len, int u) {
+      if (seq > *(volatile long long*)&s_issued + p.pf_units) {
+        const long long t0 = clock64();
+        while (seq > *(volatile long long*)&s_issued + p.pf_units) {
+          if (aborted(p) || clock64() - t0 > WAIT_CYCLES) return false;
+        }
+      }
+      const uint32_t rb = (uint32_t)g.K * 2;
+      if (g.U == 1) {
+        if (g.paired) {
+          prefetch_l2_bulk(item_row(p, lw, phase, i, 0), (uint32_t)len * rb);
+          prefetch_l2_bulk(item_row(p, lw, phase, i, 1), (uint32_t)len * rb);
+        } else {
+          prefetch_l2_bulk(item_row(p, lw, phase, i, 0), (uint32_t)consecutive_rows(p, phase, g, i, len) * rb);
+        }
+      } else {
+        const int k0 = u * g.chunk;
+        const uint32_t b = (uint32_t)min(g.chunk, g.K - k0) * 2;
+        prefetch_l2_bulk(item_row(p, lw, phase, i, 0) + k0, b);
+        if (g.paired) prefetch_l2_bulk(item_row(p, lw, phase, i, 1) + k0, b);
+        else if (g.rows == 2 && consecutive_rows(p, phase, g, i, 1) == 2)
+          prefetch_l2_bulk(item_row(p, lw, phase, i, 0) + (size_t)g.K + k0, b);
+      }
+      return true;
+    });
+    return;
+  }
+
+  // ---------------- producers ----------------
   if (warp >= NCW) {
     // Producer warp pw issues the units whose sequence number is pw mod NPW (NS is a
     // multiple of NPW, so its units always land in its own slots). Copies from one thread
@@ -618,86 +687,65 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     // warps keep the stream at full bandwidth.
     if (lane != 0) return;
     const int pw = warp - NCW;
-    long long seq = 0, last = -1;
+    long long last = -1;
     bool ok = !aborted(p);
-    for (int l = 0; l <= p.L && ok; ++l) {
-      for (int ph = 0; ph < 5 && ok; ++ph) {
-        int phase = ph;
-        if (l == p.L) {
-          if (ph > 0) break;
-          phase = P_LM;
-        } else if (ph == P_ATTN) {
-          continue;
-        }
-        const Geo g = geo(p, phase);
-        const Layer* lw = p.layers + (l < p.L ? l : 0);
-        int i0, i1;
-        item_block(g.n_items, i0, i1);
-        const uint32_t rb = (uint32_t)g.K * 2;  // bytes of a full row
-        for (int i = i0; i < i1 && ok;) {
-          const int len = unit_len(g, i, i1);
-          for (int u = 0; u < g.U && ok; ++u, ++seq) {
-            if ((int)(seq % NPW) != pw) continue;
-            const int s = (int)(seq % NS);
-            if (p.tl && blockIdx.x == 0 && pw == 0) {  // ring occupancy statistics (profiling)
-              p.tl[3 * (5 * p.L + 1) + 0] += 1;
-              if (seq >= NS && !mbar_test_now(empty0 + 8 * s, (uint32_t)(((seq / NS) - 1) & 1)))
-                p.tl[3 * (5 * p.L + 1) + 1] += 1;
-            }
-            if (seq >= NS &&
-                !slot_wait(p, empty0 + 8 * s, (uint32_t)(((seq / NS) - 1) & 1), SITE_SLOT_EMPTY, seq)) {
-              ok = false;
-              break;
-            }
-            const uint32_t bar = full0 + 8 * s;
-            const uint32_t dst = ring + s * SLOT;
-            const uint32_t rlo = ring, rhi = ring + (uint32_t)NS * SLOT;
-            const bf16* tb0;
-            const bf16* tb1;
-            size_t te0, te1;
-            item_tensor(p, lw, phase, i, 0, tb0, te0);
-            item_tensor(p, lw, phase, i, 1, tb1, te1);
-            const long long dt = seq * 1000 + phase;
-            bool cok = true;
-            if (g.U == 1) {
-              if (g.paired) {
-                const uint32_t b = (uint32_t)len * rb;
-                mbar_expect_tx(bar, 2 * b);
-                cok = checked_copy(p, dst, item_row(p, lw, phase, i, 0), b, bar, tb0, te0, rlo, rhi, dt) &&
-                      checked_copy(p, dst + (uint32_t)g.ipu * rb, item_row(p, lw, phase, i, 1), b, bar, tb1, te1,
-                                   rlo, rhi, dt);
-              } else {
-                const uint32_t b = (uint32_t)consecutive_rows(p, phase, g, i, len) * rb;
-                mbar_expect_tx(bar, b);
-                cok = checked_copy(p, dst, item_row(p, lw, phase, i, 0), b, bar, tb0, te0, rlo, rhi, dt);
-              }
-            } else {  // one item, K chunk u
-              const int k0 = u * g.chunk;
-              const uint32_t b = (uint32_t)min(g.chunk, g.K - k0) * 2;
-              const bf16* r0 = item_row(p, lw, phase, i, 0) + k0;
-              const bf16* r1 = nullptr;
-              if (g.paired) r1 = item_row(p, lw, phase, i, 1) + k0;
-              else if (g.rows == 2 && consecutive_rows(p, phase, g, i, 1) == 2) r1 = r0 + g.K;
-              mbar_expect_tx(bar, b * (r1 ? 2u : 1u));
-              cok = checked_copy(p, dst, r0, b, bar, tb0, te0, rlo, rhi, dt);
-              if (cok && r1)
-                cok = checked_copy(p, dst + (uint32_t)g.chunk * 2, r1, b, bar, g.paired ? tb1 : tb0, g.paired ? te1 : te0,
-                                   rlo, rhi, dt);
-            }
-            if (!cok) {
-              ok = false;
-              break;
-            }
-            last = seq;
-          }
-          i += len;
-        }
-        if (p.tl && blockIdx.x == 0 && pw == 0) {
-          const int pi = l == p.L ? 5 * p.L : 5 * l + ph;
-          p.tl[3 * pi + 2] = gtime();
-        }
+    if (ok) walk_units(p, [&](long long seq, int l, int phase, const Layer* lw, const Geo& g, int i, int len, int u) {
+      if ((int)(seq % NPW) != pw) return true;
+      const int s = (int)(seq % NS);
+      if (p.tl && blockIdx.x == 0 && pw == 0) {  // ring occupancy statistics (profiling)
+        p.tl[3 * (5 * p.L + 1) + 0] += 1;
+        if (seq >= NS && !mbar_test_now(empty0 + 8 * s, (uint32_t)(((seq / NS) - 1) & 1)))
+          p.tl[3 * (5 * p.L + 1) + 1] += 1;
       }
-    }
+      if (seq >= NS && !slot_wait(p, empty0 + 8 * s, (uint32_t)(((seq / NS) - 1) & 1), SITE_SLOT_EMPTY, seq)) {
+        ok = false;
+        return false;
+      }
+      const uint32_t rb = (uint32_t)g.K * 2;  // bytes of a full row
+      const uint32_t bar = full0 + 8 * s;
+      const uint32_t dst = ring + s * SLOT;
+      const uint32_t rlo = ring, rhi = ring + (uint32_t)NS * SLOT;
+      const bf16* tb0;
+      const bf16* tb1;
+      size_t te0, te1;
+      item_tensor(p, lw, phase, i, 0, tb0, te0);
+      item_tensor(p, lw, phase, i, 1, tb1, te1);
+      const long long dt = seq * 1000 + phase;
+      bool cok = true;
+      if (g.U == 1) {
+        if (g.paired) {
+          const uint32_t b = (uint32_t)len * rb;
+          mbar_expect_tx(bar, 2 * b);
+          cok = checked_copy(p, dst, item_row(p, lw, phase, i, 0), b, bar, tb0, te0, rlo, rhi, dt) &&
+                checked_copy(p, dst + (uint32_t)g.ipu * rb, item_row(p, lw, phase, i, 1), b, bar, tb1, te1,
+                             rlo, rhi, dt);
+        } else {
+          const uint32_t b = (uint32_t)consecutive_rows(p, phase, g, i, len) * rb;
+          mbar_expect_tx(bar, b);
+          cok = checked_copy(p, dst, item_row(p, lw, phase, i, 0), b, bar, tb0, te0, rlo, rhi, dt);
+        }
+      } else {  // one item, K chunk u
+        const int k0 = u * g.chunk;
+        const uint32_t b = (uint32_t)min(g.chunk, g.K - k0) * 2;
+        const bf16* r0 = item_row(p, lw, phase, i, 0) + k0;
+        const bf16* r1 = nullptr;
+        if (g.paired) r1 = item_row(p, lw, phase, i, 1) + k0;
+        else if (g.rows == 2 && consecutive_rows(p, phase, g, i, 1) == 2) r1 = r0 + g.K;
+        mbar_expect_tx(bar, b * (r1 ? 2u : 1u));
+        cok = checked_copy(p, dst, r0, b, bar, tb0, te0, rlo, rhi, dt);
+        if (cok && r1)
+          cok = checked_copy(p, dst + (uint32_t)g.chunk * 2, r1, b, bar, g.paired ? tb1 : tb0, g.paired ? te1 : te0,
+                             rlo, rhi, dt);
+      }
+      if (!cok) {
+        ok = false;
+        return false;
+      }
+      last = seq;
+      if (pw == 0) *(volatile long long*)&s_issued = seq;
+      if (p.tl && blockIdx.x == 0 && pw == 0) p.tl[3 * (l == p.L ? 5 * p.L : 5 * l + phase) + 2] = gtime();
+      return true;
+    });
     // let every copy this warp issued land before the CTA may finish
     for (long long k = last - NS + 1 > 0 ? last - NS + 1 : 0; k <= last; ++k) {
       if ((int)(k % NPW) != pw) continue;
@@ -706,6 +754,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       while (!mbar_test_now(full0 + 8 * s, (uint32_t)((k / NS) & 1)) && clock64() - t0 < WAIT_CYCLES) {
       }
     }
+    if (pw == 0 && ok) *(volatile long long*)&s_issued = 1ll << 60;  // release the prefetch warp
     return;
   }
 
@@ -719,6 +768,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   int best_i = -1;
   bool nonfinite = false;
 
+  int phase_no = 0;
+  auto stamp = [&](int which) {  // CTA 0: [start, end] of consumer phase phase_no
+    if (p.tl && blockIdx.x == 0 && ct == 0) p.tl[3 * phase_no + which] = gtime();
+  };
+  auto substamp = [&](int which) {  // CTA 0: [input staged, first unit ready, units done]
+    if (p.tl && blockIdx.x == 0 && ct == 0) p.tl[3 * (5 * p.L + 2 + phase_no) + which] = gtime();
+  };
   // consume one weight phase: warp w takes every NCW-th unit of this CTA's block; per item
   // it reduces the rows (over the chunk units of the item when K was split) and runs the
   // epilogue
@@ -748,6 +804,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
             ok = false;
             break;
           }
+          if (unit == 0 && u == 0) substamp(1);
           const unsigned char* slot = dsm + (size_t)s * SLOT;
           {  // the rows this unit reads must lie inside its slot, x inside the staged vector
             const size_t need = g.U == 1 ? (g.paired ? (size_t)(g.ipu + len) * rb : (size_t)g.rows * len * rb)
@@ -759,6 +816,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
               break;
             }
           }
+          float e0 = 0.f, e1 = 0.f;
           if (g.U == 1) {  // whole rows of len items
             const int nv = g.K >> 3;
             const float4* x4 = reinterpret_cast<const float4*>(xs);
@@ -782,7 +840,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
               }
               b0 = warp_sum(b0);
               if (g.rows == 2) b1 = warp_sum(b1);
-              if (lane == 0) epilogue(i + t, b0, b1);
+              if (lane == t) {  // lane t keeps item t; the epilogues run side by side below
+                e0 = b0;
+                e1 = b1;
+              }
             }
           } else {  // chunk u of one item
             const int k0 = u * g.chunk;
@@ -803,6 +864,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
             *(volatile int*)(rel + s) = (int)sq;
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * s) : "memory");
           }
+          if (g.U == 1 && lane < len) epilogue(i + lane, e0, e1);
         }
         if (ok && g.U > 1) {
           a0 = warp_sum(a0);
@@ -814,41 +876,58 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       i += len;
     }
     base = seq;
+    substamp(2);  // warp 0 done with its units
     return ok;
   };
 
   bool ok = !aborted(p);  // a failed earlier launch leaves the model unusable: return fast
-  int phase_no = 0;
-  auto stamp = [&](int which) {  // CTA 0: [start, end] of consumer phase phase_no
-    if (p.tl && blockIdx.x == 0 && ct == 0) p.tl[3 * phase_no + which] = gtime();
-  };
   for (int l = 0; l < p.L && ok; ++l) {
     const Layer& w = p.layers[l];
     f16* kc = p.kv + (size_t)l * 2 * p.nkv * p.cap * p.hd;
     f16* vc = kc + (size_t)p.nkv * p.cap * p.hd;
     // ---- QKV
     stamp(0);
-    if (l == 0) stage_embed(p, xs, scratch, w.in_norm);
-    else stage_norm(p, xs, scratch, p.x, w.in_norm, p.H);
-    ok = run_phase(P_QKV, l, [&](int item, float a, float b) {
-      int head = item / half;
-      const int i = item - head * half;
+    int q0, q1;  // this CTA's QKV items; their bias pairs and rotations are staged first
+    item_block((p.nq + 2 * p.nkv) * half, q0, q1);
+    auto qkv_epi = [&](int item) -> float4 {
+      const int head = item / half, i = item - head * half;
       const bf16* bias;
       int h;
       if (head < p.nq) { bias = w.bq; h = head; }
       else if (head < p.nq + p.nkv) { bias = w.bk; h = head - p.nq; }
       else { bias = w.bv; h = head - p.nq - p.nkv; }
+      float4 e = make_float4(0.f, 0.f, 1.f, 0.f);
       if (bias) {
-        a += __bfloat162float(bias[h * p.hd + i]);
-        b += __bfloat162float(bias[h * p.hd + i + half]);
+        e.x = __bfloat162float(bias[h * p.hd + i]);
+        e.y = __bfloat162float(bias[h * p.hd + i + half]);
       }
-      if (item < 0 || item >= (p.nq + 2 * p.nkv) * half || pos < 0 || pos >= p.cap) {
+      if (head < p.nq + p.nkv && pos >= 0 && pos < p.cap) {
+        const float2 cs = p.rope[(size_t)pos * half + i];
+        e.z = cs.x;
+        e.w = cs.y;
+      }
+      return e;
+    };
+    if (ct < q1 - q0 && ct < MAXQ) s_qkv_epi[ct] = qkv_epi(q0 + ct);  // published by the norm's barriers
+    if (l == 0) stage_embed(p, xs, scratch, w.in_norm);
+    else stage_norm(p, xs, scratch, p.x, w.in_norm, p.H);
+    substamp(0);
+    ok = run_phase(P_QKV, l, [&](int item, float a, float b) {
+      int head = item / half;
+      const int i = item - head * half;
+      int h;
+      if (head < p.nq) h = head;
+      else if (head < p.nq + p.nkv) h = head - p.nq;
+      else h = head - p.nq - p.nkv;
+      if (item < q0 || item >= q1 || pos < 0 || pos >= p.cap) {
         raise_abort(p, SITE_STORE, item);
         return;
       }
+      const float4 e = item - q0 < MAXQ ? s_qkv_epi[item - q0] : qkv_epi(item);
+      a += e.x;
+      b += e.y;
       if (head < p.nq + p.nkv) {
-        const float2 cs = p.rope[(size_t)pos * half + i];
-        const float ra = a * cs.x - b * cs.y, rb = b * cs.x + a * cs.y;
+        const float ra = a * e.z - b * e.w, rb = b * e.z + a * e.w;
         a = ra;
         b = rb;
       }
@@ -880,6 +959,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     // ---- OPROJ: merge the partials into xs = attention output, then x += Wo . xs
     stamp(0);
     merge_partials(p, xs, nsplit);
+    substamp(0);
     ok = cbar_and(run_phase(P_OPROJ, l, [&](int item, float a, float b) {
       if (item < 0 || 2 * item >= p.H) { raise_abort(p, SITE_STORE, 100000 + item); return; }
       atomicAdd(p.x + 2 * item, a);
@@ -892,6 +972,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     // ---- GATEUP
     stamp(0);
     stage_norm(p, xs, scratch, p.x, w.post_norm, p.H);
+    substamp(0);
     ok = cbar_and(run_phase(P_GATEUP, l, [&](int item, float gt, float up) {
       if (item < 0 || item >= p.I) { raise_abort(p, SITE_STORE, 200000 + item); return; }
       p.act[item] = (gt / (1.f + expf(-gt))) * up;
@@ -903,6 +984,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     // ---- DOWN
     stamp(0);
     stage_copy(xs, p.act, p.I);
+    substamp(0);
     ok = cbar_and(run_phase(P_DOWN, l, [&](int item, float a, float) {
       if (item < 0 || item >= p.H) { raise_abort(p, SITE_STORE, 300000 + item); return; }
       atomicAdd(p.x + item, a);
@@ -916,11 +998,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   if (ok) {
     stamp(0);
     stage_norm(p, xs, scratch, p.x, p.final_norm, p.H);
+    substamp(0);
     auto take = [&](int r, float v) {
       if (r < 0 || r >= p.V) { raise_abort(p, SITE_STORE, 400000 + r); return; }
       p.logits[r] = v;
       if (!isfinite(v)) nonfinite = true;
-      if (v > best_v || best_i < 0) {  // a warp sees its rows in increasing order
+      if (v > best_v || best_i < 0) {  // a lane sees its rows in increasing order
         best_v = v;
         best_i = r;
       }
@@ -929,9 +1012,18 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       take(2 * item, a);
       if (2 * item + 1 < p.V) take(2 * item + 1, b);
     }));
-    if (lane == 0) {
-      s_key[warp] = best_i >= 0 ? argmax_key(best_v, best_i) : 0ull;
-      s_bad[warp] = nonfinite;
+    {  // every lane kept the best of its own rows (seen in increasing order): warp maximum
+      unsigned long long k = best_i >= 0 ? argmax_key(best_v, best_i) : 0ull;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
+        k = other > k ? other : k;
+      }
+      const bool bad = __any_sync(0xffffffffu, nonfinite);
+      if (lane == 0) {
+        s_key[warp] = k;
+        s_bad[warp] = bad;
+      }
     }
     cbar();
     if (ct == 0) {
@@ -1015,7 +1107,7 @@ cudaError_t launch_step(const StepLaunch& a, cudaStream_t s) {
   p.x = a.x; p.q = a.q; p.act = a.act; p.logits = a.logits; p.part = a.part;
   p.tok = a.tok; p.pos = a.pos; p.key = a.key; p.hist = a.hist; p.hist_n = a.hist_n; p.hist_cap = a.hist_cap;
   p.bar = a.bar; p.bar_base = a.bar_base; p.abort = a.abort; p.err = a.err;
-  p.nslots = a.nslots; p.slot = a.slot; p.xs_floats = step_xs_floats(a.d);
+  p.nslots = a.nslots; p.slot = a.slot; p.pf_units = a.pf_units; p.xs_floats = step_xs_floats(a.d);
   p.tl = a.tl;
   p.diag = a.diag;
   cudaLaunchConfig_t cfg = {};
