@@ -414,6 +414,73 @@ def run_native(args):
         torch.distributed.destroy_process_group()
 
 
+def run_batched(args):
+    """Batched decode of 16 sequences (prompt lengths uniform in 256..2048, 128 tokens each,
+    KV cache 2304): prefill every sequence, then 127 decode steps of all 16 together.
+    Prints one JSON line with "profile_run": "batched"; not the headline bench line."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from qwen2_decoder_forward_decode_gb300 import DeviceWeights, Model
+    from synth import make_batch_prompts
+
+    torch.cuda.set_device(0)
+    wl = WORKLOADS["1p5b_batch"]
+    s = SHAPES[wl.shape]
+    if args.layers:
+        import dataclasses
+        s = dataclasses.replace(s, n_layers=args.layers)
+    B, n_dec = 16, wl.new_tokens - 1
+    prompts = make_batch_prompts(s, B, 256, 2048)
+    cap = 2304
+    w = make_weights(s)
+    dw = DeviceWeights(w, 1)
+    stream = torch.cuda.Stream()
+    m = Model(s, dw, cap, max_seqs=B, stream=stream.cuda_stream)
+    ids = [torch.from_numpy(p).cuda() for p in prompts]
+    torch.cuda.synchronize()
+
+    def prefill_all():
+        for b in range(B):
+            m.prefill_device(ids[b].data_ptr(), len(prompts[b]), seq=b)
+
+    for _ in range(args.warmup):
+        prefill_all()
+        m.decode_steps(n_dec)
+    m.sync()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clk:
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            prefill_all()
+            ev[k][1].record(stream)
+            m.decode_steps(n_dec)
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+    m.sync()
+    dec_s = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)) / 1000.0
+    pre_s = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)) / 1000.0
+    tokens = B * n_dec * args.steps
+    # algorithmic bytes of one batched step: the weights once, every sequence's KV rows
+    lens = np.array([len(p) for p in prompts], dtype=np.float64)
+    ctx_mean = lens + (n_dec - 1) / 2.0 + 1  # positions read per sequence, mean over steps
+    weights = decode_bytes_per_token(s, 0) - s.vocab * 4
+    kv = sum(decode_bytes_per_token(s, c) - decode_bytes_per_token(s, 0) for c in ctx_mean)
+    step_bytes = weights + kv + B * s.vocab * 4
+    step_s = dec_s / (n_dec * args.steps)
+    peak, peak_kind = read_peaks()
+    out = {"profile_run": "batched", "metric": "batched decode tok/s (Qwen2.5-1.5B shape, 16 sequences, bf16)",
+           "value": tokens / dec_s, "unit": "tok/s", "steps": args.steps, "warmup": args.warmup,
+           "layers": s.n_layers, "ms_per_decode_step": 1000.0 * step_s,
+           "prefill_tok_s": float(lens.sum()) * args.steps / pre_s,
+           "bytes_per_step": step_bytes, "achieved_gbs": step_bytes / step_s / 1e9,
+           "peak_gbs": peak, "peak_kind": peak_kind, "frac": step_bytes / step_s / 1e9 / peak,
+           "prompt_tokens": int(lens.sum()), "clocks": clk.summary()}
+    print(json.dumps(out), flush=True)
+    m.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -425,8 +492,12 @@ def main():
                     help="also print a device timeline summary of single decode steps")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: build the 1.5B shape with this many layers")
+    ap.add_argument("--batched", action="store_true",
+                    help="measure batched decode of 16 sequences instead (one JSON line, not the bench line)")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.batched:
+        run_batched(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_native(args)

@@ -397,7 +397,7 @@ cudaError_t launch_attn_batched(int nq, int nkv, int hd, int nsplit, int chunk_m
   AttnArgs<f16> a{q, kc, vc, kv_stride, hd, G, nsplit, chunk_min, 0, d_pos, 1.f / sqrtf((float)hd), nullptr,
                   (float*)ws, (unsigned int*)((char*)ws + part_bytes * nseq), nullptr,
                   (size_t)nq * hd, kv_zs, (size_t)nq * hd, part_bytes / sizeof(float), nkv, out16, active};
-  return launch_k(attn_decode_kernel<f16>, dim3(nkv, nsplit, nseq), dim3(ATTN_THREADS), smem, s, false, a);
+  return launch_k(attn_decode_kernel<f16>, dim3(nkv, nsplit, nseq), dim3(ATTN_THREADS), smem, s, batched_pdl(), a);
 }
 
 cudaError_t attn_set_attributes(size_t smem) {

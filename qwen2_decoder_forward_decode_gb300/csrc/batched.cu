@@ -22,54 +22,87 @@
 #include "internal.h"
 
 #include <math.h>
+#include <stdlib.h>
 
 namespace qw {
 
 constexpr int BT = 256;  // threads of the element-wise kernels
 
-__global__ void bembed_kernel(const bf16* E, int V, int H, const int* tok, const int* active, int nseq,
-                              float* x, int* err) {
-  const int b = blockIdx.x;
-  if (b >= nseq || !active[b]) return;
-  int t = __ldcg(tok + b);
-  if (t < 0 || t >= V) {
-    if (threadIdx.x == 0) atomicOr(err, ERR_TOKEN);
-    t = 0;
-  }
-  const bf16* row = E + (size_t)t * H;
-  float* xb = x + (size_t)b * H;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) xb[k] = __bfloat162float(row[k]);
+constexpr int MAX_SPLITS = SKINNY_MAX_SPLITS;
+
+// Sum of the split partials of column c of sequence b (fixed split order); every load is
+// issued before the first add.
+__device__ __forceinline__ float psum(const float* part, int splits, int n_total, int b, int c) {
+  float v[MAX_SPLITS];
+#pragma unroll
+  for (int s = 0; s < MAX_SPLITS; ++s) v[s] = s < splits ? __ldcg(part + ((size_t)s * 16 + b) * n_total + c) : 0.f;
+  float acc = 0.f;
+#pragma unroll
+  for (int s = 0; s < MAX_SPLITS; ++s) acc += v[s];
+  return acc;
 }
 
-// out row b = x[b] / sqrt(mean(x[b]^2) + eps) * gain, as OutT (fp16 or bf16); rows of
-// absent or inactive sequences are zero
+constexpr int RN_THREADS = 512;
+constexpr int RN_COLS = 4;  // columns per thread: H <= RN_THREADS * RN_COLS
+
+// Row b of out = RMSNorm(x[b]) * gain after x[b] += the split partials (part may be null:
+// no residual add; embed non-null: x[b] = embedding row of tok[b] first). One CTA per
+// sequence; every load of the row is issued before the first use. Rows of absent or
+// inactive sequences are zero.
 template <typename OutT>
-__global__ void bnorm_kernel(const float* x, const bf16* gain, int H, float eps, const int* active, int nseq,
-                             OutT* out) {
+__global__ void __launch_bounds__(RN_THREADS) bresid_norm_kernel(const float* part, int splits, int n_total,
+                                                                 const bf16* embed, int V, const int* tok,
+                                                                 float* x, const bf16* gain, int H, float eps,
+                                                                 const int* active, int nseq, OutT* out, int* err) {
   __shared__ float scratch[32];
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   OutT* o = out + (size_t)b * H;
   if (b >= nseq || !active[b]) {
-    for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = from_f32<OutT>(0.f);
+    for (int k = threadIdx.x; k < H; k += RN_THREADS) o[k] = from_f32<OutT>(0.f);
     return;
   }
-  const float* xb = x + (size_t)b * H;
+  float* xb = x + (size_t)b * H;
+  const bf16* erow = nullptr;
+  if (embed) {
+    int t = __ldcg(tok + b);
+    if (t < 0 || t >= V) {
+      if (threadIdx.x == 0) atomicOr(err, ERR_TOKEN);
+      t = 0;
+    }
+    erow = embed + (size_t)t * H;
+  }
+  float v[RN_COLS], g[RN_COLS];
+#pragma unroll
+  for (int j = 0; j < RN_COLS; ++j) {
+    const int k = threadIdx.x + j * RN_THREADS;
+    v[j] = 0.f;
+    g[j] = 0.f;
+    if (k < H) {
+      v[j] = erow ? __bfloat162float(erow[k]) : __ldcg(xb + k);
+      g[j] = __bfloat162float(gain[k]);
+      if (part) v[j] += psum(part, splits, n_total, b, k);
+    }
+  }
   float ss = 0.f;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) {
-    const float v = __ldcg(xb + k);
-    ss = fmaf(v, v, ss);
+#pragma unroll
+  for (int j = 0; j < RN_COLS; ++j) {
+    const int k = threadIdx.x + j * RN_THREADS;
+    if (k < H) {
+      if (part || erow) xb[k] = v[j];
+      ss = fmaf(v[j], v[j], ss);
+    }
   }
   ss = block_sum(ss, scratch);
   const float inv = rsqrtf(ss / (float)H + eps);
-  for (int k = threadIdx.x; k < H; k += blockDim.x) o[k] = from_f32<OutT>(__ldcg(xb + k) * inv * __bfloat162float(gain[k]));
+#pragma unroll
+  for (int j = 0; j < RN_COLS; ++j) {
+    const int k = threadIdx.x + j * RN_THREADS;
+    if (k < H) o[k] = from_f32<OutT>(v[j] * inv * g[j]);
+  }
 }
 
-// Sum of the split partials of column c of sequence b (fixed split order).
-__device__ __forceinline__ float psum(const float* part, int splits, int n_total, int b, int c) {
-  float acc = 0.f;
-  for (int s = 0; s < splits; ++s) acc += __ldcg(part + ((size_t)s * 16 + b) * n_total + c);
-  return acc;
-}
 
 // q/k/v of sequence b from the partials: + bias, split-half RoPE of q and k at pos[b], q to
 // q_out[b], k and v appended to the sequence's cache at pos[b]. One thread per RoPE pair.
@@ -77,6 +110,8 @@ __global__ void bqkv_epi_kernel(const float* part, int splits, int n_total, int 
                                 const bf16* bq, const bf16* bk, const bf16* bv, const float2* rope,
                                 const int* pos, const int* active, float* q_out, f16* kc0, size_t kv_zs,
                                 int cap, int* err) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.y;
   if (!active[b]) return;
   const int half = hd >> 1;
@@ -116,19 +151,12 @@ __global__ void bqkv_epi_kernel(const float* part, int splits, int n_total, int 
   }
 }
 
-// x[b][n] += sum of the partials of column n (n < N)
-__global__ void bresid_kernel(const float* part, int splits, int n_total, int N, float* x, const int* active) {
-  const int b = blockIdx.y;
-  if (!active[b]) return;
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= N) return;
-  x[(size_t)b * N + n] += psum(part, splits, n_total, b, n);
-}
-
 // A[b][i] = silu(gate) * up as fp16 (gate columns [0, I), up columns [I, 2I)); rows of
 // absent or inactive sequences are zero
 __global__ void bswiglu_kernel(const float* part, int splits, int n_total, int I, const int* active, int nseq,
                                f16* A) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= I) return;
@@ -143,6 +171,8 @@ __global__ void bswiglu_kernel(const float* part, int splits, int n_total, int I
 // per active sequence: token = argmax (lowest index among equal maxima), history, length
 __global__ void bfinalize_kernel(unsigned long long* keys, int* tok, int* pos, int* hist, int* hist_n, int cap,
                                  const int* active, int nseq) {
+  pdl_wait();
+  pdl_trigger();
   const int b = threadIdx.x;
   if (b >= nseq || !active[b]) return;
   const unsigned long long k = keys[b];
@@ -157,43 +187,70 @@ __global__ void bfinalize_kernel(unsigned long long* keys, int* tok, int* pos, i
 
 cudaError_t batched_set_attributes() { return skinny_set_attributes(); }
 
+// Programmatic dependent launch between the kernels of a batched step (QW_BATCHED_NOPDL=1:
+// plain stream order, for comparison).
+bool batched_pdl() {
+  static const bool on = [] {
+    const char* v = std::getenv("QW_BATCHED_NOPDL");
+    return !(v && v[0] == '1');
+  }();
+  return on;
+}
+
 cudaError_t batched_step(const BatchedCtx& c, cudaStream_t s) {
+  const bool pdl = batched_pdl();
   const Dims& d = c.d;
-  const int S = d.max_seqs, H = d.H, qd = d.nq * d.hd, I = d.I;
+  const int S = d.max_seqs, H = d.H, I = d.I;
+  if (H > RN_THREADS * RN_COLS) return cudaErrorInvalidValue;
   cudaError_t e;
-  bembed_kernel<<<S, BT, 0, s>>>((const bf16*)c.embed, d.V, H, c.tok, c.active, S, c.x, c.err);
-  if ((e = cudaGetLastError())) return e;
+  const dim3 rn_grid(16), rn_block(RN_THREADS);
+  const float* no_part = nullptr;
+  const bf16* no_embed = nullptr;
+  const int* no_tok = nullptr;
+  // layer 0 input: embedding rows, then the first RMSNorm
+  if ((e = launch_k(bresid_norm_kernel<f16>, rn_grid, rn_block, 0, s, pdl, no_part, 0, 0, (const bf16*)c.embed,
+                    d.V, (const int*)c.tok, c.x, (const bf16*)c.layers[0].in_norm, H, d.eps, c.active, S, c.X16,
+                    c.err)))
+    return e;
   for (int l = 0; l < d.L; ++l) {
     const LayerPtrs& w = c.layers[l];
     const BatchedLayerPlans& pl = c.plans[l];
     f16* kc0 = (f16*)c.kv + (size_t)l * 2 * d.nkv * d.cap * d.hd;  // layer l of sequence 0
-    bnorm_kernel<f16><<<16, BT, 0, s>>>(c.x, (const bf16*)w.in_norm, H, d.eps, c.active, S, c.X16);
     if ((e = skinny_run(pl.qkv, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
     const int pairs = (d.nq + 2 * d.nkv) * (d.hd / 2);
-    bqkv_epi_kernel<<<dim3((pairs + BT - 1) / BT, S), BT, 0, s>>>(
-        c.part, pl.qkv.splits, pl.qkv.n_total, d.nq, d.nkv, d.hd, (const bf16*)w.bq, (const bf16*)w.bk,
-        (const bf16*)w.bv, c.rope, c.pos, c.active, c.q, kc0, c.kv_seq_elems, d.cap, c.err);
-    if ((e = cudaGetLastError())) return e;
+    if ((e = launch_k(bqkv_epi_kernel, dim3((pairs + BT - 1) / BT, S), dim3(BT), 0, s, pdl, (const float*)c.part,
+                      pl.qkv.splits, pl.qkv.n_total, d.nq, d.nkv, d.hd, (const bf16*)w.bq, (const bf16*)w.bk,
+                      (const bf16*)w.bv, c.rope, (const int*)c.pos, c.active, c.q, kc0, c.kv_seq_elems, d.cap,
+                      c.err)))
+      return e;
     if ((e = launch_attn_batched(d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min, c.attn_smem, c.q, kc0,
                                  kc0 + (size_t)d.nkv * d.cap * d.hd, c.kv_seq_elems, d.cap, c.pos, c.active, S,
                                  c.O16, c.attn_ws, s)))
       return e;
     if ((e = skinny_run(pl.o, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
-    bresid_kernel<<<dim3((H + BT - 1) / BT, S), BT, 0, s>>>(c.part, pl.o.splits, pl.o.n_total, H, c.x, c.active);
-    bnorm_kernel<f16><<<16, BT, 0, s>>>(c.x, (const bf16*)w.post_norm, H, d.eps, c.active, S, c.X16);
+    if ((e = launch_k(bresid_norm_kernel<f16>, rn_grid, rn_block, 0, s, pdl, (const float*)c.part, pl.o.splits,
+                      pl.o.n_total, no_embed, 0, no_tok, c.x, (const bf16*)w.post_norm, H, d.eps, c.active, S, c.X16,
+                      c.err)))
+      return e;
     if ((e = skinny_run(pl.gu, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
-    bswiglu_kernel<<<dim3((I + BT - 1) / BT, 16), BT, 0, s>>>(c.part, pl.gu.splits, pl.gu.n_total, I, c.active,
-                                                              S, c.A16);
+    if ((e = launch_k(bswiglu_kernel, dim3((I + BT - 1) / BT, 16), dim3(BT), 0, s, pdl, (const float*)c.part,
+                      pl.gu.splits, pl.gu.n_total, I, c.active, S, c.A16)))
+      return e;
     if ((e = skinny_run(pl.down, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
-    bresid_kernel<<<dim3((H + BT - 1) / BT, S), BT, 0, s>>>(c.part, pl.down.splits, pl.down.n_total, H, c.x,
-                                                            c.active);
-    if ((e = cudaGetLastError())) return e;
+    // x += down partials, then the next layer's input norm (fp16) or the final norm (bf16)
+    if (l + 1 < d.L)
+      e = launch_k(bresid_norm_kernel<f16>, rn_grid, rn_block, 0, s, pdl, (const float*)c.part, pl.down.splits,
+                   pl.down.n_total, no_embed, 0, no_tok, c.x, (const bf16*)c.layers[l + 1].in_norm, H, d.eps,
+                   c.active, S, c.X16, c.err);
+    else
+      e = launch_k(bresid_norm_kernel<bf16>, rn_grid, rn_block, 0, s, pdl, (const float*)c.part, pl.down.splits,
+                   pl.down.n_total, no_embed, 0, no_tok, c.x, (const bf16*)c.final_norm, H, d.eps, c.active, S,
+                   c.Xb16, c.err);
+    if (e) return e;
   }
-  bnorm_kernel<bf16><<<16, BT, 0, s>>>(c.x, (const bf16*)c.final_norm, H, d.eps, c.active, S, c.Xb16);
   if ((e = skinny_run(c.lm, nullptr, c.logits, d.V, S, c.active, c.keys, c.err, s))) return e;
-  bfinalize_kernel<<<1, 32, 0, s>>>(c.keys, c.tok, c.pos, c.hist, c.hist_n, d.cap, c.active, S);
-  (void)qd;
-  return cudaGetLastError();
+  return launch_k(bfinalize_kernel, dim3(1), dim3(32), 0, s, pdl, c.keys, c.tok, c.pos, c.hist, c.hist_n, d.cap,
+                  c.active, S);
 }
 
 }  // namespace qw

@@ -331,7 +331,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // The LM-head variant (one split) stores the logits of active sequences and folds each
 // warp's rows into per-sequence packed argmax keys.
 namespace sk {
-constexpr int BM = 128, BN = 16, BK = 64, STAGES = 8, THREADS = 192;
+constexpr int BM = 128, BN = 16, BK = 64, STAGES = 6, THREADS = 192;
 constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE = A_BYTES + B_BYTES;
 constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 + 256;
 }  // namespace sk
@@ -389,11 +389,23 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---- TMA producer: 128 weight rows and the 16 activation rows per 64-wide K block
-    int issued = 0;
-    for (int kb = kb0; kb < kb1; ++kb) {
+    // ---- TMA producer: 128 weight rows and the 16 activation rows per 64-wide K block.
+    // The weights of the first stages do not depend on the preceding kernels: they are
+    // requested before the dependency wait, their activation rows after it.
+    const int pre = min(STAGES, kb1 - kb0);
+    for (int j = 0; j < pre; ++j) {
+      const uint32_t a_dst = tc::smem_u32(smem + j * STAGE);
+      tc::mbar_expect_tx(full0 + 8 * j, STAGE);
+      tc::tma_load_2d(a_dst, wm, full0 + 8 * j, (kb0 + j) * BK, m0);
+    }
+    pdl_wait();
+    pdl_trigger();
+    for (int j = 0; j < pre; ++j)
+      tc::tma_load_2d(tc::smem_u32(smem + j * STAGE) + A_BYTES, &xm, full0 + 8 * j, (kb0 + j) * BK, 0);
+    int issued = pre;
+    for (int kb = kb0 + pre; kb < kb1; ++kb) {
       const int j = kb - kb0, s = j % STAGES;
-      if (j >= STAGES && !tc::mbar_wait(empty0 + 8 * s, ((j / STAGES) & 1) ^ 1, a.err)) { s_abort = 1; break; }
+      if (!tc::mbar_wait(empty0 + 8 * s, ((j / STAGES) & 1) ^ 1, a.err)) { s_abort = 1; break; }
       if (s_abort) break;
       const uint32_t a_dst = tc::smem_u32(smem + s * STAGE);
       tc::mbar_expect_tx(full0 + 8 * s, STAGE);
@@ -422,6 +434,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
     if (ok && kb1 > kb0) tc::mma_commit(accum);
   } else if (warp >= 2) {
     // ---- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = weight rows of the tile
+    pdl_wait();  // the partial buffer and the flags belong to the preceding kernels until then
     const int q = warp & 3;
     const int r = m0 + q * 32 + lane;
     float v[16];
@@ -561,6 +574,7 @@ bool skinny_plan(SkinnyPlan* p, int nz, const void* const* W, const int* rows, c
   int splits = bf ? 1 : nsm / tiles;
   if (splits < 1) splits = 1;
   if (splits > nk) splits = nk;
+  if (splits > SKINNY_MAX_SPLITS) splits = SKINNY_MAX_SPLITS;  // the consumers sum at most this many
   p->splits = splits;
   return true;
 }
@@ -587,11 +601,9 @@ cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, i
   const CUtensorMap* wm = reinterpret_cast<const CUtensorMap*>(p.wmap);
   const CUtensorMap* xm = reinterpret_cast<const CUtensorMap*>(p.xmap);
   const dim3 grid(p.tiles, p.splits);
-  if (p.lm)
-    skinny_tc_kernel<true><<<grid, sk::THREADS, sk::SMEM, s>>>(wm[0], wm[1], wm[2], *xm, a);
-  else
-    skinny_tc_kernel<false><<<grid, sk::THREADS, sk::SMEM, s>>>(wm[0], wm[1], wm[2], *xm, a);
-  return cudaGetLastError();
+  const bool pdl = batched_pdl();
+  if (p.lm) return launch_k(skinny_tc_kernel<true>, grid, dim3(sk::THREADS), sk::SMEM, s, pdl, wm[0], wm[1], wm[2], *xm, a);
+  return launch_k(skinny_tc_kernel<false>, grid, dim3(sk::THREADS), sk::SMEM, s, pdl, wm[0], wm[1], wm[2], *xm, a);
 }
 
 // C[M][N] (fp32, ldc) = / += A[M][K] (fp16, lda) . B[N][K]^T (fp16, ldb) (+ bias[N], bf16)

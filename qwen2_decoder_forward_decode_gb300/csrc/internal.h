@@ -159,6 +159,8 @@ struct BatchedCtx {
   size_t attn_smem;
 };
 cudaError_t batched_set_attributes();
+bool batched_pdl();
+constexpr int SKINNY_MAX_SPLITS = 16;  // split-K partials one consumer thread sums
 cudaError_t batched_step(const BatchedCtx& c, cudaStream_t s);
 
 // ---- prefill.cu ----
