@@ -103,6 +103,8 @@ __device__ __forceinline__ void prologue_copy(float* xs, const float* x, int K) 
 template <typename T, typename KV>
 struct OpQKV {
   static constexpr bool PAIRED = true, NORM = true;
+  static constexpr bool L2_PREWAIT = false;
+  static constexpr bool LANE_EPI = true;
   static constexpr int RPI = 2;
   int K, n_items, hd, nq, nkv, cap;
   const T *wq, *wk, *wv, *bq, *bk, *bv, *gain;
@@ -183,6 +185,8 @@ struct OpQKV {
 template <typename T>
 struct OpGateUp {
   static constexpr bool PAIRED = true, NORM = true;
+  static constexpr bool L2_PREWAIT = true;  // resident during attention, when HBM is idle
+  static constexpr bool LANE_EPI = true;    // epilogues of different items may run on any lanes
   static constexpr int RPI = 2;
   int K, n_items;
   const T *wg, *wu, *gain;
@@ -203,6 +207,8 @@ struct OpGateUp {
 template <typename T, int RPI_>
 struct OpResid {
   static constexpr bool PAIRED = false, NORM = false;
+  static constexpr bool L2_PREWAIT = false;
+  static constexpr bool LANE_EPI = true;
   static constexpr int RPI = RPI_;
   int K, n_items, N;
   const T* W;
@@ -231,6 +237,8 @@ struct OpResid {
 template <typename T>
 struct OpLMHead {
   static constexpr bool PAIRED = false, NORM = true;
+  static constexpr bool L2_PREWAIT = false;
+  static constexpr bool LANE_EPI = false;  // the argmax state lives in lane 0
   static constexpr int RPI = 2;
   int K, n_items, N;
   const T *W, *gain;
@@ -322,6 +330,7 @@ struct GemvCfg {
   unsigned long long* tl;  // timeline slots or null
 };
 constexpr int MAX_SLOTS = 8;
+constexpr int MAX_DEFER = 16;  // items per warp whose K-split partials wait in shared memory
 
 template <typename T, int MAXV, class Op>
 __global__ void __launch_bounds__(GEMV_WARPS * 32, 2)
@@ -331,6 +340,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
   __shared__ __align__(8) unsigned long long bars[GEMV_WARPS][MAX_SLOTS];
   __shared__ float scratch[32];
   __shared__ float red[GEMV_WARPS][2];
+  __shared__ float red_all[GEMV_WARPS][MAX_DEFER][2];
   __shared__ volatile int s_abort[GEMV_WARPS];
   constexpr int VN = Vec<T>::N;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -381,7 +391,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
     // and while the upstream kernels finish, the next items stream into L2
     const uint32_t item_bytes = seg_bytes * (uint32_t)Op::RPI;
     int n_pf = c.pf_dist;
-    if (item_bytes && c.prewait_bytes > 0 && (int)(c.prewait_bytes / item_bytes) > n_pf)
+    if (Op::L2_PREWAIT && item_bytes && c.prewait_bytes > 0 && (int)(c.prewait_bytes / item_bytes) > n_pf)
       n_pf = (int)(c.prewait_bytes / item_bytes);
     for (int k = n0; k < min(NS + n_pf, my_items); ++k) prefetch(k);
   }
@@ -416,7 +426,58 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
 
   bool timed_out = false;
   int issued = min(NS, my_items), consumed = 0;
-  for (int k = 0; k < my_items; ++k) {
+  // K split over KS warps with at most MAX_DEFER items per warp: every warp streams its
+  // own segments without waiting for the others, parks its partial sums in shared memory,
+  // and the KS partials of each item are added (in warp order) once, after the loop.
+  const bool deferred = Op::LANE_EPI && KS > 1 && (op.n_items + step - 1) / step <= MAX_DEFER;  // CTA-uniform
+  if (deferred) {
+    for (int k = 0; k < my_items; ++k) {
+      const int slot = k % NS;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * slot, (uint32_t)((k / NS) & 1)))) {
+        timed_out = true;
+        if (lane == 0) s_abort[rg] = 1;
+        break;
+      }
+      consumed = k + 1;
+      const uint4* s0 = reinterpret_cast<const uint4*>(wslots + (size_t)slot * c.slot_bytes);
+      const uint4* s1 = reinterpret_cast<const uint4*>(wslots + (size_t)slot * c.slot_bytes + seg_bytes);
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < MAXV; ++q) {
+        const int v = lane + 32 * q;
+        if (v0 + v < v1) {
+          a0 = dotv(s0[v], xr[q], a0, T());
+          if (Op::RPI == 2) a1 = dotv(s1[v], xr[q], a1, T());
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && k + NS < my_items) {  // slot free: request item k + NS
+        fence_proxy_async();
+        issue(k + NS);
+        ++issued;
+      }
+      a0 = warp_sum(a0);
+      if (Op::RPI == 2) a1 = warp_sum(a1);
+      if (lane == 0) {
+        red_all[warp][k][0] = a0;
+        red_all[warp][k][1] = a1;
+      }
+    }
+    __syncthreads();
+    if (ks == 0 && !s_abort[rg]) {  // lane k finishes item k of this row group
+      for (int k = lane; k < my_items; k += 32) {
+        float a0 = 0.f, a1 = 0.f;
+        for (int j = 0; j < KS; ++j) {
+          a0 += red_all[warp + j][k][0];
+          a1 += red_all[warp + j][k][1];
+        }
+        const int item = first + k * step;
+        const typename Op::Epi epi = k == 0 ? pe[0] : k == 1 ? pe[1] : op.epi_load(item);
+        op.epilogue(item, a0, a1, epi);
+      }
+    }
+  }
+  for (int k = 0; k < my_items && !deferred; ++k) {
     const int slot = k % NS;
     bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * slot, (uint32_t)((k / NS) & 1)));
     if (KS > 1) {  // the KS warps sharing these items give up together
