@@ -105,6 +105,7 @@ struct OpQKV {
   static constexpr bool PAIRED = true, NORM = true;
   static constexpr bool L2_PREWAIT = false;
   static constexpr bool LANE_EPI = true;
+  static constexpr int SLOT_KNOB = 0;
   static constexpr int RPI = 2;
   int K, n_items, hd, nq, nkv, cap;
   const T *wq, *wk, *wv, *bq, *bk, *bv, *gain;
@@ -187,6 +188,7 @@ struct OpGateUp {
   static constexpr bool PAIRED = true, NORM = true;
   static constexpr bool L2_PREWAIT = true;  // resident during attention, when HBM is idle
   static constexpr bool LANE_EPI = true;    // epilogues of different items may run on any lanes
+  static constexpr int SLOT_KNOB = 1;
   static constexpr int RPI = 2;
   int K, n_items;
   const T *wg, *wu, *gain;
@@ -209,6 +211,7 @@ struct OpResid {
   static constexpr bool PAIRED = false, NORM = false;
   static constexpr bool L2_PREWAIT = false;
   static constexpr bool LANE_EPI = true;
+  static constexpr int SLOT_KNOB = 0;
   static constexpr int RPI = RPI_;
   int K, n_items, N;
   const T* W;
@@ -239,6 +242,7 @@ struct OpLMHead {
   static constexpr bool PAIRED = false, NORM = true;
   static constexpr bool L2_PREWAIT = false;
   static constexpr bool LANE_EPI = false;  // the argmax state lives in lane 0
+  static constexpr int SLOT_KNOB = 2;
   static constexpr int RPI = 2;
   int K, n_items, N;
   const T *W, *gain;
@@ -539,16 +543,23 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
 // dynamic shared memory: per-warp slot rings and, unless x is read straight into
 // registers, the input vector (and the gains of a norm prologue)
 static constexpr int X_SMEM_MAX = 16 * 1024;
-// Tuning: bytes of slots per warp (8 warps: 96 KB keeps two kernels' CTAs on one SM), the
+// Tuning: bytes of slots per warp (per kernel kind, below), the
 // in-loop L2 prefetch distance in items, and the bytes per warp prefetched into L2 before
 // the dependency wait; QW_GEMV_SLOT_KB / QW_GEMV_PF / QW_GEMV_PREWAIT_KB override them.
 static int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   return v && *v ? std::atoi(v) : dflt;
 }
-static int warp_budget() {
-  static const int b = env_int("QW_GEMV_SLOT_KB", 12) * 1024;
-  return b;
+// per warp: 0 the default, 1 gate/up, 2 the LM head (the last kernel of a step: no next
+// kernel has to fit beside it)
+static int warp_budget(int knob) {
+  // 8 KB keeps the down projection's CTAs (55 KB) resident beside gate/up's (156 KB), so
+  // its first weights stream while gate/up finishes (measured: 8 -> 839, 12 -> 803,
+  // 16 -> 837, 20 -> 818 tok/s on the 1.5B shape)
+  static const int b0 = env_int("QW_GEMV_SLOT_KB", 8) * 1024;
+  static const int b1 = env_int("QW_GEMV_SLOT_KB_GU", 18) * 1024;  // measured best of 12/18/24
+  static const int b2 = env_int("QW_GEMV_SLOT_KB_LM", 24) * 1024;  // of 12/18/24 (26 fits at most)
+  return knob == 1 ? b1 : knob == 2 ? b2 : b0;
 }
 static int pf_dist() {
   static const int p = env_int("QW_GEMV_PF", 0);
@@ -579,7 +590,7 @@ static bool plan_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, G
   // register tile fits; then split further while too few items exist to fill every warp
   int KS = 1;
   auto slot_of = [&](int ks) { return (size_t)Op::RPI * ((nvec + ks - 1) / ks) * 16; };
-  const int WARP_BUDGET = warp_budget();
+  const int WARP_BUDGET = warp_budget(Op::SLOT_KNOB);
   while (KS < GEMV_WARPS && (maxv_for(nvec, KS) > 8 || 2 * slot_of(KS) > (size_t)WARP_BUDGET)) KS *= 2;
   if (maxv_for(nvec, KS) > 8) return false;
   while (KS < GEMV_WARPS && (long long)op.n_items * KS < (long long)nsm * GEMV_WARPS) KS *= 2;
