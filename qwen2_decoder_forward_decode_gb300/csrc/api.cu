@@ -77,6 +77,7 @@ struct qw_model {
   std::vector<char> active;
   std::vector<cudaGraphExec_t> graphs;
   bool use_graphs = true;
+  bool merge_in_oproj = false;  // decode attention leaves its partials to the o_proj GEMV
   int trace_kind = -1;
   std::vector<cudaEvent_t> trace_begin, trace_end;
   // persistent decode-step kernel (bf16 models)
@@ -161,10 +162,16 @@ struct qw_model {
         return e;
       if ((e = run(1, l, [&](bool p) {
              return launch_attn(d.dtype == QW_BF16 ? 2 : 0, d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min,
-                                attn_smem, q, kc, vc, d.cap, pos + s, 0, attn, attn_ws, tl(), stream, p);
+                                attn_smem, q, kc, vc, d.cap, pos + s, 0, attn, attn_ws, tl(), stream, p,
+                                merge_in_oproj ? 0 : 1);
            })))
         return e;
-      if ((e = run(2, l, [&](bool p) { return launch_resid(d, w.wo, d.H, d.nq * d.hd, attn, xs, err, tl(), stream, p); })))
+      // the o_proj GEMV merges the attention partials into its input vector (up to 2048
+      // attention outputs), else reads the output the attention kernel merged
+      if ((e = run(2, l, [&](bool p) {
+             return merge_in_oproj ? launch_oproj(d, w.wo, (const float*)attn_ws, pos + s, xs, err, tl(), stream, p)
+                                   : launch_resid(d, w.wo, d.H, d.nq * d.hd, attn, xs, err, tl(), stream, p);
+           })))
         return e;
       if ((e = run(3, l, [&](bool p) { return launch_gateup(d, w, xs, act, err, tl(), stream, p); }))) return e;
       if ((e = run(4, l, [&](bool p) { return launch_resid(d, w.w_down, d.H, d.I, act, xs, err, tl(), stream, p); })))
@@ -470,7 +477,11 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
   if ((e = cudaGetDevice(&m->device))) return bail(e, "cudaGetDevice");
   if ((e = cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, m->device)))
     return bail(e, "cudaDeviceGetAttribute");
-  d.attn_chunk_min = ATTN_CHUNK_MIN;
+  {  // shortest context chunk of decode attention (tuning knob QW_ATTN_CHUNK_MIN)
+    const char* cm = std::getenv("QW_ATTN_CHUNK_MIN");
+    const int c = cm ? std::atoi(cm) : 0;
+    d.attn_chunk_min = c >= 8 && c <= 1024 ? c : ATTN_CHUNK_MIN;
+  }
   d.attn_nsplit = attn_nsplit_for(d.cap, d.attn_chunk_min, d.hd, cfg->dtype == QW_BF16 ? 2 : 4);
   m->attn_smem = attn_smem_bytes(d.nq / d.nkv, d.hd, d.cap, d.attn_nsplit, d.attn_chunk_min,
                                  cfg->dtype == QW_BF16 ? 2 : 4);
@@ -670,6 +681,7 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
   m->graphs.assign(S, nullptr);
   const char* ng = std::getenv("QW_NO_GRAPH");
   m->use_graphs = !(ng && ng[0] == '1');
+  m->merge_in_oproj = d.nq * d.hd <= 2048;
   *out = m;
   return QW_OK;
 }

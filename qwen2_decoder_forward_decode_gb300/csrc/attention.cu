@@ -20,7 +20,7 @@ struct AttnArgs {
   const int* d_pos;
   float scale;
   float* out;
-  float* part;            // [nq][nsplit_max][hd + 2]
+  float* part;            // [nq][nsplit_max][attn_part_stride(hd)]: output, max, sum
   unsigned int* counter;  // [nkv]
   unsigned long long* tl;  // timeline slots or null
   // several sequences (grid z): per-sequence strides of q, the KV cache, the output, the
@@ -29,6 +29,7 @@ struct AttnArgs {
   int counter_zs;
   f16* out16;
   const int* active;
+  int merge;  // 0: stop after the partials (the consumer merges them)
 };
 
 // One CTA per (KV head, context chunk). The CTA copies q of its g query heads and the K and
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
       }
     }
   }
-  const int pstride = hd + 2;
+  const int pstride = attn_part_stride(hd);
   if (tid < units) {
     float* dst = a.part + ((size_t)(g * G + th) * a.nsplit_max + split) * pstride + tv * EV;
 #pragma unroll
@@ -250,6 +251,10 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
     float* p = a.part + ((size_t)(g * G + tid) * a.nsplit_max + split) * pstride;
     p[hd] = st[2 * tid];
     p[hd + 1] = st[2 * tid + 1];
+  }
+  if (!a.merge) {
+    tl_stamp(a.tl, 2);
+    return;
   }
   __threadfence();
   __syncthreads();
@@ -331,7 +336,7 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
 // ---- host side ------------------------------------------------------------
 
 size_t attn_workspace_bytes(int nq, int nkv, int hd, int nsplit) {
-  size_t part = (size_t)nq * nsplit * (hd + 2) * sizeof(float);
+  size_t part = (size_t)nq * nsplit * attn_part_stride(hd) * sizeof(float);
   part = (part + 255) & ~(size_t)255;
   return part + (size_t)nkv * sizeof(unsigned int);
 }
@@ -362,20 +367,20 @@ size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min, in
 cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int chunk_min,
                         size_t smem, const float* q, const void* kc, const void* vc,
                         int kv_stride, const int* d_pos, int ctx_host, float* out, void* ws,
-                        unsigned long long* tl, cudaStream_t s, bool pdl) {
+                        unsigned long long* tl, cudaStream_t s, bool pdl, int merge) {  // merge: see AttnArgs
   const int G = nq / nkv;
   if (G > GMAX) return cudaErrorInvalidValue;
-  size_t part_bytes = ((size_t)nq * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
+  size_t part_bytes = ((size_t)nq * nsplit * attn_part_stride(hd) * sizeof(float) + 255) & ~(size_t)255;
   const dim3 grid(nkv, nsplit), block(ATTN_THREADS);
   if (kv_dtype == 2) {
     AttnArgs<f16> a{q, (const f16*)kc, (const f16*)vc, kv_stride, hd, G, nsplit, chunk_min,
                      ctx_host, d_pos, 1.f / sqrtf((float)hd), out, (float*)ws,
-                     (unsigned int*)((char*)ws + part_bytes), tl, 0, 0, 0, 0, 0, nullptr, nullptr};
+                     (unsigned int*)((char*)ws + part_bytes), tl, 0, 0, 0, 0, 0, nullptr, nullptr, merge};
     return launch_k(attn_decode_kernel<f16>, grid, block, smem, s, pdl, a);
   }
   AttnArgs<float> a{q, (const float*)kc, (const float*)vc, kv_stride, hd, G, nsplit, chunk_min,
                     ctx_host, d_pos, 1.f / sqrtf((float)hd), out, (float*)ws,
-                    (unsigned int*)((char*)ws + part_bytes), tl, 0, 0, 0, 0, 0, nullptr, nullptr};
+                    (unsigned int*)((char*)ws + part_bytes), tl, 0, 0, 0, 0, 0, nullptr, nullptr, merge};
   return launch_k(attn_decode_kernel<float>, grid, block, smem, s, pdl, a);
 }
 
@@ -384,7 +389,7 @@ cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int c
 // sequence z - 1; output fp16 [nseq][nq*hd]; workspace: partials [nseq][...] then counters
 // [nseq][nkv] (attn_batched_workspace_bytes).
 size_t attn_batched_workspace_bytes(int nq, int nkv, int hd, int nsplit, int nseq) {
-  const size_t part = ((size_t)nq * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
+  const size_t part = ((size_t)nq * nsplit * attn_part_stride(hd) * sizeof(float) + 255) & ~(size_t)255;
   return part * nseq + (size_t)nkv * nseq * sizeof(unsigned int);
 }
 cudaError_t launch_attn_batched(int nq, int nkv, int hd, int nsplit, int chunk_min, size_t smem,
@@ -393,10 +398,10 @@ cudaError_t launch_attn_batched(int nq, int nkv, int hd, int nsplit, int chunk_m
                                 cudaStream_t s) {
   const int G = nq / nkv;
   if (G > GMAX) return cudaErrorInvalidValue;
-  const size_t part_bytes = ((size_t)nq * nsplit * (hd + 2) * sizeof(float) + 255) & ~(size_t)255;
+  const size_t part_bytes = ((size_t)nq * nsplit * attn_part_stride(hd) * sizeof(float) + 255) & ~(size_t)255;
   AttnArgs<f16> a{q, kc, vc, kv_stride, hd, G, nsplit, chunk_min, 0, d_pos, 1.f / sqrtf((float)hd), nullptr,
                   (float*)ws, (unsigned int*)((char*)ws + part_bytes * nseq), nullptr,
-                  (size_t)nq * hd, kv_zs, (size_t)nq * hd, part_bytes / sizeof(float), nkv, out16, active};
+                  (size_t)nq * hd, kv_zs, (size_t)nq * hd, part_bytes / sizeof(float), nkv, out16, active, 1};
   return launch_k(attn_decode_kernel<f16>, dim3(nkv, nsplit, nseq), dim3(ATTN_THREADS), smem, s, batched_pdl(), a);
 }
 

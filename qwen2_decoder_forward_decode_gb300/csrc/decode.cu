@@ -106,6 +106,9 @@ struct OpQKV {
   static constexpr bool L2_PREWAIT = false;
   static constexpr bool LANE_EPI = true;
   static constexpr int SLOT_KNOB = 0;
+  static constexpr int XS_MULT = 2;         // staged floats per K (input, gains)
+  static constexpr bool DIRECT_OK = false;  // may read its input straight into registers
+  __host__ __device__ int xs_extra() const { return 0; }
   static constexpr int RPI = 2;
   int K, n_items, hd, nq, nkv, cap;
   const T *wq, *wk, *wv, *bq, *bk, *bv, *gain;
@@ -189,6 +192,9 @@ struct OpGateUp {
   static constexpr bool L2_PREWAIT = true;  // resident during attention, when HBM is idle
   static constexpr bool LANE_EPI = true;    // epilogues of different items may run on any lanes
   static constexpr int SLOT_KNOB = 1;
+  static constexpr int XS_MULT = 2;         // staged floats per K (input, gains)
+  static constexpr bool DIRECT_OK = false;  // may read its input straight into registers
+  __host__ __device__ int xs_extra() const { return 0; }
   static constexpr int RPI = 2;
   int K, n_items;
   const T *wg, *wu, *gain;
@@ -212,6 +218,9 @@ struct OpResid {
   static constexpr bool L2_PREWAIT = false;
   static constexpr bool LANE_EPI = true;
   static constexpr int SLOT_KNOB = 0;
+  static constexpr int XS_MULT = 1;         // staged floats per K (input, gains)
+  static constexpr bool DIRECT_OK = true;  // may read its input straight into registers
+  __host__ __device__ int xs_extra() const { return 0; }
   static constexpr int RPI = RPI_;
   int K, n_items, N;
   const T* W;
@@ -236,6 +245,117 @@ struct OpResid {
   __device__ void finish() {}
 };
 
+// x += Wo . o, where o (the attention output of all heads) is merged in the prologue from
+// the attention kernel's per-chunk partials: per head h and chunk s the maximum m_s, the
+// sum of exponentials l_s and the unnormalised output O_s; o_h = sum_s w_s O_s with
+// w_s = exp(m_s - M) / sum_s' l_s' exp(m_s' - M) (exact log-sum-exp combine, chunk order).
+template <typename T>
+struct OpOProj {
+  static constexpr bool PAIRED = false, NORM = false;
+  static constexpr bool L2_PREWAIT = false;
+  static constexpr bool LANE_EPI = true;
+  static constexpr int SLOT_KNOB = 0;
+  static constexpr int XS_MULT = 1;
+  static constexpr bool DIRECT_OK = false;
+  static constexpr int RPI = 2;
+  static constexpr int MB = 8;    // chunks whose partials one batch of loads covers
+  static constexpr int EPT4 = 2;  // 4-element vectors of the input per thread: K <= 8 * 256
+  int K, n_items, N;            // K = nq * hd
+  const T* W;
+  const float* part;            // [nq][nsplit_max][attn_part_stride(hd)]
+  int nq, hd, nsplit_max, chunk_min;
+  const int* d_pos;
+  int ctx;
+  float* y;
+  __host__ __device__ int xs_extra() const { return 2 * nq * nsplit_max; }  // (m, l), then weights
+  // the position is set by the previous step's LM head, finished before this step began
+  __device__ void pre() { ctx = __ldcg(d_pos) + 1; }
+  // One round trip for up to MB chunks: the thread's partial outputs of the first MB
+  // chunks (16-byte vectors, 4 consecutive outputs of one head) are requested together
+  // with the (m, l) pairs, before any of them is used.
+  __device__ void prologue(float* xs, float*, float*) {
+    const int chunk = max(chunk_min, (ctx + nsplit_max - 1) / nsplit_max);
+    const int ns = (ctx + chunk - 1) / chunk;
+    const int ps = attn_part_stride(hd);
+    float* mw = xs + K;  // [nq][nsplit_max] maxima, then weights; [nq][nsplit_max] sums
+    const int nt = blockDim.x;
+    const float* src[EPT4];  // partial row of (head, chunk 0) at this thread's 4 outputs
+    int hw[EPT4];            // offset of the head's weights in mw
+#pragma unroll
+    for (int e = 0; e < EPT4; ++e) {
+      const int idx = 4 * (threadIdx.x + e * nt);
+      const int h = idx / hd;
+      src[e] = idx < K ? part + (size_t)h * nsplit_max * ps + (idx - h * hd) : nullptr;
+      hw[e] = h * nsplit_max;
+    }
+    float4 v[EPT4][MB];
+    auto load = [&](int s0) {
+#pragma unroll
+      for (int e = 0; e < EPT4; ++e)
+#pragma unroll
+        for (int u = 0; u < MB; ++u)
+          v[e][u] = src[e] && s0 + u < ns ? __ldcg(reinterpret_cast<const float4*>(src[e] + (size_t)(s0 + u) * ps))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    load(0);
+    for (int i = threadIdx.x; i < nq * ns; i += nt) {
+      const int h = i / ns, sp = i - h * ns;
+      const float* pp = part + ((size_t)h * nsplit_max + sp) * ps + hd;
+      const float m = __ldcg(pp), l = __ldcg(pp + 1);
+      mw[h * nsplit_max + sp] = m;
+      mw[(nq + h) * nsplit_max + sp] = l;
+    }
+    __syncthreads();
+    for (int h = threadIdx.x; h < nq; h += nt) {
+      float M = -INFINITY;
+      for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, mw[h * nsplit_max + sp]);
+      float L = 0.f;
+      for (int sp = 0; sp < ns; ++sp) {
+        const float w = expf(mw[h * nsplit_max + sp] - M);
+        mw[h * nsplit_max + sp] = w;
+        L = fmaf(mw[(nq + h) * nsplit_max + sp], w, L);
+      }
+      const float inv = 1.f / L;
+      for (int sp = 0; sp < ns; ++sp) mw[h * nsplit_max + sp] *= inv;
+    }
+    __syncthreads();
+    float4 acc[EPT4];
+#pragma unroll
+    for (int e = 0; e < EPT4; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += MB) {
+      if (s0) load(s0);
+#pragma unroll
+      for (int e = 0; e < EPT4; ++e)
+#pragma unroll
+        for (int u = 0; u < MB; ++u) {
+          if (src[e] && s0 + u < ns) {  // threads past the input vector own no head
+            const float w = mw[hw[e] + s0 + u];
+            acc[e].x = fmaf(v[e][u].x, w, acc[e].x);
+            acc[e].y = fmaf(v[e][u].y, w, acc[e].y);
+            acc[e].z = fmaf(v[e][u].z, w, acc[e].z);
+            acc[e].w = fmaf(v[e][u].w, w, acc[e].w);
+          }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EPT4; ++e)
+      if (src[e]) reinterpret_cast<float4*>(xs)[threadIdx.x + e * nt] = acc[e];
+  }
+  __device__ const T* row(int item, int r) const {
+    const int rr = 2 * item + r;
+    return rr < N ? W + (size_t)rr * K : nullptr;
+  }
+  __device__ const float* xin() const { return nullptr; }
+  struct Epi {};
+  __device__ Epi epi_load(int) const { return Epi{}; }
+  __device__ void epilogue(int item, float a, float b, const Epi&) {
+    const int r0 = 2 * item;
+    atomicAdd(y + r0, a);
+    if (r0 + 1 < N) atomicAdd(y + r0 + 1, b);
+  }
+  __device__ void finish() {}
+};
+
 // logits[r] = W[r, :] . norm(x); greedy argmax over all rows
 template <typename T>
 struct OpLMHead {
@@ -243,6 +363,9 @@ struct OpLMHead {
   static constexpr bool L2_PREWAIT = false;
   static constexpr bool LANE_EPI = false;  // the argmax state lives in lane 0
   static constexpr int SLOT_KNOB = 2;
+  static constexpr int XS_MULT = 2;         // staged floats per K (input, gains)
+  static constexpr bool DIRECT_OK = false;  // may read its input straight into registers
+  __host__ __device__ int xs_extra() const { return 0; }
   static constexpr int RPI = 2;
   int K, n_items, N;
   const T *W, *gain;
@@ -584,8 +707,8 @@ struct GemvPlan {
 template <typename T, class Op>
 static bool plan_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, GemvPlan* p) {
   const int nvec = op.K / Vec<T>::N;
-  const int x_direct = (!Op::NORM && (size_t)op.K * 4 > X_SMEM_MAX) ? 1 : 0;
-  const size_t xs = x_direct ? 0 : (size_t)(Op::NORM ? 2 : 1) * op.K * 4;
+  const int x_direct = (Op::DIRECT_OK && (size_t)op.K * 4 > X_SMEM_MAX) ? 1 : 0;
+  const size_t xs = x_direct ? 0 : ((size_t)Op::XS_MULT * op.K + op.xs_extra()) * 4;
   // smallest K split whose slot (RPI row segments) fits the warp budget twice and whose
   // register tile fits; then split further while too few items exist to fill every warp
   int KS = 1;
@@ -685,6 +808,7 @@ static cudaError_t set_attrs_t() {
   if ((e = set_gemv_attrs<T, OpGateUp<T>>())) return e;
   if ((e = set_gemv_attrs<T, OpResid<T, 1>>())) return e;
   if ((e = set_gemv_attrs<T, OpResid<T, 2>>())) return e;
+  if ((e = set_gemv_attrs<T, OpOProj<T>>())) return e;
   return set_gemv_attrs<T, OpLMHead<T>>();
 }
 
@@ -737,6 +861,22 @@ cudaError_t launch_resid(const Dims& d, const void* W, int N, int K, const float
                          int* err, unsigned long long* tl, cudaStream_t s, bool pdl) {
   return d.dtype == 1 ? resid_t<bf16>(d, W, N, K, in, y, err, tl, s, pdl)
                       : resid_t<float>(d, W, N, K, in, y, err, tl, s, pdl);
+}
+
+template <typename T>
+static cudaError_t oproj_t(const Dims& d, const void* W, const float* part, const int* d_pos, float* y, int* err,
+                          unsigned long long* tl, cudaStream_t s, bool pdl) {
+  if (d.nq * d.hd > 4 * OpOProj<T>::EPT4 * GEMV_WARPS * 32 || d.hd % 4) return cudaErrorInvalidValue;
+  OpOProj<T> op{};
+  op.K = d.nq * d.hd; op.N = d.H; op.n_items = (d.H + 1) / 2; op.W = (const T*)W;
+  op.part = part; op.nq = d.nq; op.hd = d.hd; op.nsplit_max = d.attn_nsplit; op.chunk_min = d.attn_chunk_min;
+  op.d_pos = d_pos; op.y = y;
+  return run_gemv<T>(op, d.nsm, err, tl, s, pdl);
+}
+cudaError_t launch_oproj(const Dims& d, const void* W, const float* part, const int* d_pos, float* y, int* err,
+                         unsigned long long* tl, cudaStream_t s, bool pdl) {
+  return d.dtype == 1 ? oproj_t<bf16>(d, W, part, d_pos, y, err, tl, s, pdl)
+                      : oproj_t<float>(d, W, part, d_pos, y, err, tl, s, pdl);
 }
 
 template <typename T>

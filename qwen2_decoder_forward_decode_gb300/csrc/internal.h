@@ -45,6 +45,10 @@ struct Finalize {
 // ---- api.cu ----
 void set_error_message(const char* msg);  // message returned by qw_last_error on this thread
 
+// Floats per (head, chunk) row of the decode-attention partials: hd outputs, the maximum,
+// the sum of exponentials, padding to 16 bytes (rows stay aligned for vector loads).
+__host__ __device__ constexpr int attn_part_stride(int hd) { return hd + 4; }
+
 // ---- decode.cu ----
 size_t attn_workspace_bytes(int nq, int nkv, int hd, int nsplit);
 int attn_nsplit_for(int cap, int chunk_min, int hd, int kv_bytes);
@@ -68,7 +72,10 @@ cudaError_t launch_qkv(const Dims& d, const LayerPtrs& w, const float* x, const 
 cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int chunk_min,
                         size_t smem, const float* q, const void* kc, const void* vc,
                         int kv_stride, const int* d_pos, int ctx_host, float* out, void* ws,
-                        unsigned long long* tl, cudaStream_t s, bool pdl);
+                        unsigned long long* tl, cudaStream_t s, bool pdl, int merge = 1);
+// x += Wo . o with o merged from the attention partials in ws (attention run with merge 0)
+cudaError_t launch_oproj(const Dims& d, const void* W, const float* part, const int* d_pos, float* y, int* err,
+                         unsigned long long* tl, cudaStream_t s, bool pdl);
 // y[r] += W[r,:] . in  (r < N), W [N, K]
 cudaError_t launch_resid(const Dims& d, const void* W, int N, int K, const float* in, float* y,
                          int* err, unsigned long long* tl, cudaStream_t s, bool pdl);
