@@ -470,6 +470,29 @@ def run_batched(args):
     step_bytes = weights + kv + B * s.vocab * 4
     step_s = dec_s / (n_dec * args.steps)
     peak, peak_kind = read_peaks()
+    tl_out = None
+    if args.timeline:  # device timeline of single batched steps
+        kinds = (["embed_norm"] + ["qkv_gemm", "qkv_epi", "attn", "attn_merge", "o_gemm", "o_resid_norm", "gu_gemm",
+                                   "swiglu", "down_gemm", "down_resid_norm"] * s.n_layers + ["lm_gemm", "finalize"])
+        m.set_timeline(True)
+        prefill_all()
+        st = {k: {"gap_us": [], "run_us": []} for k in set(kinds)}
+        tot = []
+        for i in range(8):
+            m.decode_steps(1)
+            tl = m.read_timeline().astype(np.int64)[:len(kinds)]
+            if i < 2:
+                continue
+            tot.append((tl[-1, 2] - tl[0, 0]) / 1000.0)
+            for j, k in enumerate(kinds):
+                prev_end = tl[j - 1, 2] if j else tl[0, 0]
+                st[k]["gap_us"].append((tl[j, 1] - prev_end) / 1000.0)
+                st[k]["run_us"].append((tl[j, 2] - tl[j, 1]) / 1000.0)
+        m.set_timeline(False)
+        tl_out = {"step_us": float(np.mean(tot)), "kernels": {
+            k: {"run_us": round(float(np.mean(v["run_us"])), 3), "gap_us": round(float(np.mean(v["gap_us"])), 3),
+                "per_step_us": round(float(np.sum(v["run_us"]) + np.sum(v["gap_us"])) / len(tot), 1)}
+            for k, v in st.items()}}
     out = {"profile_run": "batched", "metric": "batched decode tok/s (Qwen2.5-1.5B shape, 16 sequences, bf16)",
            "value": tokens / dec_s, "unit": "tok/s", "steps": args.steps, "warmup": args.warmup,
            "layers": s.n_layers, "ms_per_decode_step": 1000.0 * step_s,
@@ -477,6 +500,8 @@ def run_batched(args):
            "bytes_per_step": step_bytes, "achieved_gbs": step_bytes / step_s / 1e9,
            "peak_gbs": peak, "peak_kind": peak_kind, "frac": step_bytes / step_s / 1e9 / peak,
            "prompt_tokens": int(lens.sum()), "clocks": clk.summary()}
+    if tl_out:
+        out["timeline"] = tl_out
     print(json.dumps(out), flush=True)
     m.close()
 

@@ -100,6 +100,8 @@ struct qw_model {
   __half *bX16 = nullptr, *bO16 = nullptr, *bA16 = nullptr;
   __nv_bfloat16* bXb16 = nullptr;
   void* battn_ws = nullptr;
+  int battn_nsplit = 0;            // context chunks of the batched attention
+  size_t battn_smem = 0;
   int* bactive = nullptr;          // device copy of the active flags
   bool bactive_dirty = true;
   cudaGraphExec_t bgraph = nullptr;
@@ -185,6 +187,7 @@ struct qw_model {
   void drop_graphs() {
     for (auto& g : graphs)
       if (g) { cudaGraphExecDestroy(g); g = nullptr; }
+    if (bgraph) { cudaGraphExecDestroy(bgraph); bgraph = nullptr; }
   }
 
   cudaError_t run_step_kernel(int s) {
@@ -295,7 +298,12 @@ struct qw_model {
     c.active = bactive;
     c.keys = keys;
     c.attn_ws = battn_ws;
-    c.attn_smem = attn_smem;
+    c.attn_smem = battn_smem;
+    c.attn_nsplit = battn_nsplit;
+    c.tl = tl_buf;
+    if (tl_buf && (e = cudaMemcpyAsync(tl_buf, tl_init.data(), sizeof(unsigned long long) * 3 * tl_n,
+                                       cudaMemcpyHostToDevice, stream)))
+      return e;
     if (!use_graphs) return batched_step(c, stream);
     if (!bgraph) {
       cudaGraph_t g = nullptr;
@@ -611,7 +619,9 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
   if (m->pf.use_tc && S > 1) {
     // batched decode: every weight matrix read once per step for all active sequences
     const char* bz = std::getenv("QW_BATCHED");
-    if (!(bz && bz[0] == '0') && d.H % 8 == 0 && d.I % 8 == 0 && (d.nq * d.hd) % 8 == 0) {
+    // (the merge kernel holds one head's outputs in one 128-thread CTA, 32 chunks at most)
+    if (!(bz && bz[0] == '0') && d.H % 8 == 0 && d.I % 8 == 0 && (d.nq * d.hd) % 8 == 0 && d.hd <= 128 &&
+        attn_nsplit_for(d.cap, d.attn_chunk_min, d.hd, 2, 32) <= 32) {
       const size_t H = d.H, qd = (size_t)d.nq * d.hd, kvd = (size_t)d.nkv * d.hd, I = d.I;
       auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
       const size_t sz_q = al(16 * qd * 4), sz_x16 = al(16 * H * 2), sz_o16 = al(16 * qd * 2), sz_a16 = al(16 * I * 2),
@@ -665,7 +675,13 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
         ok = ok && skinny_plan(&m->blm, 1, wlm, rlm, Xb, (int)H, true, d.nsm);
       }
       if (ok) {
-        const size_t aws = attn_batched_workspace_bytes(d.nq, d.nkv, d.hd, d.attn_nsplit, S);
+        // up to 32 chunks per sequence and KV head: smaller chunks keep four CTAs per SM
+        // for the nseq x nkv x chunks grid (QW_BATCHED_SPLITS overrides the 32)
+        const char* bs = std::getenv("QW_BATCHED_SPLITS");
+        const int bmax = bs ? std::max(1, std::min(32, std::atoi(bs))) : 32;  // the merge takes <= 32
+        m->battn_nsplit = attn_nsplit_for(d.cap, d.attn_chunk_min, d.hd, 2, bmax);
+        m->battn_smem = attn_smem_bytes(d.nq / d.nkv, d.hd, d.cap, m->battn_nsplit, d.attn_chunk_min, 2);
+        const size_t aws = attn_batched_workspace_bytes(d.nq, d.nkv, d.hd, m->battn_nsplit, S);
         if ((e = cudaMalloc(&m->battn_ws, aws))) return bail(e, "cudaMalloc(batched attention)");
         if ((e = cudaMemset(m->battn_ws, 0, aws))) return bail(e, "cudaMemset(batched attention)");
         if ((e = batched_set_attributes())) return bail(e, "batched attributes");
@@ -673,7 +689,7 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
       }
     }
   }
-  if ((e = attn_set_attributes(m->attn_smem))) return bail(e, "attention attributes");
+  if ((e = attn_set_attributes(std::max(m->attn_smem, m->battn_smem)))) return bail(e, "attention attributes");
   if ((e = prefill_set_attributes(d))) return bail(e, "prefill attributes");
   if ((e = cudaDeviceSynchronize())) return bail(e, "cudaDeviceSynchronize");
   m->h_pos.assign(S, 0);
@@ -874,6 +890,7 @@ qw_status qw_set_timeline(qw_model* m, int32_t enable) {
   }
   if (!enable) return QW_OK;
   m->tl_n = 1 + 5 * m->d.L + 1;
+  if (m->use_batched) m->tl_n = std::max(m->tl_n, 3 + 10 * m->d.L);  // launches of a batched step
   m->tl_init.assign((size_t)3 * m->tl_n, ~0ull);
   for (int i = 0; i < m->tl_n; ++i) m->tl_init[3 * i + 2] = 0ull;
   if (m->use_step) {  // per phase [start, end, producer issued]; ring counters; per phase sub-stamps

@@ -344,13 +344,12 @@ size_t attn_workspace_bytes(int nq, int nkv, int hd, int nsplit) {
 // Chunks of at least chunk_min positions and at most MAX_SPLITS chunks per KV head (short
 // contexts spread over several CTAs, the merge stays short), unless the K and V rows of a
 // chunk would exceed ~160 KB of shared memory; then the chunk count grows instead.
-constexpr int MAX_SPLITS = 16;
-int attn_nsplit_for(int cap, int chunk_min, int hd, int kv_bytes) {
+int attn_nsplit_for(int cap, int chunk_min, int hd, int kv_bytes, int max_splits) {
   int chunk_max = (160 * 1024) / (2 * hd * kv_bytes);
   if (chunk_max > 256) chunk_max = 256;
   if (chunk_max < chunk_min) chunk_max = chunk_min;
   int n = (cap + chunk_min - 1) / chunk_min;
-  if (n > MAX_SPLITS) n = MAX_SPLITS;
+  if (n > max_splits) n = max_splits;
   const int need = (cap + chunk_max - 1) / chunk_max;
   if (n < need) n = need;
   return n < 1 ? 1 : n;
@@ -388,6 +387,9 @@ cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int c
 // q [nseq][nq*hd] fp32; the fp16 caches of sequence z start kv_zs elements after those of
 // sequence z - 1; output fp16 [nseq][nq*hd]; workspace: partials [nseq][...] then counters
 // [nseq][nkv] (attn_batched_workspace_bytes).
+size_t attn_batched_part_floats(int nq, int hd, int nsplit) {
+  return (((size_t)nq * nsplit * attn_part_stride(hd) * sizeof(float) + 255) & ~(size_t)255) / sizeof(float);
+}
 size_t attn_batched_workspace_bytes(int nq, int nkv, int hd, int nsplit, int nseq) {
   const size_t part = ((size_t)nq * nsplit * attn_part_stride(hd) * sizeof(float) + 255) & ~(size_t)255;
   return part * nseq + (size_t)nkv * nseq * sizeof(unsigned int);
@@ -395,13 +397,13 @@ size_t attn_batched_workspace_bytes(int nq, int nkv, int hd, int nsplit, int nse
 cudaError_t launch_attn_batched(int nq, int nkv, int hd, int nsplit, int chunk_min, size_t smem,
                                 const float* q, const f16* kc, const f16* vc, size_t kv_zs, int kv_stride,
                                 const int* d_pos, const int* active, int nseq, f16* out16, void* ws,
-                                cudaStream_t s) {
+                                unsigned long long* tl, cudaStream_t s, int merge) {
   const int G = nq / nkv;
   if (G > GMAX) return cudaErrorInvalidValue;
   const size_t part_bytes = ((size_t)nq * nsplit * attn_part_stride(hd) * sizeof(float) + 255) & ~(size_t)255;
   AttnArgs<f16> a{q, kc, vc, kv_stride, hd, G, nsplit, chunk_min, 0, d_pos, 1.f / sqrtf((float)hd), nullptr,
-                  (float*)ws, (unsigned int*)((char*)ws + part_bytes * nseq), nullptr,
-                  (size_t)nq * hd, kv_zs, (size_t)nq * hd, part_bytes / sizeof(float), nkv, out16, active, 1};
+                  (float*)ws, (unsigned int*)((char*)ws + part_bytes * nseq), tl,
+                  (size_t)nq * hd, kv_zs, (size_t)nq * hd, part_bytes / sizeof(float), nkv, out16, active, merge};
   return launch_k(attn_decode_kernel<f16>, dim3(nkv, nsplit, nseq), dim3(ATTN_THREADS), smem, s, batched_pdl(), a);
 }
 

@@ -53,14 +53,18 @@ template <typename OutT>
 __global__ void __launch_bounds__(RN_THREADS) bresid_norm_kernel(const float* part, int splits, int n_total,
                                                                  const bf16* embed, int V, const int* tok,
                                                                  float* x, const bf16* gain, int H, float eps,
-                                                                 const int* active, int nseq, OutT* out, int* err) {
+                                                                 const int* active, int nseq, OutT* out, int* err,
+                                                                 unsigned long long* tl) {
   __shared__ float scratch[32];
+  tl_stamp(tl, 0);
   pdl_wait();
   pdl_trigger();
+  tl_stamp(tl, 1);
   const int b = blockIdx.x;
   OutT* o = out + (size_t)b * H;
   if (b >= nseq || !active[b]) {
     for (int k = threadIdx.x; k < H; k += RN_THREADS) o[k] = from_f32<OutT>(0.f);
+    tl_stamp(tl, 2);
     return;
   }
   float* xb = x + (size_t)b * H;
@@ -101,6 +105,7 @@ __global__ void __launch_bounds__(RN_THREADS) bresid_norm_kernel(const float* pa
     const int k = threadIdx.x + j * RN_THREADS;
     if (k < H) o[k] = from_f32<OutT>(v[j] * inv * g[j]);
   }
+  tl_stamp(tl, 2);
 }
 
 
@@ -109,9 +114,11 @@ __global__ void __launch_bounds__(RN_THREADS) bresid_norm_kernel(const float* pa
 __global__ void bqkv_epi_kernel(const float* part, int splits, int n_total, int nq, int nkv, int hd,
                                 const bf16* bq, const bf16* bk, const bf16* bv, const float2* rope,
                                 const int* pos, const int* active, float* q_out, f16* kc0, size_t kv_zs,
-                                int cap, int* err) {
+                                int cap, int* err, unsigned long long* tl) {
+  tl_stamp(tl, 0);
   pdl_wait();
   pdl_trigger();
+  tl_stamp(tl, 1);
   const int b = blockIdx.y;
   if (!active[b]) return;
   const int half = hd >> 1;
@@ -149,14 +156,17 @@ __global__ void bqkv_epi_kernel(const float* part, int splits, int n_total, int 
     dst[i] = __float2half_rn(a);
     dst[i + half] = __float2half_rn(c);
   }
+  tl_stamp(tl, 2);
 }
 
 // A[b][i] = silu(gate) * up as fp16 (gate columns [0, I), up columns [I, 2I)); rows of
 // absent or inactive sequences are zero
 __global__ void bswiglu_kernel(const float* part, int splits, int n_total, int I, const int* active, int nseq,
-                               f16* A) {
+                               f16* A, unsigned long long* tl) {
+  tl_stamp(tl, 0);
   pdl_wait();
   pdl_trigger();
+  tl_stamp(tl, 1);
   const int b = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= I) return;
@@ -166,13 +176,62 @@ __global__ void bswiglu_kernel(const float* part, int splits, int n_total, int I
     v = (g / (1.f + expf(-g))) * u;
   }
   A[(size_t)b * I + i] = __float2half_rn(v);
+  tl_stamp(tl, 2);
+}
+
+// Attention output of sequence b, head h from the chunk partials of the attention kernel
+// (per chunk: unnormalised output, maximum m_s, sum of exponentials l_s): o = sum_s w_s O_s
+// with w_s = exp(m_s - M) / sum_s' l_s' exp(m_s' - M) (exact log-sum-exp combine, chunk
+// order), written as the fp16 row of the o_proj GEMM. One CTA per (head, sequence), one
+// thread per output element; every partial it reads is requested before the first use.
+constexpr int BM_SPLITS = 32;  // chunks merged per (sequence, head), at most
+__global__ void __launch_bounds__(128) bmerge_kernel(const float* part, size_t part_zs, int nq, int hd,
+                                                     int nsplit_max, int chunk_min, const int* pos,
+                                                     const int* active, f16* O16, unsigned long long* tl) {
+  __shared__ float w[BM_SPLITS];
+  tl_stamp(tl, 0);
+  pdl_wait();
+  pdl_trigger();
+  tl_stamp(tl, 1);
+  const int h = blockIdx.x, b = blockIdx.y;
+  if (!active[b]) return;
+  const int ctx = __ldcg(pos + b) + 1;
+  const int chunk = max(chunk_min, (ctx + nsplit_max - 1) / nsplit_max);
+  const int ns = min((ctx + chunk - 1) / chunk, BM_SPLITS);
+  const int ps = attn_part_stride(hd);
+  const float* base = part + (size_t)b * part_zs + (size_t)h * nsplit_max * ps;
+  float v[BM_SPLITS];
+#pragma unroll
+  for (int s = 0; s < BM_SPLITS; ++s)
+    v[s] = (int)threadIdx.x < hd && s < ns ? __ldcg(base + (size_t)s * ps + threadIdx.x) : 0.f;
+  if (threadIdx.x < 32) {  // warp 0: the merge weights
+    const int s = threadIdx.x;
+    const float m = s < ns ? __ldcg(base + (size_t)s * ps + hd) : -INFINITY;
+    const float l = s < ns ? __ldcg(base + (size_t)s * ps + hd + 1) : 0.f;
+    const float M = warp_max(m);
+    const float e = s < ns ? expf(m - M) : 0.f;
+    const float L = warp_sum(l * e);
+    w[s] = e / L;
+  }
+  __syncthreads();
+  if ((int)threadIdx.x < hd) {
+    float acc = 0.f;
+#pragma unroll
+    for (int s = 0; s < BM_SPLITS; ++s)
+      if (s < ns) acc = fmaf(v[s], w[s], acc);
+    O16[((size_t)b * nq + h) * hd + threadIdx.x] = __float2half_rn(acc);
+  }
+  tl_stamp(tl, 2);
 }
 
 // per active sequence: token = argmax (lowest index among equal maxima), history, length
 __global__ void bfinalize_kernel(unsigned long long* keys, int* tok, int* pos, int* hist, int* hist_n, int cap,
-                                 const int* active, int nseq) {
+                                 const int* active, int nseq, unsigned long long* tl) {
+  tl_stamp(tl, 0);
   pdl_wait();
   pdl_trigger();
+  tl_stamp(tl, 1);
+  tl_stamp(tl, 2);
   const int b = threadIdx.x;
   if (b >= nseq || !active[b]) return;
   const unsigned long long k = keys[b];
@@ -207,50 +266,57 @@ cudaError_t batched_step(const BatchedCtx& c, cudaStream_t s) {
   const float* no_part = nullptr;
   const bf16* no_embed = nullptr;
   const int* no_tok = nullptr;
+  int li = 0;  // launch index: timeline slots [3 li, 3 li + 3)
+  auto tl = [&]() -> unsigned long long* { return c.tl ? c.tl + 3 * (li++) : nullptr; };
   // layer 0 input: embedding rows, then the first RMSNorm
   if ((e = launch_k(bresid_norm_kernel<f16>, rn_grid, rn_block, 0, s, pdl, no_part, 0, 0, (const bf16*)c.embed,
                     d.V, (const int*)c.tok, c.x, (const bf16*)c.layers[0].in_norm, H, d.eps, c.active, S, c.X16,
-                    c.err)))
+                    c.err, tl())))
     return e;
   for (int l = 0; l < d.L; ++l) {
     const LayerPtrs& w = c.layers[l];
     const BatchedLayerPlans& pl = c.plans[l];
     f16* kc0 = (f16*)c.kv + (size_t)l * 2 * d.nkv * d.cap * d.hd;  // layer l of sequence 0
-    if ((e = skinny_run(pl.qkv, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
+    if ((e = skinny_run(pl.qkv, c.part, nullptr, 0, S, c.active, nullptr, c.err, tl(), s))) return e;
     const int pairs = (d.nq + 2 * d.nkv) * (d.hd / 2);
     if ((e = launch_k(bqkv_epi_kernel, dim3((pairs + BT - 1) / BT, S), dim3(BT), 0, s, pdl, (const float*)c.part,
                       pl.qkv.splits, pl.qkv.n_total, d.nq, d.nkv, d.hd, (const bf16*)w.bq, (const bf16*)w.bk,
                       (const bf16*)w.bv, c.rope, (const int*)c.pos, c.active, c.q, kc0, c.kv_seq_elems, d.cap,
-                      c.err)))
+                      c.err, tl())))
       return e;
-    if ((e = launch_attn_batched(d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min, c.attn_smem, c.q, kc0,
+    // attention leaves its chunk partials; the merge kernel writes the fp16 rows of the o GEMM
+    if ((e = launch_attn_batched(d.nq, d.nkv, d.hd, c.attn_nsplit, d.attn_chunk_min, c.attn_smem, c.q, kc0,
                                  kc0 + (size_t)d.nkv * d.cap * d.hd, c.kv_seq_elems, d.cap, c.pos, c.active, S,
-                                 c.O16, c.attn_ws, s)))
+                                 c.O16, c.attn_ws, tl(), s, /*merge=*/0)))
       return e;
-    if ((e = skinny_run(pl.o, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
+    if ((e = launch_k(bmerge_kernel, dim3(d.nq, S), dim3(128), 0, s, pdl, (const float*)c.attn_ws,
+                      attn_batched_part_floats(d.nq, d.hd, c.attn_nsplit), d.nq, d.hd, c.attn_nsplit,
+                      d.attn_chunk_min, (const int*)c.pos, c.active, c.O16, tl())))
+      return e;
+    if ((e = skinny_run(pl.o, c.part, nullptr, 0, S, c.active, nullptr, c.err, tl(), s))) return e;
     if ((e = launch_k(bresid_norm_kernel<f16>, rn_grid, rn_block, 0, s, pdl, (const float*)c.part, pl.o.splits,
                       pl.o.n_total, no_embed, 0, no_tok, c.x, (const bf16*)w.post_norm, H, d.eps, c.active, S, c.X16,
-                      c.err)))
+                      c.err, tl())))
       return e;
-    if ((e = skinny_run(pl.gu, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
+    if ((e = skinny_run(pl.gu, c.part, nullptr, 0, S, c.active, nullptr, c.err, tl(), s))) return e;
     if ((e = launch_k(bswiglu_kernel, dim3((I + BT - 1) / BT, 16), dim3(BT), 0, s, pdl, (const float*)c.part,
-                      pl.gu.splits, pl.gu.n_total, I, c.active, S, c.A16)))
+                      pl.gu.splits, pl.gu.n_total, I, c.active, S, c.A16, tl())))
       return e;
-    if ((e = skinny_run(pl.down, c.part, nullptr, 0, S, c.active, nullptr, c.err, s))) return e;
+    if ((e = skinny_run(pl.down, c.part, nullptr, 0, S, c.active, nullptr, c.err, tl(), s))) return e;
     // x += down partials, then the next layer's input norm (fp16) or the final norm (bf16)
     if (l + 1 < d.L)
       e = launch_k(bresid_norm_kernel<f16>, rn_grid, rn_block, 0, s, pdl, (const float*)c.part, pl.down.splits,
                    pl.down.n_total, no_embed, 0, no_tok, c.x, (const bf16*)c.layers[l + 1].in_norm, H, d.eps,
-                   c.active, S, c.X16, c.err);
+                   c.active, S, c.X16, c.err, tl());
     else
       e = launch_k(bresid_norm_kernel<bf16>, rn_grid, rn_block, 0, s, pdl, (const float*)c.part, pl.down.splits,
                    pl.down.n_total, no_embed, 0, no_tok, c.x, (const bf16*)c.final_norm, H, d.eps, c.active, S,
-                   c.Xb16, c.err);
+                   c.Xb16, c.err, tl());
     if (e) return e;
   }
-  if ((e = skinny_run(c.lm, nullptr, c.logits, d.V, S, c.active, c.keys, c.err, s))) return e;
+  if ((e = skinny_run(c.lm, nullptr, c.logits, d.V, S, c.active, c.keys, c.err, tl(), s))) return e;
   return launch_k(bfinalize_kernel, dim3(1), dim3(32), 0, s, pdl, c.keys, c.tok, c.pos, c.hist, c.hist_n, d.cap,
-                  c.active, S);
+                  c.active, S, tl());
 }
 
 }  // namespace qw

@@ -349,6 +349,7 @@ struct SkinnyArgs {
   const int* active;
   unsigned long long* keys;  // [nseq]
   int* err;
+  unsigned long long* tl;    // timeline slots or null
 };
 
 template <bool LM>
@@ -372,6 +373,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
   const int kb0 = (int)((long long)blockIdx.y * nk / a.splits);
   const int kb1 = (int)((long long)(blockIdx.y + 1) * nk / a.splits);
   __shared__ int s_abort;
+  tl_stamp(a.tl, 0);
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -400,6 +402,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
     }
     pdl_wait();
     pdl_trigger();
+    tl_stamp(a.tl, 1);
     for (int j = 0; j < pre; ++j)
       tc::tma_load_2d(tc::smem_u32(smem + j * STAGE) + A_BYTES, &xm, full0 + 8 * j, (kb0 + j) * BK, 0);
     int issued = pre;
@@ -485,6 +488,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, 32);
   }
+  tl_stamp(a.tl, 2);
 }
 
 // ---- host side ------------------------------------------------------------------------------
@@ -580,7 +584,7 @@ bool skinny_plan(SkinnyPlan* p, int nz, const void* const* W, const int* rows, c
 }
 
 cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, int nseq, const int* active,
-                       unsigned long long* keys, int* err, cudaStream_t s) {
+                       unsigned long long* keys, int* err, unsigned long long* tl, cudaStream_t s) {
   SkinnyArgs a{};
   a.nz = p.nz;
   for (int i = 0; i < 3; ++i) {
@@ -598,6 +602,7 @@ cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, i
   a.active = active;
   a.keys = keys;
   a.err = err;
+  a.tl = tl;
   const CUtensorMap* wm = reinterpret_cast<const CUtensorMap*>(p.wmap);
   const CUtensorMap* xm = reinterpret_cast<const CUtensorMap*>(p.xmap);
   const dim3 grid(p.tiles, p.splits);

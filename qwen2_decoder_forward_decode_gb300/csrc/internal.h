@@ -51,7 +51,10 @@ __host__ __device__ constexpr int attn_part_stride(int hd) { return hd + 4; }
 
 // ---- decode.cu ----
 size_t attn_workspace_bytes(int nq, int nkv, int hd, int nsplit);
-int attn_nsplit_for(int cap, int chunk_min, int hd, int kv_bytes);
+// Context chunks of decode attention for a cache of cap positions: at least chunk_min
+// positions each, at most max_splits chunks unless a chunk's K and V rows would exceed
+// ~160 KB of shared memory.
+int attn_nsplit_for(int cap, int chunk_min, int hd, int kv_bytes, int max_splits = 16);
 size_t attn_smem_bytes(int group, int hd, int cap, int nsplit, int chunk_min, int kv_bytes);
 cudaError_t decode_set_attributes(const Dims& d);
 cudaError_t attn_set_attributes(size_t smem);  // not during stream capture
@@ -59,7 +62,8 @@ size_t attn_batched_workspace_bytes(int nq, int nkv, int hd, int nsplit, int nse
 cudaError_t launch_attn_batched(int nq, int nkv, int hd, int nsplit, int chunk_min, size_t smem,
                                 const float* q, const __half* kc, const __half* vc, size_t kv_zs, int kv_stride,
                                 const int* d_pos, const int* active, int nseq, __half* out16, void* ws,
-                                cudaStream_t s);
+                                unsigned long long* tl, cudaStream_t s, int merge = 1);
+size_t attn_batched_part_floats(int nq, int hd, int nsplit);  // partial floats per sequence
 
 // tl: three timeline slots (start, past the dependency wait, end) or null
 cudaError_t launch_embed(const Dims& d, const void* E, const int* tok, float* x, int* err,
@@ -140,7 +144,7 @@ cudaError_t skinny_set_attributes();
 bool skinny_plan(SkinnyPlan* p, int nz, const void* const* W, const int* rows, const void* X, int K, bool bf,
                  int nsm);
 cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, int nseq, const int* active,
-                       unsigned long long* keys, int* err, cudaStream_t s);
+                       unsigned long long* keys, int* err, unsigned long long* tl, cudaStream_t s);
 
 // ---- batched.cu ----
 struct BatchedLayerPlans {
@@ -164,6 +168,8 @@ struct BatchedCtx {
   unsigned long long* keys;         // [S]
   void* attn_ws;                    // attn_batched_workspace_bytes(.., S)
   size_t attn_smem;
+  int attn_nsplit;                  // context chunks per sequence and KV head
+  unsigned long long* tl;           // timeline: 3 slots per launch, or null
 };
 cudaError_t batched_set_attributes();
 bool batched_pdl();
