@@ -506,6 +506,71 @@ def run_batched(args):
     m.close()
 
 
+def prefill_flops(s, P):
+    """Algorithmic FLOP of a P-token prefill: the linear layers on every row, causal
+    attention (q.k and p.v over j <= i), and the LM head on the last row."""
+    H, I, V, L = s.hidden, s.intermediate, s.vocab, s.n_layers
+    qd, kvd = s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim
+    linear = 2 * P * L * (H * (qd + 2 * kvd) + qd * H + 3 * H * I)
+    attn = 2 * 2 * s.n_heads * s.head_dim * L * P * (P + 1) / 2
+    return linear + attn + 2 * V * H
+
+
+def run_long(args):
+    """Long-context single sequence (4096-token prompt, 256 tokens, KV cache 8192): TTFT,
+    prefill throughput against the tensor peak, and decode throughput. One JSON line with
+    "profile_run": "long"; not the headline bench line."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from qwen2_decoder_forward_decode_gb300 import DeviceWeights, Model
+
+    torch.cuda.set_device(0)
+    wl = WORKLOADS["1p5b_long"]
+    s = SHAPES[wl.shape]
+    n_dec = wl.new_tokens - 1
+    w = make_weights(s)
+    dw = DeviceWeights(w, 1)
+    prompt = make_prompt(s, wl.prompt_len)
+    stream = torch.cuda.Stream()
+    m = Model(s, dw, wl.kv_capacity, stream=stream.cuda_stream)
+    ids_dev = torch.from_numpy(prompt).cuda()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        m.prefill_device(ids_dev.data_ptr(), len(prompt))
+        m.decode_steps(n_dec)
+    m.sync()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clk:
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            m.prefill_device(ids_dev.data_ptr(), len(prompt))
+            ev[k][1].record(stream)
+            m.decode_steps(n_dec)
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+    m.sync()
+    pre_ms = float(np.mean([ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]))
+    dec_ms = float(np.mean([ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]))
+    fl = prefill_flops(s, wl.prompt_len)
+    ctx_mean = wl.prompt_len + (n_dec - 1) / 2.0 + 1
+    bpt = decode_bytes_per_token(s, ctx_mean)
+    peak, _ = read_peaks()
+    tflops_peak = None
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        with open(pp) as f:
+            tflops_peak = json.load(f).get("bf16_tflops")
+    out = {"profile_run": "long", "prompt_len": wl.prompt_len, "decode_steps": n_dec,
+           "ttft_ms": pre_ms, "prefill_flop": fl, "prefill_tflops": fl / (pre_ms / 1000.0) / 1e12,
+           "bf16_tflops_peak_measured": tflops_peak,
+           "decode_tok_s": n_dec / (dec_ms / 1000.0), "decode_gbs": bpt * n_dec / (dec_ms / 1000.0) / 1e9,
+           "decode_frac_of_hbm": bpt * n_dec / (dec_ms / 1000.0) / 1e9 / peak, "clocks": clk.summary()}
+    print(json.dumps(out), flush=True)
+    m.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -519,8 +584,12 @@ def main():
                     help="profiling only: build the 1.5B shape with this many layers")
     ap.add_argument("--batched", action="store_true",
                     help="measure batched decode of 16 sequences instead (one JSON line, not the bench line)")
+    ap.add_argument("--long", action="store_true",
+                    help="measure the long-context workload instead (one JSON line, not the bench line)")
     args = ap.parse_args()
-    if args.batched:
+    if args.long:
+        run_long(args)
+    elif args.batched:
         run_batched(args)
     elif args.impl == "reference":
         run_reference(args)

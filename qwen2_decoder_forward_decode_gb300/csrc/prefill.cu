@@ -10,6 +10,7 @@
 #include "internal.h"
 
 #include <math.h>
+#include <stdlib.h>
 
 namespace qw {
 
@@ -271,9 +272,12 @@ static cudaError_t set_attr_t() {
   return fa_set_attr<T, 128>();
 }
 
+static cudaError_t pm_set_attributes();
+
 cudaError_t prefill_set_attributes(const Dims& d) {
   cudaError_t e = d.dtype == 1 ? set_attr_t<f16>() : set_attr_t<float>();
   if (e || d.dtype != 1) return e;
+  if ((e = pm_set_attributes())) return e;
   return gemm_tc_available() ? gemm_tc_set_attributes() : cudaSuccess;
 }
 
@@ -306,6 +310,250 @@ static cudaError_t prefill_simt(const Dims& d, const LayerPtrs* layers, const vo
   return cudaGetLastError();
 }
 
+// ---- prefill attention on the tensor cores (bf16 models: fp16 cache) --------------------
+//
+// Causal attention of T query rows over keys 0..pos0+T-1 ("LLM Speedrun: Architecture":
+// Attention, Causal mask, Grouped Query Attention), in the streaming form with a running
+// maximum and sum per row. One CTA per (64 query rows, head), four warps of 16 rows each.
+// S = Q K^T and O += P V run as mma.sync m16n8k16 with fp16 operands and fp32
+// accumulators: q (scaled by 1/sqrt(hd)) and the probabilities are rounded to fp16 like the
+// cache. Q stays in registers as A fragments; key tiles of 64 rows arrive by cp.async
+// (two buffers, rows padded by 16 bytes so every fragment load is bank-conflict free);
+// value tiles are stored transposed so a B fragment is one 32-bit shared load. The output
+// goes straight to the fp16 operand of the o_proj GEMM.
+constexpr int PM_Q = 64, PM_K = 64, PM_WARPS = 4;
+
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void cp_async16_pf(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+template <int HD>
+__global__ void __launch_bounds__(PM_WARPS * 32) attn_prefill_mma_kernel(const float* Q, int T_, int nq, int nkv,
+                                                                        int pos0, const f16* kc, const f16* vc,
+                                                                        int cap, float scale, f16* Oh) {
+  constexpr int KS = HD + 8;      // halves per key row in shared memory
+  constexpr int VS = PM_K + 8;    // halves per transposed value row (one head dimension)
+  constexpr int NKK = HD / 16;    // k-steps of S = Q K^T
+  constexpr int NNT = HD / 8;     // n-tiles of O
+  constexpr int VPT = PM_K * HD / 8 / (PM_WARPS * 32);  // 16-byte value vectors per thread per tile
+  extern __shared__ __align__(16) unsigned char pm_smem[];
+  f16* Ks = reinterpret_cast<f16*>(pm_smem);  // [2][PM_K][KS]
+  f16* Vt = Ks + 2 * PM_K * KS;               // [2][HD][VS]
+  const int qb = gridDim.x - 1 - blockIdx.x;  // the longest (last) query blocks first
+  const int h = blockIdx.y, g = h / (nq / nkv);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+  const int q0 = qb * PM_Q;
+  const int r_lo = q0 + warp * 16 + gid, r_hi = r_lo + 8;  // this thread's two query rows
+  const int last_q = min(T_, q0 + PM_Q) - 1;
+  const int last_key = pos0 + last_q;
+  const int ntiles = last_key / PM_K + 1;
+  const f16* K = kc + (size_t)g * cap * HD;
+  const f16* V = vc + (size_t)g * cap * HD;
+
+  uint32_t qa[NKK][4];  // Q as A fragments, scaled
+#pragma unroll
+  for (int kk = 0; kk < NKK; ++kk) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int row = (r & 1) ? r_hi : r_lo;
+      const int col = 16 * kk + ((r & 2) ? 8 : 0) + 2 * tig;
+      float2 v = make_float2(0.f, 0.f);
+      if (row < T_) v = *reinterpret_cast<const float2*>(Q + (size_t)row * nq * HD + (size_t)h * HD + col);
+      qa[kk][r] = pack_half2(v.x * scale, v.y * scale);
+    }
+  }
+  auto load_k = [&](int t, int buf) {  // cp.async of key rows, zeros past the last key
+    const int k0 = t * PM_K;
+    f16* dst = Ks + (size_t)buf * PM_K * KS;
+    for (int i = tid; i < PM_K * HD / 8; i += PM_WARPS * 32) {
+      const int j = i / (HD / 8), c8 = i - j * (HD / 8);
+      if (k0 + j <= last_key) cp_async16_pf(dst + j * KS + c8 * 8, K + (size_t)(k0 + j) * HD + c8 * 8);
+      else *reinterpret_cast<uint4*>(dst + j * KS + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  uint4 vr[VPT];
+  auto fetch_v = [&](int t) {  // value rows into registers (lane = key within the warp's block)
+    const int k0 = t * PM_K;
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {
+      const int i = tid + u * PM_WARPS * 32;
+      const int j = i % PM_K, db = i / PM_K;
+      vr[u] = k0 + j <= last_key ? __ldg(reinterpret_cast<const uint4*>(V + (size_t)(k0 + j) * HD) + db)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  auto store_vt = [&](int buf) {  // transposed: Vt[d][j]
+    f16* dst = Vt + (size_t)buf * HD * VS;
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {
+      const int i = tid + u * PM_WARPS * 32;
+      const int j = i % PM_K, db = i / PM_K;
+      const f16* e = reinterpret_cast<const f16*>(&vr[u]);
+#pragma unroll
+      for (int x = 0; x < 8; ++x) dst[(size_t)(db * 8 + x) * VS + j] = e[x];
+    }
+  };
+
+  float o[NNT][4];
+#pragma unroll
+  for (int nt = 0; nt < NNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  const int pos_lo = pos0 + r_lo, pos_hi = pos0 + r_hi;
+  const int warp_first = pos0 + q0 + warp * 16;  // smallest position among this warp's rows
+
+  load_k(0, 0);
+  fetch_v(0);
+  store_vt(0);
+  for (int t = 0; t < ntiles; ++t) {
+    const int buf = t & 1, k0 = t * PM_K;
+    if (t + 1 < ntiles) {
+      load_k(t + 1, buf ^ 1);
+      fetch_v(t + 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();  // key tile t and value tile t visible to every warp
+    const f16* kt = Ks + (size_t)buf * PM_K * KS;
+    const f16* vt = Vt + (size_t)buf * HD * VS;
+    if (k0 <= pos0 + min(q0 + warp * 16 + 15, last_q)) {  // some key of the tile is visible to this warp
+      float sc[PM_K / 8][4];
+#pragma unroll
+      for (int nt = 0; nt < PM_K / 8; ++nt) {
+        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        const f16* krow = kt + (size_t)(8 * nt + gid) * KS + 2 * tig;
+#pragma unroll
+        for (int kk = 0; kk < NKK; ++kk) {
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + 16 * kk);
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + 16 * kk + 8);
+          mma16816(sc[nt], qa[kk], b0, b1);
+        }
+      }
+      if (k0 + PM_K - 1 > warp_first) {  // the tile reaches past some row's position: mask
+#pragma unroll
+        for (int nt = 0; nt < PM_K / 8; ++nt) {
+          const int j = k0 + 8 * nt + 2 * tig;
+          if (j > pos_lo) sc[nt][0] = -INFINITY;
+          if (j + 1 > pos_lo) sc[nt][1] = -INFINITY;
+          if (j > pos_hi) sc[nt][2] = -INFINITY;
+          if (j + 1 > pos_hi) sc[nt][3] = -INFINITY;
+        }
+      }
+      float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < PM_K / 8; ++nt) {
+        mx_lo = fmaxf(mx_lo, fmaxf(sc[nt][0], sc[nt][1]));
+        mx_hi = fmaxf(mx_hi, fmaxf(sc[nt][2], sc[nt][3]));
+      }
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      // rows with no visible key yet (only padding rows past T) keep a zero state
+      const float c_lo = m_lo == -INFINITY ? 0.f : expf(m_lo - mn_lo);
+      const float c_hi = m_hi == -INFINITY ? 0.f : expf(m_hi - mn_hi);
+      float s_lo = 0.f, s_hi = 0.f;
+      uint32_t pa[PM_K / 16][4];
+#pragma unroll
+      for (int nt = 0; nt < PM_K / 8; ++nt) {
+        const float p0 = mn_lo == -INFINITY ? 0.f : expf(sc[nt][0] - mn_lo);
+        const float p1 = mn_lo == -INFINITY ? 0.f : expf(sc[nt][1] - mn_lo);
+        const float p2 = mn_hi == -INFINITY ? 0.f : expf(sc[nt][2] - mn_hi);
+        const float p3 = mn_hi == -INFINITY ? 0.f : expf(sc[nt][3] - mn_hi);
+        s_lo += p0 + p1;
+        s_hi += p2 + p3;
+        pa[nt >> 1][(nt & 1) * 2 + 0] = pack_half2(p0, p1);
+        pa[nt >> 1][(nt & 1) * 2 + 1] = pack_half2(p2, p3);
+      }
+      s_lo += __shfl_xor_sync(0xffffffffu, s_lo, 1);
+      s_lo += __shfl_xor_sync(0xffffffffu, s_lo, 2);
+      s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 1);
+      s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 2);
+      l_lo = l_lo * c_lo + s_lo;
+      l_hi = l_hi * c_hi + s_hi;
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+#pragma unroll
+      for (int nt = 0; nt < NNT; ++nt) {
+        o[nt][0] *= c_lo;
+        o[nt][1] *= c_lo;
+        o[nt][2] *= c_hi;
+        o[nt][3] *= c_hi;
+        const f16* vrow = vt + (size_t)(8 * nt + gid) * VS + 2 * tig;
+#pragma unroll
+        for (int kk = 0; kk < PM_K / 16; ++kk) {
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(vrow + 16 * kk);
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(vrow + 16 * kk + 8);
+          mma16816(o[nt], pa[kk], b0, b1);
+        }
+      }
+    }
+    __syncthreads();  // every warp is done with buffer buf
+    if (t + 1 < ntiles) store_vt(buf ^ 1);
+  }
+  const float i_lo = l_lo > 0.f ? 1.f / l_lo : 0.f, i_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
+#pragma unroll
+  for (int nt = 0; nt < NNT; ++nt) {
+    const int col = h * HD + 8 * nt + 2 * tig;
+    if (r_lo < T_)
+      *reinterpret_cast<__half2*>(Oh + (size_t)r_lo * nq * HD + col) = __floats2half2_rn(o[nt][0] * i_lo, o[nt][1] * i_lo);
+    if (r_hi < T_)
+      *reinterpret_cast<__half2*>(Oh + (size_t)r_hi * nq * HD + col) = __floats2half2_rn(o[nt][2] * i_hi, o[nt][3] * i_hi);
+  }
+}
+
+template <int HD>
+static constexpr size_t pm_smem() {
+  return (size_t)(2 * PM_K * (HD + 8) + 2 * HD * (PM_K + 8)) * sizeof(f16);
+}
+
+static cudaError_t pm_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(attn_prefill_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pm_smem<128>());
+  if (e) return e;
+  return cudaFuncSetAttribute(attn_prefill_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)pm_smem<64>());
+}
+
+// tensor-core prefill attention into the fp16 o_proj operand; false if the head size has no
+// instance (the caller then uses the CUDA-core kernel)
+static bool attn_prefill_mma(const Dims& d, const float* Q, int T_, int pos0, const f16* kc, const f16* vc, f16* Oh,
+                             cudaStream_t s, cudaError_t* e) {
+  const dim3 grid((T_ + PM_Q - 1) / PM_Q, d.nq), block(PM_WARPS * 32);
+  const float scale = 1.f / sqrtf((float)d.hd);
+  if (d.hd == 128) {
+    attn_prefill_mma_kernel<128><<<grid, block, pm_smem<128>(), s>>>(Q, T_, d.nq, d.nkv, pos0, kc, vc, d.cap, scale, Oh);
+  } else if (d.hd == 64) {
+    attn_prefill_mma_kernel<64><<<grid, block, pm_smem<64>(), s>>>(Q, T_, d.nq, d.nkv, pos0, kc, vc, d.cap, scale, Oh);
+  } else {
+    return false;
+  }
+  *e = cudaGetLastError();
+  return true;
+}
+
+// QW_PREFILL_ATTN_SIMT=1: the CUDA-core prefill attention on bf16 models too (comparison)
+static bool simt_attention() {
+  static const bool v = [] {
+    const char* e = std::getenv("QW_PREFILL_ATTN_SIMT");
+    return e && e[0] == '1';
+  }();
+  return v;
+}
+
 // bf16 models: every projection on the tensor cores with fp16 operands (fp16 copies of the
 // bf16 weights are exact; fp16 activations round 8x finer than bf16), fp32 accumulation,
 // fp32 residual stream, fp16 KV cache.
@@ -325,9 +573,13 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
     if ((e = gemm_tc(b.Xh, H, (const f16*)w.wk16, H, (const bf16*)w.bk, b.Y + qd, Wd, T_, kvd, H, false, err, s))) return e;
     if ((e = gemm_tc(b.Xh, H, (const f16*)w.wv16, H, (const bf16*)w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, err, s))) return e;
     rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc);
-    if ((e = attn_prefill<f16>(d, b.Q, T_, pos0, kc, vc, b.O, s))) return e;
-    const size_t no = (size_t)T_ * qd;
-    to_half_kernel<<<(unsigned)((no + 255) / 256 < 4096 ? (no + 255) / 256 : 4096), 256, 0, s>>>(b.O, b.Oh, no);
+    const bool mma = !simt_attention() && attn_prefill_mma(d, b.Q, T_, pos0, kc, vc, b.Oh, s, &e);
+    if (mma && e) return e;
+    if (!mma) {
+      if ((e = attn_prefill<f16>(d, b.Q, T_, pos0, kc, vc, b.O, s))) return e;
+      const size_t no = (size_t)T_ * qd;
+      to_half_kernel<<<(unsigned)((no + 255) / 256 < 4096 ? (no + 255) / 256 : 4096), 256, 0, s>>>(b.O, b.Oh, no);
+    }
     if ((e = gemm_tc(b.Oh, qd, (const f16*)w.wo16, qd, nullptr, b.X, H, T_, H, qd, true, err, s))) return e;
     norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.post_norm, H, d.eps, b.Xh);
     if ((e = gemm_tc_swiglu(b.Xh, H, (const f16*)w.wg16, (const f16*)w.wu16, H, b.Ah, d.I, T_, d.I, H, err, s)))
