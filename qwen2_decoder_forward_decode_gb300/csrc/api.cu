@@ -71,6 +71,7 @@ struct qw_model {
   int* pinned = nullptr;  // host staging, max(cap, max_seqs) ints
   PrefillBufs pf{};
   void* pf_block = nullptr;
+  void* pf_ws = nullptr;  // split-K workspace of the prefill GEMMs
   void* w16 = nullptr;  // fp16 copies of the layer matrices (bf16 models)
   // host mirror
   std::vector<int> h_pos;
@@ -340,6 +341,15 @@ struct qw_model {
   cudaError_t ensure_prefill(int T) {
     if (pf.cap_tokens >= T) return cudaSuccess;
     if (pf_block) { cudaFree(pf_block); pf_block = nullptr; }
+    if (pf_ws) { cudaFree(pf_ws); pf_ws = nullptr; }
+    {  // split-K partial tiles: 16 splits of a 512-token output at most (short prompts)
+      const size_t n = std::max(16 * (size_t)std::min(T, 512) * std::max((size_t)d.nq * d.hd, (size_t)d.H),
+                                4 * (size_t)std::min(T, 512) * 2 * d.I);  // gate|up partials
+      cudaError_t e = cudaMalloc(&pf_ws, n * sizeof(float));
+      if (e) { pf_ws = nullptr; pf.cap_tokens = 0; return e; }
+      pf.ws = (float*)pf_ws;
+      pf.ws_floats = n;
+    }
     const size_t H = d.H, qd = (size_t)d.nq * d.hd, W = qd + 2 * (size_t)d.nkv * d.hd, I = d.I;
     const size_t per_tok = H * 2 + W + qd * 2 + I * 2;  // X Xn Y Q O G U (fp32)
     const size_t per_tok_h = H + qd + I;               // Xh Oh Ah (fp16)
@@ -411,7 +421,7 @@ struct qw_model {
     if (bblock) cudaFree(bblock);
     if (battn_ws) cudaFree(battn_ws);
     void* bufs[] = {kv, x, q, attn, act, logits, rope, attn_ws, keys, lm_counter, pos, tok,
-                    hist, hist_n, err, ids, pf_block, w16, tl_buf, step_layers, step_part, step_bar,
+                    hist, hist_n, err, ids, pf_block, pf_ws, w16, tl_buf, step_layers, step_part, step_bar,
                     step_abort};
     for (void* b : bufs)
       if (b) cudaFree(b);

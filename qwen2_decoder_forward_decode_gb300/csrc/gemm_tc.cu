@@ -164,10 +164,14 @@ struct TcEpi {
 // BN columns per tile. For EPI_SWIGLU the B ring holds BN/2 gate rows then BN/2 up rows of
 // the same output columns; the accumulator keeps gate in TMEM columns [0, BN/2) and up in
 // [BN/2, BN).
+// Split-K (grid.z = splits > 1, EPI_STORE / EPI_ADD only): CTA z covers a contiguous range
+// of K blocks and stores its raw fp32 tile to ws[z][M][N]; splitk_reduce_kernel then adds
+// the splits in order and applies the bias or the residual add (deterministic).
 template <int BN, int EPI>
 __global__ void __launch_bounds__(tc::THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmB2, TcEpi ep, int M, int N, int K, int* err) {
+               const __grid_constant__ CUtensorMap tmB2, TcEpi ep, int M, int N, int K, int* err, int splits,
+               float* ws) {
   using namespace tc;
   constexpr int A_BYTES = BM * BK * 2;
   constexpr int B_BYTES = BN * BK * 2;
@@ -180,7 +184,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM;
   const int n0 = blockIdx.x * (EPI == EPI_SWIGLU ? BN / 2 : BN);
-  const int nk = (K + BK - 1) / BK;
+  const int nk_all = (K + BK - 1) / BK;
+  const int kb_lo = (int)((long long)blockIdx.z * nk_all / splits);
+  const int kb_hi = (int)((long long)(blockIdx.z + 1) * nk_all / splits);
+  const int nk = kb_hi - kb_lo;  // K blocks of this CTA
   __shared__ int s_abort;
 
   if (threadIdx.x == 0) {
@@ -210,13 +217,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (s_abort) break;
       const uint32_t a_dst = smem_u32(smem + s * STAGE);
       const uint32_t b_dst = a_dst + A_BYTES;
+      const int kx = (kb_lo + kb) * BK;
       tc::mbar_expect_tx(full0 + 8 * s, STAGE);
-      tc::tma_load_2d(a_dst, &tmA, full0 + 8 * s, kb * BK, m0);
+      tc::tma_load_2d(a_dst, &tmA, full0 + 8 * s, kx, m0);
       if (EPI == EPI_SWIGLU) {
-        tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kb * BK, n0);
-        tc::tma_load_2d(b_dst + B_BYTES / 2, &tmB2, full0 + 8 * s, kb * BK, n0);
+        tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kx, n0);
+        tc::tma_load_2d(b_dst + B_BYTES / 2, &tmB2, full0 + 8 * s, kx, n0);
       } else {
-        tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kb * BK, n0);
+        tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kx, n0);
       }
       ++issued;
     }
@@ -254,7 +262,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (tc::mbar_wait(accum, 0, err)) {
       tc::tc_fence_after();
       const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-      if (EPI == EPI_SWIGLU) {
+      if (EPI == EPI_SWIGLU && splits > 1) {  // raw gate and up partials: ws[z][M][2N]
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tc::tmem_ld32(lane_base + c, v);
+          const int col = n0 + (c < BN / 2 ? c : c - BN / 2);  // column of the gate / up output
+          if (row < M && col < N) {
+            float* out = ws + ((size_t)blockIdx.z * M + row) * 2 * N + (c < BN / 2 ? 0 : N) + col;
+            if (col + 32 <= N && (N & 3) == 0) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(out + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            } else {
+              for (int i = 0; i < 32 && col + i < N; ++i) out[i] = v[i];
+            }
+          }
+        }
+      } else if (EPI == EPI_SWIGLU) {
         for (int c = 0; c < BN / 2; c += 32) {
           float g[32], u[32];
           tc::tmem_ld32(lane_base + c, g);
@@ -271,6 +295,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               } else if (col < N) {
                 out[i] = __float2half_rn(a0);
               }
+            }
+          }
+        }
+      } else if (splits > 1) {  // raw partial tile of this K range
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tc::tmem_ld32(lane_base + c, v);
+          if (row < M) {
+            float* out = ws + ((size_t)blockIdx.z * M + row) * N + n0 + c;
+            if (n0 + c + 32 <= N && (N & 3) == 0) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(out + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            } else {
+              for (int i = 0; i < 32 && n0 + c + i < N; ++i) out[i] = v[i];
             }
           }
         }
@@ -491,6 +530,37 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
   tl_stamp(a.tl, 2);
 }
 
+// Act[m][n] = fp16(silu(g) * u), g and u the split sums (in split order) of ws[s][m][n] and
+// ws[s][m][N + n]
+__global__ void splitk_swiglu_kernel(const float* ws, int splits, int M, int N, f16* Act, int ldc) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)M * N) return;
+  const int m = (int)(i / N), n = (int)(i - (size_t)m * N);
+  float g = 0.f, u = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float* row = ws + ((size_t)s * M + m) * 2 * N;
+    g += __ldcg(row + n);
+    u += __ldcg(row + N + n);
+  }
+  Act[(size_t)m * ldc + n] = __float2half_rn((g / (1.f + expf(-g))) * u);
+}
+
+// C[m][n] = (add ? C[m][n] : 0) + sum over splits of ws[s][m][n] (in split order) + bias[n]
+__global__ void splitk_reduce_kernel(const float* ws, int splits, int M, int N, const bf16* bias, float* C, int ldc,
+                                     int add) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)M * N) return;
+  const int m = (int)(i / N), n = (int)(i - (size_t)m * N);
+  float v[16];
+#pragma unroll
+  for (int s = 0; s < 16; ++s) v[s] = s < splits ? __ldcg(ws + (size_t)s * M * N + i) : 0.f;
+  float acc = add ? C[(size_t)m * ldc + n] : 0.f;
+#pragma unroll
+  for (int s = 0; s < 16; ++s) acc += v[s];
+  if (bias) acc += __bfloat162float(bias[n]);
+  C[(size_t)m * ldc + n] = acc;
+}
+
 // ---- host side ------------------------------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -613,28 +683,65 @@ cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, i
 
 // C[M][N] (fp32, ldc) = / += A[M][K] (fp16, lda) . B[N][K]^T (fp16, ldb) (+ bias[N], bf16)
 cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bias, float* C, int ldc,
-                    int M, int N, int K, bool accumulate, int* err, cudaStream_t s) {
+                    int M, int N, int K, bool accumulate, int* err, cudaStream_t s, float* ws, size_t ws_floats,
+                    int nsm) {
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mb, B, N, K, ldb, TC_BN)) return cudaErrorInvalidValue;
   TcEpi ep{C, bias, nullptr, ldc};
-  const dim3 grid((N + TC_BN - 1) / TC_BN, (M + tc::BM - 1) / tc::BM);
-  if (accumulate)
-    gemm_tc_kernel<TC_BN, EPI_ADD><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err);
+  const int tiles = ((N + TC_BN - 1) / TC_BN) * ((M + tc::BM - 1) / tc::BM);
+  const int nk = (K + tc::BK - 1) / tc::BK;
+  // too few tiles to stream the weights from every SM: split K (up to 16 ways, at least two
+  // K blocks per split, as far as the workspace holds the partial tiles)
+  int splits = 1;
+  if (ws && nsm > 0 && 2 * tiles < nsm) {
+    splits = nsm / tiles;
+    if (splits > 16) splits = 16;
+    if (splits > nk / 2) splits = nk / 2;
+    const size_t per = (size_t)M * N;
+    if ((size_t)splits * per > ws_floats) splits = (int)(ws_floats / per);
+    if (splits < 2) splits = 1;
+  }
+  const dim3 grid((N + TC_BN - 1) / TC_BN, (M + tc::BM - 1) / tc::BM, splits);
+  if (accumulate && splits == 1)
+    gemm_tc_kernel<TC_BN, EPI_ADD><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err, 1, ws);
   else
-    gemm_tc_kernel<TC_BN, EPI_STORE><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err);
+    gemm_tc_kernel<TC_BN, EPI_STORE><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err,
+                                                                                  splits, ws);
+  if (splits > 1) {
+    const size_t n = (size_t)M * N;
+    splitk_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, bias, C, ldc,
+                                                                     accumulate ? 1 : 0);
+  }
   return cudaGetLastError();
 }
 
 // Act[M][N] (fp16, ldc) = silu(A . Wg^T) * (A . Wu^T)
 cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, int ldb, f16* Act,
-                           int ldc, int M, int N, int K, int* err, cudaStream_t s) {
+                           int ldc, int M, int N, int K, int* err, cudaStream_t s, float* ws, size_t ws_floats,
+                           int nsm) {
   CUtensorMap ma, mg, mu;
   if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mg, Wg, N, K, ldb, TC_BN / 2) ||
       !make_map(&mu, Wu, N, K, ldb, TC_BN / 2))
     return cudaErrorInvalidValue;
   TcEpi ep{nullptr, nullptr, Act, ldc};
-  const dim3 grid((N + TC_BN / 2 - 1) / (TC_BN / 2), (M + tc::BM - 1) / tc::BM);
-  gemm_tc_kernel<TC_BN, EPI_SWIGLU><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mg, mu, ep, M, N, K, err);
+  const int tiles = ((N + TC_BN / 2 - 1) / (TC_BN / 2)) * ((M + tc::BM - 1) / tc::BM);
+  const int nk = (K + tc::BK - 1) / tc::BK;
+  int splits = 1;  // as in gemm_tc: split K when the tiles leave SMs idle
+  if (ws && nsm > 0 && 2 * tiles < 2 * nsm && tiles < nsm) {
+    splits = nsm / tiles;
+    if (splits > 16) splits = 16;
+    if (splits > nk / 2) splits = nk / 2;
+    const size_t per = (size_t)M * 2 * N;
+    if ((size_t)splits * per > ws_floats) splits = (int)(ws_floats / per);
+    if (splits < 2) splits = 1;
+  }
+  const dim3 grid((N + TC_BN / 2 - 1) / (TC_BN / 2), (M + tc::BM - 1) / tc::BM, splits);
+  gemm_tc_kernel<TC_BN, EPI_SWIGLU><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mg, mu, ep, M, N, K, err,
+                                                                                 splits, ws);
+  if (splits > 1) {
+    const size_t n = (size_t)M * N;
+    splitk_swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, Act, ldc);
+  }
   return cudaGetLastError();
 }
 

@@ -93,11 +93,14 @@ cudaError_t launch_lmhead(const Dims& d, const void* W, const void* final_norm, 
 bool gemm_tc_available();
 cudaError_t gemm_tc_set_attributes();
 // fp16 operands (A activations, B weights), fp32 accumulate; bias bf16
+// ws (optional): fp32 workspace of ws_floats for split-K partial tiles, used when the
+// output has too few 128x256 tiles for nsm SMs
 cudaError_t gemm_tc(const __half* A, int lda, const __half* B, int ldb, const __nv_bfloat16* bias,
                     float* C, int ldc, int M, int N, int K, bool accumulate, int* err,
-                    cudaStream_t s);
+                    cudaStream_t s, float* ws = nullptr, size_t ws_floats = 0, int nsm = 0);
 cudaError_t gemm_tc_swiglu(const __half* A, int lda, const __half* Wg, const __half* Wu, int ldb,
-                           __half* Act, int ldc, int M, int N, int K, int* err, cudaStream_t s);
+                           __half* Act, int ldc, int M, int N, int K, int* err, cudaStream_t s, float* ws = nullptr,
+                           size_t ws_floats = 0, int nsm = 0);
 
 // ---- step.cu (persistent decode step of one sequence, bf16 models) ----
 struct StepLayer {
@@ -180,6 +183,8 @@ cudaError_t batched_step(const BatchedCtx& c, cudaStream_t s);
 struct PrefillBufs {
   float *X, *Xn, *Y, *Q, *O, *G, *U;  // [T][..] fp32 activations
   __half *Xh, *Oh, *Ah;               // fp16 tensor-core operands [T][H], [T][nq*hd], [T][I]
+  float* ws;                          // split-K partial tiles of the tensor-core GEMMs
+  size_t ws_floats;
   int cap_tokens;
   bool use_tc;
 };

@@ -569,9 +569,9 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
     f16* kc = (f16*)kcache + (size_t)l * 2 * layer_stride;
     f16* vc = kc + layer_stride;
     norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.in_norm, H, d.eps, b.Xh);
-    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wq16, H, (const bf16*)w.bq, b.Y, Wd, T_, qd, H, false, err, s))) return e;
-    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wk16, H, (const bf16*)w.bk, b.Y + qd, Wd, T_, kvd, H, false, err, s))) return e;
-    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wv16, H, (const bf16*)w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, err, s))) return e;
+    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wq16, H, (const bf16*)w.bq, b.Y, Wd, T_, qd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wk16, H, (const bf16*)w.bk, b.Y + qd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wv16, H, (const bf16*)w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
     rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc);
     const bool mma = !simt_attention() && attn_prefill_mma(d, b.Q, T_, pos0, kc, vc, b.Oh, s, &e);
     if (mma && e) return e;
@@ -580,11 +580,12 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
       const size_t no = (size_t)T_ * qd;
       to_half_kernel<<<(unsigned)((no + 255) / 256 < 4096 ? (no + 255) / 256 : 4096), 256, 0, s>>>(b.O, b.Oh, no);
     }
-    if ((e = gemm_tc(b.Oh, qd, (const f16*)w.wo16, qd, nullptr, b.X, H, T_, H, qd, true, err, s))) return e;
+    if ((e = gemm_tc(b.Oh, qd, (const f16*)w.wo16, qd, nullptr, b.X, H, T_, H, qd, true, err, s, b.ws, b.ws_floats, d.nsm))) return e;
     norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.post_norm, H, d.eps, b.Xh);
-    if ((e = gemm_tc_swiglu(b.Xh, H, (const f16*)w.wg16, (const f16*)w.wu16, H, b.Ah, d.I, T_, d.I, H, err, s)))
+    if ((e = gemm_tc_swiglu(b.Xh, H, (const f16*)w.wg16, (const f16*)w.wu16, H, b.Ah, d.I, T_, d.I, H, err, s, b.ws,
+                              b.ws_floats, d.nsm)))
       return e;
-    if ((e = gemm_tc(b.Ah, d.I, (const f16*)w.wd16, d.I, nullptr, b.X, H, T_, H, d.I, true, err, s))) return e;
+    if ((e = gemm_tc(b.Ah, d.I, (const f16*)w.wd16, d.I, nullptr, b.X, H, T_, H, d.I, true, err, s, b.ws, b.ws_floats, d.nsm))) return e;
   }
   return cudaGetLastError();
 }
