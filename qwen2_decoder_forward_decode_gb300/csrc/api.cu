@@ -102,6 +102,7 @@ struct qw_model {
   __nv_bfloat16* bXb16 = nullptr;
   void* battn_ws = nullptr;
   int battn_nsplit = 0;            // context chunks of the batched attention
+  bool battn_mma = false;          // tensor-core batched attention
   size_t battn_smem = 0;
   int* bactive = nullptr;          // device copy of the active flags
   bool bactive_dirty = true;
@@ -301,6 +302,7 @@ struct qw_model {
     c.attn_ws = battn_ws;
     c.attn_smem = battn_smem;
     c.attn_nsplit = battn_nsplit;
+    c.attn_mma = battn_mma;
     c.tl = tl_buf;
     if (tl_buf && (e = cudaMemcpyAsync(tl_buf, tl_init.data(), sizeof(unsigned long long) * 3 * tl_n,
                                        cudaMemcpyHostToDevice, stream)))
@@ -687,14 +689,23 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
       if (ok) {
         // up to 32 chunks per sequence and KV head: smaller chunks keep four CTAs per SM
         // for the nseq x nkv x chunks grid (QW_BATCHED_SPLITS overrides the 32)
+        // The tensor-core kernel streams a chunk of any length in 64-position tiles: a few
+        // long chunks (8) are best; the one-pass CUDA-core kernel wants short ones (32).
+        const char* bm = std::getenv("QW_BATCHED_ATTN_MMA");  // 0: CUDA-core attention
+        m->battn_mma = !(bm && bm[0] == '0') && (d.hd == 64 || d.hd == 128) && d.nq / d.nkv <= 16;
         const char* bs = std::getenv("QW_BATCHED_SPLITS");
-        const int bmax = bs ? std::max(1, std::min(32, std::atoi(bs))) : 32;  // the merge takes <= 32
-        m->battn_nsplit = attn_nsplit_for(d.cap, d.attn_chunk_min, d.hd, 2, bmax);
-        m->battn_smem = attn_smem_bytes(d.nq / d.nkv, d.hd, d.cap, m->battn_nsplit, d.attn_chunk_min, 2);
+        const int bmax = bs ? std::max(1, std::min(32, std::atoi(bs))) : (m->battn_mma ? 8 : 32);  // merge: <= 32
+        if (m->battn_mma)
+          m->battn_nsplit = std::max(1, std::min(bmax, (d.cap + d.attn_chunk_min - 1) / d.attn_chunk_min));
+        else
+          m->battn_nsplit = attn_nsplit_for(d.cap, d.attn_chunk_min, d.hd, 2, bmax);
+        m->battn_smem = m->battn_mma ? 0  // (the tensor-core kernel sizes its own tiles)
+                                     : attn_smem_bytes(d.nq / d.nkv, d.hd, d.cap, m->battn_nsplit, d.attn_chunk_min, 2);
         const size_t aws = attn_batched_workspace_bytes(d.nq, d.nkv, d.hd, m->battn_nsplit, S);
         if ((e = cudaMalloc(&m->battn_ws, aws))) return bail(e, "cudaMalloc(batched attention)");
         if ((e = cudaMemset(m->battn_ws, 0, aws))) return bail(e, "cudaMemset(batched attention)");
         if ((e = batched_set_attributes())) return bail(e, "batched attributes");
+        if (m->battn_mma && (e = attn_decode_mma_set_attributes())) return bail(e, "decode attention attributes");
         m->use_batched = true;
       }
     }

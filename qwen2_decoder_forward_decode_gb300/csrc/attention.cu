@@ -333,6 +333,232 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
   tl_stamp(a.tl, 2);
 }
 
+// ---- decode attention of several sequences on the tensor cores (batched decode) ---------
+//
+// One CTA per (KV head, context chunk, sequence). The g query heads of the KV head are the
+// rows of one m16n8k16 A operand (fp16 q scaled by 1/sqrt(hd), rows >= g zero). Key/value
+// tiles of 64 positions arrive by cp.async into two buffers (rows padded by 16 bytes); each
+// of the four warps takes 16 positions of a tile: S = Q K^T as two n-tiles, a running
+// maximum and sum per row, O += P V with the value B fragments loaded by ldmatrix.trans.
+// The warps' states are combined (log-sum-exp) in shared memory into the chunk's partial
+// (unnormalised output, maximum, sum) for the merge kernel.
+constexpr int DM_K = 64, DM_WARPS = 4;
+
+struct DecMmaArgs {
+  const float* q;    // [nseq][nq * hd]
+  const f16 *k, *v;  // layer caches of sequence 0: [nkv][stride][hd]
+  size_t kv_zs;      // elements from one sequence's caches to the next's
+  int stride, hd, group, nq, nsplit_max, chunk_min;
+  const int* d_pos;  // [nseq]
+  const int* active; // [nseq]
+  float scale;
+  float* part;       // [nseq][part_zs]: [nq][nsplit_max][attn_part_stride(hd)]
+  size_t part_zs;
+  unsigned long long* tl;
+};
+
+template <int HD>
+static constexpr size_t dm_smem() {
+  return (size_t)2 * 2 * DM_K * (HD + 8) * sizeof(f16);  // K and V, two buffers (the combine reuses them)
+}
+
+template <int HD>
+__global__ void __launch_bounds__(DM_WARPS * 32) attn_decode_mma_kernel(const DecMmaArgs a) {
+  constexpr int KS = HD + 8, NKK = HD / 16, NNT = HD / 8;
+  extern __shared__ __align__(16) unsigned char dm_smem_raw[];
+  f16* Ks = reinterpret_cast<f16*>(dm_smem_raw);  // [2][DM_K][KS]
+  f16* Vs = Ks + 2 * DM_K * KS;                    // [2][DM_K][KS]
+  const int g = blockIdx.x, split = blockIdx.y, z = blockIdx.z;
+  if (!a.active[z]) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+  const int G = a.group;
+  tl_stamp(a.tl, 0);
+  const int ctx = __ldcg(a.d_pos + z) + 1;
+  const int chunk = max(a.chunk_min, (ctx + a.nsplit_max - 1) / a.nsplit_max);
+  const int nsplit = (ctx + chunk - 1) / chunk;
+  if (split >= nsplit) return;
+  const int j0 = split * chunk, j1 = min(ctx, j0 + chunk), n = j1 - j0;
+  const int ntiles = (n + DM_K - 1) / DM_K;
+  pdl_wait();  // q and the newest cache row come from the projections just before
+  pdl_trigger();
+  tl_stamp(a.tl, 1);
+  const f16* K = a.k + z * a.kv_zs + ((size_t)g * a.stride + j0) * HD;
+  const f16* V = a.v + z * a.kv_zs + ((size_t)g * a.stride + j0) * HD;
+  uint32_t qa[NKK][4];
+  {
+    const float* qz = a.q + (size_t)z * a.nq * HD + (size_t)g * G * HD;
+#pragma unroll
+    for (int kk = 0; kk < NKK; ++kk)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = (r & 1) ? gid + 8 : gid;
+        const int col = 16 * kk + ((r & 2) ? 8 : 0) + 2 * tig;
+        float2 v = make_float2(0.f, 0.f);
+        if (row < G) v = __ldcg(reinterpret_cast<const float2*>(qz + (size_t)row * HD + col));
+        qa[kk][r] = pack_half2(v.x * a.scale, v.y * a.scale);
+      }
+  }
+  auto load_tile = [&](int t, int buf) {
+    constexpr int NV = DM_K * HD / 8;  // 16-byte vectors of a K (or V) tile
+    for (int i = tid; i < 2 * NV; i += DM_WARPS * 32) {
+      const int which = i >= NV, idx = i - which * NV;
+      const int j = idx / (HD / 8), c8 = idx - j * (HD / 8);
+      f16* dst = (which ? Vs : Ks) + (size_t)buf * DM_K * KS + j * KS + c8 * 8;
+      const int key = t * DM_K + j;
+      if (key < n) cp_async16(dst, (which ? V : K) + (size_t)key * HD + c8 * 8);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  float o[NNT][4];
+#pragma unroll
+  for (int nt = 0; nt < NNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  const int kw = 16 * warp;  // this warp's positions within a tile
+  load_tile(0, 0);
+  for (int t = 0; t < ntiles; ++t) {
+    const int buf = t & 1;
+    if (t + 1 < ntiles) {
+      load_tile(t + 1, buf ^ 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();
+    const f16* kt = Ks + (size_t)buf * DM_K * KS;
+    const f16* vt = Vs + (size_t)buf * DM_K * KS;
+    if (t * DM_K + kw < n) {  // some of this warp's positions exist
+      float sc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        const f16* krow = kt + (size_t)(kw + 8 * nt + gid) * KS + 2 * tig;
+#pragma unroll
+        for (int kk = 0; kk < NKK; ++kk)
+          mma16816(sc[nt], qa[kk], *reinterpret_cast<const uint32_t*>(krow + 16 * kk),
+                   *reinterpret_cast<const uint32_t*>(krow + 16 * kk + 8));
+        const int key = t * DM_K + kw + 8 * nt + 2 * tig;  // positions past the chunk: masked
+        if (key >= n) sc[nt][0] = sc[nt][2] = -INFINITY;
+        if (key + 1 >= n) sc[nt][1] = sc[nt][3] = -INFINITY;
+      }
+      float mx_lo = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      float mx_hi = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      const float c_lo = m_lo == -INFINITY ? 0.f : expf(m_lo - mn_lo);
+      const float c_hi = m_hi == -INFINITY ? 0.f : expf(m_hi - mn_hi);
+      float p[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        p[nt][0] = mn_lo == -INFINITY ? 0.f : expf(sc[nt][0] - mn_lo);
+        p[nt][1] = mn_lo == -INFINITY ? 0.f : expf(sc[nt][1] - mn_lo);
+        p[nt][2] = mn_hi == -INFINITY ? 0.f : expf(sc[nt][2] - mn_hi);
+        p[nt][3] = mn_hi == -INFINITY ? 0.f : expf(sc[nt][3] - mn_hi);
+      }
+      float s_lo = p[0][0] + p[0][1] + p[1][0] + p[1][1], s_hi = p[0][2] + p[0][3] + p[1][2] + p[1][3];
+      s_lo += __shfl_xor_sync(0xffffffffu, s_lo, 1);
+      s_lo += __shfl_xor_sync(0xffffffffu, s_lo, 2);
+      s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 1);
+      s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 2);
+      l_lo = l_lo * c_lo + s_lo;
+      l_hi = l_hi * c_hi + s_hi;
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      const uint32_t pa[4] = {pack_half2(p[0][0], p[0][1]), pack_half2(p[0][2], p[0][3]),
+                              pack_half2(p[1][0], p[1][1]), pack_half2(p[1][2], p[1][3])};
+      // value rows kw + (lane % 8) + 8 ((lane / 8) % 2), columns of n-tile pair nt, nt + 1
+      const f16* vrow = vt + (size_t)(kw + (lane & 7) + ((lane >> 3) & 1) * 8) * KS + (lane >> 4) * 8;
+#pragma unroll
+      for (int nt = 0; nt < NNT; nt += 2) {
+        o[nt][0] *= c_lo;
+        o[nt][1] *= c_lo;
+        o[nt][2] *= c_hi;
+        o[nt][3] *= c_hi;
+        o[nt + 1][0] *= c_lo;
+        o[nt + 1][1] *= c_lo;
+        o[nt + 1][2] *= c_hi;
+        o[nt + 1][3] *= c_hi;
+        uint32_t b[4];
+        ldmatrix_x4_trans(b, vrow + nt * 8);
+        mma16816(o[nt], pa, b[0], b[1]);
+        mma16816(o[nt + 1], pa, b[2], b[3]);
+      }
+    }
+    __syncthreads();  // buffer buf is free again
+  }
+  // combine the four warps (rows < G) in shared memory (the tile buffers are free now)
+  float* cO = reinterpret_cast<float*>(dm_smem_raw);  // [DM_WARPS][16][HD]
+  float* cM = cO + DM_WARPS * 16 * HD;                 // [DM_WARPS][16]
+  float* cL = cM + DM_WARPS * 16;
+#pragma unroll
+  for (int nt = 0; nt < NNT; ++nt) {
+    const int col = 8 * nt + 2 * tig;
+    *reinterpret_cast<float2*>(cO + (size_t)(warp * 16 + gid) * HD + col) = make_float2(o[nt][0], o[nt][1]);
+    *reinterpret_cast<float2*>(cO + (size_t)(warp * 16 + gid + 8) * HD + col) = make_float2(o[nt][2], o[nt][3]);
+  }
+  if (tig == 0) {
+    cM[warp * 16 + gid] = m_lo;
+    cM[warp * 16 + gid + 8] = m_hi;
+    cL[warp * 16 + gid] = l_lo;
+    cL[warp * 16 + gid + 8] = l_hi;
+  }
+  __syncthreads();
+  const int ps = attn_part_stride(HD);
+  float* part = a.part + (size_t)z * a.part_zs;
+  for (int idx = tid; idx < G * HD; idx += DM_WARPS * 32) {
+    const int r = idx / HD, d = idx - r * HD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < DM_WARPS; ++w) M = fmaxf(M, cM[w * 16 + r]);
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < DM_WARPS; ++w) {
+      const float mw = cM[w * 16 + r];
+      if (mw != -INFINITY) acc = fmaf(expf(mw - M), cO[(size_t)(w * 16 + r) * HD + d], acc);
+    }
+    part[((size_t)(g * G + r) * a.nsplit_max + split) * ps + d] = acc;
+  }
+  if (tid < G) {
+    float M = -INFINITY, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < DM_WARPS; ++w) M = fmaxf(M, cM[w * 16 + tid]);
+#pragma unroll
+    for (int w = 0; w < DM_WARPS; ++w) {
+      const float mw = cM[w * 16 + tid];
+      if (mw != -INFINITY) L = fmaf(expf(mw - M), cL[w * 16 + tid], L);
+    }
+    float* pp = part + ((size_t)(g * G + tid) * a.nsplit_max + split) * ps;
+    pp[HD] = M;
+    pp[HD + 1] = L;
+  }
+  tl_stamp(a.tl, 2);
+}
+
+// Tensor-core decode attention of nseq sequences (fp16 caches, head_dim 64 or 128, at most
+// 16 query heads per KV head): chunk partials in ws as for launch_attn_batched (merge 0).
+cudaError_t launch_attn_decode_mma(int nq, int nkv, int hd, int nsplit, int chunk_min, const float* q, const f16* kc,
+                                   const f16* vc, size_t kv_zs, int kv_stride, const int* d_pos, const int* active,
+                                   int nseq, void* ws, unsigned long long* tl, cudaStream_t s, bool pdl) {
+  const int G = nq / nkv;
+  if (G > 16 || (hd != 64 && hd != 128)) return cudaErrorInvalidValue;
+  DecMmaArgs a{q, kc, vc, kv_zs, kv_stride, hd, G, nq, nsplit, chunk_min, d_pos, active, 1.f / sqrtf((float)hd),
+               (float*)ws, attn_batched_part_floats(nq, hd, nsplit), tl};
+  const dim3 grid(nkv, nsplit, nseq), block(DM_WARPS * 32);
+  if (hd == 128) return launch_k(attn_decode_mma_kernel<128>, grid, block, dm_smem<128>(), s, pdl, a);
+  return launch_k(attn_decode_mma_kernel<64>, grid, block, dm_smem<64>(), s, pdl, a);
+}
+
+cudaError_t attn_decode_mma_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)dm_smem<128>());
+  if (e) return e;
+  return cudaFuncSetAttribute(attn_decode_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)dm_smem<64>());
+}
+
 // ---- host side ------------------------------------------------------------
 
 size_t attn_workspace_bytes(int nq, int nkv, int hd, int nsplit) {

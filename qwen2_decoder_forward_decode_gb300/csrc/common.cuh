@@ -167,6 +167,32 @@ __device__ __forceinline__ void tl_stamp(unsigned long long* tl, int which) {
   }
 }
 
+// ---- warp-level tensor-core helpers (mma.sync m16n8k16, fp16 operands, fp32 accumulators) --
+// Fragments follow the PTX ISA layout: with g = lane / 4 and t = lane % 4, A holds rows g and
+// g + 8 at columns 2t, 2t + 1 (and + 8); B holds rows (k) 2t, 2t + 1 (and + 8) at column g;
+// C holds rows g and g + 8 at columns 2t, 2t + 1.
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// four 8x8 b16 matrices, transposed: thread i gives the row address of row i % 8 of matrix
+// i / 8; register j receives matrix j's elements (2t, g) and (2t + 1, g)
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, const void* row_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(row_addr)));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
 // Ask L2 to fetch bytes (multiple of 16) at src (16-byte aligned); no completion tracking.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

@@ -64,6 +64,11 @@ cudaError_t launch_attn_batched(int nq, int nkv, int hd, int nsplit, int chunk_m
                                 const int* d_pos, const int* active, int nseq, __half* out16, void* ws,
                                 unsigned long long* tl, cudaStream_t s, int merge = 1);
 size_t attn_batched_part_floats(int nq, int hd, int nsplit);  // partial floats per sequence
+cudaError_t launch_attn_decode_mma(int nq, int nkv, int hd, int nsplit, int chunk_min, const float* q,
+                                   const __half* kc, const __half* vc, size_t kv_zs, int kv_stride, const int* d_pos,
+                                   const int* active, int nseq, void* ws, unsigned long long* tl, cudaStream_t s,
+                                   bool pdl);
+cudaError_t attn_decode_mma_set_attributes();
 
 // tl: three timeline slots (start, past the dependency wait, end) or null
 cudaError_t launch_embed(const Dims& d, const void* E, const int* tok, float* x, int* err,
@@ -172,6 +177,7 @@ struct BatchedCtx {
   void* attn_ws;                    // attn_batched_workspace_bytes(.., S)
   size_t attn_smem;
   int attn_nsplit;                  // context chunks per sequence and KV head
+  bool attn_mma;                    // tensor-core attention (else CUDA cores)
   unsigned long long* tl;           // timeline: 3 slots per launch, or null
 };
 cudaError_t batched_set_attributes();

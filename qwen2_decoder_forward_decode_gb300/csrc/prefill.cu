@@ -323,21 +323,6 @@ static cudaError_t prefill_simt(const Dims& d, const LayerPtrs* layers, const vo
 // goes straight to the fp16 operand of the o_proj GEMM.
 constexpr int PM_Q = 64, PM_K = 64, PM_WARPS = 4;
 
-__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-__device__ __forceinline__ void cp_async16_pf(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-
 template <int HD>
 __global__ void __launch_bounds__(PM_WARPS * 32) attn_prefill_mma_kernel(const float* Q, int T_, int nq, int nkv,
                                                                         int pos0, const f16* kc, const f16* vc,
@@ -378,7 +363,7 @@ __global__ void __launch_bounds__(PM_WARPS * 32) attn_prefill_mma_kernel(const f
     f16* dst = Ks + (size_t)buf * PM_K * KS;
     for (int i = tid; i < PM_K * HD / 8; i += PM_WARPS * 32) {
       const int j = i / (HD / 8), c8 = i - j * (HD / 8);
-      if (k0 + j <= last_key) cp_async16_pf(dst + j * KS + c8 * 8, K + (size_t)(k0 + j) * HD + c8 * 8);
+      if (k0 + j <= last_key) cp_async16(dst + j * KS + c8 * 8, K + (size_t)(k0 + j) * HD + c8 * 8);
       else *reinterpret_cast<uint4*>(dst + j * KS + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
