@@ -79,6 +79,7 @@ struct qw_model {
   std::vector<cudaGraphExec_t> graphs;
   bool use_graphs = true;
   bool merge_in_oproj = false;  // decode attention leaves its partials to the o_proj GEMV
+  bool attn_mma = false;        // decode attention on the tensor cores (fp16 cache)
   int trace_kind = -1;
   std::vector<cudaEvent_t> trace_begin, trace_end;
   // persistent decode-step kernel (bf16 models)
@@ -165,6 +166,10 @@ struct qw_model {
       if ((e = run(0, l, [&](bool p) { return launch_qkv(d, w, xs, pos + s, rope, q, kc, vc, err, tl(), stream, p); })))
         return e;
       if ((e = run(1, l, [&](bool p) {
+             if (attn_mma)  // tensor cores; the o_proj GEMV merges the chunks
+               return launch_attn_decode_mma(d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min, q,
+                                             (const __half*)kc, (const __half*)vc, 0, d.cap, pos + s, nullptr, 1,
+                                             attn_ws, tl(), stream, p);
              return launch_attn(d.dtype == QW_BF16 ? 2 : 0, d.nq, d.nkv, d.hd, d.attn_nsplit, d.attn_chunk_min,
                                 attn_smem, q, kc, vc, d.cap, pos + s, 0, attn, attn_ws, tl(), stream, p,
                                 merge_in_oproj ? 0 : 1);
@@ -719,6 +724,14 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
   const char* ng = std::getenv("QW_NO_GRAPH");
   m->use_graphs = !(ng && ng[0] == '1');
   m->merge_in_oproj = d.nq * d.hd <= 2048;
+  {
+    // tensor-core decode attention (QW_ATTN_MMA=0: CUDA cores); measured on the 1.5B shape:
+    // equal at a 128-token context, 662 -> 688 tok/s at 4096-4351 positions
+    const char* am = std::getenv("QW_ATTN_MMA");
+    m->attn_mma = !(am && am[0] == '0') && m->merge_in_oproj && cfg->dtype == QW_BF16 && (d.hd == 64 || d.hd == 128) &&
+                  d.nq / d.nkv <= 16;
+    if (m->attn_mma) QW_CUDA(attn_decode_mma_set_attributes());
+  }
   *out = m;
   return QW_OK;
 }

@@ -350,7 +350,7 @@ struct DecMmaArgs {
   size_t kv_zs;      // elements from one sequence's caches to the next's
   int stride, hd, group, nq, nsplit_max, chunk_min;
   const int* d_pos;  // [nseq]
-  const int* active; // [nseq]
+  const int* active; // [nseq], or null: all
   float scale;
   float* part;       // [nseq][part_zs]: [nq][nsplit_max][attn_part_stride(hd)]
   size_t part_zs;
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(DM_WARPS * 32) attn_decode_mma_kernel(const De
   f16* Ks = reinterpret_cast<f16*>(dm_smem_raw);  // [2][DM_K][KS]
   f16* Vs = Ks + 2 * DM_K * KS;                    // [2][DM_K][KS]
   const int g = blockIdx.x, split = blockIdx.y, z = blockIdx.z;
-  if (!a.active[z]) return;
+  if (a.active && !a.active[z]) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   const int G = a.group;
   tl_stamp(a.tl, 0);
