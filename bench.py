@@ -472,8 +472,12 @@ def run_batched(args):
     peak, peak_kind = read_peaks()
     tl_out = None
     if args.timeline:  # device timeline of single batched steps
-        kinds = (["embed_norm"] + ["qkv_gemm", "qkv_epi", "attn", "attn_merge", "o_gemm", "o_resid_norm", "gu_gemm",
-                                   "swiglu", "down_gemm", "down_resid_norm"] * s.n_layers + ["lm_gemm", "finalize"])
+        # SwiGLU runs in the gate/up GEMM's epilogue when its 64-row tiles cover half the SMs
+        nsm = torch.cuda.get_device_properties(0).multi_processor_count
+        glu = os.environ.get("QW_BATCHED_GLU") != "0" and 2 * ((s.intermediate + 63) // 64) >= nsm
+        layer = ["qkv_gemm", "qkv_epi", "attn", "attn_merge", "o_gemm", "o_resid_norm", "gu_gemm"]
+        layer += ([] if glu else ["swiglu"]) + ["down_gemm", "down_resid_norm"]
+        kinds = ["embed_norm"] + layer * s.n_layers + ["lm_gemm", "finalize"]
         m.set_timeline(True)
         prefill_all()
         st = {k: {"gap_us": [], "run_us": []} for k in set(kinds)}

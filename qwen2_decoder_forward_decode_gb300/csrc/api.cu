@@ -679,9 +679,11 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
           const void* wgu[2] = {L.wg16, L.wu16};
           const int rgu[2] = {(int)I, (int)I};
           const void* wd[1] = {L.wd16};
+          const char* fg = std::getenv("QW_BATCHED_GLU");  // 0: SwiGLU as its own kernel
+          const bool glu = !(fg && fg[0] == '0') && skinny_plan_glu(&P.gu, L.wg16, L.wu16, (int)I, X16, (int)H, d.nsm);
           ok = skinny_plan(&P.qkv, 3, wqkv, rqkv, X16, (int)H, false, d.nsm) &&
                skinny_plan(&P.o, 1, wo, ro, O16, (int)qd, false, d.nsm) &&
-               skinny_plan(&P.gu, 2, wgu, rgu, X16, (int)H, false, d.nsm) &&
+               (glu || skinny_plan(&P.gu, 2, wgu, rgu, X16, (int)H, false, d.nsm)) &&
                skinny_plan(&P.down, 1, wd, ro, A16, (int)I, false, d.nsm);
           if (ok && pass == 0)
             for (const SkinnyPlan* sp : {&P.qkv, &P.o, &P.gu, &P.down})

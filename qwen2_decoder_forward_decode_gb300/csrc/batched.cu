@@ -303,10 +303,14 @@ cudaError_t batched_step(const BatchedCtx& c, cudaStream_t s) {
                       pl.o.n_total, no_embed, 0, no_tok, c.x, (const bf16*)w.post_norm, H, d.eps, c.active, S, c.X16,
                       c.err, tl())))
       return e;
-    if ((e = skinny_run(pl.gu, c.part, nullptr, 0, S, c.active, nullptr, c.err, tl(), s))) return e;
-    if ((e = launch_k(bswiglu_kernel, dim3((I + BT - 1) / BT, 16), dim3(BT), 0, s, pdl, (const float*)c.part,
-                      pl.gu.splits, pl.gu.n_total, I, c.active, S, c.A16, tl())))
-      return e;
+    if (pl.gu.glu) {  // SwiGLU in the GEMM's epilogue
+      if ((e = skinny_run(pl.gu, nullptr, nullptr, 0, S, c.active, nullptr, c.err, tl(), s, c.A16))) return e;
+    } else {
+      if ((e = skinny_run(pl.gu, c.part, nullptr, 0, S, c.active, nullptr, c.err, tl(), s))) return e;
+      if ((e = launch_k(bswiglu_kernel, dim3((I + BT - 1) / BT, 16), dim3(BT), 0, s, pdl, (const float*)c.part,
+                        pl.gu.splits, pl.gu.n_total, I, c.active, S, c.A16, tl())))
+        return e;
+    }
     if ((e = skinny_run(pl.down, c.part, nullptr, 0, S, c.active, nullptr, c.err, tl(), s))) return e;
     // x += down partials, then the next layer's input norm (fp16) or the final norm (bf16)
     if (l + 1 < d.L)

@@ -389,9 +389,14 @@ struct SkinnyArgs {
   unsigned long long* keys;  // [nseq]
   int* err;
   unsigned long long* tl;    // timeline slots or null
+  // fused SwiGLU (MODE 2): w0 / w1 = gate / up maps of 64-row boxes; act[b][i] fp16
+  f16* act;
+  int n_act;
 };
 
-template <bool LM>
+// MODE 0: split-K partials; 1: LM head (logits and argmax keys); 2: gate/up with SwiGLU
+// (a tile holds 64 gate rows then the 64 up rows of the same outputs; one split)
+template <int MODE>
 __global__ void __launch_bounds__(sk::THREADS, 1)
 skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUtensorMap w1,
                  const __grid_constant__ CUtensorMap w2, const __grid_constant__ CUtensorMap xm,
@@ -405,9 +410,10 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
                  accum = tc::smem_u32(bars + 2 * STAGES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x;
-  const int z = (a.nz > 1 && tile >= a.tile_start[1]) + (a.nz > 2 && tile >= a.tile_start[2]);
+  constexpr bool LM = MODE == 1, GLU = MODE == 2;
+  const int z = GLU ? 0 : (a.nz > 1 && tile >= a.tile_start[1]) + (a.nz > 2 && tile >= a.tile_start[2]);
   const CUtensorMap* wm = z == 0 ? &w0 : z == 1 ? &w1 : &w2;
-  const int m0 = (tile - a.tile_start[z]) * BM;
+  const int m0 = GLU ? tile * (BM / 2) : (tile - a.tile_start[z]) * BM;
   const int nk = (a.K + BK - 1) / BK;
   const int kb0 = (int)((long long)blockIdx.y * nk / a.splits);
   const int kb1 = (int)((long long)(blockIdx.y + 1) * nk / a.splits);
@@ -437,7 +443,12 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
     for (int j = 0; j < pre; ++j) {
       const uint32_t a_dst = tc::smem_u32(smem + j * STAGE);
       tc::mbar_expect_tx(full0 + 8 * j, STAGE);
-      tc::tma_load_2d(a_dst, wm, full0 + 8 * j, (kb0 + j) * BK, m0);
+      if (GLU) {
+        tc::tma_load_2d(a_dst, &w0, full0 + 8 * j, (kb0 + j) * BK, m0);
+        tc::tma_load_2d(a_dst + A_BYTES / 2, &w1, full0 + 8 * j, (kb0 + j) * BK, m0);
+      } else {
+        tc::tma_load_2d(a_dst, wm, full0 + 8 * j, (kb0 + j) * BK, m0);
+      }
     }
     pdl_wait();
     pdl_trigger();
@@ -451,7 +462,12 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
       if (s_abort) break;
       const uint32_t a_dst = tc::smem_u32(smem + s * STAGE);
       tc::mbar_expect_tx(full0 + 8 * s, STAGE);
-      tc::tma_load_2d(a_dst, wm, full0 + 8 * s, kb * BK, m0);
+      if (GLU) {
+        tc::tma_load_2d(a_dst, &w0, full0 + 8 * s, kb * BK, m0);
+        tc::tma_load_2d(a_dst + A_BYTES / 2, &w1, full0 + 8 * s, kb * BK, m0);
+      } else {
+        tc::tma_load_2d(a_dst, wm, full0 + 8 * s, kb * BK, m0);
+      }
       tc::tma_load_2d(a_dst + A_BYTES, &xm, full0 + 8 * s, kb * BK, 0);
       ++issued;
     }
@@ -490,7 +506,27 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
       for (int b = 0; b < 16; ++b) v[b] = 0.f;
       have = true;
     }
-    if (have) {
+    if (GLU) {
+      // TMEM lanes 0-63: gate rows m0.., lanes 64-127: the up rows of the same outputs. The
+      // gate warps park their values in shared memory (the drained stage buffers), the up
+      // warps form silu(gate) * up for the 16 activation rows.
+      float* gbuf = reinterpret_cast<float*>(smem);  // [64][17]
+      if (q < 2 && have) {
+#pragma unroll
+        for (int b = 0; b < 16; ++b) gbuf[(q * 32 + lane) * 17 + b] = v[b];
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+      if (q >= 2 && have) {
+        const int i = m0 + (q - 2) * 32 + lane;
+        if (i < a.n_act) {
+#pragma unroll
+          for (int b = 0; b < 16; ++b) {
+            const float g = gbuf[((q - 2) * 32 + lane) * 17 + b];
+            a.act[(size_t)b * a.n_act + i] = __float2half_rn((g / (1.f + expf(-g))) * v[b]);
+          }
+        }
+      }
+    } else if (have) {
       const bool in = r < a.rows[z];
       if (!LM) {
         if (in) {
@@ -614,10 +650,32 @@ cudaError_t gemm_tc_set_attributes() {
 bool gemm_tc_available() { return encode_fn() != nullptr; }
 
 cudaError_t skinny_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(skinny_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(skinny_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)sk::SMEM);
   if (e) return e;
-  return cudaFuncSetAttribute(skinny_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk::SMEM);
+  if ((e = cudaFuncSetAttribute(skinny_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk::SMEM)))
+    return e;
+  return cudaFuncSetAttribute(skinny_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sk::SMEM);
+}
+
+// Fused gate/up + SwiGLU: tiles of 64 gate rows and the 64 up rows of the same outputs
+// (64-row boxes), one split; false unless that keeps at least half the SMs busy.
+bool skinny_plan_glu(SkinnyPlan* p, const void* Wg, const void* Wu, int I, const void* X, int K, int nsm) {
+  std::memset(p, 0, sizeof(*p));
+  const int tiles = (I + sk::BM / 2 - 1) / (sk::BM / 2);
+  if (2 * tiles < nsm) return false;
+  if (!make_map(reinterpret_cast<CUtensorMap*>(p->wmap[0]), Wg, I, K, K, sk::BM / 2) ||
+      !make_map(reinterpret_cast<CUtensorMap*>(p->wmap[1]), Wu, I, K, K, sk::BM / 2) ||
+      !make_map(reinterpret_cast<CUtensorMap*>(p->wmap[2]), Wu, I, K, K, sk::BM / 2) ||
+      !make_map(reinterpret_cast<CUtensorMap*>(p->xmap), X, 16, K, K, sk::BN))
+    return false;
+  p->nz = 2;
+  p->K = K;
+  p->tiles = tiles;
+  p->splits = 1;
+  p->n_total = I;
+  p->glu = true;
+  return true;
 }
 
 // Tensor maps of one skinny GEMM: nz weight matrices [rows_z][K] (fp16, or bf16 for the LM
@@ -654,7 +712,7 @@ bool skinny_plan(SkinnyPlan* p, int nz, const void* const* W, const int* rows, c
 }
 
 cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, int nseq, const int* active,
-                       unsigned long long* keys, int* err, unsigned long long* tl, cudaStream_t s) {
+                       unsigned long long* keys, int* err, unsigned long long* tl, cudaStream_t s, __half* act) {
   SkinnyArgs a{};
   a.nz = p.nz;
   for (int i = 0; i < 3; ++i) {
@@ -676,9 +734,12 @@ cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, i
   const CUtensorMap* wm = reinterpret_cast<const CUtensorMap*>(p.wmap);
   const CUtensorMap* xm = reinterpret_cast<const CUtensorMap*>(p.xmap);
   const dim3 grid(p.tiles, p.splits);
+  a.act = act;
+  a.n_act = p.n_total;
   const bool pdl = batched_pdl();
-  if (p.lm) return launch_k(skinny_tc_kernel<true>, grid, dim3(sk::THREADS), sk::SMEM, s, pdl, wm[0], wm[1], wm[2], *xm, a);
-  return launch_k(skinny_tc_kernel<false>, grid, dim3(sk::THREADS), sk::SMEM, s, pdl, wm[0], wm[1], wm[2], *xm, a);
+  if (p.lm) return launch_k(skinny_tc_kernel<1>, grid, dim3(sk::THREADS), sk::SMEM, s, pdl, wm[0], wm[1], wm[2], *xm, a);
+  if (p.glu) return launch_k(skinny_tc_kernel<2>, grid, dim3(sk::THREADS), sk::SMEM, s, pdl, wm[0], wm[1], wm[2], *xm, a);
+  return launch_k(skinny_tc_kernel<0>, grid, dim3(sk::THREADS), sk::SMEM, s, pdl, wm[0], wm[1], wm[2], *xm, a);
 }
 
 // C[M][N] (fp32, ldc) = / += A[M][K] (fp16, lda) . B[N][K]^T (fp16, ldb) (+ bias[N], bf16)

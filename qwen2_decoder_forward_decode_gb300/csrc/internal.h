@@ -146,13 +146,16 @@ struct SkinnyPlan {
   alignas(64) unsigned char xmap[128];
   int nz, K, tiles, splits, n_total;
   int tile_start[3], rows[3], col_off[3];
-  bool lm;  // bf16 operands, one split, logits + argmax epilogue
+  bool lm;   // bf16 operands, one split, logits + argmax epilogue
+  bool glu;  // gate/up with SwiGLU into fp16 activation rows (one split)
 };
 cudaError_t skinny_set_attributes();
 bool skinny_plan(SkinnyPlan* p, int nz, const void* const* W, const int* rows, const void* X, int K, bool bf,
                  int nsm);
 cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, int nseq, const int* active,
-                       unsigned long long* keys, int* err, unsigned long long* tl, cudaStream_t s);
+                       unsigned long long* keys, int* err, unsigned long long* tl, cudaStream_t s,
+                       __half* act = nullptr);
+bool skinny_plan_glu(SkinnyPlan* p, const void* Wg, const void* Wu, int I, const void* X, int K, int nsm);
 
 // ---- batched.cu ----
 struct BatchedLayerPlans {
