@@ -179,6 +179,22 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def prefill_launches(s, T, nsm=152):
+    """Kernels one prefill of T tokens launches on a bf16 model: embedding, per layer two
+    norms, RoPE/KV append, attention and the tensor-core GEMMs (q, k, v, o, gate/up, down),
+    each followed by a split-K reduce when its 128x256 tile grid leaves more than half the
+    SMs idle, then the LM head."""
+    qd, kvd, H, I = s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim, s.hidden, s.intermediate
+    mt = (T + 127) // 128
+    def gemm(n_out, wide=256):
+        return 1 + (1 if 2 * ((n_out + wide - 1) // wide) * mt < nsm else 0)
+    per_layer = 4 + gemm(qd) + 2 * gemm(kvd) + gemm(H)  # norms, rope, attention; q, k, v, o
+    gu_tiles = ((I + 127) // 128) * mt
+    per_layer += 1 + (1 if gu_tiles < nsm else 0)  # gate/up (SwiGLU epilogue or split reduce)
+    per_layer += gemm(H)  # down
+    return 1 + s.n_layers * per_layer + 1
+
+
 def decode_launches_per_token(s):
     """Kernels one decode step launches: the persistent step kernel (QW_STEP_KERNEL=1), or
     embedding, 5 per layer and the LM head."""
@@ -401,7 +417,7 @@ def run_native(args):
                     "d2h_bytes_per_step": 4 * wl.new_tokens + 4,
                     "how": "qw_generate with host buffers minus qw_prefill with host buffers, host wall clock",
                     "generate_ms": 1000 * float(np.mean(t_gen)), "ttft_ms": 1000 * float(np.mean(t_pref))},
-            "gpu_launches": args.steps * ((2 + 12 * s.n_layers) + decode_launches_per_token(s) * n_dec),
+            "gpu_launches": args.steps * (prefill_launches(s, wl.prompt_len) + decode_launches_per_token(s) * n_dec),
             "clocks": clk.summary(),
             "host_ms_per_step": 1000 * t_host / args.steps,
             "source_hash": src,
