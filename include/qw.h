@@ -40,7 +40,7 @@ extern "C" {
 typedef enum {
   QW_OK = 0,
   QW_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent config */
-  QW_ERR_UNSUPPORTED = 2,   /* a shape this build has no kernel for */
+  QW_ERR_UNSUPPORTED = 2,   /* a shape the library has no kernel for */
   QW_ERR_CAPACITY = 3,      /* a sequence would exceed kv_capacity */
   QW_ERR_TOKEN_RANGE = 4,   /* a token id outside [0, vocab) */
   QW_ERR_CUDA = 5,          /* a CUDA runtime call failed; destroy the model */
