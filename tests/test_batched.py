@@ -100,3 +100,16 @@ def test_batched_1p5b_shape_sampled():
     prompts = make_batch_prompts(s, 8, 8, 40)
     rep = _run_batch(s, w, prompts, 4, 64, {0, 5})
     print(f"1p5b batched: steps {rep.steps} max rel {rep.max_rel:.4f} near-ties {rep.near_ties}")
+
+
+@pytest.mark.parametrize("env", [{"QW_BATCHED_ATTN_MMA": "0"}, {"QW_BATCHED_SPLITS": "1"}])
+def test_batched_alternative_kernels(monkeypatch, env):
+    """The CUDA-core batched attention (off by default), and the tensor-core one with a
+    single chunk per sequence (contexts of 65+ positions then span two 64-position tiles),
+    match the oracle on 16 ragged sequences."""
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    s = SHAPES["hd128_bf16"]
+    w = make_weights(s)
+    prompts = make_batch_prompts(s, 16, 40, 120)
+    _run_batch(s, w, prompts, 4, 128, {0, 7, 15})

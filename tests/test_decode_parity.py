@@ -112,6 +112,18 @@ def test_1p5b_long_context_sampled():
         m.close()
 
 
+def test_cuda_core_decode_attention(monkeypatch):
+    """Decode attention on CUDA cores (QW_ATTN_MMA=0; the tensor-core kernel is the default)
+    with its chunks merged in the o_proj GEMV, on a head_dim-128 shape."""
+    monkeypatch.setenv("QW_ATTN_MMA", "0")
+    w, prompt, toks, logits = oracle_run("hd128_bf16", 150, 12)
+    m = _model("hd128_bf16", w, 200)
+    try:
+        run_teacher_forced(m, SHAPES["hd128_bf16"], prompt, toks, logits)
+    finally:
+        m.close()
+
+
 # ---- persistent step kernel (one cooperative launch per decode step) ------------------
 
 @pytest.mark.parametrize("shape_name,P,n_new,cap,slot_kb", [
