@@ -314,27 +314,25 @@ static cudaError_t prefill_simt(const Dims& d, const LayerPtrs* layers, const vo
 //
 // Causal attention of T query rows over keys 0..pos0+T-1 ("LLM Speedrun: Architecture":
 // Attention, Causal mask, Grouped Query Attention), in the streaming form with a running
-// maximum and sum per row. One CTA per (64 query rows, head), four warps of 16 rows each.
+// maximum and sum per row. One CTA per (128 query rows, head), eight warps of 16 rows each.
 // S = Q K^T and O += P V run as mma.sync m16n8k16 with fp16 operands and fp32
 // accumulators: q (scaled by 1/sqrt(hd)) and the probabilities are rounded to fp16 like the
-// cache. Q stays in registers as A fragments; key tiles of 64 rows arrive by cp.async
-// (two buffers, rows padded by 16 bytes so every fragment load is bank-conflict free);
-// value tiles are stored transposed so a B fragment is one 32-bit shared load. The output
-// goes straight to the fp16 operand of the o_proj GEMM.
-constexpr int PM_Q = 64, PM_K = 64, PM_WARPS = 4;
+// cache. Q stays in registers as A fragments; key and value tiles of 64 rows arrive by
+// cp.async (two buffers, rows padded by 16 bytes so fragment loads are bank-conflict free):
+// key B fragments are 32-bit shared loads, value B fragments come from ldmatrix.trans. The
+// output goes straight to the fp16 operand of the o_proj GEMM.
+constexpr int PM_WARPS = 8, PM_Q = 16 * PM_WARPS, PM_K = 64;
 
 template <int HD>
 __global__ void __launch_bounds__(PM_WARPS * 32) attn_prefill_mma_kernel(const float* Q, int T_, int nq, int nkv,
                                                                         int pos0, const f16* kc, const f16* vc,
                                                                         int cap, float scale, f16* Oh) {
-  constexpr int KS = HD + 8;      // halves per key row in shared memory
-  constexpr int VS = PM_K + 8;    // halves per transposed value row (one head dimension)
+  constexpr int KS = HD + 8;      // halves per key / value row in shared memory (16-byte pad)
   constexpr int NKK = HD / 16;    // k-steps of S = Q K^T
   constexpr int NNT = HD / 8;     // n-tiles of O
-  constexpr int VPT = PM_K * HD / 8 / (PM_WARPS * 32);  // 16-byte value vectors per thread per tile
   extern __shared__ __align__(16) unsigned char pm_smem[];
   f16* Ks = reinterpret_cast<f16*>(pm_smem);  // [2][PM_K][KS]
-  f16* Vt = Ks + 2 * PM_K * KS;               // [2][HD][VS]
+  f16* Vs = Ks + 2 * PM_K * KS;               // [2][PM_K][KS]
   const int qb = gridDim.x - 1 - blockIdx.x;  // the longest (last) query blocks first
   const int h = blockIdx.y, g = h / (nq / nkv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
@@ -358,37 +356,17 @@ __global__ void __launch_bounds__(PM_WARPS * 32) attn_prefill_mma_kernel(const f
       qa[kk][r] = pack_half2(v.x * scale, v.y * scale);
     }
   }
-  auto load_k = [&](int t, int buf) {  // cp.async of key rows, zeros past the last key
+  auto load_tile = [&](int t, int buf) {  // key and value rows by cp.async, zeros past the last key
+    constexpr int NV = PM_K * HD / 8;
     const int k0 = t * PM_K;
-    f16* dst = Ks + (size_t)buf * PM_K * KS;
-    for (int i = tid; i < PM_K * HD / 8; i += PM_WARPS * 32) {
-      const int j = i / (HD / 8), c8 = i - j * (HD / 8);
-      if (k0 + j <= last_key) cp_async16(dst + j * KS + c8 * 8, K + (size_t)(k0 + j) * HD + c8 * 8);
-      else *reinterpret_cast<uint4*>(dst + j * KS + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < 2 * NV; i += PM_WARPS * 32) {
+      const int which = i >= NV, idx = i - which * NV;
+      const int j = idx / (HD / 8), c8 = idx - j * (HD / 8);
+      f16* dst = (which ? Vs : Ks) + (size_t)buf * PM_K * KS + j * KS + c8 * 8;
+      if (k0 + j <= last_key) cp_async16(dst, (which ? V : K) + (size_t)(k0 + j) * HD + c8 * 8);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-  };
-  uint4 vr[VPT];
-  auto fetch_v = [&](int t) {  // value rows into registers (lane = key within the warp's block)
-    const int k0 = t * PM_K;
-#pragma unroll
-    for (int u = 0; u < VPT; ++u) {
-      const int i = tid + u * PM_WARPS * 32;
-      const int j = i % PM_K, db = i / PM_K;
-      vr[u] = k0 + j <= last_key ? __ldg(reinterpret_cast<const uint4*>(V + (size_t)(k0 + j) * HD) + db)
-                                 : make_uint4(0u, 0u, 0u, 0u);
-    }
-  };
-  auto store_vt = [&](int buf) {  // transposed: Vt[d][j]
-    f16* dst = Vt + (size_t)buf * HD * VS;
-#pragma unroll
-    for (int u = 0; u < VPT; ++u) {
-      const int i = tid + u * PM_WARPS * 32;
-      const int j = i % PM_K, db = i / PM_K;
-      const f16* e = reinterpret_cast<const f16*>(&vr[u]);
-#pragma unroll
-      for (int x = 0; x < 8; ++x) dst[(size_t)(db * 8 + x) * VS + j] = e[x];
-    }
   };
 
   float o[NNT][4];
@@ -397,22 +375,22 @@ __global__ void __launch_bounds__(PM_WARPS * 32) attn_prefill_mma_kernel(const f
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
   const int pos_lo = pos0 + r_lo, pos_hi = pos0 + r_hi;
   const int warp_first = pos0 + q0 + warp * 16;  // smallest position among this warp's rows
+  // value rows of ldmatrix.trans: row (lane % 8) + 8 ((lane / 8) % 2) of a 16-key step,
+  // columns of n-tile pair (lane / 16)
+  const int v_row = (lane & 7) + ((lane >> 3) & 1) * 8, v_col = (lane >> 4) * 8;
 
-  load_k(0, 0);
-  fetch_v(0);
-  store_vt(0);
+  load_tile(0, 0);
   for (int t = 0; t < ntiles; ++t) {
     const int buf = t & 1, k0 = t * PM_K;
     if (t + 1 < ntiles) {
-      load_k(t + 1, buf ^ 1);
-      fetch_v(t + 1);
+      load_tile(t + 1, buf ^ 1);
       asm volatile("cp.async.wait_group 1;" ::: "memory");
     } else {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
-    __syncthreads();  // key tile t and value tile t visible to every warp
+    __syncthreads();  // tile t visible to every warp
     const f16* kt = Ks + (size_t)buf * PM_K * KS;
-    const f16* vt = Vt + (size_t)buf * HD * VS;
+    const f16* vt = Vs + (size_t)buf * PM_K * KS;
     if (k0 <= pos0 + min(q0 + warp * 16 + 15, last_q)) {  // some key of the tile is visible to this warp
       float sc[PM_K / 8][4];
 #pragma unroll
@@ -477,17 +455,20 @@ __global__ void __launch_bounds__(PM_WARPS * 32) attn_prefill_mma_kernel(const f
         o[nt][1] *= c_lo;
         o[nt][2] *= c_hi;
         o[nt][3] *= c_hi;
-        const f16* vrow = vt + (size_t)(8 * nt + gid) * VS + 2 * tig;
+      }
 #pragma unroll
-        for (int kk = 0; kk < PM_K / 16; ++kk) {
-          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(vrow + 16 * kk);
-          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(vrow + 16 * kk + 8);
-          mma16816(o[nt], pa[kk], b0, b1);
+      for (int kk = 0; kk < PM_K / 16; ++kk) {
+        const f16* vrow = vt + (size_t)(16 * kk + v_row) * KS + v_col;
+#pragma unroll
+        for (int nt = 0; nt < NNT; nt += 2) {
+          uint32_t b[4];
+          ldmatrix_x4_trans(b, vrow + nt * 8);
+          mma16816(o[nt], pa[kk], b[0], b[1]);
+          mma16816(o[nt + 1], pa[kk], b[2], b[3]);
         }
       }
     }
     __syncthreads();  // every warp is done with buffer buf
-    if (t + 1 < ntiles) store_vt(buf ^ 1);
   }
   const float i_lo = l_lo > 0.f ? 1.f / l_lo : 0.f, i_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
 #pragma unroll
@@ -502,7 +483,7 @@ __global__ void __launch_bounds__(PM_WARPS * 32) attn_prefill_mma_kernel(const f
 
 template <int HD>
 static constexpr size_t pm_smem() {
-  return (size_t)(2 * PM_K * (HD + 8) + 2 * HD * (PM_K + 8)) * sizeof(f16);
+  return (size_t)2 * 2 * PM_K * (HD + 8) * sizeof(f16);
 }
 
 static cudaError_t pm_set_attributes() {
