@@ -379,11 +379,37 @@ __global__ void __launch_bounds__(DM_WARPS * 32) attn_decode_mma_kernel(const De
   if (split >= nsplit) return;
   const int j0 = split * chunk, j1 = min(ctx, j0 + chunk), n = j1 - j0;
   const int ntiles = (n + DM_K - 1) / DM_K;
-  pdl_wait();  // q and the newest cache row come from the projections just before
-  pdl_trigger();
-  tl_stamp(a.tl, 1);
   const f16* K = a.k + z * a.kv_zs + ((size_t)g * a.stride + j0) * HD;
   const f16* V = a.v + z * a.kv_zs + ((size_t)g * a.stride + j0) * HD;
+  // the first tile's rows written by earlier steps are fetched before the dependency wait;
+  // q and the newest row (written by the projections just before) only after it
+  const int newest = j1 == ctx ? n - 1 : -1;  // chunk-relative, or none in this chunk
+  auto load_tile = [&](int t, int buf, int skip) {  // rows t*DM_K.. of K and V (row skip left out)
+    constexpr int NV = DM_K * HD / 8;  // 16-byte vectors of a K (or V) tile
+    for (int i = tid; i < 2 * NV; i += DM_WARPS * 32) {
+      const int which = i >= NV, idx = i - which * NV;
+      const int j = idx / (HD / 8), c8 = idx - j * (HD / 8);
+      f16* dst = (which ? Vs : Ks) + (size_t)buf * DM_K * KS + j * KS + c8 * 8;
+      const int key = t * DM_K + j;
+      if (key == skip) continue;
+      if (key < n) cp_async16(dst, (which ? V : K) + (size_t)key * HD + c8 * 8);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  const bool newest_in_first = newest >= 0 && newest < DM_K;
+  load_tile(0, 0, newest_in_first ? newest : -1);
+  pdl_wait();
+  pdl_trigger();
+  tl_stamp(a.tl, 1);
+  if (newest_in_first) {  // its own copy group, after the rest of tile 0
+    for (int i = tid; i < 2 * (HD / 8); i += DM_WARPS * 32) {
+      const int which = i >= HD / 8, c8 = i - which * (HD / 8);
+      f16* dst = (which ? Vs : Ks) + (size_t)newest * KS + c8 * 8;
+      cp_async16(dst, (which ? V : K) + (size_t)newest * HD + c8 * 8);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   uint32_t qa[NKK][4];
   {
     const float* qz = a.q + (size_t)z * a.nq * HD + (size_t)g * G * HD;
@@ -398,28 +424,15 @@ __global__ void __launch_bounds__(DM_WARPS * 32) attn_decode_mma_kernel(const De
         qa[kk][r] = pack_half2(v.x * a.scale, v.y * a.scale);
       }
   }
-  auto load_tile = [&](int t, int buf) {
-    constexpr int NV = DM_K * HD / 8;  // 16-byte vectors of a K (or V) tile
-    for (int i = tid; i < 2 * NV; i += DM_WARPS * 32) {
-      const int which = i >= NV, idx = i - which * NV;
-      const int j = idx / (HD / 8), c8 = idx - j * (HD / 8);
-      f16* dst = (which ? Vs : Ks) + (size_t)buf * DM_K * KS + j * KS + c8 * 8;
-      const int key = t * DM_K + j;
-      if (key < n) cp_async16(dst, (which ? V : K) + (size_t)key * HD + c8 * 8);
-      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
   float o[NNT][4];
 #pragma unroll
   for (int nt = 0; nt < NNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
   const int kw = 16 * warp;  // this warp's positions within a tile
-  load_tile(0, 0);
   for (int t = 0; t < ntiles; ++t) {
     const int buf = t & 1;
     if (t + 1 < ntiles) {
-      load_tile(t + 1, buf ^ 1);
+      load_tile(t + 1, buf ^ 1, -1);  // (the newest row lies in tile 0 or is loaded here after the wait)
       asm volatile("cp.async.wait_group 1;" ::: "memory");
     } else {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
