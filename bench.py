@@ -548,6 +548,9 @@ def run_long(args):
     torch.cuda.set_device(0)
     wl = WORKLOADS["1p5b_long"]
     s = SHAPES[wl.shape]
+    if args.layers:
+        import dataclasses
+        s = dataclasses.replace(s, n_layers=args.layers)
     n_dec = wl.new_tokens - 1
     w = make_weights(s)
     dw = DeviceWeights(w, 1)
@@ -582,7 +585,7 @@ def run_long(args):
     if os.path.exists(pp):
         with open(pp) as f:
             tflops_peak = json.load(f).get("bf16_tflops")
-    out = {"profile_run": "long", "prompt_len": wl.prompt_len, "decode_steps": n_dec,
+    out = {"profile_run": "long", "layers": s.n_layers, "prompt_len": wl.prompt_len, "decode_steps": n_dec,
            "ttft_ms": pre_ms, "prefill_flop": fl, "prefill_tflops": fl / (pre_ms / 1000.0) / 1e12,
            "bf16_tflops_peak_measured": tflops_peak,
            "decode_tok_s": n_dec / (dec_ms / 1000.0), "decode_gbs": bpt * n_dec / (dec_ms / 1000.0) / 1e9,

@@ -4,8 +4,9 @@
 // Implementing Qwen; "augur", Features):
 //   qkv    : RMSNorm(x) -> q/k/v projections + bias -> split-half RoPE -> KV append
 //   attn   : GQA attention of the new token over the cache, context split into chunks
-//            whose softmax partials are merged by the last CTA of each KV head
-//   resid  : o_proj, x += Wo . attn          (also the down projection, x += Wd . act)
+//            that leave softmax partials (maximum, sum, unnormalised output)
+//   oproj  : merge of those partials in the prologue, then x += Wo . attn
+//   resid  : the down projection, x += Wd . act
 //   gateup : RMSNorm(x) -> gate/up projections -> SwiGLU
 // then the LM head: final RMSNorm -> logits = E . h -> greedy argmax.
 //
@@ -545,9 +546,23 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
         xr[q][e] = t.x; xr[q][e + 1] = t.y; xr[q][e + 2] = t.z; xr[q][e + 3] = t.w;
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < VN; ++e) xr[q][e] = v < v1 ? xs[v * VN + e] : 0.f;
+    } else if constexpr (VN == 8) {
+      // Two 16-byte shared loads per vector. Lane l's vector starts 32 bytes after lane
+      // l-1's, so lanes l and l+4 would share banks; lanes with bit 2 set take the halves
+      // in the other order, and each 8-lane phase of a 16-byte load hits all 32 banks once.
+      const bool sw = (lane & 4) != 0;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (v < v1) {
+        const float4* p = reinterpret_cast<const float4*>(xs) + 2 * v;
+        a = p[sw ? 1 : 0];
+        b = p[sw ? 0 : 1];
+      }
+      const float4 lo = sw ? b : a, hi = sw ? a : b;
+      xr[q][0] = lo.x; xr[q][1] = lo.y; xr[q][2] = lo.z; xr[q][3] = lo.w;
+      xr[q][4] = hi.x; xr[q][5] = hi.y; xr[q][6] = hi.z; xr[q][7] = hi.w;
+    } else {  // one 16-byte vector per lane, consecutive: conflict-free
+      const float4 a = v < v1 ? reinterpret_cast<const float4*>(xs)[v] : make_float4(0.f, 0.f, 0.f, 0.f);
+      xr[q][0] = a.x; xr[q][1] = a.y; xr[q][2] = a.z; xr[q][3] = a.w;
     }
   }
 
