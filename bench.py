@@ -133,6 +133,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(seconds, ws, device):
+    """Per entry, the largest of every rank's timings: the job is as slow as its slowest
+    replica. One all-reduce of float64 values over the initialised process group."""
+    if ws == 1:
+        return [float(x) for x in seconds]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(units_per_rank, ws, max_seconds):
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * ws / max_seconds
+
+
 def oracle_decode_sample(s, wl, n_decode, warmup=0):
     """Time the CPU oracle: one untimed prefill of the workload's prompt, then decode
     steps; returns (seconds per decode step list, threads)."""
@@ -286,15 +303,8 @@ def run_native(args):
     prefill_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
     decode_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
     step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(args.steps)]
-    dec_s = sum(decode_ms) / 1000.0
-    if ws > 1:
-        t = torch.tensor([dec_s, sum(step_ms) / 1000.0], device=f"cuda:{local}", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dec_s, tot_s = float(t[0]), float(t[1])
-    else:
-        tot_s = sum(step_ms) / 1000.0
-    tokens = n_dec * args.steps * ws
-    value = tokens / dec_s
+    dec_s, tot_s = max_over_ranks([sum(decode_ms) / 1000.0, sum(step_ms) / 1000.0], ws, f"cuda:{local}")
+    value = job_throughput(n_dec * args.steps, ws, dec_s)
     ctx_mean = wl.prompt_len + (n_dec - 1) / 2.0 + 1  # positions read per decode token, mean
     bpt = decode_bytes_per_token(s, ctx_mean)
     peak, peak_kind = read_peaks()
@@ -382,7 +392,8 @@ def run_native(args):
         m.prefill(prompt)
         t_pref.append(time.perf_counter() - t0)
     e2e_decode_s = max(1e-9, float(np.mean(t_gen)) - float(np.mean(t_pref)))
-    e2e_value = n_dec / e2e_decode_s * ws
+    e2e_decode_s, = max_over_ranks([e2e_decode_s], ws, f"cuda:{local}")
+    e2e_value = job_throughput(n_dec, ws, e2e_decode_s)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
