@@ -17,7 +17,7 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("shape_name", ["small_f32", "small_bf16"])
+@pytest.mark.parametrize("shape_name", ["small_f32", "small_bf16", "untied_bf16"])
 def test_batched_sequences_match_oracle(shape_name):
     from qwen2_decoder_forward_decode_gb300 import DeviceWeights, Model
     s = SHAPES[shape_name]

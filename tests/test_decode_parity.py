@@ -36,6 +36,7 @@ def _model(shape_name, w, cap, max_seqs=1):
     ("mha_f32", 70, 10, 96),     # n_kv_heads == n_heads, prompt spans two attention tiles
     ("small_bf16", 100, 40, 160),
     ("hd128_bf16", 150, 12, 200),
+    ("untied_bf16", 45, 12, 64),  # separate LM head, no q/k/v bias, vocab 2051
 ])
 def test_small_shapes_teacher_forced(shape_name, P, n_new, cap):
     w, prompt, toks, logits = oracle_run(shape_name, P, n_new)

@@ -262,6 +262,45 @@ def test_eos_is_appended_then_stops():
     assert t2 == t[:t.index(t[2]) + 1]
 
 
+# --- optional weights: a separate LM head, no q/k/v bias ---------------------------------
+
+def test_untied_head_copy_of_embedding_matches_tied():
+    """A separate LM head equal to the embedding gives the tied model's logits exactly;
+    a different head changes them, so the separate head is the one read."""
+    s = SHAPES["untied_bf16"]
+    w = make_weights(s)
+    ids = make_prompt(s, 6)
+    tied = OracleModel(OracleConfig.from_shape(s), w)
+    tied.cfg.tied = True
+    w_copy = dict(w)
+    w_copy["lm_head.weight"] = w["model.embed_tokens.weight"].copy()
+    untied_copy = OracleModel(OracleConfig.from_shape(s), w_copy)
+    assert untied_copy.cfg.tied is False
+    t1, z1 = oracle.generate(tied, ids, 4)
+    t2, z2 = oracle.generate(untied_copy, ids, 4)
+    assert t1 == t2
+    for a, b in zip(z1, z2):
+        np.testing.assert_array_equal(a, b)
+    _, z3 = oracle.generate(OracleModel(OracleConfig.from_shape(s), w), ids, 1)
+    assert np.max(np.abs(z3[0] - z1[0])) > 1e-3
+
+
+def test_missing_qkv_bias_equals_zero_bias():
+    s = SHAPES["untied_bf16"]
+    w = make_weights(s)
+    assert not any(k.endswith("_proj.bias") for k in w)
+    w0 = dict(w)
+    for i in range(s.n_layers):
+        for name, n in (("q_proj", s.n_heads), ("k_proj", s.n_kv_heads), ("v_proj", s.n_kv_heads)):
+            w0[f"model.layers.{i}.self_attn.{name}.bias"] = np.zeros(n * s.head_dim, dtype=np.float32)
+    ids = make_prompt(s, 6)
+    t1, z1 = oracle.generate(OracleModel(OracleConfig.from_shape(s), w), ids, 4)
+    t2, z2 = oracle.generate(OracleModel(OracleConfig.from_shape(s), w0), ids, 4)
+    assert t1 == t2
+    for a, b in zip(z1, z2):
+        np.testing.assert_array_equal(a, b)
+
+
 # --- closed-form reduction: zero blocks --------------------------------------------------
 
 def test_zero_blocks_reduce_to_normed_embedding_logits():
