@@ -213,6 +213,15 @@ def test_bad_tokens_rejected():
             m.prefill(np.array([1, 2, 256], dtype=np.int32))
         assert e.value.status == 4
         with pytest.raises(QwError) as e:
+            m.prefill(np.array([], dtype=np.int32))   # empty prompt
+        assert e.value.status == 1
+        with pytest.raises(QwError) as e:
+            m.prefill(np.array([1], dtype=np.int32), seq=1)   # the model holds one sequence
+        assert e.value.status == 1
+        with pytest.raises(QwError) as e:
+            m.generate(np.array([1, 2], dtype=np.int32), 0)   # max_new counts the first token
+        assert e.value.status == 1
+        with pytest.raises(QwError) as e:
             m.decode_step()   # nothing prefilled
         assert e.value.status == 1
         m.prefill(np.array([1, 2, 3], dtype=np.int32))
