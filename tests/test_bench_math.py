@@ -1,0 +1,41 @@
+"""The bench's roofline arithmetic, checked against independent counts.
+
+Decode bytes per token are rebuilt from the parameter count, which test_oracle_pins
+checks against the page's printed figure. Each token reads every parameter once (the
+LM head is the tied embedding), the token's embedding row, each layer's K and V rows of
+every position, and writes fp32 logits. The FLOP counts are the rounded figures of the
+long-context and short prefill workloads."""
+import pytest
+
+import bench
+from synth import SHAPES, param_count
+
+
+@pytest.mark.parametrize("shape,ctx", [("1p5b", 178), ("0p5b", 48), ("1p5b", 4224)])
+def test_decode_bytes_per_token(shape, ctx):
+    s = SHAPES[shape]
+    kv_per_pos = s.n_layers * 2 * s.n_kv_heads * s.head_dim * 2  # fp16 K and V rows
+    want = param_count(s) * 2 + s.hidden * 2 + kv_per_pos * ctx + s.vocab * 4
+    assert bench.decode_bytes_per_token(s, ctx) == want
+
+
+def test_decode_bytes_match_the_quoted_figures():
+    # 1.5B at a 178-position mean context: 3093.1 MB; 0.5B at 48 positions: 989.3 MB
+    assert bench.decode_bytes_per_token(SHAPES["1p5b"], 178) / 1e6 == pytest.approx(3093.1, abs=0.1)
+    assert bench.decode_bytes_per_token(SHAPES["0p5b"], 48) / 1e6 == pytest.approx(989.3, abs=0.1)
+    assert SHAPES["1p5b"].n_layers * 2 * SHAPES["1p5b"].n_kv_heads * SHAPES["1p5b"].head_dim * 2 == 28672
+
+
+def test_gate_up_bytes_per_launch():
+    s = SHAPES["1p5b"]
+    assert bench.gateup_bytes(s) == 2 * 8960 * 1536 * 2 + 1536 * 2 == 55053312
+
+
+@pytest.mark.parametrize("shape,P,flop", [("1p5b", 4096, 1.218e13), ("1p5b", 128, 3.37e11), ("0p5b", 32, 2.32e10)])
+def test_prefill_flops(shape, P, flop):
+    assert bench.prefill_flops(SHAPES[shape], P) == pytest.approx(flop, rel=2e-3)
+
+
+def test_decode_launches_per_token():
+    # embedding, five kernels per layer (q/k/v, attention, o_proj, gate/up, down), LM head
+    assert bench.decode_launches_per_token(SHAPES["1p5b"]) == 1 + 5 * 28 + 1
