@@ -46,7 +46,8 @@ typedef enum {
   QW_ERR_CUDA = 5,          /* a CUDA runtime call failed; destroy the model */
   QW_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up; destroy the model */
   QW_ERR_FAULT_INJECTED = 7,/* QW_FAULT environment variable forced a failure */
-  QW_ERR_NUMERIC = 8        /* non-finite logits */
+  QW_ERR_NUMERIC = 8        /* non-finite logits, or a value outside the fp16 range of the
+                               KV cache (QW_BF16 models) or of a tensor-core operand */
 } qw_status;
 
 typedef enum { QW_F32 = 0, QW_BF16 = 1, QW_F16 = 2 } qw_dtype;
@@ -57,8 +58,10 @@ typedef enum { QW_F32 = 0, QW_BF16 = 1, QW_F16 = 2 } qw_dtype;
  * type of the weights, QW_F32 or QW_BF16. The KV cache is fp32 for QW_F32 models and fp16
  * for QW_BF16 models (same two bytes as bf16, eight times finer rounding); decode
  * activations, accumulators and logits are fp32; the prefill projections of QW_BF16 models
- * run on the tensor cores with fp16 operands (exact fp16 copies of the weights, made by
- * qw_create) and fp32 accumulation. */
+ * run on the tensor cores with fp16 operands (fp16 copies of the weights made by qw_create:
+ * exact for 2^-17 <= |w| <= 65504, smaller weights round to a multiple of 2^-24, larger ones
+ * are rejected) and fp32 accumulation. A key, value or operand that would overflow fp16 is
+ * reported as QW_ERR_NUMERIC by the next call that checks device errors. */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab;
   float rms_eps;          /* RMSNorm epsilon, inside the square root (1e-6) */
@@ -89,9 +92,16 @@ typedef struct {
 
 typedef struct qw_model qw_model;
 
-/* Validate the shape, allocate the KV cache [max_seqs][n_layers][2][n_kv_heads]
- * [kv_capacity][head_dim] and the working buffers, and build the RoPE cos/sin table
- * (angles in float64 on the host). cuda_stream is a cudaStream_t or NULL. */
+/* Build a model from its configuration and borrowed weights [LSA Implementing Qwen: the
+ * model configuration and the Decoder that holds the embedding, the layers, the final
+ * norm and the LM head; AUG Features: preallocated KV cache]. Validates the shape,
+ * allocates the KV cache [max_seqs][n_layers][2][n_kv_heads][kv_capacity][head_dim] and
+ * the working buffers, and builds the RoPE cos/sin table [LSA RoPE: angle = position *
+ * theta^(-2i/head_dim)] with float64 angles on the host. cuda_stream is a cudaStream_t or
+ * NULL. On success *out holds the model (release it with qw_destroy); on failure *out is
+ * NULL and nothing stays allocated. Errors: QW_ERR_INVALID_ARG for a null, misaligned or
+ * inconsistent argument, QW_ERR_UNSUPPORTED for a shape without kernels, QW_ERR_CUDA when
+ * no GPU is usable or an allocation fails, QW_ERR_FAULT_INJECTED under QW_FAULT=alloc. */
 qw_status qw_create(const qw_config *cfg, const qw_weights *w, void *cuda_stream,
                     qw_model **out);
 void qw_destroy(qw_model *m);
@@ -133,8 +143,10 @@ qw_status qw_generate(qw_model *m, const int32_t *ids, int32_t n, int32_t max_ne
 /* Wait for queued work and report a device-side error (token range, non-finite logits). */
 qw_status qw_sync(qw_model *m);
 
-/* Device pointer to the fp32 logits [max_seqs][vocab] of the last step; valid until the
- * next call that runs the model. */
+/* Device pointer to the fp32 logits [max_seqs][vocab] of the last step [LSA Decoding and
+ * Decoder.step: the logits of the last position, LM head applied to the final norm];
+ * row seq holds sequence seq's. Owned by the model; valid until the next call that runs
+ * it. NULL for a null model. */
 const float *qw_logits(const qw_model *m);
 
 /* Copy the fp32 logits [vocab] of sequence seq's last step to host memory (synchronises). */
@@ -143,10 +155,15 @@ qw_status qw_read_logits(qw_model *m, int32_t seq, float *host_out);
 /* Device pointer to int32 [max_seqs]: the greedy token of each sequence's last step. */
 const int32_t *qw_tokens_device(const qw_model *m);
 
-/* Current length (positions held in the cache) of sequence seq. */
+/* Current length of sequence seq: the positions its KV cache holds, which is also the
+ * position the next decode step runs at [LSA Decoder.step: positions of the new token;
+ * KV cache]. 0 for a sequence that is not active. Errors: QW_ERR_INVALID_ARG. */
 qw_status qw_position(const qw_model *m, int32_t seq, int32_t *pos);
 
-/* Forget sequence seq (length 0, inactive). */
+/* Forget sequence seq [LSA KVCache: a fresh cache per sequence; AUG Features:
+ * preallocated KV cache]: its length becomes 0 and it leaves the set of active sequences;
+ * its cache rows are overwritten by its next prefill. Does not synchronise. Errors:
+ * QW_ERR_INVALID_ARG for a null model or a sequence index outside [0, max_seqs). */
 qw_status qw_reset(qw_model *m, int32_t seq);
 
 /* Profiling hook. With begin and end non-NULL (host arrays of n_layers cudaEvent_t created
@@ -163,11 +180,7 @@ qw_status qw_set_trace(qw_model *m, int32_t kind, void *const *begin, void *cons
  * its wait for the previous kernel, and the last CTA's end. qw_read_timeline copies the
  * stamps of the last step, 3 per launch in launch order, into out (host, 3 * max_launches
  * uint64) and the launch count into n_launches. Timing differs slightly from an
- * uninstrumented run (one atomic per CTA per stamp). enable 0 frees the buffer.
- * When the model runs decode steps as one persistent kernel (bf16 models), the entries
- * are instead per phase of the step (q/k/v, attention, o_proj, gate/up, down per layer,
- * then the LM head), each [consumer start, consumer end, producer finished issuing the
- * phase's weight copies], stamped by the first CTA. */
+ * uninstrumented run (one atomic per CTA per stamp). enable 0 frees the buffer. */
 qw_status qw_set_timeline(qw_model *m, int32_t enable);
 qw_status qw_read_timeline(qw_model *m, uint64_t *out, int32_t max_launches, int32_t *n_launches);
 
@@ -212,7 +225,8 @@ qw_status qw_op_decode_attention(int32_t kv_dtype, int32_t n_heads, int32_t n_kv
  *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library routine. Every
  *     GPU that loads the library holds the array until the process exits.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- *     with that device current); make that first call before any stream capture.
+ *     with that device current); make that first call before any stream capture. A first
+ *     call on a stream that is capturing returns QW_ERR_INVALID_ARG and does nothing.
  *   - Each call clears the counters it needs (cudaMemsetAsync on cuda_stream). All calls
  *     share the one array: calls that overlap on the GPU (other streams, other threads)
  *     race on it and must be serialised by the caller. */

@@ -252,10 +252,8 @@ class Model:
         check(lib().qw_set_timeline(self.h, int(enable)))
 
     def read_timeline(self):
-        """[(start_ns, wait_released_ns, end_ns)] per kernel of the last decode step (with the
-        step kernel: per phase [start, end, producer issued], the ring counters, then per
-        phase [input staged, first unit ready, units done])."""
-        n_max = 3 + 10 * self.shape.n_layers  # the step kernel's layout is the longer one
+        """[(start_ns, wait_released_ns, end_ns)] per kernel of the last decode step."""
+        n_max = 3 + 10 * self.shape.n_layers  # a batched step launches the most kernels
         buf = (ctypes.c_uint64 * (3 * n_max))()
         n = np.zeros(1, dtype=np.int32)
         check(lib().qw_read_timeline(self.h, buf, n_max, _iptr(n)))

@@ -82,17 +82,6 @@ struct qw_model {
   bool attn_mma = false;        // decode attention on the tensor cores (fp16 cache)
   int trace_kind = -1;
   std::vector<cudaEvent_t> trace_begin, trace_end;
-  // persistent decode-step kernel (bf16 models)
-  bool use_step = false;
-  StepLayer* step_layers = nullptr;
-  float* step_part = nullptr;
-  unsigned long long* step_bar = nullptr;
-  unsigned long long step_bar_base = 0;  // barrier counter value before the next launch
-  int* step_abort = nullptr;  // [0] abort flag, [1..] diagnostics of expired waits
-  int step_nslots = 0;
-  int step_slot = 0;
-  int step_pf_units = 0;
-  size_t step_smem = 0;
   // batched decode (bf16 models with the fp16 matrix copies, several sequences)
   bool use_batched = false;
   std::vector<BatchedLayerPlans> bplans;
@@ -197,50 +186,7 @@ struct qw_model {
     if (bgraph) { cudaGraphExecDestroy(bgraph); bgraph = nullptr; }
   }
 
-  cudaError_t run_step_kernel(int s) {
-    StepLaunch a{};
-    a.d = d;
-    a.layers_dev = step_layers;
-    a.embed = embed;
-    a.final_norm = final_norm;
-    a.head = head_w();
-    a.rope = rope;
-    a.kv_seq = kv_seq(s);
-    a.x = x + (size_t)s * d.H;
-    a.q = q;
-    a.act = act;
-    a.logits = logits + (size_t)s * d.V;
-    a.part = step_part;
-    a.tok = tok + s;
-    a.pos = pos + s;
-    a.key = keys + s;
-    a.hist = hist + (size_t)s * d.cap;
-    a.hist_n = hist_n + s;
-    a.hist_cap = d.cap;
-    a.bar = step_bar;
-    a.bar_base = step_bar_base;
-    step_bar_base += (unsigned long long)step_barriers_per_launch(d) * d.nsm;
-    a.abort = step_abort;
-    a.diag = step_abort + 1;
-    a.err = err;
-    a.nslots = step_nslots;
-    a.slot = step_slot;
-    a.pf_units = step_pf_units;
-    a.grid = d.nsm;
-    a.smem = step_smem;
-    a.tl = tl_buf;
-    return launch_step(a, stream);
-  }
-
   cudaError_t run_decode(int s) {
-    if (use_step && trace_kind < 0) {
-      if (tl_buf) {  // fresh counters for this step
-        cudaError_t e = cudaMemcpyAsync(tl_buf, tl_init.data(), sizeof(unsigned long long) * 3 * tl_n,
-                                        cudaMemcpyHostToDevice, stream);
-        if (e) return e;
-      }
-      return run_step_kernel(s);
-    }
     if (tl_buf) {  // per launch: start and wait-release reduce with min, end with max
       cudaError_t e = cudaMemcpyAsync(tl_buf, tl_init.data(), sizeof(unsigned long long) * 3 * tl_n,
                                       cudaMemcpyHostToDevice, stream);
@@ -399,22 +345,9 @@ struct qw_model {
       QW_CUDA(cudaStreamSynchronize(stream));
       if (h & ERR_TOKEN) return fail(QW_ERR_TOKEN_RANGE, "token id outside [0, vocab) on the device");
       if (h & ERR_NONFINITE) return fail(QW_ERR_NUMERIC, "non-finite logits");
-      if (h & ERR_TIMEOUT) {
-        int dg[5] = {0, 0, 0, 0, 0};
-        if (step_abort) cudaMemcpy(dg, step_abort, sizeof(dg), cudaMemcpyDeviceToHost);
-        std::string msg = "device wait timed out (site " + std::to_string(dg[1]) + ", CTA " +
-                          std::to_string(dg[2]) + ", warp " + std::to_string(dg[3]) + ", detail " +
-                          std::to_string(dg[4]) + ")";
-        if (step_abort) {  // per CTA: where each gave up (site, warp, detail)
-          std::vector<int> all(4 * (size_t)d.nsm);
-          cudaMemcpy(all.data(), step_abort + 5, all.size() * sizeof(int), cudaMemcpyDeviceToHost);
-          msg += "; per CTA:";
-          for (int c = 0; c < d.nsm; ++c)
-            if (all[4 * c]) msg += " " + std::to_string(c) + ":" + std::to_string(all[4 * c]) + "/" +
-                                   std::to_string(all[4 * c + 1]) + "/" + std::to_string(all[4 * c + 2]);
-        }
-        return fail(QW_ERR_TIMEOUT, msg);
-      }
+      if (h & ERR_RANGE)
+        return fail(QW_ERR_NUMERIC, "a value outside the fp16 range of the KV cache or of a tensor-core operand");
+      if (h & ERR_TIMEOUT) return fail(QW_ERR_TIMEOUT, "a bounded device-side wait gave up");
     }
     return QW_OK;
   }
@@ -428,8 +361,7 @@ struct qw_model {
     if (bblock) cudaFree(bblock);
     if (battn_ws) cudaFree(battn_ws);
     void* bufs[] = {kv, x, q, attn, act, logits, rope, attn_ws, keys, lm_counter, pos, tok,
-                    hist, hist_n, err, ids, pf_block, pf_ws, w16, tl_buf, step_layers, step_part, step_bar,
-                    step_abort};
+                    hist, hist_n, err, ids, pf_block, pf_ws, w16, tl_buf};
     for (void* b : bufs)
       if (b) cudaFree(b);
     if (pinned) cudaFreeHost(pinned);
@@ -472,6 +404,17 @@ static qw_status validate(const qw_config* c, const qw_weights* w) {
   if ((uintptr_t)w->embed % 16) return fail(QW_ERR_INVALID_ARG, "embedding not 16-byte aligned");
   if (w->lm_head && (uintptr_t)w->lm_head % 16) return fail(QW_ERR_INVALID_ARG, "lm_head not 16-byte aligned");
   return QW_OK;
+}
+
+static int op_attn_nsplit(int head_dim, int max_ctx, int kv_bytes) {
+  return attn_nsplit_for(max_ctx, ATTN_CHUNK_MIN, head_dim, kv_bytes);
+}
+
+// Workspace bytes that qw_op_decode_attention uses for this shape and KV element type; its
+// per-KV-head counters are the last n_kv_heads * 4 bytes of that range.
+size_t qw::op_attn_workspace_exact(int kv_dtype, int n_heads, int n_kv_heads, int head_dim, int kv_stride) {
+  const int nsplit = op_attn_nsplit(head_dim, kv_stride, kv_dtype == QW_F16 ? 2 : 4);
+  return attn_workspace_bytes(n_heads, n_kv_heads, head_dim, nsplit);
 }
 
 extern "C" {
@@ -600,39 +543,6 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
     }
   }
   if ((e = decode_set_attributes(d))) return bail(e, "decode attributes");
-  {
-    // decode path: one kernel per operation (default), or the persistent step kernel
-    // (QW_STEP_KERNEL=1) where the shape supports it
-    const char* sk = std::getenv("QW_STEP_KERNEL");
-    int coop = 0;
-    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device);
-    if (step_kernel_supported(d) && coop && sk && sk[0] == '1') {
-      const char* skb = std::getenv("QW_STEP_SLOT_KB");  // ring slot size (tuning knob)
-      const int slot_bytes = skb ? (int)(std::atof(skb) * 1024) : 0;
-      const char* spf = std::getenv("QW_STEP_PF_UNITS");  // L2 prefetch distance (tuning knob)
-      m->step_pf_units = spf ? std::atoi(spf) : 0;
-      if ((e = step_set_attributes(d, slot_bytes, &m->step_slot, &m->step_nslots, &m->step_smem)))
-        return bail(e, "step attributes");
-      std::vector<StepLayer> sl(d.L);
-      for (int l = 0; l < d.L; ++l) {
-        const LayerPtrs& w = m->layers[l];
-        sl[l] = StepLayer{(const bf16*)w.in_norm, (const bf16*)w.wq, (const bf16*)w.wk, (const bf16*)w.wv,
-                          (const bf16*)w.bq, (const bf16*)w.bk, (const bf16*)w.bv, (const bf16*)w.wo,
-                          (const bf16*)w.post_norm, (const bf16*)w.w_gate, (const bf16*)w.w_up,
-                          (const bf16*)w.w_down};
-      }
-      if ((e = cudaMalloc(&m->step_layers, sizeof(StepLayer) * d.L))) return bail(e, "cudaMalloc");
-      if ((e = cudaMemcpy(m->step_layers, sl.data(), sizeof(StepLayer) * d.L, cudaMemcpyHostToDevice)))
-        return bail(e, "cudaMemcpy");
-      if ((e = cudaMalloc(&m->step_part, step_part_bytes(d)))) return bail(e, "cudaMalloc");
-      if ((e = cudaMalloc(&m->step_bar, sizeof(unsigned long long)))) return bail(e, "cudaMalloc");
-      if ((e = cudaMemset(m->step_bar, 0, sizeof(unsigned long long)))) return bail(e, "cudaMemset");
-      const size_t nd = 5 + 4 * (size_t)d.nsm;
-      if ((e = cudaMalloc(&m->step_abort, nd * sizeof(int)))) return bail(e, "cudaMalloc");
-      if ((e = cudaMemset(m->step_abort, 0, nd * sizeof(int)))) return bail(e, "cudaMemset");
-      m->use_step = true;
-    }
-  }
   if (m->pf.use_tc && S > 1) {
     // batched decode: every weight matrix read once per step for all active sequences
     const char* bz = std::getenv("QW_BATCHED");
@@ -929,10 +839,6 @@ qw_status qw_set_timeline(qw_model* m, int32_t enable) {
   if (m->use_batched) m->tl_n = std::max(m->tl_n, 3 + 10 * m->d.L);  // launches of a batched step
   m->tl_init.assign((size_t)3 * m->tl_n, ~0ull);
   for (int i = 0; i < m->tl_n; ++i) m->tl_init[3 * i + 2] = 0ull;
-  if (m->use_step) {  // per phase [start, end, producer issued]; ring counters; per phase sub-stamps
-    m->tl_n = 2 * (5 * m->d.L + 1) + 1;
-    m->tl_init.assign((size_t)3 * m->tl_n, 0ull);
-  }
   QW_CUDA(cudaMalloc(&m->tl_buf, sizeof(unsigned long long) * 3 * m->tl_n));
   QW_CUDA(cudaMemcpy(m->tl_buf, m->tl_init.data(), sizeof(unsigned long long) * 3 * m->tl_n,
                      cudaMemcpyHostToDevice));
@@ -962,6 +868,7 @@ qw_status qw_read_logits(qw_model* m, int32_t seq, float* host_out) {
 const int32_t* qw_tokens_device(const qw_model* m) { return m ? m->tok : nullptr; }
 
 qw_status qw_position(const qw_model* m, int32_t seq, int32_t* pos) {
+  g_err.clear();
   if (!m || !pos) return fail(QW_ERR_INVALID_ARG, "null argument");
   if (seq < 0 || seq >= m->d.max_seqs) return fail(QW_ERR_INVALID_ARG, "sequence index out of range");
   *pos = m->active[seq] ? m->h_pos[seq] : 0;
@@ -969,6 +876,7 @@ qw_status qw_position(const qw_model* m, int32_t seq, int32_t* pos) {
 }
 
 qw_status qw_reset(qw_model* m, int32_t seq) {
+  g_err.clear();
   if (!m) return fail(QW_ERR_INVALID_ARG, "null model");
   if (seq < 0 || seq >= m->d.max_seqs) return fail(QW_ERR_INVALID_ARG, "sequence index out of range");
   m->active[seq] = 0;
@@ -979,10 +887,6 @@ qw_status qw_reset(qw_model* m, int32_t seq) {
 }
 
 // ---- single-op entry points ----
-
-static int op_attn_nsplit(int head_dim, int max_ctx, int kv_bytes) {
-  return attn_nsplit_for(max_ctx, ATTN_CHUNK_MIN, head_dim, kv_bytes);
-}
 
 size_t qw_op_decode_attention_workspace(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                         int32_t max_ctx) {
@@ -1004,7 +908,7 @@ qw_status qw_op_decode_attention(int32_t kv_dtype, int32_t n_heads, int32_t n_kv
   if (head_dim % 8 || (n_heads / n_kv_heads) * head_dim > 1024)
     return fail(QW_ERR_UNSUPPORTED, "head_dim must be a multiple of 8 with (n_heads / n_kv_heads) * head_dim <= 1024");
   const int nsplit = op_attn_nsplit(head_dim, kv_stride, kv_dtype == QW_F16 ? 2 : 4);
-  const size_t need = attn_workspace_bytes(n_heads, n_kv_heads, head_dim, nsplit);
+  const size_t need = op_attn_workspace_exact(kv_dtype, n_heads, n_kv_heads, head_dim, kv_stride);
   if (workspace_bytes < need) return fail(QW_ERR_INVALID_ARG, "workspace too small");
   if ((uintptr_t)workspace % 16) return fail(QW_ERR_INVALID_ARG, "workspace not 16-byte aligned");
   const size_t smem = attn_smem_bytes(n_heads / n_kv_heads, head_dim, kv_stride, nsplit, ATTN_CHUNK_MIN,

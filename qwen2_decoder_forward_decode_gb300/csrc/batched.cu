@@ -42,6 +42,11 @@ __device__ __forceinline__ float psum(const float* part, int splits, int n_total
   return acc;
 }
 
+// one element of a normalised row: fp16 rows feed the tensor cores (range checked), bf16
+// rows the LM head (the fp32 range)
+__device__ __forceinline__ void store_row(f16* o, float v, int* err) { *o = to_half_checked(v, err); }
+__device__ __forceinline__ void store_row(bf16* o, float v, int*) { *o = __float2bfloat16_rn(v); }
+
 constexpr int RN_THREADS = 512;
 constexpr int RN_COLS = 4;  // columns per thread: H <= RN_THREADS * RN_COLS
 
@@ -103,7 +108,7 @@ __global__ void __launch_bounds__(RN_THREADS) bresid_norm_kernel(const float* pa
 #pragma unroll
   for (int j = 0; j < RN_COLS; ++j) {
     const int k = threadIdx.x + j * RN_THREADS;
-    if (k < H) o[k] = from_f32<OutT>(v[j] * inv * g[j]);
+    if (k < H) store_row(o + k, v[j] * inv * g[j], err);
   }
   tl_stamp(tl, 2);
 }
@@ -153,8 +158,8 @@ __global__ void bqkv_epi_kernel(const float* part, int splits, int n_total, int 
     // the layer's cache of sequence b: [2][nkv][cap][hd], K then V
     f16* base = kc0 + (size_t)b * kv_zs + (head < nq + nkv ? 0 : (size_t)nkv * cap * hd);
     f16* dst = base + ((size_t)h * cap + p) * hd;
-    dst[i] = __float2half_rn(a);
-    dst[i + half] = __float2half_rn(c);
+    dst[i] = to_half_checked(a, err);
+    dst[i + half] = to_half_checked(c, err);
   }
   tl_stamp(tl, 2);
 }
@@ -162,7 +167,7 @@ __global__ void bqkv_epi_kernel(const float* part, int splits, int n_total, int 
 // A[b][i] = silu(gate) * up as fp16 (gate columns [0, I), up columns [I, 2I)); rows of
 // absent or inactive sequences are zero
 __global__ void bswiglu_kernel(const float* part, int splits, int n_total, int I, const int* active, int nseq,
-                               f16* A, unsigned long long* tl) {
+                               f16* A, int* err, unsigned long long* tl) {
   tl_stamp(tl, 0);
   pdl_wait();
   pdl_trigger();
@@ -175,7 +180,7 @@ __global__ void bswiglu_kernel(const float* part, int splits, int n_total, int I
     const float g = psum(part, splits, n_total, b, i), u = psum(part, splits, n_total, b, I + i);
     v = (g / (1.f + expf(-g))) * u;
   }
-  A[(size_t)b * I + i] = __float2half_rn(v);
+  A[(size_t)b * I + i] = to_half_checked(v, err);
   tl_stamp(tl, 2);
 }
 
@@ -308,7 +313,7 @@ cudaError_t batched_step(const BatchedCtx& c, cudaStream_t s) {
     } else {
       if ((e = skinny_run(pl.gu, c.part, nullptr, 0, S, c.active, nullptr, c.err, tl(), s))) return e;
       if ((e = launch_k(bswiglu_kernel, dim3((I + BT - 1) / BT, 16), dim3(BT), 0, s, pdl, (const float*)c.part,
-                        pl.gu.splits, pl.gu.n_total, I, c.active, S, c.A16, tl())))
+                        pl.gu.splits, pl.gu.n_total, I, c.active, S, c.A16, c.err, tl())))
         return e;
     }
     if ((e = skinny_run(pl.down, c.part, nullptr, 0, S, c.active, nullptr, c.err, tl(), s))) return e;

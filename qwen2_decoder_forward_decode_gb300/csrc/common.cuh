@@ -11,6 +11,28 @@ namespace qw {
 typedef __nv_bfloat16 bf16;
 typedef __half f16;
 
+// Device-side error bits, OR-ed into the model's status word:
+//   ERR_TOKEN     a token id outside [0, vocab)
+//   ERR_NONFINITE non-finite logits
+//   ERR_TIMEOUT   a bounded wait gave up
+//   ERR_RANGE     a value written to an fp16 KV cache or fp16 tensor-core operand lay
+//                 outside the fp16 range (or was not finite)
+enum : int { ERR_TOKEN = 1, ERR_NONFINITE = 2, ERR_TIMEOUT = 4, ERR_RANGE = 8 };
+
+// fp32 -> fp16 (round to nearest even) for data whose range the model does not bound: a
+// value that would round to infinity, or a non-finite one, sets ERR_RANGE in *err.
+__device__ __forceinline__ f16 to_half_checked(float v, int* err) {
+  if (!(fabsf(v) < 65520.f)) atomicOr(err, ERR_RANGE);
+  return __float2half_rn(v);
+}
+__device__ __forceinline__ __half2 to_half2_checked(float a, float b, int* err) {
+  if (!(fabsf(a) < 65520.f) || !(fabsf(b) < 65520.f)) atomicOr(err, ERR_RANGE);
+  return __floats2half2_rn(a, b);
+}
+// the KV-cache store of either element type (fp32 caches cannot overflow)
+__device__ __forceinline__ void store_kv(float* dst, float v, int*) { *dst = v; }
+__device__ __forceinline__ void store_kv(f16* dst, float v, int* err) { *dst = to_half_checked(v, err); }
+
 // Programmatic dependent launch: wait for the upstream grid's completion and memory,
 // and allow the downstream grid to be scheduled.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -119,6 +119,7 @@ struct OpQKV {
   const float2* rope;  // [cap][hd/2] (cos, sin)
   float* q_out;
   KV *kc, *vc;  // [nkv][cap][hd] of this layer and sequence
+  int* err;     // ERR_RANGE: a key or value outside the fp16 range of the cache
   int pos;
 
   // the position is set by the previous step's LM head, finished before this step began
@@ -179,8 +180,8 @@ struct OpQKV {
     } else {
       KV* c = head < nq + nkv ? kc : vc;
       KV* dst = c + ((size_t)h * cap + pos) * hd;
-      dst[i] = from_f32<KV>(a);
-      dst[i + half] = from_f32<KV>(b);
+      store_kv(dst + i, a, err);
+      store_kv(dst + i + half, b, err);
     }
   }
   __device__ void finish() {}
@@ -851,6 +852,7 @@ static cudaError_t qkv_t(const Dims& d, const LayerPtrs& w, const float* x, cons
   op.gain = (const T*)w.in_norm;
   op.x = x; op.eps = d.eps; op.d_pos = d_pos; op.rope = rope; op.q_out = q;
   op.kc = (KV*)kc; op.vc = (KV*)vc;
+  op.err = err;
   return run_gemv<T>(op, d.nsm, err, tl, s, pdl);
 }
 cudaError_t launch_qkv(const Dims& d, const LayerPtrs& w, const float* x, const int* d_pos,

@@ -291,9 +291,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               const float a0 = (g[i] / (1.f + expf(-g[i]))) * u[i];
               const float a1 = (g[i + 1] / (1.f + expf(-g[i + 1]))) * u[i + 1];
               if (col + 1 < N) {
-                *reinterpret_cast<__half2*>(out + i) = __floats2half2_rn(a0, a1);
+                *reinterpret_cast<__half2*>(out + i) = to_half2_checked(a0, a1, err);
               } else if (col < N) {
-                out[i] = __float2half_rn(a0);
+                out[i] = to_half_checked(a0, err);
               }
             }
           }
@@ -522,7 +522,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
 #pragma unroll
           for (int b = 0; b < 16; ++b) {
             const float g = gbuf[((q - 2) * 32 + lane) * 17 + b];
-            a.act[(size_t)b * a.n_act + i] = __float2half_rn((g / (1.f + expf(-g))) * v[b]);
+            a.act[(size_t)b * a.n_act + i] = to_half_checked((g / (1.f + expf(-g))) * v[b], a.err);
           }
         }
       }
@@ -568,7 +568,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
 
 // Act[m][n] = fp16(silu(g) * u), g and u the split sums (in split order) of ws[s][m][n] and
 // ws[s][m][N + n]
-__global__ void splitk_swiglu_kernel(const float* ws, int splits, int M, int N, f16* Act, int ldc) {
+__global__ void splitk_swiglu_kernel(const float* ws, int splits, int M, int N, f16* Act, int ldc, int* err) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)M * N) return;
   const int m = (int)(i / N), n = (int)(i - (size_t)m * N);
@@ -578,7 +578,7 @@ __global__ void splitk_swiglu_kernel(const float* ws, int splits, int M, int N, 
     g += __ldcg(row + n);
     u += __ldcg(row + N + n);
   }
-  Act[(size_t)m * ldc + n] = __float2half_rn((g / (1.f + expf(-g))) * u);
+  Act[(size_t)m * ldc + n] = to_half_checked((g / (1.f + expf(-g))) * u, err);
 }
 
 // C[m][n] = (add ? C[m][n] : 0) + sum over splits of ws[s][m][n] (in split order) + bias[n]
@@ -801,7 +801,7 @@ cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, 
                                                                                  splits, ws);
   if (splits > 1) {
     const size_t n = (size_t)M * N;
-    splitk_swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, Act, ldc);
+    splitk_swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, Act, ldc, err);
   }
   return cudaGetLastError();
 }

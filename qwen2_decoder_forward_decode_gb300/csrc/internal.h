@@ -9,8 +9,7 @@
 
 namespace qw {
 
-// Device-side error bits, OR-ed into the model's status word.
-enum : int { ERR_TOKEN = 1, ERR_NONFINITE = 2, ERR_TIMEOUT = 4 };
+// Device-side error bits (ERR_*) are defined in common.cuh.
 
 struct Dims {
   int L, H, nq, nkv, hd, I, V;
@@ -44,6 +43,9 @@ struct Finalize {
 
 // ---- api.cu ----
 void set_error_message(const char* msg);  // message returned by qw_last_error on this thread
+// bytes of workspace qw_op_decode_attention uses for this shape and KV type (kv_dtype a
+// qw_dtype); the per-KV-head counters occupy its last n_kv_heads * 4 bytes
+size_t op_attn_workspace_exact(int kv_dtype, int n_heads, int n_kv_heads, int head_dim, int kv_stride);
 
 // Floats per (head, chunk) row of the decode-attention partials: hd outputs, the maximum,
 // the sum of exponentials, padding to 16 bytes (rows stay aligned for vector loads).
@@ -106,37 +108,6 @@ cudaError_t gemm_tc(const __half* A, int lda, const __half* B, int ldb, const __
 cudaError_t gemm_tc_swiglu(const __half* A, int lda, const __half* Wg, const __half* Wu, int ldb,
                            __half* Act, int ldc, int M, int N, int K, int* err, cudaStream_t s, float* ws = nullptr,
                            size_t ws_floats = 0, int nsm = 0);
-
-// ---- step.cu (persistent decode step of one sequence, bf16 models) ----
-struct StepLayer {
-  const __nv_bfloat16 *in_norm, *wq, *wk, *wv, *bq, *bk, *bv, *wo, *post_norm, *wg, *wu, *wd;
-};
-struct StepLaunch {
-  Dims d;
-  const StepLayer* layers_dev;  // device array [L]
-  const void *embed, *final_norm, *head;
-  const float2* rope;
-  void* kv_seq;                 // fp16 cache of the sequence [L][2][nkv][cap][hd]
-  float *x, *q, *act, *logits, *part;
-  int *tok, *pos;
-  unsigned long long* key;
-  int *hist, *hist_n;
-  int hist_cap;
-  unsigned long long* bar;      // monotonic barrier counter, zero at creation
-  unsigned long long bar_base;  // its value before this launch
-  int *abort, *err;
-  int nslots, slot, grid;
-  int pf_units;                 // L2 prefetch distance in ring units (0: off)
-  size_t smem;
-  unsigned long long* tl;       // per phase [start, end, producer issued] or null
-  int* diag;                    // 4 ints: first expired wait (site, CTA, warp, detail)
-};
-int step_xs_floats(const Dims& d);
-int step_barriers_per_launch(const Dims& d);
-bool step_kernel_supported(const Dims& d);
-size_t step_part_bytes(const Dims& d);
-cudaError_t step_set_attributes(const Dims& d, int slot_bytes, int* slot_out, int* nslots_out, size_t* smem_out);
-cudaError_t launch_step(const StepLaunch& a, cudaStream_t s);
 
 // ---- gemm_tc.cu: skinny GEMM of batched decode ----
 // Precomputed tensor maps (opaque 128-byte CUtensorMap storage) and the launch shape of one

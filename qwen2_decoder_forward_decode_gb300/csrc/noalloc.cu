@@ -26,13 +26,20 @@ qw_status fail(qw_status s, const char* msg) {
   return s;
 }
 
-// Device address of the scratch array on the current device (set-up on first use).
-qw_status scratch_on_current_device(void** out) {
+// Device address of the scratch array on the current device. The first call on a device
+// looks it up (cudaGetSymbolAddress); that may not happen inside a stream capture.
+qw_status scratch_on_current_device(cudaStream_t s, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(QW_ERR_CUDA, "cudaGetDevice failed");
   if (dev < 0 || dev >= MAX_DEVICES) return fail(QW_ERR_UNSUPPORTED, "device index too large");
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_addr[dev]) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess)
+      return fail(QW_ERR_CUDA, "cudaStreamIsCapturing failed");
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(QW_ERR_INVALID_ARG,
+                  "the first qw_op_decode_attention_noalloc call on a device must come before any stream capture");
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_scratch);
     if (e != cudaSuccess || !p) return fail(QW_ERR_CUDA, cudaGetErrorString(e));
@@ -57,15 +64,18 @@ qw_status qw_op_decode_attention_noalloc(int32_t kv_dtype, int32_t n_heads, int3
   if (n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || head_dim < 2 || ctx < 1 || kv_stride < ctx)
     return fail(QW_ERR_INVALID_ARG, "bad attention shape");
   if (n_heads / n_kv_heads > 8) return fail(QW_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
-  const size_t need = qw_op_decode_attention_workspace(n_heads, n_kv_heads, head_dim, kv_stride);
+  // exactly the workspace the attention kernel will use for this KV type: its split count
+  // (and so where its counters sit) depends on the element size
+  const size_t need = qw::op_attn_workspace_exact(kv_dtype, n_heads, n_kv_heads, head_dim, kv_stride);
   if (need == 0 || need > NOALLOC_SCRATCH_BYTES)
     return fail(QW_ERR_UNSUPPORTED, "shape needs more scratch than the fixed 1 MiB array holds");
-  void* ws = nullptr;
-  qw_status st = scratch_on_current_device(&ws);
-  if (st) return st;
-  // the per-KV-head arrival counters sit at the end of the workspace and must start at zero
-  const size_t counters = (size_t)n_kv_heads * sizeof(unsigned int);
   cudaStream_t s = (cudaStream_t)cuda_stream;
+  void* ws = nullptr;
+  qw_status st = scratch_on_current_device(s, &ws);
+  if (st) return st;
+  // the per-KV-head arrival counters are the last bytes of that workspace and must start at
+  // zero; an earlier call of another shape may have left partials there
+  const size_t counters = (size_t)n_kv_heads * sizeof(unsigned int);
   if (cudaMemsetAsync((char*)ws + need - counters, 0, counters, s) != cudaSuccess)
     return fail(QW_ERR_CUDA, "cudaMemsetAsync of the scratch counters failed");
   return qw_op_decode_attention(kv_dtype, n_heads, n_kv_heads, head_dim, ctx, kv_stride, q, k, v, out, ws,

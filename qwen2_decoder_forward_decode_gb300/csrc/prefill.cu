@@ -28,8 +28,11 @@ __global__ void embed_rows_kernel(const T* E, int V, int H, const int* ids, floa
   for (int k = threadIdx.x; k < H; k += blockDim.x) X[(size_t)t * H + k] = to_f32(row[k]);
 }
 
+__device__ __forceinline__ void store_norm(float* y, float v, int*) { *y = v; }
+__device__ __forceinline__ void store_norm(f16* y, float v, int* err) { *y = to_half_checked(v, err); }
+
 template <typename T, typename OutT>
-__global__ void norm_rows_kernel(const float* X, const T* gain, int H, float eps, OutT* Y) {
+__global__ void norm_rows_kernel(const float* X, const T* gain, int H, float eps, OutT* Y, int* err) {
   __shared__ float scratch[32];
   const float* x = X + (size_t)blockIdx.x * H;
   float ss = 0.f;
@@ -37,13 +40,13 @@ __global__ void norm_rows_kernel(const float* X, const T* gain, int H, float eps
   ss = block_sum(ss, scratch);
   const float inv = rsqrtf(ss / (float)H + eps);
   OutT* y = Y + (size_t)blockIdx.x * H;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) y[k] = from_f32<OutT>(x[k] * inv * to_f32(gain[k]));
+  for (int k = threadIdx.x; k < H; k += blockDim.x) store_norm(y + k, x[k] * inv * to_f32(gain[k]), err);
 }
 
 // fp32 -> fp16 rows (tensor-core A operand)
-__global__ void to_half_kernel(const float* X, f16* Y, size_t n) {
+__global__ void to_half_kernel(const float* X, f16* Y, size_t n, int* err) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-    Y[i] = __float2half_rn(X[i]);
+    Y[i] = to_half_checked(X[i], err);
 }
 
 __global__ void swiglu_kernel(const float* G, const float* U, float* A, size_t n) {
@@ -57,7 +60,7 @@ __global__ void swiglu_kernel(const float* G, const float* U, float* A, size_t n
 // K, V rotated/copied into the cache at positions pos0 + t.
 template <typename KV>
 __global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, int pos0, int cap,
-                               const float2* rope, float* Q, KV* kc, KV* vc) {
+                               const float2* rope, float* Q, KV* kc, KV* vc, int* err) {
   const int t = blockIdx.x;
   const int half = hd / 2;
   const int width = (nq + 2 * nkv) * hd;
@@ -74,13 +77,13 @@ __global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, 
         Q[(size_t)t * nq * hd + head * hd + i + half] = rb;
       } else {
         KV* dst = kc + ((size_t)(head - nq) * cap + pos) * hd;
-        dst[i] = from_f32<KV>(ra);
-        dst[i + half] = from_f32<KV>(rb);
+        store_kv(dst + i, ra, err);
+        store_kv(dst + i + half, rb, err);
       }
     } else {
       KV* dst = vc + ((size_t)(head - nq - nkv) * cap + pos) * hd;
-      dst[i] = from_f32<KV>(a);
-      dst[i + half] = from_f32<KV>(b);
+      store_kv(dst + i, a, err);
+      store_kv(dst + i + half, b, err);
     }
   }
 }
@@ -292,15 +295,15 @@ static cudaError_t prefill_simt(const Dims& d, const LayerPtrs* layers, const vo
     const LayerPtrs& w = layers[l];
     KV* kc = (KV*)kcache + (size_t)l * 2 * layer_stride;
     KV* vc = kc + layer_stride;
-    norm_rows_kernel<W, float><<<T_, 256, 0, s>>>(b.X, (const W*)w.in_norm, H, d.eps, b.Xn);
+    norm_rows_kernel<W, float><<<T_, 256, 0, s>>>(b.X, (const W*)w.in_norm, H, d.eps, b.Xn, err);
     gemm_simt<W>(b.Xn, H, w.wq, H, w.bq, b.Y, Wd, T_, qd, H, false, s);
     gemm_simt<W>(b.Xn, H, w.wk, H, w.bk, b.Y + qd, Wd, T_, kvd, H, false, s);
     gemm_simt<W>(b.Xn, H, w.wv, H, w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, s);
-    rope_kv_kernel<KV><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc);
+    rope_kv_kernel<KV><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err);
     cudaError_t e = attn_prefill<KV>(d, b.Q, T_, pos0, kc, vc, b.O, s);
     if (e) return e;
     gemm_simt<W>(b.O, qd, w.wo, qd, nullptr, b.X, H, T_, H, qd, true, s);
-    norm_rows_kernel<W, float><<<T_, 256, 0, s>>>(b.X, (const W*)w.post_norm, H, d.eps, b.Xn);
+    norm_rows_kernel<W, float><<<T_, 256, 0, s>>>(b.X, (const W*)w.post_norm, H, d.eps, b.Xn, err);
     gemm_simt<W>(b.Xn, H, w.w_gate, H, nullptr, b.G, d.I, T_, d.I, H, false, s);
     gemm_simt<W>(b.Xn, H, w.w_up, H, nullptr, b.U, d.I, T_, d.I, H, false, s);
     const size_t n = (size_t)T_ * d.I;
@@ -534,20 +537,20 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
     const LayerPtrs& w = layers[l];
     f16* kc = (f16*)kcache + (size_t)l * 2 * layer_stride;
     f16* vc = kc + layer_stride;
-    norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.in_norm, H, d.eps, b.Xh);
+    norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.in_norm, H, d.eps, b.Xh, err);
     if ((e = gemm_tc(b.Xh, H, (const f16*)w.wq16, H, (const bf16*)w.bq, b.Y, Wd, T_, qd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
     if ((e = gemm_tc(b.Xh, H, (const f16*)w.wk16, H, (const bf16*)w.bk, b.Y + qd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
     if ((e = gemm_tc(b.Xh, H, (const f16*)w.wv16, H, (const bf16*)w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-    rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc);
+    rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err);
     const bool mma = !simt_attention() && attn_prefill_mma(d, b.Q, T_, pos0, kc, vc, b.Oh, s, &e);
     if (mma && e) return e;
     if (!mma) {
       if ((e = attn_prefill<f16>(d, b.Q, T_, pos0, kc, vc, b.O, s))) return e;
       const size_t no = (size_t)T_ * qd;
-      to_half_kernel<<<(unsigned)((no + 255) / 256 < 4096 ? (no + 255) / 256 : 4096), 256, 0, s>>>(b.O, b.Oh, no);
+      to_half_kernel<<<(unsigned)((no + 255) / 256 < 4096 ? (no + 255) / 256 : 4096), 256, 0, s>>>(b.O, b.Oh, no, err);
     }
     if ((e = gemm_tc(b.Oh, qd, (const f16*)w.wo16, qd, nullptr, b.X, H, T_, H, qd, true, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-    norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.post_norm, H, d.eps, b.Xh);
+    norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.post_norm, H, d.eps, b.Xh, err);
     if ((e = gemm_tc_swiglu(b.Xh, H, (const f16*)w.wg16, (const f16*)w.wu16, H, b.Ah, d.I, T_, d.I, H, err, s, b.ws,
                               b.ws_floats, d.nsm)))
       return e;
@@ -566,13 +569,12 @@ cudaError_t prefill_layers(const Dims& d, const LayerPtrs* layers, const void* e
   return prefill_simt<float, float>(d, layers, embed, ids_dev, T, pos0, rope, kcache_seq, b, err, s);
 }
 
-// bf16 -> fp16 weight copy (exact for |x| >= 2^-24 * 2^8 and below 65504); flags overflow
+// bf16 -> fp16 weight copy. A bf16 value has 8 significant bits, so the copy is exact for
+// 2^-17 <= |x| <= 65504; smaller magnitudes land among the fp16 subnormals and round to a
+// multiple of 2^-24 (an absolute error below 2^-25), larger ones set ERR_RANGE.
 __global__ void bf16_to_half_kernel(const bf16* src, f16* dst, size_t n, int* err) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const float v = __bfloat162float(src[i]);
-    if (fabsf(v) > 65504.f) atomicOr(err, ERR_NONFINITE);
-    dst[i] = __float2half_rn(v);
-  }
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = to_half_checked(__bfloat162float(src[i]), err);
 }
 
 cudaError_t convert_bf16_to_half(const void* src, void* dst, size_t n, int* err, cudaStream_t s) {

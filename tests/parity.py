@@ -60,16 +60,33 @@ def run_teacher_forced(model, shape, prompt, ref_toks, ref_logits, seq=0):
     return rep
 
 
+_weight_cache = {}
 _oracle_cache = {}
 
+# (test, steps compared, near-tie steps, max |dz| / std) of every parity run, printed in the
+# session summary (tests/conftest.py)
+REPORTS = []
 
-def oracle_run(shape_name, prompt_len, n_new, seed_prompt=1, layers=None):
+
+def record(name, rep: StepReport):
+    REPORTS.append((name, rep.steps, rep.near_ties, rep.max_rel if rep.max_rel else rep.max_err))
+
+
+def shape_weights(shape_name):
+    """(float32 weights, float64 oracle model) of a shape, drawn once per session."""
+    if shape_name not in _weight_cache:
+        s = SHAPES[shape_name]
+        w = make_weights(s)
+        _weight_cache[shape_name] = (w, oracle.OracleModel(oracle.OracleConfig.from_shape(s), w))
+    return _weight_cache[shape_name]
+
+
+def oracle_run(shape_name, prompt_len, n_new, seed_prompt=1):
     key = (shape_name, prompt_len, n_new, seed_prompt)
     if key not in _oracle_cache:
         s = SHAPES[shape_name]
-        w = make_weights(s)
+        w, om = shape_weights(shape_name)
         prompt = make_prompt(s, prompt_len, seed=seed_prompt)
-        om = oracle.OracleModel(oracle.OracleConfig.from_shape(s), w)
         toks, logits = oracle.generate(om, prompt, n_new)
         _oracle_cache[key] = (w, prompt, toks, logits)
     return _oracle_cache[key]

@@ -117,3 +117,29 @@ def test_valid_config_without_gpu_fails_loudly(L):
     w, _keep = _weights()
     st, msg = _create(L, _cfg(), w)
     assert st == 5, msg  # QW_ERR_CUDA: no silent CPU path
+
+
+def test_fault_injection_at_create_then_the_library_still_works(L, monkeypatch):
+    """QW_FAULT=alloc makes qw_create fail with QW_ERR_FAULT_INJECTED after validation and
+    before any device work; without it the same call proceeds normally again."""
+    w, _keep = _weights()
+    monkeypatch.setenv("QW_FAULT", "alloc")
+    st, msg = _create(L, _cfg(), w)
+    assert st == 7 and "QW_FAULT" in msg
+    st, msg = _create(L, _cfg(hidden=0), w)  # validation still comes first
+    assert st == 1
+    monkeypatch.delenv("QW_FAULT")
+    st, msg = _create(L, _cfg(), w)
+    assert st != 7
+    if st == 0:
+        pytest.skip("a GPU is present: the model was created")
+    assert st == 5  # no GPU here: QW_ERR_CUDA
+
+
+def test_last_error_is_cleared_by_the_next_call(L):
+    assert L.qw_reset(None, 0) == 1
+    assert L.qw_last_error().decode()
+    assert L.qw_op_decode_attention_workspace(12, 2, 128, 64) > 0  # (sets no error)
+    assert L.qw_position(None, 0, None) == 1
+    msg = L.qw_last_error().decode()
+    assert msg and "null" in msg

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle
-from parity import StepReport, check_step
+from parity import StepReport, check_step, record, shape_weights
 from synth import SHAPES, WORKLOADS, make_batch_prompts, make_weights
 
 pytestmark = pytest.mark.gpu
@@ -44,12 +44,13 @@ def test_batched_sequences_match_oracle(shape_name):
         m.close()
 
 
-def _run_batch(s, w, prompts, n_new, cap, check_seqs, reset_at=None, reset_seq=None):
+def _run_batch(s, w, prompts, n_new, cap, check_seqs, reset_at=None, reset_seq=None, om=None):
     """Prefill every prompt into its own sequence slot, then decode all slots together,
     feeding the oracle's tokens to the sequences in check_seqs (compared every step) and
     the device's own tokens to the others."""
     from qwen2_decoder_forward_decode_gb300 import DeviceWeights, Model
-    om = oracle.OracleModel(oracle.OracleConfig.from_shape(s), w)
+    if om is None:
+        om = oracle.OracleModel(oracle.OracleConfig.from_shape(s), w)
     refs = {b: oracle.generate(om, prompts[b], n_new) for b in check_seqs}
     S = len(prompts)
     m = Model(s, DeviceWeights(w, 1), cap, max_seqs=S)
@@ -89,17 +90,37 @@ def test_batched_16_sequences_match_oracle():
     w = make_weights(s)
     prompts = make_batch_prompts(s, 16, 5, 60)
     rep = _run_batch(s, w, prompts, 5, 96, set(range(16)) - {9}, reset_at=3, reset_seq=9)
-    print(f"16 sequences: steps {rep.steps} max rel {rep.max_rel:.4f} near-ties {rep.near_ties}")
+    record("hd128 batched, 16 ragged sequences", rep)
 
 
-def test_batched_1p5b_shape_sampled():
-    """The Qwen2.5-1.5B shape with 8 sequences decoded together; two of them are compared
-    with the oracle at every step."""
+def test_batched_1p5b_workload():
+    """The batched workload at its own configuration: 16 sequences of the Qwen2.5-1.5B
+    shape with prompts of 256-2048 tokens (the workload's seeds), a 2304-position cache per
+    sequence, all 16 decoding together. Four of them (the longest and shortest prompts and
+    two others) follow the oracle's tokens and are compared at every one of 17 steps (the
+    prefill and 16 decode steps) at the chunk sizes the bench runs; the other twelve run
+    their own tokens."""
+    wl = WORKLOADS["1p5b_batch"]
+    s = SHAPES[wl.shape]
+    w, om = shape_weights(wl.shape)
+    prompts = make_batch_prompts(s, wl.n_seqs, *wl.batch_len_range)
+    lens = [len(p) for p in prompts]
+    longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
+    check = {longest, shortest} | {b for b in (3, 11) if b not in (longest, shortest)}
+    assert len(check) >= 4
+    rep = _run_batch(s, w, prompts, 17, wl.kv_capacity, check, om=om)
+    assert rep.steps == 17 * len(check)
+    record(f"1p5b batched, 16 sequences ({min(lens)}-{max(lens)} tokens), {len(check)} compared", rep)
+
+
+def test_batched_1p5b_shape_small_prompts():
+    """The Qwen2.5-1.5B shape with 8 short sequences decoded together; two of them are
+    compared with the oracle at every step."""
     s = SHAPES[WORKLOADS["1p5b_batch"].shape]
-    w = make_weights(s)
+    w, om = shape_weights("1p5b")
     prompts = make_batch_prompts(s, 8, 8, 40)
-    rep = _run_batch(s, w, prompts, 4, 64, {0, 5})
-    print(f"1p5b batched: steps {rep.steps} max rel {rep.max_rel:.4f} near-ties {rep.near_ties}")
+    rep = _run_batch(s, w, prompts, 4, 64, {0, 5}, om=om)
+    record("1p5b batched, 8 short sequences", rep)
 
 
 @pytest.mark.parametrize("env", [{"QW_BATCHED_ATTN_MMA": "0"}, {"QW_BATCHED_SPLITS": "1"}])

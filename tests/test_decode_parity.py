@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
-from parity import check_step, oracle_run, run_teacher_forced, StepReport
+from parity import check_step, oracle_run, record, run_teacher_forced, StepReport
 from synth import SHAPES, WORKLOADS, make_prompt, make_weights
 
 pytestmark = pytest.mark.gpu
@@ -84,31 +84,36 @@ def test_0p5b_workload_full():
     m = _model(wl.shape, w, wl.kv_capacity)
     try:
         rep = run_teacher_forced(m, SHAPES[wl.shape], prompt, toks, logits)
-        print(f"0p5b: steps {rep.steps} max|dz| {rep.max_err:.4f} max rel {rep.max_rel:.4f} "
-              f"near-ties {rep.near_ties}")
+        assert rep.steps == wl.new_tokens
+        record("0p5b 32-token prompt, 32 tokens", rep)
     finally:
         m.close()
 
 
-def test_1p5b_workload_sampled():
+def test_1p5b_workload_full():
+    """The Qwen2.5-1.5B workload as the bench runs it: 128-token prompt, cache 2048, every
+    one of the 100 tokens compared under teacher forcing."""
     wl = WORKLOADS["1p5b"]
-    w, prompt, toks, logits = oracle_run(wl.shape, wl.prompt_len, 6)
+    w, prompt, toks, logits = oracle_run(wl.shape, wl.prompt_len, wl.new_tokens)
     m = _model(wl.shape, w, wl.kv_capacity)
     try:
         rep = run_teacher_forced(m, SHAPES[wl.shape], prompt, toks, logits)
-        print(f"1p5b: steps {rep.steps} max|dz| {rep.max_err:.4f} max rel {rep.max_rel:.4f} "
-              f"near-ties {rep.near_ties}")
+        assert rep.steps == wl.new_tokens
+        record("1p5b 128-token prompt, 100 tokens", rep)
     finally:
         m.close()
 
 
-def test_1p5b_long_context_sampled():
+def test_1p5b_long_context():
+    """The long-context workload: a 4096-token prompt (tensor-core prefill at full size)
+    into an 8192-position cache, then 32 of its 256 decode steps at 4096+ positions."""
     wl = WORKLOADS["1p5b_long"]
-    w, prompt, toks, logits = oracle_run(wl.shape, wl.prompt_len, 3)
+    w, prompt, toks, logits = oracle_run(wl.shape, wl.prompt_len, 33)
     m = _model(wl.shape, w, wl.kv_capacity)
     try:
         rep = run_teacher_forced(m, SHAPES[wl.shape], prompt, toks, logits)
-        print(f"1p5b long: steps {rep.steps} max|dz| {rep.max_err:.4f} max rel {rep.max_rel:.4f}")
+        assert rep.steps == 33
+        record("1p5b 4096-token prompt, 33 tokens", rep)
     finally:
         m.close()
 
@@ -123,42 +128,6 @@ def test_cuda_core_decode_attention(monkeypatch):
         run_teacher_forced(m, SHAPES["hd128_bf16"], prompt, toks, logits)
     finally:
         m.close()
-
-
-# ---- persistent step kernel (one cooperative launch per decode step) ------------------
-
-@pytest.mark.parametrize("shape_name,P,n_new,cap,slot_kb", [
-    ("small_bf16", 100, 40, 160, None),
-    ("hd128_bf16", 150, 12, 200, None),
-    ("hd128_bf16", 150, 12, 200, "4"),   # 4 KB slots: each 4.5 KB down row split over two units
-])
-def test_step_kernel_small_shapes(monkeypatch, shape_name, P, n_new, cap, slot_kb):
-    monkeypatch.setenv("QW_STEP_KERNEL", "1")
-    if slot_kb:
-        monkeypatch.setenv("QW_STEP_SLOT_KB", slot_kb)
-    w, prompt, toks, logits = oracle_run(shape_name, P, n_new)
-    m = _model(shape_name, w, cap)
-    try:
-        rep = run_teacher_forced(m, SHAPES[shape_name], prompt, toks, logits)
-        assert rep.steps == n_new
-    finally:
-        m.close()
-
-
-@pytest.mark.parametrize("slot_kb", [None, "12"])  # 6 ring slots (fewer than consumer warps), 14
-def test_step_kernel_workloads(monkeypatch, slot_kb):
-    monkeypatch.setenv("QW_STEP_KERNEL", "1")
-    if slot_kb:
-        monkeypatch.setenv("QW_STEP_SLOT_KB", slot_kb)
-    for name, n in (("0p5b", None), ("1p5b", 6)):
-        wl = WORKLOADS[name]
-        w, prompt, toks, logits = oracle_run(wl.shape, wl.prompt_len, n or wl.new_tokens)
-        m = _model(wl.shape, w, wl.kv_capacity)
-        try:
-            rep = run_teacher_forced(m, SHAPES[wl.shape], prompt, toks, logits)
-            print(f"step kernel {name} slot {slot_kb}: steps {rep.steps} max|dz| {rep.max_err:.4f}")
-        finally:
-            m.close()
 
 
 # ---- edge cases ----------------------------------------------------------------------
@@ -264,5 +233,74 @@ def test_decode_is_deterministic():
         zb = m.logits()
         assert a == b
         np.testing.assert_array_equal(za, zb)
+    finally:
+        m.close()
+
+
+def test_fault_injection_at_decode_leaves_the_model_usable(monkeypatch):
+    """QW_FAULT=launch fails a decode call with QW_ERR_FAULT_INJECTED before any launch;
+    the sequence keeps its length and the next call continues it exactly."""
+    from qwen2_decoder_forward_decode_gb300 import QwError
+    w, prompt, toks, logits = oracle_run("tiny", 8, 8)
+    m = _model("tiny", w, 16)
+    try:
+        m.prefill(prompt)
+        monkeypatch.setenv("QW_FAULT", "launch")
+        with pytest.raises(QwError) as e:
+            m.decode_step(feed=[toks[0]])
+        assert e.value.status == 7
+        assert m.position() == len(prompt)
+        monkeypatch.delenv("QW_FAULT")
+        rep = StepReport()
+        t = int(m.decode_step(feed=[toks[0]])[0])
+        check_step(SHAPES["tiny"], m.logits(), t, logits[1], toks[1], rep, "after the injected fault")
+    finally:
+        m.close()
+
+
+def test_reset_clears_the_last_error():
+    from qwen2_decoder_forward_decode_gb300 import QwError, lib
+    w, prompt, _, _ = oracle_run("tiny", 8, 8)
+    m = _model("tiny", w, 16)
+    try:
+        m.prefill(prompt)
+        with pytest.raises(QwError):
+            m.decode_step(feed=[-5])
+        assert lib().qw_last_error().decode()
+        m.reset(0)
+        assert lib().qw_last_error().decode() == ""
+        assert m.position() == 0
+    finally:
+        m.close()
+
+
+def _overflowing_weights(shape_name):
+    """The shape's weights with layer 0's value bias at 70144 (a bf16 value above the fp16
+    maximum 65504): every value written to the fp16 KV cache of layer 0 overflows."""
+    from synth import round_to_bf16
+    s = SHAPES[shape_name]
+    w = dict(make_weights(s))
+    b = np.full(s.n_kv_heads * s.head_dim, 70000.0, dtype=np.float32)
+    w["model.layers.0.self_attn.v_proj.bias"] = round_to_bf16(b)
+    assert float(w["model.layers.0.self_attn.v_proj.bias"][0]) == 70144.0
+    return s, w
+
+
+@pytest.mark.parametrize("max_seqs", [1, 2])
+def test_fp16_overflow_is_reported(max_seqs):
+    """A value beyond the fp16 range written to the KV cache is an error (QW_ERR_NUMERIC),
+    reported by the prefill and by decode steps (single-sequence and batched), never a
+    silent infinity."""
+    from qwen2_decoder_forward_decode_gb300 import QwError
+    s, w = _overflowing_weights("small_bf16")
+    m = _model("small_bf16", w, 64, max_seqs=max_seqs)
+    try:
+        for b in range(max_seqs):
+            with pytest.raises(QwError) as e:
+                m.prefill(make_prompt(s, 10 + b), seq=b)
+            assert e.value.status == 8
+        with pytest.raises(QwError) as e:
+            m.decode_step(feed=np.ones(max_seqs, dtype=np.int32))
+        assert e.value.status == 8
     finally:
         m.close()

@@ -262,6 +262,49 @@ def test_eos_is_appended_then_stops():
     assert t2 == t[:t.index(t[2]) + 1]
 
 
+# --- greedy choice ------------------------------------------------------------------------
+# "augur", Features (greedy generation) and the argmax of the "LLM Speedrun: Architecture"
+# model code: the largest logit wins; among equal maxima the lowest index (numpy's rule).
+
+def test_greedy_takes_the_lowest_index_of_a_tie():
+    assert oracle.greedy(np.array([1.0, 3.0, 3.0])) == 1
+    assert oracle.greedy(np.array([3.0, 1.0, 3.0])) == 0
+    assert oracle.greedy(np.array([-2.0, -1.0, -1.0, -5.0])) == 1
+
+
+def test_greedy_ties_far_apart_and_at_the_end_of_a_full_vocabulary():
+    V = 151936
+    z = np.zeros(V)
+    z[V - 2] = z[V - 1] = 1.0
+    assert oracle.greedy(z) == V - 2
+    z = np.full(V, -1.0)
+    z[100000] = z[5] = 2.0
+    assert oracle.greedy(z) == 5
+    z = np.zeros(V)
+    z[V - 1] = 1e-300  # a strictly larger last element still wins
+    assert oracle.greedy(z) == V - 1
+
+
+def test_greedy_agrees_with_a_scan_over_planted_ties():
+    rng = np.random.default_rng(7)
+    for _ in range(200):
+        n = int(rng.integers(1, 64))
+        z = rng.integers(-3, 4, n).astype(np.float64)  # many equal values
+        best = 0
+        for i in range(1, n):  # the first strictly larger value moves the choice
+            if z[i] > z[best]:
+                best = i
+        assert oracle.greedy(z) == best
+
+
+@pytest.mark.parametrize("bad", [np.nan, np.inf, -np.inf])
+def test_greedy_rejects_non_finite_logits(bad):
+    z = np.zeros(10)
+    z[3] = bad
+    with pytest.raises(FloatingPointError):
+        oracle.greedy(z)
+
+
 # --- optional weights: a separate LM head, no q/k/v bias ---------------------------------
 
 def test_untied_head_copy_of_embedding_matches_tied():
