@@ -167,7 +167,7 @@ struct qw_model {
       // the o_proj GEMV merges the attention partials into its input vector (up to 2048
       // attention outputs), else reads the output the attention kernel merged
       if ((e = run(2, l, [&](bool p) {
-             return merge_in_oproj ? launch_oproj(d, w.wo, (const float*)attn_ws, pos + s, xs, err, tl(), stream, p)
+             return merge_in_oproj ? launch_oproj(d, w.wo, (const float*)attn_ws, pos + s, xs, err, tl(), stream, p, &w)
                                    : launch_resid(d, w.wo, d.H, d.nq * d.hd, attn, xs, err, tl(), stream, p);
            })))
         return e;

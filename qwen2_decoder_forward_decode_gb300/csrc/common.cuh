@@ -214,6 +214,14 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, const void* row_a
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// The barrier's current phase counts one arrival when every cp.async this thread issued
+// so far has landed (the barrier's expected count includes that arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 
 // Ask L2 to fetch bytes (multiple of 16) at src (16-byte aligned); no completion tracking.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {

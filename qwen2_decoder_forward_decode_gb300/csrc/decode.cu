@@ -452,9 +452,22 @@ struct OpLMHead {
 // The first NS items are requested before griddepcontrol.wait, and a CTA stays under half
 // an SM, so under programmatic dependent launch the next kernel's weights are in flight
 // while this one finishes. Partial sums over K segments add in a fixed order.
+// Regions of a later kernel's weights that every CTA asks L2 to fetch before its dependency
+// wait (the HBM stream then keeps running while this kernel waits and computes). Each region
+// is cut into pieces of `piece` bytes; CTA b requests pieces b, b + grid, ... in address
+// order, interleaving the regions, so data arrives roughly in the order it is consumed.
+struct L2Ahead {
+  const char* ptr[3];
+  unsigned long long bytes[3];
+  int n;
+  unsigned piece;
+};
+
 struct GemvCfg {
   int KS, NS, slot_bytes, x_direct, pf_dist;
   int prewait_bytes;  // per warp: weight bytes beyond the ring prefetched into L2 before the wait
+  int cpasync;        // 1: every lane fills the ring with 16-byte cp.async (else lane 0, bulk copies)
+  L2Ahead ahead;
   int* err;
   unsigned long long* tl;  // timeline slots or null
 };
@@ -496,6 +509,20 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
       if (r1) prefetch_l2_bulk(reinterpret_cast<const unsigned char*>(r1) + (size_t)v0 * 16, seg_bytes);
     }
   };
+  auto issue_cp = [&](int k) {  // every lane: its 16-byte vectors of item k's row segments
+    const int slot = k % NS;
+    const int item = first + k * step;
+    const unsigned char* r0 = reinterpret_cast<const unsigned char*>(op.row(item, 0)) + (size_t)v0 * 16;
+    const T* r1t = Op::RPI == 2 ? op.row(item, 1) : nullptr;
+    const uint32_t dst = wslot0 + slot * c.slot_bytes;
+    const int nv = (int)(seg_bytes >> 4);
+    for (int v = lane; v < nv; v += 32) cp_async16_s(dst + 16 * v, r0 + 16 * v);
+    if (r1t) {
+      const unsigned char* r1 = reinterpret_cast<const unsigned char*>(r1t) + (size_t)v0 * 16;
+      for (int v = lane; v < nv; v += 32) cp_async16_s(dst + seg_bytes + 16 * v, r1 + 16 * v);
+    }
+    cp_async_arrive_noinc(bar0 + 8 * slot);
+  };
   auto issue = [&](int k) {  // lane 0: copy this warp's K segment of item k's rows
     const int slot = k % NS;
     const int item = first + k * step;
@@ -511,18 +538,40 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
   };
 
   tl_stamp(c.tl, 0);
+  const int n0 = min(NS, my_items);  // weights do not depend on upstream kernels
+  if (c.cpasync) {
+    if (lane == 0) {
+      s_abort[warp] = 0;
+      for (int sl = 0; sl < NS; ++sl) mbar_init(bar0 + 8 * sl, 32);  // one arrival per lane
+      mbar_fence_init();
+    }
+    __syncwarp();
+    for (int k = 0; k < n0; ++k) issue_cp(k);
+  }
   if (lane == 0) {
-    s_abort[warp] = 0;
-    for (int sl = 0; sl < NS; ++sl) mbar_init(bar0 + 8 * sl, 1);
-    mbar_fence_init();
-    const int n0 = min(NS, my_items);  // weights do not depend on upstream kernels
-    for (int k = 0; k < n0; ++k) issue(k);
+    if (!c.cpasync) {
+      s_abort[warp] = 0;
+      for (int sl = 0; sl < NS; ++sl) mbar_init(bar0 + 8 * sl, 1);
+      mbar_fence_init();
+      for (int k = 0; k < n0; ++k) issue(k);
+    }
     // and while the upstream kernels finish, the next items stream into L2
     const uint32_t item_bytes = seg_bytes * (uint32_t)Op::RPI;
     int n_pf = c.pf_dist;
     if (Op::L2_PREWAIT && item_bytes && c.prewait_bytes > 0 && (int)(c.prewait_bytes / item_bytes) > n_pf)
       n_pf = (int)(c.prewait_bytes / item_bytes);
     for (int k = n0; k < min(NS + n_pf, my_items); ++k) prefetch(k);
+    if (warp == GEMV_WARPS - 1 && c.ahead.n) {  // a later kernel's weights, into L2
+      const unsigned long long np = (c.ahead.bytes[0] + c.ahead.piece - 1) / c.ahead.piece;
+      for (unsigned long long j = blockIdx.x; j < np; j += gridDim.x)
+        for (int r = 0; r < c.ahead.n; ++r) {
+          const unsigned long long a = j * c.ahead.piece;
+          if (a >= c.ahead.bytes[r]) continue;
+          unsigned long long n = c.ahead.bytes[r] - a;
+          if (n > c.ahead.piece) n = c.ahead.piece;
+          prefetch_l2_bulk(c.ahead.ptr[r] + a, (uint32_t)(n & ~15ull));
+        }
+    }
   }
   // inputs of the epilogue that do not depend on upstream kernels (first two items)
   op.pre();
@@ -568,7 +617,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
   }
 
   bool timed_out = false;
-  int issued = min(NS, my_items), consumed = 0;
+  int issued = n0, consumed = 0;
   // K split over KS warps with at most MAX_DEFER items per warp: every warp streams its
   // own segments without waiting for the others, parks its partial sums in shared memory,
   // and the KS partials of each item are added (in warp order) once, after the loop.
@@ -594,9 +643,13 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
         }
       }
       __syncwarp();
-      if (lane == 0 && k + NS < my_items) {  // slot free: request item k + NS
-        fence_proxy_async();
-        issue(k + NS);
+      if (k + NS < my_items) {  // slot free: request item k + NS
+        if (c.cpasync) {
+          issue_cp(k + NS);
+        } else if (lane == 0) {
+          fence_proxy_async();
+          issue(k + NS);
+        }
         ++issued;
       }
       a0 = warp_sum(a0);
@@ -644,11 +697,15 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
       }
     }
     __syncwarp();
-    if (lane == 0 && k + NS < my_items) {  // slot free: request item k + NS
-      fence_proxy_async();
-      issue(k + NS);
+    if (k + NS < my_items) {  // slot free: request item k + NS
+      if (c.cpasync) {
+        issue_cp(k + NS);
+      } else if (lane == 0) {
+        fence_proxy_async();
+        issue(k + NS);
+      }
       ++issued;
-      if (c.pf_dist && k + NS + c.pf_dist < my_items) prefetch(k + NS + c.pf_dist);
+      if (lane == 0 && c.pf_dist && k + NS + c.pf_dist < my_items) prefetch(k + NS + c.pf_dist);
     }
     a0 = warp_sum(a0);
     if (Op::RPI == 2) a1 = warp_sum(a1);
@@ -675,6 +732,7 @@ gemv_kernel(const Op op_in, const GemvCfg c) {
     for (int j = consumed; j < issued; ++j)  // copies in flight must land before exit
       mbar_wait_bounded(bar0 + 8 * (j % NS), (uint32_t)((j / NS) & 1));
   }
+  if (c.cpasync) asm volatile("cp.async.wait_all;" ::: "memory");  // (nothing left unless a wait gave up)
   op.finish();
   tl_stamp(c.tl, 2);
 }
@@ -707,6 +765,21 @@ static int pf_dist() {
 static int prewait_bytes() {
   static const int b = env_int("QW_GEMV_PREWAIT_KB", 0) * 1024;
   return b;
+}
+// ring fill: 1 = per-lane cp.async, 0 = bulk copies issued by lane 0
+static int gemv_cpasync() {
+  static const int v = env_int("QW_GEMV_CPASYNC", 0);
+  return v;
+}
+// which later weights are requested into L2 ahead of use (bit 0: the o_proj kernel asks for
+// gate/up, bit 1: the o_proj kernel asks for down, bit 2: the gate/up kernel asks for down)
+int l2_ahead_mask() {
+  static const int v = env_int("QW_L2_AHEAD", 0);
+  return v;
+}
+static unsigned l2_ahead_piece() {
+  static const unsigned v = (unsigned)env_int("QW_L2_AHEAD_PIECE_KB", 32) * 1024u;
+  return v;
 }
 
 static int maxv_for(int nvec, int KS) {
@@ -746,6 +819,8 @@ static bool plan_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, G
   p->c.x_direct = x_direct;
   p->c.pf_dist = pf_dist();
   p->c.prewait_bytes = prewait_bytes();
+  p->c.cpasync = gemv_cpasync();
+  p->c.ahead = L2Ahead{};
   p->c.err = err;
   p->c.tl = tl;
   p->maxv = maxv_for(nvec, KS);
@@ -756,9 +831,11 @@ static bool plan_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, G
 }
 
 template <typename T, class Op>
-static cudaError_t run_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, cudaStream_t s, bool pdl) {
+static cudaError_t run_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, cudaStream_t s, bool pdl,
+                            const L2Ahead* ahead = nullptr) {
   GemvPlan p;
   if (!plan_gemv<T, Op>(op, nsm, err, tl, &p)) return cudaErrorInvalidValue;
+  if (ahead) p.c.ahead = *ahead;
   const dim3 g(p.grid), b(GEMV_WARPS * 32);
   switch (p.maxv) {
     case 1: return launch_k(gemv_kernel<T, 1, Op>, g, b, p.smem, s, pdl, op, p.c);
@@ -880,20 +957,35 @@ cudaError_t launch_resid(const Dims& d, const void* W, int N, int K, const float
                       : resid_t<float>(d, W, N, K, in, y, err, tl, s, pdl);
 }
 
+// L2 requests of a layer's MLP weights (mask bits as l2_ahead_mask: 1 gate and up, 2 down)
+static L2Ahead mlp_ahead(const Dims& d, const LayerPtrs* w, int bits) {
+  L2Ahead a{};
+  a.piece = l2_ahead_piece();
+  if (!w) return a;
+  const unsigned long long mat = (unsigned long long)d.I * d.H * (d.dtype == 1 ? 2 : 4);
+  if (bits & 1) {
+    a.ptr[a.n] = (const char*)w->w_gate; a.bytes[a.n++] = mat;
+    a.ptr[a.n] = (const char*)w->w_up; a.bytes[a.n++] = mat;
+  }
+  if (bits & 2) { a.ptr[a.n] = (const char*)w->w_down; a.bytes[a.n++] = mat; }
+  return a;
+}
+
 template <typename T>
 static cudaError_t oproj_t(const Dims& d, const void* W, const float* part, const int* d_pos, float* y, int* err,
-                          unsigned long long* tl, cudaStream_t s, bool pdl) {
+                          unsigned long long* tl, cudaStream_t s, bool pdl, const LayerPtrs* mlp) {
   if (d.nq * d.hd > 4 * OpOProj<T>::EPT4 * GEMV_WARPS * 32 || d.hd % 4) return cudaErrorInvalidValue;
   OpOProj<T> op{};
   op.K = d.nq * d.hd; op.N = d.H; op.n_items = (d.H + 1) / 2; op.W = (const T*)W;
   op.part = part; op.nq = d.nq; op.hd = d.hd; op.nsplit_max = d.attn_nsplit; op.chunk_min = d.attn_chunk_min;
   op.d_pos = d_pos; op.y = y;
-  return run_gemv<T>(op, d.nsm, err, tl, s, pdl);
+  const L2Ahead a = mlp_ahead(d, mlp, l2_ahead_mask() & 3);
+  return run_gemv<T>(op, d.nsm, err, tl, s, pdl, a.n ? &a : nullptr);
 }
 cudaError_t launch_oproj(const Dims& d, const void* W, const float* part, const int* d_pos, float* y, int* err,
-                         unsigned long long* tl, cudaStream_t s, bool pdl) {
-  return d.dtype == 1 ? oproj_t<bf16>(d, W, part, d_pos, y, err, tl, s, pdl)
-                      : oproj_t<float>(d, W, part, d_pos, y, err, tl, s, pdl);
+                         unsigned long long* tl, cudaStream_t s, bool pdl, const LayerPtrs* mlp) {
+  return d.dtype == 1 ? oproj_t<bf16>(d, W, part, d_pos, y, err, tl, s, pdl, mlp)
+                      : oproj_t<float>(d, W, part, d_pos, y, err, tl, s, pdl, mlp);
 }
 
 template <typename T>
@@ -902,7 +994,8 @@ static cudaError_t gateup_t(const Dims& d, const LayerPtrs& w, const float* x, f
   OpGateUp<T> op{};
   op.K = d.H; op.n_items = d.I; op.wg = (const T*)w.w_gate; op.wu = (const T*)w.w_up;
   op.gain = (const T*)w.post_norm; op.x = x; op.eps = d.eps; op.act = act;
-  return run_gemv<T>(op, d.nsm, err, tl, s, pdl);
+  const L2Ahead a = mlp_ahead(d, &w, (l2_ahead_mask() & 4) ? 2 : 0);
+  return run_gemv<T>(op, d.nsm, err, tl, s, pdl, a.n ? &a : nullptr);
 }
 cudaError_t launch_gateup(const Dims& d, const LayerPtrs& w, const float* x, float* act, int* err,
                           unsigned long long* tl, cudaStream_t s, bool pdl) {

@@ -84,9 +84,10 @@ cudaError_t launch_attn(int kv_dtype, int nq, int nkv, int hd, int nsplit, int c
                         size_t smem, const float* q, const void* kc, const void* vc,
                         int kv_stride, const int* d_pos, int ctx_host, float* out, void* ws,
                         unsigned long long* tl, cudaStream_t s, bool pdl, int merge = 1);
-// x += Wo . o with o merged from the attention partials in ws (attention run with merge 0)
+// x += Wo . o with o merged from the attention partials in ws (attention run with merge 0);
+// mlp (may be null): the layer whose MLP weights may be requested into L2 ahead of use
 cudaError_t launch_oproj(const Dims& d, const void* W, const float* part, const int* d_pos, float* y, int* err,
-                         unsigned long long* tl, cudaStream_t s, bool pdl);
+                         unsigned long long* tl, cudaStream_t s, bool pdl, const LayerPtrs* mlp = nullptr);
 // y[r] += W[r,:] . in  (r < N), W [N, K]
 cudaError_t launch_resid(const Dims& d, const void* W, int N, int K, const float* in, float* y,
                          int* err, unsigned long long* tl, cudaStream_t s, bool pdl);
