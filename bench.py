@@ -219,9 +219,37 @@ def prefill_launches(s, T, nsm=152):
     return 1 + s.n_layers * per_layer + 1
 
 
-def decode_launches_per_token(s):
-    """Kernels one decode step launches: embedding, 5 per layer and the LM head."""
-    return 5 * s.n_layers + 2
+def decode_launches_per_token(s, persistent=False):
+    """Kernels one decode step launches: the persistent decode-step kernel, or embedding,
+    5 per layer and the LM head."""
+    return 1 if persistent else 5 * s.n_layers + 2
+
+
+def timeline_persistent(m, s, ids_dev, prompt, rank):
+    """Device timeline of the persistent decode-step kernel: per phase kind, the time from
+    the phase's start to its units consumed, to its end, and the grid barrier after it."""
+    m.set_timeline(True)
+    m.prefill_device(ids_dev.data_ptr(), len(prompt))
+    kinds = ["qkv", "attn", "o_proj", "gate_up", "down"] * s.n_layers + ["lm_head"]
+    st = {k: {"units_us": [], "run_us": [], "barrier_us": []} for k in set(kinds)}
+    tot = []
+    for i in range(12):
+        m.decode_steps(1)
+        tl = m.read_timeline().astype(np.int64)[:len(kinds)]
+        if i < 2:
+            continue
+        tot.append((tl[-1, 2] - tl[0, 0]) / 1000.0)
+        for j, k in enumerate(kinds):
+            if k != "attn":
+                st[k]["units_us"].append((tl[j, 1] - tl[j, 0]) / 1000.0)
+            st[k]["run_us"].append((tl[j, 2] - tl[j, 0]) / 1000.0)
+            if j + 1 < len(kinds):
+                st[k]["barrier_us"].append((tl[j + 1, 0] - tl[j, 2]) / 1000.0)
+    m.set_timeline(False)
+    out = {"persistent_step_us": float(np.mean(tot)), "phases": {
+        k: {f: round(float(np.mean(x)), 3) if x else None for f, x in v.items()} for k, v in st.items()}}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
 
 
 def timeline_per_kernel(m, s, ids_dev, prompt, rank):
@@ -332,12 +360,29 @@ def run_native(args):
     m.set_trace(3, None, None)
     gu_ms = float(np.mean(kt))
     gu_bytes = gateup_bytes(s)
-    achieved = gu_bytes / (gu_ms / 1000.0) / 1e9
     src = source_hash()
-    traffic = recorded_traffic("gateup_gemv", src)
+    persistent = m.decode_kernels_per_step() == 1
+    if persistent:
+        # the dominant kernel is the decode-step kernel itself: one launch per token, timed
+        # with CUDA events on its stream around the timed decode loop
+        roofline = {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": bpt * value / ws / 1e9,
+                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": bpt * value / ws / 1e9 / peak,
+                    "traffic": recorded_traffic("decode_step_kernel", src), "algorithmic_bytes_per_launch": bpt,
+                    "launch_us": 1e6 * ws / value,
+                    "timing": "CUDA events on the decode stream around the timed decode loop (one launch per token)",
+                    "gateup_gemv_us_one_kernel_per_op": gu_ms * 1000.0}
+    else:
+        achieved = gu_bytes / (gu_ms / 1000.0) / 1e9
+        roofline = {"bound": "hbm", "kernel": "gateup_gemv", "achieved": achieved,
+                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": recorded_traffic("gateup_gemv", src),
+                    "algorithmic_bytes_per_launch": gu_bytes, "launch_us": gu_ms * 1000.0}
 
     if args.timeline:
-        timeline_per_kernel(m, s, ids_dev, prompt, rank)
+        if persistent:
+            timeline_persistent(m, s, ids_dev, prompt, rank)
+        else:
+            timeline_per_kernel(m, s, ids_dev, prompt, rank)
 
     if args.layers:
         # profiling run on a reduced stack: timed loop only, not a bench line
@@ -397,15 +442,13 @@ def run_native(args):
             "hbm_gbs": bpt * value / ws / 1e9,
             "decode_bytes_per_token": bpt,
             "decode_frac_of_hbm_peak": bpt * value / ws / 1e9 / peak,
-            "roofline": {"bound": "hbm", "kernel": "gateup_gemv", "achieved": achieved,
-                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": gu_bytes, "launch_us": gu_ms * 1000.0},
+            "roofline": roofline,
             "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4 * wl.prompt_len,
                     "d2h_bytes_per_step": 4 * wl.new_tokens + 4,
                     "how": "qw_generate with host buffers minus qw_prefill with host buffers, host wall clock",
                     "generate_ms": 1000 * float(np.mean(t_gen)), "ttft_ms": 1000 * float(np.mean(t_pref))},
-            "gpu_launches": args.steps * (prefill_launches(s, wl.prompt_len) + decode_launches_per_token(s) * n_dec),
+            "gpu_launches": args.steps * (prefill_launches(s, wl.prompt_len) +
+                                          decode_launches_per_token(s, persistent) * n_dec),
             "clocks": clk.summary(),
             "host_ms_per_step": 1000 * t_host / args.steps,
             "source_hash": src,

@@ -160,6 +160,12 @@ const int32_t *qw_tokens_device(const qw_model *m);
  * KV cache]. 0 for a sequence that is not active. Errors: QW_ERR_INVALID_ARG. */
 qw_status qw_position(const qw_model *m, int32_t seq, int32_t *pos);
 
+/* Kernel launches one single-sequence decode step makes: 1 when the step runs as one
+ * persistent kernel (bf16 models whose shape it supports, the default), else
+ * n_layers * 5 + 2 (embedding, q/k/v, attention, o_proj, gate/up, down per layer, LM head).
+ * 0 for a null model. */
+int32_t qw_decode_kernels_per_step(const qw_model *m);
+
 /* Forget sequence seq [LSA KVCache: a fresh cache per sequence; AUG Features:
  * preallocated KV cache]: its length becomes 0 and it leaves the set of active sequences;
  * its cache rows are overwritten by its next prefill. Does not synchronise. Errors:
@@ -180,7 +186,12 @@ qw_status qw_set_trace(qw_model *m, int32_t kind, void *const *begin, void *cons
  * its wait for the previous kernel, and the last CTA's end. qw_read_timeline copies the
  * stamps of the last step, 3 per launch in launch order, into out (host, 3 * max_launches
  * uint64) and the launch count into n_launches. Timing differs slightly from an
- * uninstrumented run (one atomic per CTA per stamp). enable 0 frees the buffer. */
+ * uninstrumented run (one atomic per CTA per stamp). enable 0 frees the buffer.
+ * When a single-sequence step runs as one persistent kernel (qw_decode_kernels_per_step
+ * is 1), entry k < 5 * n_layers + 1 is phase k of the step instead (q/k/v, attention,
+ * o_proj, gate/up, down per layer, then the LM head): [start after the previous grid
+ * barrier, its weight units consumed, end before the next grid barrier], stamped by the
+ * first CTA. */
 qw_status qw_set_timeline(qw_model *m, int32_t enable);
 qw_status qw_read_timeline(qw_model *m, uint64_t *out, int32_t max_launches, int32_t *n_launches);
 

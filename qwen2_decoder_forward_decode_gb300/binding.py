@@ -74,6 +74,7 @@ def lib():
         "qw_logits": ([VP], VP),
         "qw_read_logits": ([VP, I32, P(ctypes.c_float)], I32),
         "qw_tokens_device": ([VP], VP),
+        "qw_decode_kernels_per_step": ([VP], I32),
         "qw_position": ([VP, I32, pi], I32),
         "qw_reset": ([VP, I32], I32),
         "qw_last_error": ([], ctypes.c_char_p),
@@ -98,7 +99,8 @@ def lib():
 def exported_symbols():
     return ["qw_create", "qw_destroy", "qw_prefill", "qw_prefill_device", "qw_decode_step",
             "qw_decode_steps", "qw_generate", "qw_sync", "qw_logits", "qw_read_logits",
-            "qw_tokens_device", "qw_position", "qw_reset", "qw_last_error", "qw_set_trace",
+            "qw_tokens_device", "qw_decode_kernels_per_step", "qw_position", "qw_reset",
+            "qw_last_error", "qw_set_trace",
             "qw_set_timeline", "qw_read_timeline",
             "qw_op_decode_attention_workspace", "qw_op_decode_attention",
             "qw_op_decode_attention_noalloc", "qw_op_decode_attention_noalloc_limit", "qw_op_gemm_f16",
@@ -230,6 +232,10 @@ class Model:
 
     def tokens_ptr(self):
         return lib().qw_tokens_device(self.h)
+
+    def decode_kernels_per_step(self):
+        """1 when a single-sequence decode step runs as one persistent kernel."""
+        return int(lib().qw_decode_kernels_per_step(self.h))
 
     def position(self, seq=0):
         p = np.zeros(1, dtype=np.int32)

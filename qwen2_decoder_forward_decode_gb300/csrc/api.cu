@@ -82,6 +82,12 @@ struct qw_model {
   bool attn_mma = false;        // decode attention on the tensor cores (fp16 cache)
   int trace_kind = -1;
   std::vector<cudaEvent_t> trace_begin, trace_end;
+  // one persistent kernel per decode step of one sequence (bf16 models)
+  bool use_mega = false;
+  void* mega_layers = nullptr;       // device layer records
+  float* mega_part = nullptr;        // attention chunk partials
+  unsigned long long* mega_bar = nullptr;  // [0] barrier counter, [1] its value at a step start
+  int* mega_abort = nullptr;
   // batched decode (bf16 models with the fp16 matrix copies, several sequences)
   bool use_batched = false;
   std::vector<BatchedLayerPlans> bplans;
@@ -186,7 +192,37 @@ struct qw_model {
     if (bgraph) { cudaGraphExecDestroy(bgraph); bgraph = nullptr; }
   }
 
+  cudaError_t run_mega(int s) {
+    MegaLaunch a{};
+    a.d = d;
+    a.layers_dev = mega_layers;
+    a.embed = embed;
+    a.final_norm = final_norm;
+    a.head = head_w();
+    a.rope = rope;
+    a.kv_seq = kv_seq(s);
+    a.x = x + (size_t)s * d.H;
+    a.q = q;
+    a.act = act;
+    a.logits = logits + (size_t)s * d.V;
+    a.part = mega_part;
+    a.tok = tok + s;
+    a.pos = pos + s;
+    a.key = keys + s;
+    a.hist = hist + (size_t)s * d.cap;
+    a.hist_n = hist_n + s;
+    a.hist_cap = d.cap;
+    a.bar = mega_bar;
+    a.bar_base = mega_bar + 1;
+    a.abort = mega_abort;
+    a.err = err;
+    a.tl = tl_buf;
+    a.grid = d.nsm;
+    return launch_megastep(a, stream);
+  }
+
   cudaError_t run_decode(int s) {
+    if (use_mega && trace_kind < 0) return run_mega(s);
     if (tl_buf) {  // per launch: start and wait-release reduce with min, end with max
       cudaError_t e = cudaMemcpyAsync(tl_buf, tl_init.data(), sizeof(unsigned long long) * 3 * tl_n,
                                       cudaMemcpyHostToDevice, stream);
@@ -361,7 +397,8 @@ struct qw_model {
     if (bblock) cudaFree(bblock);
     if (battn_ws) cudaFree(battn_ws);
     void* bufs[] = {kv, x, q, attn, act, logits, rope, attn_ws, keys, lm_counter, pos, tok,
-                    hist, hist_n, err, ids, pf_block, pf_ws, w16, tl_buf};
+                    hist, hist_n, err, ids, pf_block, pf_ws, w16, tl_buf, mega_layers, mega_part,
+                    mega_bar, mega_abort};
     for (void* b : bufs)
       if (b) cudaFree(b);
     if (pinned) cudaFreeHost(pinned);
@@ -543,6 +580,31 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
     }
   }
   if ((e = decode_set_attributes(d))) return bail(e, "decode attributes");
+  {
+    // single-sequence decode steps of bf16 models as one persistent kernel (QW_MEGA=0: one
+    // kernel per operation) when the shape has an instance and one CTA per SM can be
+    // resident with its shared memory (cooperative launch)
+    const char* mv = std::getenv("QW_MEGA");
+    int coop = 0, per_sm = 0;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device);
+    if (!(mv && mv[0] == '0') && coop && megastep_supported(d, d.nsm)) {
+      if ((e = megastep_set_attributes(d.hd))) return bail(e, "decode step attributes");
+      if ((e = megastep_occupancy(d.hd, &per_sm))) return bail(e, "decode step occupancy");
+    }
+    if (per_sm >= 1) {
+      std::vector<unsigned char> recs(megastep_layer_bytes() * d.L);
+      for (int l = 0; l < d.L; ++l) megastep_fill_layer(recs.data() + l * megastep_layer_bytes(), m->layers[l]);
+      if ((e = cudaMalloc(&m->mega_layers, recs.size()))) return bail(e, "cudaMalloc");
+      if ((e = cudaMemcpy(m->mega_layers, recs.data(), recs.size(), cudaMemcpyHostToDevice)))
+        return bail(e, "cudaMemcpy");
+      if ((e = cudaMalloc(&m->mega_part, megastep_part_bytes(d)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMalloc(&m->mega_bar, 2 * sizeof(unsigned long long)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMemset(m->mega_bar, 0, 2 * sizeof(unsigned long long)))) return bail(e, "cudaMemset");
+      if ((e = cudaMalloc(&m->mega_abort, sizeof(int)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMemset(m->mega_abort, 0, sizeof(int)))) return bail(e, "cudaMemset");
+      m->use_mega = true;
+    }
+  }
   if (m->pf.use_tc && S > 1) {
     // batched decode: every weight matrix read once per step for all active sequences
     const char* bz = std::getenv("QW_BATCHED");
@@ -866,6 +928,11 @@ qw_status qw_read_logits(qw_model* m, int32_t seq, float* host_out) {
 }
 
 const int32_t* qw_tokens_device(const qw_model* m) { return m ? m->tok : nullptr; }
+
+int32_t qw_decode_kernels_per_step(const qw_model* m) {
+  if (!m) return 0;
+  return m->use_mega ? 1 : 5 * m->d.L + 2;
+}
 
 qw_status qw_position(const qw_model* m, int32_t seq, int32_t* pos) {
   g_err.clear();

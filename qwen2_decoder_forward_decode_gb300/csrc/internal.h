@@ -110,6 +110,33 @@ cudaError_t gemm_tc_swiglu(const __half* A, int lda, const __half* Wg, const __h
                            __half* Act, int ldc, int M, int N, int K, int* err, cudaStream_t s, float* ws = nullptr,
                            size_t ws_floats = 0, int nsm = 0);
 
+// ---- megastep.cu (one persistent kernel per decode step of one sequence, bf16 models) ----
+struct MegaLaunch {
+  Dims d;
+  const void* layers_dev;          // device array of n_layers megastep layer records
+  const void *embed, *final_norm, *head;
+  const float2* rope;
+  void* kv_seq;                    // fp16 cache of the sequence [L][2][nkv][cap][hd]
+  float *x, *q, *act, *logits, *part;
+  int *tok, *pos;
+  unsigned long long* key;
+  int *hist, *hist_n;
+  int hist_cap;
+  unsigned long long *bar, *bar_base;  // grid-barrier counter and its value at the step start
+  int *abort, *err;
+  unsigned long long* tl;          // per phase [start, units done, end] or null
+  int grid;
+};
+bool megastep_supported(const Dims& d, int nsm);
+size_t megastep_smem(int hd);
+size_t megastep_part_bytes(const Dims& d);
+cudaError_t megastep_set_attributes(int hd);
+int megastep_threads();
+cudaError_t megastep_occupancy(int hd, int* per_sm);  // resident CTAs per SM
+size_t megastep_layer_bytes();
+void megastep_fill_layer(void* dst, const LayerPtrs& w);
+cudaError_t launch_megastep(const MegaLaunch& a, cudaStream_t s);
+
 // ---- gemm_tc.cu: skinny GEMM of batched decode ----
 // Precomputed tensor maps (opaque 128-byte CUtensorMap storage) and the launch shape of one
 // skinny GEMM: nz weight matrices against the 16 activation rows of the sequences.

@@ -1,0 +1,1027 @@
+// Persistent decode step of one sequence of a bf16 model: one cooperative launch runs the
+// whole greedy decode step ("LLM Speedrun: Architecture", Transformer architecture and
+// Implementing Qwen: embedding, per layer RMSNorm -> q/k/v with bias -> split-half RoPE ->
+// KV append -> GQA attention -> o_proj + residual -> RMSNorm -> gate/up -> SwiGLU -> down +
+// residual, then the final RMSNorm, the LM head and the greedy argmax; "augur", Features:
+// preallocated KV cache, greedy generation).
+//
+// Why one kernel: a decode token streams every weight once (HBM-bound) through five
+// dependent phases per layer. Launched as separate kernels, the HBM stream stops at every
+// phase boundary and ramps up again. Here every CTA (one per SM) owns a ring of shared-memory
+// slots that its producer warps keep filling with the weights of the phases ahead, in the
+// order they will be used, without waiting for any data dependency; only the consumer warps
+// wait for the phase inputs (grid barriers). So the HBM stream keeps running while the
+// consumers go through the latency-bound q/k/v -> attention -> o_proj chain.
+//
+// Work split, per phase, in contiguous blocks over the CTAs (block b of n items is
+// [b n / G, (b + 1) n / G)):
+//   QKV     RoPE pairs (rows i and i + hd/2 of a head)     units: up to R/2 pairs of a head
+//   ATTN    (KV head, context chunk) per CTA               no weights
+//   OPROJ   rows of Wo                                     units: up to R rows
+//   GATEUP  items i (gate row i, up row i)                 units: up to R/2 items
+//   DOWN    rows of Wd (K = intermediate)                  units: one row, K split 8 ways
+//   LM      rows of the LM head                            units: up to R rows
+// R = rows of hidden elements per ring slot (8 for hidden 1536). Each unit is one or two
+// 1-D bulk copies (TMA) into a slot. All eight consumer warps read every unit: in the row
+// phases warp w takes row w of the unit (the input vector in registers), in DOWN warp w
+// takes the w-th eighth of the row. Row results go to shared memory; after the phase each
+// CTA applies its epilogue (bias + RoPE + KV append, residual adds, SwiGLU, logits and
+// argmax) and meets the other CTAs at a grid barrier.
+//
+// Every wait is bounded: on expiry the kernel raises an abort flag that every other wait
+// observes, sets ERR_TIMEOUT, lets its own copies land and returns.
+#include "common.cuh"
+#include "internal.h"
+
+#include <math.h>
+
+#include <algorithm>
+#include <cstring>
+
+namespace qw {
+namespace mk {
+
+constexpr int NCW = 8;                     // consumer warps
+constexpr int NPW = 4;                     // producer warps (lane 0 of each issues copies)
+constexpr int NCT = NCW * 32;              // consumer threads
+constexpr int THREADS = (NCW + NPW) * 32;
+constexpr int NS = 8;                      // ring slots (a multiple of NPW)
+constexpr int SLOT = 24 * 1024;            // bytes per slot
+constexpr int MAXV = 8;                    // 16-byte vectors per lane of a row (K <= 2048)
+constexpr int MAXD = 8;                    // vectors per lane of a DOWN segment
+constexpr int MAX_LOCAL = 128;             // items of one phase per CTA
+constexpr int NSPLIT = 16;                 // most attention chunks per KV head
+constexpr int CHUNK_MIN = 32;              // fewest positions per chunk
+constexpr int AT_K = 32;                   // positions per attention tile
+constexpr int GMAX = 8;                    // most query heads per KV head
+constexpr int XS_FLOATS = 2048;            // staged input vector (hidden <= 2048)
+
+enum : int { P_QKV = 0, P_ATTN = 1, P_OPROJ = 2, P_GATEUP = 3, P_DOWN = 4, P_LM = 5 };
+
+struct LayerW {
+  const bf16 *in_norm, *wq, *wk, *wv, *bq, *bk, *bv, *wo, *post_norm, *wg, *wu, *wd;
+};
+
+struct Params {
+  const LayerW* layers;      // device array [L]
+  int L, H, nq, nkv, I, V, cap;
+  float eps;
+  const bf16 *embed, *final_norm, *head;
+  const float2* rope;        // [cap][hd/2] (cos, sin)
+  f16* kv;                   // this sequence's cache [L][2][nkv][cap][hd]
+  float *x, *q, *act, *logits, *part;
+  int *tok, *pos;
+  unsigned long long* key;   // packed argmax key (zero between steps)
+  int *hist, *hist_n;
+  int hist_cap;
+  unsigned long long* bar;   // monotonic arrival counter
+  unsigned long long* bar_base;  // its value when a step starts (updated by CTA 0 at the end)
+  int* abort;                // nonzero: a wait gave up somewhere
+  int* err;
+  unsigned long long* tl;    // timeline: per phase [start, units done, end] (CTA 0), or null
+};
+
+template <int HD>
+struct Smem {
+  static constexpr int KS = HD + 8;  // halves per attention tile row (16-byte pad)
+  static constexpr size_t RING = (size_t)NS * SLOT;
+  static constexpr size_t ATT = (size_t)2 * AT_K * KS * 2;  // K and V tiles (the combine reuses them)
+  static constexpr size_t OFF_ATT = RING;
+  static constexpr size_t OFF_XS = OFF_ATT + ATT;
+  static constexpr size_t OFF_DA = OFF_XS + XS_FLOATS * 4;
+  static constexpr size_t OFF_DB = OFF_DA + MAX_LOCAL * 4;
+  static constexpr size_t OFF_DP = OFF_DB + MAX_LOCAL * 4;       // DOWN partials [rows][NCW]
+  static constexpr size_t OFF_MW = OFF_DP + 64 * NCW * 4;          // merge (m, w) [2][nq][NSPLIT]
+  static constexpr size_t OFF_BAR = OFF_MW + 2 * 32 * NSPLIT * 4;
+  static constexpr size_t OFF_SCR = OFF_BAR + 2 * NS * 8;
+  static constexpr size_t TOTAL = OFF_SCR + 64 * 4;
+  static constexpr size_t ALLOC = TOTAL + 1024;  // base aligned to 1024 inside
+  static_assert(2 * 16 * HD * 4 + 4 * 16 * 4 <= ATT, "attention combine must fit the tile area");
+};
+
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory"); }
+// consumer barrier that also ANDs a predicate over every consumer thread
+__device__ __forceinline__ bool cbar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, 1, %2, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(NCT)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ bool aborted(const Params& p) { return *(volatile int*)p.abort != 0; }
+
+__device__ __forceinline__ void raise_abort(const Params& p) {
+  atomicExch(p.abort, 1);
+  atomicOr(p.err, ERR_TIMEOUT);
+}
+
+// Bounded wait on an mbarrier phase that also gives up once the launch has aborted.
+__device__ __forceinline__ bool slot_wait(const Params& p, uint32_t bar, uint32_t parity) {
+  if (mbar_test_now(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (int it = 0;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 31) == 31) {
+      if (aborted(p)) return false;
+      if (clock64() - t0 > WAIT_CYCLES) {
+        raise_abort(p);
+        return false;
+      }
+    }
+  }
+}
+
+// block [i0, i1) of n items for this CTA
+__device__ __forceinline__ void block_of(int n, int& i0, int& i1) {
+  i0 = (int)((long long)blockIdx.x * n / gridDim.x);
+  i1 = (int)((long long)(blockIdx.x + 1) * n / gridDim.x);
+}
+
+// rows of hidden (K = H) elements per slot, even, at most one per consumer warp
+__device__ __forceinline__ int rows_per_slot(int H) {
+  int r = SLOT / (2 * H);
+  r &= ~1;
+  return r > NCW ? NCW : r;
+}
+
+struct Unit {
+  const unsigned char* src[2];
+  uint32_t bytes[2];
+  uint32_t off2;  // slot offset of the second copy
+  int a, n;       // first item (pair, row) and count
+};
+
+// Calls f(unit) for each unit of phase ph of layer l for this CTA, in stream order, until f
+// returns false; returns false in that case.
+template <class F>
+__device__ __forceinline__ bool phase_units(const Params& p, int hd, int l, int ph, F&& f) {
+  const int R = rows_per_slot(p.H);
+  const size_t rowH = (size_t)p.H * 2;  // bytes of a row of K = H
+  const LayerW& w = p.layers[l < p.L ? l : 0];
+  int i0, i1;
+  Unit u;
+  u.bytes[1] = 0;
+  u.src[1] = nullptr;
+  u.off2 = 0;
+  switch (ph) {
+    case P_QKV: {
+      const int half = hd >> 1;
+      block_of((p.nq + 2 * p.nkv) * half, i0, i1);
+      for (int a = i0; a < i1;) {
+        const int head = a / half, i = a - head * half;
+        int n = min(min(R / 2, i1 - a), half - i);
+        const bf16* m;
+        int hrow;
+        if (head < p.nq) { m = w.wq; hrow = head * hd; }
+        else if (head < p.nq + p.nkv) { m = w.wk; hrow = (head - p.nq) * hd; }
+        else { m = w.wv; hrow = (head - p.nq - p.nkv) * hd; }
+        u.src[0] = reinterpret_cast<const unsigned char*>(m + (size_t)(hrow + i) * p.H);
+        u.src[1] = reinterpret_cast<const unsigned char*>(m + (size_t)(hrow + half + i) * p.H);
+        u.bytes[0] = u.bytes[1] = (uint32_t)(n * rowH);
+        u.off2 = (uint32_t)((R / 2) * rowH);
+        u.a = a;
+        u.n = n;
+        if (!f(u)) return false;
+        a += n;
+      }
+      return true;
+    }
+    case P_OPROJ:
+    case P_LM: {
+      const int N = ph == P_OPROJ ? p.H : p.V;
+      const bf16* m = ph == P_OPROJ ? w.wo : p.head;
+      block_of(N, i0, i1);
+      for (int a = i0; a < i1;) {
+        const int n = min(R, i1 - a);
+        u.src[0] = reinterpret_cast<const unsigned char*>(m + (size_t)a * p.H);
+        u.bytes[0] = (uint32_t)(n * rowH);
+        u.bytes[1] = 0;
+        u.a = a;
+        u.n = n;
+        if (!f(u)) return false;
+        a += n;
+      }
+      return true;
+    }
+    case P_GATEUP: {
+      block_of(p.I, i0, i1);
+      for (int a = i0; a < i1;) {
+        const int n = min(R / 2, i1 - a);
+        u.src[0] = reinterpret_cast<const unsigned char*>(w.wg + (size_t)a * p.H);
+        u.src[1] = reinterpret_cast<const unsigned char*>(w.wu + (size_t)a * p.H);
+        u.bytes[0] = u.bytes[1] = (uint32_t)(n * rowH);
+        u.off2 = (uint32_t)((R / 2) * rowH);
+        u.a = a;
+        u.n = n;
+        if (!f(u)) return false;
+        a += n;
+      }
+      return true;
+    }
+    case P_DOWN: {
+      block_of(p.H, i0, i1);
+      for (int a = i0; a < i1; ++a) {
+        u.src[0] = reinterpret_cast<const unsigned char*>(w.wd + (size_t)a * p.I);
+        u.bytes[0] = (uint32_t)p.I * 2;
+        u.bytes[1] = 0;
+        u.a = a;
+        u.n = 1;
+        if (!f(u)) return false;
+      }
+      return true;
+    }
+    default: return true;
+  }
+}
+
+// attention chunking for a context of ctx positions
+__device__ __forceinline__ void att_chunks(int ctx, int& chunk, int& ns) {
+  chunk = max(CHUNK_MIN, (ctx + NSPLIT - 1) / NSPLIT);
+  ns = (ctx + chunk - 1) / chunk;
+}
+
+// ---- producers -----------------------------------------------------------------------
+
+template <int HD>
+__device__ void producer(const Params& p, unsigned char* smem, uint32_t full0, uint32_t empty0, int pw, int ctx) {
+  long long u = 0;                 // unit counter (same sequence as the consumers')
+  long long last_mine[NS / NPW];   // most recent unit issued into each of my slots
+  for (int i = 0; i < NS / NPW; ++i) last_mine[i] = -1;
+  bool ok = true;
+  const uint32_t ring = smem_addr(smem);
+  int chunk, ns;
+  att_chunks(ctx, chunk, ns);
+  auto issue = [&](const Unit& un) -> bool {
+    const long long my = u++;
+    if ((int)(my % NPW) != pw) return true;
+    const int s = (int)(my % NS);
+    if (my >= NS) {  // the slot's previous unit (also mine) has been read by every consumer
+      if (!slot_wait(p, empty0 + 8 * s, (uint32_t)(((my / NS) - 1) & 1))) return false;
+      fence_proxy_async();
+    }
+    const uint32_t total = un.bytes[0] + un.bytes[1];
+    // copies stay inside the slot, start 16-byte aligned and move multiples of 16 bytes
+    if (total == 0 || total > SLOT || (un.bytes[0] & 15) || (un.bytes[1] & 15) ||
+        un.off2 + un.bytes[1] > SLOT || (un.bytes[1] && un.off2 < un.bytes[0])) {
+      raise_abort(p);
+      return false;
+    }
+    const uint32_t dst = ring + (uint32_t)s * SLOT;
+    mbar_expect_tx(full0 + 8 * s, total);
+    bulk_copy_g2s(dst, un.src[0], un.bytes[0], full0 + 8 * s);
+    if (un.bytes[1]) bulk_copy_g2s(dst + un.off2, un.src[1], un.bytes[1], full0 + 8 * s);
+    last_mine[s / NPW] = my;
+    return true;
+  };
+  for (int l = 0; l <= p.L && ok; ++l) {
+    if (l < p.L) {
+      // this CTA's attention chunk of layer l: its rows written by earlier steps into L2
+      if (pw == 0 && (int)blockIdx.x < p.nkv * ns) {
+        const int g = blockIdx.x / ns, c = blockIdx.x - g * ns;
+        const int j0 = c * chunk, j1 = min(ctx - 1, j0 + chunk);  // the newest row is written this step
+        if (j1 > j0) {
+          const f16* kc = p.kv + (size_t)l * 2 * p.nkv * p.cap * HD;
+          const size_t off = ((size_t)g * p.cap + j0) * HD;
+          const uint32_t bytes = (uint32_t)(j1 - j0) * HD * 2;
+          prefetch_l2_bulk(kc + off, bytes);
+          prefetch_l2_bulk(kc + (size_t)p.nkv * p.cap * HD + off, bytes);
+        }
+      }
+      const int phs[4] = {P_QKV, P_OPROJ, P_GATEUP, P_DOWN};
+      for (int k = 0; k < 4 && ok; ++k) {
+        ok = phase_units(p, HD, l, phs[k], issue);
+        if (ok && aborted(p)) ok = false;
+      }
+    } else {
+      ok = phase_units(p, HD, l, P_LM, issue);
+    }
+  }
+  // copies in flight land before the CTA may exit (they were all consumed unless aborted)
+  for (int i = 0; i < NS / NPW; ++i) {
+    const long long m = last_mine[i];
+    if (m >= 0) slot_wait(p, full0 + 8 * (int)(m % NS), (uint32_t)((m / NS) & 1));
+  }
+}
+
+// ---- consumer helpers ----------------------------------------------------------------
+
+// dot of one row held in a slot (16-byte vectors of bf16) with the input vector in registers
+__device__ __forceinline__ float row_dot(const unsigned char* row, const float (&xr)[MAXV][8], int nvec, int lane) {
+  const uint4* r = reinterpret_cast<const uint4*>(row);
+  float acc = 0.f;
+#pragma unroll
+  for (int q = 0; q < MAXV; ++q) {
+    const int v = lane + 32 * q;
+    if (v < nvec) acc = dotv(r[v], xr[q], acc, bf16());
+  }
+  return warp_sum(acc);
+}
+
+// input vector of the row phases from the staged xs (floats) into registers: lane l holds
+// vectors l, l + 32, ... (8 floats each); two 16-byte shared loads per vector, lanes with bit
+// 2 set taking the halves in the other order (conflict-free)
+__device__ __forceinline__ void load_xr(float (&xr)[MAXV][8], const float* xs, int nvec, int lane) {
+  const bool sw = (lane & 4) != 0;
+#pragma unroll
+  for (int q = 0; q < MAXV; ++q) {
+    const int v = lane + 32 * q;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (v < nvec) {
+      const float4* s = reinterpret_cast<const float4*>(xs) + 2 * v;
+      a = s[sw ? 1 : 0];
+      b = s[sw ? 0 : 1];
+    }
+    const float4 lo = sw ? b : a, hi = sw ? a : b;
+    xr[q][0] = lo.x; xr[q][1] = lo.y; xr[q][2] = lo.z; xr[q][3] = lo.w;
+    xr[q][4] = hi.x; xr[q][5] = hi.y; xr[q][6] = hi.z; xr[q][7] = hi.w;
+  }
+}
+
+// xs = src / sqrt(mean(src^2) + eps) * gain over H elements (consumer threads); src is the
+// residual x (global, written by other CTAs: read through L2) or, when erow is given, the
+// bf16 embedding row.
+__device__ void stage_norm(const Params& p, float* xs, float* scr, const float* src, const bf16* erow,
+                           const bf16* gain) {
+  const int t = threadIdx.x;
+  const int n4 = p.H >> 2;
+  float4 v[2];
+  uint2 g[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int j = t + i * NCT;
+    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    g[i] = make_uint2(0u, 0u);
+    if (j < n4) {
+      if (erow) {
+        const uint2 e = __ldg(reinterpret_cast<const uint2*>(erow) + j);
+        v[i] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
+      } else {
+        v[i] = __ldcg(reinterpret_cast<const float4*>(src) + j);
+      }
+      g[i] = __ldg(reinterpret_cast<const uint2*>(gain) + j);
+    }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    ss = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, fmaf(v[i].w, v[i].w, ss))));
+  ss = warp_sum(ss);
+  if ((t & 31) == 0) scr[t >> 5] = ss;
+  cbar();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < NCW; ++i) tot += scr[i];  // fixed order: deterministic
+  const float inv = rsqrtf(tot / (float)p.H + p.eps);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int j = t + i * NCT;
+    if (j < n4)
+      reinterpret_cast<float4*>(xs)[j] = make_float4(v[i].x * inv * bf_lo(g[i].x), v[i].y * inv * bf_hi(g[i].x),
+                                                     v[i].z * inv * bf_lo(g[i].y), v[i].w * inv * bf_hi(g[i].y));
+  }
+  cbar();
+}
+
+// Grid barrier of the consumers of all CTAs: each CTA adds one to a monotonic counter and
+// waits until it reaches base + nb * CTAs. Returns false (uniformly) after an abort.
+__device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int* s_flag) {
+  cbar();
+  ++nb;
+  if (threadIdx.x == 0) {
+    int ok = 0;
+    if (!aborted(p)) {
+      __threadfence();
+      atomicAdd(p.bar, 1ull);
+      const unsigned long long target = base + (unsigned long long)nb * gridDim.x;
+      const long long t0 = clock64();
+      ok = 1;
+      for (int it = 0;; ++it) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p.bar) : "memory");
+        if (v >= target) break;
+        if ((it & 15) == 15) {
+          if (aborted(p)) { ok = 0; break; }
+          if (clock64() - t0 > WAIT_CYCLES) { raise_abort(p); ok = 0; break; }
+        }
+      }
+    }
+    *s_flag = ok;
+  }
+  cbar();
+  return *(volatile int*)s_flag != 0;
+}
+
+__device__ __forceinline__ void tl_mark(const Params& p, int k, int which) {
+  if (p.tl && blockIdx.x == 0 && threadIdx.x == 0) p.tl[3 * k + which] = gtime();
+}
+
+// ---- attention of one (KV head, chunk) -----------------------------------------------------
+//
+// Tiles of AT_K positions: all consumer threads copy the K and V rows (cp.async, rows padded
+// by 16 bytes); warps 0 and 1 each take 16 positions with mma.sync m16n8k16 (the G query
+// heads of the KV head are the rows of the A operand, fp16 q scaled by 1/sqrt(hd)), keeping a
+// running maximum and sum per row; the two warps' states are combined into the chunk's
+// partial (unnormalised output, maximum, sum), which the o_proj phase merges.
+template <int HD>
+__device__ void attention_chunk(const Params& p, unsigned char* att, int l, int g, int c, int chunk, int ctx) {
+  constexpr int KS = HD + 8, NKK = HD / 16, NNT = HD / 8;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, gid = lane >> 2, tig = lane & 3;
+  const int G = p.nq / p.nkv;
+  f16* Ks = reinterpret_cast<f16*>(att);
+  f16* Vs = Ks + AT_K * KS;
+  const int j0 = c * chunk, j1 = min(ctx, j0 + chunk), n = j1 - j0;
+  const f16* kc = p.kv + (size_t)l * 2 * p.nkv * p.cap * HD + ((size_t)g * p.cap + j0) * HD;
+  const f16* vc = kc + (size_t)p.nkv * p.cap * HD;
+  const float scale = rsqrtf((float)HD);
+  uint32_t qa[NKK][4];
+  if (warp < 2) {
+    const float* qz = p.q + (size_t)g * G * HD;
+#pragma unroll
+    for (int kk = 0; kk < NKK; ++kk)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = (r & 1) ? gid + 8 : gid;
+        const int col = 16 * kk + ((r & 2) ? 8 : 0) + 2 * tig;
+        float2 v = make_float2(0.f, 0.f);
+        if (row < G) v = __ldcg(reinterpret_cast<const float2*>(qz + (size_t)row * HD + col));
+        qa[kk][r] = pack_half2(v.x * scale, v.y * scale);
+      }
+  }
+  float o[NNT][4];
+#pragma unroll
+  for (int nt = 0; nt < NNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  const int ntiles = (n + AT_K - 1) / AT_K;
+  const int kw = 16 * warp;
+  for (int tt = 0; tt < ntiles; ++tt) {
+    constexpr int NV = AT_K * HD / 8;  // 16-byte vectors of a K (or V) tile
+    for (int i = t; i < 2 * NV; i += NCT) {
+      const int which = i >= NV, idx = i - which * NV;
+      const int j = idx / (HD / 8), c8 = idx - j * (HD / 8);
+      f16* dst = (which ? Vs : Ks) + j * KS + c8 * 8;
+      const int key = tt * AT_K + j;
+      if (key < n) cp_async16(dst, (which ? vc : kc) + (size_t)key * HD + c8 * 8);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    cbar();
+    if (warp < 2 && tt * AT_K + kw < n) {
+      float sc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        const f16* krow = Ks + (size_t)(kw + 8 * nt + gid) * KS + 2 * tig;
+#pragma unroll
+        for (int kk = 0; kk < NKK; ++kk)
+          mma16816(sc[nt], qa[kk], *reinterpret_cast<const uint32_t*>(krow + 16 * kk),
+                   *reinterpret_cast<const uint32_t*>(krow + 16 * kk + 8));
+        const int key = tt * AT_K + kw + 8 * nt + 2 * tig;  // positions past the chunk: masked
+        if (key >= n) sc[nt][0] = sc[nt][2] = -INFINITY;
+        if (key + 1 >= n) sc[nt][1] = sc[nt][3] = -INFINITY;
+      }
+      float mx_lo = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      float mx_hi = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      const float c_lo = m_lo == -INFINITY ? 0.f : expf(m_lo - mn_lo);
+      const float c_hi = m_hi == -INFINITY ? 0.f : expf(m_hi - mn_hi);
+      float pr[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        pr[nt][0] = mn_lo == -INFINITY ? 0.f : expf(sc[nt][0] - mn_lo);
+        pr[nt][1] = mn_lo == -INFINITY ? 0.f : expf(sc[nt][1] - mn_lo);
+        pr[nt][2] = mn_hi == -INFINITY ? 0.f : expf(sc[nt][2] - mn_hi);
+        pr[nt][3] = mn_hi == -INFINITY ? 0.f : expf(sc[nt][3] - mn_hi);
+      }
+      float s_lo = pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1], s_hi = pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
+      s_lo += __shfl_xor_sync(0xffffffffu, s_lo, 1);
+      s_lo += __shfl_xor_sync(0xffffffffu, s_lo, 2);
+      s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 1);
+      s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 2);
+      l_lo = l_lo * c_lo + s_lo;
+      l_hi = l_hi * c_hi + s_hi;
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      const uint32_t pa[4] = {pack_half2(pr[0][0], pr[0][1]), pack_half2(pr[0][2], pr[0][3]),
+                              pack_half2(pr[1][0], pr[1][1]), pack_half2(pr[1][2], pr[1][3])};
+      // value rows kw + (lane % 8) + 8 ((lane / 8) % 2), columns of n-tile pair nt, nt + 1
+      const f16* vrow = Vs + (size_t)(kw + (lane & 7) + ((lane >> 3) & 1) * 8) * KS + (lane >> 4) * 8;
+#pragma unroll
+      for (int nt = 0; nt < NNT; nt += 2) {
+        o[nt][0] *= c_lo; o[nt][1] *= c_lo; o[nt][2] *= c_hi; o[nt][3] *= c_hi;
+        o[nt + 1][0] *= c_lo; o[nt + 1][1] *= c_lo; o[nt + 1][2] *= c_hi; o[nt + 1][3] *= c_hi;
+        uint32_t b[4];
+        ldmatrix_x4_trans(b, vrow + nt * 8);
+        mma16816(o[nt], pa, b[0], b[1]);
+        mma16816(o[nt + 1], pa, b[2], b[3]);
+      }
+    }
+    cbar();  // the tile buffers are free again
+  }
+  // combine warps 0 and 1 (rows < G) in the tile area
+  float* cO = reinterpret_cast<float*>(att);  // [2][16][HD]
+  float* cM = cO + 2 * 16 * HD;               // [2][16]
+  float* cL = cM + 2 * 16;
+  if (warp < 2) {
+#pragma unroll
+    for (int nt = 0; nt < NNT; ++nt) {
+      const int col = 8 * nt + 2 * tig;
+      *reinterpret_cast<float2*>(cO + (size_t)(warp * 16 + gid) * HD + col) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(cO + (size_t)(warp * 16 + gid + 8) * HD + col) = make_float2(o[nt][2], o[nt][3]);
+    }
+    if (tig == 0) {
+      cM[warp * 16 + gid] = m_lo;
+      cM[warp * 16 + gid + 8] = m_hi;
+      cL[warp * 16 + gid] = l_lo;
+      cL[warp * 16 + gid + 8] = l_hi;
+    }
+  }
+  cbar();
+  const int ps = attn_part_stride(HD);
+  for (int idx = t; idx < G * HD; idx += NCT) {
+    const int r = idx / HD, d = idx - r * HD;
+    const float M = fmaxf(cM[r], cM[16 + r]);
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const float mw = cM[w * 16 + r];
+      if (mw != -INFINITY) acc = fmaf(expf(mw - M), cO[(size_t)(w * 16 + r) * HD + d], acc);
+    }
+    p.part[((size_t)(g * G + r) * NSPLIT + c) * ps + d] = acc;
+  }
+  if (t < G) {
+    const float M = fmaxf(cM[t], cM[16 + t]);
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const float mw = cM[w * 16 + t];
+      if (mw != -INFINITY) L = fmaf(expf(mw - M), cL[w * 16 + t], L);
+    }
+    float* pp = p.part + ((size_t)(g * G + t) * NSPLIT + c) * ps;
+    pp[HD] = M;
+    pp[HD + 1] = L;
+  }
+}
+
+// o (the attention output of all heads) merged from the chunk partials into xs:
+// o_h = sum_c w_c O_c, w_c = exp(m_c - M) / sum_c' l_c' exp(m_c' - M) (chunk order).
+template <int HD>
+__device__ void stage_merge(const Params& p, float* xs, float* mw, int ns) {
+  const int t = threadIdx.x;
+  const int K = p.nq * HD, ps = attn_part_stride(HD);
+  constexpr int MB = 8;  // chunks per batch of loads
+  // (m, l) of every (head, chunk), requested together with the first batch of outputs
+  const int groups = K / 4;  // float4 groups; thread t takes groups t and t + NCT
+  float4 v[2][MB];
+  auto load = [&](int c0) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int gi = t + e * NCT;
+      const int h = (4 * gi) / HD, d = 4 * gi - h * HD;
+#pragma unroll
+      for (int u = 0; u < MB; ++u)
+        v[e][u] = (gi < groups && c0 + u < ns)
+                      ? __ldcg(reinterpret_cast<const float4*>(p.part + ((size_t)h * NSPLIT + c0 + u) * ps + d))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load(0);
+  for (int i = t; i < p.nq * ns; i += NCT) {
+    const int h = i / ns, c = i - h * ns;
+    const float* pp = p.part + ((size_t)h * NSPLIT + c) * ps + HD;
+    mw[h * NSPLIT + c] = __ldcg(pp);
+    mw[(p.nq + h) * NSPLIT + c] = __ldcg(pp + 1);
+  }
+  cbar();
+  for (int h = t; h < p.nq; h += NCT) {  // weights of head h, in chunk order
+    float M = -INFINITY;
+    for (int c = 0; c < ns; ++c) M = fmaxf(M, mw[h * NSPLIT + c]);
+    float L = 0.f;
+    for (int c = 0; c < ns; ++c) {
+      const float e = expf(mw[h * NSPLIT + c] - M);
+      mw[h * NSPLIT + c] = e;
+      L = fmaf(mw[(p.nq + h) * NSPLIT + c], e, L);
+    }
+    const float inv = 1.f / L;
+    for (int c = 0; c < ns; ++c) mw[h * NSPLIT + c] *= inv;
+  }
+  cbar();
+  float4 acc[2];
+  acc[0] = acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < ns; c0 += MB) {
+    if (c0) load(c0);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int gi = t + e * NCT;
+      if (gi >= groups) continue;
+      const int h = (4 * gi) / HD;
+#pragma unroll
+      for (int u = 0; u < MB; ++u)
+        if (c0 + u < ns) {
+          const float wgt = mw[h * NSPLIT + c0 + u];
+          acc[e].x = fmaf(v[e][u].x, wgt, acc[e].x);
+          acc[e].y = fmaf(v[e][u].y, wgt, acc[e].y);
+          acc[e].z = fmaf(v[e][u].z, wgt, acc[e].z);
+          acc[e].w = fmaf(v[e][u].w, wgt, acc[e].w);
+        }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int gi = t + e * NCT;
+    if (gi < groups) reinterpret_cast<float4*>(xs)[gi] = acc[e];
+  }
+  cbar();
+}
+
+// ---- the kernel ------------------------------------------------------------------------
+
+template <int HD>
+__global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p) {
+  using S = Smem<HD>;
+  extern __shared__ unsigned char mk_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)mk_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* att = smem + S::OFF_ATT;
+  float* xs = reinterpret_cast<float*>(smem + S::OFF_XS);
+  float* dA = reinterpret_cast<float*>(smem + S::OFF_DA);
+  float* dB = reinterpret_cast<float*>(smem + S::OFF_DB);
+  float* dP = reinterpret_cast<float*>(smem + S::OFF_DP);
+  float* mwv = reinterpret_cast<float*>(smem + S::OFF_MW);
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + S::OFF_BAR);
+  float* scr = reinterpret_cast<float*>(smem + S::OFF_SCR);
+  int* s_flag = reinterpret_cast<int*>(scr + 48);
+  const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + NS);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+
+  // the position and the token were written by the previous step (or the prefill), before
+  // this launch; the key is zero between steps
+  const int pos = __ldcg(p.pos);
+  const int ctx = pos + 1;
+  if (t == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, NCW);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();  // the only block-wide barrier: producers and consumers part here
+
+  if (warp >= NCW) {
+    if (lane == 0) producer<HD>(p, smem, full0, empty0, warp - NCW, ctx);
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const unsigned long long base = __ldcg(p.bar_base);
+  int nb = 0;        // grid barriers passed
+  long long u = 0;   // unit counter
+  int tok = __ldcg(p.tok);
+  if (tok < 0 || tok >= p.V) {
+    if (t == 0 && blockIdx.x == 0) atomicOr(p.err, ERR_TOKEN);
+    tok = 0;
+  }
+  const bf16* erow = p.embed + (size_t)tok * p.H;
+  const int half = HD >> 1;
+  const int nvecH = p.H >> 3;
+  int chunk, ns;
+  att_chunks(ctx, chunk, ns);
+  {  // the residual stream starts as the embedding row (each CTA writes its own rows)
+    int r0, r1;
+    block_of(p.H, r0, r1);
+    for (int r = r0 + t; r < r1; r += NCT) p.x[r] = __bfloat162float(erow[r]);
+  }
+  float xr[MAXV][8];
+  bool alive = true;
+  int ph_idx = 0;  // timeline index
+
+  // wait for unit u, apply fn to it, release the slot
+  auto consume = [&](const Unit& un, auto&& fn) -> bool {
+    const long long my = u++;
+    const int s = (int)(my % NS);
+    const bool ok = __all_sync(0xffffffffu, slot_wait(p, full0 + 8 * s, (uint32_t)((my / NS) & 1)));
+    if (!ok) return false;
+    fn(smem + (size_t)s * SLOT, un);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    return true;
+  };
+
+  for (int l = 0; l < p.L && alive; ++l) {
+    const LayerW& w = p.layers[l];
+    // ===== QKV: RMSNorm -> q/k/v rows (+ bias) -> RoPE -> q out, K/V append
+    tl_mark(p, ph_idx, 0);
+    int i0, i1;
+    block_of((p.nq + 2 * p.nkv) * half, i0, i1);
+    // epilogue inputs of this thread's pair (independent of the barrier's data)
+    float ba = 0.f, bb = 0.f;
+    float2 cs = make_float2(1.f, 0.f);
+    int e_head = 0, e_i = 0;
+    const bool e_mine = t < i1 - i0;
+    if (e_mine) {
+      const int item = i0 + t;
+      e_head = item / half;
+      e_i = item - e_head * half;
+      const bf16* bias;
+      int hh;
+      if (e_head < p.nq) { bias = w.bq; hh = e_head; }
+      else if (e_head < p.nq + p.nkv) { bias = w.bk; hh = e_head - p.nq; }
+      else { bias = w.bv; hh = e_head - p.nq - p.nkv; }
+      if (bias) {
+        ba = __bfloat162float(bias[hh * HD + e_i]);
+        bb = __bfloat162float(bias[hh * HD + e_i + half]);
+      }
+      if (e_head < p.nq + p.nkv) cs = p.rope[(size_t)pos * half + e_i];
+    }
+    stage_norm(p, xs, scr, p.x, l == 0 ? erow : nullptr, w.in_norm);
+    load_xr(xr, xs, nvecH, lane);
+    {
+      const int R = rows_per_slot(p.H);
+      const int hp = R / 2;
+      auto fn = [&](const unsigned char* slot, const Unit& un) {
+        const int j = warp < hp ? warp : warp - hp;
+        if (warp < R && j < un.n) {
+          const unsigned char* row = slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2;
+          const float d = row_dot(row, xr, nvecH, lane);
+          if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
+        }
+      };
+      alive = phase_units(p, HD, l, P_QKV, [&](const Unit& un) { return consume(un, fn); });
+    }
+    tl_mark(p, ph_idx, 1);
+    alive = cbar_and(alive);
+    if (alive && e_mine) {
+      float a = dA[t] + ba, b = dB[t] + bb;
+      if (e_head < p.nq + p.nkv) {  // rotate the pair (i, i + hd/2)
+        const float ra = a * cs.x - b * cs.y, rb = b * cs.x + a * cs.y;
+        a = ra;
+        b = rb;
+      }
+      if (e_head < p.nq) {
+        p.q[e_head * HD + e_i] = a;
+        p.q[e_head * HD + e_i + half] = b;
+      } else {
+        const bool is_k = e_head < p.nq + p.nkv;
+        const int hh = is_k ? e_head - p.nq : e_head - p.nq - p.nkv;
+        f16* dst = p.kv + (size_t)l * 2 * p.nkv * p.cap * HD + (is_k ? 0 : (size_t)p.nkv * p.cap * HD) +
+                   ((size_t)hh * p.cap + pos) * HD;
+        store_kv(dst + e_i, a, p.err);
+        store_kv(dst + e_i + half, b, p.err);
+      }
+    }
+    tl_mark(p, ph_idx++, 2);
+    alive = alive && grid_sync(p, base, nb, s_flag);
+    if (!alive) break;
+
+    // ===== ATTN: (KV head, chunk) partials
+    tl_mark(p, ph_idx, 0);
+    if ((int)blockIdx.x < p.nkv * ns) {
+      const int g = blockIdx.x / ns, c = blockIdx.x - g * ns;
+      attention_chunk<HD>(p, att, l, g, c, chunk, ctx);
+    }
+    tl_mark(p, ph_idx++, 2);
+    if (!grid_sync(p, base, nb, s_flag)) { alive = false; break; }
+
+    // ===== OPROJ: merge -> x += Wo o
+    tl_mark(p, ph_idx, 0);
+    stage_merge<HD>(p, xs, mwv, ns);
+    load_xr(xr, xs, (p.nq * HD) >> 3, lane);
+    block_of(p.H, i0, i1);
+    {
+      const int R = rows_per_slot(p.H);
+      auto fn = [&](const unsigned char* slot, const Unit& un) {
+        if (warp < R && warp < un.n) {
+          const float d = row_dot(slot + (size_t)warp * p.H * 2, xr, (p.nq * HD) >> 3, lane);
+          if (lane == 0) dA[un.a - i0 + warp] = d;
+        }
+      };
+      alive = phase_units(p, HD, l, P_OPROJ, [&](const Unit& un) { return consume(un, fn); });
+    }
+    tl_mark(p, ph_idx, 1);
+    alive = cbar_and(alive);
+    if (alive)
+      for (int r = i0 + t; r < i1; r += NCT) p.x[r] = __ldcg(p.x + r) + dA[r - i0];
+    tl_mark(p, ph_idx++, 2);
+    alive = alive && grid_sync(p, base, nb, s_flag);
+    if (!alive) break;
+
+    // ===== GATEUP: RMSNorm -> gate/up rows -> SwiGLU
+    tl_mark(p, ph_idx, 0);
+    stage_norm(p, xs, scr, p.x, nullptr, w.post_norm);
+    load_xr(xr, xs, nvecH, lane);
+    block_of(p.I, i0, i1);
+    {
+      const int R = rows_per_slot(p.H);
+      const int hp = R / 2;
+      auto fn = [&](const unsigned char* slot, const Unit& un) {
+        const int j = warp < hp ? warp : warp - hp;
+        if (warp < R && j < un.n) {
+          const unsigned char* row = slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2;
+          const float d = row_dot(row, xr, nvecH, lane);
+          if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
+        }
+      };
+      alive = phase_units(p, HD, l, P_GATEUP, [&](const Unit& un) { return consume(un, fn); });
+    }
+    tl_mark(p, ph_idx, 1);
+    alive = cbar_and(alive);
+    if (alive)
+      for (int i = i0 + t; i < i1; i += NCT) {
+        const float gv = dA[i - i0], uv = dB[i - i0];
+        p.act[i] = (gv / (1.f + expf(-gv))) * uv;
+      }
+    tl_mark(p, ph_idx++, 2);
+    alive = alive && grid_sync(p, base, nb, s_flag);
+    if (!alive) break;
+
+    // ===== DOWN: x += Wd act, each row's K split over the eight warps
+    tl_mark(p, ph_idx, 0);
+    {
+      const int nvecI = p.I >> 3;
+      const int segv = (nvecI + NCW - 1) / NCW;
+      const int v0 = warp * segv, v1 = min(nvecI, v0 + segv);
+      float xd[MAXD][8];
+#pragma unroll
+      for (int qd = 0; qd < MAXD; ++qd) {
+        const int v = v0 + lane + 32 * qd;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        if (v < v1) {
+          a = __ldcg(reinterpret_cast<const float4*>(p.act) + 2 * v);
+          b = __ldcg(reinterpret_cast<const float4*>(p.act) + 2 * v + 1);
+        }
+        xd[qd][0] = a.x; xd[qd][1] = a.y; xd[qd][2] = a.z; xd[qd][3] = a.w;
+        xd[qd][4] = b.x; xd[qd][5] = b.y; xd[qd][6] = b.z; xd[qd][7] = b.w;
+      }
+      block_of(p.H, i0, i1);
+      auto fn = [&](const unsigned char* slot, const Unit& un) {
+        const uint4* r = reinterpret_cast<const uint4*>(slot);
+        float acc = 0.f;
+#pragma unroll
+        for (int qd = 0; qd < MAXD; ++qd) {
+          const int v = v0 + lane + 32 * qd;
+          if (v < v1) acc = dotv(r[v], xd[qd], acc, bf16());
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) dP[(un.a - i0) * NCW + warp] = acc;
+      };
+      alive = phase_units(p, HD, l, P_DOWN, [&](const Unit& un) { return consume(un, fn); });
+    }
+    tl_mark(p, ph_idx, 1);
+    alive = cbar_and(alive);
+    if (alive)
+      for (int r = i0 + t; r < i1; r += NCT) {
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NCW; ++k) s += dP[(r - i0) * NCW + k];  // warp order
+        p.x[r] = __ldcg(p.x + r) + s;
+      }
+    tl_mark(p, ph_idx++, 2);
+    alive = alive && grid_sync(p, base, nb, s_flag);
+  }
+
+  // ===== LM head: final RMSNorm -> logits -> greedy argmax
+  if (alive) {
+    tl_mark(p, ph_idx, 0);
+    stage_norm(p, xs, scr, p.x, nullptr, p.final_norm);
+    load_xr(xr, xs, nvecH, lane);
+    float best_v = -INFINITY;
+    int best_i = -1;
+    bool bad = false;
+    {
+      const int R = rows_per_slot(p.H);
+      auto fn = [&](const unsigned char* slot, const Unit& un) {
+        if (warp < R && warp < un.n) {
+          const float z = row_dot(slot + (size_t)warp * p.H * 2, xr, nvecH, lane);
+          const int r = un.a + warp;
+          if (lane == 0) p.logits[r] = z;
+          if (!isfinite(z)) bad = true;
+          if (z > best_v || best_i < 0) { best_v = z; best_i = r; }  // rows arrive in increasing order
+        }
+      };
+      alive = phase_units(p, HD, p.L, P_LM, [&](const Unit& un) { return consume(un, fn); });
+    }
+    tl_mark(p, ph_idx, 1);
+    if (lane == 0) {
+      reinterpret_cast<unsigned long long*>(dP)[warp] = best_i >= 0 ? argmax_key(best_v, best_i) : 0ull;
+      reinterpret_cast<int*>(dA)[warp] = bad;
+    }
+    alive = cbar_and(alive);
+    if (alive && t == 0) {
+      unsigned long long k = 0;
+      int anybad = 0;
+      for (int i = 0; i < NCW; ++i) {
+        const unsigned long long ki = reinterpret_cast<unsigned long long*>(dP)[i];
+        k = ki > k ? ki : k;
+        anybad |= reinterpret_cast<int*>(dA)[i];
+      }
+      if (k) atomicMax(p.key, k);
+      if (anybad) atomicOr(p.err, ERR_NONFINITE);
+    }
+    tl_mark(p, ph_idx++, 2);
+    alive = alive && grid_sync(p, base, nb, s_flag);
+    if (alive && blockIdx.x == 0 && t == 0) {
+      const unsigned long long k = atomicAdd(p.key, 0ull);
+      const int idx = argmax_key_index(k);
+      *p.tok = idx;
+      const int hn = __ldcg(p.hist_n);
+      if (hn < p.hist_cap) p.hist[hn] = idx;
+      *p.hist_n = hn + 1;
+      *p.pos = pos + 1;
+      *p.key = 0ull;
+      *p.bar_base = base + (unsigned long long)nb * gridDim.x;  // every CTA has arrived nb times
+    }
+  }
+  if (!alive && blockIdx.x == 0 && t == 0) {
+    // after an abort the counter is left in an unknown state: the next step starts from it
+    __threadfence();
+  }
+}
+
+}  // namespace mk
+
+// ---- host side ---------------------------------------------------------------------------
+
+bool megastep_supported(const Dims& d, int nsm) {
+  if (d.dtype != 1) return false;
+  if (d.hd != 64 && d.hd != 128) return false;
+  if (d.nq / d.nkv > mk::GMAX || d.nq * d.hd != d.H) return false;
+  if (d.H % 8 || d.H > mk::XS_FLOATS || d.H > 8 * 32 * mk::MAXV) return false;
+  if (d.nq > 32) return false;  // merge weights [2][nq][NSPLIT] of 32 heads at most
+  if (d.I % 8 || (size_t)d.I * 2 > (size_t)mk::SLOT) return false;
+  if (((d.I / 8 + mk::NCW - 1) / mk::NCW + 31) / 32 > mk::MAXD) return false;
+  const int R = std::min(mk::NCW, (mk::SLOT / (2 * d.H)) & ~1);
+  if (R < 2) return false;
+  const int pairs = (d.nq + 2 * d.nkv) * d.hd / 2;
+  auto per_cta = [&](int n) { return (n + nsm - 1) / nsm; };
+  if (per_cta(pairs) > mk::MAX_LOCAL || per_cta(d.I) > mk::MAX_LOCAL || per_cta(d.H) > 64) return false;
+  if (d.nkv * mk::NSPLIT > nsm) return false;
+  return true;
+}
+
+size_t megastep_smem(int hd) { return hd == 128 ? mk::Smem<128>::ALLOC : mk::Smem<64>::ALLOC; }
+
+size_t megastep_part_bytes(const Dims& d) {
+  return (size_t)d.nq * mk::NSPLIT * attn_part_stride(d.hd) * sizeof(float);
+}
+
+cudaError_t megastep_set_attributes(int hd) {
+  if (hd == 128)
+    return cudaFuncSetAttribute(mk::decode_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)mk::Smem<128>::ALLOC);
+  return cudaFuncSetAttribute(mk::decode_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)mk::Smem<64>::ALLOC);
+}
+
+int megastep_threads() { return mk::THREADS; }
+
+cudaError_t megastep_occupancy(int hd, int* per_sm) {
+  if (hd == 128)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk::decode_step_kernel<128>, mk::THREADS,
+                                                         mk::Smem<128>::ALLOC);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk::decode_step_kernel<64>, mk::THREADS,
+                                                       mk::Smem<64>::ALLOC);
+}
+
+size_t megastep_layer_bytes() { return sizeof(mk::LayerW); }
+
+void megastep_fill_layer(void* dst, const LayerPtrs& w) {
+  mk::LayerW lw{(const bf16*)w.in_norm, (const bf16*)w.wq, (const bf16*)w.wk, (const bf16*)w.wv,
+                (const bf16*)w.bq, (const bf16*)w.bk, (const bf16*)w.bv, (const bf16*)w.wo,
+                (const bf16*)w.post_norm, (const bf16*)w.w_gate, (const bf16*)w.w_up, (const bf16*)w.w_down};
+  std::memcpy(dst, &lw, sizeof(lw));
+}
+
+cudaError_t launch_megastep(const MegaLaunch& a, cudaStream_t s) {
+  mk::Params p{};
+  p.layers = (const mk::LayerW*)a.layers_dev;
+  p.L = a.d.L; p.H = a.d.H; p.nq = a.d.nq; p.nkv = a.d.nkv; p.I = a.d.I; p.V = a.d.V; p.cap = a.d.cap;
+  p.eps = a.d.eps;
+  p.embed = (const bf16*)a.embed; p.final_norm = (const bf16*)a.final_norm; p.head = (const bf16*)a.head;
+  p.rope = a.rope; p.kv = (f16*)a.kv_seq;
+  p.x = a.x; p.q = a.q; p.act = a.act; p.logits = a.logits; p.part = a.part;
+  p.tok = a.tok; p.pos = a.pos; p.key = a.key; p.hist = a.hist; p.hist_n = a.hist_n; p.hist_cap = a.hist_cap;
+  p.bar = a.bar; p.bar_base = a.bar_base; p.abort = a.abort; p.err = a.err; p.tl = a.tl;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(mk::THREADS);
+  cfg.dynamicSmemBytes = megastep_smem(a.d.hd);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.d.hd == 128) return cudaLaunchKernelEx(&cfg, mk::decode_step_kernel<128>, p);
+  return cudaLaunchKernelEx(&cfg, mk::decode_step_kernel<64>, p);
+}
+
+}  // namespace qw

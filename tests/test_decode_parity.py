@@ -55,6 +55,40 @@ def test_small_shapes_teacher_forced(shape_name, P, n_new, cap):
         m.close()
 
 
+@pytest.mark.parametrize("shape_name,P,n_new,cap", [
+    ("small_bf16", 100, 12, 160),
+    ("hd128_bf16", 150, 12, 200),
+    ("untied_bf16", 45, 12, 64),
+])
+def test_one_kernel_per_operation_path(monkeypatch, shape_name, P, n_new, cap):
+    """bf16 decode steps as one kernel per operation (QW_MEGA=0) instead of the persistent
+    decode-step kernel: the same parity."""
+    monkeypatch.setenv("QW_MEGA", "0")
+    w, prompt, toks, logits = oracle_run(shape_name, P, n_new)
+    m = _model(shape_name, w, cap)
+    try:
+        assert m.decode_kernels_per_step() == 5 * SHAPES[shape_name].n_layers + 2
+        rep = run_teacher_forced(m, SHAPES[shape_name], prompt, toks, logits)
+        assert rep.steps == n_new
+    finally:
+        m.close()
+
+
+def test_persistent_step_kernel_is_the_default_for_bf16():
+    w, prompt, toks, logits = oracle_run("hd128_bf16", 150, 12)
+    m = _model("hd128_bf16", w, 200)
+    try:
+        assert m.decode_kernels_per_step() == 1
+    finally:
+        m.close()
+    wt, _, _, _ = oracle_run("tiny", 8, 8)
+    m = _model("tiny", wt, 16)
+    try:
+        assert m.decode_kernels_per_step() == 5 * SHAPES["tiny"].n_layers + 2  # fp32: one per operation
+    finally:
+        m.close()
+
+
 def test_tiny_without_graphs_matches(monkeypatch):
     monkeypatch.setenv("QW_NO_GRAPH", "1")
     w, prompt, toks, logits = oracle_run("tiny", 8, 8)
