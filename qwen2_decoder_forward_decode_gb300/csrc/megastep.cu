@@ -293,12 +293,40 @@ __device__ void producer(const Params& p, unsigned char* smem, uint32_t full0, u
           prefetch_l2_bulk(kc + (size_t)p.nkv * p.cap * HD + off, bytes);
         }
       }
+      const LayerW& w = p.layers[l];
+      if (pw == 0) {  // small per-layer vectors every CTA reads (a few CTAs ask for them)
+        const uint32_t hb = (uint32_t)p.H * 2;
+        switch (blockIdx.x) {
+          case 0: prefetch_l2_bulk(w.in_norm, hb); break;
+          case 1: prefetch_l2_bulk(w.post_norm, hb); break;
+          case 2: if (w.bq) prefetch_l2_bulk(w.bq, (uint32_t)p.nq * HD * 2); break;
+          case 3: if (w.bk) prefetch_l2_bulk(w.bk, (uint32_t)p.nkv * HD * 2); break;
+          case 4: if (w.bv) prefetch_l2_bulk(w.bv, (uint32_t)p.nkv * HD * 2); break;
+          case 5: if (l == 0) prefetch_l2_bulk(p.rope + (size_t)(ctx - 1) * (HD / 2), HD * 4); break;
+          default: break;
+        }
+      }
       const int phs[4] = {P_QKV, P_OPROJ, P_GATEUP, P_DOWN};
       for (int k = 0; k < 4 && ok; ++k) {
+        if (phs[k] == P_GATEUP && pw == 0) {
+          // the ring now runs ahead into this layer's MLP while the consumers are in the
+          // latency-bound attention chain: ask L2 for this CTA's gate, up and down rows so
+          // that HBM keeps streaming once the ring is full
+          int a0, a1;
+          block_of(p.I, a0, a1);
+          if (a1 > a0) {
+            const uint32_t gb = (uint32_t)(a1 - a0) * p.H * 2;
+            prefetch_l2_bulk(w.wg + (size_t)a0 * p.H, gb);
+            prefetch_l2_bulk(w.wu + (size_t)a0 * p.H, gb);
+          }
+          block_of(p.H, a0, a1);
+          if (a1 > a0) prefetch_l2_bulk(w.wd + (size_t)a0 * p.I, (uint32_t)(a1 - a0) * p.I * 2);
+        }
         ok = phase_units(p, HD, l, phs[k], issue);
         if (ok && aborted(p)) ok = false;
       }
     } else {
+      if (pw == 0 && blockIdx.x == 0) prefetch_l2_bulk(p.final_norm, (uint32_t)p.H * 2);
       ok = phase_units(p, HD, l, P_LM, issue);
     }
   }
@@ -396,8 +424,8 @@ __device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int
   if (threadIdx.x == 0) {
     int ok = 0;
     if (!aborted(p)) {
-      __threadfence();
-      atomicAdd(p.bar, 1ull);
+      // release: this CTA's writes of the phase (ordered before by the consumer barrier)
+      asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar), "l"(1ull) : "memory");
       const unsigned long long target = base + (unsigned long long)nb * gridDim.x;
       const long long t0 = clock64();
       ok = 1;
@@ -428,6 +456,47 @@ __device__ __forceinline__ void tl_mark(const Params& p, int k, int which) {
 // heads of the KV head are the rows of the A operand, fp16 q scaled by 1/sqrt(hd)), keeping a
 // running maximum and sum per row; the two warps' states are combined into the chunk's
 // partial (unnormalised output, maximum, sum), which the o_proj phase merges.
+// Copies of tile tt's K and V rows into the tile buffers (cp.async; rows past the chunk are
+// zero). With skip_newest the newest position of the context (written by this step's q/k/v
+// phase) is left out: the first tile's other rows were written by earlier steps and are
+// requested before the grid barrier.
+template <int HD>
+__device__ __forceinline__ void att_tile_load(f16* Ks, f16* Vs, const f16* kc, const f16* vc, int tt, int n,
+                                              int newest, bool skip_newest) {
+  constexpr int KS = HD + 8;
+  constexpr int NV = AT_K * HD / 8;  // 16-byte vectors of a K (or V) tile
+  for (int i = threadIdx.x; i < 2 * NV; i += NCT) {
+    const int which = i >= NV, idx = i - which * NV;
+    const int j = idx / (HD / 8), c8 = idx - j * (HD / 8);
+    f16* dst = (which ? Vs : Ks) + j * KS + c8 * 8;
+    const int key = tt * AT_K + j;
+    if (key >= n) *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    else if (!(skip_newest && key == newest)) cp_async16(dst, (which ? vc : kc) + (size_t)key * HD + c8 * 8);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int HD>
+__device__ __forceinline__ void att_rows(const Params& p, int l, int g, int c, int chunk, int ctx, const f16*& kc,
+                                         const f16*& vc, int& n, int& newest) {
+  const int j0 = c * chunk, j1 = min(ctx, j0 + chunk);
+  n = j1 - j0;
+  newest = j1 == ctx ? n - 1 : -1;  // chunk-relative position of the newest row, if in this chunk
+  kc = p.kv + (size_t)l * 2 * p.nkv * p.cap * HD + ((size_t)g * p.cap + j0) * HD;
+  vc = kc + (size_t)p.nkv * p.cap * HD;
+}
+
+// the first tile's rows written by earlier steps, before the grid barrier
+template <int HD>
+__device__ void attention_preload(const Params& p, unsigned char* att, int l, int g, int c, int chunk, int ctx) {
+  f16* Ks = reinterpret_cast<f16*>(att);
+  f16* Vs = Ks + AT_K * (HD + 8);
+  const f16 *kc, *vc;
+  int n, newest;
+  att_rows<HD>(p, l, g, c, chunk, ctx, kc, vc, n, newest);
+  att_tile_load<HD>(Ks, Vs, kc, vc, 0, n, newest, true);
+}
+
 template <int HD>
 __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int g, int c, int chunk, int ctx) {
   constexpr int KS = HD + 8, NKK = HD / 16, NNT = HD / 8;
@@ -435,9 +504,17 @@ __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int 
   const int G = p.nq / p.nkv;
   f16* Ks = reinterpret_cast<f16*>(att);
   f16* Vs = Ks + AT_K * KS;
-  const int j0 = c * chunk, j1 = min(ctx, j0 + chunk), n = j1 - j0;
-  const f16* kc = p.kv + (size_t)l * 2 * p.nkv * p.cap * HD + ((size_t)g * p.cap + j0) * HD;
-  const f16* vc = kc + (size_t)p.nkv * p.cap * HD;
+  const f16 *kc, *vc;
+  int n, newest;
+  att_rows<HD>(p, l, g, c, chunk, ctx, kc, vc, n, newest);
+  // the first tile's newest row (the rest was requested before the barrier)
+  if (newest >= 0 && newest < AT_K) {
+    for (int i = t; i < 2 * (HD / 8); i += NCT) {
+      const int which = i >= HD / 8, c8 = i - which * (HD / 8);
+      cp_async16((which ? Vs : Ks) + newest * KS + c8 * 8, (which ? vc : kc) + (size_t)newest * HD + c8 * 8);
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   const float scale = rsqrtf((float)HD);
   uint32_t qa[NKK][4];
   if (warp < 2) {
@@ -460,16 +537,7 @@ __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int 
   const int ntiles = (n + AT_K - 1) / AT_K;
   const int kw = 16 * warp;
   for (int tt = 0; tt < ntiles; ++tt) {
-    constexpr int NV = AT_K * HD / 8;  // 16-byte vectors of a K (or V) tile
-    for (int i = t; i < 2 * NV; i += NCT) {
-      const int which = i >= NV, idx = i - which * NV;
-      const int j = idx / (HD / 8), c8 = idx - j * (HD / 8);
-      f16* dst = (which ? Vs : Ks) + j * KS + c8 * 8;
-      const int key = tt * AT_K + j;
-      if (key < n) cp_async16(dst, (which ? vc : kc) + (size_t)key * HD + c8 * 8);
-      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
+    if (tt > 0) att_tile_load<HD>(Ks, Vs, kc, vc, tt, n, newest, false);
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     cbar();
     if (warp < 2 && tt * AT_K + kw < n) {
@@ -695,11 +763,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   const int nvecH = p.H >> 3;
   int chunk, ns;
   att_chunks(ctx, chunk, ns);
-  {  // the residual stream starts as the embedding row (each CTA writes its own rows)
-    int r0, r1;
-    block_of(p.H, r0, r1);
-    for (int r = r0 + t; r < r1; r += NCT) p.x[r] = __bfloat162float(erow[r]);
-  }
+  // The residual rows this CTA updates (o_proj and down rows r0 + t, one per thread) stay
+  // in a register; the stream starts as the embedding row.
+  int r0, r1;
+  block_of(p.H, r0, r1);
+  const bool own = t < r1 - r0;
+  float xown = own ? __bfloat162float(erow[r0 + t]) : 0.f;
+  if (own) p.x[r0 + t] = xown;
   float xr[MAXV][8];
   bool alive = true;
   int ph_idx = 0;  // timeline index
@@ -778,6 +848,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         store_kv(dst + e_i + half, b, p.err);
       }
     }
+    if (alive && (int)blockIdx.x < p.nkv * ns) {
+      const int g = blockIdx.x / ns, c = blockIdx.x - g * ns;
+      attention_preload<HD>(p, att, l, g, c, chunk, ctx);
+    }
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag);
     if (!alive) break;
@@ -809,7 +883,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
     if (alive)
-      for (int r = i0 + t; r < i1; r += NCT) p.x[r] = __ldcg(p.x + r) + dA[r - i0];
+      if (own) {
+        xown += dA[t];
+        p.x[r0 + t] = xown;
+      }
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag);
     if (!alive) break;
@@ -878,11 +955,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
     if (alive)
-      for (int r = i0 + t; r < i1; r += NCT) {
+      if (own) {
         float s = 0.f;
 #pragma unroll
-        for (int k = 0; k < NCW; ++k) s += dP[(r - i0) * NCW + k];  // warp order
-        p.x[r] = __ldcg(p.x + r) + s;
+        for (int k = 0; k < NCW; ++k) s += dP[t * NCW + k];  // warp order
+        xown += s;
+        p.x[r0 + t] = xown;
       }
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag);
@@ -940,10 +1018,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       *p.bar_base = base + (unsigned long long)nb * gridDim.x;  // every CTA has arrived nb times
     }
   }
-  if (!alive && blockIdx.x == 0 && t == 0) {
-    // after an abort the counter is left in an unknown state: the next step starts from it
-    __threadfence();
-  }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // (copies are only left after an abort)
 }
 
 }  // namespace mk
