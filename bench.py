@@ -231,20 +231,26 @@ def timeline_persistent(m, s, ids_dev, prompt, rank):
     m.set_timeline(True)
     m.prefill_device(ids_dev.data_ptr(), len(prompt))
     kinds = ["qkv", "attn", "o_proj", "gate_up", "down"] * s.n_layers + ["lm_head"]
-    st = {k: {"units_us": [], "run_us": [], "barrier_us": []} for k in set(kinds)}
+    n = len(kinds)
+    fields = ("staged_us", "units_us", "run_us", "skew_us", "barrier_us")
+    st = {k: {f: [] for f in fields} for k in set(kinds)}
     tot = []
     for i in range(12):
         m.decode_steps(1)
-        tl = m.read_timeline().astype(np.int64)[:len(kinds)]
+        full = m.read_timeline().astype(np.int64)
+        tl, t2 = full[:n], full[n:2 * n]
         if i < 2:
             continue
         tot.append((tl[-1, 2] - tl[0, 0]) / 1000.0)
         for j, k in enumerate(kinds):
             if k != "attn":
+                st[k]["staged_us"].append((t2[j, 0] - tl[j, 0]) / 1000.0)
                 st[k]["units_us"].append((tl[j, 1] - tl[j, 0]) / 1000.0)
             st[k]["run_us"].append((tl[j, 2] - tl[j, 0]) / 1000.0)
-            if j + 1 < len(kinds):
-                st[k]["barrier_us"].append((tl[j + 1, 0] - tl[j, 2]) / 1000.0)
+            if j + 1 < n:
+                # CTA 0's phase end -> the last CTA's arrival -> CTA 0 past the barrier
+                st[k]["skew_us"].append((t2[j, 2] - tl[j, 2]) / 1000.0)
+                st[k]["barrier_us"].append((t2[j, 1] - t2[j, 2]) / 1000.0)
     m.set_timeline(False)
     out = {"persistent_step_us": float(np.mean(tot)), "phases": {
         k: {f: round(float(np.mean(x)), 3) if x else None for f, x in v.items()} for k, v in st.items()}}

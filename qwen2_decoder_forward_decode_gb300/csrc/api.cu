@@ -218,6 +218,15 @@ struct qw_model {
     a.err = err;
     a.tl = tl_buf;
     a.grid = d.nsm;
+    static const int pf = [] {
+      const char* v = std::getenv("QW_MK_PF");
+      return v ? std::atoi(v) : 1;
+    }();
+    a.pf_mode = pf;
+    if (tl_buf) {  // atomicMax stamps start from zero
+      cudaError_t e = cudaMemsetAsync(tl_buf, 0, sizeof(unsigned long long) * 3 * tl_n, stream);
+      if (e) return e;
+    }
     return launch_megastep(a, stream);
   }
 
@@ -898,6 +907,7 @@ qw_status qw_set_timeline(qw_model* m, int32_t enable) {
   }
   if (!enable) return QW_OK;
   m->tl_n = 1 + 5 * m->d.L + 1;
+  if (m->use_mega) m->tl_n = std::max(m->tl_n, 2 * (5 * m->d.L + 1));  // two records per phase
   if (m->use_batched) m->tl_n = std::max(m->tl_n, 3 + 10 * m->d.L);  // launches of a batched step
   m->tl_init.assign((size_t)3 * m->tl_n, ~0ull);
   for (int i = 0; i < m->tl_n; ++i) m->tl_init[3 * i + 2] = 0ull;

@@ -124,8 +124,11 @@ struct MegaLaunch {
   int hist_cap;
   unsigned long long *bar, *bar_base;  // grid-barrier counter and its value at the step start
   int *abort, *err;
-  unsigned long long* tl;          // per phase [start, units done, end] or null
+  unsigned long long* tl;          // per phase [start, units done, end], then per phase [input
+                                   // staged, barrier passed, last arrival], or null
   int grid;
+  int pf_mode;                     // when the MLP rows are requested into L2 (0 never, 1 at the
+                                   // attention phase, 2 at the o_proj phase, 3 by the producers)
 };
 bool megastep_supported(const Dims& d, int nsm);
 size_t megastep_smem(int hd);

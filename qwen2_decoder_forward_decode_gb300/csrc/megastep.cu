@@ -79,6 +79,8 @@ struct Params {
   int* abort;                // nonzero: a wait gave up somewhere
   int* err;
   unsigned long long* tl;    // timeline: per phase [start, units done, end] (CTA 0), or null
+  int pf_mode;               // when the MLP rows are asked into L2: 0 never, 1 attention start,
+                             // 2 o_proj start, 3 when the producers reach them
 };
 
 template <int HD>
@@ -246,6 +248,20 @@ __device__ __forceinline__ void att_chunks(int ctx, int& chunk, int& ns) {
   ns = (ctx + chunk - 1) / chunk;
 }
 
+// L2 requests of this CTA's gate, up and down rows of layer l (they are read by the ring
+// later; asking early keeps HBM streaming while the consumers are in the attention chain)
+__device__ __forceinline__ void mlp_l2_ahead(const Params& p, const LayerW& w) {
+  int a0, a1;
+  block_of(p.I, a0, a1);
+  if (a1 > a0) {
+    const uint32_t gb = (uint32_t)(a1 - a0) * p.H * 2;
+    prefetch_l2_bulk(w.wg + (size_t)a0 * p.H, gb);
+    prefetch_l2_bulk(w.wu + (size_t)a0 * p.H, gb);
+  }
+  block_of(p.H, a0, a1);
+  if (a1 > a0) prefetch_l2_bulk(w.wd + (size_t)a0 * p.I, (uint32_t)(a1 - a0) * p.I * 2);
+}
+
 // ---- producers -----------------------------------------------------------------------
 
 template <int HD>
@@ -308,20 +324,7 @@ __device__ void producer(const Params& p, unsigned char* smem, uint32_t full0, u
       }
       const int phs[4] = {P_QKV, P_OPROJ, P_GATEUP, P_DOWN};
       for (int k = 0; k < 4 && ok; ++k) {
-        if (phs[k] == P_GATEUP && pw == 0) {
-          // the ring now runs ahead into this layer's MLP while the consumers are in the
-          // latency-bound attention chain: ask L2 for this CTA's gate, up and down rows so
-          // that HBM keeps streaming once the ring is full
-          int a0, a1;
-          block_of(p.I, a0, a1);
-          if (a1 > a0) {
-            const uint32_t gb = (uint32_t)(a1 - a0) * p.H * 2;
-            prefetch_l2_bulk(w.wg + (size_t)a0 * p.H, gb);
-            prefetch_l2_bulk(w.wu + (size_t)a0 * p.H, gb);
-          }
-          block_of(p.H, a0, a1);
-          if (a1 > a0) prefetch_l2_bulk(w.wd + (size_t)a0 * p.I, (uint32_t)(a1 - a0) * p.I * 2);
-        }
+        if (phs[k] == P_GATEUP && pw == 0 && p.pf_mode == 3) mlp_l2_ahead(p, w);
         ok = phase_units(p, HD, l, phs[k], issue);
         if (ok && aborted(p)) ok = false;
       }
@@ -418,7 +421,7 @@ __device__ void stage_norm(const Params& p, float* xs, float* scr, const float* 
 
 // Grid barrier of the consumers of all CTAs: each CTA adds one to a monotonic counter and
 // waits until it reaches base + nb * CTAs. Returns false (uniformly) after an abort.
-__device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int* s_flag) {
+__device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int* s_flag, int k) {
   cbar();
   ++nb;
   if (threadIdx.x == 0) {
@@ -426,6 +429,7 @@ __device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int
     if (!aborted(p)) {
       // release: this CTA's writes of the phase (ordered before by the consumer barrier)
       asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar), "l"(1ull) : "memory");
+      if (p.tl) atomicMax(p.tl + 3 * (5 * p.L + 1 + k) + 2, gtime());  // the last CTA's arrival
       const unsigned long long target = base + (unsigned long long)nb * gridDim.x;
       const long long t0 = clock64();
       ok = 1;
@@ -440,6 +444,7 @@ __device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int
       }
     }
     *s_flag = ok;
+    if (p.tl && blockIdx.x == 0) p.tl[3 * (5 * p.L + 1 + k) + 1] = gtime();
   }
   cbar();
   return *(volatile int*)s_flag != 0;
@@ -448,6 +453,12 @@ __device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int
 __device__ __forceinline__ void tl_mark(const Params& p, int k, int which) {
   if (p.tl && blockIdx.x == 0 && threadIdx.x == 0) p.tl[3 * k + which] = gtime();
 }
+// second timeline record of phase k: [0] input staged, [1] barrier passed (CTA 0), [2] the
+// last CTA's arrival at the barrier after the phase
+__device__ __forceinline__ void tl_mark2(const Params& p, int k) {
+  if (p.tl && blockIdx.x == 0 && threadIdx.x == 0) p.tl[3 * (5 * p.L + 1 + k)] = gtime();
+}
+
 
 // ---- attention of one (KV head, chunk) -----------------------------------------------------
 //
@@ -814,6 +825,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     }
     stage_norm(p, xs, scr, p.x, l == 0 ? erow : nullptr, w.in_norm);
     load_xr(xr, xs, nvecH, lane);
+    tl_mark2(p, ph_idx);
     {
       const int R = rows_per_slot(p.H);
       const int hp = R / 2;
@@ -853,22 +865,25 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       attention_preload<HD>(p, att, l, g, c, chunk, ctx);
     }
     tl_mark(p, ph_idx++, 2);
-    alive = alive && grid_sync(p, base, nb, s_flag);
+    alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (!alive) break;
 
     // ===== ATTN: (KV head, chunk) partials
     tl_mark(p, ph_idx, 0);
+    if (p.pf_mode == 1 && t == 0) mlp_l2_ahead(p, w);
     if ((int)blockIdx.x < p.nkv * ns) {
       const int g = blockIdx.x / ns, c = blockIdx.x - g * ns;
       attention_chunk<HD>(p, att, l, g, c, chunk, ctx);
     }
     tl_mark(p, ph_idx++, 2);
-    if (!grid_sync(p, base, nb, s_flag)) { alive = false; break; }
+    if (!grid_sync(p, base, nb, s_flag, ph_idx - 1)) { alive = false; break; }
 
     // ===== OPROJ: merge -> x += Wo o
     tl_mark(p, ph_idx, 0);
+    if (p.pf_mode == 2 && t == 0) mlp_l2_ahead(p, w);
     stage_merge<HD>(p, xs, mwv, ns);
     load_xr(xr, xs, (p.nq * HD) >> 3, lane);
+    tl_mark2(p, ph_idx);
     block_of(p.H, i0, i1);
     {
       const int R = rows_per_slot(p.H);
@@ -888,13 +903,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         p.x[r0 + t] = xown;
       }
     tl_mark(p, ph_idx++, 2);
-    alive = alive && grid_sync(p, base, nb, s_flag);
+    alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (!alive) break;
 
     // ===== GATEUP: RMSNorm -> gate/up rows -> SwiGLU
     tl_mark(p, ph_idx, 0);
     stage_norm(p, xs, scr, p.x, nullptr, w.post_norm);
     load_xr(xr, xs, nvecH, lane);
+    tl_mark2(p, ph_idx);
     block_of(p.I, i0, i1);
     {
       const int R = rows_per_slot(p.H);
@@ -917,7 +933,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         p.act[i] = (gv / (1.f + expf(-gv))) * uv;
       }
     tl_mark(p, ph_idx++, 2);
-    alive = alive && grid_sync(p, base, nb, s_flag);
+    alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (!alive) break;
 
     // ===== DOWN: x += Wd act, each row's K split over the eight warps
@@ -939,6 +955,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         xd[qd][4] = b.x; xd[qd][5] = b.y; xd[qd][6] = b.z; xd[qd][7] = b.w;
       }
       block_of(p.H, i0, i1);
+      tl_mark2(p, ph_idx);
       auto fn = [&](const unsigned char* slot, const Unit& un) {
         const uint4* r = reinterpret_cast<const uint4*>(slot);
         float acc = 0.f;
@@ -963,7 +980,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         p.x[r0 + t] = xown;
       }
     tl_mark(p, ph_idx++, 2);
-    alive = alive && grid_sync(p, base, nb, s_flag);
+    alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
   }
 
   // ===== LM head: final RMSNorm -> logits -> greedy argmax
@@ -971,6 +988,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     tl_mark(p, ph_idx, 0);
     stage_norm(p, xs, scr, p.x, nullptr, p.final_norm);
     load_xr(xr, xs, nvecH, lane);
+    tl_mark2(p, ph_idx);
     float best_v = -INFINITY;
     int best_i = -1;
     bool bad = false;
@@ -1005,7 +1023,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       if (anybad) atomicOr(p.err, ERR_NONFINITE);
     }
     tl_mark(p, ph_idx++, 2);
-    alive = alive && grid_sync(p, base, nb, s_flag);
+    alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (alive && blockIdx.x == 0 && t == 0) {
       const unsigned long long k = atomicAdd(p.key, 0ull);
       const int idx = argmax_key_index(k);
@@ -1085,6 +1103,7 @@ cudaError_t launch_megastep(const MegaLaunch& a, cudaStream_t s) {
   p.x = a.x; p.q = a.q; p.act = a.act; p.logits = a.logits; p.part = a.part;
   p.tok = a.tok; p.pos = a.pos; p.key = a.key; p.hist = a.hist; p.hist_n = a.hist_n; p.hist_cap = a.hist_cap;
   p.bar = a.bar; p.bar_base = a.bar_base; p.abort = a.abort; p.err = a.err; p.tl = a.tl;
+  p.pf_mode = a.pf_mode;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(mk::THREADS);
