@@ -232,28 +232,43 @@ def timeline_persistent(m, s, ids_dev, prompt, rank):
     m.prefill_device(ids_dev.data_ptr(), len(prompt))
     kinds = ["qkv", "attn", "o_proj", "gate_up", "down"] * s.n_layers + ["lm_head"]
     n = len(kinds)
-    fields = ("staged_us", "units_us", "run_us", "skew_us", "barrier_us")
+    fields = ("staged_us", "first_unit_us", "units_us", "epi_start_us", "run_us", "skew_us", "barrier_us")
     st = {k: {f: [] for f in fields} for k in set(kinds)}
     tot = []
+    spread = {k: [] for k in ("qkv", "attn", "o_proj", "gate_up", "down")}
+    late = {k: {} for k in spread}
+    import torch
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
     for i in range(12):
         m.decode_steps(1)
         full = m.read_timeline().astype(np.int64)
-        tl, t2 = full[:n], full[n:2 * n]
+        tl, t2, t3 = full[:n], full[n:2 * n], full[2 * n:3 * n]
+        flat = full.reshape(-1)
         if i < 2:
             continue
         tot.append((tl[-1, 2] - tl[0, 0]) / 1000.0)
         for j, k in enumerate(kinds):
             if k != "attn":
                 st[k]["staged_us"].append((t2[j, 0] - tl[j, 0]) / 1000.0)
+                st[k]["first_unit_us"].append((t3[j, 0] - tl[j, 0]) / 1000.0)
                 st[k]["units_us"].append((tl[j, 1] - tl[j, 0]) / 1000.0)
+                st[k]["epi_start_us"].append((t3[j, 1] - tl[j, 0]) / 1000.0)
             st[k]["run_us"].append((tl[j, 2] - tl[j, 0]) / 1000.0)
             if j + 1 < n:
                 # CTA 0's phase end -> the last CTA's arrival -> CTA 0 past the barrier
                 st[k]["skew_us"].append((t2[j, 2] - tl[j, 2]) / 1000.0)
                 st[k]["barrier_us"].append((t2[j, 1] - t2[j, 2]) / 1000.0)
+        if len(flat) >= 9 * n + 5 * nsm:  # every CTA's arrival after layer 1's phases
+            for kk, k in enumerate(("qkv", "attn", "o_proj", "gate_up", "down")):
+                arr = flat[9 * n + kk * nsm: 9 * n + (kk + 1) * nsm]
+                spread[k].append((arr.max() - arr.min()) / 1000.0)
+                for b in np.argsort(arr)[-4:]:
+                    late[k][int(b)] = late[k].get(int(b), 0) + 1
     m.set_timeline(False)
     out = {"persistent_step_us": float(np.mean(tot)), "phases": {
-        k: {f: round(float(np.mean(x)), 3) if x else None for f, x in v.items()} for k, v in st.items()}}
+        k: {f: round(float(np.mean(x)), 3) if x else None for f, x in v.items()} for k, v in st.items()},
+        "layer1_arrival_spread_us": {k: round(float(np.mean(v)), 3) if v else None for k, v in spread.items()},
+        "layer1_latest_ctas": {k: sorted(v.items(), key=lambda kv: -kv[1])[:6] for k, v in late.items()}}
     if rank == 0:
         print(json.dumps(out), flush=True)
 

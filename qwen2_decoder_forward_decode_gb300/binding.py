@@ -259,7 +259,9 @@ class Model:
 
     def read_timeline(self):
         """[(start_ns, wait_released_ns, end_ns)] per kernel of the last decode step."""
-        n_max = 3 + 10 * self.shape.n_layers  # a batched step launches the most kernels
+        # a batched step launches the most kernels; the persistent step kernel writes three
+        # records per phase and per-CTA barrier arrivals
+        n_max = max(3 + 10 * self.shape.n_layers, 3 * (5 * self.shape.n_layers + 1) + 1024)
         buf = (ctypes.c_uint64 * (3 * n_max))()
         n = np.zeros(1, dtype=np.int32)
         check(lib().qw_read_timeline(self.h, buf, n_max, _iptr(n)))

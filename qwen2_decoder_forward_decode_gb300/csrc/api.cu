@@ -220,7 +220,7 @@ struct qw_model {
     a.grid = d.nsm;
     static const int pf = [] {
       const char* v = std::getenv("QW_MK_PF");
-      return v ? std::atoi(v) : 1;
+      return v ? std::atoi(v) : 0;
     }();
     a.pf_mode = pf;
     if (tl_buf) {  // atomicMax stamps start from zero
@@ -597,8 +597,8 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
     int coop = 0, per_sm = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device);
     if (!(mv && mv[0] == '0') && coop && megastep_supported(d, d.nsm)) {
-      if ((e = megastep_set_attributes(d.hd))) return bail(e, "decode step attributes");
-      if ((e = megastep_occupancy(d.hd, &per_sm))) return bail(e, "decode step occupancy");
+      if ((e = megastep_set_attributes(d))) return bail(e, "decode step attributes");
+      if ((e = megastep_occupancy(d, &per_sm))) return bail(e, "decode step occupancy");
     }
     if (per_sm >= 1) {
       std::vector<unsigned char> recs(megastep_layer_bytes() * d.L);
@@ -907,7 +907,8 @@ qw_status qw_set_timeline(qw_model* m, int32_t enable) {
   }
   if (!enable) return QW_OK;
   m->tl_n = 1 + 5 * m->d.L + 1;
-  if (m->use_mega) m->tl_n = std::max(m->tl_n, 2 * (5 * m->d.L + 1));  // two records per phase
+  if (m->use_mega)  // three records per phase, then every CTA's arrival after layer 1's phases
+    m->tl_n = std::max(m->tl_n, 3 * (5 * m->d.L + 1) + (5 * m->d.nsm + 2) / 3);
   if (m->use_batched) m->tl_n = std::max(m->tl_n, 3 + 10 * m->d.L);  // launches of a batched step
   m->tl_init.assign((size_t)3 * m->tl_n, ~0ull);
   for (int i = 0; i < m->tl_n; ++i) m->tl_init[3 * i + 2] = 0ull;

@@ -131,11 +131,11 @@ struct MegaLaunch {
                                    // attention phase, 2 at the o_proj phase, 3 by the producers)
 };
 bool megastep_supported(const Dims& d, int nsm);
-size_t megastep_smem(int hd);
+size_t megastep_smem(const Dims& d);
 size_t megastep_part_bytes(const Dims& d);
-cudaError_t megastep_set_attributes(int hd);
+cudaError_t megastep_set_attributes(const Dims& d);
 int megastep_threads();
-cudaError_t megastep_occupancy(int hd, int* per_sm);  // resident CTAs per SM
+cudaError_t megastep_occupancy(const Dims& d, int* per_sm);  // resident CTAs per SM
 size_t megastep_layer_bytes();
 void megastep_fill_layer(void* dst, const LayerPtrs& w);
 cudaError_t launch_megastep(const MegaLaunch& a, cudaStream_t s);

@@ -62,6 +62,27 @@ struct LayerW {
   const bf16 *in_norm, *wq, *wk, *wv, *bq, *bk, *bv, *wo, *post_norm, *wg, *wu, *wd;
 };
 
+// Shared-memory layout (byte offsets from the 1024-aligned base), sized for the model.
+struct Layout {
+  uint32_t att, xs, da, db, dp, mw, lt, bar, scr, total;
+};
+__host__ __device__ inline uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
+inline Layout make_layout(int hd, int H, int nq, int L) {
+  Layout o;
+  uint32_t off = (uint32_t)NS * SLOT;  // the ring
+  o.att = off; off += align16(2u * AT_K * (hd + 8) * 2);  // K and V tiles (the combine reuses them)
+  o.xs = off; off += align16((uint32_t)H * 4);
+  o.da = off; off += MAX_LOCAL * 4;
+  o.db = off; off += MAX_LOCAL * 4;
+  o.dp = off; off += 64 * NCW * 4;                       // DOWN partials [rows][warps]
+  o.mw = off; off += align16(2u * nq * NSPLIT * 4);      // merge (m, weight) and l
+  o.lt = off; off += align16((uint32_t)L * sizeof(LayerW));  // the layer pointer table
+  o.bar = off; off += 2 * NS * 8;
+  o.scr = off; off += 64 * 4;
+  o.total = off + 1024;  // base alignment
+  return o;
+}
+
 struct Params {
   const LayerW* layers;      // device array [L]
   int L, H, nq, nkv, I, V, cap;
@@ -81,25 +102,9 @@ struct Params {
   unsigned long long* tl;    // timeline: per phase [start, units done, end] (CTA 0), or null
   int pf_mode;               // when the MLP rows are asked into L2: 0 never, 1 attention start,
                              // 2 o_proj start, 3 when the producers reach them
+  Layout lay;
 };
 
-template <int HD>
-struct Smem {
-  static constexpr int KS = HD + 8;  // halves per attention tile row (16-byte pad)
-  static constexpr size_t RING = (size_t)NS * SLOT;
-  static constexpr size_t ATT = (size_t)2 * AT_K * KS * 2;  // K and V tiles (the combine reuses them)
-  static constexpr size_t OFF_ATT = RING;
-  static constexpr size_t OFF_XS = OFF_ATT + ATT;
-  static constexpr size_t OFF_DA = OFF_XS + XS_FLOATS * 4;
-  static constexpr size_t OFF_DB = OFF_DA + MAX_LOCAL * 4;
-  static constexpr size_t OFF_DP = OFF_DB + MAX_LOCAL * 4;       // DOWN partials [rows][NCW]
-  static constexpr size_t OFF_MW = OFF_DP + 64 * NCW * 4;          // merge (m, w) [2][nq][NSPLIT]
-  static constexpr size_t OFF_BAR = OFF_MW + 2 * 32 * NSPLIT * 4;
-  static constexpr size_t OFF_SCR = OFF_BAR + 2 * NS * 8;
-  static constexpr size_t TOTAL = OFF_SCR + 64 * 4;
-  static constexpr size_t ALLOC = TOTAL + 1024;  // base aligned to 1024 inside
-  static_assert(2 * 16 * HD * 4 + 4 * 16 * 4 <= ATT, "attention combine must fit the tile area");
-};
 
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory"); }
 // consumer barrier that also ANDs a predicate over every consumer thread
@@ -162,10 +167,10 @@ struct Unit {
 // Calls f(unit) for each unit of phase ph of layer l for this CTA, in stream order, until f
 // returns false; returns false in that case.
 template <class F>
-__device__ __forceinline__ bool phase_units(const Params& p, int hd, int l, int ph, F&& f) {
+__device__ __forceinline__ bool phase_units(const Params& p, const LayerW* lt, int hd, int l, int ph, F&& f) {
   const int R = rows_per_slot(p.H);
   const size_t rowH = (size_t)p.H * 2;  // bytes of a row of K = H
-  const LayerW& w = p.layers[l < p.L ? l : 0];
+  const LayerW& w = lt[l < p.L ? l : 0];
   int i0, i1;
   Unit u;
   u.bytes[1] = 0;
@@ -265,7 +270,8 @@ __device__ __forceinline__ void mlp_l2_ahead(const Params& p, const LayerW& w) {
 // ---- producers -----------------------------------------------------------------------
 
 template <int HD>
-__device__ void producer(const Params& p, unsigned char* smem, uint32_t full0, uint32_t empty0, int pw, int ctx) {
+__device__ void producer(const Params& p, const LayerW* lt, unsigned char* smem, uint32_t full0, uint32_t empty0,
+                         int pw, int ctx) {
   long long u = 0;                 // unit counter (same sequence as the consumers')
   long long last_mine[NS / NPW];   // most recent unit issued into each of my slots
   for (int i = 0; i < NS / NPW; ++i) last_mine[i] = -1;
@@ -309,7 +315,7 @@ __device__ void producer(const Params& p, unsigned char* smem, uint32_t full0, u
           prefetch_l2_bulk(kc + (size_t)p.nkv * p.cap * HD + off, bytes);
         }
       }
-      const LayerW& w = p.layers[l];
+      const LayerW& w = lt[l];
       if (pw == 0) {  // small per-layer vectors every CTA reads (a few CTAs ask for them)
         const uint32_t hb = (uint32_t)p.H * 2;
         switch (blockIdx.x) {
@@ -325,12 +331,12 @@ __device__ void producer(const Params& p, unsigned char* smem, uint32_t full0, u
       const int phs[4] = {P_QKV, P_OPROJ, P_GATEUP, P_DOWN};
       for (int k = 0; k < 4 && ok; ++k) {
         if (phs[k] == P_GATEUP && pw == 0 && p.pf_mode == 3) mlp_l2_ahead(p, w);
-        ok = phase_units(p, HD, l, phs[k], issue);
+        ok = phase_units(p, lt, HD, l, phs[k], issue);
         if (ok && aborted(p)) ok = false;
       }
     } else {
       if (pw == 0 && blockIdx.x == 0) prefetch_l2_bulk(p.final_norm, (uint32_t)p.H * 2);
-      ok = phase_units(p, HD, l, P_LM, issue);
+      ok = phase_units(p, lt, HD, l, P_LM, issue);
     }
   }
   // copies in flight land before the CTA may exit (they were all consumed unless aborted)
@@ -429,7 +435,12 @@ __device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int
     if (!aborted(p)) {
       // release: this CTA's writes of the phase (ordered before by the consumer barrier)
       asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar), "l"(1ull) : "memory");
-      if (p.tl) atomicMax(p.tl + 3 * (5 * p.L + 1 + k) + 2, gtime());  // the last CTA's arrival
+      if (p.tl) {
+        const unsigned long long now = gtime();
+        atomicMax(p.tl + 3 * (5 * p.L + 1 + k) + 2, now);  // the last CTA's arrival
+        if (k >= 5 && k < 10)  // every CTA's arrival after the phases of layer 1
+          p.tl[9 * (5 * p.L + 1) + (k - 5) * gridDim.x + blockIdx.x] = now;
+      }
       const unsigned long long target = base + (unsigned long long)nb * gridDim.x;
       const long long t0 = clock64();
       ok = 1;
@@ -457,6 +468,10 @@ __device__ __forceinline__ void tl_mark(const Params& p, int k, int which) {
 // last CTA's arrival at the barrier after the phase
 __device__ __forceinline__ void tl_mark2(const Params& p, int k) {
   if (p.tl && blockIdx.x == 0 && threadIdx.x == 0) p.tl[3 * (5 * p.L + 1 + k)] = gtime();
+}
+// third record of phase k: [0] first unit consumed, [1] epilogue start, [2] epilogue end
+__device__ __forceinline__ void tl_mark3(const Params& p, int k, int which) {
+  if (p.tl && blockIdx.x == 0 && threadIdx.x == 0) p.tl[3 * (2 * (5 * p.L + 1) + k) + which] = gtime();
 }
 
 
@@ -511,6 +526,7 @@ __device__ void attention_preload(const Params& p, unsigned char* att, int l, in
 template <int HD>
 __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int g, int c, int chunk, int ctx) {
   constexpr int KS = HD + 8, NKK = HD / 16, NNT = HD / 8;
+  static_assert(2 * 16 * HD * 4 + 4 * 16 * 4 <= 2 * AT_K * KS * 2, "the combine must fit the tile area");
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, gid = lane >> 2, tig = lane & 3;
   const int G = p.nq / p.nkv;
   f16* Ks = reinterpret_cast<f16*>(att);
@@ -727,17 +743,17 @@ __device__ void stage_merge(const Params& p, float* xs, float* mw, int ns) {
 
 template <int HD>
 __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p) {
-  using S = Smem<HD>;
   extern __shared__ unsigned char mk_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)mk_raw + 1023) & ~(uintptr_t)1023);
-  unsigned char* att = smem + S::OFF_ATT;
-  float* xs = reinterpret_cast<float*>(smem + S::OFF_XS);
-  float* dA = reinterpret_cast<float*>(smem + S::OFF_DA);
-  float* dB = reinterpret_cast<float*>(smem + S::OFF_DB);
-  float* dP = reinterpret_cast<float*>(smem + S::OFF_DP);
-  float* mwv = reinterpret_cast<float*>(smem + S::OFF_MW);
-  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + S::OFF_BAR);
-  float* scr = reinterpret_cast<float*>(smem + S::OFF_SCR);
+  unsigned char* att = smem + p.lay.att;
+  float* xs = reinterpret_cast<float*>(smem + p.lay.xs);
+  float* dA = reinterpret_cast<float*>(smem + p.lay.da);
+  float* dB = reinterpret_cast<float*>(smem + p.lay.db);
+  float* dP = reinterpret_cast<float*>(smem + p.lay.dp);
+  float* mwv = reinterpret_cast<float*>(smem + p.lay.mw);
+  LayerW* lt = reinterpret_cast<LayerW*>(smem + p.lay.lt);
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + p.lay.bar);
+  float* scr = reinterpret_cast<float*>(smem + p.lay.scr);
   int* s_flag = reinterpret_cast<int*>(scr + 48);
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + NS);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -753,10 +769,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     }
     mbar_fence_init();
   }
+  {  // the layer pointer table, read at every phase, lives in shared memory
+    const int n8 = p.L * (int)(sizeof(LayerW) / 8);
+    const unsigned long long* src = reinterpret_cast<const unsigned long long*>(p.layers);
+    unsigned long long* dst = reinterpret_cast<unsigned long long*>(lt);
+    for (int i = t; i < n8; i += THREADS) dst[i] = __ldg(src + i);
+  }
   __syncthreads();  // the only block-wide barrier: producers and consumers part here
 
   if (warp >= NCW) {
-    if (lane == 0) producer<HD>(p, smem, full0, empty0, warp - NCW, ctx);
+    if (lane == 0) producer<HD>(p, lt, smem, full0, empty0, warp - NCW, ctx);
     return;
   }
 
@@ -786,6 +808,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   int ph_idx = 0;  // timeline index
 
   // wait for unit u, apply fn to it, release the slot
+  int phase_u = 0;  // units consumed in the current phase
   auto consume = [&](const Unit& un, auto&& fn) -> bool {
     const long long my = u++;
     const int s = (int)(my % NS);
@@ -794,13 +817,15 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     fn(smem + (size_t)s * SLOT, un);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (phase_u++ == 0) tl_mark3(p, ph_idx, 0);
     return true;
   };
 
   for (int l = 0; l < p.L && alive; ++l) {
-    const LayerW& w = p.layers[l];
+    const LayerW& w = lt[l];
     // ===== QKV: RMSNorm -> q/k/v rows (+ bias) -> RoPE -> q out, K/V append
     tl_mark(p, ph_idx, 0);
+    phase_u = 0;
     int i0, i1;
     block_of((p.nq + 2 * p.nkv) * half, i0, i1);
     // epilogue inputs of this thread's pair (independent of the barrier's data)
@@ -837,10 +862,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
         }
       };
-      alive = phase_units(p, HD, l, P_QKV, [&](const Unit& un) { return consume(un, fn); });
+      alive = phase_units(p, lt, HD, l, P_QKV, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
+    tl_mark3(p, ph_idx, 1);
     if (alive && e_mine) {
       float a = dA[t] + ba, b = dB[t] + bb;
       if (e_head < p.nq + p.nkv) {  // rotate the pair (i, i + hd/2)
@@ -864,22 +890,26 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       const int g = blockIdx.x / ns, c = blockIdx.x - g * ns;
       attention_preload<HD>(p, att, l, g, c, chunk, ctx);
     }
+    tl_mark3(p, ph_idx, 2);
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (!alive) break;
 
     // ===== ATTN: (KV head, chunk) partials
     tl_mark(p, ph_idx, 0);
+    phase_u = 0;
     if (p.pf_mode == 1 && t == 0) mlp_l2_ahead(p, w);
     if ((int)blockIdx.x < p.nkv * ns) {
       const int g = blockIdx.x / ns, c = blockIdx.x - g * ns;
       attention_chunk<HD>(p, att, l, g, c, chunk, ctx);
     }
+    tl_mark3(p, ph_idx, 2);
     tl_mark(p, ph_idx++, 2);
     if (!grid_sync(p, base, nb, s_flag, ph_idx - 1)) { alive = false; break; }
 
     // ===== OPROJ: merge -> x += Wo o
     tl_mark(p, ph_idx, 0);
+    phase_u = 0;
     if (p.pf_mode == 2 && t == 0) mlp_l2_ahead(p, w);
     stage_merge<HD>(p, xs, mwv, ns);
     load_xr(xr, xs, (p.nq * HD) >> 3, lane);
@@ -893,21 +923,24 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (lane == 0) dA[un.a - i0 + warp] = d;
         }
       };
-      alive = phase_units(p, HD, l, P_OPROJ, [&](const Unit& un) { return consume(un, fn); });
+      alive = phase_units(p, lt, HD, l, P_OPROJ, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
+    tl_mark3(p, ph_idx, 1);
     if (alive)
       if (own) {
         xown += dA[t];
         p.x[r0 + t] = xown;
       }
+    tl_mark3(p, ph_idx, 2);
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (!alive) break;
 
     // ===== GATEUP: RMSNorm -> gate/up rows -> SwiGLU
     tl_mark(p, ph_idx, 0);
+    phase_u = 0;
     stage_norm(p, xs, scr, p.x, nullptr, w.post_norm);
     load_xr(xr, xs, nvecH, lane);
     tl_mark2(p, ph_idx);
@@ -923,21 +956,24 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
         }
       };
-      alive = phase_units(p, HD, l, P_GATEUP, [&](const Unit& un) { return consume(un, fn); });
+      alive = phase_units(p, lt, HD, l, P_GATEUP, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
+    tl_mark3(p, ph_idx, 1);
     if (alive)
       for (int i = i0 + t; i < i1; i += NCT) {
         const float gv = dA[i - i0], uv = dB[i - i0];
         p.act[i] = (gv / (1.f + expf(-gv))) * uv;
       }
+    tl_mark3(p, ph_idx, 2);
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (!alive) break;
 
     // ===== DOWN: x += Wd act, each row's K split over the eight warps
     tl_mark(p, ph_idx, 0);
+    phase_u = 0;
     {
       const int nvecI = p.I >> 3;
       const int segv = (nvecI + NCW - 1) / NCW;
@@ -967,10 +1003,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         acc = warp_sum(acc);
         if (lane == 0) dP[(un.a - i0) * NCW + warp] = acc;
       };
-      alive = phase_units(p, HD, l, P_DOWN, [&](const Unit& un) { return consume(un, fn); });
+      alive = phase_units(p, lt, HD, l, P_DOWN, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
+    tl_mark3(p, ph_idx, 1);
     if (alive)
       if (own) {
         float s = 0.f;
@@ -979,6 +1016,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         xown += s;
         p.x[r0 + t] = xown;
       }
+    tl_mark3(p, ph_idx, 2);
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
   }
@@ -986,6 +1024,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   // ===== LM head: final RMSNorm -> logits -> greedy argmax
   if (alive) {
     tl_mark(p, ph_idx, 0);
+    phase_u = 0;
     stage_norm(p, xs, scr, p.x, nullptr, p.final_norm);
     load_xr(xr, xs, nvecH, lane);
     tl_mark2(p, ph_idx);
@@ -1003,7 +1042,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (z > best_v || best_i < 0) { best_v = z; best_i = r; }  // rows arrive in increasing order
         }
       };
-      alive = phase_units(p, HD, p.L, P_LM, [&](const Unit& un) { return consume(un, fn); });
+      alive = phase_units(p, lt, HD, p.L, P_LM, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
     if (lane == 0) {
@@ -1011,6 +1050,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       reinterpret_cast<int*>(dA)[warp] = bad;
     }
     alive = cbar_and(alive);
+    tl_mark3(p, ph_idx, 1);
     if (alive && t == 0) {
       unsigned long long k = 0;
       int anybad = 0;
@@ -1022,6 +1062,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       if (k) atomicMax(p.key, k);
       if (anybad) atomicOr(p.err, ERR_NONFINITE);
     }
+    tl_mark3(p, ph_idx, 2);
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (alive && blockIdx.x == 0 && t == 0) {
@@ -1057,31 +1098,29 @@ bool megastep_supported(const Dims& d, int nsm) {
   auto per_cta = [&](int n) { return (n + nsm - 1) / nsm; };
   if (per_cta(pairs) > mk::MAX_LOCAL || per_cta(d.I) > mk::MAX_LOCAL || per_cta(d.H) > 64) return false;
   if (d.nkv * mk::NSPLIT > nsm) return false;
+  if (megastep_smem(d) > 227 * 1024) return false;
   return true;
 }
 
-size_t megastep_smem(int hd) { return hd == 128 ? mk::Smem<128>::ALLOC : mk::Smem<64>::ALLOC; }
+size_t megastep_smem(const Dims& d) { return mk::make_layout(d.hd, d.H, d.nq, d.L).total; }
 
 size_t megastep_part_bytes(const Dims& d) {
   return (size_t)d.nq * mk::NSPLIT * attn_part_stride(d.hd) * sizeof(float);
 }
 
-cudaError_t megastep_set_attributes(int hd) {
-  if (hd == 128)
-    return cudaFuncSetAttribute(mk::decode_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)mk::Smem<128>::ALLOC);
-  return cudaFuncSetAttribute(mk::decode_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)mk::Smem<64>::ALLOC);
+cudaError_t megastep_set_attributes(const Dims& d) {
+  const int bytes = (int)megastep_smem(d);
+  if (d.hd == 128) return cudaFuncSetAttribute(mk::decode_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return cudaFuncSetAttribute(mk::decode_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 int megastep_threads() { return mk::THREADS; }
 
-cudaError_t megastep_occupancy(int hd, int* per_sm) {
-  if (hd == 128)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk::decode_step_kernel<128>, mk::THREADS,
-                                                         mk::Smem<128>::ALLOC);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk::decode_step_kernel<64>, mk::THREADS,
-                                                       mk::Smem<64>::ALLOC);
+cudaError_t megastep_occupancy(const Dims& d, int* per_sm) {
+  const size_t bytes = megastep_smem(d);
+  if (d.hd == 128)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk::decode_step_kernel<128>, mk::THREADS, bytes);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk::decode_step_kernel<64>, mk::THREADS, bytes);
 }
 
 size_t megastep_layer_bytes() { return sizeof(mk::LayerW); }
@@ -1104,10 +1143,11 @@ cudaError_t launch_megastep(const MegaLaunch& a, cudaStream_t s) {
   p.tok = a.tok; p.pos = a.pos; p.key = a.key; p.hist = a.hist; p.hist_n = a.hist_n; p.hist_cap = a.hist_cap;
   p.bar = a.bar; p.bar_base = a.bar_base; p.abort = a.abort; p.err = a.err; p.tl = a.tl;
   p.pf_mode = a.pf_mode;
+  p.lay = mk::make_layout(a.d.hd, a.d.H, a.d.nq, a.d.L);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(mk::THREADS);
-  cfg.dynamicSmemBytes = megastep_smem(a.d.hd);
+  cfg.dynamicSmemBytes = p.lay.total;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
