@@ -809,10 +809,27 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
 
   // wait for unit u, apply fn to it, release the slot
   int phase_u = 0;  // units consumed in the current phase
+  // timeline diagnostics (CTA 0, thread 0): per phase kind, cycles waited for units, units
+  // not yet landed when first tested, and cycles of the first unit's wait
+  unsigned long long* diag = p.tl ? p.tl + 9 * (5 * p.L + 1) + 5 * gridDim.x : nullptr;
+  int kind = 0;
   auto consume = [&](const Unit& un, auto&& fn) -> bool {
     const long long my = u++;
     const int s = (int)(my % NS);
+    long long c0 = 0;
+    bool ready = true;
+    if (diag && blockIdx.x == 0 && threadIdx.x == 0) {
+      c0 = clock64();
+      ready = mbar_test_now(full0 + 8 * s, (uint32_t)((my / NS) & 1));
+    }
     const bool ok = __all_sync(0xffffffffu, slot_wait(p, full0 + 8 * s, (uint32_t)((my / NS) & 1)));
+    if (diag && blockIdx.x == 0 && threadIdx.x == 0) {
+      const unsigned long long dc = (unsigned long long)(clock64() - c0);
+      diag[4 * kind + 0] += dc;
+      diag[4 * kind + 1] += ready ? 0 : 1;
+      if (phase_u == 0) diag[4 * kind + 2] += dc;
+      diag[4 * kind + 3] += 1;
+    }
     if (!ok) return false;
     fn(smem + (size_t)s * SLOT, un);
     __syncwarp();
@@ -862,6 +879,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
         }
       };
+      kind = 0;
       alive = phase_units(p, lt, HD, l, P_QKV, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
@@ -923,6 +941,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (lane == 0) dA[un.a - i0 + warp] = d;
         }
       };
+      kind = 1;
       alive = phase_units(p, lt, HD, l, P_OPROJ, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
@@ -956,6 +975,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
         }
       };
+      kind = 2;
       alive = phase_units(p, lt, HD, l, P_GATEUP, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
@@ -1003,6 +1023,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         acc = warp_sum(acc);
         if (lane == 0) dP[(un.a - i0) * NCW + warp] = acc;
       };
+      kind = 3;
       alive = phase_units(p, lt, HD, l, P_DOWN, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
@@ -1042,6 +1063,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (z > best_v || best_i < 0) { best_v = z; best_i = r; }  // rows arrive in increasing order
         }
       };
+      kind = 4;
       alive = phase_units(p, lt, HD, p.L, P_LM, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
