@@ -47,8 +47,7 @@ constexpr int NCT = NCW * 32;              // consumer threads
 constexpr int THREADS = (NCW + NPW) * 32;
 constexpr int NS = 8;                      // ring slots (a multiple of NPW)
 constexpr int SLOT = 24 * 1024;            // bytes per slot
-constexpr int MAXV = 8;                    // 16-byte vectors per lane of a row (K <= 2048)
-constexpr int MAXD = 8;                    // vectors per lane of a DOWN segment
+constexpr int MAXV = 8;                    // 16-byte vectors per lane of the register tile, at most
 constexpr int MAX_LOCAL = 128;             // items of one phase per CTA
 constexpr int NSPLIT = 16;                 // most attention chunks per KV head
 constexpr int CHUNK_MIN = 32;              // fewest positions per chunk
@@ -348,25 +347,49 @@ __device__ void producer(const Params& p, const LayerW* lt, unsigned char* smem,
 
 // ---- consumer helpers ----------------------------------------------------------------
 
-// dot of one row held in a slot (16-byte vectors of bf16) with the input vector in registers
-__device__ __forceinline__ float row_dot(const unsigned char* row, const float (&xr)[MAXV][8], int nvec, int lane) {
-  const uint4* r = reinterpret_cast<const uint4*>(row);
-  float acc = 0.f;
+
+// Dots of this warp's vectors of two rows (either may be null: 0) with the input vector in
+// registers: lane l takes vectors v_lo + l + 32 q < v_hi, one independent 8-term chain per
+// vector and row, and the two warp reductions run interleaved.
+template <int NV>
+__device__ __forceinline__ void dot2(const uint4* ra, const uint4* rb, const float (&xv)[NV][8], int v_lo, int v_hi,
+                                     int lane, float& da, float& db) {
+  float pa[NV], pb[NV];
 #pragma unroll
-  for (int q = 0; q < MAXV; ++q) {
-    const int v = lane + 32 * q;
-    if (v < nvec) acc = dotv(r[v], xr[q], acc, bf16());
+  for (int q = 0; q < NV; ++q) {
+    const int v = v_lo + lane + 32 * q;
+    pa[q] = 0.f;
+    pb[q] = 0.f;
+    if (v < v_hi) {
+      if (ra) pa[q] = dotv(ra[v], xv[q], 0.f, bf16());
+      if (rb) pb[q] = dotv(rb[v], xv[q], 0.f, bf16());
+    }
   }
-  return warp_sum(acc);
+#pragma unroll
+  for (int st = 1; st < NV; st *= 2)
+#pragma unroll
+    for (int q = 0; q + st < NV; q += 2 * st) {
+      pa[q] += pa[q + st];
+      pb[q] += pb[q + st];
+    }
+  float a = pa[0], b = pb[0];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  da = a;
+  db = b;
 }
 
 // input vector of the row phases from the staged xs (floats) into registers: lane l holds
 // vectors l, l + 32, ... (8 floats each); two 16-byte shared loads per vector, lanes with bit
 // 2 set taking the halves in the other order (conflict-free)
-__device__ __forceinline__ void load_xr(float (&xr)[MAXV][8], const float* xs, int nvec, int lane) {
+template <int NV>
+__device__ __forceinline__ void load_xr(float (&xr)[NV][8], const float* xs, int nvec, int lane) {
   const bool sw = (lane & 4) != 0;
 #pragma unroll
-  for (int q = 0; q < MAXV; ++q) {
+  for (int q = 0; q < NV; ++q) {
     const int v = lane + 32 * q;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
     if (v < nvec) {
@@ -741,7 +764,9 @@ __device__ void stage_merge(const Params& p, float* xs, float* mw, int ns) {
 
 // ---- the kernel ------------------------------------------------------------------------
 
-template <int HD>
+// NV: 16-byte vectors per lane of the register tile of the input vector (a row of hidden
+// elements, or a warp's eighth of a down-projection row)
+template <int HD, int NV>
 __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p) {
   extern __shared__ unsigned char mk_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)mk_raw + 1023) & ~(uintptr_t)1023);
@@ -803,18 +828,18 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   const bool own = t < r1 - r0;
   float xown = own ? __bfloat162float(erow[r0 + t]) : 0.f;
   if (own) p.x[r0 + t] = xown;
-  float xr[MAXV][8];
+  float xr[NV][8];
   bool alive = true;
   int ph_idx = 0;  // timeline index
 
-  // wait for unit u, apply fn to it, release the slot
+  // Units are consumed two at a time: wait for both, take this warp's row (pick) of each,
+  // dot both with the input vector, emit, release both slots.
   int phase_u = 0;  // units consumed in the current phase
   // timeline diagnostics (CTA 0, thread 0): per phase kind, cycles waited for units, units
   // not yet landed when first tested, and cycles of the first unit's wait
   unsigned long long* diag = p.tl ? p.tl + 9 * (5 * p.L + 1) + 5 * gridDim.x : nullptr;
   int kind = 0;
-  auto consume = [&](const Unit& un, auto&& fn) -> bool {
-    const long long my = u++;
+  auto wait_unit = [&](long long my) -> bool {
     const int s = (int)(my % NS);
     long long c0 = 0;
     bool ready = true;
@@ -830,12 +855,47 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       if (phase_u == 0) diag[4 * kind + 2] += dc;
       diag[4 * kind + 3] += 1;
     }
-    if (!ok) return false;
-    fn(smem + (size_t)s * SLOT, un);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);
-    if (phase_u++ == 0) tl_mark3(p, ph_idx, 0);
-    return true;
+    return ok;
+  };
+  // runs the units of phase ph of layer l; pick(unit, slot) gives this warp's row as 16-byte
+  // vectors (vectors v_lo .. v_hi - 1 of it are this warp's) or null, emit(unit, dot) stores
+  auto run_units = [&](int l, int ph, const float (&xv)[NV][8], int v_lo, int v_hi, auto&& pick,
+                       auto&& emit) -> bool {
+    Unit pend;
+    bool has = false;
+    auto process = [&](const Unit& A, const Unit* B) -> bool {
+      const long long ua = u++;
+      const long long ub = B ? u++ : -1;
+      if (!wait_unit(ua)) return false;
+      if (B && !wait_unit(ub)) return false;
+      const unsigned char* sa = smem + (size_t)(ua % NS) * SLOT;
+      const unsigned char* sb = B ? smem + (size_t)(ub % NS) * SLOT : nullptr;
+      const uint4* ra = pick(A, sa);
+      const uint4* rb = B ? pick(*B, sb) : nullptr;
+      float da, db;
+      dot2<NV>(ra, rb, xv, v_lo, v_hi, lane, da, db);
+      if (ra) emit(A, da);
+      if (rb) emit(*B, db);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(empty0 + 8 * (int)(ua % NS));
+        if (B) mbar_arrive(empty0 + 8 * (int)(ub % NS));
+      }
+      if (phase_u == 0) tl_mark3(p, ph_idx, 0);
+      phase_u += B ? 2 : 1;
+      return true;
+    };
+    bool ok = phase_units(p, lt, HD, l, ph, [&](const Unit& un) -> bool {
+      if (!has) {
+        pend = un;
+        has = true;
+        return true;
+      }
+      has = false;
+      return process(pend, &un);
+    });
+    if (ok && has) ok = process(pend, nullptr);
+    return ok;
   };
 
   for (int l = 0; l < p.L && alive; ++l) {
@@ -871,16 +931,17 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     {
       const int R = rows_per_slot(p.H);
       const int hp = R / 2;
-      auto fn = [&](const unsigned char* slot, const Unit& un) {
-        const int j = warp < hp ? warp : warp - hp;
-        if (warp < R && j < un.n) {
-          const unsigned char* row = slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2;
-          const float d = row_dot(row, xr, nvecH, lane);
-          if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
-        }
-      };
+      const int j = warp < hp ? warp : warp - hp;
       kind = 0;
-      alive = phase_units(p, lt, HD, l, P_QKV, [&](const Unit& un) { return consume(un, fn); });
+      alive = run_units(
+          l, P_QKV, xr, 0, nvecH,
+          [&](const Unit& un, const unsigned char* slot) -> const uint4* {
+            if (warp >= R || j >= un.n) return nullptr;
+            return reinterpret_cast<const uint4*>(slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2);
+          },
+          [&](const Unit& un, float d) {
+            if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
+          });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
@@ -935,14 +996,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     block_of(p.H, i0, i1);
     {
       const int R = rows_per_slot(p.H);
-      auto fn = [&](const unsigned char* slot, const Unit& un) {
-        if (warp < R && warp < un.n) {
-          const float d = row_dot(slot + (size_t)warp * p.H * 2, xr, (p.nq * HD) >> 3, lane);
-          if (lane == 0) dA[un.a - i0 + warp] = d;
-        }
-      };
       kind = 1;
-      alive = phase_units(p, lt, HD, l, P_OPROJ, [&](const Unit& un) { return consume(un, fn); });
+      alive = run_units(
+          l, P_OPROJ, xr, 0, (p.nq * HD) >> 3,
+          [&](const Unit& un, const unsigned char* slot) -> const uint4* {
+            if (warp >= R || warp >= un.n) return nullptr;
+            return reinterpret_cast<const uint4*>(slot + (size_t)warp * p.H * 2);
+          },
+          [&](const Unit& un, float d) {
+            if (lane == 0) dA[un.a - i0 + warp] = d;
+          });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
@@ -967,16 +1030,17 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     {
       const int R = rows_per_slot(p.H);
       const int hp = R / 2;
-      auto fn = [&](const unsigned char* slot, const Unit& un) {
-        const int j = warp < hp ? warp : warp - hp;
-        if (warp < R && j < un.n) {
-          const unsigned char* row = slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2;
-          const float d = row_dot(row, xr, nvecH, lane);
-          if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
-        }
-      };
+      const int j = warp < hp ? warp : warp - hp;
       kind = 2;
-      alive = phase_units(p, lt, HD, l, P_GATEUP, [&](const Unit& un) { return consume(un, fn); });
+      alive = run_units(
+          l, P_GATEUP, xr, 0, nvecH,
+          [&](const Unit& un, const unsigned char* slot) -> const uint4* {
+            if (warp >= R || j >= un.n) return nullptr;
+            return reinterpret_cast<const uint4*>(slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2);
+          },
+          [&](const Unit& un, float d) {
+            if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
+          });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
@@ -998,33 +1062,28 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       const int nvecI = p.I >> 3;
       const int segv = (nvecI + NCW - 1) / NCW;
       const int v0 = warp * segv, v1 = min(nvecI, v0 + segv);
-      float xd[MAXD][8];
 #pragma unroll
-      for (int qd = 0; qd < MAXD; ++qd) {
+      for (int qd = 0; qd < NV; ++qd) {
         const int v = v0 + lane + 32 * qd;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
         if (v < v1) {
           a = __ldcg(reinterpret_cast<const float4*>(p.act) + 2 * v);
           b = __ldcg(reinterpret_cast<const float4*>(p.act) + 2 * v + 1);
         }
-        xd[qd][0] = a.x; xd[qd][1] = a.y; xd[qd][2] = a.z; xd[qd][3] = a.w;
-        xd[qd][4] = b.x; xd[qd][5] = b.y; xd[qd][6] = b.z; xd[qd][7] = b.w;
+        xr[qd][0] = a.x; xr[qd][1] = a.y; xr[qd][2] = a.z; xr[qd][3] = a.w;
+        xr[qd][4] = b.x; xr[qd][5] = b.y; xr[qd][6] = b.z; xr[qd][7] = b.w;
       }
       block_of(p.H, i0, i1);
       tl_mark2(p, ph_idx);
-      auto fn = [&](const unsigned char* slot, const Unit& un) {
-        const uint4* r = reinterpret_cast<const uint4*>(slot);
-        float acc = 0.f;
-#pragma unroll
-        for (int qd = 0; qd < MAXD; ++qd) {
-          const int v = v0 + lane + 32 * qd;
-          if (v < v1) acc = dotv(r[v], xd[qd], acc, bf16());
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) dP[(un.a - i0) * NCW + warp] = acc;
-      };
       kind = 3;
-      alive = phase_units(p, lt, HD, l, P_DOWN, [&](const Unit& un) { return consume(un, fn); });
+      alive = run_units(
+          l, P_DOWN, xr, v0, v1,
+          [&](const Unit&, const unsigned char* slot) -> const uint4* {
+            return reinterpret_cast<const uint4*>(slot);
+          },
+          [&](const Unit& un, float d) {
+            if (lane == 0) dP[(un.a - i0) * NCW + warp] = d;
+          });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
@@ -1054,17 +1113,19 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     bool bad = false;
     {
       const int R = rows_per_slot(p.H);
-      auto fn = [&](const unsigned char* slot, const Unit& un) {
-        if (warp < R && warp < un.n) {
-          const float z = row_dot(slot + (size_t)warp * p.H * 2, xr, nvecH, lane);
-          const int r = un.a + warp;
-          if (lane == 0) p.logits[r] = z;
-          if (!isfinite(z)) bad = true;
-          if (z > best_v || best_i < 0) { best_v = z; best_i = r; }  // rows arrive in increasing order
-        }
-      };
       kind = 4;
-      alive = phase_units(p, lt, HD, p.L, P_LM, [&](const Unit& un) { return consume(un, fn); });
+      alive = run_units(
+          p.L, P_LM, xr, 0, nvecH,
+          [&](const Unit& un, const unsigned char* slot) -> const uint4* {
+            if (warp >= R || warp >= un.n) return nullptr;
+            return reinterpret_cast<const uint4*>(slot + (size_t)warp * p.H * 2);
+          },
+          [&](const Unit& un, float z) {
+            const int r = un.a + warp;
+            if (lane == 0) p.logits[r] = z;
+            if (!isfinite(z)) bad = true;
+            if (z > best_v || best_i < 0) { best_v = z; best_i = r; }  // rows arrive in increasing order
+          });
     }
     tl_mark(p, ph_idx, 1);
     if (lane == 0) {
@@ -1106,14 +1167,23 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
 
 // ---- host side ---------------------------------------------------------------------------
 
+// 16-byte vectors per lane the register tile needs: a row of hidden elements, or a warp's
+// eighth of a down-projection row
+static int megastep_nv(const Dims& d) {
+  const int row = (d.H / 8 + 31) / 32;
+  const int seg = ((d.I / 8 + mk::NCW - 1) / mk::NCW + 31) / 32;
+  const int need = std::max(row, seg);
+  return need <= 4 ? 4 : need <= 6 ? 6 : need <= 8 ? 8 : 0;
+}
+
 bool megastep_supported(const Dims& d, int nsm) {
   if (d.dtype != 1) return false;
   if (d.hd != 64 && d.hd != 128) return false;
   if (d.nq / d.nkv > mk::GMAX || d.nq * d.hd != d.H) return false;
-  if (d.H % 8 || d.H > mk::XS_FLOATS || d.H > 8 * 32 * mk::MAXV) return false;
+  if (d.H % 8 || d.H > mk::XS_FLOATS) return false;
   if (d.nq > 32) return false;  // merge weights [2][nq][NSPLIT] of 32 heads at most
   if (d.I % 8 || (size_t)d.I * 2 > (size_t)mk::SLOT) return false;
-  if (((d.I / 8 + mk::NCW - 1) / mk::NCW + 31) / 32 > mk::MAXD) return false;
+  if (megastep_nv(d) == 0) return false;
   const int R = std::min(mk::NCW, (mk::SLOT / (2 * d.H)) & ~1);
   if (R < 2) return false;
   const int pairs = (d.nq + 2 * d.nkv) * d.hd / 2;
@@ -1126,23 +1196,27 @@ bool megastep_supported(const Dims& d, int nsm) {
 
 size_t megastep_smem(const Dims& d) { return mk::make_layout(d.hd, d.H, d.nq, d.L).total; }
 
+static const void* megastep_fn(const Dims& d) {
+  const int nv = megastep_nv(d);
+  if (d.hd == 128)
+    return nv == 4 ? (const void*)mk::decode_step_kernel<128, 4>
+                   : nv == 6 ? (const void*)mk::decode_step_kernel<128, 6> : (const void*)mk::decode_step_kernel<128, 8>;
+  return nv == 4 ? (const void*)mk::decode_step_kernel<64, 4>
+                 : nv == 6 ? (const void*)mk::decode_step_kernel<64, 6> : (const void*)mk::decode_step_kernel<64, 8>;
+}
+
 size_t megastep_part_bytes(const Dims& d) {
   return (size_t)d.nq * mk::NSPLIT * attn_part_stride(d.hd) * sizeof(float);
 }
 
 cudaError_t megastep_set_attributes(const Dims& d) {
-  const int bytes = (int)megastep_smem(d);
-  if (d.hd == 128) return cudaFuncSetAttribute(mk::decode_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  return cudaFuncSetAttribute(mk::decode_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return cudaFuncSetAttribute(megastep_fn(d), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)megastep_smem(d));
 }
 
 int megastep_threads() { return mk::THREADS; }
 
 cudaError_t megastep_occupancy(const Dims& d, int* per_sm) {
-  const size_t bytes = megastep_smem(d);
-  if (d.hd == 128)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk::decode_step_kernel<128>, mk::THREADS, bytes);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk::decode_step_kernel<64>, mk::THREADS, bytes);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, megastep_fn(d), mk::THREADS, megastep_smem(d));
 }
 
 size_t megastep_layer_bytes() { return sizeof(mk::LayerW); }
@@ -1176,8 +1250,8 @@ cudaError_t launch_megastep(const MegaLaunch& a, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.d.hd == 128) return cudaLaunchKernelEx(&cfg, mk::decode_step_kernel<128>, p);
-  return cudaLaunchKernelEx(&cfg, mk::decode_step_kernel<64>, p);
+  void* args[] = {&p};
+  return cudaLaunchKernelExC(&cfg, megastep_fn(a.d), args);
 }
 
 }  // namespace qw
