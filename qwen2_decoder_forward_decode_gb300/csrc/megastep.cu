@@ -347,39 +347,22 @@ __device__ void producer(const Params& p, const LayerW* lt, unsigned char* smem,
 
 // ---- consumer helpers ----------------------------------------------------------------
 
-
-// Dots of this warp's vectors of two rows (either may be null: 0) with the input vector in
-// registers: lane l takes vectors v_lo + l + 32 q < v_hi, one independent 8-term chain per
-// vector and row, and the two warp reductions run interleaved.
+// dot of this warp's vectors of a row held in a slot (16-byte vectors of bf16) with the input
+// vector in registers: lane l takes vectors v_lo + l + 32 q < v_hi; one independent 8-term
+// chain per vector, added pairwise, then the warp reduction
 template <int NV>
-__device__ __forceinline__ void dot2(const uint4* ra, const uint4* rb, const float (&xv)[NV][8], int v_lo, int v_hi,
-                                     int lane, float& da, float& db) {
-  float pa[NV], pb[NV];
+__device__ __forceinline__ float row_dot(const uint4* r, const float (&xr)[NV][8], int v_lo, int v_hi, int lane) {
+  float part[NV];
 #pragma unroll
   for (int q = 0; q < NV; ++q) {
     const int v = v_lo + lane + 32 * q;
-    pa[q] = 0.f;
-    pb[q] = 0.f;
-    if (v < v_hi) {
-      if (ra) pa[q] = dotv(ra[v], xv[q], 0.f, bf16());
-      if (rb) pb[q] = dotv(rb[v], xv[q], 0.f, bf16());
-    }
+    part[q] = v < v_hi ? dotv(r[v], xr[q], 0.f, bf16()) : 0.f;
   }
 #pragma unroll
   for (int st = 1; st < NV; st *= 2)
 #pragma unroll
-    for (int q = 0; q + st < NV; q += 2 * st) {
-      pa[q] += pa[q + st];
-      pb[q] += pb[q + st];
-    }
-  float a = pa[0], b = pb[0];
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    a += __shfl_xor_sync(0xffffffffu, a, o);
-    b += __shfl_xor_sync(0xffffffffu, b, o);
-  }
-  da = a;
-  db = b;
+    for (int q = 0; q + st < NV; q += 2 * st) part[q] += part[q + st];
+  return warp_sum(part[0]);
 }
 
 // input vector of the row phases from the staged xs (floats) into registers: lane l holds
@@ -832,14 +815,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   bool alive = true;
   int ph_idx = 0;  // timeline index
 
-  // Units are consumed two at a time: wait for both, take this warp's row (pick) of each,
-  // dot both with the input vector, emit, release both slots.
+  // wait for unit u, apply fn to it, release the slot
   int phase_u = 0;  // units consumed in the current phase
   // timeline diagnostics (CTA 0, thread 0): per phase kind, cycles waited for units, units
   // not yet landed when first tested, and cycles of the first unit's wait
   unsigned long long* diag = p.tl ? p.tl + 9 * (5 * p.L + 1) + 5 * gridDim.x : nullptr;
   int kind = 0;
-  auto wait_unit = [&](long long my) -> bool {
+  auto consume = [&](const Unit& un, auto&& fn) -> bool {
+    const long long my = u++;
     const int s = (int)(my % NS);
     long long c0 = 0;
     bool ready = true;
@@ -855,47 +838,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       if (phase_u == 0) diag[4 * kind + 2] += dc;
       diag[4 * kind + 3] += 1;
     }
-    return ok;
-  };
-  // runs the units of phase ph of layer l; pick(unit, slot) gives this warp's row as 16-byte
-  // vectors (vectors v_lo .. v_hi - 1 of it are this warp's) or null, emit(unit, dot) stores
-  auto run_units = [&](int l, int ph, const float (&xv)[NV][8], int v_lo, int v_hi, auto&& pick,
-                       auto&& emit) -> bool {
-    Unit pend;
-    bool has = false;
-    auto process = [&](const Unit& A, const Unit* B) -> bool {
-      const long long ua = u++;
-      const long long ub = B ? u++ : -1;
-      if (!wait_unit(ua)) return false;
-      if (B && !wait_unit(ub)) return false;
-      const unsigned char* sa = smem + (size_t)(ua % NS) * SLOT;
-      const unsigned char* sb = B ? smem + (size_t)(ub % NS) * SLOT : nullptr;
-      const uint4* ra = pick(A, sa);
-      const uint4* rb = B ? pick(*B, sb) : nullptr;
-      float da, db;
-      dot2<NV>(ra, rb, xv, v_lo, v_hi, lane, da, db);
-      if (ra) emit(A, da);
-      if (rb) emit(*B, db);
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(empty0 + 8 * (int)(ua % NS));
-        if (B) mbar_arrive(empty0 + 8 * (int)(ub % NS));
-      }
-      if (phase_u == 0) tl_mark3(p, ph_idx, 0);
-      phase_u += B ? 2 : 1;
-      return true;
-    };
-    bool ok = phase_units(p, lt, HD, l, ph, [&](const Unit& un) -> bool {
-      if (!has) {
-        pend = un;
-        has = true;
-        return true;
-      }
-      has = false;
-      return process(pend, &un);
-    });
-    if (ok && has) ok = process(pend, nullptr);
-    return ok;
+    if (!ok) return false;
+    fn(smem + (size_t)s * SLOT, un);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (phase_u++ == 0) tl_mark3(p, ph_idx, 0);
+    return true;
   };
 
   for (int l = 0; l < p.L && alive; ++l) {
@@ -931,17 +879,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     {
       const int R = rows_per_slot(p.H);
       const int hp = R / 2;
-      const int j = warp < hp ? warp : warp - hp;
+      auto fn = [&](const unsigned char* slot, const Unit& un) {
+        const int j = warp < hp ? warp : warp - hp;
+        if (warp < R && j < un.n) {
+          const unsigned char* row = slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2;
+          const float d = row_dot<NV>(reinterpret_cast<const uint4*>(row), xr, 0, nvecH, lane);
+          if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
+        }
+      };
       kind = 0;
-      alive = run_units(
-          l, P_QKV, xr, 0, nvecH,
-          [&](const Unit& un, const unsigned char* slot) -> const uint4* {
-            if (warp >= R || j >= un.n) return nullptr;
-            return reinterpret_cast<const uint4*>(slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2);
-          },
-          [&](const Unit& un, float d) {
-            if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
-          });
+      alive = phase_units(p, lt, HD, l, P_QKV, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
@@ -996,16 +943,15 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     block_of(p.H, i0, i1);
     {
       const int R = rows_per_slot(p.H);
+      auto fn = [&](const unsigned char* slot, const Unit& un) {
+        if (warp < R && warp < un.n) {
+          const float d =
+              row_dot<NV>(reinterpret_cast<const uint4*>(slot + (size_t)warp * p.H * 2), xr, 0, (p.nq * HD) >> 3, lane);
+          if (lane == 0) dA[un.a - i0 + warp] = d;
+        }
+      };
       kind = 1;
-      alive = run_units(
-          l, P_OPROJ, xr, 0, (p.nq * HD) >> 3,
-          [&](const Unit& un, const unsigned char* slot) -> const uint4* {
-            if (warp >= R || warp >= un.n) return nullptr;
-            return reinterpret_cast<const uint4*>(slot + (size_t)warp * p.H * 2);
-          },
-          [&](const Unit& un, float d) {
-            if (lane == 0) dA[un.a - i0 + warp] = d;
-          });
+      alive = phase_units(p, lt, HD, l, P_OPROJ, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
@@ -1030,17 +976,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     {
       const int R = rows_per_slot(p.H);
       const int hp = R / 2;
-      const int j = warp < hp ? warp : warp - hp;
+      auto fn = [&](const unsigned char* slot, const Unit& un) {
+        const int j = warp < hp ? warp : warp - hp;
+        if (warp < R && j < un.n) {
+          const unsigned char* row = slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2;
+          const float d = row_dot<NV>(reinterpret_cast<const uint4*>(row), xr, 0, nvecH, lane);
+          if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
+        }
+      };
       kind = 2;
-      alive = run_units(
-          l, P_GATEUP, xr, 0, nvecH,
-          [&](const Unit& un, const unsigned char* slot) -> const uint4* {
-            if (warp >= R || j >= un.n) return nullptr;
-            return reinterpret_cast<const uint4*>(slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2);
-          },
-          [&](const Unit& un, float d) {
-            if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
-          });
+      alive = phase_units(p, lt, HD, l, P_GATEUP, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
@@ -1075,15 +1020,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       }
       block_of(p.H, i0, i1);
       tl_mark2(p, ph_idx);
+      auto fn = [&](const unsigned char* slot, const Unit& un) {
+        const float acc = row_dot<NV>(reinterpret_cast<const uint4*>(slot), xr, v0, v1, lane);
+        if (lane == 0) dP[(un.a - i0) * NCW + warp] = acc;
+      };
       kind = 3;
-      alive = run_units(
-          l, P_DOWN, xr, v0, v1,
-          [&](const Unit&, const unsigned char* slot) -> const uint4* {
-            return reinterpret_cast<const uint4*>(slot);
-          },
-          [&](const Unit& un, float d) {
-            if (lane == 0) dP[(un.a - i0) * NCW + warp] = d;
-          });
+      alive = phase_units(p, lt, HD, l, P_DOWN, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
     alive = cbar_and(alive);
@@ -1113,19 +1055,17 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     bool bad = false;
     {
       const int R = rows_per_slot(p.H);
+      auto fn = [&](const unsigned char* slot, const Unit& un) {
+        if (warp < R && warp < un.n) {
+          const float z = row_dot<NV>(reinterpret_cast<const uint4*>(slot + (size_t)warp * p.H * 2), xr, 0, nvecH, lane);
+          const int r = un.a + warp;
+          if (lane == 0) p.logits[r] = z;
+          if (!isfinite(z)) bad = true;
+          if (z > best_v || best_i < 0) { best_v = z; best_i = r; }  // rows arrive in increasing order
+        }
+      };
       kind = 4;
-      alive = run_units(
-          p.L, P_LM, xr, 0, nvecH,
-          [&](const Unit& un, const unsigned char* slot) -> const uint4* {
-            if (warp >= R || warp >= un.n) return nullptr;
-            return reinterpret_cast<const uint4*>(slot + (size_t)warp * p.H * 2);
-          },
-          [&](const Unit& un, float z) {
-            const int r = un.a + warp;
-            if (lane == 0) p.logits[r] = z;
-            if (!isfinite(z)) bad = true;
-            if (z > best_v || best_i < 0) { best_v = z; best_i = r; }  // rows arrive in increasing order
-          });
+      alive = phase_units(p, lt, HD, p.L, P_LM, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
     if (lane == 0) {
