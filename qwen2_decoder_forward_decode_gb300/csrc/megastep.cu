@@ -821,28 +821,37 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   // not yet landed when first tested, and cycles of the first unit's wait
   unsigned long long* diag = p.tl ? p.tl + 9 * (5 * p.L + 1) + 5 * gridDim.x : nullptr;
   int kind = 0;
+  long long c_last = 0;  // (diagnostics) clock at the end of the previous unit
   auto consume = [&](const Unit& un, auto&& fn) -> bool {
     const long long my = u++;
     const int s = (int)(my % NS);
     long long c0 = 0;
     bool ready = true;
-    if (diag && blockIdx.x == 0 && threadIdx.x == 0) {
+    const bool dg = diag && blockIdx.x == 0 && threadIdx.x == 0;
+    if (dg) {
       c0 = clock64();
+      if (phase_u > 0) diag[8 * kind + 5] += (unsigned long long)(c0 - c_last);
       ready = mbar_test_now(full0 + 8 * s, (uint32_t)((my / NS) & 1));
     }
     const bool ok = __all_sync(0xffffffffu, slot_wait(p, full0 + 8 * s, (uint32_t)((my / NS) & 1)));
-    if (diag && blockIdx.x == 0 && threadIdx.x == 0) {
-      const unsigned long long dc = (unsigned long long)(clock64() - c0);
-      diag[4 * kind + 0] += dc;
-      diag[4 * kind + 1] += ready ? 0 : 1;
-      if (phase_u == 0) diag[4 * kind + 2] += dc;
-      diag[4 * kind + 3] += 1;
+    long long c1 = 0;
+    if (dg) {
+      c1 = clock64();
+      const unsigned long long dc = (unsigned long long)(c1 - c0);
+      diag[8 * kind + 0] += dc;
+      diag[8 * kind + 1] += ready ? 0 : 1;
+      if (phase_u == 0) diag[8 * kind + 2] += dc;
+      diag[8 * kind + 3] += 1;
     }
     if (!ok) return false;
     fn(smem + (size_t)s * SLOT, un);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
     if (phase_u++ == 0) tl_mark3(p, ph_idx, 0);
+    if (dg) {
+      c_last = clock64();
+      diag[8 * kind + 4] += (unsigned long long)(c_last - c1);
+    }
     return true;
   };
 
