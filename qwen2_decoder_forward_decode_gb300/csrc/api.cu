@@ -85,7 +85,7 @@ struct qw_model {
   // one persistent kernel per decode step of one sequence (bf16 models)
   bool use_mega = false;
   void* mega_layers = nullptr;       // device layer records
-  float* mega_part = nullptr;        // attention chunk partials
+  float* mega_part = nullptr;        // copies of the residual, the activation and the attention partials
   unsigned long long* mega_bar = nullptr;  // [0] barrier counter, [1] its value at a step start
   int* mega_abort = nullptr;
   // batched decode (bf16 models with the fp16 matrix copies, several sequences)
@@ -201,11 +201,9 @@ struct qw_model {
     a.head = head_w();
     a.rope = rope;
     a.kv_seq = kv_seq(s);
-    a.x = x + (size_t)s * d.H;
     a.q = q;
-    a.act = act;
     a.logits = logits + (size_t)s * d.V;
-    a.part = mega_part;
+    a.work = mega_part;
     a.tok = tok + s;
     a.pos = pos + s;
     a.key = keys + s;
@@ -606,7 +604,7 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
       if ((e = cudaMalloc(&m->mega_layers, recs.size()))) return bail(e, "cudaMalloc");
       if ((e = cudaMemcpy(m->mega_layers, recs.data(), recs.size(), cudaMemcpyHostToDevice)))
         return bail(e, "cudaMemcpy");
-      if ((e = cudaMalloc(&m->mega_part, megastep_part_bytes(d)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMalloc(&m->mega_part, megastep_work_floats(d) * sizeof(float)))) return bail(e, "cudaMalloc");
       if ((e = cudaMalloc(&m->mega_bar, 2 * sizeof(unsigned long long)))) return bail(e, "cudaMalloc");
       if ((e = cudaMemset(m->mega_bar, 0, 2 * sizeof(unsigned long long)))) return bail(e, "cudaMemset");
       if ((e = cudaMalloc(&m->mega_abort, sizeof(int)))) return bail(e, "cudaMalloc");

@@ -117,7 +117,8 @@ struct MegaLaunch {
   const void *embed, *final_norm, *head;
   const float2* rope;
   void* kv_seq;                    // fp16 cache of the sequence [L][2][nkv][cap][hd]
-  float *x, *q, *act, *logits, *part;
+  float *q, *logits;
+  float* work;                     // megastep_work_floats: copies of x, the activation, partials
   int *tok, *pos;
   unsigned long long* key;
   int *hist, *hist_n;
@@ -132,7 +133,7 @@ struct MegaLaunch {
 };
 bool megastep_supported(const Dims& d, int nsm);
 size_t megastep_smem(const Dims& d);
-size_t megastep_part_bytes(const Dims& d);
+size_t megastep_work_floats(const Dims& d);
 cudaError_t megastep_set_attributes(const Dims& d);
 int megastep_threads();
 cudaError_t megastep_occupancy(const Dims& d, int* per_sm);  // resident CTAs per SM

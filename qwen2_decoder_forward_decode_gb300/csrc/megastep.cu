@@ -54,6 +54,10 @@ constexpr int CHUNK_MIN = 32;              // fewest positions per chunk
 constexpr int AT_K = 32;                   // positions per attention tile
 constexpr int GMAX = 8;                    // most query heads per KV head
 constexpr int XS_FLOATS = 2048;            // staged input vector (hidden <= 2048)
+// Vectors that every CTA reads after a grid barrier (the residual stream, the SwiGLU
+// activation, the attention partials) are written REP times at different addresses and CTA b
+// reads copy b % REP, so that 152 CTAs do not all queue on the same L2 lines.
+constexpr int REP = 8;
 
 enum : int { P_QKV = 0, P_ATTN = 1, P_OPROJ = 2, P_GATEUP = 3, P_DOWN = 4, P_LM = 5 };
 
@@ -89,7 +93,7 @@ struct Params {
   const bf16 *embed, *final_norm, *head;
   const float2* rope;        // [cap][hd/2] (cos, sin)
   f16* kv;                   // this sequence's cache [L][2][nkv][cap][hd]
-  float *x, *q, *act, *logits, *part;
+  float *x, *q, *act, *logits, *part;  // x [REP][H], act [REP][I], part [REP][nq][NSPLIT][hd + 4]
   int *tok, *pos;
   unsigned long long* key;   // packed argmax key (zero between steps)
   int *hist, *hist_n;
@@ -658,7 +662,9 @@ __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int 
       const float mw = cM[w * 16 + r];
       if (mw != -INFINITY) acc = fmaf(expf(mw - M), cO[(size_t)(w * 16 + r) * HD + d], acc);
     }
-    p.part[((size_t)(g * G + r) * NSPLIT + c) * ps + d] = acc;
+    const size_t off = ((size_t)(g * G + r) * NSPLIT + c) * ps + d, rs = (size_t)p.nq * NSPLIT * ps;
+#pragma unroll
+    for (int k = 0; k < REP; ++k) p.part[k * rs + off] = acc;
   }
   if (t < G) {
     const float M = fmaxf(cM[t], cM[16 + t]);
@@ -668,9 +674,13 @@ __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int 
       const float mw = cM[w * 16 + t];
       if (mw != -INFINITY) L = fmaf(expf(mw - M), cL[w * 16 + t], L);
     }
+    const size_t rs = (size_t)p.nq * NSPLIT * ps;
     float* pp = p.part + ((size_t)(g * G + t) * NSPLIT + c) * ps;
-    pp[HD] = M;
-    pp[HD + 1] = L;
+#pragma unroll
+    for (int k = 0; k < REP; ++k) {
+      pp[k * rs + HD] = M;
+      pp[k * rs + HD + 1] = L;
+    }
   }
 }
 
@@ -680,6 +690,7 @@ template <int HD>
 __device__ void stage_merge(const Params& p, float* xs, float* mw, int ns) {
   const int t = threadIdx.x;
   const int K = p.nq * HD, ps = attn_part_stride(HD);
+  const float* part = p.part + (size_t)(blockIdx.x % REP) * p.nq * NSPLIT * ps;  // this CTA's copy
   constexpr int MB = 8;  // chunks per batch of loads
   // (m, l) of every (head, chunk), requested together with the first batch of outputs
   const int groups = K / 4;  // float4 groups; thread t takes groups t and t + NCT
@@ -692,14 +703,14 @@ __device__ void stage_merge(const Params& p, float* xs, float* mw, int ns) {
 #pragma unroll
       for (int u = 0; u < MB; ++u)
         v[e][u] = (gi < groups && c0 + u < ns)
-                      ? __ldcg(reinterpret_cast<const float4*>(p.part + ((size_t)h * NSPLIT + c0 + u) * ps + d))
+                      ? __ldcg(reinterpret_cast<const float4*>(part + ((size_t)h * NSPLIT + c0 + u) * ps + d))
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
   load(0);
   for (int i = t; i < p.nq * ns; i += NCT) {
     const int h = i / ns, c = i - h * ns;
-    const float* pp = p.part + ((size_t)h * NSPLIT + c) * ps + HD;
+    const float* pp = part + ((size_t)h * NSPLIT + c) * ps + HD;
     mw[h * NSPLIT + c] = __ldcg(pp);
     mw[(p.nq + h) * NSPLIT + c] = __ldcg(pp + 1);
   }
@@ -810,7 +821,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   block_of(p.H, r0, r1);
   const bool own = t < r1 - r0;
   float xown = own ? __bfloat162float(erow[r0 + t]) : 0.f;
-  if (own) p.x[r0 + t] = xown;
+  if (own)
+#pragma unroll
+    for (int k = 0; k < REP; ++k) p.x[k * p.H + r0 + t] = xown;
+  const float* xmine = p.x + (size_t)(blockIdx.x % REP) * p.H;      // this CTA's copies
+  const float* actmine = p.act + (size_t)(blockIdx.x % REP) * p.I;
   float xr[NV][8];
   bool alive = true;
   int ph_idx = 0;  // timeline index
@@ -882,7 +897,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       }
       if (e_head < p.nq + p.nkv) cs = p.rope[(size_t)pos * half + e_i];
     }
-    stage_norm(p, xs, scr, p.x, l == 0 ? erow : nullptr, w.in_norm);
+    stage_norm(p, xs, scr, xmine, l == 0 ? erow : nullptr, w.in_norm);
     load_xr(xr, xs, nvecH, lane);
     tl_mark2(p, ph_idx);
     {
@@ -968,7 +983,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     if (alive)
       if (own) {
         xown += dA[t];
-        p.x[r0 + t] = xown;
+#pragma unroll
+        for (int k = 0; k < REP; ++k) p.x[k * p.H + r0 + t] = xown;
       }
     tl_mark3(p, ph_idx, 2);
     tl_mark(p, ph_idx++, 2);
@@ -978,7 +994,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     // ===== GATEUP: RMSNorm -> gate/up rows -> SwiGLU
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
-    stage_norm(p, xs, scr, p.x, nullptr, w.post_norm);
+    stage_norm(p, xs, scr, xmine, nullptr, w.post_norm);
     load_xr(xr, xs, nvecH, lane);
     tl_mark2(p, ph_idx);
     block_of(p.I, i0, i1);
@@ -1002,7 +1018,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     if (alive)
       for (int i = i0 + t; i < i1; i += NCT) {
         const float gv = dA[i - i0], uv = dB[i - i0];
-        p.act[i] = (gv / (1.f + expf(-gv))) * uv;
+        const float a = (gv / (1.f + expf(-gv))) * uv;
+#pragma unroll
+        for (int k = 0; k < REP; ++k) p.act[(size_t)k * p.I + i] = a;
       }
     tl_mark3(p, ph_idx, 2);
     tl_mark(p, ph_idx++, 2);
@@ -1021,8 +1039,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         const int v = v0 + lane + 32 * qd;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
         if (v < v1) {
-          a = __ldcg(reinterpret_cast<const float4*>(p.act) + 2 * v);
-          b = __ldcg(reinterpret_cast<const float4*>(p.act) + 2 * v + 1);
+          a = __ldcg(reinterpret_cast<const float4*>(actmine) + 2 * v);
+          b = __ldcg(reinterpret_cast<const float4*>(actmine) + 2 * v + 1);
         }
         xr[qd][0] = a.x; xr[qd][1] = a.y; xr[qd][2] = a.z; xr[qd][3] = a.w;
         xr[qd][4] = b.x; xr[qd][5] = b.y; xr[qd][6] = b.z; xr[qd][7] = b.w;
@@ -1045,7 +1063,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
 #pragma unroll
         for (int k = 0; k < NCW; ++k) s += dP[t * NCW + k];  // warp order
         xown += s;
-        p.x[r0 + t] = xown;
+#pragma unroll
+        for (int k = 0; k < REP; ++k) p.x[k * p.H + r0 + t] = xown;
       }
     tl_mark3(p, ph_idx, 2);
     tl_mark(p, ph_idx++, 2);
@@ -1056,7 +1075,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   if (alive) {
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
-    stage_norm(p, xs, scr, p.x, nullptr, p.final_norm);
+    stage_norm(p, xs, scr, xmine, nullptr, p.final_norm);
     load_xr(xr, xs, nvecH, lane);
     tl_mark2(p, ph_idx);
     float best_v = -INFINITY;
@@ -1154,9 +1173,10 @@ static const void* megastep_fn(const Dims& d) {
                  : nv == 6 ? (const void*)mk::decode_step_kernel<64, 6> : (const void*)mk::decode_step_kernel<64, 8>;
 }
 
-size_t megastep_part_bytes(const Dims& d) {
-  return (size_t)d.nq * mk::NSPLIT * attn_part_stride(d.hd) * sizeof(float);
+size_t megastep_work_floats(const Dims& d) {  // x, act and partial copies
+  return (size_t)mk::REP * ((size_t)d.H + d.I + (size_t)d.nq * mk::NSPLIT * attn_part_stride(d.hd));
 }
+
 
 cudaError_t megastep_set_attributes(const Dims& d) {
   return cudaFuncSetAttribute(megastep_fn(d), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)megastep_smem(d));
@@ -1184,7 +1204,10 @@ cudaError_t launch_megastep(const MegaLaunch& a, cudaStream_t s) {
   p.eps = a.d.eps;
   p.embed = (const bf16*)a.embed; p.final_norm = (const bf16*)a.final_norm; p.head = (const bf16*)a.head;
   p.rope = a.rope; p.kv = (f16*)a.kv_seq;
-  p.x = a.x; p.q = a.q; p.act = a.act; p.logits = a.logits; p.part = a.part;
+  p.x = a.work;
+  p.act = a.work + (size_t)mk::REP * a.d.H;
+  p.part = a.work + (size_t)mk::REP * (a.d.H + a.d.I);
+  p.q = a.q; p.logits = a.logits;
   p.tok = a.tok; p.pos = a.pos; p.key = a.key; p.hist = a.hist; p.hist_n = a.hist_n; p.hist_cap = a.hist_cap;
   p.bar = a.bar; p.bar_base = a.bar_base; p.abort = a.abort; p.err = a.err; p.tl = a.tl;
   p.pf_mode = a.pf_mode;
