@@ -259,13 +259,13 @@ def timeline_persistent(m, s, ids_dev, prompt, rank):
                 # CTA 0's phase end -> the last CTA's arrival -> CTA 0 past the barrier
                 st[k]["skew_us"].append((t2[j, 2] - tl[j, 2]) / 1000.0)
                 st[k]["barrier_us"].append((t2[j, 1] - t2[j, 2]) / 1000.0)
-        if len(flat) >= 9 * n + 5 * nsm + 40:  # unit waits of CTA 0 per phase kind
-            dg = flat[9 * n + 5 * nsm: 9 * n + 5 * nsm + 40].reshape(5, 8)
-            for kk, k in enumerate(("qkv", "o_proj", "gate_up", "down", "lm_head")):
-                nl = s.n_layers if k != "lm_head" else 1
-                cnt = max(1, dg[kk, 3])
-                waits.setdefault(k, []).append((dg[kk, 0] / cnt, dg[kk, 1] / nl, dg[kk, 2] / nl, dg[kk, 3] / nl,
-                                                dg[kk, 4] / cnt, dg[kk, 5] / max(1, cnt - nl)))
+        if len(flat) >= 9 * n + 5 * nsm + 8 * n:  # SM clock stamps of CTA 0 per phase
+            cks = flat[9 * n + 5 * nsm: 9 * n + 5 * nsm + 8 * n].reshape(n, 8)
+            for j, k in enumerate(kinds):
+                c = cks[j]
+                def d(a, b_):
+                    return float(c[b_] - c[a]) if c[a] and c[b_] and c[b_] >= c[a] else float("nan")
+                waits.setdefault(k, []).append((d(0, 1), d(1, 2), d(2, 3), d(3, 4), d(4, 5), d(5, 6), d(6, 7)))
         if len(flat) >= 9 * n + 5 * nsm:  # every CTA's arrival after layer 1's phases
             for kk, k in enumerate(("qkv", "attn", "o_proj", "gate_up", "down")):
                 arr = flat[9 * n + kk * nsm: 9 * n + (kk + 1) * nsm]
@@ -277,9 +277,10 @@ def timeline_persistent(m, s, ids_dev, prompt, rank):
         k: {f: round(float(np.mean(x)), 3) if x else None for f, x in v.items()} for k, v in st.items()},
         "layer1_arrival_spread_us": {k: round(float(np.mean(v)), 3) if v else None for k, v in spread.items()},
         "layer1_latest_ctas": {k: sorted(v.items(), key=lambda kv: -kv[1])[:6] for k, v in late.items()},
-        "cta0_unit_waits": {k: dict(zip(("wait_cycles_per_unit", "not_landed_per_phase", "first_unit_cycles",
-                                         "units_per_phase", "compute_cycles_per_unit", "between_units_cycles"),
-                                        [round(float(x), 2) for x in np.mean(v, axis=0)])) for k, v in waits.items()}}
+        "cta0_cycles": {k: dict(zip(("loads", "reduce", "to_staged", "first_unit", "rest_units", "end_barrier",
+                                     "epilogue"),
+                                    [round(float(x), 1) for x in np.nanmean(np.array(v, dtype=float), axis=0)]))
+                        for k, v in waits.items()}}
     if rank == 0:
         print(json.dumps(out), flush=True)
 

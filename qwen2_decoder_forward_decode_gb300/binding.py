@@ -261,7 +261,7 @@ class Model:
         """[(start_ns, wait_released_ns, end_ns)] per kernel of the last decode step."""
         # a batched step launches the most kernels; the persistent step kernel writes three
         # records per phase and per-CTA barrier arrivals
-        n_max = max(3 + 10 * self.shape.n_layers, 3 * (5 * self.shape.n_layers + 1) + 1024)
+        n_max = max(3 + 10 * self.shape.n_layers, 3 * (5 * self.shape.n_layers + 1) + 2048)
         buf = (ctypes.c_uint64 * (3 * n_max))()
         n = np.zeros(1, dtype=np.int32)
         check(lib().qw_read_timeline(self.h, buf, n_max, _iptr(n)))

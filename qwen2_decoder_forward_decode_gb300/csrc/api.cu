@@ -906,7 +906,7 @@ qw_status qw_set_timeline(qw_model* m, int32_t enable) {
   if (!enable) return QW_OK;
   m->tl_n = 1 + 5 * m->d.L + 1;
   if (m->use_mega)  // three records per phase, then every CTA's arrival after layer 1's phases
-    m->tl_n = std::max(m->tl_n, 3 * (5 * m->d.L + 1) + (5 * m->d.nsm + 40 + 2) / 3);
+    m->tl_n = std::max(m->tl_n, 3 * (5 * m->d.L + 1) + (5 * m->d.nsm + 8 * (5 * m->d.L + 1) + 2) / 3);
   if (m->use_batched) m->tl_n = std::max(m->tl_n, 3 + 10 * m->d.L);  // launches of a batched step
   m->tl_init.assign((size_t)3 * m->tl_n, ~0ull);
   for (int i = 0; i < m->tl_n; ++i) m->tl_init[3 * i + 2] = 0ull;

@@ -256,6 +256,11 @@ __device__ __forceinline__ void att_chunks(int ctx, int& chunk, int& ns) {
   ns = (ctx + chunk - 1) / chunk;
 }
 
+// SM clock stamp idx (< 8) of phase k (CTA 0, thread 0), a plain store
+__device__ __forceinline__ void ck(const Params& p, int k, int idx) {
+  if (p.tl && blockIdx.x == 0 && threadIdx.x == 0) p.tl[9 * (5 * p.L + 1) + 5 * gridDim.x + 8 * k + idx] = clock64();
+}
+
 // L2 requests of this CTA's gate, up and down rows of layer l (they are read by the ring
 // later; asking early keeps HBM streaming while the consumers are in the attention chain)
 __device__ __forceinline__ void mlp_l2_ahead(const Params& p, const LayerW& w) {
@@ -394,7 +399,7 @@ __device__ __forceinline__ void load_xr(float (&xr)[NV][8], const float* xs, int
 // residual x (global, written by other CTAs: read through L2) or, when erow is given, the
 // bf16 embedding row.
 __device__ void stage_norm(const Params& p, float* xs, float* scr, const float* src, const bf16* erow,
-                           const bf16* gain) {
+                           const bf16* gain, int k) {
   const int t = threadIdx.x;
   const int n4 = p.H >> 2;
   float4 v[2];
@@ -418,9 +423,11 @@ __device__ void stage_norm(const Params& p, float* xs, float* scr, const float* 
 #pragma unroll
   for (int i = 0; i < 2; ++i)
     ss = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, fmaf(v[i].w, v[i].w, ss))));
+  ck(p, k, 1);  // the loads have returned
   ss = warp_sum(ss);
   if ((t & 31) == 0) scr[t >> 5] = ss;
   cbar();
+  ck(p, k, 2);  // after the reduction barrier
   float tot = 0.f;
 #pragma unroll
   for (int i = 0; i < NCW; ++i) tot += scr[i];  // fixed order: deterministic
@@ -687,7 +694,7 @@ __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int 
 // o (the attention output of all heads) merged from the chunk partials into xs:
 // o_h = sum_c w_c O_c, w_c = exp(m_c - M) / sum_c' l_c' exp(m_c' - M) (chunk order).
 template <int HD>
-__device__ void stage_merge(const Params& p, float* xs, float* mw, int ns) {
+__device__ void stage_merge(const Params& p, float* xs, float* mw, int ns, int k) {
   const int t = threadIdx.x;
   const int K = p.nq * HD, ps = attn_part_stride(HD);
   const float* part = p.part + (size_t)(blockIdx.x % REP) * p.nq * NSPLIT * ps;  // this CTA's copy
@@ -707,6 +714,7 @@ __device__ void stage_merge(const Params& p, float* xs, float* mw, int ns) {
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
+  ck(p, k, 0);
   load(0);
   for (int i = t; i < p.nq * ns; i += NCT) {
     const int h = i / ns, c = i - h * ns;
@@ -714,7 +722,9 @@ __device__ void stage_merge(const Params& p, float* xs, float* mw, int ns) {
     mw[h * NSPLIT + c] = __ldcg(pp);
     mw[(p.nq + h) * NSPLIT + c] = __ldcg(pp + 1);
   }
+  ck(p, k, 1);
   cbar();
+  ck(p, k, 2);
   for (int h = t; h < p.nq; h += NCT) {  // weights of head h, in chunk order
     float M = -INFINITY;
     for (int c = 0; c < ns; ++c) M = fmaxf(M, mw[h * NSPLIT + c]);
@@ -832,40 +842,17 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
 
   // wait for unit u, apply fn to it, release the slot
   int phase_u = 0;  // units consumed in the current phase
-  // timeline diagnostics (CTA 0, thread 0): per phase kind, cycles waited for units, units
-  // not yet landed when first tested, and cycles of the first unit's wait
-  unsigned long long* diag = p.tl ? p.tl + 9 * (5 * p.L + 1) + 5 * gridDim.x : nullptr;
-  int kind = 0;
-  long long c_last = 0;  // (diagnostics) clock at the end of the previous unit
   auto consume = [&](const Unit& un, auto&& fn) -> bool {
     const long long my = u++;
     const int s = (int)(my % NS);
-    long long c0 = 0;
-    bool ready = true;
-    const bool dg = diag && blockIdx.x == 0 && threadIdx.x == 0;
-    if (dg) {
-      c0 = clock64();
-      if (phase_u > 0) diag[8 * kind + 5] += (unsigned long long)(c0 - c_last);
-      ready = mbar_test_now(full0 + 8 * s, (uint32_t)((my / NS) & 1));
-    }
     const bool ok = __all_sync(0xffffffffu, slot_wait(p, full0 + 8 * s, (uint32_t)((my / NS) & 1)));
-    long long c1 = 0;
-    if (dg) {
-      c1 = clock64();
-      const unsigned long long dc = (unsigned long long)(c1 - c0);
-      diag[8 * kind + 0] += dc;
-      diag[8 * kind + 1] += ready ? 0 : 1;
-      if (phase_u == 0) diag[8 * kind + 2] += dc;
-      diag[8 * kind + 3] += 1;
-    }
     if (!ok) return false;
     fn(smem + (size_t)s * SLOT, un);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
-    if (phase_u++ == 0) tl_mark3(p, ph_idx, 0);
-    if (dg) {
-      c_last = clock64();
-      diag[8 * kind + 4] += (unsigned long long)(c_last - c1);
+    if (phase_u++ == 0) {
+      tl_mark3(p, ph_idx, 0);
+      ck(p, ph_idx, 4);
     }
     return true;
   };
@@ -897,9 +884,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       }
       if (e_head < p.nq + p.nkv) cs = p.rope[(size_t)pos * half + e_i];
     }
-    stage_norm(p, xs, scr, xmine, l == 0 ? erow : nullptr, w.in_norm);
+    ck(p, ph_idx, 0);
+    stage_norm(p, xs, scr, xmine, l == 0 ? erow : nullptr, w.in_norm, ph_idx);
     load_xr(xr, xs, nvecH, lane);
     tl_mark2(p, ph_idx);
+    ck(p, ph_idx, 3);
     {
       const int R = rows_per_slot(p.H);
       const int hp = R / 2;
@@ -911,12 +900,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
         }
       };
-      kind = 0;
       alive = phase_units(p, lt, HD, l, P_QKV, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
+    ck(p, ph_idx, 5);
     alive = cbar_and(alive);
     tl_mark3(p, ph_idx, 1);
+    ck(p, ph_idx, 6);
     if (alive && e_mine) {
       float a = dA[t] + ba, b = dB[t] + bb;
       if (e_head < p.nq + p.nkv) {  // rotate the pair (i, i + hd/2)
@@ -941,6 +931,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       attention_preload<HD>(p, att, l, g, c, chunk, ctx);
     }
     tl_mark3(p, ph_idx, 2);
+    ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (!alive) break;
@@ -954,6 +945,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       attention_chunk<HD>(p, att, l, g, c, chunk, ctx);
     }
     tl_mark3(p, ph_idx, 2);
+    ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
     if (!grid_sync(p, base, nb, s_flag, ph_idx - 1)) { alive = false; break; }
 
@@ -961,9 +953,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
     if (p.pf_mode == 2 && t == 0) mlp_l2_ahead(p, w);
-    stage_merge<HD>(p, xs, mwv, ns);
+    stage_merge<HD>(p, xs, mwv, ns, ph_idx);
     load_xr(xr, xs, (p.nq * HD) >> 3, lane);
     tl_mark2(p, ph_idx);
+    ck(p, ph_idx, 3);
     block_of(p.H, i0, i1);
     {
       const int R = rows_per_slot(p.H);
@@ -974,12 +967,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (lane == 0) dA[un.a - i0 + warp] = d;
         }
       };
-      kind = 1;
       alive = phase_units(p, lt, HD, l, P_OPROJ, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
+    ck(p, ph_idx, 5);
     alive = cbar_and(alive);
     tl_mark3(p, ph_idx, 1);
+    ck(p, ph_idx, 6);
     if (alive)
       if (own) {
         xown += dA[t];
@@ -987,6 +981,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         for (int k = 0; k < REP; ++k) p.x[k * p.H + r0 + t] = xown;
       }
     tl_mark3(p, ph_idx, 2);
+    ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (!alive) break;
@@ -994,9 +989,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     // ===== GATEUP: RMSNorm -> gate/up rows -> SwiGLU
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
-    stage_norm(p, xs, scr, xmine, nullptr, w.post_norm);
+    ck(p, ph_idx, 0);
+    stage_norm(p, xs, scr, xmine, nullptr, w.post_norm, ph_idx);
     load_xr(xr, xs, nvecH, lane);
     tl_mark2(p, ph_idx);
+    ck(p, ph_idx, 3);
     block_of(p.I, i0, i1);
     {
       const int R = rows_per_slot(p.H);
@@ -1009,12 +1006,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
         }
       };
-      kind = 2;
       alive = phase_units(p, lt, HD, l, P_GATEUP, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
+    ck(p, ph_idx, 5);
     alive = cbar_and(alive);
     tl_mark3(p, ph_idx, 1);
+    ck(p, ph_idx, 6);
     if (alive)
       for (int i = i0 + t; i < i1; i += NCT) {
         const float gv = dA[i - i0], uv = dB[i - i0];
@@ -1023,6 +1021,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         for (int k = 0; k < REP; ++k) p.act[(size_t)k * p.I + i] = a;
       }
     tl_mark3(p, ph_idx, 2);
+    ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (!alive) break;
@@ -1047,16 +1046,19 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       }
       block_of(p.H, i0, i1);
       tl_mark2(p, ph_idx);
+      ck(p, ph_idx, 3);
+    ck(p, ph_idx, 3);
       auto fn = [&](const unsigned char* slot, const Unit& un) {
         const float acc = row_dot<NV>(reinterpret_cast<const uint4*>(slot), xr, v0, v1, lane);
         if (lane == 0) dP[(un.a - i0) * NCW + warp] = acc;
       };
-      kind = 3;
       alive = phase_units(p, lt, HD, l, P_DOWN, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
+    ck(p, ph_idx, 5);
     alive = cbar_and(alive);
     tl_mark3(p, ph_idx, 1);
+    ck(p, ph_idx, 6);
     if (alive)
       if (own) {
         float s = 0.f;
@@ -1067,6 +1069,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         for (int k = 0; k < REP; ++k) p.x[k * p.H + r0 + t] = xown;
       }
     tl_mark3(p, ph_idx, 2);
+    ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
   }
@@ -1075,9 +1078,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   if (alive) {
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
-    stage_norm(p, xs, scr, xmine, nullptr, p.final_norm);
+    ck(p, ph_idx, 0);
+    stage_norm(p, xs, scr, xmine, nullptr, p.final_norm, ph_idx);
     load_xr(xr, xs, nvecH, lane);
     tl_mark2(p, ph_idx);
+    ck(p, ph_idx, 3);
     float best_v = -INFINITY;
     int best_i = -1;
     bool bad = false;
@@ -1092,7 +1097,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
           if (z > best_v || best_i < 0) { best_v = z; best_i = r; }  // rows arrive in increasing order
         }
       };
-      kind = 4;
       alive = phase_units(p, lt, HD, p.L, P_LM, [&](const Unit& un) { return consume(un, fn); });
     }
     tl_mark(p, ph_idx, 1);
@@ -1114,6 +1118,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       if (anybad) atomicOr(p.err, ERR_NONFINITE);
     }
     tl_mark3(p, ph_idx, 2);
+    ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
     alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
     if (alive && blockIdx.x == 0 && t == 0) {
