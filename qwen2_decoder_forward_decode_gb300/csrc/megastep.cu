@@ -54,10 +54,7 @@ constexpr int CHUNK_MIN = 32;              // fewest positions per chunk
 constexpr int AT_K = 32;                   // positions per attention tile
 constexpr int GMAX = 8;                    // most query heads per KV head
 constexpr int XS_FLOATS = 2048;            // staged input vector (hidden <= 2048)
-// Vectors that every CTA reads after a grid barrier (the residual stream, the SwiGLU
-// activation, the attention partials) are written REP times at different addresses and CTA b
-// reads copy b % REP, so that 152 CTAs do not all queue on the same L2 lines.
-constexpr int REP = 8;
+
 
 enum : int { P_QKV = 0, P_ATTN = 1, P_OPROJ = 2, P_GATEUP = 3, P_DOWN = 4, P_LM = 5 };
 
@@ -67,7 +64,7 @@ struct LayerW {
 
 // Shared-memory layout (byte offsets from the 1024-aligned base), sized for the model.
 struct Layout {
-  uint32_t att, xs, da, db, dp, mw, lt, bar, scr, total;
+  uint32_t att, xs, da, db, dp, qe, xo, lt, bar, scr, total;
 };
 __host__ __device__ inline uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
 inline Layout make_layout(int hd, int H, int nq, int L) {
@@ -78,7 +75,8 @@ inline Layout make_layout(int hd, int H, int nq, int L) {
   o.da = off; off += MAX_LOCAL * 4;
   o.db = off; off += MAX_LOCAL * 4;
   o.dp = off; off += 64 * NCW * 4;                       // DOWN partials [rows][warps]
-  o.mw = off; off += align16(2u * nq * NSPLIT * 4);      // merge (m, weight) and l
+  o.qe = off; off += MAX_LOCAL * 4 * 4;                  // per q/k/v pair: bias a, bias b, cos, sin
+  o.xo = off; off += 64 * 4;                             // this CTA's residual rows
   o.lt = off; off += align16((uint32_t)L * sizeof(LayerW));  // the layer pointer table
   o.bar = off; off += 2 * NS * 8;
   o.scr = off; off += 64 * 4;
@@ -93,7 +91,7 @@ struct Params {
   const bf16 *embed, *final_norm, *head;
   const float2* rope;        // [cap][hd/2] (cos, sin)
   f16* kv;                   // this sequence's cache [L][2][nkv][cap][hd]
-  float *x, *q, *act, *logits, *part;  // x [REP][H], act [REP][I], part [REP][nq][NSPLIT][hd + 4]
+  float *x, *q, *act, *logits, *part;  // x [H], act [I], part [nq][NSPLIT][hd + 4]
   int *tok, *pos;
   unsigned long long* key;   // packed argmax key (zero between steps)
   int *hist, *hist_n;
@@ -395,61 +393,57 @@ __device__ __forceinline__ void load_xr(float (&xr)[NV][8], const float* xs, int
   }
 }
 
-// xs = src / sqrt(mean(src^2) + eps) * gain over H elements (consumer threads); src is the
-// residual x (global, written by other CTAs: read through L2) or, when erow is given, the
-// bf16 embedding row.
-__device__ void stage_norm(const Params& p, float* xs, float* scr, const float* src, const bf16* erow,
-                           const bf16* gain, int k) {
-  const int t = threadIdx.x;
-  const int n4 = p.H >> 2;
-  float4 v[2];
-  uint2 g[2];
+// gain * src (the residual, or the bf16 embedding row when erow is given) into the register
+// tile as the row phases use it (lane l: vectors l + 32 q of 8 elements); returns
+// 1 / sqrt(mean(src^2) + eps), by which the row results are scaled. Every warp reads and
+// reduces the whole vector itself (same order in every warp): no block barrier.
+template <int NV>
+__device__ __forceinline__ float load_norm_regs(const Params& p, float (&xr)[NV][8], const float* src,
+                                                const bf16* erow, const bf16* gain, int lane) {
+  const int nvec = p.H >> 3;
+  uint4 g[NV];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int j = t + i * NCT;
-    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    g[i] = make_uint2(0u, 0u);
-    if (j < n4) {
+  for (int q = 0; q < NV; ++q) {  // every load first
+    const int v = lane + 32 * q;
+    g[q] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xr[q][e] = 0.f;
+    if (v < nvec) {
       if (erow) {
-        const uint2 e = __ldg(reinterpret_cast<const uint2*>(erow) + j);
-        v[i] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(erow) + v);
+        xr[q][0] = bf_lo(r.x); xr[q][1] = bf_hi(r.x); xr[q][2] = bf_lo(r.y); xr[q][3] = bf_hi(r.y);
+        xr[q][4] = bf_lo(r.z); xr[q][5] = bf_hi(r.z); xr[q][6] = bf_lo(r.w); xr[q][7] = bf_hi(r.w);
       } else {
-        v[i] = __ldcg(reinterpret_cast<const float4*>(src) + j);
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(src) + 2 * v);
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 2 * v + 1);
+        xr[q][0] = a.x; xr[q][1] = a.y; xr[q][2] = a.z; xr[q][3] = a.w;
+        xr[q][4] = b.x; xr[q][5] = b.y; xr[q][6] = b.z; xr[q][7] = b.w;
       }
-      g[i] = __ldg(reinterpret_cast<const uint2*>(gain) + j);
+      g[q] = __ldg(reinterpret_cast<const uint4*>(gain) + v);
     }
   }
   float ss = 0.f;
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
-    ss = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, fmaf(v[i].w, v[i].w, ss))));
-  ck(p, k, 1);  // the loads have returned
-  ss = warp_sum(ss);
-  if ((t & 31) == 0) scr[t >> 5] = ss;
-  cbar();
-  ck(p, k, 2);  // after the reduction barrier
-  float tot = 0.f;
+  for (int q = 0; q < NV; ++q) {
 #pragma unroll
-  for (int i = 0; i < NCW; ++i) tot += scr[i];  // fixed order: deterministic
-  const float inv = rsqrtf(tot / (float)p.H + p.eps);
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int j = t + i * NCT;
-    if (j < n4)
-      reinterpret_cast<float4*>(xs)[j] = make_float4(v[i].x * inv * bf_lo(g[i].x), v[i].y * inv * bf_hi(g[i].x),
-                                                     v[i].z * inv * bf_lo(g[i].y), v[i].w * inv * bf_hi(g[i].y));
+    for (int e = 0; e < 8; ++e) ss = fmaf(xr[q][e], xr[q][e], ss);
+    xr[q][0] *= bf_lo(g[q].x); xr[q][1] *= bf_hi(g[q].x); xr[q][2] *= bf_lo(g[q].y); xr[q][3] *= bf_hi(g[q].y);
+    xr[q][4] *= bf_lo(g[q].z); xr[q][5] *= bf_hi(g[q].z); xr[q][6] *= bf_lo(g[q].w); xr[q][7] *= bf_hi(g[q].w);
   }
-  cbar();
+  ss = warp_sum(ss);
+  return rsqrtf(ss / (float)p.H + p.eps);
 }
 
 // Grid barrier of the consumers of all CTAs: each CTA adds one to a monotonic counter and
-// waits until it reaches base + nb * CTAs. Returns false (uniformly) after an abort.
-__device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int* s_flag, int k) {
-  cbar();
+// waits until it reaches base + nb * CTAs. ok is this thread's status; the result (the same
+// for every consumer thread of the CTA) is false if any consumer thread of the CTA, or any
+// CTA's wait, gave up.
+__device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int* s_flag, int k, bool ok) {
+  const bool all_ok = cbar_and(ok);
   ++nb;
   if (threadIdx.x == 0) {
-    int ok = 0;
-    if (!aborted(p)) {
+    int res = 0;
+    if (all_ok && !aborted(p)) {
       // release: this CTA's writes of the phase (ordered before by the consumer barrier)
       asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.bar), "l"(1ull) : "memory");
       if (p.tl) {
@@ -460,18 +454,18 @@ __device__ bool grid_sync(const Params& p, unsigned long long base, int& nb, int
       }
       const unsigned long long target = base + (unsigned long long)nb * gridDim.x;
       const long long t0 = clock64();
-      ok = 1;
+      res = 1;
       for (int it = 0;; ++it) {
         unsigned long long v;
         asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p.bar) : "memory");
         if (v >= target) break;
         if ((it & 15) == 15) {
-          if (aborted(p)) { ok = 0; break; }
-          if (clock64() - t0 > WAIT_CYCLES) { raise_abort(p); ok = 0; break; }
+          if (aborted(p)) { res = 0; break; }
+          if (clock64() - t0 > WAIT_CYCLES) { raise_abort(p); res = 0; break; }
         }
       }
     }
-    *s_flag = ok;
+    *s_flag = res;
     if (p.tl && blockIdx.x == 0) p.tl[3 * (5 * p.L + 1 + k) + 1] = gtime();
   }
   cbar();
@@ -669,9 +663,7 @@ __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int 
       const float mw = cM[w * 16 + r];
       if (mw != -INFINITY) acc = fmaf(expf(mw - M), cO[(size_t)(w * 16 + r) * HD + d], acc);
     }
-    const size_t off = ((size_t)(g * G + r) * NSPLIT + c) * ps + d, rs = (size_t)p.nq * NSPLIT * ps;
-#pragma unroll
-    for (int k = 0; k < REP; ++k) p.part[k * rs + off] = acc;
+    p.part[((size_t)(g * G + r) * NSPLIT + c) * ps + d] = acc;
   }
   if (t < G) {
     const float M = fmaxf(cM[t], cM[16 + t]);
@@ -681,87 +673,76 @@ __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int 
       const float mw = cM[w * 16 + t];
       if (mw != -INFINITY) L = fmaf(expf(mw - M), cL[w * 16 + t], L);
     }
-    const size_t rs = (size_t)p.nq * NSPLIT * ps;
     float* pp = p.part + ((size_t)(g * G + t) * NSPLIT + c) * ps;
-#pragma unroll
-    for (int k = 0; k < REP; ++k) {
-      pp[k * rs + HD] = M;
-      pp[k * rs + HD + 1] = L;
-    }
+    pp[HD] = M;
+    pp[HD + 1] = L;
   }
 }
 
 // o (the attention output of all heads) merged from the chunk partials into xs:
-// o_h = sum_c w_c O_c, w_c = exp(m_c - M) / sum_c' l_c' exp(m_c' - M) (chunk order).
+// o_h = sum_c w_c O_c / sum_c w_c l_c, w_c = exp(m_c - M), M = max_c m_c (chunk order).
+// Thread t merges the 4-element groups t and t + NCT, computing its heads' weights itself,
+// so the partials, maxima and sums it needs are requested together (one round trip for up to
+// MB chunks; a running maximum carries across batches).
 template <int HD>
-__device__ void stage_merge(const Params& p, float* xs, float* mw, int ns, int k) {
+__device__ void stage_merge(const Params& p, float* xs, int ns) {
   const int t = threadIdx.x;
-  const int K = p.nq * HD, ps = attn_part_stride(HD);
-  const float* part = p.part + (size_t)(blockIdx.x % REP) * p.nq * NSPLIT * ps;  // this CTA's copy
-  constexpr int MB = 8;  // chunks per batch of loads
-  // (m, l) of every (head, chunk), requested together with the first batch of outputs
-  const int groups = K / 4;  // float4 groups; thread t takes groups t and t + NCT
-  float4 v[2][MB];
-  auto load = [&](int c0) {
+  const int ps = attn_part_stride(HD), groups = p.nq * HD / 4;
+  constexpr int MB = 8;
+  float4 acc[2];
+  float M[2], L[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    M[e] = -INFINITY;
+    L[e] = 0.f;
+  }
+  for (int c0 = 0; c0 < ns; c0 += MB) {
+    float4 v[2][MB];
+    float2 ml[2][MB];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int gi = t + e * NCT;
       const int h = (4 * gi) / HD, d = 4 * gi - h * HD;
+      const float* base = p.part + (size_t)h * NSPLIT * ps;
 #pragma unroll
-      for (int u = 0; u < MB; ++u)
-        v[e][u] = (gi < groups && c0 + u < ns)
-                      ? __ldcg(reinterpret_cast<const float4*>(part + ((size_t)h * NSPLIT + c0 + u) * ps + d))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < MB; ++u) {
+        const bool in = gi < groups && c0 + u < ns;
+        v[e][u] = in ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)(c0 + u) * ps + d))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        ml[e][u] = in ? __ldcg(reinterpret_cast<const float2*>(base + (size_t)(c0 + u) * ps + HD))
+                      : make_float2(-INFINITY, 0.f);
+      }
     }
-  };
-  ck(p, k, 0);
-  load(0);
-  for (int i = t; i < p.nq * ns; i += NCT) {
-    const int h = i / ns, c = i - h * ns;
-    const float* pp = part + ((size_t)h * NSPLIT + c) * ps + HD;
-    mw[h * NSPLIT + c] = __ldcg(pp);
-    mw[(p.nq + h) * NSPLIT + c] = __ldcg(pp + 1);
-  }
-  ck(p, k, 1);
-  cbar();
-  ck(p, k, 2);
-  for (int h = t; h < p.nq; h += NCT) {  // weights of head h, in chunk order
-    float M = -INFINITY;
-    for (int c = 0; c < ns; ++c) M = fmaxf(M, mw[h * NSPLIT + c]);
-    float L = 0.f;
-    for (int c = 0; c < ns; ++c) {
-      const float e = expf(mw[h * NSPLIT + c] - M);
-      mw[h * NSPLIT + c] = e;
-      L = fmaf(mw[(p.nq + h) * NSPLIT + c], e, L);
-    }
-    const float inv = 1.f / L;
-    for (int c = 0; c < ns; ++c) mw[h * NSPLIT + c] *= inv;
-  }
-  cbar();
-  float4 acc[2];
-  acc[0] = acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < ns; c0 += MB) {
-    if (c0) load(c0);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int gi = t + e * NCT;
-      if (gi >= groups) continue;
-      const int h = (4 * gi) / HD;
+      float mb = M[e];
 #pragma unroll
-      for (int u = 0; u < MB; ++u)
-        if (c0 + u < ns) {
-          const float wgt = mw[h * NSPLIT + c0 + u];
-          acc[e].x = fmaf(v[e][u].x, wgt, acc[e].x);
-          acc[e].y = fmaf(v[e][u].y, wgt, acc[e].y);
-          acc[e].z = fmaf(v[e][u].z, wgt, acc[e].z);
-          acc[e].w = fmaf(v[e][u].w, wgt, acc[e].w);
-        }
+      for (int u = 0; u < MB; ++u) mb = fmaxf(mb, ml[e][u].x);
+      if (mb == -INFINITY) continue;  // (groups past the vector)
+      const float r = M[e] == -INFINITY ? 0.f : expf(M[e] - mb);  // rescale the earlier batches
+      acc[e].x *= r; acc[e].y *= r; acc[e].z *= r; acc[e].w *= r;
+      L[e] *= r;
+#pragma unroll
+      for (int u = 0; u < MB; ++u) {
+        if (ml[e][u].x == -INFINITY) continue;
+        const float wgt = expf(ml[e][u].x - mb);
+        L[e] = fmaf(ml[e][u].y, wgt, L[e]);
+        acc[e].x = fmaf(v[e][u].x, wgt, acc[e].x);
+        acc[e].y = fmaf(v[e][u].y, wgt, acc[e].y);
+        acc[e].z = fmaf(v[e][u].z, wgt, acc[e].z);
+        acc[e].w = fmaf(v[e][u].w, wgt, acc[e].w);
+      }
+      M[e] = mb;
     }
   }
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     const int gi = t + e * NCT;
-    if (gi < groups) reinterpret_cast<float4*>(xs)[gi] = acc[e];
+    if (gi < groups) {
+      const float inv = 1.f / L[e];
+      reinterpret_cast<float4*>(xs)[gi] = make_float4(acc[e].x * inv, acc[e].y * inv, acc[e].z * inv, acc[e].w * inv);
+    }
   }
   cbar();
 }
@@ -779,18 +760,49 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   float* dA = reinterpret_cast<float*>(smem + p.lay.da);
   float* dB = reinterpret_cast<float*>(smem + p.lay.db);
   float* dP = reinterpret_cast<float*>(smem + p.lay.dp);
-  float* mwv = reinterpret_cast<float*>(smem + p.lay.mw);
+  float* qe = reinterpret_cast<float*>(smem + p.lay.qe);
+  float* xo = reinterpret_cast<float*>(smem + p.lay.xo);
   LayerW* lt = reinterpret_cast<LayerW*>(smem + p.lay.lt);
   unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + p.lay.bar);
   float* scr = reinterpret_cast<float*>(smem + p.lay.scr);
   int* s_flag = reinterpret_cast<int*>(scr + 48);
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + NS);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int half = HD >> 1;
+  const int npairs = (p.nq + 2 * p.nkv) * half;
 
   // the position and the token were written by the previous step (or the prefill), before
   // this launch; the key is zero between steps
   const int pos = __ldcg(p.pos);
   const int ctx = pos + 1;
+  int tok = __ldcg(p.tok);
+  if (tok < 0 || tok >= p.V) {
+    if (t == 0 && blockIdx.x == 0) atomicOr(p.err, ERR_TOKEN);
+    tok = 0;
+  }
+  const bf16* erow = p.embed + (size_t)tok * p.H;
+  int r0, r1;  // this CTA's residual rows (the o_proj and down rows)
+  block_of(p.H, r0, r1);
+  int q0, q1;  // this CTA's q/k/v pairs
+  block_of(npairs, q0, q1);
+  // per pair of layer l: bias of both rows and the rotation at pos (weights and the position
+  // only: ready before the phase)
+  auto fill_qe = [&](const LayerW& w) {
+    for (int i = t; i < q1 - q0; i += NCT) {
+      const int item = q0 + i, head = item / half, e = item - head * half;
+      const bf16* bias;
+      int hh;
+      if (head < p.nq) { bias = w.bq; hh = head; }
+      else if (head < p.nq + p.nkv) { bias = w.bk; hh = head - p.nq; }
+      else { bias = w.bv; hh = head - p.nq - p.nkv; }
+      float2 cs = make_float2(1.f, 0.f);
+      if (head < p.nq + p.nkv) cs = p.rope[(size_t)pos * half + e];
+      qe[4 * i + 0] = bias ? __bfloat162float(bias[hh * HD + e]) : 0.f;
+      qe[4 * i + 1] = bias ? __bfloat162float(bias[hh * HD + e + half]) : 0.f;
+      qe[4 * i + 2] = cs.x;
+      qe[4 * i + 3] = cs.y;
+    }
+  };
   if (t == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -804,6 +816,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     unsigned long long* dst = reinterpret_cast<unsigned long long*>(lt);
     for (int i = t; i < n8; i += THREADS) dst[i] = __ldg(src + i);
   }
+  if (t < NCT) {
+    fill_qe(reinterpret_cast<const LayerW*>(p.layers)[0]);
+    // the residual stream starts as the embedding row (this CTA's rows)
+    for (int i = t; i < r1 - r0; i += NCT) {
+      xo[i] = __bfloat162float(erow[r0 + i]);
+      p.x[r0 + i] = xo[i];
+    }
+  }
   __syncthreads();  // the only block-wide barrier: producers and consumers part here
 
   if (warp >= NCW) {
@@ -815,32 +835,15 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   const unsigned long long base = __ldcg(p.bar_base);
   int nb = 0;        // grid barriers passed
   long long u = 0;   // unit counter
-  int tok = __ldcg(p.tok);
-  if (tok < 0 || tok >= p.V) {
-    if (t == 0 && blockIdx.x == 0) atomicOr(p.err, ERR_TOKEN);
-    tok = 0;
-  }
-  const bf16* erow = p.embed + (size_t)tok * p.H;
-  const int half = HD >> 1;
   const int nvecH = p.H >> 3;
+  const size_t rowH = (size_t)p.H * 2;
   int chunk, ns;
   att_chunks(ctx, chunk, ns);
-  // The residual rows this CTA updates (o_proj and down rows r0 + t, one per thread) stay
-  // in a register; the stream starts as the embedding row.
-  int r0, r1;
-  block_of(p.H, r0, r1);
-  const bool own = t < r1 - r0;
-  float xown = own ? __bfloat162float(erow[r0 + t]) : 0.f;
-  if (own)
-#pragma unroll
-    for (int k = 0; k < REP; ++k) p.x[k * p.H + r0 + t] = xown;
-  const float* xmine = p.x + (size_t)(blockIdx.x % REP) * p.H;      // this CTA's copies
-  const float* actmine = p.act + (size_t)(blockIdx.x % REP) * p.I;
   float xr[NV][8];
   bool alive = true;
   int ph_idx = 0;  // timeline index
 
-  // wait for unit u, apply fn to it, release the slot
+  // wait for unit u, apply fn to it (fn sees the unit's index in its phase), release the slot
   int phase_u = 0;  // units consumed in the current phase
   auto consume = [&](const Unit& un, auto&& fn) -> bool {
     const long long my = u++;
@@ -856,179 +859,132 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     }
     return true;
   };
+  // In the paired phases (q/k/v: rows i, i + hd/2 of a RoPE pair; gate/up: gate row i, up row
+  // i) a unit holds up to 4 pairs: pair j in row j of the first and of the second copy. The
+  // units of a phase alternate between warps 0-3 and 4-7; warp w takes pair w % 4 of its
+  // units, both rows, and finishes the pair itself.
+  const int pj = warp & 3, pgroup = warp >> 2;
 
   for (int l = 0; l < p.L && alive; ++l) {
     const LayerW& w = lt[l];
     // ===== QKV: RMSNorm -> q/k/v rows (+ bias) -> RoPE -> q out, K/V append
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
-    int i0, i1;
-    block_of((p.nq + 2 * p.nkv) * half, i0, i1);
-    // epilogue inputs of this thread's pair (independent of the barrier's data)
-    float ba = 0.f, bb = 0.f;
-    float2 cs = make_float2(1.f, 0.f);
-    int e_head = 0, e_i = 0;
-    const bool e_mine = t < i1 - i0;
-    if (e_mine) {
-      const int item = i0 + t;
-      e_head = item / half;
-      e_i = item - e_head * half;
-      const bf16* bias;
-      int hh;
-      if (e_head < p.nq) { bias = w.bq; hh = e_head; }
-      else if (e_head < p.nq + p.nkv) { bias = w.bk; hh = e_head - p.nq; }
-      else { bias = w.bv; hh = e_head - p.nq - p.nkv; }
-      if (bias) {
-        ba = __bfloat162float(bias[hh * HD + e_i]);
-        bb = __bfloat162float(bias[hh * HD + e_i + half]);
-      }
-      if (e_head < p.nq + p.nkv) cs = p.rope[(size_t)pos * half + e_i];
-    }
-    ck(p, ph_idx, 0);
-    stage_norm(p, xs, scr, xmine, l == 0 ? erow : nullptr, w.in_norm, ph_idx);
-    load_xr(xr, xs, nvecH, lane);
-    tl_mark2(p, ph_idx);
-    ck(p, ph_idx, 3);
-    {
-      const int R = rows_per_slot(p.H);
-      const int hp = R / 2;
-      auto fn = [&](const unsigned char* slot, const Unit& un) {
-        const int j = warp < hp ? warp : warp - hp;
-        if (warp < R && j < un.n) {
-          const unsigned char* row = slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2;
-          const float d = row_dot<NV>(reinterpret_cast<const uint4*>(row), xr, 0, nvecH, lane);
-          if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
-        }
-      };
-      alive = phase_units(p, lt, HD, l, P_QKV, [&](const Unit& un) { return consume(un, fn); });
-    }
-    tl_mark(p, ph_idx, 1);
-    ck(p, ph_idx, 5);
-    alive = cbar_and(alive);
-    tl_mark3(p, ph_idx, 1);
-    ck(p, ph_idx, 6);
-    if (alive && e_mine) {
-      float a = dA[t] + ba, b = dB[t] + bb;
-      if (e_head < p.nq + p.nkv) {  // rotate the pair (i, i + hd/2)
-        const float ra = a * cs.x - b * cs.y, rb = b * cs.x + a * cs.y;
-        a = ra;
-        b = rb;
-      }
-      if (e_head < p.nq) {
-        p.q[e_head * HD + e_i] = a;
-        p.q[e_head * HD + e_i + half] = b;
-      } else {
-        const bool is_k = e_head < p.nq + p.nkv;
-        const int hh = is_k ? e_head - p.nq : e_head - p.nq - p.nkv;
-        f16* dst = p.kv + (size_t)l * 2 * p.nkv * p.cap * HD + (is_k ? 0 : (size_t)p.nkv * p.cap * HD) +
-                   ((size_t)hh * p.cap + pos) * HD;
-        store_kv(dst + e_i, a, p.err);
-        store_kv(dst + e_i + half, b, p.err);
-      }
-    }
-    if (alive && (int)blockIdx.x < p.nkv * ns) {
+    if ((int)blockIdx.x < p.nkv * ns) {  // the first attention tile's rows of earlier steps
       const int g = blockIdx.x / ns, c = blockIdx.x - g * ns;
       attention_preload<HD>(p, att, l, g, c, chunk, ctx);
     }
+    ck(p, ph_idx, 0);
+    float inv = load_norm_regs<NV>(p, xr, p.x, l == 0 ? erow : nullptr, w.in_norm, lane);
+    tl_mark2(p, ph_idx);
+    ck(p, ph_idx, 3);
+    alive = phase_units(p, lt, HD, l, P_QKV, [&](const Unit& un) {
+      return consume(un, [&](const unsigned char* slot, const Unit& v) {
+        if (pgroup != (phase_u & 1) || pj >= v.n) return;
+        float a = row_dot<NV>(reinterpret_cast<const uint4*>(slot + pj * rowH), xr, 0, nvecH, lane) * inv;
+        float b = row_dot<NV>(reinterpret_cast<const uint4*>(slot + v.off2 + pj * rowH), xr, 0, nvecH, lane) * inv;
+        if (lane == 0) {
+          const int pi = v.a + pj - q0, item = v.a + pj, head = item / half, e = item - head * half;
+          a += qe[4 * pi + 0];
+          b += qe[4 * pi + 1];
+          if (head < p.nq + p.nkv) {  // rotate the pair (e, e + hd/2)
+            const float c = qe[4 * pi + 2], sn = qe[4 * pi + 3];
+            const float ra = a * c - b * sn, rb = b * c + a * sn;
+            a = ra;
+            b = rb;
+          }
+          if (head < p.nq) {
+            p.q[head * HD + e] = a;
+            p.q[head * HD + e + half] = b;
+          } else {
+            const bool is_k = head < p.nq + p.nkv;
+            const int hh = is_k ? head - p.nq : head - p.nq - p.nkv;
+            f16* dst = p.kv + (size_t)l * 2 * p.nkv * p.cap * HD + (is_k ? 0 : (size_t)p.nkv * p.cap * HD) +
+                       ((size_t)hh * p.cap + pos) * HD;
+            store_kv(dst + e, a, p.err);
+            store_kv(dst + e + half, b, p.err);
+          }
+        }
+      });
+    });
+    tl_mark(p, ph_idx, 1);
+    ck(p, ph_idx, 5);
     tl_mark3(p, ph_idx, 2);
     ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
-    alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
+    alive = grid_sync(p, base, nb, s_flag, ph_idx - 1, alive);
     if (!alive) break;
 
     // ===== ATTN: (KV head, chunk) partials
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
-    if (p.pf_mode == 1 && t == 0) mlp_l2_ahead(p, w);
     if ((int)blockIdx.x < p.nkv * ns) {
       const int g = blockIdx.x / ns, c = blockIdx.x - g * ns;
       attention_chunk<HD>(p, att, l, g, c, chunk, ctx);
     }
     tl_mark3(p, ph_idx, 2);
-    ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
-    if (!grid_sync(p, base, nb, s_flag, ph_idx - 1)) { alive = false; break; }
-
-    // ===== OPROJ: merge -> x += Wo o
-    tl_mark(p, ph_idx, 0);
-    phase_u = 0;
-    if (p.pf_mode == 2 && t == 0) mlp_l2_ahead(p, w);
-    stage_merge<HD>(p, xs, mwv, ns, ph_idx);
-    load_xr(xr, xs, (p.nq * HD) >> 3, lane);
-    tl_mark2(p, ph_idx);
-    ck(p, ph_idx, 3);
-    block_of(p.H, i0, i1);
-    {
-      const int R = rows_per_slot(p.H);
-      auto fn = [&](const unsigned char* slot, const Unit& un) {
-        if (warp < R && warp < un.n) {
-          const float d =
-              row_dot<NV>(reinterpret_cast<const uint4*>(slot + (size_t)warp * p.H * 2), xr, 0, (p.nq * HD) >> 3, lane);
-          if (lane == 0) dA[un.a - i0 + warp] = d;
-        }
-      };
-      alive = phase_units(p, lt, HD, l, P_OPROJ, [&](const Unit& un) { return consume(un, fn); });
-    }
-    tl_mark(p, ph_idx, 1);
-    ck(p, ph_idx, 5);
-    alive = cbar_and(alive);
-    tl_mark3(p, ph_idx, 1);
-    ck(p, ph_idx, 6);
-    if (alive)
-      if (own) {
-        xown += dA[t];
-#pragma unroll
-        for (int k = 0; k < REP; ++k) p.x[k * p.H + r0 + t] = xown;
-      }
-    tl_mark3(p, ph_idx, 2);
-    ck(p, ph_idx, 7);
-    tl_mark(p, ph_idx++, 2);
-    alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
+    alive = grid_sync(p, base, nb, s_flag, ph_idx - 1, true);
     if (!alive) break;
 
-    // ===== GATEUP: RMSNorm -> gate/up rows -> SwiGLU
+    // ===== OPROJ: merge -> x += Wo o (each row's warp updates the CTA's residual row)
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
     ck(p, ph_idx, 0);
-    stage_norm(p, xs, scr, xmine, nullptr, w.post_norm, ph_idx);
-    load_xr(xr, xs, nvecH, lane);
+    stage_merge<HD>(p, xs, ns);
+    load_xr(xr, xs, (p.nq * HD) >> 3, lane);
     tl_mark2(p, ph_idx);
     ck(p, ph_idx, 3);
-    block_of(p.I, i0, i1);
     {
       const int R = rows_per_slot(p.H);
-      const int hp = R / 2;
-      auto fn = [&](const unsigned char* slot, const Unit& un) {
-        const int j = warp < hp ? warp : warp - hp;
-        if (warp < R && j < un.n) {
-          const unsigned char* row = slot + (warp < hp ? 0u : un.off2) + (size_t)j * p.H * 2;
-          const float d = row_dot<NV>(reinterpret_cast<const uint4*>(row), xr, 0, nvecH, lane);
-          if (lane == 0) (warp < hp ? dA : dB)[un.a - i0 + j] = d;
-        }
-      };
-      alive = phase_units(p, lt, HD, l, P_GATEUP, [&](const Unit& un) { return consume(un, fn); });
+      alive = phase_units(p, lt, HD, l, P_OPROJ, [&](const Unit& un) {
+        return consume(un, [&](const unsigned char* slot, const Unit& v) {
+          if (warp >= R || warp >= v.n) return;
+          const float d = row_dot<NV>(reinterpret_cast<const uint4*>(slot + (size_t)warp * rowH), xr, 0,
+                                      (p.nq * HD) >> 3, lane);
+          if (lane == 0) {
+            const int r = v.a + warp;
+            xo[r - r0] += d;
+            p.x[r] = xo[r - r0];
+          }
+        });
+      });
     }
     tl_mark(p, ph_idx, 1);
     ck(p, ph_idx, 5);
-    alive = cbar_and(alive);
-    tl_mark3(p, ph_idx, 1);
-    ck(p, ph_idx, 6);
-    if (alive)
-      for (int i = i0 + t; i < i1; i += NCT) {
-        const float gv = dA[i - i0], uv = dB[i - i0];
-        const float a = (gv / (1.f + expf(-gv))) * uv;
-#pragma unroll
-        for (int k = 0; k < REP; ++k) p.act[(size_t)k * p.I + i] = a;
-      }
     tl_mark3(p, ph_idx, 2);
     ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
-    alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
+    alive = grid_sync(p, base, nb, s_flag, ph_idx - 1, alive);
+    if (!alive) break;
+
+    // ===== GATEUP: RMSNorm -> gate/up rows -> SwiGLU (each pair's warp writes its output)
+    tl_mark(p, ph_idx, 0);
+    phase_u = 0;
+    ck(p, ph_idx, 0);
+    inv = load_norm_regs<NV>(p, xr, p.x, nullptr, w.post_norm, lane);
+    tl_mark2(p, ph_idx);
+    ck(p, ph_idx, 3);
+    alive = phase_units(p, lt, HD, l, P_GATEUP, [&](const Unit& un) {
+      return consume(un, [&](const unsigned char* slot, const Unit& v) {
+        if (pgroup != (phase_u & 1) || pj >= v.n) return;
+        const float gv = row_dot<NV>(reinterpret_cast<const uint4*>(slot + pj * rowH), xr, 0, nvecH, lane) * inv;
+        const float uv = row_dot<NV>(reinterpret_cast<const uint4*>(slot + v.off2 + pj * rowH), xr, 0, nvecH, lane) * inv;
+        if (lane == 0) p.act[v.a + pj] = (gv / (1.f + expf(-gv))) * uv;
+      });
+    });
+    tl_mark(p, ph_idx, 1);
+    ck(p, ph_idx, 5);
+    tl_mark3(p, ph_idx, 2);
+    ck(p, ph_idx, 7);
+    tl_mark(p, ph_idx++, 2);
+    alive = grid_sync(p, base, nb, s_flag, ph_idx - 1, alive);
     if (!alive) break;
 
     // ===== DOWN: x += Wd act, each row's K split over the eight warps
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
+    ck(p, ph_idx, 0);
     {
       const int nvecI = p.I >> 3;
       const int segv = (nvecI + NCW - 1) / NCW;
@@ -1038,21 +994,20 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         const int v = v0 + lane + 32 * qd;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
         if (v < v1) {
-          a = __ldcg(reinterpret_cast<const float4*>(actmine) + 2 * v);
-          b = __ldcg(reinterpret_cast<const float4*>(actmine) + 2 * v + 1);
+          a = __ldcg(reinterpret_cast<const float4*>(p.act) + 2 * v);
+          b = __ldcg(reinterpret_cast<const float4*>(p.act) + 2 * v + 1);
         }
         xr[qd][0] = a.x; xr[qd][1] = a.y; xr[qd][2] = a.z; xr[qd][3] = a.w;
         xr[qd][4] = b.x; xr[qd][5] = b.y; xr[qd][6] = b.z; xr[qd][7] = b.w;
       }
-      block_of(p.H, i0, i1);
       tl_mark2(p, ph_idx);
       ck(p, ph_idx, 3);
-    ck(p, ph_idx, 3);
-      auto fn = [&](const unsigned char* slot, const Unit& un) {
-        const float acc = row_dot<NV>(reinterpret_cast<const uint4*>(slot), xr, v0, v1, lane);
-        if (lane == 0) dP[(un.a - i0) * NCW + warp] = acc;
-      };
-      alive = phase_units(p, lt, HD, l, P_DOWN, [&](const Unit& un) { return consume(un, fn); });
+      alive = phase_units(p, lt, HD, l, P_DOWN, [&](const Unit& un) {
+        return consume(un, [&](const unsigned char* slot, const Unit& v) {
+          const float acc = row_dot<NV>(reinterpret_cast<const uint4*>(slot), xr, v0, v1, lane);
+          if (lane == 0) dP[(v.a - r0) * NCW + warp] = acc;
+        });
+      });
     }
     tl_mark(p, ph_idx, 1);
     ck(p, ph_idx, 5);
@@ -1060,18 +1015,18 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     tl_mark3(p, ph_idx, 1);
     ck(p, ph_idx, 6);
     if (alive)
-      if (own) {
-        float s = 0.f;
+      for (int i = t; i < r1 - r0; i += NCT) {
+        float sum = 0.f;
 #pragma unroll
-        for (int k = 0; k < NCW; ++k) s += dP[t * NCW + k];  // warp order
-        xown += s;
-#pragma unroll
-        for (int k = 0; k < REP; ++k) p.x[k * p.H + r0 + t] = xown;
+        for (int k = 0; k < NCW; ++k) sum += dP[i * NCW + k];  // warp order
+        xo[i] += sum;
+        p.x[r0 + i] = xo[i];
       }
+    if (l + 1 < p.L) fill_qe(lt[l + 1]);  // the next layer's pair inputs
     tl_mark3(p, ph_idx, 2);
     ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
-    alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
+    alive = grid_sync(p, base, nb, s_flag, ph_idx - 1, alive);
   }
 
   // ===== LM head: final RMSNorm -> logits -> greedy argmax
@@ -1079,8 +1034,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
     ck(p, ph_idx, 0);
-    stage_norm(p, xs, scr, xmine, nullptr, p.final_norm, ph_idx);
-    load_xr(xr, xs, nvecH, lane);
+    const float inv = load_norm_regs<NV>(p, xr, p.x, nullptr, p.final_norm, lane);
     tl_mark2(p, ph_idx);
     ck(p, ph_idx, 3);
     float best_v = -INFINITY;
@@ -1088,24 +1042,26 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     bool bad = false;
     {
       const int R = rows_per_slot(p.H);
-      auto fn = [&](const unsigned char* slot, const Unit& un) {
-        if (warp < R && warp < un.n) {
-          const float z = row_dot<NV>(reinterpret_cast<const uint4*>(slot + (size_t)warp * p.H * 2), xr, 0, nvecH, lane);
-          const int r = un.a + warp;
+      alive = phase_units(p, lt, HD, p.L, P_LM, [&](const Unit& un) {
+        return consume(un, [&](const unsigned char* slot, const Unit& v) {
+          if (warp >= R || warp >= v.n) return;
+          const float z = row_dot<NV>(reinterpret_cast<const uint4*>(slot + (size_t)warp * rowH), xr, 0, nvecH, lane) * inv;
+          const int r = v.a + warp;
           if (lane == 0) p.logits[r] = z;
           if (!isfinite(z)) bad = true;
           if (z > best_v || best_i < 0) { best_v = z; best_i = r; }  // rows arrive in increasing order
-        }
-      };
-      alive = phase_units(p, lt, HD, p.L, P_LM, [&](const Unit& un) { return consume(un, fn); });
+        });
+      });
     }
     tl_mark(p, ph_idx, 1);
+    ck(p, ph_idx, 5);
     if (lane == 0) {
       reinterpret_cast<unsigned long long*>(dP)[warp] = best_i >= 0 ? argmax_key(best_v, best_i) : 0ull;
       reinterpret_cast<int*>(dA)[warp] = bad;
     }
     alive = cbar_and(alive);
     tl_mark3(p, ph_idx, 1);
+    ck(p, ph_idx, 6);
     if (alive && t == 0) {
       unsigned long long k = 0;
       int anybad = 0;
@@ -1120,7 +1076,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     tl_mark3(p, ph_idx, 2);
     ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
-    alive = alive && grid_sync(p, base, nb, s_flag, ph_idx - 1);
+    alive = grid_sync(p, base, nb, s_flag, ph_idx - 1, alive);
     if (alive && blockIdx.x == 0 && t == 0) {
       const unsigned long long k = atomicAdd(p.key, 0ull);
       const int idx = argmax_key_index(k);
@@ -1178,8 +1134,8 @@ static const void* megastep_fn(const Dims& d) {
                  : nv == 6 ? (const void*)mk::decode_step_kernel<64, 6> : (const void*)mk::decode_step_kernel<64, 8>;
 }
 
-size_t megastep_work_floats(const Dims& d) {  // x, act and partial copies
-  return (size_t)mk::REP * ((size_t)d.H + d.I + (size_t)d.nq * mk::NSPLIT * attn_part_stride(d.hd));
+size_t megastep_work_floats(const Dims& d) {  // x, act and the attention partials
+  return (size_t)d.H + d.I + (size_t)d.nq * mk::NSPLIT * attn_part_stride(d.hd);
 }
 
 
@@ -1210,8 +1166,8 @@ cudaError_t launch_megastep(const MegaLaunch& a, cudaStream_t s) {
   p.embed = (const bf16*)a.embed; p.final_norm = (const bf16*)a.final_norm; p.head = (const bf16*)a.head;
   p.rope = a.rope; p.kv = (f16*)a.kv_seq;
   p.x = a.work;
-  p.act = a.work + (size_t)mk::REP * a.d.H;
-  p.part = a.work + (size_t)mk::REP * (a.d.H + a.d.I);
+  p.act = a.work + a.d.H;
+  p.part = a.work + a.d.H + a.d.I;
   p.q = a.q; p.logits = a.logits;
   p.tok = a.tok; p.pos = a.pos; p.key = a.key; p.hist = a.hist; p.hist_n = a.hist_n; p.hist_cap = a.hist_cap;
   p.bar = a.bar; p.bar_base = a.bar_base; p.abort = a.abort; p.err = a.err; p.tl = a.tl;
