@@ -393,45 +393,50 @@ __device__ __forceinline__ void load_xr(float (&xr)[NV][8], const float* xs, int
   }
 }
 
-// gain * src (the residual, or the bf16 embedding row when erow is given) into the register
-// tile as the row phases use it (lane l: vectors l + 32 q of 8 elements); returns
-// 1 / sqrt(mean(src^2) + eps), by which the row results are scaled. Every warp reads and
-// reduces the whole vector itself (same order in every warp): no block barrier.
-template <int NV>
-__device__ __forceinline__ float load_norm_regs(const Params& p, float (&xr)[NV][8], const float* src,
-                                                const bf16* erow, const bf16* gain, int lane) {
-  const int nvec = p.H >> 3;
-  uint4 g[NV];
+// xs = gain * src over H elements (consumer threads, each element once per CTA), src the
+// residual (written by other CTAs: read through L2) or, when erow is given, the bf16 embedding
+// row; each warp's sum of squares goes to scr. After the one consumer barrier every thread
+// can take its slice of xs into registers and norm_scale(scr) gives 1 / sqrt(mean(src^2) +
+// eps), by which the row results are scaled.
+__device__ void stage_gain(const Params& p, float* xs, float* scr, const float* src, const bf16* erow,
+                           const bf16* gain) {
+  const int t = threadIdx.x;
+  const int n4 = p.H >> 2;
+  float4 v[2];
+  uint2 g[2];
 #pragma unroll
-  for (int q = 0; q < NV; ++q) {  // every load first
-    const int v = lane + 32 * q;
-    g[q] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) xr[q][e] = 0.f;
-    if (v < nvec) {
+  for (int i = 0; i < 2; ++i) {  // every load first
+    const int j = t + i * NCT;
+    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    g[i] = make_uint2(0u, 0u);
+    if (j < n4) {
       if (erow) {
-        const uint4 r = __ldg(reinterpret_cast<const uint4*>(erow) + v);
-        xr[q][0] = bf_lo(r.x); xr[q][1] = bf_hi(r.x); xr[q][2] = bf_lo(r.y); xr[q][3] = bf_hi(r.y);
-        xr[q][4] = bf_lo(r.z); xr[q][5] = bf_hi(r.z); xr[q][6] = bf_lo(r.w); xr[q][7] = bf_hi(r.w);
+        const uint2 e = __ldg(reinterpret_cast<const uint2*>(erow) + j);
+        v[i] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
       } else {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(src) + 2 * v);
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 2 * v + 1);
-        xr[q][0] = a.x; xr[q][1] = a.y; xr[q][2] = a.z; xr[q][3] = a.w;
-        xr[q][4] = b.x; xr[q][5] = b.y; xr[q][6] = b.z; xr[q][7] = b.w;
+        v[i] = __ldcg(reinterpret_cast<const float4*>(src) + j);
       }
-      g[q] = __ldg(reinterpret_cast<const uint4*>(gain) + v);
+      g[i] = __ldg(reinterpret_cast<const uint2*>(gain) + j);
     }
   }
   float ss = 0.f;
 #pragma unroll
-  for (int q = 0; q < NV; ++q) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ss = fmaf(xr[q][e], xr[q][e], ss);
-    xr[q][0] *= bf_lo(g[q].x); xr[q][1] *= bf_hi(g[q].x); xr[q][2] *= bf_lo(g[q].y); xr[q][3] *= bf_hi(g[q].y);
-    xr[q][4] *= bf_lo(g[q].z); xr[q][5] *= bf_hi(g[q].z); xr[q][6] *= bf_lo(g[q].w); xr[q][7] *= bf_hi(g[q].w);
+  for (int i = 0; i < 2; ++i) {
+    const int j = t + i * NCT;
+    ss = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, fmaf(v[i].w, v[i].w, ss))));
+    if (j < n4)
+      reinterpret_cast<float4*>(xs)[j] = make_float4(v[i].x * bf_lo(g[i].x), v[i].y * bf_hi(g[i].x),
+                                                     v[i].z * bf_lo(g[i].y), v[i].w * bf_hi(g[i].y));
   }
   ss = warp_sum(ss);
-  return rsqrtf(ss / (float)p.H + p.eps);
+  if ((t & 31) == 0) scr[t >> 5] = ss;
+  cbar();
+}
+__device__ __forceinline__ float norm_scale(const Params& p, const float* scr) {
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < NCW; ++i) tot += scr[i];  // fixed order: deterministic
+  return rsqrtf(tot / (float)p.H + p.eps);
 }
 
 // Grid barrier of the consumers of all CTAs: each CTA adds one to a monotonic counter and
@@ -817,7 +822,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     for (int i = t; i < n8; i += THREADS) dst[i] = __ldg(src + i);
   }
   if (t < NCT) {
-    fill_qe(reinterpret_cast<const LayerW*>(p.layers)[0]);
     // the residual stream starts as the embedding row (this CTA's rows)
     for (int i = t; i < r1 - r0; i += NCT) {
       xo[i] = __bfloat162float(erow[r0 + i]);
@@ -875,7 +879,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       attention_preload<HD>(p, att, l, g, c, chunk, ctx);
     }
     ck(p, ph_idx, 0);
-    float inv = load_norm_regs<NV>(p, xr, p.x, l == 0 ? erow : nullptr, w.in_norm, lane);
+    fill_qe(w);  // (ordered before the units by the staging barrier)
+    stage_gain(p, xs, scr, p.x, l == 0 ? erow : nullptr, w.in_norm);
+    load_xr(xr, xs, nvecH, lane);
+    float inv = norm_scale(p, scr);
     tl_mark2(p, ph_idx);
     ck(p, ph_idx, 3);
     alive = phase_units(p, lt, HD, l, P_QKV, [&](const Unit& un) {
@@ -962,7 +969,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
     ck(p, ph_idx, 0);
-    inv = load_norm_regs<NV>(p, xr, p.x, nullptr, w.post_norm, lane);
+    stage_gain(p, xs, scr, p.x, nullptr, w.post_norm);
+    load_xr(xr, xs, nvecH, lane);
+    inv = norm_scale(p, scr);
     tl_mark2(p, ph_idx);
     ck(p, ph_idx, 3);
     alive = phase_units(p, lt, HD, l, P_GATEUP, [&](const Unit& un) {
@@ -1022,7 +1031,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
         xo[i] += sum;
         p.x[r0 + i] = xo[i];
       }
-    if (l + 1 < p.L) fill_qe(lt[l + 1]);  // the next layer's pair inputs
     tl_mark3(p, ph_idx, 2);
     ck(p, ph_idx, 7);
     tl_mark(p, ph_idx++, 2);
@@ -1034,7 +1042,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
     ck(p, ph_idx, 0);
-    const float inv = load_norm_regs<NV>(p, xr, p.x, nullptr, p.final_norm, lane);
+    stage_gain(p, xs, scr, p.x, nullptr, p.final_norm);
+    load_xr(xr, xs, nvecH, lane);
+    const float inv = norm_scale(p, scr);
     tl_mark2(p, ph_idx);
     ck(p, ph_idx, 3);
     float best_v = -INFINITY;
