@@ -399,7 +399,7 @@ __device__ __forceinline__ void load_xr(float (&xr)[NV][8], const float* xs, int
 // can take its slice of xs into registers and norm_scale(scr) gives 1 / sqrt(mean(src^2) +
 // eps), by which the row results are scaled.
 __device__ void stage_gain(const Params& p, float* xs, float* scr, const float* src, const bf16* erow,
-                           const bf16* gain) {
+                           const bf16* gain, float4* extra_dst = nullptr, float4 extra = float4{}) {
   const int t = threadIdx.x;
   const int n4 = p.H >> 2;
   float4 v[2];
@@ -430,6 +430,7 @@ __device__ void stage_gain(const Params& p, float* xs, float* scr, const float* 
   }
   ss = warp_sum(ss);
   if ((t & 31) == 0) scr[t >> 5] = ss;
+  if (extra_dst) *extra_dst = extra;  // (a value loaded earlier, published by the same barrier)
   cbar();
 }
 __device__ __forceinline__ float norm_scale(const Params& p, const float* scr) {
@@ -790,23 +791,28 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   block_of(p.H, r0, r1);
   int q0, q1;  // this CTA's q/k/v pairs
   block_of(npairs, q0, q1);
-  // per pair of layer l: bias of both rows and the rotation at pos (weights and the position
-  // only: ready before the phase)
-  auto fill_qe = [&](const LayerW& w) {
-    for (int i = t; i < q1 - q0; i += NCT) {
-      const int item = q0 + i, head = item / half, e = item - head * half;
+  // pair t of layer l (t < q1 - q0): bias of both rows and the rotation at pos (weights and
+  // the position only, so they are requested before anything the phase waits for)
+  auto load_qe = [&](const LayerW& w) -> float4 {
+    float4 r = make_float4(0.f, 0.f, 1.f, 0.f);
+    if (t < q1 - q0) {
+      const int item = q0 + t, head = item / half, e = item - head * half;
       const bf16* bias;
       int hh;
       if (head < p.nq) { bias = w.bq; hh = head; }
       else if (head < p.nq + p.nkv) { bias = w.bk; hh = head - p.nq; }
       else { bias = w.bv; hh = head - p.nq - p.nkv; }
-      float2 cs = make_float2(1.f, 0.f);
-      if (head < p.nq + p.nkv) cs = p.rope[(size_t)pos * half + e];
-      qe[4 * i + 0] = bias ? __bfloat162float(bias[hh * HD + e]) : 0.f;
-      qe[4 * i + 1] = bias ? __bfloat162float(bias[hh * HD + e + half]) : 0.f;
-      qe[4 * i + 2] = cs.x;
-      qe[4 * i + 3] = cs.y;
+      if (bias) {
+        r.x = __bfloat162float(bias[hh * HD + e]);
+        r.y = __bfloat162float(bias[hh * HD + e + half]);
+      }
+      if (head < p.nq + p.nkv) {
+        const float2 cs = p.rope[(size_t)pos * half + e];
+        r.z = cs.x;
+        r.w = cs.y;
+      }
     }
+    return r;
   };
   if (t == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -879,8 +885,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       attention_preload<HD>(p, att, l, g, c, chunk, ctx);
     }
     ck(p, ph_idx, 0);
-    fill_qe(w);  // (ordered before the units by the staging barrier)
-    stage_gain(p, xs, scr, p.x, l == 0 ? erow : nullptr, w.in_norm);
+    const float4 qv = load_qe(w);  // stored into qe just before the staging barrier
+    stage_gain(p, xs, scr, p.x, l == 0 ? erow : nullptr, w.in_norm,
+               t < q1 - q0 ? reinterpret_cast<float4*>(qe) + t : nullptr, qv);
     load_xr(xr, xs, nvecH, lane);
     float inv = norm_scale(p, scr);
     tl_mark2(p, ph_idx);
