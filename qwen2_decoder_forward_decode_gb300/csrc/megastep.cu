@@ -791,29 +791,29 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   block_of(p.H, r0, r1);
   int q0, q1;  // this CTA's q/k/v pairs
   block_of(npairs, q0, q1);
-  // pair t of layer l (t < q1 - q0): bias of both rows and the rotation at pos (weights and
-  // the position only, so they are requested before anything the phase waits for)
-  auto load_qe = [&](const LayerW& w) -> float4 {
-    float4 r = make_float4(0.f, 0.f, 1.f, 0.f);
+  // pair t (t < q1 - q0): the rotation at pos (the same in every layer) and the bias of both
+  // rows, requested well before the q/k/v phase that uses them (weights and the position only)
+  float4 qv = make_float4(0.f, 0.f, 1.f, 0.f);
+  const int qhead = (q0 + t) / half, qe_i = q0 + t - qhead * half;
+  if (t < q1 - q0 && qhead < p.nq + p.nkv) {
+    const float2 cs = p.rope[(size_t)pos * half + qe_i];
+    qv.z = cs.x;
+    qv.w = cs.y;
+  }
+  auto load_bias = [&](const LayerW& w) {
     if (t < q1 - q0) {
-      const int item = q0 + t, head = item / half, e = item - head * half;
       const bf16* bias;
       int hh;
-      if (head < p.nq) { bias = w.bq; hh = head; }
-      else if (head < p.nq + p.nkv) { bias = w.bk; hh = head - p.nq; }
-      else { bias = w.bv; hh = head - p.nq - p.nkv; }
+      if (qhead < p.nq) { bias = w.bq; hh = qhead; }
+      else if (qhead < p.nq + p.nkv) { bias = w.bk; hh = qhead - p.nq; }
+      else { bias = w.bv; hh = qhead - p.nq - p.nkv; }
       if (bias) {
-        r.x = __bfloat162float(bias[hh * HD + e]);
-        r.y = __bfloat162float(bias[hh * HD + e + half]);
-      }
-      if (head < p.nq + p.nkv) {
-        const float2 cs = p.rope[(size_t)pos * half + e];
-        r.z = cs.x;
-        r.w = cs.y;
+        qv.x = __bfloat162float(bias[hh * HD + qe_i]);
+        qv.y = __bfloat162float(bias[hh * HD + qe_i + half]);
       }
     }
-    return r;
   };
+  load_bias(reinterpret_cast<const LayerW*>(p.layers)[0]);
   if (t == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -885,7 +885,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       attention_preload<HD>(p, att, l, g, c, chunk, ctx);
     }
     ck(p, ph_idx, 0);
-    const float4 qv = load_qe(w);  // stored into qe just before the staging barrier
     stage_gain(p, xs, scr, p.x, l == 0 ? erow : nullptr, w.in_norm,
                t < q1 - q0 ? reinterpret_cast<float4*>(qe) + t : nullptr, qv);
     load_xr(xr, xs, nvecH, lane);
@@ -1001,6 +1000,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
     ck(p, ph_idx, 0);
+    if (l + 1 < p.L) load_bias(lt[l + 1]);  // (used by the next layer's q/k/v phase)
     {
       const int nvecI = p.I >> 3;
       const int segv = (nvecI + NCW - 1) / NCW;
