@@ -99,6 +99,10 @@ cudaError_t launch_lmhead(const Dims& d, const void* W, const void* final_norm, 
 
 // ---- gemm_tc.cu (tcgen05 tensor-core GEMMs, bf16 in, fp32 accumulate) ----
 bool gemm_tc_available();
+// Tensor map (128-byte CUtensorMap) of a 2-D fp16 (bf16 when bf) row-major [rows][cols] array with
+// a row pitch of ld elements, box of 64 columns x box_rows rows, 128-byte swizzle; false if the
+// encoder is unavailable or the arguments break its rules.
+bool make_map(void* map, const void* base, int rows, int cols, int ld, int box_rows, bool bf = false);
 cudaError_t gemm_tc_set_attributes();
 // fp16 operands (A activations, B weights), fp32 accumulate; bias bf16
 // ws (optional): fp32 workspace of ws_floats for split-K partial tiles, used when the
