@@ -97,12 +97,23 @@ cudaError_t launch_lmhead(const Dims& d, const void* W, const void* final_norm, 
                           float* logits, const Finalize& f, unsigned long long* tl, cudaStream_t s,
                           bool pdl);
 
+// ---- attn_tc.cu (causal prefill attention on tcgen05 / TMEM) ----
+bool attn_prefill_tc_supported(int hd);
+cudaError_t attn_prefill_tc_set_attributes();
+// Qh [T][nq*hd] fp16 holding q * log2(e) / sqrt(hd) for positions pos0 .. pos0+T-1; kc, vc: the
+// layer's fp16 cache [nkv][cap][hd], filled through position pos0+T-1; Oh [T][nq*hd] fp16.
+cudaError_t attn_prefill_tc(const Dims& d, int T, int pos0, const __half* Qh, const __half* kc, const __half* vc,
+                            __half* Oh, int* err, cudaStream_t s);
+
 // ---- gemm_tc.cu (tcgen05 tensor-core GEMMs, bf16 in, fp32 accumulate) ----
 bool gemm_tc_available();
 // Tensor map (128-byte CUtensorMap) of a 2-D fp16 (bf16 when bf) row-major [rows][cols] array with
 // a row pitch of ld elements, box of 64 columns x box_rows rows, 128-byte swizzle; false if the
 // encoder is unavailable or the arguments break its rules.
 bool make_map(void* map, const void* base, int rows, int cols, int ld, int box_rows, bool bf = false);
+// Tensor map of one layer's fp16 K or V cache [nkv][cap][hd] over its first `keys` positions:
+// boxes of 64 head columns x 64 positions of one KV head, 128-byte swizzle.
+bool make_map_kv(void* map, const void* base, int hd, int keys, int nkv, int cap);
 cudaError_t gemm_tc_set_attributes();
 // fp16 operands (A activations, B weights), fp32 accumulate; bias bf16
 // ws (optional): fp32 workspace of ws_floats for split-K partial tiles, used when the

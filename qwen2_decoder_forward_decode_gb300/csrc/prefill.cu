@@ -11,6 +11,7 @@
 
 #include <math.h>
 #include <stdlib.h>
+#include <cstring>
 
 namespace qw {
 
@@ -56,11 +57,12 @@ __global__ void swiglu_kernel(const float* G, const float* U, float* A, size_t n
   }
 }
 
-// Y [T][nq*hd + 2*nkv*hd] (q | k | v, bias included) -> Q [T][nq*hd] rotated;
-// K, V rotated/copied into the cache at positions pos0 + t.
+// Y [T][nq*hd + 2*nkv*hd] (q | k | v, bias included) -> Q [T][nq*hd] rotated (fp32, or fp16
+// times qscale into Qh when Qh is given); K, V rotated/copied into the cache at positions pos0 + t.
 template <typename KV>
 __global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, int pos0, int cap,
-                               const float2* rope, float* Q, KV* kc, KV* vc, int* err) {
+                               const float2* rope, float* Q, KV* kc, KV* vc, int* err, f16* Qh = nullptr,
+                               float qscale = 1.f) {
   const int t = blockIdx.x;
   const int half = hd / 2;
   const int width = (nq + 2 * nkv) * hd;
@@ -73,8 +75,14 @@ __global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, 
       const float2 cs = rope[(size_t)pos * half + i];
       const float ra = a * cs.x - b * cs.y, rb = b * cs.x + a * cs.y;
       if (head < nq) {
-        Q[(size_t)t * nq * hd + head * hd + i] = ra;
-        Q[(size_t)t * nq * hd + head * hd + i + half] = rb;
+        const size_t o = (size_t)t * nq * hd + head * hd + i;
+        if (Qh) {
+          Qh[o] = to_half_checked(ra * qscale, err);
+          Qh[o + half] = to_half_checked(rb * qscale, err);
+        } else {
+          Q[o] = ra;
+          Q[o + half] = rb;
+        }
       } else {
         KV* dst = kc + ((size_t)(head - nq) * cap + pos) * hd;
         store_kv(dst + i, ra, err);
@@ -281,7 +289,9 @@ cudaError_t prefill_set_attributes(const Dims& d) {
   cudaError_t e = d.dtype == 1 ? set_attr_t<f16>() : set_attr_t<float>();
   if (e || d.dtype != 1) return e;
   if ((e = pm_set_attributes())) return e;
-  return gemm_tc_available() ? gemm_tc_set_attributes() : cudaSuccess;
+  if (!gemm_tc_available()) return cudaSuccess;
+  if ((e = attn_prefill_tc_set_attributes())) return e;
+  return gemm_tc_set_attributes();
 }
 
 template <typename W, typename KV>
@@ -514,11 +524,15 @@ static bool attn_prefill_mma(const Dims& d, const float* Q, int T_, int pos0, co
   return true;
 }
 
-// QW_PREFILL_ATTN_SIMT=1: the CUDA-core prefill attention on bf16 models too (comparison)
-static bool simt_attention() {
-  static const bool v = [] {
-    const char* e = std::getenv("QW_PREFILL_ATTN_SIMT");
-    return e && e[0] == '1';
+// Prefill attention of the bf16 models: QW_PREFILL_ATTN=tc (tcgen05, the default), mma
+// (mma.sync) or simt (CUDA cores), for comparison.
+enum { PA_TC, PA_MMA, PA_SIMT };
+static int prefill_attention_kind() {
+  static const int v = [] {
+    const char* e = std::getenv("QW_PREFILL_ATTN");
+    if (e && !std::strcmp(e, "mma")) return (int)PA_MMA;
+    if (e && !std::strcmp(e, "simt")) return (int)PA_SIMT;
+    return (int)PA_TC;
   }();
   return v;
 }
@@ -541,13 +555,23 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
     if ((e = gemm_tc(b.Xh, H, (const f16*)w.wq16, H, (const bf16*)w.bq, b.Y, Wd, T_, qd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
     if ((e = gemm_tc(b.Xh, H, (const f16*)w.wk16, H, (const bf16*)w.bk, b.Y + qd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
     if ((e = gemm_tc(b.Xh, H, (const f16*)w.wv16, H, (const bf16*)w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-    rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err);
-    const bool mma = !simt_attention() && attn_prefill_mma(d, b.Q, T_, pos0, kc, vc, b.Oh, s, &e);
-    if (mma && e) return e;
-    if (!mma) {
-      if ((e = attn_prefill<f16>(d, b.Q, T_, pos0, kc, vc, b.O, s))) return e;
-      const size_t no = (size_t)T_ * qd;
-      to_half_kernel<<<(unsigned)((no + 255) / 256 < 4096 ? (no + 255) / 256 : 4096), 256, 0, s>>>(b.O, b.Oh, no, err);
+    const int kind = prefill_attention_kind();
+    if (kind == PA_TC && attn_prefill_tc_supported(d.hd) && d.I >= qd) {
+      // q in fp16, scaled into base-2 scores, in the (still free) SwiGLU operand buffer
+      const float qs = 1.4426950408889634f / sqrtf((float)d.hd);
+      rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err, b.Ah,
+                                            qs);
+      if ((e = attn_prefill_tc(d, T_, pos0, b.Ah, kc, vc, b.Oh, err, s))) return e;
+    } else {
+      rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err);
+      const bool mma = kind != PA_SIMT && attn_prefill_mma(d, b.Q, T_, pos0, kc, vc, b.Oh, s, &e);
+      if (mma && e) return e;
+      if (!mma) {
+        if ((e = attn_prefill<f16>(d, b.Q, T_, pos0, kc, vc, b.O, s))) return e;
+        const size_t no = (size_t)T_ * qd;
+        to_half_kernel<<<(unsigned)((no + 255) / 256 < 4096 ? (no + 255) / 256 : 4096), 256, 0, s>>>(b.O, b.Oh, no,
+                                                                                                     err);
+      }
     }
     if ((e = gemm_tc(b.Oh, qd, (const f16*)w.wo16, qd, nullptr, b.X, H, T_, H, qd, true, err, s, b.ws, b.ws_floats, d.nsm))) return e;
     norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.post_norm, H, d.eps, b.Xh, err);

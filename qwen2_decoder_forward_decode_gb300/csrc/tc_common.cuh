@@ -79,6 +79,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major tile written by TMA with 128-byte swizzle:
+// each 128-byte row holds 64 consecutive MN elements of one K index, consecutive rows step
+// K. Groups of 8 K rows (1024-byte atoms) are `sbo` bytes apart, 64-element MN chunks `lbo`
+// bytes apart. The start address must be 1024-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16 (type code 0 in
 // bits 7-9 and 10-12), both K-major (bits 15, 16 = 0), N/8 in bits 17-22, M/16 in 24-28.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
@@ -129,6 +143,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// kind::f16 with the B operand MN-major (bit 16)
+__host__ __device__ constexpr uint32_t idesc_f16_bmn(int M, int N) { return idesc_f16(M, N) | (1u << 16); }
+
+// 3-D tensor load (x innermost)
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 
 // kind::f16 with bf16 A and B (type code 1 in bits 7-9 and 10-12)

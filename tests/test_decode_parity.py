@@ -99,15 +99,19 @@ def test_tiny_without_graphs_matches(monkeypatch):
         m.close()
 
 
-@pytest.mark.parametrize("simt", ["0", "1"])
-def test_bf16_prefill_paths(monkeypatch, simt):
-    """The tensor-core prefill (default for bf16) and the CUDA-core prefill
-    (QW_PREFILL_SIMT=1) both match the oracle on a ragged shape."""
+@pytest.mark.parametrize("shape_name", ["small_bf16", "hd128_bf16"])
+@pytest.mark.parametrize("simt,attn", [("0", "tc"), ("0", "mma"), ("0", "simt"), ("1", "tc")])
+def test_bf16_prefill_paths(monkeypatch, shape_name, simt, attn):
+    """The tensor-core prefill (default for bf16) with each of its attention kernels
+    (QW_PREFILL_ATTN: tcgen05, mma.sync, CUDA cores) and the CUDA-core prefill
+    (QW_PREFILL_SIMT=1) all match the oracle; 300 prompt tokens leave ragged query and
+    key blocks, on head sizes 64 and 128."""
     monkeypatch.setenv("QW_PREFILL_SIMT", simt)
-    w, prompt, toks, logits = oracle_run("small_bf16", 300, 4)
-    m = _model("small_bf16", w, 320)
+    monkeypatch.setenv("QW_PREFILL_ATTN", attn)
+    w, prompt, toks, logits = oracle_run(shape_name, 300, 4)
+    m = _model(shape_name, w, 320)
     try:
-        run_teacher_forced(m, SHAPES["small_bf16"], prompt, toks, logits)
+        run_teacher_forced(m, SHAPES[shape_name], prompt, toks, logits)
     finally:
         m.close()
 
