@@ -391,6 +391,7 @@ struct qw_model {
       if (h & ERR_RANGE)
         return fail(QW_ERR_NUMERIC, "a value outside the fp16 range of the KV cache or of a tensor-core operand");
       if (h & ERR_TIMEOUT) return fail(QW_ERR_TIMEOUT, "a bounded device-side wait gave up");
+      if (h & ERR_LAYOUT) return fail(QW_ERR_CUDA, "a kernel found its shared memory misaligned");
     }
     return QW_OK;
   }

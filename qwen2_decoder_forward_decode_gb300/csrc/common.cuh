@@ -17,7 +17,8 @@ typedef __half f16;
 //   ERR_TIMEOUT   a bounded wait gave up
 //   ERR_RANGE     a value written to an fp16 KV cache or fp16 tensor-core operand lay
 //                 outside the fp16 range (or was not finite)
-enum : int { ERR_TOKEN = 1, ERR_NONFINITE = 2, ERR_TIMEOUT = 4, ERR_RANGE = 8 };
+//   ERR_LAYOUT    a kernel found its shared-memory window misaligned and skipped its work
+enum : int { ERR_TOKEN = 1, ERR_NONFINITE = 2, ERR_TIMEOUT = 4, ERR_RANGE = 8, ERR_LAYOUT = 16 };
 
 // fp32 -> fp16 (round to nearest even) for data whose range the model does not bound: a
 // value that would round to infinity, or a non-finite one, sets ERR_RANGE in *err.

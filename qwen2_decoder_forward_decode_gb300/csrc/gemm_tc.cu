@@ -512,14 +512,14 @@ bool make_map(void* mv, const void* base, int rows, int cols, int ld, int box_ro
 
 // Tensor map of one layer's fp16 key or value cache [nkv][cap][hd]: dims {hd, keys, nkv}
 // (keys = the positions written so far, so boxes past them read zeros), boxes of 64 head
-// columns x 64 positions of one KV head, 128-byte swizzle.
-bool make_map_kv(void* mv, const void* base, int hd, int keys, int nkv, int cap) {
+// columns x box_keys positions of one KV head, 128-byte swizzle.
+bool make_map_kv(void* mv, const void* base, int hd, int keys, int nkv, int cap, int box_keys) {
   CUtensorMap* m = reinterpret_cast<CUtensorMap*>(mv);
   EncodeTiledFn f = encode_fn();
-  if (!f || ((uintptr_t)base & 15) || hd % 64 || keys < 1 || keys > cap) return false;
+  if (!f || ((uintptr_t)base & 15) || hd % 64 || keys < 1 || keys > cap || box_keys < 8 || box_keys > 256) return false;
   cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)keys, (cuuint64_t)nkv};
   cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)cap * hd * 2};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_keys, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

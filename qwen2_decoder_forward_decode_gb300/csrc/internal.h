@@ -112,8 +112,8 @@ bool gemm_tc_available();
 // encoder is unavailable or the arguments break its rules.
 bool make_map(void* map, const void* base, int rows, int cols, int ld, int box_rows, bool bf = false);
 // Tensor map of one layer's fp16 K or V cache [nkv][cap][hd] over its first `keys` positions:
-// boxes of 64 head columns x 64 positions of one KV head, 128-byte swizzle.
-bool make_map_kv(void* map, const void* base, int hd, int keys, int nkv, int cap);
+// boxes of 64 head columns x box_keys positions of one KV head, 128-byte swizzle.
+bool make_map_kv(void* map, const void* base, int hd, int keys, int nkv, int cap, int box_keys);
 cudaError_t gemm_tc_set_attributes();
 // fp16 operands (A activations, B weights), fp32 accumulate; bias bf16
 // ws (optional): fp32 workspace of ws_floats for split-K partial tiles, used when the

@@ -53,6 +53,9 @@ SHAPES = {
     "small_f32": Shape("small_f32", 3, 96, 3, 1, 32, 200, 1000, "f32"),
     "mha_f32": Shape("mha_f32", 2, 64, 4, 4, 16, 96, 300, "f32"),
     "hd128_bf16": Shape("hd128_bf16", 2, 768, 6, 2, 128, 2304, 5000, "bf16"),
+    # even query heads per KV head (4 and 2), head sizes 64 and 128
+    "gqa4_bf16": Shape("gqa4_bf16", 2, 512, 8, 2, 64, 1024, 3001, "bf16"),
+    "gqa2_hd128_bf16": Shape("gqa2_hd128_bf16", 2, 512, 4, 2, 128, 1408, 3001, "bf16"),
     # the optional weights switched the other way: a separate LM head, no q/k/v bias
     "untied_bf16": Shape("untied_bf16", 2, 256, 4, 2, 64, 704, 2051, "bf16", tied=False, qkv_bias=False),
 }

@@ -99,13 +99,13 @@ def test_tiny_without_graphs_matches(monkeypatch):
         m.close()
 
 
-@pytest.mark.parametrize("shape_name", ["small_bf16", "hd128_bf16"])
+@pytest.mark.parametrize("shape_name", ["small_bf16", "hd128_bf16", "gqa4_bf16", "gqa2_hd128_bf16"])
 @pytest.mark.parametrize("simt,attn", [("0", "tc"), ("0", "mma"), ("0", "simt"), ("1", "tc")])
 def test_bf16_prefill_paths(monkeypatch, shape_name, simt, attn):
     """The tensor-core prefill (default for bf16) with each of its attention kernels
     (QW_PREFILL_ATTN: tcgen05, mma.sync, CUDA cores) and the CUDA-core prefill
     (QW_PREFILL_SIMT=1) all match the oracle; 300 prompt tokens leave ragged query and
-    key blocks, on head sizes 64 and 128."""
+    key blocks, on head sizes 64 and 128 with odd and even query heads per KV head."""
     monkeypatch.setenv("QW_PREFILL_SIMT", simt)
     monkeypatch.setenv("QW_PREFILL_ATTN", attn)
     w, prompt, toks, logits = oracle_run(shape_name, 300, 4)
