@@ -511,7 +511,7 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
     const qw_layer_weights& L = w->layers[l];
     LayerPtrs p{L.in_norm, L.wq, cfg->qkv_bias ? L.bq : nullptr, L.wk, cfg->qkv_bias ? L.bk : nullptr,
                 L.wv, cfg->qkv_bias ? L.bv : nullptr, L.wo, L.post_norm, L.w_gate, L.w_up, L.w_down,
-                nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+                nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     m->layers.push_back(p);
   }
   const int S = d.max_seqs;
@@ -565,19 +565,33 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
     // fp16 copies of the layer matrices: the tensor-core operands of the prefill GEMMs
     const size_t H = d.H, qd = (size_t)d.nq * d.hd, kvd = (size_t)d.nkv * d.hd, I = d.I;
     const size_t sizes[7] = {qd * H, kvd * H, kvd * H, H * qd, I * H, I * H, H * I};
-    size_t per_layer = 0;
-    for (size_t n : sizes) per_layer += (n * 2 + 255) & ~(size_t)255;
+    // q, k, v back to back (no padding between them: one fused projection); the rest on
+    // 256-byte boundaries; then the concatenated q/k/v bias
+    const size_t qkv_bytes = ((sizes[0] + sizes[1] + sizes[2]) * 2 + 255) & ~(size_t)255;
+    const size_t bias_bytes = ((qd + 2 * kvd) * 2 + 255) & ~(size_t)255;
+    size_t per_layer = qkv_bytes + bias_bytes;
+    for (int i = 3; i < 7; ++i) per_layer += (sizes[i] * 2 + 255) & ~(size_t)255;
     if ((e = cudaMalloc(&m->w16, per_layer * d.L))) return bail(e, "cudaMalloc(fp16 weights)");
     char* p = (char*)m->w16;
     for (int l = 0; l < d.L; ++l) {
       LayerPtrs& L = m->layers[l];
       const void* src[7] = {L.wq, L.wk, L.wv, L.wo, L.w_gate, L.w_up, L.w_down};
       const void** dst[7] = {&L.wq16, &L.wk16, &L.wv16, &L.wo16, &L.wg16, &L.wu16, &L.wd16};
+      char* q0 = p;
       for (int i = 0; i < 7; ++i) {
         *dst[i] = p;
         if ((e = convert_bf16_to_half(src[i], p, sizes[i], m->err, 0))) return bail(e, "fp16 weight copy");
-        p += (sizes[i] * 2 + 255) & ~(size_t)255;
+        p += i < 2 ? sizes[i] * 2 : i == 2 ? q0 + qkv_bytes - p : (sizes[i] * 2 + 255) & ~(size_t)255;
       }
+      L.bqkv = nullptr;
+      if (L.bq) {
+        if ((e = cudaMemcpy(p, L.bq, qd * 2, cudaMemcpyDeviceToDevice)) ||
+            (e = cudaMemcpy(p + qd * 2, L.bk, kvd * 2, cudaMemcpyDeviceToDevice)) ||
+            (e = cudaMemcpy(p + (qd + kvd) * 2, L.bv, kvd * 2, cudaMemcpyDeviceToDevice)))
+          return bail(e, "q/k/v bias copy");
+        L.bqkv = p;
+      }
+      p += bias_bytes;
     }
     int h_err = 0;
     if ((e = cudaMemcpy(&h_err, m->err, sizeof(int), cudaMemcpyDeviceToHost))) return bail(e, "cudaMemcpy");
@@ -1017,8 +1031,11 @@ qw_status qw_op_gemm_f16(int32_t M, int32_t N, int32_t K, const void* A, const v
   if ((uintptr_t)C & 15) return fail(QW_ERR_INVALID_ARG, "C not 16-byte aligned");
   cudaError_t e = gemm_tc_set_attributes();
   if (e) return cuda_fail(e, "gemm attributes");
+  int dev = 0, nsm = 0;  // persistent CTAs, one per SM
+  if ((e = cudaGetDevice(&dev)) || (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)))
+    return cuda_fail(e, "device query");
   e = gemm_tc((const f16*)A, K, (const f16*)B, K, (const bf16*)bias, C, N, M, N, K, accumulate != 0,
-              err_dev, (cudaStream_t)cuda_stream);
+              err_dev, (cudaStream_t)cuda_stream, nullptr, 0, nsm);
   if (e) return cuda_fail(e, "gemm launch");
   return QW_OK;
 }
@@ -1032,8 +1049,11 @@ qw_status qw_op_gemm_swiglu_f16(int32_t M, int32_t N, int32_t K, const void* A, 
   if (((uintptr_t)Wu | (uintptr_t)act) & 15) return fail(QW_ERR_INVALID_ARG, "operand not 16-byte aligned");
   cudaError_t e = gemm_tc_set_attributes();
   if (e) return cuda_fail(e, "gemm attributes");
+  int dev = 0, nsm = 0;  // persistent CTAs, one per SM
+  if ((e = cudaGetDevice(&dev)) || (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)))
+    return cuda_fail(e, "device query");
   e = gemm_tc_swiglu((const f16*)A, K, (const f16*)Wg, (const f16*)Wu, K, (f16*)act, N, M, N, K, err_dev,
-                     (cudaStream_t)cuda_stream);
+                     (cudaStream_t)cuda_stream, nullptr, 0, nsm);
   if (e) return cuda_fail(e, "gemm launch");
   return QW_OK;
 }

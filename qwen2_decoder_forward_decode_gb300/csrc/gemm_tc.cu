@@ -2,13 +2,15 @@
 //
 //   C[M, N] = A[M, K] . B[N, K]^T     A: fp16 activations, B: fp16 weights, both K-major
 //
-// One CTA computes a 128 x BN tile with a TMEM fp32 accumulator:
+// A persistent CTA per SM computes 128 x BN tiles into two TMEM fp32 accumulators:
 //   warp 0 (one lane)  TMA producer: 128-byte-swizzled A and B tiles of 64 K-elements into
 //                      a STAGES-deep shared-memory ring (mbarrier full/empty pairs)
 //   warp 1 (one lane)  MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16,
 //                      four per stage; tcgen05.commit frees a stage when its MMAs retire
-//   warps 2..5         epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows), fused
-//                      bias / residual-add / SwiGLU, stores to global memory
+//   warps 2..9         epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows; warps w and
+//                      w + 4 split the columns), fused bias / residual-add / SwiGLU,
+//                      coalesced stores to global memory, while the next tile accumulates
+//                      in the other buffer
 // Every mbarrier wait is bounded (clock budget); on expiry the CTA flags ERR_TIMEOUT,
 // stops issuing work, and still releases its TMEM.
 #include <cuda.h>
@@ -24,7 +26,7 @@ namespace qw {
 namespace tc {
 
 constexpr int BM = 128, BK = 64, STAGES = 4;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;  // producer, MMA issuer, eight epilogue warps
 
 }  // namespace tc
 
@@ -38,33 +40,49 @@ struct TcEpi {
   int ldc;
 };
 
+// Persistent: grid = min(units, SMs); CTA c takes work units c, c + grid, ... in order, a unit
+// being one 128 x BN output tile (of one K range under split-K). The producer streams the
+// A and B blocks of consecutive units through one ring without a pause, the MMA warp
+// accumulates unit i into TMEM buffer i % 2 (2 x BN columns), and the epilogue warps drain
+// unit i while the MMAs of unit i + 1 run.
 // BN columns per tile. For EPI_SWIGLU the B ring holds BN/2 gate rows then BN/2 up rows of
-// the same output columns; the accumulator keeps gate in TMEM columns [0, BN/2) and up in
-// [BN/2, BN).
-// Split-K (grid.z = splits > 1, EPI_STORE / EPI_ADD only): CTA z covers a contiguous range
-// of K blocks and stores its raw fp32 tile to ws[z][M][N]; splitk_reduce_kernel then adds
-// the splits in order and applies the bias or the residual add (deterministic).
+// the same output columns, so one N = BN product leaves gate in accumulator columns
+// [0, BN/2) and up in [BN/2, BN).
+// Split-K (splits > 1, EPI_STORE / EPI_ADD / EPI_SWIGLU): unit z of a tile covers a
+// contiguous range of K blocks and stores its raw fp32 tile to ws[z]; the reduce kernels then
+// add the splits in order and apply the bias, the residual add or SwiGLU (deterministic).
+struct TcGrid {
+  int tiles_m, tiles_n, splits;
+};
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(tc::THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmB2, TcEpi ep, int M, int N, int K, int* err, int splits,
+               const __grid_constant__ CUtensorMap tmB2, TcEpi ep, int M, int N, int K, int* err, TcGrid g,
                float* ws) {
   using namespace tc;
   constexpr int A_BYTES = BM * BK * 2;
   constexpr int B_BYTES = BN * BK * 2;
   constexpr int STAGE = A_BYTES + B_BYTES;
+  constexpr int NOUT = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE);
-  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 1);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES), accum = smem_u32(bars + 2 * STAGES);
+  uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 4);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+  const uint32_t acc_full0 = smem_u32(bars + 2 * STAGES), acc_empty0 = acc_full0 + 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM;
-  const int n0 = blockIdx.x * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+  const int tiles = g.tiles_m * g.tiles_n, units = tiles * g.splits;
   const int nk_all = (K + BK - 1) / BK;
-  const int kb_lo = (int)((long long)blockIdx.z * nk_all / splits);
-  const int kb_hi = (int)((long long)(blockIdx.z + 1) * nk_all / splits);
-  const int nk = kb_hi - kb_lo;  // K blocks of this CTA
+  // unit -> first row, first output column, split index, K block range
+  auto unit_of = [&](int u, int& m0, int& n0, int& z, int& kb_lo, int& kb_hi) {
+    z = u / tiles;
+    const int t = u - z * tiles;
+    m0 = (t % g.tiles_m) * BM;
+    n0 = (t / g.tiles_m) * NOUT;
+    kb_lo = (int)((long long)z * nk_all / g.splits);
+    kb_hi = (int)((long long)(z + 1) * nk_all / g.splits);
+  };
   __shared__ int s_abort;
 
   if (threadIdx.x == 0) {
@@ -73,165 +91,155 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc::mbar_init(full0 + 8 * s, 1);
       tc::mbar_init(empty0 + 8 * s, 1);
     }
-    tc::mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(acc_full0 + 8 * b, 1);
+      tc::mbar_init(acc_empty0 + 8 * b, 8);  // one arrival per epilogue warp
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) tc::tmem_alloc(smem_u32(tmem_slot), BN);
+  if (warp == 0) tc::tmem_alloc(smem_u32(tmem_slot), 2 * BN);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---- TMA producer
+    // ---- TMA producer: the K blocks of this CTA's units, back to back
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
-    int issued = 0;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (kb / STAGES) & 1;
-      if (kb >= STAGES && !tc::mbar_wait(empty0 + 8 * s, ph ^ 1, err)) { s_abort = 1; break; }
-      if (s_abort) break;
-      const uint32_t a_dst = smem_u32(smem + s * STAGE);
-      const uint32_t b_dst = a_dst + A_BYTES;
-      const int kx = (kb_lo + kb) * BK;
-      tc::mbar_expect_tx(full0 + 8 * s, STAGE);
-      tc::tma_load_2d(a_dst, &tmA, full0 + 8 * s, kx, m0);
-      if (EPI == EPI_SWIGLU) {
-        tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kx, n0);
-        tc::tma_load_2d(b_dst + B_BYTES / 2, &tmB2, full0 + 8 * s, kx, n0);
-      } else {
-        tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kx, n0);
+    int it = 0;  // K blocks issued
+    for (int u = blockIdx.x; u < units && !s_abort; u += gridDim.x) {
+      int m0, n0, z, kb_lo, kb_hi;
+      unit_of(u, m0, n0, z, kb_lo, kb_hi);
+      for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+        const int s = it % STAGES;
+        if (it >= STAGES && !tc::mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, err)) { s_abort = 1; break; }
+        if (s_abort) break;
+        const uint32_t a_dst = smem_u32(smem + s * STAGE);
+        const uint32_t b_dst = a_dst + A_BYTES;
+        tc::mbar_expect_tx(full0 + 8 * s, STAGE);
+        tc::tma_load_2d(a_dst, &tmA, full0 + 8 * s, kb * BK, m0);
+        if (EPI == EPI_SWIGLU) {
+          tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kb * BK, n0);
+          tc::tma_load_2d(b_dst + B_BYTES / 2, &tmB2, full0 + 8 * s, kb * BK, n0);
+        } else {
+          tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kb * BK, n0);
+        }
       }
-      ++issued;
     }
     // drain: every issued stage must land before the CTA may exit
-    for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
-      tc::mbar_wait(full0 + 8 * (kb % STAGES), (kb / STAGES) & 1, err);
+    for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+      tc::mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1, err);
   } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    constexpr uint32_t idesc = EPI == EPI_SWIGLU ? tc::idesc_f16(BM, BN / 2) : tc::idesc_f16(BM, BN);
+    // ---- MMA issuer: one N = BN product per 16 K (gate and up together for SwiGLU)
+    constexpr uint32_t idesc = tc::idesc_f16(BM, BN);
+    int it = 0, i = 0;  // K blocks consumed, units done
     bool ok = true;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      if (!tc::mbar_wait(full0 + 8 * s, (kb / STAGES) & 1, err)) { ok = false; s_abort = 1; break; }
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
+      int m0, n0, z, kb_lo, kb_hi;
+      unit_of(u, m0, n0, z, kb_lo, kb_hi);
+      const int b = i & 1;
+      // the epilogue has drained this accumulator's previous unit
+      if (i >= 2 && !tc::mbar_wait(acc_empty0 + 8 * b, ((i >> 1) & 1) ^ 1, err)) { ok = false; break; }
       tc::tc_fence_after();
-      const uint32_t a_base = smem_u32(smem + s * STAGE);
-      const uint32_t b_base = a_base + A_BYTES;
+      for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+        const int s = it % STAGES;
+        if (!tc::mbar_wait(full0 + 8 * s, (it / STAGES) & 1, err)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint32_t a_base = smem_u32(smem + s * STAGE);
+        const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k) {
-        const uint64_t da = tc::smem_desc_sw128(a_base + 32 * k);
-        if (EPI == EPI_SWIGLU) {
-          tc::mma_f16(tmem, da, tc::smem_desc_sw128(b_base + 32 * k), idesc, (kb | k) != 0);
-          tc::mma_f16(tmem + BN / 2, da, tc::smem_desc_sw128(b_base + B_BYTES / 2 + 32 * k), idesc,
-                       (kb | k) != 0);
-        } else {
-          tc::mma_f16(tmem, da, tc::smem_desc_sw128(b_base + 32 * k), idesc, (kb | k) != 0);
-        }
+        for (int k = 0; k < BK / 16; ++k)
+          tc::mma_f16(tmem + b * BN, tc::smem_desc_sw128(a_base + 32 * k), tc::smem_desc_sw128(b_base + 32 * k),
+                      idesc, (kb > kb_lo) || k);
+        tc::mma_commit(empty0 + 8 * s);
       }
-      tc::mma_commit(empty0 + 8 * s);
+      if (!ok) break;
+      tc::mma_commit(acc_full0 + 8 * b);
     }
-    if (ok) tc::mma_commit(accum);
+    if (!ok) s_abort = 1;
   } else if (warp >= 2) {
-    // ---- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
-    const int q = warp & 3;
-    const int row = m0 + q * 32 + lane;
-    if (tc::mbar_wait(accum, 0, err)) {
+    // ---- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, columns of half (w-2)/4
+    const int q = warp & 3, eh = (warp - 2) >> 2;
+    int i = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+      int m0, n0, z, kb_lo, kb_hi;
+      unit_of(u, m0, n0, z, kb_lo, kb_hi);
+      const int b = i & 1;
+      if (!tc::mbar_wait(acc_full0 + 8 * b, (i >> 1) & 1, err)) break;
       tc::tc_fence_after();
-      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-      if (EPI == EPI_SWIGLU && splits > 1) {  // raw gate and up partials: ws[z][M][2N]
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + b * BN;
+      // Each 32 x 32 block goes through the warp's shared-memory scratch (row stride 33 words,
+      // conflict-free both ways) so that every store instruction writes 32 consecutive
+      // columns of one row.
+      float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE + 256) + (warp - 2) * 32 * 33;
+      const int rbase = m0 + q * 32;
+      constexpr bool GLU_OUT = EPI == EPI_SWIGLU;  // SwiGLU applied here (no split)
+      const int ncol = GLU_OUT && g.splits == 1 ? BN / 2 : BN;
+      for (int c = eh * ncol / 2; c < (eh + 1) * ncol / 2; c += 32) {
+        float v[32];
+        if (GLU_OUT && g.splits == 1) {
+          float gv[32], uv[32];
+          tc::tmem_ld32(lane_base + c, gv);
+          tc::tmem_ld32(lane_base + BN / 2 + c, uv);
+#pragma unroll
+          for (int i1 = 0; i1 < 32; ++i1) v[i1] = __fdividef(gv[i1], 1.f + __expf(-gv[i1])) * uv[i1];
+        } else {
           tc::tmem_ld32(lane_base + c, v);
-          const int col = n0 + (c < BN / 2 ? c : c - BN / 2);  // column of the gate / up output
-          if (row < M && col < N) {
-            float* out = ws + ((size_t)blockIdx.z * M + row) * 2 * N + (c < BN / 2 ? 0 : N) + col;
-            if (col + 32 <= N && (N & 3) == 0) {
-#pragma unroll
-              for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4*>(out + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-            } else {
-              for (int i = 0; i < 32 && col + i < N; ++i) out[i] = v[i];
-            }
-          }
         }
-      } else if (EPI == EPI_SWIGLU) {
-        for (int c = 0; c < BN / 2; c += 32) {
-          float g[32], u[32];
-          tc::tmem_ld32(lane_base + c, g);
-          tc::tmem_ld32(lane_base + BN / 2 + c, u);
-          if (row < M) {
-            f16* out = ep.Cb + (size_t)row * ep.ldc + n0 + c;
+        __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int col = n0 + c + i;
-              const float a0 = (g[i] / (1.f + expf(-g[i]))) * u[i];
-              const float a1 = (g[i + 1] / (1.f + expf(-g[i + 1]))) * u[i + 1];
-              if (col + 1 < N) {
-                *reinterpret_cast<__half2*>(out + i) = to_half2_checked(a0, a1, err);
-              } else if (col < N) {
-                out[i] = to_half_checked(a0, err);
-              }
-            }
-          }
+        for (int i1 = 0; i1 < 32; ++i1) stg[lane * 33 + i1] = v[i1];
+        __syncwarp();
+        // this lane's output column and where the block's rows go
+        int col = n0 + c + lane;
+        size_t base_off = 0;
+        if (GLU_OUT && g.splits > 1) {  // raw gate then up partials: ws[z][M][2N]
+          const bool up = c >= BN / 2;
+          col = n0 + (up ? c - BN / 2 : c) + lane;
+          base_off = up ? (size_t)N : 0;
         }
-      } else if (splits > 1) {  // raw partial tile of this K range
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tc::tmem_ld32(lane_base + c, v);
-          if (row < M) {
-            float* out = ws + ((size_t)blockIdx.z * M + row) * N + n0 + c;
-            if (n0 + c + 32 <= N && (N & 3) == 0) {
+        if (col < N) {
+          const float bias = EPI == EPI_STORE && g.splits == 1 && ep.bias ? to_f32(ep.bias[col]) : 0.f;
+          const int nr = min(32, M - rbase);
+          if (EPI == EPI_ADD && g.splits == 1) {  // residual add: all loads first
+            float old[32];
 #pragma unroll
-              for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4*>(out + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-            } else {
-              for (int i = 0; i < 32 && n0 + c + i < N; ++i) out[i] = v[i];
-            }
-          }
-        }
-      } else {
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tc::tmem_ld32(lane_base + c, v);
-          if (row < M) {
-            float* out = ep.C + (size_t)row * ep.ldc + n0 + c;
-            if (n0 + c + 32 <= N) {
+            for (int rr = 0; rr < 32; ++rr)
+              old[rr] = rr < nr ? ep.C[(size_t)(rbase + rr) * ep.ldc + col] : 0.f;
 #pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                float4 o;
-                if (EPI == EPI_ADD) {
-                  o = *reinterpret_cast<const float4*>(out + i);
-                  o.x += v[i]; o.y += v[i + 1]; o.z += v[i + 2]; o.w += v[i + 3];
-                } else {
-                  o = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                  if (ep.bias) {
-                    o.x += to_f32(ep.bias[n0 + c + i]);
-                    o.y += to_f32(ep.bias[n0 + c + i + 1]);
-                    o.z += to_f32(ep.bias[n0 + c + i + 2]);
-                    o.w += to_f32(ep.bias[n0 + c + i + 3]);
-                  }
-                }
-                *reinterpret_cast<float4*>(out + i) = o;
-              }
-            } else {
-              for (int i = 0; i < 32 && n0 + c + i < N; ++i) {
-                float o = v[i];
-                if (EPI == EPI_ADD) o += out[i];
-                else if (ep.bias) o += to_f32(ep.bias[n0 + c + i]);
-                out[i] = o;
+            for (int rr = 0; rr < 32; ++rr)
+              if (rr < nr) ep.C[(size_t)(rbase + rr) * ep.ldc + col] = old[rr] + stg[rr * 33 + lane];
+          } else {
+#pragma unroll 4
+            for (int rr = 0; rr < nr; ++rr) {
+              const float x = stg[rr * 33 + lane];
+              const int row = rbase + rr;
+              if (g.splits > 1) {
+                if (GLU_OUT)
+                  ws[((size_t)z * M + row) * 2 * N + base_off + col] = x;
+                else
+                  ws[((size_t)z * M + row) * N + col] = x;
+              } else if (GLU_OUT) {
+                ep.Cb[(size_t)row * ep.ldc + col] = to_half_checked(x, err);
+              } else {
+                ep.C[(size_t)row * ep.ldc + col] = x + bias;
               }
             }
           }
         }
       }
+      // the accumulator is free for unit i + 2
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty0 + 8 * b);
     }
   }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, BN);
+    tc::tmem_dealloc(tmem, 2 * BN);
   }
 }
 
@@ -528,7 +536,8 @@ bool make_map_kv(void* mv, const void* base, int hd, int keys, int nkv, int cap,
 
 template <int BN>
 static constexpr size_t tc_smem() {
-  return (size_t)tc::STAGES * (tc::BM * tc::BK * 2 + BN * tc::BK * 2) + 1024 + 256;
+  // ring, barriers, the epilogue warps' 32 x 33 scratch blocks, alignment slack
+  return (size_t)tc::STAGES * (tc::BM * tc::BK * 2 + BN * tc::BK * 2) + 256 + 8 * 32 * 33 * 4 + 1024;
 }
 
 constexpr int TC_BN = 256;
@@ -655,12 +664,14 @@ cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bi
     if ((size_t)splits * per > ws_floats) splits = (int)(ws_floats / per);
     if (splits < 2) splits = 1;
   }
-  const dim3 grid((N + TC_BN - 1) / TC_BN, (M + tc::BM - 1) / tc::BM, splits);
+  const TcGrid g{(M + tc::BM - 1) / tc::BM, (N + TC_BN - 1) / TC_BN, splits};
+  const int units = g.tiles_m * g.tiles_n * splits;
+  const int grid = nsm > 0 && units > nsm ? nsm : units;  // persistent CTAs
   if (accumulate && splits == 1)
-    gemm_tc_kernel<TC_BN, EPI_ADD><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err, 1, ws);
+    gemm_tc_kernel<TC_BN, EPI_ADD><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err, g, ws);
   else
-    gemm_tc_kernel<TC_BN, EPI_STORE><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err,
-                                                                                  splits, ws);
+    gemm_tc_kernel<TC_BN, EPI_STORE><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err, g,
+                                                                                  ws);
   if (splits > 1) {
     const size_t n = (size_t)M * N;
     splitk_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, bias, C, ldc,
@@ -689,9 +700,11 @@ cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, 
     if ((size_t)splits * per > ws_floats) splits = (int)(ws_floats / per);
     if (splits < 2) splits = 1;
   }
-  const dim3 grid((N + TC_BN / 2 - 1) / (TC_BN / 2), (M + tc::BM - 1) / tc::BM, splits);
-  gemm_tc_kernel<TC_BN, EPI_SWIGLU><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mg, mu, ep, M, N, K, err,
-                                                                                 splits, ws);
+  const TcGrid g{(M + tc::BM - 1) / tc::BM, (N + TC_BN / 2 - 1) / (TC_BN / 2), splits};
+  const int units = g.tiles_m * g.tiles_n * splits;
+  const int grid = nsm > 0 && units > nsm ? nsm : units;  // persistent CTAs
+  gemm_tc_kernel<TC_BN, EPI_SWIGLU><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mg, mu, ep, M, N, K, err, g,
+                                                                                 ws);
   if (splits > 1) {
     const size_t n = (size_t)M * N;
     splitk_swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, Act, ldc, err);

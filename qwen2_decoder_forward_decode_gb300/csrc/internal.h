@@ -24,8 +24,11 @@ struct Dims {
 
 struct LayerPtrs {
   const void *in_norm, *wq, *bq, *wk, *bk, *wv, *bv, *wo, *post_norm, *w_gate, *w_up, *w_down;
-  // fp16 copies of the matrices (bf16 models; prefill tensor-core operands)
+  // fp16 copies of the matrices (bf16 models; prefill tensor-core operands). wq16, wk16 and
+  // wv16 lie back to back (one [nq*hd + 2*nkv*hd][H] matrix), bqkv holds bq | bk | bv (bf16)
+  // or is null without q/k/v biases.
   const void *wq16, *wk16, *wv16, *wo16, *wg16, *wu16, *wd16;
+  const void* bqkv;
 };
 
 // Argmax / position bookkeeping written by the last CTA of the LM-head kernel.

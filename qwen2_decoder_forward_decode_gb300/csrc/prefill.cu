@@ -552,9 +552,16 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
     f16* kc = (f16*)kcache + (size_t)l * 2 * layer_stride;
     f16* vc = kc + layer_stride;
     norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.in_norm, H, d.eps, b.Xh, err);
-    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wq16, H, (const bf16*)w.bq, b.Y, Wd, T_, qd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wk16, H, (const bf16*)w.bk, b.Y + qd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-    if ((e = gemm_tc(b.Xh, H, (const f16*)w.wv16, H, (const bf16*)w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+    if (w.wk16 == (const f16*)w.wq16 + (size_t)qd * H && w.wv16 == (const f16*)w.wk16 + (size_t)kvd * H &&
+        (w.bqkv || !w.bq)) {
+      // q | k | v as one projection: the three matrices lie back to back, and so do the
+      // columns of Y
+      if ((e = gemm_tc(b.Xh, H, (const f16*)w.wq16, H, (const bf16*)w.bqkv, b.Y, Wd, T_, Wd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+    } else {
+      if ((e = gemm_tc(b.Xh, H, (const f16*)w.wq16, H, (const bf16*)w.bq, b.Y, Wd, T_, qd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+      if ((e = gemm_tc(b.Xh, H, (const f16*)w.wk16, H, (const bf16*)w.bk, b.Y + qd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+      if ((e = gemm_tc(b.Xh, H, (const f16*)w.wv16, H, (const bf16*)w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+    }
     const int kind = prefill_attention_kind();
     if (kind == PA_TC && attn_prefill_tc_supported(d.hd) && d.I >= qd) {
       // q in fp16, scaled into base-2 scores, in the (still free) SwiGLU operand buffer

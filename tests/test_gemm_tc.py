@@ -1,6 +1,7 @@
 """The tcgen05 tensor-core GEMMs of the prefill (qw_op_gemm_f16, qw_op_gemm_swiglu_f16)
 against float64 numpy on the same fp16 operands: tile-aligned and ragged M, N, K, the
-bias, residual-accumulate and fused SwiGLU epilogues."""
+bias, residual-accumulate and fused SwiGLU epilogues, and more output tiles than SMs (each
+persistent CTA then runs several tiles through its two TMEM accumulators)."""
 import numpy as np
 import pytest
 
@@ -26,6 +27,8 @@ def _f16(a):
     (257, 128, 1000, True, False),    # K not a multiple of the 64-element stage
     (129, 2048, 1536, False, True),
     (512, 1536, 8960, False, True),   # the down projection's K
+    (2048, 4096, 256, True, False),   # more tiles than SMs: each persistent CTA takes several
+    (1000, 2056, 320, False, True),   # several tiles per CTA with ragged M and N
 ])
 def test_gemm_f16(M, N, K, bias, acc):
     from qwen2_decoder_forward_decode_gb300 import binding
@@ -54,7 +57,7 @@ def test_gemm_f16(M, N, K, bias, acc):
     assert np.all(np.abs(got - ref) <= tol), float(np.max(np.abs(got - ref) / tol))
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (33, 1000, 384), (200, 8960, 1536)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (33, 1000, 384), (200, 8960, 1536), (1100, 8960, 256)])
 def test_gemm_swiglu_f16(M, N, K):
     from qwen2_decoder_forward_decode_gb300 import binding
     rng = np.random.default_rng(M + N + K)
