@@ -97,7 +97,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) tc::tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+  constexpr uint32_t TCOLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators, a power of two
+  if (warp == 0) tc::tmem_alloc(smem_u32(tmem_slot), TCOLS);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -239,7 +240,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   __syncthreads();
   if (warp == 0) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 2 * BN);
+    tc::tmem_dealloc(tmem, TCOLS);
   }
 }
 
@@ -545,6 +546,8 @@ constexpr int TC_BN = 256;
 cudaError_t gemm_tc_set_attributes() {
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>()))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<192, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<192>()))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<192, EPI_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<192>()))) return e;
   if ((e = cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>()))) return e;
   return cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>());
 }
@@ -645,14 +648,30 @@ cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, i
 }
 
 // C[M][N] (fp32, ldc) = / += A[M][K] (fp16, lda) . B[N][K]^T (fp16, ldb) (+ bias[N], bf16)
+template <int BN>
+static void launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const TcEpi& ep, int M, int N, int K,
+                        bool add, int* err, const TcGrid& g, float* ws, int nsm, cudaStream_t s) {
+  const int units = g.tiles_m * g.tiles_n * g.splits;
+  const int grid = nsm > 0 && units > nsm ? nsm : units;  // persistent CTAs
+  if (add)
+    gemm_tc_kernel<BN, EPI_ADD><<<grid, tc::THREADS, tc_smem<BN>(), s>>>(ma, mb, mb, ep, M, N, K, err, g, ws);
+  else
+    gemm_tc_kernel<BN, EPI_STORE><<<grid, tc::THREADS, tc_smem<BN>(), s>>>(ma, mb, mb, ep, M, N, K, err, g, ws);
+}
+
 cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bias, float* C, int ldc,
                     int M, int N, int K, bool accumulate, int* err, cudaStream_t s, float* ws, size_t ws_floats,
                     int nsm) {
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mb, B, N, K, ldb, TC_BN)) return cudaErrorInvalidValue;
-  TcEpi ep{C, bias, nullptr, ldc};
-  const int tiles = ((N + TC_BN - 1) / TC_BN) * ((M + tc::BM - 1) / tc::BM);
+  const int tiles_m = (M + tc::BM - 1) / tc::BM;
   const int nk = (K + tc::BK - 1) / tc::BK;
+  // tile width: 256 or 192 columns, whichever finishes first when the tiles go round the
+  // SMs in whole rounds (time of a round ~ tile width)
+  int bn = TC_BN;
+  if (nsm > 0) {
+    auto rounds = [&](int w) { const int u = tiles_m * ((N + w - 1) / w); return (u + nsm - 1) / nsm; };
+    if ((long long)rounds(192) * 192 < (long long)rounds(TC_BN) * TC_BN) bn = 192;
+  }
+  const int tiles = ((N + bn - 1) / bn) * tiles_m;
   // too few tiles to stream the weights from every SM: split K (up to 16 ways, at least two
   // K blocks per split, as far as the workspace holds the partial tiles)
   int splits = 1;
@@ -664,14 +683,13 @@ cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bi
     if ((size_t)splits * per > ws_floats) splits = (int)(ws_floats / per);
     if (splits < 2) splits = 1;
   }
-  const TcGrid g{(M + tc::BM - 1) / tc::BM, (N + TC_BN - 1) / TC_BN, splits};
-  const int units = g.tiles_m * g.tiles_n * splits;
-  const int grid = nsm > 0 && units > nsm ? nsm : units;  // persistent CTAs
-  if (accumulate && splits == 1)
-    gemm_tc_kernel<TC_BN, EPI_ADD><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err, g, ws);
-  else
-    gemm_tc_kernel<TC_BN, EPI_STORE><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mb, mb, ep, M, N, K, err, g,
-                                                                                  ws);
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mb, B, N, K, ldb, bn)) return cudaErrorInvalidValue;
+  TcEpi ep{C, bias, nullptr, ldc};
+  const TcGrid g{tiles_m, (N + bn - 1) / bn, splits};
+  const bool add = accumulate && splits == 1;
+  if (bn == 192) launch_gemm<192>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
+  else launch_gemm<TC_BN>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
   if (splits > 1) {
     const size_t n = (size_t)M * N;
     splitk_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, bias, C, ldc,

@@ -44,6 +44,41 @@ __global__ void norm_rows_kernel(const float* X, const T* gain, int H, float eps
   for (int k = threadIdx.x; k < H; k += blockDim.x) store_norm(y + k, x[k] * inv * to_f32(gain[k]), err);
 }
 
+// The same for fp16 output rows with H a multiple of 128: one warp per row, float4 loads
+// and 8-byte stores. The row is read twice (sum of squares, then the scaled values); the
+// second read comes from L2. Sums in a fixed order: deterministic.
+__global__ void norm_rows_h_kernel(const float* X, const bf16* gain, int T, int H, float eps, f16* Y, int* err) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= T) return;
+  const float4* x = reinterpret_cast<const float4*>(X + (size_t)row * H);
+  float ss = 0.f;
+  for (int k = lane; k < H / 4; k += 32) {
+    const float4 v = x[k];
+    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+  }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)H + eps);
+  const uint2* gp = reinterpret_cast<const uint2*>(gain);
+  uint2* y = reinterpret_cast<uint2*>(Y + (size_t)row * H);
+  for (int k = lane; k < H / 4; k += 32) {
+    const float4 v = x[k];
+    const uint2 gb = gp[k];
+    const float g0 = __uint_as_float(gb.x << 16), g1 = __uint_as_float(gb.x & 0xffff0000u);
+    const float g2 = __uint_as_float(gb.y << 16), g3 = __uint_as_float(gb.y & 0xffff0000u);
+    const __half2 lo = to_half2_checked(v.x * inv * g0, v.y * inv * g1, err);
+    const __half2 hi = to_half2_checked(v.z * inv * g2, v.w * inv * g3, err);
+    y[k] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  }
+}
+
+static void norm_rows_h(const float* X, const bf16* gain, int T_, int H, float eps, f16* Y, int* err, cudaStream_t s) {
+  if (H % 128 == 0 && ((uintptr_t)gain & 7) == 0) {
+    norm_rows_h_kernel<<<(T_ + 7) / 8, 256, 0, s>>>(X, gain, T_, H, eps, Y, err);
+  } else {
+    norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(X, gain, H, eps, Y, err);
+  }
+}
+
 // fp32 -> fp16 rows (tensor-core A operand)
 __global__ void to_half_kernel(const float* X, f16* Y, size_t n, int* err) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
@@ -93,6 +128,42 @@ __global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, 
       store_kv(dst + i, a, err);
       store_kv(dst + i + half, b, err);
     }
+  }
+}
+
+// The tensor-core path's variant: fp16 cache, Q to fp16 times qscale; two adjacent pairs
+// (i, i + 1) per thread with 8-byte loads and 4-byte stores (hd a multiple of 4).
+__global__ void rope_kv_h_kernel(const float* Y, int nq, int nkv, int hd, int pos0, int cap, const float2* rope,
+                                 f16* Qh, float qscale, f16* kc, f16* vc, int* err) {
+  const int t = blockIdx.x;
+  const int half = hd / 2, hp = half / 2;  // pairs of i per head
+  const int pos = pos0 + t;
+  const float* y = Y + (size_t)t * (nq + 2 * nkv) * hd;
+  for (int idx = threadIdx.x; idx < (nq + 2 * nkv) * hp; idx += blockDim.x) {
+    const int head = idx / hp, i = 2 * (idx - head * hp);
+    const float2 a = *reinterpret_cast<const float2*>(y + head * hd + i);
+    const float2 b = *reinterpret_cast<const float2*>(y + head * hd + i + half);
+    __half2 lo, hi;
+    f16* dst;
+    if (head < nq + nkv) {
+      const float4 cs = *reinterpret_cast<const float4*>(rope + (size_t)pos * half + i);  // (cos, sin) of i, i + 1
+      float ra0 = a.x * cs.x - b.x * cs.y, rb0 = b.x * cs.x + a.x * cs.y;
+      float ra1 = a.y * cs.z - b.y * cs.w, rb1 = b.y * cs.z + a.y * cs.w;
+      if (head < nq) {
+        ra0 *= qscale; ra1 *= qscale; rb0 *= qscale; rb1 *= qscale;
+        dst = Qh + (size_t)t * nq * hd + head * hd;
+      } else {
+        dst = kc + ((size_t)(head - nq) * cap + pos) * hd;
+      }
+      lo = to_half2_checked(ra0, ra1, err);
+      hi = to_half2_checked(rb0, rb1, err);
+    } else {
+      dst = vc + ((size_t)(head - nq - nkv) * cap + pos) * hd;
+      lo = to_half2_checked(a.x, a.y, err);
+      hi = to_half2_checked(b.x, b.y, err);
+    }
+    *reinterpret_cast<__half2*>(dst + i) = lo;
+    *reinterpret_cast<__half2*>(dst + i + half) = hi;
   }
 }
 
@@ -551,7 +622,7 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
     const LayerPtrs& w = layers[l];
     f16* kc = (f16*)kcache + (size_t)l * 2 * layer_stride;
     f16* vc = kc + layer_stride;
-    norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.in_norm, H, d.eps, b.Xh, err);
+    norm_rows_h(b.X, (const bf16*)w.in_norm, T_, H, d.eps, b.Xh, err, s);
     if (w.wk16 == (const f16*)w.wq16 + (size_t)qd * H && w.wv16 == (const f16*)w.wk16 + (size_t)kvd * H &&
         (w.bqkv || !w.bq)) {
       // q | k | v as one projection: the three matrices lie back to back, and so do the
@@ -566,8 +637,11 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
     if (kind == PA_TC && attn_prefill_tc_supported(d.hd) && d.I >= qd) {
       // q in fp16, scaled into base-2 scores, in the (still free) SwiGLU operand buffer
       const float qs = 1.4426950408889634f / sqrtf((float)d.hd);
-      rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err, b.Ah,
-                                            qs);
+      if (d.hd % 4 == 0)
+        rope_kv_h_kernel<<<T_, 256, 0, s>>>(b.Y, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Ah, qs, kc, vc, err);
+      else
+        rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err,
+                                              b.Ah, qs);
       if ((e = attn_prefill_tc(d, T_, pos0, b.Ah, kc, vc, b.Oh, err, s))) return e;
     } else {
       rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err);
@@ -581,7 +655,7 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
       }
     }
     if ((e = gemm_tc(b.Oh, qd, (const f16*)w.wo16, qd, nullptr, b.X, H, T_, H, qd, true, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-    norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(b.X, (const bf16*)w.post_norm, H, d.eps, b.Xh, err);
+    norm_rows_h(b.X, (const bf16*)w.post_norm, T_, H, d.eps, b.Xh, err, s);
     if ((e = gemm_tc_swiglu(b.Xh, H, (const f16*)w.wg16, (const f16*)w.wu16, H, b.Ah, d.I, T_, d.I, H, err, s, b.ws,
                               b.ws_floats, d.nsm)))
       return e;

@@ -29,6 +29,8 @@ def _f16(a):
     (512, 1536, 8960, False, True),   # the down projection's K
     (2048, 4096, 256, True, False),   # more tiles than SMs: each persistent CTA takes several
     (1000, 2056, 320, False, True),   # several tiles per CTA with ragged M and N
+    (4096, 1536, 256, True, False),   # 192-column tiles, several per CTA
+    (2000, 1536, 512, False, True),   # 192-column tiles, residual add, ragged M
 ])
 def test_gemm_f16(M, N, K, bias, acc):
     from qwen2_decoder_forward_decode_gb300 import binding
