@@ -704,6 +704,50 @@ def read_tensor_peak():
     return 1900.0, "fallback"
 
 
+def measure_gemms(s, M, reps=20):
+    """Profiling: the prefill projections of one layer of shape s for an M-token prompt, each
+    timed alone through the GEMM entry points (CUDA events, `reps` launches back to back)."""
+    import torch
+    from qwen2_decoder_forward_decode_gb300 import binding
+    H, I = s.hidden, s.intermediate
+    qkv = (s.n_heads + 2 * s.n_kv_heads) * s.head_dim
+    shapes = [("qkv", qkv, H, True, False), ("o_proj", H, s.n_heads * s.head_dim, False, True),
+              ("gate_up", I, H, None, None), ("down", H, I, False, True)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    out = {}
+    for name, N, K, bias, acc in shapes:
+        A = (torch.randn(M, K, device="cuda", generator=g) * 0.5).half()
+        if name == "gate_up":
+            Wg = (torch.randn(N, K, device="cuda", generator=g) * 0.02).half()
+            Wu = (torch.randn(N, K, device="cuda", generator=g) * 0.02).half()
+            act = torch.empty(M, N, dtype=torch.float16, device="cuda")
+            f = lambda: binding.gemm_swiglu_f16(M, N, K, A.data_ptr(), Wg.data_ptr(), Wu.data_ptr(),
+                                                act.data_ptr(), err.data_ptr())
+            flop = 2.0 * M * 2 * N * K
+        else:
+            B = (torch.randn(N, K, device="cuda", generator=g) * 0.02).half()
+            bb = (torch.randn(N, device="cuda", generator=g) * 0.02).bfloat16()
+            C = torch.zeros(M, N, device="cuda")
+            f = lambda: binding.gemm_f16(M, N, K, A.data_ptr(), B.data_ptr(), bb.data_ptr() if bias else None,
+                                         C.data_ptr(), acc, err.data_ptr())
+            flop = 2.0 * M * N * K
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, "device error bits set"
+        us = e0.elapsed_time(e1) * 1000.0 / reps
+        out[name] = {"N": N, "K": K, "us": us, "tflops": flop / us / 1e6}
+    return out
+
+
 def run_section(args):
     """Profiling: one of the extra workloads alone (one JSON line, not the bench line)."""
     import torch
@@ -715,6 +759,14 @@ def run_section(args):
     if args.layers:
         import dataclasses
         s = dataclasses.replace(s, n_layers=args.layers)
+    if args.gemm:
+        peak, kind = read_tensor_peak()
+        out = {"profile_run": "gemm", "M": 4096, "shape": s.name, "gemms": measure_gemms(s, 4096),
+               "tensor_peak_tflops": peak, "tensor_peak_kind": kind}
+        for v in out["gemms"].values():
+            v["frac_of_tensor_peak"] = v["tflops"] / peak
+        print(json.dumps(out), flush=True)
+        return
     dw = DeviceWeights(make_weights(s), 1)
     if args.long:
         out = measure_long(dw, s, args.steps, args.warmup, 1, 0)
@@ -742,8 +794,10 @@ def main():
                     help="profiling: only the batched section (one JSON line, not the bench line)")
     ap.add_argument("--long", action="store_true",
                     help="profiling: only the long-context section (one JSON line, not the bench line)")
+    ap.add_argument("--gemm", action="store_true",
+                    help="profiling: the prefill projections of one layer at 4096 tokens, each timed alone")
     args = ap.parse_args()
-    if args.long or args.batched:
+    if args.long or args.batched or args.gemm:
         run_section(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -140,6 +140,16 @@ qw_status qw_decode_steps(qw_model *m, int32_t n_steps);
 qw_status qw_generate(qw_model *m, const int32_t *ids, int32_t n, int32_t max_new,
                       int32_t eos, int32_t *out, int32_t *n_out);
 
+/* The same with a set of stop ids [LSA Implementing Qwen: generate_tokens stops on any id of
+ * its eos_ids set, the chat template's end tokens among them]: generation stops after the
+ * first produced token that equals any of stop_ids[0 .. n_stop-1] (host array, may hold
+ * duplicates; n_stop = 0: no stop id). That token is kept, and the sequence continues
+ * from it as after qw_generate. Errors: QW_ERR_INVALID_ARG for n_stop < 0 or a null
+ * stop_ids with n_stop > 0, and those of qw_generate. */
+qw_status qw_generate_stops(qw_model *m, const int32_t *ids, int32_t n, int32_t max_new,
+                            const int32_t *stop_ids, int32_t n_stop, int32_t *out,
+                            int32_t *n_out);
+
 /* Wait for queued work and report a device-side error (token range, non-finite logits). */
 qw_status qw_sync(qw_model *m);
 

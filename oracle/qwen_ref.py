@@ -237,15 +237,21 @@ def step(m: OracleModel, token_ids, positions, cache):
     return greedy(z), z
 
 
-def generate(m: OracleModel, prompt, max_new, eos=-1, feed=None):
+def _is_stop(t, eos, eos_ids):
+    return (eos >= 0 and t == eos) or (eos_ids is not None and t in eos_ids)
+
+
+def generate(m: OracleModel, prompt, max_new, eos=-1, feed=None, eos_ids=None):
     """Greedy generation with a KV cache [AUG Prefill/decode split, EOS stopping].
 
     Step 0 runs the whole prompt at positions 0..P-1; each later step runs the last
     token alone at position len-1. ``max_new`` counts every generated token, the
     prefill's included. With ``feed`` (teacher forcing) the token run at decode step i
-    is feed[i-1] instead of the previous argmax. A token equal to ``eos`` is appended,
-    then generation stops. Returns (tokens, [logits per step]).
+    is feed[i-1] instead of the previous argmax. A token equal to ``eos``, or to any id
+    of the set ``eos_ids`` ([LSA] Implementing Qwen: generate_tokens and its eos_ids), is
+    appended, then generation stops. Returns (tokens, [logits per step]).
     """
+    eos_ids = None if eos_ids is None else {int(e) for e in eos_ids}
     cache = KVCache(m.cfg.n_layers)
     seq = [int(t) for t in prompt]
     out, logits = [], []
@@ -260,7 +266,7 @@ def generate(m: OracleModel, prompt, max_new, eos=-1, feed=None):
         out.append(t)
         logits.append(z)
         seq.append(t)
-        if eos >= 0 and t == eos:
+        if _is_stop(t, eos, eos_ids):
             break
     return out, logits
 

@@ -70,6 +70,7 @@ def lib():
         "qw_decode_step": ([VP, pi, pi], I32),
         "qw_decode_steps": ([VP, I32], I32),
         "qw_generate": ([VP, pi, I32, I32, I32, pi, pi], I32),
+        "qw_generate_stops": ([VP, pi, I32, I32, pi, I32, pi, pi], I32),
         "qw_sync": ([VP], I32),
         "qw_logits": ([VP], VP),
         "qw_read_logits": ([VP, I32, P(ctypes.c_float)], I32),
@@ -98,7 +99,7 @@ def lib():
 
 def exported_symbols():
     return ["qw_create", "qw_destroy", "qw_prefill", "qw_prefill_device", "qw_decode_step",
-            "qw_decode_steps", "qw_generate", "qw_sync", "qw_logits", "qw_read_logits",
+            "qw_decode_steps", "qw_generate", "qw_generate_stops", "qw_sync", "qw_logits", "qw_read_logits",
             "qw_tokens_device", "qw_decode_kernels_per_step", "qw_position", "qw_reset",
             "qw_last_error", "qw_set_trace",
             "qw_set_timeline", "qw_read_timeline",
@@ -212,11 +213,18 @@ class Model:
     def decode_steps(self, n):
         check(lib().qw_decode_steps(self.h, n))
 
-    def generate(self, ids, max_new, eos=-1):
+    def generate(self, ids, max_new, eos=-1, eos_ids=None):
+        """Greedy generation of sequence 0; stops after a token equal to eos (eos >= 0) or
+        to any id of eos_ids (qw_generate_stops), which is kept."""
         ids = np.ascontiguousarray(ids, dtype=np.int32)
         out = np.zeros(max_new, dtype=np.int32)
         n_out = np.zeros(1, dtype=np.int32)
-        check(lib().qw_generate(self.h, _iptr(ids), len(ids), max_new, eos, _iptr(out), _iptr(n_out)))
+        if eos_ids is None:
+            check(lib().qw_generate(self.h, _iptr(ids), len(ids), max_new, eos, _iptr(out), _iptr(n_out)))
+        else:
+            stops = np.ascontiguousarray(list(eos_ids) + ([eos] if eos >= 0 else []), dtype=np.int32)
+            check(lib().qw_generate_stops(self.h, _iptr(ids), len(ids), max_new, _iptr(stops), len(stops),
+                                          _iptr(out), _iptr(n_out)))
         return out[:int(n_out[0])].tolist()
 
     def sync(self):

@@ -433,7 +433,7 @@ static qw_status validate(const qw_config* c, const qw_weights* w) {
   const int vec = c->dtype == QW_BF16 ? 8 : 4;
   if (c->hidden % vec || c->intermediate % vec)
     return fail(QW_ERR_UNSUPPORTED, "hidden and intermediate must be multiples of 16 bytes of weights");
-  if (c->hidden > 8 * 32 * 8 * vec || c->intermediate > 8 * 32 * 8 * vec)
+  if (c->hidden > 8 * 32 * 12 * vec || c->intermediate > 8 * 32 * 12 * vec)
     return fail(QW_ERR_UNSUPPORTED, "hidden or intermediate too large for the decode GEMV");
   if (!w->embed || !w->final_norm || !w->layers) return fail(QW_ERR_INVALID_ARG, "null weight pointer");
   if (!c->tied_embeddings && !w->lm_head) return fail(QW_ERR_INVALID_ARG, "untied model without lm_head");
@@ -833,10 +833,10 @@ qw_status qw_decode_steps(qw_model* m, int32_t n_steps) {
   return QW_OK;
 }
 
-qw_status qw_generate(qw_model* m, const int32_t* ids, int32_t n, int32_t max_new, int32_t eos,
-                      int32_t* out, int32_t* n_out) {
-  g_err.clear();
+static qw_status generate_impl(qw_model* m, const int32_t* ids, int32_t n, int32_t max_new,
+                               const int32_t* stops, int32_t n_stops, int32_t* out, int32_t* n_out) {
   if (!m || !out || !n_out) return fail(QW_ERR_INVALID_ARG, "null argument");
+  if (n_stops < 0 || (n_stops > 0 && !stops)) return fail(QW_ERR_INVALID_ARG, "bad stop-id set");
   if (max_new < 1) return fail(QW_ERR_INVALID_ARG, "max_new must be positive");
   qw_status st = prefill_common(m, 0, n);
   if (st) return st;
@@ -845,7 +845,7 @@ qw_status qw_generate(qw_model* m, const int32_t* ids, int32_t n, int32_t max_ne
   m->bactive_dirty = true;
   st = qw_prefill(m, 0, ids, n, nullptr);
   if (st) return st;
-  const int chunk = eos >= 0 ? 16 : max_new;
+  const int chunk = n_stops > 0 ? 16 : max_new;
   int done = 1;  // tokens produced so far
   int produced_total = 1;
   while (true) {
@@ -860,9 +860,9 @@ qw_status qw_generate(qw_model* m, const int32_t* ids, int32_t n, int32_t max_ne
     st = m->check_device_errors();
     if (st) return st;
     int cut = -1;
-    if (eos >= 0)
-      for (int i = 0; i < done; ++i)
-        if (m->pinned[i] == eos) { cut = i + 1; break; }
+    for (int i = 0; i < done && cut < 0; ++i)
+      for (int k = 0; k < n_stops; ++k)
+        if (m->pinned[i] == stops[k]) { cut = i + 1; break; }
     if (cut > 0 || done >= max_new) {
       const int k = cut > 0 ? cut : done;
       std::memcpy(out, m->pinned, sizeof(int) * k);
@@ -879,6 +879,18 @@ qw_status qw_generate(qw_model* m, const int32_t* ids, int32_t n, int32_t max_ne
       return QW_OK;
     }
   }
+}
+
+qw_status qw_generate(qw_model* m, const int32_t* ids, int32_t n, int32_t max_new, int32_t eos,
+                      int32_t* out, int32_t* n_out) {
+  g_err.clear();
+  return generate_impl(m, ids, n, max_new, &eos, eos >= 0 ? 1 : 0, out, n_out);
+}
+
+qw_status qw_generate_stops(qw_model* m, const int32_t* ids, int32_t n, int32_t max_new, const int32_t* stop_ids,
+                            int32_t n_stop, int32_t* out, int32_t* n_out) {
+  g_err.clear();
+  return generate_impl(m, ids, n, max_new, stop_ids, n_stop, out, n_out);
 }
 
 qw_status qw_sync(qw_model* m) {

@@ -784,7 +784,7 @@ static unsigned l2_ahead_piece() {
 
 static int maxv_for(int nvec, int KS) {
   const int need = (((nvec + KS - 1) / KS) + 31) / 32;
-  return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 6 ? 6 : need <= 8 ? 8 : 99;
+  return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 6 ? 6 : need <= 8 ? 8 : need <= 12 ? 12 : 99;
 }
 
 struct GemvPlan {
@@ -804,7 +804,7 @@ static bool plan_gemv(const Op& op, int nsm, int* err, unsigned long long* tl, G
   auto slot_of = [&](int ks) { return (size_t)Op::RPI * ((nvec + ks - 1) / ks) * 16; };
   const int WARP_BUDGET = warp_budget(Op::SLOT_KNOB);
   while (KS < GEMV_WARPS && (maxv_for(nvec, KS) > 8 || 2 * slot_of(KS) > (size_t)WARP_BUDGET)) KS *= 2;
-  if (maxv_for(nvec, KS) > 8) return false;
+  if (maxv_for(nvec, KS) > 12) return false;
   while (KS < GEMV_WARPS && (long long)op.n_items * KS < (long long)nsm * GEMV_WARPS) KS *= 2;
   const size_t slot = (slot_of(KS) + 127) & ~(size_t)127;
   int NS = (int)(WARP_BUDGET / slot);
@@ -842,14 +842,15 @@ static cudaError_t run_gemv(const Op& op, int nsm, int* err, unsigned long long*
     case 2: return launch_k(gemv_kernel<T, 2, Op>, g, b, p.smem, s, pdl, op, p.c);
     case 4: return launch_k(gemv_kernel<T, 4, Op>, g, b, p.smem, s, pdl, op, p.c);
     case 6: return launch_k(gemv_kernel<T, 6, Op>, g, b, p.smem, s, pdl, op, p.c);
-    default: return launch_k(gemv_kernel<T, 8, Op>, g, b, p.smem, s, pdl, op, p.c);
+    case 8: return launch_k(gemv_kernel<T, 8, Op>, g, b, p.smem, s, pdl, op, p.c);
+    default: return launch_k(gemv_kernel<T, 12, Op>, g, b, p.smem, s, pdl, op, p.c);
   }
 }
 
 template <typename T, class Op>
 static cudaError_t set_gemv_attrs() {
-  void* fns[5] = {(void*)gemv_kernel<T, 1, Op>, (void*)gemv_kernel<T, 2, Op>, (void*)gemv_kernel<T, 4, Op>,
-                  (void*)gemv_kernel<T, 6, Op>, (void*)gemv_kernel<T, 8, Op>};
+  void* fns[6] = {(void*)gemv_kernel<T, 1, Op>, (void*)gemv_kernel<T, 2, Op>, (void*)gemv_kernel<T, 4, Op>,
+                  (void*)gemv_kernel<T, 6, Op>, (void*)gemv_kernel<T, 8, Op>, (void*)gemv_kernel<T, 12, Op>};
   for (void* f : fns) {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e) return e;

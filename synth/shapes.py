@@ -48,6 +48,10 @@ SHAPES = {
     "0p5b": Shape("0p5b", 24, 896, 14, 2, 64, 4864, 151936, "bf16"),
     # Qwen2.5-1.5B shape, bf16
     "1p5b": Shape("1p5b", 28, 1536, 12, 2, 128, 8960, 151936, "bf16"),
+    # Qwen2.5-Coder-7B shape, bf16 (28 query / 4 KV heads: 7 per group; MLP 18944), and its
+    # first two layers with the full widths and vocabulary for parity runs
+    "7b": Shape("7b", 28, 3584, 28, 4, 128, 18944, 152064, "bf16"),
+    "7b_2l": Shape("7b_2l", 2, 3584, 28, 4, 128, 18944, 152064, "bf16"),
     # small shapes with ragged tails for fast parity tests
     "small_bf16": Shape("small_bf16", 2, 384, 6, 2, 64, 1000, 3001, "bf16"),
     "small_f32": Shape("small_f32", 3, 96, 3, 1, 32, 200, 1000, "f32"),

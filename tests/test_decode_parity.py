@@ -156,6 +156,20 @@ def test_1p5b_long_context():
         m.close()
 
 
+def test_7b_shape_two_layers():
+    """The Qwen2.5-Coder-7B shape (hidden 3584, 28/4 heads, MLP 18944, vocab 152064) on its
+    first two layers: tensor-core prefill of a ragged 150-token prompt, then decode steps
+    whose down projection runs K = 18944 through the GEMV's widest register tile."""
+    w, prompt, toks, logits = oracle_run("7b_2l", 150, 6)
+    m = _model("7b_2l", w, 200)
+    try:
+        rep = run_teacher_forced(m, SHAPES["7b_2l"], prompt, toks, logits)
+        assert rep.steps == 6
+        record("7b shape, 2 layers, 150-token prompt, 6 tokens", rep)
+    finally:
+        m.close()
+
+
 def test_cuda_core_decode_attention(monkeypatch):
     """Decode attention on CUDA cores (QW_ATTN_MMA=0; the tensor-core kernel is the default)
     with its chunks merged in the o_proj GEMV, on a head_dim-128 shape."""
@@ -236,6 +250,27 @@ def test_bad_tokens_rejected():
             m.decode_step(feed=[-1])
         assert e.value.status == 4
         m.decode_step(feed=[5])   # still usable
+    finally:
+        m.close()
+
+
+def test_stop_set_ends_generation_like_the_oracle():
+    """qw_generate_stops: the first produced token in the stop set ends the run, as in the
+    oracle's generate with eos_ids; a set without produced ids runs to max_new."""
+    s = SHAPES["tiny"]
+    w = make_weights(s)
+    prompt = make_prompt(s, 5)
+    om = oracle.OracleModel(oracle.OracleConfig.from_shape(s), w)
+    toks, _ = oracle.generate(om, prompt, 12)
+    absent = next(v for v in range(s.vocab) if v not in toks)
+    stops = [absent, toks[6], toks[4]]
+    want, _ = oracle.generate(om, prompt, 12, eos_ids=stops)
+    m = _model("tiny", w, 20)
+    try:
+        assert m.generate(prompt, 12, eos_ids=stops) == want
+        assert m.position() == len(prompt) + len(want) - 1
+        assert m.generate(prompt, 12, eos_ids=[absent]) == toks
+        assert m.generate(prompt, 12, eos_ids=[]) == toks
     finally:
         m.close()
 

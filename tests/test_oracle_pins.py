@@ -262,6 +262,23 @@ def test_eos_is_appended_then_stops():
     assert t2 == t[:t.index(t[2]) + 1]
 
 
+def test_a_stop_set_stops_at_its_first_member():
+    """generate_tokens' eos_ids: the first produced token found in the set ends the run
+    (and is kept); ids that never come up do nothing; an empty set never stops."""
+    m, w, s = tiny_model()
+    ids = make_prompt(s, 8)
+    t, _ = oracle.generate(m, ids, 10)
+    absent = next(v for v in range(s.vocab) if v not in t)
+    first = min(t.index(t[5]), t.index(t[3]))
+    t2, _ = oracle.generate(m, ids, 10, eos_ids=[t[5], absent, t[3]])
+    assert t2 == t[:first + 1]
+    assert oracle.generate(m, ids, 10, eos_ids=[absent])[0] == t
+    assert oracle.generate(m, ids, 10, eos_ids=[])[0] == t
+    # the single eos and the set combine
+    t3, _ = oracle.generate(m, ids, 10, eos=t[6], eos_ids=[absent])
+    assert t3 == t[:t.index(t[6]) + 1]
+
+
 # --- greedy choice ------------------------------------------------------------------------
 # "augur", Features (greedy generation) and the argmax of the "LLM Speedrun: Architecture"
 # model code: the largest logit wins; among equal maxima the lowest index (numpy's rule).
