@@ -620,8 +620,11 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
       if ((e = cudaMemcpy(m->mega_layers, recs.data(), recs.size(), cudaMemcpyHostToDevice)))
         return bail(e, "cudaMemcpy");
       if ((e = cudaMalloc(&m->mega_part, megastep_work_floats(d) * sizeof(float)))) return bail(e, "cudaMalloc");
-      if ((e = cudaMalloc(&m->mega_bar, 2 * sizeof(unsigned long long)))) return bail(e, "cudaMalloc");
-      if ((e = cudaMemset(m->mega_bar, 0, 2 * sizeof(unsigned long long)))) return bail(e, "cudaMemset");
+      // [0] grid-barrier counter, [1] its step base, [2, 18) attention arrival counters per KV
+      // head, [18, 34) their step bases
+      const size_t nbar = 2 + 2 * 16;
+      if ((e = cudaMalloc(&m->mega_bar, nbar * sizeof(unsigned long long)))) return bail(e, "cudaMalloc");
+      if ((e = cudaMemset(m->mega_bar, 0, nbar * sizeof(unsigned long long)))) return bail(e, "cudaMemset");
       if ((e = cudaMalloc(&m->mega_abort, sizeof(int)))) return bail(e, "cudaMalloc");
       if ((e = cudaMemset(m->mega_abort, 0, sizeof(int)))) return bail(e, "cudaMemset");
       m->use_mega = true;

@@ -19,6 +19,7 @@
 // error of the bf16 path inside its tolerance); the LM head uses the bf16 embedding with
 // bf16 activations (a one-layer error, far inside the tolerance).
 #include "common.cuh"
+#include <cooperative_groups.h>
 #include "internal.h"
 
 #include <math.h>
@@ -47,28 +48,34 @@ __device__ __forceinline__ float psum(const float* part, int splits, int n_total
 __device__ __forceinline__ void store_row(f16* o, float v, int* err) { *o = to_half_checked(v, err); }
 __device__ __forceinline__ void store_row(bf16* o, float v, int*) { *o = __float2bfloat16_rn(v); }
 
-constexpr int RN_THREADS = 512;
-constexpr int RN_COLS = 4;  // columns per thread: H <= RN_THREADS * RN_COLS
+constexpr int RN_CL = 8;         // CTAs per sequence (one thread-block cluster)
+constexpr int RN_THREADS = 256;
+constexpr int RN_COLS = 4;       // columns per thread: H <= RN_CL * RN_THREADS * RN_COLS
 
 // Row b of out = RMSNorm(x[b]) * gain after x[b] += the split partials (part may be null:
-// no residual add; embed non-null: x[b] = embedding row of tok[b] first). One CTA per
-// sequence; every load of the row is issued before the first use. Rows of absent or
-// inactive sequences are zero.
+// no residual add; embed non-null: x[b] = embedding row of tok[b] first). A cluster of RN_CL
+// CTAs per sequence, each owning a contiguous share of the columns: every load of a share is
+// issued before the first use, and the CTAs' sums of squares meet through distributed shared
+// memory, added in rank order (deterministic). Rows of absent or inactive sequences are zero.
 template <typename OutT>
-__global__ void __launch_bounds__(RN_THREADS) bresid_norm_kernel(const float* part, int splits, int n_total,
-                                                                 const bf16* embed, int V, const int* tok,
-                                                                 float* x, const bf16* gain, int H, float eps,
-                                                                 const int* active, int nseq, OutT* out, int* err,
-                                                                 unsigned long long* tl) {
+__global__ void __cluster_dims__(RN_CL, 1, 1) __launch_bounds__(RN_THREADS)
+bresid_norm_kernel(const float* part, int splits, int n_total, const bf16* embed, int V, const int* tok, float* x,
+                   const bf16* gain, int H, float eps, const int* active, int nseq, OutT* out, int* err,
+                   unsigned long long* tl) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
   __shared__ float scratch[32];
+  __shared__ float s_ss;
   tl_stamp(tl, 0);
   pdl_wait();
   pdl_trigger();
   tl_stamp(tl, 1);
-  const int b = blockIdx.x;
+  const int rank = (int)cl.block_rank(), b = blockIdx.y;
+  const int per = (H + RN_CL - 1) / RN_CL;
+  const int c0 = rank * per, c1 = min(H, c0 + per);
   OutT* o = out + (size_t)b * H;
-  if (b >= nseq || !active[b]) {
-    for (int k = threadIdx.x; k < H; k += RN_THREADS) o[k] = from_f32<OutT>(0.f);
+  if (b >= nseq || !active[b]) {  // the whole cluster takes this branch
+    for (int k = c0 + threadIdx.x; k < c1; k += RN_THREADS) o[k] = from_f32<OutT>(0.f);
     tl_stamp(tl, 2);
     return;
   }
@@ -77,7 +84,7 @@ __global__ void __launch_bounds__(RN_THREADS) bresid_norm_kernel(const float* pa
   if (embed) {
     int t = __ldcg(tok + b);
     if (t < 0 || t >= V) {
-      if (threadIdx.x == 0) atomicOr(err, ERR_TOKEN);
+      if (threadIdx.x == 0 && rank == 0) atomicOr(err, ERR_TOKEN);
       t = 0;
     }
     erow = embed + (size_t)t * H;
@@ -85,10 +92,10 @@ __global__ void __launch_bounds__(RN_THREADS) bresid_norm_kernel(const float* pa
   float v[RN_COLS], g[RN_COLS];
 #pragma unroll
   for (int j = 0; j < RN_COLS; ++j) {
-    const int k = threadIdx.x + j * RN_THREADS;
+    const int k = c0 + threadIdx.x + j * RN_THREADS;
     v[j] = 0.f;
     g[j] = 0.f;
-    if (k < H) {
+    if (k < c1) {
       v[j] = erow ? __bfloat162float(erow[k]) : __ldcg(xb + k);
       g[j] = __bfloat162float(gain[k]);
       if (part) v[j] += psum(part, splits, n_total, b, k);
@@ -97,18 +104,24 @@ __global__ void __launch_bounds__(RN_THREADS) bresid_norm_kernel(const float* pa
   float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < RN_COLS; ++j) {
-    const int k = threadIdx.x + j * RN_THREADS;
-    if (k < H) {
+    const int k = c0 + threadIdx.x + j * RN_THREADS;
+    if (k < c1) {
       if (part || erow) xb[k] = v[j];
       ss = fmaf(v[j], v[j], ss);
     }
   }
   ss = block_sum(ss, scratch);
-  const float inv = rsqrtf(ss / (float)H + eps);
+  if (threadIdx.x == 0) s_ss = ss;
+  cl.sync();  // every CTA's share of the sum is in its shared memory
+  float tot = 0.f;
+#pragma unroll
+  for (int r = 0; r < RN_CL; ++r) tot += *cl.map_shared_rank(&s_ss, r);
+  cl.sync();  // the peers have read this CTA's share: it may exit
+  const float inv = rsqrtf(tot / (float)H + eps);
 #pragma unroll
   for (int j = 0; j < RN_COLS; ++j) {
-    const int k = threadIdx.x + j * RN_THREADS;
-    if (k < H) store_row(o + k, v[j] * inv * g[j], err);
+    const int k = c0 + threadIdx.x + j * RN_THREADS;
+    if (k < c1) store_row(o + k, v[j] * inv * g[j], err);
   }
   tl_stamp(tl, 2);
 }
@@ -265,9 +278,9 @@ cudaError_t batched_step(const BatchedCtx& c, cudaStream_t s) {
   const bool pdl = batched_pdl();
   const Dims& d = c.d;
   const int S = d.max_seqs, H = d.H, I = d.I;
-  if (H > RN_THREADS * RN_COLS) return cudaErrorInvalidValue;
+  if (H > RN_CL * RN_THREADS * RN_COLS) return cudaErrorInvalidValue;
   cudaError_t e;
-  const dim3 rn_grid(16), rn_block(RN_THREADS);
+  const dim3 rn_grid(RN_CL, 16), rn_block(RN_THREADS);
   const float* no_part = nullptr;
   const bf16* no_embed = nullptr;
   const int* no_tok = nullptr;

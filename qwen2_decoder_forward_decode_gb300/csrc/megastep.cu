@@ -49,7 +49,9 @@ constexpr int NS = 8;                      // ring slots (a multiple of NPW)
 constexpr int SLOT = 24 * 1024;            // bytes per slot
 constexpr int MAXV = 8;                    // 16-byte vectors per lane of the register tile, at most
 constexpr int MAX_LOCAL = 128;             // items of one phase per CTA
-constexpr int NSPLIT = 16;                 // most attention chunks per KV head
+constexpr int NSPLIT = 16;                 // most chunks per KV head merged by every o_proj CTA
+constexpr int NSPLIT_MAX = 64;             // most attention chunks per KV head
+constexpr int MAX_KV_GROUPS = 16;          // KV heads with an attention arrival counter
 constexpr int CHUNK_MIN = 32;              // fewest positions per chunk
 constexpr int AT_K = 32;                   // positions per attention tile
 constexpr int GMAX = 8;                    // most query heads per KV head
@@ -91,7 +93,11 @@ struct Params {
   const bf16 *embed, *final_norm, *head;
   const float2* rope;        // [cap][hd/2] (cos, sin)
   f16* kv;                   // this sequence's cache [L][2][nkv][cap][hd]
-  float *x, *q, *act, *logits, *part;  // x [H], act [I], part [nq][NSPLIT][hd + 4]
+  float *x, *q, *act, *logits, *part;  // x [H], act [I], part [nq][nsplit][hd + 4]
+  float* att_o;              // [nq * hd] attention output merged by the attention CTAs (ns > NSPLIT)
+  int nsplit;                // most chunks per KV head (<= NSPLIT_MAX, nkv * nsplit <= CTAs)
+  unsigned long long* att_cnt;   // [nkv] monotonic arrival counters of the attention CTAs
+  unsigned long long* att_base;  // [nkv] their values when a step starts (updated by CTA 0)
   int *tok, *pos;
   unsigned long long* key;   // packed argmax key (zero between steps)
   int *hist, *hist_n;
@@ -248,9 +254,11 @@ __device__ __forceinline__ bool phase_units(const Params& p, const LayerW* lt, i
   }
 }
 
-// attention chunking for a context of ctx positions
-__device__ __forceinline__ void att_chunks(int ctx, int& chunk, int& ns) {
-  chunk = max(CHUNK_MIN, (ctx + NSPLIT - 1) / NSPLIT);
+// attention chunking for a context of ctx positions: at most nsplit chunks per KV head of at
+// least CHUNK_MIN positions. Up to NSPLIT chunks the o_proj CTAs merge them while staging
+// their input; beyond, the attention CTAs of a KV head merge them (below).
+__device__ __forceinline__ void att_chunks(int ctx, int nsplit, int& chunk, int& ns) {
+  chunk = max(CHUNK_MIN, (ctx + nsplit - 1) / nsplit);
   ns = (ctx + chunk - 1) / chunk;
 }
 
@@ -284,7 +292,7 @@ __device__ void producer(const Params& p, const LayerW* lt, unsigned char* smem,
   bool ok = true;
   const uint32_t ring = smem_addr(smem);
   int chunk, ns;
-  att_chunks(ctx, chunk, ns);
+  att_chunks(ctx, p.nsplit, chunk, ns);
   auto issue = [&](const Unit& un) -> bool {
     const long long my = u++;
     if ((int)(my % NPW) != pw) return true;
@@ -669,7 +677,7 @@ __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int 
       const float mw = cM[w * 16 + r];
       if (mw != -INFINITY) acc = fmaf(expf(mw - M), cO[(size_t)(w * 16 + r) * HD + d], acc);
     }
-    p.part[((size_t)(g * G + r) * NSPLIT + c) * ps + d] = acc;
+    p.part[((size_t)(g * G + r) * p.nsplit + c) * ps + d] = acc;
   }
   if (t < G) {
     const float M = fmaxf(cM[t], cM[16 + t]);
@@ -679,7 +687,7 @@ __device__ void attention_chunk(const Params& p, unsigned char* att, int l, int 
       const float mw = cM[w * 16 + t];
       if (mw != -INFINITY) L = fmaf(expf(mw - M), cL[w * 16 + t], L);
     }
-    float* pp = p.part + ((size_t)(g * G + t) * NSPLIT + c) * ps;
+    float* pp = p.part + ((size_t)(g * G + t) * p.nsplit + c) * ps;
     pp[HD] = M;
     pp[HD + 1] = L;
   }
@@ -710,7 +718,7 @@ __device__ void stage_merge(const Params& p, float* xs, int ns) {
     for (int e = 0; e < 2; ++e) {
       const int gi = t + e * NCT;
       const int h = (4 * gi) / HD, d = 4 * gi - h * HD;
-      const float* base = p.part + (size_t)h * NSPLIT * ps;
+      const float* base = p.part + (size_t)h * p.nsplit * ps;
 #pragma unroll
       for (int u = 0; u < MB; ++u) {
         const bool in = gi < groups && c0 + u < ns;
@@ -750,6 +758,88 @@ __device__ void stage_merge(const Params& p, float* xs, int ns) {
       reinterpret_cast<float4*>(xs)[gi] = make_float4(acc[e].x * inv, acc[e].y * inv, acc[e].z * inv, acc[e].w * inv);
     }
   }
+  cbar();
+}
+
+// Attention output of KV head g merged by the group's own ns attention CTAs (ns > NSPLIT, long
+// contexts): each CTA publishes its chunk partials (release on the group's monotonic counter),
+// waits (bounded) until the group's ns chunks of layer l are in, then merges a contiguous share
+// of the group's G * HD outputs into att_o: o = sum_c w_c O_c / sum_c w_c l_c with
+// w_c = exp(m_c - M), M = max_c m_c, in chunk order (deterministic). gbase: the counter's value
+// when the step started. False if a wait gave up.
+template <int HD>
+__device__ bool group_merge(const Params& p, int l, int g, int c, int ns, unsigned long long gbase, int* s_flag) {
+  const int t = threadIdx.x, G = p.nq / p.nkv, ps = attn_part_stride(HD);
+  cbar();  // this CTA's partials are written
+  if (t == 0) {
+    int res = 0;
+    if (!aborted(p)) {
+      asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p.att_cnt + g), "l"(1ull) : "memory");
+      const unsigned long long target = gbase + (unsigned long long)(l + 1) * ns;
+      const long long t0 = clock64();
+      res = 1;
+      for (int it = 0;; ++it) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p.att_cnt + g) : "memory");
+        if (v >= target) break;
+        if ((it & 15) == 15) {
+          if (aborted(p)) { res = 0; break; }
+          if (clock64() - t0 > WAIT_CYCLES) { raise_abort(p); res = 0; break; }
+        }
+      }
+    }
+    *s_flag = res;
+  }
+  cbar();
+  if (!*(volatile int*)s_flag) return false;
+  // warp w merges outputs o0 + w + 8k, lane j reads chunks j and j + 32 (ns <= 64): every
+  // load of the share first, then warp reductions in a fixed order
+  constexpr int KM = 8;  // outputs per warp: G * HD / ns <= 8 * HD / 17 < 8 * NCW
+  const int n_out = G * HD, per = (n_out + ns - 1) / ns;
+  const int o0 = c * per, o1 = min(n_out, o0 + per);
+  const int warp = t >> 5, lane = t & 31;
+  float2 ml[KM][2];
+  float ov[KM][2];
+#pragma unroll
+  for (int k = 0; k < KM; ++k) {
+    const int i = o0 + warp + NCW * k;
+    const int h = g * G + i / HD, d = i - (i / HD) * HD;
+    const float* base = p.part + (size_t)h * p.nsplit * ps;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int cc = lane + 32 * j;
+      const bool in = i < o1 && cc < ns;
+      ml[k][j] = in ? __ldcg(reinterpret_cast<const float2*>(base + (size_t)cc * ps + HD)) : make_float2(-INFINITY, 0.f);
+      ov[k][j] = in ? __ldcg(base + (size_t)cc * ps + d) : 0.f;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < KM; ++k) {
+    const int i = o0 + warp + NCW * k;
+    float M = fmaxf(ml[k][0].x, ml[k][1].x);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float w = ml[k][j].x == -INFINITY ? 0.f : expf(ml[k][j].x - M);
+      L = fmaf(ml[k][j].y, w, L);
+      acc = fmaf(ov[k][j], w, acc);
+    }
+    L = warp_sum(L);
+    acc = warp_sum(acc);
+    if (lane == 0 && i < o1) {
+      const int h = g * G + i / HD, d = i - (i / HD) * HD;
+      p.att_o[(size_t)h * HD + d] = acc / L;
+    }
+  }
+  return true;
+}
+
+// xs = src[0 .. n) (the merged attention output), one barrier
+__device__ void stage_vec(float* xs, const float* src, int n) {
+  for (int i = threadIdx.x; i < (n >> 2); i += NCT)
+    reinterpret_cast<float4*>(xs)[i] = __ldcg(reinterpret_cast<const float4*>(src) + i);
   cbar();
 }
 
@@ -848,7 +938,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
   const int nvecH = p.H >> 3;
   const size_t rowH = (size_t)p.H * 2;
   int chunk, ns;
-  att_chunks(ctx, chunk, ns);
+  att_chunks(ctx, p.nsplit, chunk, ns);
   float xr[NV][8];
   bool alive = true;
   int ph_idx = 0;  // timeline index
@@ -931,20 +1021,25 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
     // ===== ATTN: (KV head, chunk) partials
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
+    bool att_ok = true;
     if ((int)blockIdx.x < p.nkv * ns) {
       const int g = blockIdx.x / ns, c = blockIdx.x - g * ns;
       attention_chunk<HD>(p, att, l, g, c, chunk, ctx);
+      if (ns > NSPLIT) att_ok = group_merge<HD>(p, l, g, c, ns, __ldcg(p.att_base + g), s_flag);
     }
     tl_mark3(p, ph_idx, 2);
     tl_mark(p, ph_idx++, 2);
-    alive = grid_sync(p, base, nb, s_flag, ph_idx - 1, true);
+    alive = grid_sync(p, base, nb, s_flag, ph_idx - 1, att_ok);
     if (!alive) break;
 
     // ===== OPROJ: merge -> x += Wo o (each row's warp updates the CTA's residual row)
     tl_mark(p, ph_idx, 0);
     phase_u = 0;
     ck(p, ph_idx, 0);
-    stage_merge<HD>(p, xs, ns);
+    if (ns > NSPLIT)
+      stage_vec(xs, p.att_o, p.nq * HD);
+    else
+      stage_merge<HD>(p, xs, ns);
     load_xr(xr, xs, (p.nq * HD) >> 3, lane);
     tl_mark2(p, ph_idx);
     ck(p, ph_idx, 3);
@@ -1104,6 +1199,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const Params p)
       *p.pos = pos + 1;
       *p.key = 0ull;
       *p.bar_base = base + (unsigned long long)nb * gridDim.x;  // every CTA has arrived nb times
+      if (ns > NSPLIT)  // every attention CTA of each KV head has arrived once per layer
+        for (int g = 0; g < p.nkv; ++g) p.att_base[g] += (unsigned long long)p.L * ns;
     }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // (copies are only left after an abort)
@@ -1136,6 +1233,7 @@ bool megastep_supported(const Dims& d, int nsm) {
   auto per_cta = [&](int n) { return (n + nsm - 1) / nsm; };
   if (per_cta(pairs) > mk::MAX_LOCAL || per_cta(d.I) > mk::MAX_LOCAL || per_cta(d.H) > 64) return false;
   if (d.nkv * mk::NSPLIT > nsm) return false;
+  if (d.nkv > mk::MAX_KV_GROUPS) return false;
   if (megastep_smem(d) > 227 * 1024) return false;
   return true;
 }
@@ -1151,8 +1249,11 @@ static const void* megastep_fn(const Dims& d) {
                  : nv == 6 ? (const void*)mk::decode_step_kernel<64, 6> : (const void*)mk::decode_step_kernel<64, 8>;
 }
 
-size_t megastep_work_floats(const Dims& d) {  // x, act and the attention partials
-  return (size_t)d.H + d.I + (size_t)d.nq * mk::NSPLIT * attn_part_stride(d.hd);
+// most attention chunks per KV head: every (KV head, chunk) pair has its own CTA
+int megastep_nsplit(const Dims& d, int nsm) { return std::min(mk::NSPLIT_MAX, nsm / d.nkv); }
+
+size_t megastep_work_floats(const Dims& d) {  // x, act, the attention partials, the merged output
+  return (size_t)d.H + d.I + (size_t)d.nq * megastep_nsplit(d, d.nsm) * attn_part_stride(d.hd) + (size_t)d.nq * d.hd;
 }
 
 
@@ -1185,6 +1286,10 @@ cudaError_t launch_megastep(const MegaLaunch& a, cudaStream_t s) {
   p.x = a.work;
   p.act = a.work + a.d.H;
   p.part = a.work + a.d.H + a.d.I;
+  p.nsplit = megastep_nsplit(a.d, a.d.nsm);
+  p.att_o = p.part + (size_t)a.d.nq * p.nsplit * attn_part_stride(a.d.hd);
+  p.att_cnt = a.bar + 2;
+  p.att_base = a.bar + 2 + mk::MAX_KV_GROUPS;
   p.q = a.q; p.logits = a.logits;
   p.tok = a.tok; p.pos = a.pos; p.key = a.key; p.hist = a.hist; p.hist_n = a.hist_n; p.hist_cap = a.hist_cap;
   p.bar = a.bar; p.bar_base = a.bar_base; p.abort = a.abort; p.err = a.err; p.tl = a.tl;
