@@ -547,6 +547,9 @@ cudaError_t gemm_tc_set_attributes() {
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>()))) return e;
   if ((e = cudaFuncSetAttribute(gemm_tc_kernel<192, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<192>()))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<64, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<64>()))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<64, EPI_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<64>()))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<128, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<128>()))) return e;
   if ((e = cudaFuncSetAttribute(gemm_tc_kernel<192, EPI_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<192>()))) return e;
   if ((e = cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>()))) return e;
   return cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>());
@@ -665,9 +668,12 @@ cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bi
   const int tiles_m = (M + tc::BM - 1) / tc::BM;
   const int nk = (K + tc::BK - 1) / tc::BK;
   // tile width: 256 or 192 columns, whichever finishes first when the tiles go round the
-  // SMs in whole rounds (time of a round ~ tile width)
+  // SMs in whole rounds (time of a round ~ tile width); 64 for short prompts (M <= 256),
+  // whose GEMMs stream weights: narrow tiles give the SMs work with fewer K splits
   int bn = TC_BN;
-  if (nsm > 0) {
+  if (nsm > 0 && tiles_m <= 2) {
+    bn = 64;
+  } else if (nsm > 0) {
     auto rounds = [&](int w) { const int u = tiles_m * ((N + w - 1) / w); return (u + nsm - 1) / nsm; };
     if ((long long)rounds(192) * 192 < (long long)rounds(TC_BN) * TC_BN) bn = 192;
   }
@@ -689,6 +695,7 @@ cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bi
   const TcGrid g{tiles_m, (N + bn - 1) / bn, splits};
   const bool add = accumulate && splits == 1;
   if (bn == 192) launch_gemm<192>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
+  else if (bn == 64) launch_gemm<64>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
   else launch_gemm<TC_BN>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
   if (splits > 1) {
     const size_t n = (size_t)M * N;
@@ -702,15 +709,19 @@ cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bi
 cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, int ldb, f16* Act,
                            int ldc, int M, int N, int K, int* err, cudaStream_t s, float* ws, size_t ws_floats,
                            int nsm) {
+  // 128 output columns per tile (128 gate + 128 up rows); 64 for short prompts, whose gate/up
+  // then fills the SMs without K splits
+  const int tiles_m = (M + tc::BM - 1) / tc::BM;
+  const int bn = nsm > 0 && tiles_m <= 2 ? 128 : TC_BN;
   CUtensorMap ma, mg, mu;
-  if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mg, Wg, N, K, ldb, TC_BN / 2) ||
-      !make_map(&mu, Wu, N, K, ldb, TC_BN / 2))
+  if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mg, Wg, N, K, ldb, bn / 2) ||
+      !make_map(&mu, Wu, N, K, ldb, bn / 2))
     return cudaErrorInvalidValue;
   TcEpi ep{nullptr, nullptr, Act, ldc};
-  const int tiles = ((N + TC_BN / 2 - 1) / (TC_BN / 2)) * ((M + tc::BM - 1) / tc::BM);
+  const int tiles = ((N + bn / 2 - 1) / (bn / 2)) * tiles_m;
   const int nk = (K + tc::BK - 1) / tc::BK;
   int splits = 1;  // as in gemm_tc: split K when the tiles leave SMs idle
-  if (ws && nsm > 0 && 2 * tiles < 2 * nsm && tiles < nsm) {
+  if (ws && nsm > 0 && 2 * tiles < 2 * nsm && tiles < nsm / 2) {
     splits = nsm / tiles;
     if (splits > 16) splits = 16;
     if (splits > nk / 2) splits = nk / 2;
@@ -718,11 +729,14 @@ cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, 
     if ((size_t)splits * per > ws_floats) splits = (int)(ws_floats / per);
     if (splits < 2) splits = 1;
   }
-  const TcGrid g{(M + tc::BM - 1) / tc::BM, (N + TC_BN / 2 - 1) / (TC_BN / 2), splits};
+  const TcGrid g{tiles_m, (N + bn / 2 - 1) / (bn / 2), splits};
   const int units = g.tiles_m * g.tiles_n * splits;
   const int grid = nsm > 0 && units > nsm ? nsm : units;  // persistent CTAs
-  gemm_tc_kernel<TC_BN, EPI_SWIGLU><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mg, mu, ep, M, N, K, err, g,
-                                                                                 ws);
+  if (bn == 128)
+    gemm_tc_kernel<128, EPI_SWIGLU><<<grid, tc::THREADS, tc_smem<128>(), s>>>(ma, mg, mu, ep, M, N, K, err, g, ws);
+  else
+    gemm_tc_kernel<TC_BN, EPI_SWIGLU><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mg, mu, ep, M, N, K, err, g,
+                                                                                   ws);
   if (splits > 1) {
     const size_t n = (size_t)M * N;
     splitk_swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, Act, ldc, err);

@@ -71,8 +71,46 @@ __global__ void norm_rows_h_kernel(const float* X, const bf16* gain, int T, int 
   }
 }
 
-static void norm_rows_h(const float* X, const bf16* gain, int T_, int H, float eps, f16* Y, int* err, cudaStream_t s) {
-  if (H % 128 == 0 && ((uintptr_t)gain & 7) == 0) {
+// Short prompts: one 128-thread block per row (float4 loads, 8-byte stores), so that every
+// SM has rows.
+__global__ void __launch_bounds__(128) norm_row_block_h_kernel(const float* X, const bf16* gain, int H, float eps,
+                                                               f16* Y, int* err) {
+  __shared__ float scratch[32];
+  const int row = blockIdx.x;
+  const float4* x = reinterpret_cast<const float4*>(X + (size_t)row * H);
+  const uint2* gp = reinterpret_cast<const uint2*>(gain);
+  uint2* y = reinterpret_cast<uint2*>(Y + (size_t)row * H);
+  constexpr int MAXV = 8;  // float4 per thread: H <= 4096
+  float4 v[MAXV];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    const int k = threadIdx.x + 128 * j;
+    v[j] = k < H / 4 ? x[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss = fmaf(v[j].x, v[j].x, fmaf(v[j].y, v[j].y, fmaf(v[j].z, v[j].z, fmaf(v[j].w, v[j].w, ss))));
+  }
+  ss = block_sum(ss, scratch);
+  const float inv = rsqrtf(ss / (float)H + eps);
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    const int k = threadIdx.x + 128 * j;
+    if (k < H / 4) {
+      const uint2 gb = gp[k];
+      const __half2 lo = to_half2_checked(v[j].x * inv * __uint_as_float(gb.x << 16),
+                                          v[j].y * inv * __uint_as_float(gb.x & 0xffff0000u), err);
+      const __half2 hi = to_half2_checked(v[j].z * inv * __uint_as_float(gb.y << 16),
+                                          v[j].w * inv * __uint_as_float(gb.y & 0xffff0000u), err);
+      y[k] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
+  }
+}
+
+static void norm_rows_h(const float* X, const bf16* gain, int T_, int H, float eps, f16* Y, int* err, cudaStream_t s,
+                        int nsm) {
+  const bool vec = H % 128 == 0 && ((uintptr_t)gain & 7) == 0;
+  if (vec && T_ < 4 * nsm && H <= 4096) {
+    norm_row_block_h_kernel<<<T_, 128, 0, s>>>(X, gain, H, eps, Y, err);
+  } else if (vec) {
     norm_rows_h_kernel<<<(T_ + 7) / 8, 256, 0, s>>>(X, gain, T_, H, eps, Y, err);
   } else {
     norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(X, gain, H, eps, Y, err);
@@ -622,7 +660,7 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
     const LayerPtrs& w = layers[l];
     f16* kc = (f16*)kcache + (size_t)l * 2 * layer_stride;
     f16* vc = kc + layer_stride;
-    norm_rows_h(b.X, (const bf16*)w.in_norm, T_, H, d.eps, b.Xh, err, s);
+    norm_rows_h(b.X, (const bf16*)w.in_norm, T_, H, d.eps, b.Xh, err, s, d.nsm);
     if (w.wk16 == (const f16*)w.wq16 + (size_t)qd * H && w.wv16 == (const f16*)w.wk16 + (size_t)kvd * H &&
         (w.bqkv || !w.bq)) {
       // q | k | v as one projection: the three matrices lie back to back, and so do the
@@ -655,7 +693,7 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
       }
     }
     if ((e = gemm_tc(b.Oh, qd, (const f16*)w.wo16, qd, nullptr, b.X, H, T_, H, qd, true, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-    norm_rows_h(b.X, (const bf16*)w.post_norm, T_, H, d.eps, b.Xh, err, s);
+    norm_rows_h(b.X, (const bf16*)w.post_norm, T_, H, d.eps, b.Xh, err, s, d.nsm);
     if ((e = gemm_tc_swiglu(b.Xh, H, (const f16*)w.wg16, (const f16*)w.wu16, H, b.Ah, d.I, T_, d.I, H, err, s, b.ws,
                               b.ws_floats, d.nsm)))
       return e;

@@ -31,6 +31,8 @@ def _f16(a):
     (1000, 2056, 320, False, True),   # several tiles per CTA with ragged M and N
     (4096, 1536, 256, True, False),   # 192-column tiles, several per CTA
     (2000, 1536, 512, False, True),   # 192-column tiles, residual add, ragged M
+    (128, 1536, 8960, False, True),   # short prompt: 64-column tiles, the down projection's K
+    (77, 2048, 1536, True, False),    # short ragged prompt, fused q/k/v width
 ])
 def test_gemm_f16(M, N, K, bias, acc):
     from qwen2_decoder_forward_decode_gb300 import binding
