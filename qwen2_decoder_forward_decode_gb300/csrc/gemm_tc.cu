@@ -11,6 +11,8 @@
 //                      w + 4 split the columns), fused bias / residual-add / SwiGLU,
 //                      coalesced stores to global memory, while the next tile accumulates
 //                      in the other buffer
+// With two or more row tiles, CTA pairs (clusters of two) run the same roles on 256 x BN
+// tiles with the pair form of the MMA (cta_group::2), each CTA staging half of B.
 // Every mbarrier wait is bounded (clock budget); on expiry the CTA flags ERR_TIMEOUT,
 // stops issuing work, and still releases its TMEM.
 #include <cuda.h>
@@ -51,19 +53,42 @@ struct TcEpi {
 // Split-K (splits > 1, EPI_STORE / EPI_ADD / EPI_SWIGLU): unit z of a tile covers a
 // contiguous range of K blocks and stores its raw fp32 tile to ws[z]; the reduce kernels then
 // add the splits in order and apply the bias, the residual add or SwiGLU (deterministic).
+// CL = 2: a cluster of two CTAs (one per SM) computes a 256 x BN tile with the pair form of
+// the MMA (tcgen05 cta_group::2, M = 256): each CTA stages its 128 rows of A and its half of
+// the BN rows of B, so an SM takes in a third fewer operand bytes per FLOP, and the stage
+// ring gets deeper. The even CTA's MMA thread issues for both; its full barriers count the
+// bytes landing in both CTAs, its commits free both CTAs' stages and hand each CTA's
+// epilogue its 128 accumulator rows, and both CTAs' epilogue warps release its
+// accumulators.
 struct TcGrid {
   int tiles_m, tiles_n, splits;
 };
 
-template <int BN, int EPI>
+template <int BN, int CL>
+__host__ __device__ constexpr int tc_stages() {
+  return CL == 2 ? 6 : tc::STAGES;
+}
+template <int BN, int CL>
+__host__ __device__ constexpr size_t tc_stage_bytes() {
+  return (size_t)tc::BM * tc::BK * 2 + (size_t)(CL == 2 ? BN / 2 : BN) * tc::BK * 2;
+}
+// ring, barriers (256 B), epilogue scratch (8 warps x 32 x 33 floats), 1024-B alignment slack
+template <int BN, int CL>
+__host__ __device__ constexpr size_t tc_smem() {
+  return tc_stages<BN, CL>() * tc_stage_bytes<BN, CL>() + 256 + 8 * 32 * 33 * 4 + 1024;
+}
+
+template <int BN, int EPI, int CL>
 __global__ void __launch_bounds__(tc::THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB2, TcEpi ep, int M, int N, int K, int* err, TcGrid g,
                float* ws) {
   using namespace tc;
   constexpr int A_BYTES = BM * BK * 2;
-  constexpr int B_BYTES = BN * BK * 2;
+  constexpr int B_BYTES = (CL == 2 ? BN / 2 : BN) * BK * 2;  // this CTA's rows of B
   constexpr int STAGE = A_BYTES + B_BYTES;
+  constexpr int STAGES = tc_stages<BN, CL>();
+  static_assert(tc_smem<BN, CL>() <= 232448, "shared memory");
   constexpr int NOUT = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -72,14 +97,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t acc_full0 = smem_u32(bars + 2 * STAGES), acc_empty0 = acc_full0 + 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles = g.tiles_m * g.tiles_n, units = tiles * g.splits;
+  // CL = 2: a unit is a pair of row tiles, the cluster's CTAs take one each (rank)
+  const int rank = CL == 2 ? (int)tc::cluster_ctarank() : 0;
+  const int tiles_mu = (g.tiles_m + CL - 1) / CL;  // row units
+  const int tiles = tiles_mu * g.tiles_n, units = tiles * g.splits;
+  const int first = (int)blockIdx.x / CL, step = (int)gridDim.x / CL;
   const int nk_all = (K + BK - 1) / BK;
   // unit -> first row, first output column, split index, K block range
   auto unit_of = [&](int u, int& m0, int& n0, int& z, int& kb_lo, int& kb_hi) {
     z = u / tiles;
     const int t = u - z * tiles;
-    m0 = (t % g.tiles_m) * BM;
-    n0 = (t / g.tiles_m) * NOUT;
+    m0 = ((t % tiles_mu) * CL + rank) * BM;
+    n0 = (t / tiles_mu) * NOUT;
     kb_lo = (int)((long long)z * nk_all / g.splits);
     kb_hi = (int)((long long)(z + 1) * nk_all / g.splits);
   };
@@ -93,14 +122,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(acc_full0 + 8 * b, 1);
-      tc::mbar_init(acc_empty0 + 8 * b, 8);  // one arrival per epilogue warp
+      tc::mbar_init(acc_empty0 + 8 * b, 8 * CL);  // one arrival per epilogue warp of the pair
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   constexpr uint32_t TCOLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators, a power of two
-  if (warp == 0) tc::tmem_alloc(smem_u32(tmem_slot), TCOLS);
+  if (warp == 0) {
+    if (CL == 2) tc::tmem_alloc_pair(smem_u32(tmem_slot), TCOLS);
+    else tc::tmem_alloc(smem_u32(tmem_slot), TCOLS);
+  }
   tc::tc_fence_before();
   __syncthreads();
+  if (CL == 2) tc::cluster_sync();  // the pair's barriers exist before either CTA signals one
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -109,7 +142,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
     int it = 0;  // K blocks issued
-    for (int u = blockIdx.x; u < units && !s_abort; u += gridDim.x) {
+    for (int u = first; u < units && !s_abort; u += step) {
       int m0, n0, z, kb_lo, kb_hi;
       unit_of(u, m0, n0, z, kb_lo, kb_hi);
       for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
@@ -118,6 +151,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (s_abort) break;
         const uint32_t a_dst = smem_u32(smem + s * STAGE);
         const uint32_t b_dst = a_dst + A_BYTES;
+        if (CL == 2) {  // bytes counted on the even CTA's barrier (SwiGLU: rank 0 gate, rank 1 up)
+          const uint32_t bar = tc::mapa_shared(full0 + 8 * s, 0);
+          if (rank == 0) tc::mbar_expect_tx(full0 + 8 * s, 2 * STAGE);
+          tc::tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, m0);
+          if (EPI == EPI_SWIGLU)
+            tc::tma_load_2d_pair(b_dst, rank ? &tmB2 : &tmB, bar, kb * BK, n0);
+          else
+            tc::tma_load_2d_pair(b_dst, &tmB, bar, kb * BK, n0 + rank * (BN / 2));
+          continue;
+        }
         tc::mbar_expect_tx(full0 + 8 * s, STAGE);
         tc::tma_load_2d(a_dst, &tmA, full0 + 8 * s, kb * BK, m0);
         if (EPI == EPI_SWIGLU) {
@@ -128,15 +171,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
     }
-    // drain: every issued stage must land before the CTA may exit
-    for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-      tc::mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1, err);
-  } else if (warp == 1 && lane == 0) {
+    // drain: every issued stage must land before the CTA may exit (the odd CTA's bytes are
+    // counted on the even CTA's barriers, which drains them before the closing cluster barrier)
+    if (rank == 0)
+      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+        tc::mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1, err);
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---- MMA issuer: one N = BN product per 16 K (gate and up together for SwiGLU)
-    constexpr uint32_t idesc = tc::idesc_f16(BM, BN);
+    constexpr uint32_t idesc = tc::idesc_f16(CL * BM, BN);
     int it = 0, i = 0;  // K blocks consumed, units done
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
+    for (int u = first; u < units && ok; u += step, ++i) {
       int m0, n0, z, kb_lo, kb_hi;
       unit_of(u, m0, n0, z, kb_lo, kb_hi);
       const int b = i & 1;
@@ -150,20 +195,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const uint32_t a_base = smem_u32(smem + s * STAGE);
         const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          tc::mma_f16(tmem + b * BN, tc::smem_desc_sw128(a_base + 32 * k), tc::smem_desc_sw128(b_base + 32 * k),
-                      idesc, (kb > kb_lo) || k);
-        tc::mma_commit(empty0 + 8 * s);
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t da = tc::smem_desc_sw128(a_base + 32 * k), db = tc::smem_desc_sw128(b_base + 32 * k);
+          if (CL == 2) tc::mma_f16_pair(tmem + b * BN, da, db, idesc, (kb > kb_lo) || k);
+          else tc::mma_f16(tmem + b * BN, da, db, idesc, (kb > kb_lo) || k);
+        }
+        if (CL == 2) tc::mma_commit_pair(empty0 + 8 * s, 3);  // the stage is free in both CTAs
+        else tc::mma_commit(empty0 + 8 * s);
       }
       if (!ok) break;
-      tc::mma_commit(acc_full0 + 8 * b);
+      if (CL == 2) tc::mma_commit_pair(acc_full0 + 8 * b, 3);
+      else tc::mma_commit(acc_full0 + 8 * b);
     }
     if (!ok) s_abort = 1;
   } else if (warp >= 2) {
     // ---- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, columns of half (w-2)/4
     const int q = warp & 3, eh = (warp - 2) >> 2;
     int i = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+    for (int u = first; u < units; u += step, ++i) {
       int m0, n0, z, kb_lo, kb_hi;
       unit_of(u, m0, n0, z, kb_lo, kb_hi);
       const int b = i & 1;
@@ -233,14 +282,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // the accumulator is free for unit i + 2
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty0 + 8 * b);
+      if (lane == 0) {
+        if (CL == 2) tc::mbar_arrive_cluster(tc::mapa_shared(acc_empty0 + 8 * b, 0));
+        else mbar_arrive(acc_empty0 + 8 * b);
+      }
     }
   }
   tc::tc_fence_before();
   __syncthreads();
+  if (CL == 2) tc::cluster_sync();  // the pair's MMAs and loads are all done
   if (warp == 0) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, TCOLS);
+    if (CL == 2) tc::tmem_dealloc_pair(tmem, TCOLS);
+    else tc::tmem_dealloc(tmem, TCOLS);
   }
 }
 
@@ -535,25 +589,67 @@ bool make_map_kv(void* mv, const void* base, int hd, int keys, int nkv, int cap,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
-static constexpr size_t tc_smem() {
-  // ring, barriers, the epilogue warps' 32 x 33 scratch blocks, alignment slack
-  return (size_t)tc::STAGES * (tc::BM * tc::BK * 2 + BN * tc::BK * 2) + 256 + 8 * 32 * 33 * 4 + 1024;
-}
 
 constexpr int TC_BN = 256;
 
+template <int BN, int EPI, int CL>
+static cudaError_t set_tc_attr() {
+  return cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)tc_smem<BN, CL>());
+}
+
 cudaError_t gemm_tc_set_attributes() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>()))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<192, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<192>()))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<64, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<64>()))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<64, EPI_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<64>()))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<128, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<128>()))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<192, EPI_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<192>()))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>()))) return e;
-  return cudaFuncSetAttribute(gemm_tc_kernel<TC_BN, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<TC_BN>());
+  if ((e = set_tc_attr<TC_BN, EPI_STORE, 1>()) || (e = set_tc_attr<TC_BN, EPI_STORE, 2>())) return e;
+  if ((e = set_tc_attr<TC_BN, EPI_ADD, 1>()) || (e = set_tc_attr<TC_BN, EPI_ADD, 2>())) return e;
+  if ((e = set_tc_attr<TC_BN, EPI_SWIGLU, 1>()) || (e = set_tc_attr<TC_BN, EPI_SWIGLU, 2>())) return e;
+  if ((e = set_tc_attr<192, EPI_STORE, 1>()) || (e = set_tc_attr<192, EPI_STORE, 2>())) return e;
+  if ((e = set_tc_attr<192, EPI_ADD, 1>()) || (e = set_tc_attr<192, EPI_ADD, 2>())) return e;
+  if ((e = set_tc_attr<64, EPI_STORE, 1>()) || (e = set_tc_attr<64, EPI_ADD, 1>())) return e;
+  return set_tc_attr<128, EPI_SWIGLU, 1>();
 }
+
+// One launch of the persistent GEMM: clusters of CL CTAs, as many as fit one per SM (at most
+// one per unit)
+template <int BN, int EPI, int CL>
+static cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb2, const TcEpi& ep,
+                             int M, int N, int K, int* err, const TcGrid& g, float* ws, int nsm, cudaStream_t s) {
+  const int units = ((g.tiles_m + CL - 1) / CL) * g.tiles_n * g.splits;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(tc::THREADS);
+  cfg.dynamicSmemBytes = tc_smem<BN, CL>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CL > 1 ? 1 : 0;
+  // the pairs that can be resident at once (an SM left over in a GPC takes none)
+  static int resident = -1;
+  if (resident < 0) {
+    int n = 0;
+    cfg.gridDim = dim3(CL);
+    if (CL == 1 || cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI, CL>, &cfg) != cudaSuccess || n <= 0)
+      n = nsm / CL;
+    resident = n;
+  }
+  int clusters = nsm > 0 ? std::min(resident, nsm / CL) : units;
+  if (clusters > units || clusters <= 0) clusters = units;
+  cfg.gridDim = dim3(clusters * CL);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, CL>, ma, mb, mb2, ep, M, N, K, err, g, ws);
+}
+
+// QW_GEMM_CLUSTER=0: no CTA pairs (for comparison)
+static bool gemm_pairs() {
+  static const bool v = [] {
+    const char* e = std::getenv("QW_GEMM_CLUSTER");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
+
 
 bool gemm_tc_available() { return encode_fn() != nullptr; }
 
@@ -651,15 +747,11 @@ cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, i
 }
 
 // C[M][N] (fp32, ldc) = / += A[M][K] (fp16, lda) . B[N][K]^T (fp16, ldb) (+ bias[N], bf16)
-template <int BN>
-static void launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const TcEpi& ep, int M, int N, int K,
-                        bool add, int* err, const TcGrid& g, float* ws, int nsm, cudaStream_t s) {
-  const int units = g.tiles_m * g.tiles_n * g.splits;
-  const int grid = nsm > 0 && units > nsm ? nsm : units;  // persistent CTAs
-  if (add)
-    gemm_tc_kernel<BN, EPI_ADD><<<grid, tc::THREADS, tc_smem<BN>(), s>>>(ma, mb, mb, ep, M, N, K, err, g, ws);
-  else
-    gemm_tc_kernel<BN, EPI_STORE><<<grid, tc::THREADS, tc_smem<BN>(), s>>>(ma, mb, mb, ep, M, N, K, err, g, ws);
+template <int BN, int CL>
+static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const TcEpi& ep, int M, int N, int K,
+                               bool add, int* err, const TcGrid& g, float* ws, int nsm, cudaStream_t s) {
+  if (add) return launch_tc<BN, EPI_ADD, CL>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
+  return launch_tc<BN, EPI_STORE, CL>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
 }
 
 cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bias, float* C, int ldc,
@@ -689,14 +781,21 @@ cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bi
     if ((size_t)splits * per > ws_floats) splits = (int)(ws_floats / per);
     if (splits < 2) splits = 1;
   }
+  // CTA pairs (M = 256 products, each CTA staging half of B) when there are row tiles to pair
+  const bool pair = bn != 64 && tiles_m >= 2 && nsm >= 2 && gemm_pairs();
   CUtensorMap ma, mb;
-  if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mb, B, N, K, ldb, bn)) return cudaErrorInvalidValue;
+  if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mb, B, N, K, ldb, pair ? bn / 2 : bn))
+    return cudaErrorInvalidValue;
   TcEpi ep{C, bias, nullptr, ldc};
   const TcGrid g{tiles_m, (N + bn - 1) / bn, splits};
   const bool add = accumulate && splits == 1;
-  if (bn == 192) launch_gemm<192>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
-  else if (bn == 64) launch_gemm<64>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
-  else launch_gemm<TC_BN>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
+  cudaError_t e;
+  if (bn == 192) e = pair ? launch_gemm<192, 2>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s)
+                          : launch_gemm<192, 1>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
+  else if (bn == 64) e = launch_gemm<64, 1>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
+  else e = pair ? launch_gemm<TC_BN, 2>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s)
+                : launch_gemm<TC_BN, 1>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
+  if (e) return e;
   if (splits > 1) {
     const size_t n = (size_t)M * N;
     splitk_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, bias, C, ldc,
@@ -730,13 +829,14 @@ cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, 
     if (splits < 2) splits = 1;
   }
   const TcGrid g{tiles_m, (N + bn / 2 - 1) / (bn / 2), splits};
-  const int units = g.tiles_m * g.tiles_n * splits;
-  const int grid = nsm > 0 && units > nsm ? nsm : units;  // persistent CTAs
+  cudaError_t e;
   if (bn == 128)
-    gemm_tc_kernel<128, EPI_SWIGLU><<<grid, tc::THREADS, tc_smem<128>(), s>>>(ma, mg, mu, ep, M, N, K, err, g, ws);
+    e = launch_tc<128, EPI_SWIGLU, 1>(ma, mg, mu, ep, M, N, K, err, g, ws, nsm, s);
+  else if (tiles_m >= 2 && nsm >= 2 && gemm_pairs())  // CTA pairs: rank 0 stages gate, rank 1 up
+    e = launch_tc<TC_BN, EPI_SWIGLU, 2>(ma, mg, mu, ep, M, N, K, err, g, ws, nsm, s);
   else
-    gemm_tc_kernel<TC_BN, EPI_SWIGLU><<<grid, tc::THREADS, tc_smem<TC_BN>(), s>>>(ma, mg, mu, ep, M, N, K, err, g,
-                                                                                   ws);
+    e = launch_tc<TC_BN, EPI_SWIGLU, 1>(ma, mg, mu, ep, M, N, K, err, g, ws, nsm, s);
+  if (e) return e;
   if (splits > 1) {
     const size_t n = (size_t)M * N;
     splitk_swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, Act, ldc, err);
