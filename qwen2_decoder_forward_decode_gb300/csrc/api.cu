@@ -580,14 +580,18 @@ qw_status qw_create(const qw_config* cfg, const qw_weights* w, void* cuda_stream
       char* q0 = p;
       for (int i = 0; i < 7; ++i) {
         *dst[i] = p;
-        if ((e = convert_bf16_to_half(src[i], p, sizes[i], m->err, 0))) return bail(e, "fp16 weight copy");
+        // q, k, v: each head's rows in RoPE-pair order (the projection's epilogue rotates
+        // adjacent columns)
+        e = i < 3 ? convert_bf16_to_half_pairs(src[i], p, sizes[i] / H, (int)H, d.hd, m->err, 0)
+                  : convert_bf16_to_half(src[i], p, sizes[i], m->err, 0);
+        if (e) return bail(e, "fp16 weight copy");
         p += i < 2 ? sizes[i] * 2 : i == 2 ? q0 + qkv_bytes - p : (sizes[i] * 2 + 255) & ~(size_t)255;
       }
       L.bqkv = nullptr;
       if (L.bq) {
-        if ((e = cudaMemcpy(p, L.bq, qd * 2, cudaMemcpyDeviceToDevice)) ||
-            (e = cudaMemcpy(p + qd * 2, L.bk, kvd * 2, cudaMemcpyDeviceToDevice)) ||
-            (e = cudaMemcpy(p + (qd + kvd) * 2, L.bv, kvd * 2, cudaMemcpyDeviceToDevice)))
+        if ((e = copy_bias_pairs(L.bq, p, (int)qd, d.hd, 0)) ||
+            (e = copy_bias_pairs(L.bk, p + qd * 2, (int)kvd, d.hd, 0)) ||
+            (e = copy_bias_pairs(L.bv, p + (qd + kvd) * 2, (int)kvd, d.hd, 0)))
           return bail(e, "q/k/v bias copy");
         L.bqkv = p;
       }

@@ -127,7 +127,8 @@ bresid_norm_kernel(const float* part, int splits, int n_total, const bf16* embed
 }
 
 
-// q/k/v of sequence b from the partials: + bias, split-half RoPE of q and k at pos[b], q to
+// q/k/v of sequence b from the partials (each head's columns in RoPE-pair order, as the fp16
+// weight copies' rows are): + bias, split-half RoPE of q and k at pos[b], q to
 // q_out[b], k and v appended to the sequence's cache at pos[b]. One thread per RoPE pair.
 __global__ void bqkv_epi_kernel(const float* part, int splits, int n_total, int nq, int nkv, int hd,
                                 const bf16* bq, const bf16* bk, const bf16* bv, const float2* rope,
@@ -146,7 +147,7 @@ __global__ void bqkv_epi_kernel(const float* part, int splits, int n_total, int 
   if (p < 0 || p >= cap) return;  // the host checks capacity before every step
   int head = item / half;
   const int i = item - head * half;
-  const int ca = head * hd + i, cb = ca + half;  // columns of the pair in q|k|v
+  const int ca = head * hd + 2 * i, cb = ca + 1;  // columns of the pair in q|k|v (pair-ordered weights)
   float a = psum(part, splits, n_total, b, ca), c = psum(part, splits, n_total, b, cb);
   const bf16* bias;
   int h;

@@ -33,13 +33,14 @@ constexpr int THREADS = 320;  // producer, MMA issuer, eight epilogue warps
 }  // namespace tc
 
 // Epilogues
-enum : int { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2 };
+enum : int { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
 
 struct TcEpi {
   float* C;          // EPI_STORE: C = acc (+ bias); EPI_ADD: C += acc   (fp32, ld = ldc)
-  const bf16* bias;  // [N] or null (EPI_STORE)
+  const bf16* bias;  // [N] or null (EPI_STORE, EPI_QKV)
   f16* Cb;           // EPI_SWIGLU: Cb[m][n] = silu(gate) * up as fp16, ld = ldc
   int ldc;
+  QkvOut qkv;        // EPI_QKV: + bias, RoPE of adjacent column pairs, fp16 q and K/V rows
 };
 
 // Persistent: grid = min(units, SMs); CTA c takes work units c, c + grid, ... in order, a unit
@@ -76,6 +77,116 @@ __host__ __device__ constexpr size_t tc_stage_bytes() {
 template <int BN, int CL>
 __host__ __device__ constexpr size_t tc_smem() {
   return tc_stages<BN, CL>() * tc_stage_bytes<BN, CL>() + 256 + 8 * 32 * 33 * 4 + 1024;
+}
+
+// EPI_QKV epilogue of one thread: v holds row `row` of the 32 columns col0 .. col0 + 31 (of
+// q | k | v, pair order: columns 2i and 2i + 1 of a head are the rotation pair (a, b) of
+// head columns i and i + hd/2). Adds the bias, rotates q and k rows by the position's
+// (cos, sin): a' = a cos - b sin, b' = b cos + a sin, and stores fp16 at head columns i and
+// i + hd/2 of Qh (times qscale) or of the K or V cache row at position pos0 + row.
+__device__ __forceinline__ void qkv_row(const TcEpi& ep, const float* v, int col0, int N, int row, int M,
+                                        int* err) {
+  const QkvOut& o = ep.qkv;
+  if (row >= M) return;
+  const int hd = o.hd, half = hd >> 1;
+  bool bad = false;  // a value fp16 cannot hold
+  if ((hd & 31) == 0) {  // the 32 columns lie in one head: 16 pairs, vector loads and stores
+    if (col0 >= N) return;
+    const int head = col0 / hd, i0 = (col0 - head * hd) >> 1;
+    const bool rot = head < o.nq + o.nkv;
+    float a[16], b[16];
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      a[p] = v[2 * p];
+      b[p] = v[2 * p + 1];
+    }
+    if (ep.bias) {
+      const uint4* bp = reinterpret_cast<const uint4*>(ep.bias + col0);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 w = __ldg(bp + q4);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+          a[4 * q4 + k] += f.x;
+          b[4 * q4 + k] += f.y;
+        }
+      }
+    }
+    float scale = 1.f;
+    f16* dst;
+    if (head < o.nq) {
+      dst = o.Qh + (size_t)row * o.nq * hd + (size_t)head * hd;
+      scale = o.qscale;
+    } else {
+      const int hh = rot ? head - o.nq : head - o.nq - o.nkv;
+      dst = (rot ? o.kc : o.vc) + ((size_t)hh * o.cap + o.pos0 + row) * hd;
+    }
+    if (rot) {
+      const float4* cp = reinterpret_cast<const float4*>(o.rope + (size_t)(o.pos0 + row) * half + i0);
+#pragma unroll
+      for (int q2 = 0; q2 < 8; ++q2) {
+        const float4 c2 = __ldg(cp + q2);  // (cos, sin) of pairs 2 q2 and 2 q2 + 1
+        const int p = 2 * q2;
+        const float ra = a[p] * c2.x - b[p] * c2.y, rb = b[p] * c2.x + a[p] * c2.y;
+        const float sa = a[p + 1] * c2.z - b[p + 1] * c2.w, sb = b[p + 1] * c2.z + a[p + 1] * c2.w;
+        a[p] = ra;
+        b[p] = rb;
+        a[p + 1] = sa;
+        b[p + 1] = sb;
+      }
+    }
+    uint32_t ha[8], hb[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float x0 = a[2 * k] * scale, x1 = a[2 * k + 1] * scale;
+      const float y0 = b[2 * k] * scale, y1 = b[2 * k + 1] * scale;
+      bad |= !(fabsf(x0) < 65520.f) || !(fabsf(x1) < 65520.f) || !(fabsf(y0) < 65520.f) || !(fabsf(y1) < 65520.f);
+      const __half2 hx = __floats2half2_rn(x0, x1), hy = __floats2half2_rn(y0, y1);
+      ha[k] = *reinterpret_cast<const uint32_t*>(&hx);
+      hb[k] = *reinterpret_cast<const uint32_t*>(&hy);
+    }
+    uint4* da = reinterpret_cast<uint4*>(dst + i0);
+    uint4* db = reinterpret_cast<uint4*>(dst + i0 + half);
+    da[0] = make_uint4(ha[0], ha[1], ha[2], ha[3]);
+    da[1] = make_uint4(ha[4], ha[5], ha[6], ha[7]);
+    db[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+    db[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+  } else {  // any even head size: pair by pair
+    for (int p = 0; p < 16; ++p) {
+      const int col = col0 + 2 * p;
+      if (col >= N) break;
+      float x = v[2 * p], y = v[2 * p + 1];
+      if (ep.bias) {
+        x += to_f32(ep.bias[col]);
+        y += to_f32(ep.bias[col + 1]);
+      }
+      const int head = col / hd, i = (col - head * hd) >> 1;
+      float scale = 1.f;
+      f16* dst;
+      if (head < o.nq + o.nkv) {
+        const float2 cs = o.rope[(size_t)(o.pos0 + row) * half + i];
+        const float rx = x * cs.x - y * cs.y, ry = y * cs.x + x * cs.y;
+        x = rx;
+        y = ry;
+      }
+      if (head < o.nq) {
+        dst = o.Qh + (size_t)row * o.nq * hd + (size_t)head * hd;
+        scale = o.qscale;
+      } else {
+        const bool is_k = head < o.nq + o.nkv;
+        const int hh = is_k ? head - o.nq : head - o.nq - o.nkv;
+        dst = (is_k ? o.kc : o.vc) + ((size_t)hh * o.cap + o.pos0 + row) * hd;
+      }
+      x *= scale;
+      y *= scale;
+      bad |= !(fabsf(x) < 65520.f) || !(fabsf(y) < 65520.f);
+      dst[i] = __float2half_rn(x);
+      dst[i + half] = __float2half_rn(y);
+    }
+  }
+  if (bad) atomicOr(err, ERR_RANGE);
 }
 
 template <int BN, int EPI, int CL>
@@ -236,6 +347,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int i1 = 0; i1 < 32; ++i1) v[i1] = __fdividef(gv[i1], 1.f + __expf(-gv[i1])) * uv[i1];
         } else {
           tc::tmem_ld32(lane_base + c, v);
+        }
+        if (EPI == EPI_QKV && g.splits == 1) {  // row per thread: the pairs sit in adjacent registers
+          qkv_row(ep, v, n0 + c, N, rbase + lane, M, err);
+          continue;
         }
         __syncwarp();
 #pragma unroll
@@ -537,6 +652,43 @@ __global__ void splitk_reduce_kernel(const float* ws, int splits, int M, int N, 
   C[(size_t)m * ldc + n] = acc;
 }
 
+// EPI_QKV after split-K: one thread per (row, rotation pair), the splits added in order
+__global__ void splitk_qkv_kernel(const float* ws, int splits, int M, int N, const bf16* bias, QkvOut o, int* err) {
+  const int np = N >> 1;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)M * np) return;
+  const int m = (int)(idx / np), col = 2 * (int)(idx - (size_t)m * np);
+  float a = 0.f, b = 0.f;
+  for (int z = 0; z < splits; ++z) {
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(ws + ((size_t)z * M + m) * N + col));
+    a += v.x;
+    b += v.y;
+  }
+  if (bias) {
+    a += __bfloat162float(bias[col]);
+    b += __bfloat162float(bias[col + 1]);
+  }
+  const int head = col / o.hd, half = o.hd >> 1, i = (col - head * o.hd) >> 1;
+  f16* dst;
+  if (head < o.nq + o.nkv) {
+    const float2 cs = o.rope[(size_t)(o.pos0 + m) * half + i];
+    const float ra = a * cs.x - b * cs.y, rb = b * cs.x + a * cs.y;
+    a = ra;
+    b = rb;
+  }
+  if (head < o.nq) {
+    dst = o.Qh + (size_t)m * o.nq * o.hd + (size_t)head * o.hd;
+    a *= o.qscale;
+    b *= o.qscale;
+  } else {
+    const bool is_k = head < o.nq + o.nkv;
+    const int hh = is_k ? head - o.nq : head - o.nq - o.nkv;
+    dst = (is_k ? o.kc : o.vc) + ((size_t)hh * o.cap + o.pos0 + m) * o.hd;
+  }
+  dst[i] = to_half_checked(a, err);
+  dst[i + half] = to_half_checked(b, err);
+}
+
 // ---- host side ------------------------------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -606,6 +758,9 @@ cudaError_t gemm_tc_set_attributes() {
   if ((e = set_tc_attr<192, EPI_STORE, 1>()) || (e = set_tc_attr<192, EPI_STORE, 2>())) return e;
   if ((e = set_tc_attr<192, EPI_ADD, 1>()) || (e = set_tc_attr<192, EPI_ADD, 2>())) return e;
   if ((e = set_tc_attr<64, EPI_STORE, 1>()) || (e = set_tc_attr<64, EPI_ADD, 1>())) return e;
+  if ((e = set_tc_attr<TC_BN, EPI_QKV, 1>()) || (e = set_tc_attr<TC_BN, EPI_QKV, 2>())) return e;
+  if ((e = set_tc_attr<192, EPI_QKV, 1>()) || (e = set_tc_attr<192, EPI_QKV, 2>())) return e;
+  if ((e = set_tc_attr<64, EPI_QKV, 1>())) return e;
   return set_tc_attr<128, EPI_SWIGLU, 1>();
 }
 
@@ -754,9 +909,12 @@ static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, con
   return launch_tc<BN, EPI_STORE, CL>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
 }
 
-cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bias, float* C, int ldc,
-                    int M, int N, int K, bool accumulate, int* err, cudaStream_t s, float* ws, size_t ws_floats,
-                    int nsm) {
+// Tile width, K splits and CTA pairing of a C[M, N] = A . B^T launch
+struct TcPlan {
+  int bn, splits, tiles_m;
+  bool pair;
+};
+static TcPlan tc_plan(int M, int N, int K, const float* ws, size_t ws_floats, int nsm) {
   const int tiles_m = (M + tc::BM - 1) / tc::BM;
   const int nk = (K + tc::BK - 1) / tc::BK;
   // tile width: 256 or 192 columns, whichever finishes first when the tiles go round the
@@ -783,10 +941,19 @@ cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bi
   }
   // CTA pairs (M = 256 products, each CTA staging half of B) when there are row tiles to pair
   const bool pair = bn != 64 && tiles_m >= 2 && nsm >= 2 && gemm_pairs();
+  return TcPlan{bn, splits, tiles_m, pair};
+}
+
+cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bias, float* C, int ldc,
+                    int M, int N, int K, bool accumulate, int* err, cudaStream_t s, float* ws, size_t ws_floats,
+                    int nsm) {
+  const TcPlan pl = tc_plan(M, N, K, ws, ws_floats, nsm);
+  const int bn = pl.bn, splits = pl.splits, tiles_m = pl.tiles_m;
+  const bool pair = pl.pair;
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mb, B, N, K, ldb, pair ? bn / 2 : bn))
     return cudaErrorInvalidValue;
-  TcEpi ep{C, bias, nullptr, ldc};
+  TcEpi ep{C, bias, nullptr, ldc, {}};
   const TcGrid g{tiles_m, (N + bn - 1) / bn, splits};
   const bool add = accumulate && splits == 1;
   cudaError_t e;
@@ -804,6 +971,33 @@ cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bi
   return cudaGetLastError();
 }
 
+// q | k | v = A . B^T (+ bias), rotated and stored in fp16 (QkvOut)
+cudaError_t gemm_tc_qkv(const f16* A, int lda, const f16* B, int ldb, const bf16* bias, int M, int N, int K,
+                        const QkvOut& o, int* err, cudaStream_t s, float* ws, size_t ws_floats, int nsm) {
+  if (o.hd <= 0 || (o.hd & 1) || N != (o.nq + 2 * o.nkv) * o.hd) return cudaErrorInvalidValue;
+  const TcPlan pl = tc_plan(M, N, K, ws, ws_floats, nsm);
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mb, B, N, K, ldb, pl.pair ? pl.bn / 2 : pl.bn))
+    return cudaErrorInvalidValue;
+  TcEpi ep{nullptr, bias, nullptr, 0, o};
+  const TcGrid g{pl.tiles_m, (N + pl.bn - 1) / pl.bn, pl.splits};
+  cudaError_t e;
+  if (pl.bn == 192)
+    e = pl.pair ? launch_tc<192, EPI_QKV, 2>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s)
+                : launch_tc<192, EPI_QKV, 1>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
+  else if (pl.bn == 64)
+    e = launch_tc<64, EPI_QKV, 1>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
+  else
+    e = pl.pair ? launch_tc<TC_BN, EPI_QKV, 2>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s)
+                : launch_tc<TC_BN, EPI_QKV, 1>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
+  if (e) return e;
+  if (pl.splits > 1) {
+    const size_t n = (size_t)M * (N / 2);
+    splitk_qkv_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, pl.splits, M, N, bias, o, err);
+  }
+  return cudaGetLastError();
+}
+
 // Act[M][N] (fp16, ldc) = silu(A . Wg^T) * (A . Wu^T)
 cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, int ldb, f16* Act,
                            int ldc, int M, int N, int K, int* err, cudaStream_t s, float* ws, size_t ws_floats,
@@ -816,7 +1010,7 @@ cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, 
   if (!make_map(&ma, A, M, K, lda, tc::BM) || !make_map(&mg, Wg, N, K, ldb, bn / 2) ||
       !make_map(&mu, Wu, N, K, ldb, bn / 2))
     return cudaErrorInvalidValue;
-  TcEpi ep{nullptr, nullptr, Act, ldc};
+  TcEpi ep{nullptr, nullptr, Act, ldc, {}};
   const int tiles = ((N + bn / 2 - 1) / (bn / 2)) * tiles_m;
   const int nk = (K + tc::BK - 1) / tc::BK;
   int splits = 1;  // as in gemm_tc: split K when the tiles leave SMs idle

@@ -25,8 +25,9 @@ struct Dims {
 struct LayerPtrs {
   const void *in_norm, *wq, *bq, *wk, *bk, *wv, *bv, *wo, *post_norm, *w_gate, *w_up, *w_down;
   // fp16 copies of the matrices (bf16 models; prefill tensor-core operands). wq16, wk16 and
-  // wv16 lie back to back (one [nq*hd + 2*nkv*hd][H] matrix), bqkv holds bq | bk | bv (bf16)
-  // or is null without q/k/v biases.
+  // wv16 lie back to back (one [nq*hd + 2*nkv*hd][H] matrix) with every head's rows in
+  // RoPE-pair order (row 2i + e = source row i + e hd/2), bqkv holds bq | bk | bv (bf16) in
+  // the same order, or is null without q/k/v biases.
   const void *wq16, *wk16, *wv16, *wo16, *wg16, *wu16, *wd16;
   const void* bqkv;
 };
@@ -124,6 +125,20 @@ cudaError_t gemm_tc_set_attributes();
 cudaError_t gemm_tc(const __half* A, int lda, const __half* B, int ldb, const __nv_bfloat16* bias,
                     float* C, int ldc, int M, int N, int K, bool accumulate, int* err,
                     cudaStream_t s, float* ws = nullptr, size_t ws_floats = 0, int nsm = 0);
+// Outputs of the fused q/k/v projection (columns q | k | v, each head's columns in RoPE-pair
+// order as the weights' rows are): + bias, rotation of q and k rows m at position pos0 + m,
+// q times qscale to Qh [M][nq*hd] (fp16), k and v to the layer's fp16 caches [nkv][cap][hd]
+// at positions pos0 .. pos0 + M - 1 (fp16 range errors set ERR_RANGE).
+struct QkvOut {
+  __half* Qh;
+  __half *kc, *vc;
+  const float2* rope;  // (cos, sin) [position][hd/2]
+  float qscale;
+  int nq, nkv, hd, pos0, cap;
+};
+cudaError_t gemm_tc_qkv(const __half* A, int lda, const __half* B, int ldb, const __nv_bfloat16* bias, int M, int N,
+                        int K, const QkvOut& o, int* err, cudaStream_t s, float* ws = nullptr, size_t ws_floats = 0,
+                        int nsm = 0);
 cudaError_t gemm_tc_swiglu(const __half* A, int lda, const __half* Wg, const __half* Wu, int ldb,
                            __half* Act, int ldc, int M, int N, int K, int* err, cudaStream_t s, float* ws = nullptr,
                            size_t ws_floats = 0, int nsm = 0);
@@ -224,5 +239,10 @@ cudaError_t prefill_layers(const Dims& d, const LayerPtrs* layers, const void* e
                            const int* ids_dev, int T, int pos0, const float2* rope,
                            void* kcache_seq, const PrefillBufs& b, int* err, cudaStream_t s);
 cudaError_t convert_bf16_to_half(const void* src, void* dst, size_t n, int* err, cudaStream_t s);
+// fp16 copy of a matrix of whole heads with each head's rows in RoPE-pair order (row 2i + e
+// of a head = source row i + e hd/2), and a bf16 bias vector into the same order
+cudaError_t convert_bf16_to_half_pairs(const void* src, void* dst, size_t rows, int K, int hd, int* err,
+                                       cudaStream_t s);
+cudaError_t copy_bias_pairs(const void* src, void* dst, int n, int hd, cudaStream_t s);
 
 }  // namespace qw

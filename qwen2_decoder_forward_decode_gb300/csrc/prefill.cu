@@ -130,12 +130,12 @@ __global__ void swiglu_kernel(const float* G, const float* U, float* A, size_t n
   }
 }
 
-// Y [T][nq*hd + 2*nkv*hd] (q | k | v, bias included) -> Q [T][nq*hd] rotated (fp32, or fp16
-// times qscale into Qh when Qh is given); K, V rotated/copied into the cache at positions pos0 + t.
+// Y [T][nq*hd + 2*nkv*hd] (q | k | v, bias included; with pairs, each head's columns in
+// RoPE-pair order) -> Q [T][nq*hd] rotated (fp32); K, V rotated/copied into the cache at
+// positions pos0 + t.
 template <typename KV>
 __global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, int pos0, int cap,
-                               const float2* rope, float* Q, KV* kc, KV* vc, int* err, f16* Qh = nullptr,
-                               float qscale = 1.f) {
+                               const float2* rope, float* Q, KV* kc, KV* vc, int* err, bool pairs = false) {
   const int t = blockIdx.x;
   const int half = hd / 2;
   const int width = (nq + 2 * nkv) * hd;
@@ -143,19 +143,16 @@ __global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, 
   const float* y = Y + (size_t)t * width;
   for (int idx = threadIdx.x; idx < (nq + 2 * nkv) * half; idx += blockDim.x) {
     const int head = idx / half, i = idx - head * half;
-    const float a = y[head * hd + i], b = y[head * hd + i + half];
+    // pairs: Y's head columns in pair order (2i, 2i + 1), else split-half (i, i + hd/2)
+    const float a = pairs ? y[head * hd + 2 * i] : y[head * hd + i];
+    const float b = pairs ? y[head * hd + 2 * i + 1] : y[head * hd + i + half];
     if (head < nq + nkv) {
       const float2 cs = rope[(size_t)pos * half + i];
       const float ra = a * cs.x - b * cs.y, rb = b * cs.x + a * cs.y;
       if (head < nq) {
         const size_t o = (size_t)t * nq * hd + head * hd + i;
-        if (Qh) {
-          Qh[o] = to_half_checked(ra * qscale, err);
-          Qh[o + half] = to_half_checked(rb * qscale, err);
-        } else {
-          Q[o] = ra;
-          Q[o + half] = rb;
-        }
+        Q[o] = ra;
+        Q[o + half] = rb;
       } else {
         KV* dst = kc + ((size_t)(head - nq) * cap + pos) * hd;
         store_kv(dst + i, ra, err);
@@ -166,42 +163,6 @@ __global__ void rope_kv_kernel(const float* Y, int T_, int nq, int nkv, int hd, 
       store_kv(dst + i, a, err);
       store_kv(dst + i + half, b, err);
     }
-  }
-}
-
-// The tensor-core path's variant: fp16 cache, Q to fp16 times qscale; two adjacent pairs
-// (i, i + 1) per thread with 8-byte loads and 4-byte stores (hd a multiple of 4).
-__global__ void rope_kv_h_kernel(const float* Y, int nq, int nkv, int hd, int pos0, int cap, const float2* rope,
-                                 f16* Qh, float qscale, f16* kc, f16* vc, int* err) {
-  const int t = blockIdx.x;
-  const int half = hd / 2, hp = half / 2;  // pairs of i per head
-  const int pos = pos0 + t;
-  const float* y = Y + (size_t)t * (nq + 2 * nkv) * hd;
-  for (int idx = threadIdx.x; idx < (nq + 2 * nkv) * hp; idx += blockDim.x) {
-    const int head = idx / hp, i = 2 * (idx - head * hp);
-    const float2 a = *reinterpret_cast<const float2*>(y + head * hd + i);
-    const float2 b = *reinterpret_cast<const float2*>(y + head * hd + i + half);
-    __half2 lo, hi;
-    f16* dst;
-    if (head < nq + nkv) {
-      const float4 cs = *reinterpret_cast<const float4*>(rope + (size_t)pos * half + i);  // (cos, sin) of i, i + 1
-      float ra0 = a.x * cs.x - b.x * cs.y, rb0 = b.x * cs.x + a.x * cs.y;
-      float ra1 = a.y * cs.z - b.y * cs.w, rb1 = b.y * cs.z + a.y * cs.w;
-      if (head < nq) {
-        ra0 *= qscale; ra1 *= qscale; rb0 *= qscale; rb1 *= qscale;
-        dst = Qh + (size_t)t * nq * hd + head * hd;
-      } else {
-        dst = kc + ((size_t)(head - nq) * cap + pos) * hd;
-      }
-      lo = to_half2_checked(ra0, ra1, err);
-      hi = to_half2_checked(rb0, rb1, err);
-    } else {
-      dst = vc + ((size_t)(head - nq - nkv) * cap + pos) * hd;
-      lo = to_half2_checked(a.x, a.y, err);
-      hi = to_half2_checked(b.x, b.y, err);
-    }
-    *reinterpret_cast<__half2*>(dst + i) = lo;
-    *reinterpret_cast<__half2*>(dst + i + half) = hi;
   }
 }
 
@@ -661,28 +622,23 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
     f16* kc = (f16*)kcache + (size_t)l * 2 * layer_stride;
     f16* vc = kc + layer_stride;
     norm_rows_h(b.X, (const bf16*)w.in_norm, T_, H, d.eps, b.Xh, err, s, d.nsm);
-    if (w.wk16 == (const f16*)w.wq16 + (size_t)qd * H && w.wv16 == (const f16*)w.wk16 + (size_t)kvd * H &&
-        (w.bqkv || !w.bq)) {
-      // q | k | v as one projection: the three matrices lie back to back, and so do the
-      // columns of Y
-      if ((e = gemm_tc(b.Xh, H, (const f16*)w.wq16, H, (const bf16*)w.bqkv, b.Y, Wd, T_, Wd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-    } else {
-      if ((e = gemm_tc(b.Xh, H, (const f16*)w.wq16, H, (const bf16*)w.bq, b.Y, Wd, T_, qd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-      if ((e = gemm_tc(b.Xh, H, (const f16*)w.wk16, H, (const bf16*)w.bk, b.Y + qd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-      if ((e = gemm_tc(b.Xh, H, (const f16*)w.wv16, H, (const bf16*)w.bv, b.Y + qd + kvd, Wd, T_, kvd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
-    }
+    // q | k | v as one projection: the three fp16 matrices lie back to back (each head's rows
+    // in RoPE-pair order), and so do the columns of the output
+    if (w.wk16 != (const f16*)w.wq16 + (size_t)qd * H || w.wv16 != (const f16*)w.wk16 + (size_t)kvd * H ||
+        (w.bq && !w.bqkv))
+      return cudaErrorInvalidValue;
+    const f16* wqkv = (const f16*)w.wq16;
+    const bf16* bqkv = (const bf16*)w.bqkv;
     const int kind = prefill_attention_kind();
     if (kind == PA_TC && attn_prefill_tc_supported(d.hd) && d.I >= qd) {
-      // q in fp16, scaled into base-2 scores, in the (still free) SwiGLU operand buffer
-      const float qs = 1.4426950408889634f / sqrtf((float)d.hd);
-      if (d.hd % 4 == 0)
-        rope_kv_h_kernel<<<T_, 256, 0, s>>>(b.Y, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Ah, qs, kc, vc, err);
-      else
-        rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err,
-                                              b.Ah, qs);
+      // bias, RoPE and the K/V append in the projection's epilogue; q in fp16, scaled into
+      // base-2 scores, in the (still free) SwiGLU operand buffer
+      const QkvOut o{b.Ah, kc, vc, rope, 1.4426950408889634f / sqrtf((float)d.hd), d.nq, d.nkv, d.hd, pos0, d.cap};
+      if ((e = gemm_tc_qkv(b.Xh, H, wqkv, H, bqkv, T_, Wd, H, o, err, s, b.ws, b.ws_floats, d.nsm))) return e;
       if ((e = attn_prefill_tc(d, T_, pos0, b.Ah, kc, vc, b.Oh, err, s))) return e;
     } else {
-      rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err);
+      if ((e = gemm_tc(b.Xh, H, wqkv, H, bqkv, b.Y, Wd, T_, Wd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+      rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err, true);
       const bool mma = kind != PA_SIMT && attn_prefill_mma(d, b.Q, T_, pos0, kc, vc, b.Oh, s, &e);
       if (mma && e) return e;
       if (!mma) {
@@ -723,6 +679,43 @@ __global__ void bf16_to_half_kernel(const bf16* src, f16* dst, size_t n, int* er
 cudaError_t convert_bf16_to_half(const void* src, void* dst, size_t n, int* err, cudaStream_t s) {
   const size_t blocks = (n + 255) / 256;
   bf16_to_half_kernel<<<(unsigned)(blocks < 8192 ? blocks : 8192), 256, 0, s>>>((const bf16*)src, (f16*)dst, n, err);
+  return cudaGetLastError();
+}
+
+// The same copy of a matrix of whole heads (rows = heads x hd, K columns each) with every
+// head's rows in RoPE-pair order: row 2i + e of a head is source row i + e hd/2, so the two
+// members of each rotation pair come out of a projection as adjacent columns.
+__global__ void bf16_to_half_pairs_kernel(const bf16* src, f16* dst, size_t rows, int K, int hd, int* err) {
+  const int half = hd >> 1;
+  for (size_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const size_t head = r / hd;
+    const int j = (int)(r - head * hd);
+    const bf16* s_row = src + (head * hd + (j >> 1) + (j & 1) * half) * (size_t)K;
+    f16* d_row = dst + r * (size_t)K;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) d_row[k] = to_half_checked(__bfloat162float(s_row[k]), err);
+  }
+}
+
+cudaError_t convert_bf16_to_half_pairs(const void* src, void* dst, size_t rows, int K, int hd, int* err,
+                                       cudaStream_t s) {
+  if (hd <= 0 || hd % 2 || rows % hd) return cudaErrorInvalidValue;
+  bf16_to_half_pairs_kernel<<<(unsigned)(rows < 8192 ? rows : 8192), 256, 0, s>>>((const bf16*)src, (f16*)dst, rows,
+                                                                                 K, hd, err);
+  return cudaGetLastError();
+}
+
+// a bias vector of whole heads into the same pair order (bf16 kept)
+__global__ void bias_pairs_kernel(const bf16* src, bf16* dst, int n, int hd) {
+  const int half = hd >> 1;
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < n; c += gridDim.x * blockDim.x) {
+    const int head = c / hd, j = c - head * hd;
+    dst[c] = src[head * hd + (j >> 1) + (j & 1) * half];
+  }
+}
+
+cudaError_t copy_bias_pairs(const void* src, void* dst, int n, int hd, cudaStream_t s) {
+  if (hd <= 0 || hd % 2 || n % hd) return cudaErrorInvalidValue;
+  bias_pairs_kernel<<<(n + 255) / 256, 256, 0, s>>>((const bf16*)src, (bf16*)dst, n, hd);
   return cudaGetLastError();
 }
 
