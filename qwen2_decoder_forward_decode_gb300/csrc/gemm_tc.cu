@@ -376,6 +376,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int rr = 0; rr < 32; ++rr)
               if (rr < nr) ep.C[(size_t)(rbase + rr) * ep.ldc + col] = old[rr] + stg[rr * 33 + lane];
           } else {
+            bool bad = false;  // fp16 range (SwiGLU output), raised once after the block
 #pragma unroll 4
             for (int rr = 0; rr < nr; ++rr) {
               const float x = stg[rr * 33 + lane];
@@ -386,11 +387,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 else
                   ws[((size_t)z * M + row) * N + col] = x;
               } else if (GLU_OUT) {
-                ep.Cb[(size_t)row * ep.ldc + col] = to_half_checked(x, err);
+                bad |= !(fabsf(x) < 65520.f);
+                ep.Cb[(size_t)row * ep.ldc + col] = __float2half_rn(x);
               } else {
                 ep.C[(size_t)row * ep.ldc + col] = x + bias;
               }
             }
+            if (bad) atomicOr(err, ERR_RANGE);
           }
         }
       }

@@ -47,28 +47,39 @@ __global__ void norm_rows_kernel(const float* X, const T* gain, int H, float eps
 // The same for fp16 output rows with H a multiple of 128: one warp per row, float4 loads
 // and 8-byte stores. The row is read twice (sum of squares, then the scaled values); the
 // second read comes from L2. Sums in a fixed order: deterministic.
+// Warp per row, the row held in registers (MAXV float4 per lane: H <= 128 MAXV), one read
+// of X; fp16 range errors gathered per lane and raised once.
+template <int MAXV>
 __global__ void norm_rows_h_kernel(const float* X, const bf16* gain, int T, int H, float eps, f16* Y, int* err) {
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= T) return;
+  const int nv = H >> 7;  // float4 per lane
   const float4* x = reinterpret_cast<const float4*>(X + (size_t)row * H);
+  float4 v[MAXV];
   float ss = 0.f;
-  for (int k = lane; k < H / 4; k += 32) {
-    const float4 v = x[k];
-    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    v[j] = j < nv ? __ldcg(x + lane + 32 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss = fmaf(v[j].x, v[j].x, fmaf(v[j].y, v[j].y, fmaf(v[j].z, v[j].z, fmaf(v[j].w, v[j].w, ss))));
   }
   ss = warp_sum(ss);
   const float inv = rsqrtf(ss / (float)H + eps);
   const uint2* gp = reinterpret_cast<const uint2*>(gain);
   uint2* y = reinterpret_cast<uint2*>(Y + (size_t)row * H);
-  for (int k = lane; k < H / 4; k += 32) {
-    const float4 v = x[k];
-    const uint2 gb = gp[k];
-    const float g0 = __uint_as_float(gb.x << 16), g1 = __uint_as_float(gb.x & 0xffff0000u);
-    const float g2 = __uint_as_float(gb.y << 16), g3 = __uint_as_float(gb.y & 0xffff0000u);
-    const __half2 lo = to_half2_checked(v.x * inv * g0, v.y * inv * g1, err);
-    const __half2 hi = to_half2_checked(v.z * inv * g2, v.w * inv * g3, err);
-    y[k] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    if (j < nv) {
+      const int k = lane + 32 * j;
+      const uint2 gb = __ldg(gp + k);
+      const float a = v[j].x * inv * __uint_as_float(gb.x << 16), b = v[j].y * inv * __uint_as_float(gb.x & 0xffff0000u);
+      const float c = v[j].z * inv * __uint_as_float(gb.y << 16), d = v[j].w * inv * __uint_as_float(gb.y & 0xffff0000u);
+      bad |= !(fabsf(a) < 65520.f) || !(fabsf(b) < 65520.f) || !(fabsf(c) < 65520.f) || !(fabsf(d) < 65520.f);  // NaN too
+      const __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
+      y[k] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
   }
+  if (bad) atomicOr(err, ERR_RANGE);
 }
 
 // Short prompts: one 128-thread block per row (float4 loads, 8-byte stores), so that every
@@ -91,18 +102,20 @@ __global__ void __launch_bounds__(128) norm_row_block_h_kernel(const float* X, c
   }
   ss = block_sum(ss, scratch);
   const float inv = rsqrtf(ss / (float)H + eps);
+  bool bad = false;
 #pragma unroll
   for (int j = 0; j < MAXV; ++j) {
     const int k = threadIdx.x + 128 * j;
     if (k < H / 4) {
-      const uint2 gb = gp[k];
-      const __half2 lo = to_half2_checked(v[j].x * inv * __uint_as_float(gb.x << 16),
-                                          v[j].y * inv * __uint_as_float(gb.x & 0xffff0000u), err);
-      const __half2 hi = to_half2_checked(v[j].z * inv * __uint_as_float(gb.y << 16),
-                                          v[j].w * inv * __uint_as_float(gb.y & 0xffff0000u), err);
+      const uint2 gb = __ldg(gp + k);
+      const float a = v[j].x * inv * __uint_as_float(gb.x << 16), b = v[j].y * inv * __uint_as_float(gb.x & 0xffff0000u);
+      const float c = v[j].z * inv * __uint_as_float(gb.y << 16), d = v[j].w * inv * __uint_as_float(gb.y & 0xffff0000u);
+      bad |= !(fabsf(a) < 65520.f) || !(fabsf(b) < 65520.f) || !(fabsf(c) < 65520.f) || !(fabsf(d) < 65520.f);  // NaN too
+      const __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
       y[k] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
     }
   }
+  if (bad) atomicOr(err, ERR_RANGE);
 }
 
 static void norm_rows_h(const float* X, const bf16* gain, int T_, int H, float eps, f16* Y, int* err, cudaStream_t s,
@@ -110,8 +123,10 @@ static void norm_rows_h(const float* X, const bf16* gain, int T_, int H, float e
   const bool vec = H % 128 == 0 && ((uintptr_t)gain & 7) == 0;
   if (vec && T_ < 4 * nsm && H <= 4096) {
     norm_row_block_h_kernel<<<T_, 128, 0, s>>>(X, gain, H, eps, Y, err);
-  } else if (vec) {
-    norm_rows_h_kernel<<<(T_ + 7) / 8, 256, 0, s>>>(X, gain, T_, H, eps, Y, err);
+  } else if (vec && H <= 128 * 12) {
+    norm_rows_h_kernel<12><<<(T_ + 7) / 8, 256, 0, s>>>(X, gain, T_, H, eps, Y, err);
+  } else if (vec && H <= 128 * 32) {
+    norm_rows_h_kernel<32><<<(T_ + 7) / 8, 256, 0, s>>>(X, gain, T_, H, eps, Y, err);
   } else {
     norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(X, gain, H, eps, Y, err);
   }
