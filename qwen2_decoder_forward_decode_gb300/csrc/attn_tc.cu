@@ -108,6 +108,7 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
                        const __grid_constant__ CUtensorMap tmV, const Args a) {
   using Lay = L<HD>;
   constexpr int KS = Lay::KS;
+  pdl_trigger();  // the next kernel may be scheduled once every CTA of this one has started
   extern __shared__ __align__(1024) uint8_t fa_raw[];
   uint8_t* smem = fa_raw;
   uint64_t* bars = (uint64_t*)(smem + Lay::OFF_BAR);
@@ -133,6 +134,7 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
     if (threadIdx.x == 0) atomicOr(a.err, ERR_LAYOUT);
     return;
   }
+  pdl_wait();  // q and the caches come from the previous kernel
   // after a timeout anywhere on the stream the remaining CTAs do nothing
   if (threadIdx.x == 0) *s_abort = (*(volatile int*)a.err & ERR_TIMEOUT) != 0;
   __syncthreads();
@@ -401,10 +403,10 @@ cudaError_t attn_prefill_tc(const Dims& d, int T, int pos0, const f16* Qh, const
   const CUtensorMap& k = *reinterpret_cast<const CUtensorMap*>(mk);
   const CUtensorMap& v = *reinterpret_cast<const CUtensorMap*>(mv);
   if (d.hd == 128)
-    fa::attn_prefill_tc_kernel<128><<<nqb * d.nq, fa::THREADS, fa::L<128>::SMEM, s>>>(q, k, v, a);
-  else
-    fa::attn_prefill_tc_kernel<64><<<nqb * d.nq, fa::THREADS, fa::L<64>::SMEM, s>>>(q, k, v, a);
-  return cudaGetLastError();
+    return launch_k(fa::attn_prefill_tc_kernel<128>, dim3(nqb * d.nq), dim3(fa::THREADS), fa::L<128>::SMEM, s,
+                    tc_pdl(), q, k, v, a);
+  return launch_k(fa::attn_prefill_tc_kernel<64>, dim3(nqb * d.nq), dim3(fa::THREADS), fa::L<64>::SMEM, s, tc_pdl(),
+                  q, k, v, a);
 }
 
 }  // namespace qw

@@ -202,6 +202,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   static_assert(tc_smem<BN, CL>() <= 232448, "shared memory");
   constexpr int NOUT = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
+  // launched with programmatic dependent launch: the next kernel may be scheduled once every
+  // CTA of this one runs (it waits for this grid's completion before touching its outputs)
+  pdl_trigger();
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE);
   uint32_t* tmem_slot = (uint32_t*)(bars + 2 * STAGES + 4);
@@ -252,34 +255,58 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ---- TMA producer: the K blocks of this CTA's units, back to back
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
-    int it = 0;  // K blocks issued
-    for (int u = first; u < units && !s_abort; u += step) {
-      int m0, n0, z, kb_lo, kb_hi;
-      unit_of(u, m0, n0, z, kb_lo, kb_hi);
-      for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
-        const int s = it % STAGES;
-        if (it >= STAGES && !tc::mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, err)) { s_abort = 1; break; }
-        if (s_abort) break;
-        const uint32_t a_dst = smem_u32(smem + s * STAGE);
-        const uint32_t b_dst = a_dst + A_BYTES;
-        if (CL == 2) {  // bytes counted on the even CTA's barrier (SwiGLU: rank 0 gate, rank 1 up)
-          const uint32_t bar = tc::mapa_shared(full0 + 8 * s, 0);
-          if (rank == 0) tc::mbar_expect_tx(full0 + 8 * s, 2 * STAGE);
-          tc::tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, m0);
+    // stage s of K block kb of the unit at (m0, n0): the byte count, then A and/or B
+    auto issue = [&](int s, int kb, int m0, int n0, bool load_a, bool load_b) {
+      const uint32_t a_dst = smem_u32(smem + s * STAGE);
+      const uint32_t b_dst = a_dst + A_BYTES;
+      if (CL == 2) {  // bytes counted on the even CTA's barrier (SwiGLU: rank 0 gate, rank 1 up)
+        const uint32_t bar = tc::mapa_shared(full0 + 8 * s, 0);
+        if (load_b && rank == 0) tc::mbar_expect_tx(full0 + 8 * s, 2 * STAGE);
+        if (load_a) tc::tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, m0);
+        if (load_b) {
           if (EPI == EPI_SWIGLU)
             tc::tma_load_2d_pair(b_dst, rank ? &tmB2 : &tmB, bar, kb * BK, n0);
           else
             tc::tma_load_2d_pair(b_dst, &tmB, bar, kb * BK, n0 + rank * (BN / 2));
-          continue;
         }
-        tc::mbar_expect_tx(full0 + 8 * s, STAGE);
-        tc::tma_load_2d(a_dst, &tmA, full0 + 8 * s, kb * BK, m0);
+        return;
+      }
+      if (load_b) tc::mbar_expect_tx(full0 + 8 * s, STAGE);
+      if (load_a) tc::tma_load_2d(a_dst, &tmA, full0 + 8 * s, kb * BK, m0);
+      if (load_b) {
         if (EPI == EPI_SWIGLU) {
           tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kb * BK, n0);
           tc::tma_load_2d(b_dst + B_BYTES / 2, &tmB2, full0 + 8 * s, kb * BK, n0);
         } else {
           tc::tma_load_2d(b_dst, &tmB, full0 + 8 * s, kb * BK, n0);
         }
+      }
+    };
+    // The weights (B) of the first stages are requested before waiting for the kernel that
+    // writes A; A follows once that kernel's grid is complete.
+    int pre = 0, pre_m0[STAGES], pre_n0[STAGES], pre_kb[STAGES];
+    for (int u = first; u < units && pre < STAGES; u += step) {
+      int m0, n0, z, kb_lo, kb_hi;
+      unit_of(u, m0, n0, z, kb_lo, kb_hi);
+      for (int kb = kb_lo; kb < kb_hi && pre < STAGES; ++kb, ++pre) {
+        pre_m0[pre] = m0;
+        pre_n0[pre] = n0;
+        pre_kb[pre] = kb;
+        issue(pre, kb, m0, n0, false, true);
+      }
+    }
+    pdl_wait();
+    for (int j = 0; j < pre; ++j) issue(j, pre_kb[j], pre_m0[j], pre_n0[j], true, false);
+    int it = 0;  // K blocks issued
+    for (int u = first; u < units && !s_abort; u += step) {
+      int m0, n0, z, kb_lo, kb_hi;
+      unit_of(u, m0, n0, z, kb_lo, kb_hi);
+      for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+        if (it < pre) continue;  // issued above
+        const int s = it % STAGES;
+        if (it >= STAGES && !tc::mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, err)) { s_abort = 1; break; }
+        if (s_abort) break;
+        issue(s, kb, m0, n0, true, true);
       }
     }
     // drain: every issued stage must land before the CTA may exit (the odd CTA's bytes are
@@ -322,6 +349,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp >= 2) {
     // ---- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, columns of half (w-2)/4
     const int q = warp & 3, eh = (warp - 2) >> 2;
+    pdl_wait();  // outputs (and C) belong to this kernel only once the previous grid is done
     int i = 0;
     for (int u = first; u < units; u += step, ++i) {
       int m0, n0, z, kb_lo, kb_hi;
@@ -627,6 +655,8 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__
 // Act[m][n] = fp16(silu(g) * u), g and u the split sums (in split order) of ws[s][m][n] and
 // ws[s][m][N + n]
 __global__ void splitk_swiglu_kernel(const float* ws, int splits, int M, int N, f16* Act, int ldc, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)M * N) return;
   const int m = (int)(i / N), n = (int)(i - (size_t)m * N);
@@ -642,6 +672,8 @@ __global__ void splitk_swiglu_kernel(const float* ws, int splits, int M, int N, 
 // C[m][n] = (add ? C[m][n] : 0) + sum over splits of ws[s][m][n] (in split order) + bias[n]
 __global__ void splitk_reduce_kernel(const float* ws, int splits, int M, int N, const bf16* bias, float* C, int ldc,
                                      int add) {
+  pdl_trigger();
+  pdl_wait();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)M * N) return;
   const int m = (int)(i / N), n = (int)(i - (size_t)m * N);
@@ -657,6 +689,8 @@ __global__ void splitk_reduce_kernel(const float* ws, int splits, int M, int N, 
 
 // EPI_QKV after split-K: one thread per (row, rotation pair), the splits added in order
 __global__ void splitk_qkv_kernel(const float* ws, int splits, int M, int N, const bf16* bias, QkvOut o, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int np = N >> 1;
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (size_t)M * np) return;
@@ -767,11 +801,21 @@ cudaError_t gemm_tc_set_attributes() {
   return set_tc_attr<128, EPI_SWIGLU, 1>();
 }
 
+// QW_PREFILL_PDL=0: launch the prefill kernels without programmatic dependent launch
+bool tc_pdl() {
+  static const bool v = [] {
+    const char* e = std::getenv("QW_PREFILL_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
+
 // One launch of the persistent GEMM: clusters of CL CTAs, as many as fit one per SM (at most
 // one per unit)
 template <int BN, int EPI, int CL>
 static cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb2, const TcEpi& ep,
-                             int M, int N, int K, int* err, const TcGrid& g, float* ws, int nsm, cudaStream_t s) {
+                             int M, int N, int K, int* err, const TcGrid& g, float* ws, int nsm, cudaStream_t s,
+                             bool pdl) {
   const int units = ((g.tiles_m + CL - 1) / CL) * g.tiles_n * g.splits;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(tc::THREADS);
@@ -796,6 +840,14 @@ static cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const
   int clusters = nsm > 0 ? std::min(resident, nsm / CL) : units;
   if (clusters > units || clusters <= 0) clusters = units;
   cfg.gridDim = dim3(clusters * CL);
+  // programmatic dependent launch: the CTAs may start (and request their weights) while the
+  // previous kernel finishes
+  cudaLaunchAttribute attrs[2] = {attr[0], {}};
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = CL > 1 ? attrs : attrs + 1;
+  cfg.numAttrs = (CL > 1 ? 1 : 0) + (pdl ? 1 : 0);
+  if (cfg.numAttrs == 0) cfg.attrs = nullptr;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, CL>, ma, mb, mb2, ep, M, N, K, err, g, ws);
 }
 
@@ -907,9 +959,9 @@ cudaError_t skinny_run(const SkinnyPlan& p, float* part, float* logits, int V, i
 // C[M][N] (fp32, ldc) = / += A[M][K] (fp16, lda) . B[N][K]^T (fp16, ldb) (+ bias[N], bf16)
 template <int BN, int CL>
 static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const TcEpi& ep, int M, int N, int K,
-                               bool add, int* err, const TcGrid& g, float* ws, int nsm, cudaStream_t s) {
-  if (add) return launch_tc<BN, EPI_ADD, CL>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
-  return launch_tc<BN, EPI_STORE, CL>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
+                               bool add, int* err, const TcGrid& g, float* ws, int nsm, cudaStream_t s, bool pdl) {
+  if (add) return launch_tc<BN, EPI_ADD, CL>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s, pdl);
+  return launch_tc<BN, EPI_STORE, CL>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s, pdl);
 }
 
 // Tile width, K splits and CTA pairing of a C[M, N] = A . B^T launch
@@ -949,7 +1001,7 @@ static TcPlan tc_plan(int M, int N, int K, const float* ws, size_t ws_floats, in
 
 cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bias, float* C, int ldc,
                     int M, int N, int K, bool accumulate, int* err, cudaStream_t s, float* ws, size_t ws_floats,
-                    int nsm) {
+                    int nsm, bool pdl) {
   const TcPlan pl = tc_plan(M, N, K, ws, ws_floats, nsm);
   const int bn = pl.bn, splits = pl.splits, tiles_m = pl.tiles_m;
   const bool pair = pl.pair;
@@ -960,23 +1012,24 @@ cudaError_t gemm_tc(const f16* A, int lda, const f16* B, int ldb, const bf16* bi
   const TcGrid g{tiles_m, (N + bn - 1) / bn, splits};
   const bool add = accumulate && splits == 1;
   cudaError_t e;
-  if (bn == 192) e = pair ? launch_gemm<192, 2>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s)
-                          : launch_gemm<192, 1>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
-  else if (bn == 64) e = launch_gemm<64, 1>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
-  else e = pair ? launch_gemm<TC_BN, 2>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s)
-                : launch_gemm<TC_BN, 1>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s);
+  if (bn == 192) e = pair ? launch_gemm<192, 2>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s, pdl)
+                          : launch_gemm<192, 1>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s, pdl);
+  else if (bn == 64) e = launch_gemm<64, 1>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s, pdl);
+  else e = pair ? launch_gemm<TC_BN, 2>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s, pdl)
+                : launch_gemm<TC_BN, 1>(ma, mb, ep, M, N, K, add, err, g, ws, nsm, s, pdl);
   if (e) return e;
   if (splits > 1) {
     const size_t n = (size_t)M * N;
-    splitk_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, bias, C, ldc,
-                                                                     accumulate ? 1 : 0);
+    if ((e = launch_k(splitk_reduce_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, pdl,
+                      (const float*)ws, splits, M, N, bias, C, ldc, accumulate ? 1 : 0)))
+      return e;
   }
   return cudaGetLastError();
 }
 
 // q | k | v = A . B^T (+ bias), rotated and stored in fp16 (QkvOut)
 cudaError_t gemm_tc_qkv(const f16* A, int lda, const f16* B, int ldb, const bf16* bias, int M, int N, int K,
-                        const QkvOut& o, int* err, cudaStream_t s, float* ws, size_t ws_floats, int nsm) {
+                        const QkvOut& o, int* err, cudaStream_t s, float* ws, size_t ws_floats, int nsm, bool pdl) {
   if (o.hd <= 0 || (o.hd & 1) || N != (o.nq + 2 * o.nkv) * o.hd) return cudaErrorInvalidValue;
   const TcPlan pl = tc_plan(M, N, K, ws, ws_floats, nsm);
   CUtensorMap ma, mb;
@@ -986,17 +1039,19 @@ cudaError_t gemm_tc_qkv(const f16* A, int lda, const f16* B, int ldb, const bf16
   const TcGrid g{pl.tiles_m, (N + pl.bn - 1) / pl.bn, pl.splits};
   cudaError_t e;
   if (pl.bn == 192)
-    e = pl.pair ? launch_tc<192, EPI_QKV, 2>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s)
-                : launch_tc<192, EPI_QKV, 1>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
+    e = pl.pair ? launch_tc<192, EPI_QKV, 2>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s, pdl)
+                : launch_tc<192, EPI_QKV, 1>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s, pdl);
   else if (pl.bn == 64)
-    e = launch_tc<64, EPI_QKV, 1>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
+    e = launch_tc<64, EPI_QKV, 1>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s, pdl);
   else
-    e = pl.pair ? launch_tc<TC_BN, EPI_QKV, 2>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s)
-                : launch_tc<TC_BN, EPI_QKV, 1>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s);
+    e = pl.pair ? launch_tc<TC_BN, EPI_QKV, 2>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s, pdl)
+                : launch_tc<TC_BN, EPI_QKV, 1>(ma, mb, mb, ep, M, N, K, err, g, ws, nsm, s, pdl);
   if (e) return e;
   if (pl.splits > 1) {
     const size_t n = (size_t)M * (N / 2);
-    splitk_qkv_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, pl.splits, M, N, bias, o, err);
+    if ((e = launch_k(splitk_qkv_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, pdl,
+                      (const float*)ws, pl.splits, M, N, bias, o, err)))
+      return e;
   }
   return cudaGetLastError();
 }
@@ -1004,7 +1059,7 @@ cudaError_t gemm_tc_qkv(const f16* A, int lda, const f16* B, int ldb, const bf16
 // Act[M][N] (fp16, ldc) = silu(A . Wg^T) * (A . Wu^T)
 cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, int ldb, f16* Act,
                            int ldc, int M, int N, int K, int* err, cudaStream_t s, float* ws, size_t ws_floats,
-                           int nsm) {
+                           int nsm, bool pdl) {
   // 128 output columns per tile (128 gate + 128 up rows); 64 for short prompts, whose gate/up
   // then fills the SMs without K splits
   const int tiles_m = (M + tc::BM - 1) / tc::BM;
@@ -1028,15 +1083,17 @@ cudaError_t gemm_tc_swiglu(const f16* A, int lda, const f16* Wg, const f16* Wu, 
   const TcGrid g{tiles_m, (N + bn / 2 - 1) / (bn / 2), splits};
   cudaError_t e;
   if (bn == 128)
-    e = launch_tc<128, EPI_SWIGLU, 1>(ma, mg, mu, ep, M, N, K, err, g, ws, nsm, s);
+    e = launch_tc<128, EPI_SWIGLU, 1>(ma, mg, mu, ep, M, N, K, err, g, ws, nsm, s, pdl);
   else if (tiles_m >= 2 && nsm >= 2 && gemm_pairs())  // CTA pairs: rank 0 stages gate, rank 1 up
-    e = launch_tc<TC_BN, EPI_SWIGLU, 2>(ma, mg, mu, ep, M, N, K, err, g, ws, nsm, s);
+    e = launch_tc<TC_BN, EPI_SWIGLU, 2>(ma, mg, mu, ep, M, N, K, err, g, ws, nsm, s, pdl);
   else
-    e = launch_tc<TC_BN, EPI_SWIGLU, 1>(ma, mg, mu, ep, M, N, K, err, g, ws, nsm, s);
+    e = launch_tc<TC_BN, EPI_SWIGLU, 1>(ma, mg, mu, ep, M, N, K, err, g, ws, nsm, s, pdl);
   if (e) return e;
   if (splits > 1) {
     const size_t n = (size_t)M * N;
-    splitk_swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, splits, M, N, Act, ldc, err);
+    if ((e = launch_k(splitk_swiglu_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, pdl,
+                      (const float*)ws, splits, M, N, Act, ldc, err)))
+      return e;
   }
   return cudaGetLastError();
 }

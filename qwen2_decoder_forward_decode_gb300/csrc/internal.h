@@ -119,12 +119,17 @@ bool make_map(void* map, const void* base, int rows, int cols, int ld, int box_r
 // boxes of 64 head columns x box_keys positions of one KV head, 128-byte swizzle.
 bool make_map_kv(void* map, const void* base, int hd, int keys, int nkv, int cap, int box_keys);
 cudaError_t gemm_tc_set_attributes();
+// whether the prefill's tensor-core path launches its kernels with programmatic dependent
+// launch (QW_PREFILL_PDL=0 turns it off)
+bool tc_pdl();
 // fp16 operands (A activations, B weights), fp32 accumulate; bias bf16
 // ws (optional): fp32 workspace of ws_floats for split-K partial tiles, used when the
 // output has too few 128x256 tiles for nsm SMs
+// pdl: programmatic dependent launch after the previous kernel of the stream; the kernels then
+// request B (which no kernel of the stream may be writing: weights) before that kernel ends
 cudaError_t gemm_tc(const __half* A, int lda, const __half* B, int ldb, const __nv_bfloat16* bias,
                     float* C, int ldc, int M, int N, int K, bool accumulate, int* err,
-                    cudaStream_t s, float* ws = nullptr, size_t ws_floats = 0, int nsm = 0);
+                    cudaStream_t s, float* ws = nullptr, size_t ws_floats = 0, int nsm = 0, bool pdl = false);
 // Outputs of the fused q/k/v projection (columns q | k | v, each head's columns in RoPE-pair
 // order as the weights' rows are): + bias, rotation of q and k rows m at position pos0 + m,
 // q times qscale to Qh [M][nq*hd] (fp16), k and v to the layer's fp16 caches [nkv][cap][hd]
@@ -138,10 +143,10 @@ struct QkvOut {
 };
 cudaError_t gemm_tc_qkv(const __half* A, int lda, const __half* B, int ldb, const __nv_bfloat16* bias, int M, int N,
                         int K, const QkvOut& o, int* err, cudaStream_t s, float* ws = nullptr, size_t ws_floats = 0,
-                        int nsm = 0);
+                        int nsm = 0, bool pdl = false);
 cudaError_t gemm_tc_swiglu(const __half* A, int lda, const __half* Wg, const __half* Wu, int ldb,
                            __half* Act, int ldc, int M, int N, int K, int* err, cudaStream_t s, float* ws = nullptr,
-                           size_t ws_floats = 0, int nsm = 0);
+                           size_t ws_floats = 0, int nsm = 0, bool pdl = false);
 
 // ---- megastep.cu (one persistent kernel per decode step of one sequence, bf16 models) ----
 struct MegaLaunch {

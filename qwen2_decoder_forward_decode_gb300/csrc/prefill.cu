@@ -51,6 +51,8 @@ __global__ void norm_rows_kernel(const float* X, const T* gain, int H, float eps
 // of X; fp16 range errors gathered per lane and raised once.
 template <int MAXV>
 __global__ void norm_rows_h_kernel(const float* X, const bf16* gain, int T, int H, float eps, f16* Y, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= T) return;
   const int nv = H >> 7;  // float4 per lane
@@ -86,6 +88,8 @@ __global__ void norm_rows_h_kernel(const float* X, const bf16* gain, int T, int 
 // SM has rows.
 __global__ void __launch_bounds__(128) norm_row_block_h_kernel(const float* X, const bf16* gain, int H, float eps,
                                                                f16* Y, int* err) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float scratch[32];
   const int row = blockIdx.x;
   const float4* x = reinterpret_cast<const float4*>(X + (size_t)row * H);
@@ -121,12 +125,14 @@ __global__ void __launch_bounds__(128) norm_row_block_h_kernel(const float* X, c
 static void norm_rows_h(const float* X, const bf16* gain, int T_, int H, float eps, f16* Y, int* err, cudaStream_t s,
                         int nsm) {
   const bool vec = H % 128 == 0 && ((uintptr_t)gain & 7) == 0;
+  // programmatic dependent launch (the kernels wait for the previous grid before reading X)
+  const bool pdl = tc_pdl();
   if (vec && T_ < 4 * nsm && H <= 4096) {
-    norm_row_block_h_kernel<<<T_, 128, 0, s>>>(X, gain, H, eps, Y, err);
+    launch_k(norm_row_block_h_kernel, dim3(T_), dim3(128), 0, s, pdl, X, gain, H, eps, Y, err);
   } else if (vec && H <= 128 * 12) {
-    norm_rows_h_kernel<12><<<(T_ + 7) / 8, 256, 0, s>>>(X, gain, T_, H, eps, Y, err);
+    launch_k(norm_rows_h_kernel<12>, dim3((T_ + 7) / 8), dim3(256), 0, s, pdl, X, gain, T_, H, eps, Y, err);
   } else if (vec && H <= 128 * 32) {
-    norm_rows_h_kernel<32><<<(T_ + 7) / 8, 256, 0, s>>>(X, gain, T_, H, eps, Y, err);
+    launch_k(norm_rows_h_kernel<32>, dim3((T_ + 7) / 8), dim3(256), 0, s, pdl, X, gain, T_, H, eps, Y, err);
   } else {
     norm_rows_kernel<bf16, f16><<<T_, 256, 0, s>>>(X, gain, H, eps, Y, err);
   }
@@ -629,6 +635,10 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
                               const int* ids, int T_, int pos0, const float2* rope, void* kcache,
                               const PrefillBufs& b, int* err, cudaStream_t s) {
   const int H = d.H, qd = d.nq * d.hd, kvd = d.nkv * d.hd, Wd = qd + 2 * kvd;
+  // Every kernel after the embedding is launched with programmatic dependent launch: it starts
+  // while the previous one drains, requests its weights, and waits for that grid before it
+  // touches activations.
+  const bool pdl = tc_pdl();
   embed_rows_kernel<bf16><<<T_, 256, 0, s>>>((const bf16*)embed, d.V, H, ids, b.X, err);
   const size_t layer_stride = (size_t)d.nkv * d.cap * d.hd;
   cudaError_t e;
@@ -649,10 +659,10 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
       // bias, RoPE and the K/V append in the projection's epilogue; q in fp16, scaled into
       // base-2 scores, in the (still free) SwiGLU operand buffer
       const QkvOut o{b.Ah, kc, vc, rope, 1.4426950408889634f / sqrtf((float)d.hd), d.nq, d.nkv, d.hd, pos0, d.cap};
-      if ((e = gemm_tc_qkv(b.Xh, H, wqkv, H, bqkv, T_, Wd, H, o, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+      if ((e = gemm_tc_qkv(b.Xh, H, wqkv, H, bqkv, T_, Wd, H, o, err, s, b.ws, b.ws_floats, d.nsm, pdl))) return e;
       if ((e = attn_prefill_tc(d, T_, pos0, b.Ah, kc, vc, b.Oh, err, s))) return e;
     } else {
-      if ((e = gemm_tc(b.Xh, H, wqkv, H, bqkv, b.Y, Wd, T_, Wd, H, false, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+      if ((e = gemm_tc(b.Xh, H, wqkv, H, bqkv, b.Y, Wd, T_, Wd, H, false, err, s, b.ws, b.ws_floats, d.nsm, pdl))) return e;
       rope_kv_kernel<f16><<<T_, 256, 0, s>>>(b.Y, T_, d.nq, d.nkv, d.hd, pos0, d.cap, rope, b.Q, kc, vc, err, true);
       const bool mma = kind != PA_SIMT && attn_prefill_mma(d, b.Q, T_, pos0, kc, vc, b.Oh, s, &e);
       if (mma && e) return e;
@@ -663,12 +673,12 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
                                                                                                      err);
       }
     }
-    if ((e = gemm_tc(b.Oh, qd, (const f16*)w.wo16, qd, nullptr, b.X, H, T_, H, qd, true, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+    if ((e = gemm_tc(b.Oh, qd, (const f16*)w.wo16, qd, nullptr, b.X, H, T_, H, qd, true, err, s, b.ws, b.ws_floats, d.nsm, pdl))) return e;
     norm_rows_h(b.X, (const bf16*)w.post_norm, T_, H, d.eps, b.Xh, err, s, d.nsm);
     if ((e = gemm_tc_swiglu(b.Xh, H, (const f16*)w.wg16, (const f16*)w.wu16, H, b.Ah, d.I, T_, d.I, H, err, s, b.ws,
-                              b.ws_floats, d.nsm)))
+                              b.ws_floats, d.nsm, pdl)))
       return e;
-    if ((e = gemm_tc(b.Ah, d.I, (const f16*)w.wd16, d.I, nullptr, b.X, H, T_, H, d.I, true, err, s, b.ws, b.ws_floats, d.nsm))) return e;
+    if ((e = gemm_tc(b.Ah, d.I, (const f16*)w.wd16, d.I, nullptr, b.X, H, T_, H, d.I, true, err, s, b.ws, b.ws_floats, d.nsm, pdl))) return e;
   }
   return cudaGetLastError();
 }
