@@ -4,7 +4,8 @@
 //
 // A persistent CTA per SM computes 128 x BN tiles into two TMEM fp32 accumulators:
 //   warp 0 (one lane)  TMA producer: 128-byte-swizzled A and B tiles of 64 K-elements into
-//                      a STAGES-deep shared-memory ring (mbarrier full/empty pairs)
+//                      a shared-memory ring of 4 to 8 stages, as many as fit (mbarrier
+//                      full/empty pairs)
 //   warp 1 (one lane)  MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16,
 //                      four per stage; tcgen05.commit frees a stage when its MMAs retire
 //   warps 2..9         epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows; warps w and
@@ -27,7 +28,7 @@ namespace qw {
 
 namespace tc {
 
-constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int THREADS = 320;  // producer, MMA issuer, eight epilogue warps
 
 }  // namespace tc
@@ -66,12 +67,16 @@ struct TcGrid {
 };
 
 template <int BN, int CL>
-__host__ __device__ constexpr int tc_stages() {
-  return CL == 2 ? 6 : tc::STAGES;
-}
-template <int BN, int CL>
 __host__ __device__ constexpr size_t tc_stage_bytes() {
   return (size_t)tc::BM * tc::BK * 2 + (size_t)(CL == 2 ? BN / 2 : BN) * tc::BK * 2;
+}
+// as many stages as fit beside the barriers, the epilogue scratch and the alignment slack (at
+// most 8): narrow tiles keep more weight bytes in flight
+template <int BN, int CL>
+__host__ __device__ constexpr int tc_stages() {
+  return (232448 - 256 - 8 * 32 * 33 * 4 - 1024) / tc_stage_bytes<BN, CL>() < 8
+             ? (int)((232448 - 256 - 8 * 32 * 33 * 4 - 1024) / tc_stage_bytes<BN, CL>())
+             : 8;
 }
 // ring, barriers (256 B), epilogue scratch (8 warps x 32 x 33 floats), 1024-B alignment slack
 template <int BN, int CL>
