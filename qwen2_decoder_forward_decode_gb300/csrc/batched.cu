@@ -305,17 +305,17 @@ cudaError_t batched_step(const BatchedCtx& c, cudaStream_t s) {
       return e;
     // attention leaves its chunk partials; the merge kernel writes the fp16 rows of the o GEMM
     if (c.attn_mma)
-      e = launch_attn_decode_mma(d.nq, d.nkv, d.hd, c.attn_nsplit, d.attn_chunk_min, c.q, kc0,
+      e = launch_attn_decode_mma(d.nq, d.nkv, d.hd, c.attn_nsplit, c.attn_chunk, c.q, kc0,
                                  kc0 + (size_t)d.nkv * d.cap * d.hd, c.kv_seq_elems, d.cap, c.pos, c.active, S,
                                  c.attn_ws, tl(), s, pdl);
     else
-      e = launch_attn_batched(d.nq, d.nkv, d.hd, c.attn_nsplit, d.attn_chunk_min, c.attn_smem, c.q, kc0,
+      e = launch_attn_batched(d.nq, d.nkv, d.hd, c.attn_nsplit, c.attn_chunk, c.attn_smem, c.q, kc0,
                               kc0 + (size_t)d.nkv * d.cap * d.hd, c.kv_seq_elems, d.cap, c.pos, c.active, S, c.O16,
                               c.attn_ws, tl(), s, /*merge=*/0);
     if (e) return e;
     if ((e = launch_k(bmerge_kernel, dim3(d.nq, S), dim3(128), 0, s, pdl, (const float*)c.attn_ws,
                       attn_batched_part_floats(d.nq, d.hd, c.attn_nsplit), d.nq, d.hd, c.attn_nsplit,
-                      d.attn_chunk_min, (const int*)c.pos, c.active, c.O16, tl())))
+                      c.attn_chunk, (const int*)c.pos, c.active, c.O16, tl())))
       return e;
     if ((e = skinny_run(pl.o, c.part, nullptr, 0, S, c.active, nullptr, c.err, tl(), s))) return e;
     if ((e = launch_k(bresid_norm_kernel<f16>, rn_grid, rn_block, 0, s, pdl, (const float*)c.part, pl.o.splits,

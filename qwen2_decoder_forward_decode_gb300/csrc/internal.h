@@ -221,6 +221,7 @@ struct BatchedCtx {
   void* attn_ws;                    // attn_batched_workspace_bytes(.., S)
   size_t attn_smem;
   int attn_nsplit;                  // context chunks per sequence and KV head
+  int attn_chunk;                   // fewest positions per chunk
   bool attn_mma;                    // tensor-core attention (else CUDA cores)
   unsigned long long* tl;           // timeline: 3 slots per launch, or null
 };
