@@ -337,7 +337,8 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_decode_kernel(const AttnArg
 //
 // One CTA per (KV head, context chunk, sequence). The g query heads of the KV head are the
 // rows of one m16n8k16 A operand (fp16 q scaled by 1/sqrt(hd), rows >= g zero). Key/value
-// tiles of 64 positions arrive by cp.async into two buffers (rows padded by 16 bytes); each
+// tiles of 64 positions arrive by cp.async into two buffers (rows padded by 16 bytes; the
+// first two tiles are requested before the dependency wait, but for the newest row); each
 // of the four warps takes 16 positions of a tile: S = Q K^T as two n-tiles, a running
 // maximum and sum per row, O += P V with the value B fragments loaded by ldmatrix.trans.
 // The warps' states are combined (log-sum-exp) in shared memory into the chunk's partial
@@ -397,15 +398,18 @@ __global__ void __launch_bounds__(DM_WARPS * 32) attn_decode_mma_kernel(const De
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  const bool newest_in_first = newest >= 0 && newest < DM_K;
-  load_tile(0, 0, newest_in_first ? newest : -1);
+  // the first two tiles (both buffers) are requested before the wait, all but the newest row
+  const int pre = ntiles < 2 ? ntiles : 2;
+  const bool newest_in_pre = newest >= 0 && newest < pre * DM_K;
+  load_tile(0, 0, newest_in_pre ? newest : -1);
+  if (pre == 2) load_tile(1, 1, newest_in_pre ? newest : -1);
   pdl_wait();
   pdl_trigger();
   tl_stamp(a.tl, 1);
-  if (newest_in_first) {  // its own copy group, after the rest of tile 0
+  if (newest_in_pre) {  // its own copy group, after the rest of the preloaded tiles
     for (int i = tid; i < 2 * (HD / 8); i += DM_WARPS * 32) {
       const int which = i >= HD / 8, c8 = i - which * (HD / 8);
-      f16* dst = (which ? Vs : Ks) + (size_t)newest * KS + c8 * 8;
+      f16* dst = (which ? Vs : Ks) + (size_t)newest * KS + c8 * 8;  // (buffer newest / DM_K)
       cp_async16(dst, (which ? V : K) + (size_t)newest * HD + c8 * 8);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -431,8 +435,8 @@ __global__ void __launch_bounds__(DM_WARPS * 32) attn_decode_mma_kernel(const De
   const int kw = 16 * warp;  // this warp's positions within a tile
   for (int t = 0; t < ntiles; ++t) {
     const int buf = t & 1;
-    if (t + 1 < ntiles) {
-      load_tile(t + 1, buf ^ 1, -1);  // (the newest row lies in tile 0 or is loaded here after the wait)
+    if (t + 1 < ntiles && t + 1 >= pre) {
+      load_tile(t + 1, buf ^ 1, -1);  // (the newest row lies in a preloaded tile or is loaded here after the wait)
       asm volatile("cp.async.wait_group 1;" ::: "memory");
     } else {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
