@@ -14,7 +14,7 @@ TFLOP/s against the tensor peak, then 255 decode steps at 4096+ positions) and
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
-``--impl reference`` times the CPU oracle (float64 numpy) on a bounded sample of the same
+``--impl reference`` times the CPU oracle (its float32 numpy mode) on a bounded sample of the same
 workload, on the host cores. Under torchrun every rank runs its own replica of the batch-1
 workloads (batch-1 decode does not shard; no collective is used on the data path), the
 16 batched sequences are split over the ranks (each with a full weight replica; token ids
@@ -157,16 +157,38 @@ def job_throughput(units_per_rank, ws, max_seconds):
     return units_per_rank * ws / max_seconds
 
 
-def oracle_decode_sample(s, wl, n_decode, warmup=0):
-    """Time the CPU oracle: one untimed prefill of the workload's prompt, then decode
-    steps; returns (seconds per decode step list, threads)."""
+def host_cpu():
+    """The host CPU's model, from /proc/cpuinfo (x86: model name; Arm: implementer/part)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return "unknown"
+    for line in info:
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    fields = {}
+    for line in info:
+        if ":" in line:
+            k, v = (x.strip() for x in line.split(":", 1))
+            fields.setdefault(k, v)
+    if "CPU implementer" in fields:
+        return f"arm implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    return "unknown"
+
+
+def oracle_sample(s, wl, n_decode, warmup=0, dtype=np.float32):
+    """Time the CPU oracle in its float32 mode (numpy BLAS on every host core; the precision
+    of the pages' own numpy model): the workload's prompt prefill (TTFT), then decode steps.
+    Returns (prefill seconds, seconds per decode step list, threads)."""
     import oracle
     w = make_weights(s)
     prompt = make_prompt(s, wl.prompt_len)
-    om = oracle.OracleModel(oracle.OracleConfig.from_shape(s), w)
+    om = oracle.OracleModel(oracle.OracleConfig.from_shape(s), w, dtype=dtype)
     del w
     cache = oracle.KVCache(s.n_layers)
+    t0 = time.perf_counter()
     t, _ = oracle.step(om, list(prompt), np.arange(len(prompt)), cache)
+    ttft = time.perf_counter() - t0
     seq = list(prompt) + [t]
     times = []
     for i in range(warmup + n_decode):
@@ -176,7 +198,7 @@ def oracle_decode_sample(s, wl, n_decode, warmup=0):
         seq.append(t)
         if i >= warmup:
             times.append(dt)
-    return times, os.cpu_count()
+    return ttft, times, os.cpu_count()
 
 
 def run_reference(args):
@@ -185,19 +207,22 @@ def run_reference(args):
         return
     wl = WORKLOADS[WORKLOAD]
     s = SHAPES[wl.shape]
-    times, cores = oracle_decode_sample(s, wl, args.steps, warmup=args.warmup)
+    ttft, times, cores = oracle_sample(s, wl, args.steps, warmup=args.warmup)
     total = sum(times)
     value = len(times) / total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000 * total / len(times), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "Qwen2.5-1.5B shape, bs1, 128-token prompt, KV cache 2048, "
-                               "greedy decode; one step = one oracle decode step after an untimed prefill",
+                               "greedy decode; one step = one oracle decode step after the prefill (timed apart: "
+                               "cpu_baseline.ttft_ms)",
                    "global_batch": 1, "seq_len": wl.prompt_len},
-        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{len(times)} decode steps at context {wl.prompt_len}+, float64 numpy"},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "cpu": host_cpu(),
+                         "ttft_ms": 1000 * ttft,
+                         "sample": f"{len(times)} decode steps at context {wl.prompt_len}+ after the "
+                                   f"{wl.prompt_len}-token prefill (timed as ttft_ms), float32 numpy (BLAS)"},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -452,10 +477,11 @@ def run_native(args):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        times, cores = oracle_decode_sample(s, wl, 3)
+        ttft, times, cores = oracle_sample(s, wl, 5)
         cpu = {"value": len(times) / sum(times), "unit": "tok/s", "cores": cores, "kind": "oracle",
-               "sample": "3 float64-numpy decode steps after an untimed 128-token prefill "
-                         "(same weights, prompt and cache length)"}
+               "cpu": host_cpu(), "ttft_ms": 1000 * ttft,
+               "sample": f"the {wl.prompt_len}-token prefill (ttft_ms) and 5 decode steps, float32 numpy "
+                         "(BLAS, every host core; same weights, prompt and cache length)"}
 
     if rank == 0:
         line = {

@@ -1,5 +1,9 @@
 """Plain CPU oracle of the Qwen2 decoder forward pass, in float64.
 
+(A float32 mode, ``OracleModel(..., dtype=np.float32)``, runs the same steps in the precision
+of [LSA]'s numpy model code, whose arrays are all float32. It only serves as the timed CPU
+baseline; parity always uses float64.)
+
 TEST INFRASTRUCTURE ONLY. Only the tests, the package's smoke check and the bench's
 CPU-baseline / reference legs may import this module. It shares no code with the CUDA
 library: the only thing both sides use is the seeded input generator in ``synth``.
@@ -31,6 +35,7 @@ Readings where the pages are garbled or silent:
     embedding matrix (tied) unless an untied one is given.
   * Greedy argmax takes the lowest index among equal maxima.
 """
+import math
 from dataclasses import dataclass
 
 import numpy as np
@@ -58,11 +63,13 @@ class OracleConfig:
 
 
 class OracleModel:
-    """Weights held as float64 copies of the given arrays (bf16 values are exact in f64)."""
+    """Weights held as float64 copies of the given arrays (bf16 values are exact in f64),
+    or float32 copies with dtype=np.float32 (every activation then stays float32)."""
 
-    def __init__(self, cfg: OracleConfig, weights: dict):
+    def __init__(self, cfg: OracleConfig, weights: dict, dtype=np.float64):
         self.cfg = cfg
-        self.w = {k: np.asarray(v, dtype=np.float64) for k, v in weights.items()}
+        self.dtype = np.dtype(dtype)
+        self.w = {k: np.asarray(v, dtype=self.dtype) for k, v in weights.items()}
 
     def layer(self, i, name):
         return self.w.get(f"model.layers.{i}.{name}")
@@ -107,7 +114,7 @@ def rope_rotate(x, positions, theta):
     hd = x.shape[0]
     half = hd // 2
     ang = np.outer(rope_frequencies(hd, theta), np.asarray(positions, dtype=np.float64))
-    c, s = np.cos(ang), np.sin(ang)
+    c, s = np.cos(ang).astype(x.dtype, copy=False), np.sin(ang).astype(x.dtype, copy=False)  # (f32 mode)
     re, im = x[:half], x[half:]
     out = np.empty_like(x)
     out[:half] = re * c - im * s
@@ -134,7 +141,7 @@ def attend_one_head(q, K, V, q_positions, d_k):
     q: [hd, T] rotated queries at absolute positions q_positions; K, V: [hd, Ttot] keys
     (rotated) and values for positions 0..Ttot-1. Returns [hd, T].
     """
-    scores = (q.T @ K) / np.sqrt(d_k)                      # [T, Ttot]
+    scores = (q.T @ K) / math.sqrt(d_k)                    # [T, Ttot] (a Python float keeps f32 mode f32)
     key_pos = np.arange(K.shape[1])
     masked = key_pos[None, :] > np.asarray(q_positions)[:, None]
     scores = np.where(masked, MASK_VALUE, scores)

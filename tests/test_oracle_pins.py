@@ -476,3 +476,25 @@ def test_weights_are_deterministic_and_layer_subsets_agree():
     wq = a["model.layers.0.self_attn.q_proj.weight"]
     assert abs(wq.std() - 0.02) < 0.001
     np.testing.assert_array_equal(round_to_bf16(wq), wq)
+
+
+# --- float32 mode (the timed CPU baseline) ----------------------------------------------
+
+@pytest.mark.parametrize("shape", ["tiny", "small_f32"])
+def test_float32_mode_stays_float32_and_follows_float64(shape):
+    # The float32 mode runs the float64 oracle's steps in the precision of the numpy model
+    # code on "LLM Speedrun: Architecture" (every array float32). It must keep its arrays
+    # float32 (else it would not time float32 BLAS) and agree with the pinned float64 oracle
+    # to float32 rounding: the same greedy tokens under teacher forcing, logits within 1e-4 of
+    # their spread.
+    m64, w, s = tiny_model(shape)
+    m32 = OracleModel(OracleConfig.from_shape(s), w, dtype=np.float32)
+    assert all(v.dtype == np.float32 for v in m32.w.values())
+    prompt = make_prompt(s, 12)
+    t64, z64 = oracle.generate(m64, prompt, 6)
+    t32, z32 = oracle.generate(m32, prompt, 6, feed=t64[:-1])
+    assert all(z.dtype == np.float32 for z in z32)
+    assert all(z.dtype == np.float64 for z in z64)
+    for a, b in zip(z64, z32):
+        assert np.max(np.abs(a - b)) <= 1e-4 * np.std(a)
+    assert t32 == t64
