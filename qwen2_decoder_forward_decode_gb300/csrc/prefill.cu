@@ -629,8 +629,9 @@ static int prefill_attention_kind() {
 }
 
 // bf16 models: every projection on the tensor cores with fp16 operands (fp16 copies of the
-// bf16 weights are exact; fp16 activations round 8x finer than bf16), fp32 accumulation,
-// fp32 residual stream, fp16 KV cache.
+// bf16 weights are exact from 2^-14 to 65504 in magnitude, smaller ones round among the fp16
+// subnormals; fp16 activations round 8x finer than bf16), fp32 accumulation, fp32 residual
+// stream, fp16 KV cache.
 static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void* embed,
                               const int* ids, int T_, int pos0, const float2* rope, void* kcache,
                               const PrefillBufs& b, int* err, cudaStream_t s) {
