@@ -229,18 +229,39 @@ def run_reference(args):
 
 
 def prefill_launches(s, T, nsm=152):
-    """Kernels one prefill of T tokens launches on a bf16 model: embedding, per layer two
-    norms, RoPE/KV append, attention and the tensor-core GEMMs (q, k, v, o, gate/up, down),
-    each followed by a split-K reduce when its 128x256 tile grid leaves more than half the
-    SMs idle, then the LM head."""
-    qd, kvd, H, I = s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim, s.hidden, s.intermediate
+    """Kernels one prefill of T tokens launches on a bf16 model (the tensor-core path): the
+    embedding; per layer two RMSNorms, the fused q/k/v GEMM (bias, RoPE and the KV append in
+    its epilogue), attention, o_proj, gate/up (SwiGLU in its epilogue) and down, each GEMM
+    followed by a split-K reduce where the planner splits K; then the LM head. Mirrors the
+    GEMM planner: 64-column tiles (128 for gate/up) up to two row tiles, else 256 or 192;
+    K split when the tiles leave more than half the SMs idle (gate/up: fewer than half the
+    SMs' worth of tiles), at least two K blocks per split."""
+    H, I = s.hidden, s.intermediate
+    qd, Wd = s.n_heads * s.head_dim, (s.n_heads + 2 * s.n_kv_heads) * s.head_dim
     mt = (T + 127) // 128
-    def gemm(n_out, wide=256):
-        return 1 + (1 if 2 * ((n_out + wide - 1) // wide) * mt < nsm else 0)
-    per_layer = 4 + gemm(qd) + 2 * gemm(kvd) + gemm(H)  # norms, rope, attention; q, k, v, o
-    gu_tiles = ((I + 127) // 128) * mt
-    per_layer += 1 + (1 if gu_tiles < nsm else 0)  # gate/up (SwiGLU epilogue or split reduce)
-    per_layer += gemm(H)  # down
+
+    def cdiv(a, b):
+        return -(-a // b)
+
+    def splits(tiles, k):
+        n = min(16, nsm // tiles, cdiv(k, 64) // 2)
+        return n >= 2
+
+    def gemm(n, k):
+        if mt <= 2:
+            bn = 64
+        else:
+            def rounds(w):
+                return cdiv(mt * cdiv(n, w), nsm)
+            bn = 192 if rounds(192) * 192 < rounds(256) * 256 else 256
+        tiles = cdiv(n, bn) * mt
+        return 1 + (1 if 2 * tiles < nsm and splits(tiles, k) else 0)
+
+    def glu(n, k):
+        tiles = cdiv(n, 64 if mt <= 2 else 128) * mt
+        return 1 + (1 if tiles < nsm // 2 and splits(tiles, k) else 0)
+
+    per_layer = 2 + 1 + gemm(Wd, H) + gemm(H, qd) + glu(I, H) + gemm(H, I)
     return 1 + s.n_layers * per_layer + 1
 
 

@@ -39,3 +39,13 @@ def test_prefill_flops(shape, P, flop):
 def test_decode_launches_per_token():
     # embedding, five kernels per layer (q/k/v, attention, o_proj, gate/up, down), LM head
     assert bench.decode_launches_per_token(SHAPES["1p5b"]) == 1 + 5 * 28 + 1
+
+
+def test_prefill_launch_count_matches_the_recorded_launch_lists():
+    # The ncu launch lists of a 128-token and of a 4096-token prefill of the 1.5B shape
+    # show, per layer: two RMSNorms, the fused q/k/v GEMM, attention, o_proj, gate/up and
+    # down; at 128 tokens q/k/v, o_proj and down each add a split-K reduce (gate/up does
+    # not). One embedding launch before the layers, one LM-head launch after them.
+    s = SHAPES["1p5b"]
+    assert bench.prefill_launches(s, 128) == 1 + s.n_layers * 10 + 1
+    assert bench.prefill_launches(s, 4096) == 1 + s.n_layers * 7 + 1
