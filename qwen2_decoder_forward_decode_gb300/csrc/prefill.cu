@@ -616,16 +616,13 @@ static bool attn_prefill_mma(const Dims& d, const float* Q, int T_, int pos0, co
 }
 
 // Prefill attention of the bf16 models: QW_PREFILL_ATTN=tc (tcgen05, the default), mma
-// (mma.sync) or simt (CUDA cores), for comparison.
+// (mma.sync) or simt (CUDA cores), for comparison; read at every prefill.
 enum { PA_TC, PA_MMA, PA_SIMT };
 static int prefill_attention_kind() {
-  static const int v = [] {
-    const char* e = std::getenv("QW_PREFILL_ATTN");
-    if (e && !std::strcmp(e, "mma")) return (int)PA_MMA;
-    if (e && !std::strcmp(e, "simt")) return (int)PA_SIMT;
-    return (int)PA_TC;
-  }();
-  return v;
+  const char* e = std::getenv("QW_PREFILL_ATTN");
+  if (e && !std::strcmp(e, "mma")) return PA_MMA;
+  if (e && !std::strcmp(e, "simt")) return PA_SIMT;
+  return PA_TC;
 }
 
 // bf16 models: every projection on the tensor cores with fp16 operands (fp16 copies of the
@@ -640,6 +637,7 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
   // while the previous one drains, requests its weights, and waits for that grid before it
   // touches activations.
   const bool pdl = tc_pdl();
+  const int kind = prefill_attention_kind();
   embed_rows_kernel<bf16><<<T_, 256, 0, s>>>((const bf16*)embed, d.V, H, ids, b.X, err);
   const size_t layer_stride = (size_t)d.nkv * d.cap * d.hd;
   cudaError_t e;
@@ -655,7 +653,6 @@ static cudaError_t prefill_tc(const Dims& d, const LayerPtrs* layers, const void
       return cudaErrorInvalidValue;
     const f16* wqkv = (const f16*)w.wq16;
     const bf16* bqkv = (const bf16*)w.bqkv;
-    const int kind = prefill_attention_kind();
     if (kind == PA_TC && attn_prefill_tc_supported(d.hd) && d.I >= qd) {
       // bias, RoPE and the K/V append in the projection's epilogue; q in fp16, scaled into
       // base-2 scores, in the (still free) SwiGLU operand buffer
