@@ -30,6 +30,8 @@
 // Each CTA starts at its own key block and wraps around, so that CTAs do not all read the
 // same lines at the same time.
 // Q arrives in fp16, already multiplied by log2(e) / sqrt(d), so scores are in base 2.
+// Launched with programmatic dependent launch (the prefill), the CTAs may start while the
+// q/k/v projection finishes; they wait for it before reading anything.
 // Every mbarrier wait is bounded: on expiry the thread flags ERR_TIMEOUT, the CTA stops
 // issuing work, waits (bounded) for what it issued, and releases its TMEM.
 #include <cuda.h>

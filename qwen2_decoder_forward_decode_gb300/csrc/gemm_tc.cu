@@ -9,11 +9,13 @@
 //   warp 1 (one lane)  MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16,
 //                      four per stage; tcgen05.commit frees a stage when its MMAs retire
 //   warps 2..9         epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows; warps w and
-//                      w + 4 split the columns), fused bias / residual-add / SwiGLU,
-//                      coalesced stores to global memory, while the next tile accumulates
-//                      in the other buffer
+//                      w + 4 split the columns), fused bias / residual-add / SwiGLU / q|k|v
+//                      RoPE and KV append, stores to global memory, while the next tile
+//                      accumulates in the other buffer
 // With two or more row tiles, CTA pairs (clusters of two) run the same roles on 256 x BN
 // tiles with the pair form of the MMA (cta_group::2), each CTA staging half of B.
+// Launched with programmatic dependent launch (the prefill), a CTA requests the B (weight)
+// tiles of its first stages before it waits for the previous kernel, then A.
 // Every mbarrier wait is bounded (clock budget); on expiry the CTA flags ERR_TIMEOUT,
 // stops issuing work, and still releases its TMEM.
 #include <cuda.h>
@@ -52,9 +54,9 @@ struct TcEpi {
 // BN columns per tile. For EPI_SWIGLU the B ring holds BN/2 gate rows then BN/2 up rows of
 // the same output columns, so one N = BN product leaves gate in accumulator columns
 // [0, BN/2) and up in [BN/2, BN).
-// Split-K (splits > 1, EPI_STORE / EPI_ADD / EPI_SWIGLU): unit z of a tile covers a
-// contiguous range of K blocks and stores its raw fp32 tile to ws[z]; the reduce kernels then
-// add the splits in order and apply the bias, the residual add or SwiGLU (deterministic).
+// Split-K (splits > 1): unit z of a tile covers a contiguous range of K blocks and stores its
+// raw fp32 tile to ws[z]; a reduce kernel then adds the splits in order and applies the bias,
+// the residual add, SwiGLU, or the q|k|v bias, RoPE and KV append (deterministic).
 // CL = 2: a cluster of two CTAs (one per SM) computes a 256 x BN tile with the pair form of
 // the MMA (tcgen05 cta_group::2, M = 256): each CTA stages its 128 rows of A and its half of
 // the BN rows of B, so an SM takes in a third fewer operand bytes per FLOP, and the stage

@@ -4,8 +4,12 @@
 // Row-major activations [T][features] in fp32. Per layer:
 //   norm rows -> Q/K/V GEMMs (+bias) -> RoPE + KV-cache write -> causal GQA attention ->
 //   o_proj GEMM (+= residual) -> norm rows -> gate/up GEMMs -> SwiGLU -> down GEMM (+=).
-// This translation unit holds the CUDA-core (SIMT) versions: exact fp32 arithmetic on
-// any shape, used by the fp32 models and as the general path.
+// This translation unit holds the CUDA-core (SIMT) versions (exact fp32 arithmetic on any
+// shape: the fp32 models and the general path), the row kernels, the mma.sync attention,
+// and prefill_tc, the bf16 models' chain on the tensor cores: RMSNorm -> one q|k|v GEMM with
+// bias, RoPE and the KV append in its epilogue -> tcgen05 attention -> o_proj GEMM
+// (+= residual) -> RMSNorm -> gate/up GEMM with SwiGLU in its epilogue -> down GEMM (+=),
+// every kernel after the embedding launched with programmatic dependent launch.
 #include "common.cuh"
 #include "internal.h"
 
