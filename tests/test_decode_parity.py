@@ -310,6 +310,28 @@ def test_decode_is_deterministic():
         m.close()
 
 
+@pytest.mark.parametrize("P", [128, 600])
+def test_prefill_is_deterministic(P):
+    """Two prefills of the same prompt give bit-identical logits and token: the tensor-core
+    chain (split-K GEMMs at 128 tokens, CTA-pair GEMMs at 600, the tcgen05 attention,
+    programmatic dependent launch between every kernel) reduces in a fixed order and adds no
+    floats atomically."""
+    s = SHAPES["1p5b"]
+    w = make_weights(s)
+    prompt = make_prompt(s, P)
+    m = _model("1p5b", w, P + 8)
+    try:
+        ta = m.prefill(prompt)
+        za = np.array(m.logits(), copy=True)
+        m.reset()
+        tb = m.prefill(prompt)
+        zb = np.array(m.logits(), copy=True)
+        assert ta == tb
+        np.testing.assert_array_equal(za, zb)
+    finally:
+        m.close()
+
+
 def test_fault_injection_at_decode_leaves_the_model_usable(monkeypatch):
     """QW_FAULT=launch fails a decode call with QW_ERR_FAULT_INJECTED before any launch;
     the sequence keeps its length and the next call continues it exactly."""
