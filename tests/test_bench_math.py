@@ -49,3 +49,24 @@ def test_prefill_launch_count_matches_the_recorded_launch_lists():
     s = SHAPES["1p5b"]
     assert bench.prefill_launches(s, 128) == 1 + s.n_layers * 10 + 1
     assert bench.prefill_launches(s, 4096) == 1 + s.n_layers * 7 + 1
+
+
+def test_reference_arm_line_keeps_the_contract():
+    # `bench.py --impl reference` runs the CPU oracle (float32 mode) on the 1.5B workload and
+    # prints one JSON line with the contract's keys; no GPU is involved.
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "0"], cwd=root, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads([ln for ln in out.stdout.splitlines() if ln.startswith("{")][-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["dtype"] == "f32"
+    assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == os.cpu_count() and cb["ttft_ms"] > 0 and cb["cpu"]
